@@ -1,0 +1,224 @@
+/*
+ * cusync.h -- C ABI of a GB300 (sm_103a) library for tile-level synchronisation of a
+ * chain of two dependent kernels: a producer GEMM (or implicit-GEMM convolution) with a
+ * fused GeLU / SwiGLU / ReLU epilogue, and a consumer GEMM (or convolution) that reads
+ * the producer's output.  Consumer thread blocks start on each input tile as soon as
+ * that tile has been produced, instead of waiting for the whole producer grid, so the
+ * under-filled last wave of one kernel overlaps the first wave of the next.
+ *
+ * Sources (cited by title and section):
+ *  [cuSync]   "A Framework for Fine-Grained Synchronization of Dependent GPU Kernels"
+ *             (arXiv 2305.13450).
+ *  [CUDA-FGS] CUDA Programming Guide, section 4.6 "Fine-Grained Synchronization".
+ *
+ * Conventions shared by every entry point:
+ *  - All tensors are bf16, row-major, device-resident, 16-byte aligned and owned by the
+ *    caller.  The library never allocates or frees memory in a run call.
+ *  - Weights are passed with the reduction dimension contiguous ("[out, in]", the
+ *    layout torch.nn.Linear stores): W1t is [N1, K] where the chain computes X x W1.
+ *  - Run calls are asynchronous on the caller's stream (a cudaStream_t passed as
+ *    cusync_stream_t; NULL is the legacy default stream).  They return launch-time
+ *    errors immediately; a device-side timeout is reported by cusync_chain_check.
+ *  - A chain object owns its synchronisation state (semaphores, tile counters, error
+ *    word) and is not thread-safe: use one chain per stream at a time.
+ *  - Shapes the kernels cannot cover return CUSYNC_ERR_UNSUPPORTED; there is no
+ *    fallback path.
+ *  - Every synchronisation policy yields byte-identical outputs: the tiles, the k order
+ *    inside a tile and the epilogue arithmetic do not depend on the policy.
+ */
+#ifndef CUSYNC_H_
+#define CUSYNC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st* cusync_stream_t;
+
+/* Synchronisation policy between the producer and the consumer ([cuSync] §IV-E,
+ * "Synchronization Policies"; [CUDA-FGS] §4.6.2, Table 14). */
+typedef enum {
+  /* Stream synchronisation ([cuSync] §II-A "Stream Synchronization"): the consumer
+   * kernel is launched after the producer kernel on the same stream; the baseline. */
+  CUSYNC_POLICY_STREAM = 0,
+  /* RowSync: one semaphore per producer row of tiles; a consumer tile waits, before
+   * its first k-block, until every tile of the rows it reads has been posted. */
+  CUSYNC_POLICY_ROW = 1,
+  /* TileSync: one semaphore per producer tile; a consumer tile waits on each producer
+   * tile just before the first k-block that reads it. */
+  CUSYNC_POLICY_TILE = 2,
+  /* StridedSync: producer column tiles D = n_tiles/G apart share one semaphore (G
+   * members per group), and the producer visits each group's members consecutively. */
+  CUSYNC_POLICY_STRIDED_TILE = 3,
+  /* Sentinel in data ([CUDA-FGS] §4.6.4): the intermediate buffer is filled with the
+   * bf16 pattern 0x8000 (-0.0) before the producer runs, the producer never stores that
+   * pattern, and the consumer re-loads an input tile while it still holds it.  On
+   * sm_103a the check is done in software on every element of the landed tile (the
+   * copy-time validity report of compute capability 10.7 is not used). */
+  CUSYNC_POLICY_SENTINEL = 4
+} cusync_policy_t;
+
+/* The chain computed ([cuSync] §II-B, Fig. fig:gpt-3:mlp, Table tab:resnet-sizes). */
+typedef enum {
+  /* H = GeLU_tanh(X x W1) (bf16), Y = H x W2.  X [M,K], W1t [N1,K], H [M,N1],
+   * W2t [N2,N1], Y [M,N2]. */
+  CUSYNC_CHAIN_MLP_GELU = 0,
+  /* H = silu(X x Wgate) * (X x Wup) (bf16), Y = H x Wdown.  W1t [2*N1, K] holds the
+   * rows of Wgate^T (0..N1-1) followed by those of Wup^T (N1..2*N1-1); W2t = Wdown^T
+   * [N2, N1]. */
+  CUSYNC_CHAIN_MLP_SWIGLU = 1,
+  /* H = ReLU(conv3x3(x, w1)) (bf16), y = conv3x3(H, w2); stride 1, pad 1, NHWC images
+   * x [n,h,w,c], H and y [n,h,w,k_out], KRSC weights w1 [k_out,3,3,c] and
+   * w2 [k_out,3,3,k_out]. */
+  CUSYNC_CHAIN_CONV_RELU = 2
+} cusync_chain_kind_t;
+
+/* How the two grids are made co-resident so that a waiting consumer can never starve
+ * the producer ([cuSync] §IV-B "Stage Processing Order"; [CUDA-FGS] §4.6.5). */
+typedef enum {
+  /* One persistent kernel (cooperative launch: every CTA resident) with a single tile
+   * queue holding all producer tiles before all consumer tiles. */
+  CUSYNC_LAUNCH_PERSISTENT = 0,
+  /* Two persistent kernels on one stream; the consumer is launched with programmatic
+   * stream serialisation and the producer triggers its dependents at its start. */
+  CUSYNC_LAUNCH_PDL = 1
+} cusync_launch_t;
+
+typedef enum {
+  CUSYNC_OK = 0,
+  CUSYNC_ERR_INVALID_ARG = 1, /* null, misaligned or inconsistent argument */
+  CUSYNC_ERR_UNSUPPORTED = 2, /* shape or option the kernels do not cover */
+  CUSYNC_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  CUSYNC_ERR_NOMEM = 4,       /* allocation of the chain's state failed */
+  CUSYNC_ERR_TIMEOUT = 5,     /* a device wait on a semaphore or sentinel gave up */
+  CUSYNC_ERR_DEVICE = 6       /* a device-internal wait gave up (pipeline fault) */
+} cusync_status_t;
+
+/* cusync_chain_desc_t.flags */
+#define CUSYNC_FLAG_NO_REORDER (1u << 0)  /* disable [cuSync] §V "Reorder Tile Loads and
+                                             Synchronization": weight tiles are then
+                                             loaded only after the A-tile wait */
+/* Fault injection for tests; each makes a device wait expire, never a GPU fault. */
+#define CUSYNC_DEBUG_SKIP_POST (1u << 8)     /* the producer never posts tile (0,0) */
+#define CUSYNC_DEBUG_SKIP_INIT (1u << 9)     /* SENTINEL: skip the sentinel fill */
+
+typedef struct {
+  int32_t kind;     /* cusync_chain_kind_t */
+  int32_t policy;   /* cusync_policy_t */
+  int32_t launch;   /* cusync_launch_t (ignored for CUSYNC_POLICY_STREAM) */
+  int32_t _pad0;
+  int64_t M, K, N1, N2;              /* MLP chains (see cusync_chain_kind_t) */
+  int32_t n, h, w, c, k_out;         /* CONV_RELU: NHWC image and output channels */
+  int32_t tile_n;                    /* accumulator tile width: 128 or 256; 0 = choose */
+  int32_t strided_group;             /* G for STRIDED_TILE; 0 = 2 */
+  uint32_t flags;                    /* CUSYNC_FLAG_* | CUSYNC_DEBUG_* */
+  int32_t num_sms;                   /* SMs the kernels may use; 0 = all of the device */
+  int32_t _pad1;
+  uint64_t timeout_ns;               /* bound of every device wait on a semaphore or a
+                                        sentinel; 0 = 1e9 (one second) */
+} cusync_chain_desc_t;
+
+/* Wave arithmetic of a two-kernel chain ([cuSync] §II-A "Thread block Wave Execution",
+ * Table tab:intro, §III-A). */
+typedef struct {
+  int64_t tbs[2];          /* thread blocks (tiles) of the producer and consumer */
+  double waves[2];         /* fractional waves tbs / cap */
+  int32_t waves_ceil[2];   /* ceil(tbs / cap) */
+  double util[2];          /* tbs / (ceil(waves) * cap) */
+  int32_t stream_waves;    /* waves_ceil[0] + waves_ceil[1]: stream synchronisation */
+  int32_t fused_waves;     /* ceil((tbs[0] + tbs[1]) / cap): tile synchronisation */
+  double fused_waves_frac; /* (tbs[0] + tbs[1]) / cap */
+  int64_t last_wave_tbs;   /* thread blocks in the fused last wave */
+  int32_t cap;             /* occupancy * num_sms */
+  int32_t occupancy;
+  int32_t num_sms;
+  int32_t tile_m, tile_n, tile_k; /* tile chosen by cusync_plan_waves (0 from
+                                     cusync_wave_stats) */
+} cusync_wave_report_t;
+
+/* Geometry of a chain (for tests and introspection). */
+typedef struct {
+  int32_t m_tiles[2], n_tiles[2], k_blocks[2];
+  int32_t n_out[2];        /* output columns written per tile */
+  int32_t tile_m, tile_n, tile_k;
+  int32_t strided_group, strided_distance;
+  int32_t num_flags;       /* semaphores of the policy */
+  int32_t grid[2];         /* CTAs of the producer / consumer launch (fused: grid[0]) */
+  int32_t num_sms;
+  int32_t conv_rows_per_tile; /* CONV_RELU: image rows per row tile */
+} cusync_chain_info_t;
+
+/* Status code as a static string. */
+const char* cusync_status_string(cusync_status_t s);
+
+/* Raw wave arithmetic for grids of tbs0 and tbs1 thread blocks with the given occupancy
+ * (thread blocks per SM) on num_sms SMs.  tbs1 may be 0 (a single kernel).
+ * INVALID_ARG if out is NULL, a count is negative or occupancy/num_sms < 1. */
+cusync_status_t cusync_wave_stats(int64_t tbs0, int64_t tbs1, int32_t occupancy, int32_t num_sms,
+                                  cusync_wave_report_t* out);
+
+/* Tiles the chain described by *d would launch and their wave arithmetic on
+ * d->num_sms SMs (0: the current device's count) at this library's occupancy of one
+ * CTA per SM.  Pure host computation. */
+cusync_status_t cusync_plan_waves(const cusync_chain_desc_t* d, cusync_wave_report_t* out);
+
+/* Validate *d, allocate the chain's synchronisation state on the current device and
+ * prepare the kernels.  *out receives an opaque handle owned by the caller (release it
+ * with cusync_destroy_chain).  INVALID_ARG / UNSUPPORTED for bad descriptors, NOMEM or
+ * CUDA on allocation or device errors. */
+typedef struct cusync_chain* cusync_chain_t;
+cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t* out);
+
+/* Run an MLP chain (kinds MLP_GELU, MLP_SWIGLU) on `stream`: writes H (the
+ * intermediate, caller-owned scratch of M*N1 bf16 that holds the producer's output on
+ * return) and Y.  Pointers: X [M,K], W1t [N1,K] (SwiGLU: [2*N1,K]), W2t [N2,N1],
+ * H [M,N1], Y [M,N2]; device memory, 16-byte aligned, not overlapping H or Y.
+ * Asynchronous; INVALID_ARG / UNSUPPORTED / CUDA on launch-time errors. */
+cusync_status_t cusync_run_mlp(cusync_chain_t chain, const void* X, const void* W1t, const void* W2t, void* H,
+                               void* Y, cusync_stream_t stream);
+
+/* Run a CONV_RELU chain: x [n,h,w,c], w1 [k_out,3,3,c], w2 [k_out,3,3,k_out] (KRSC),
+ * y1 (intermediate, [n,h,w,k_out]) and y2 ([n,h,w,k_out]).  Same rules as
+ * cusync_run_mlp. */
+cusync_status_t cusync_run_conv_chain(cusync_chain_t chain, const void* x, const void* w1, const void* w2, void* y1,
+                                      void* y2, cusync_stream_t stream);
+
+/* Synchronise `stream` and read the chain's device error word.  Returns OK, TIMEOUT (a
+ * consumer gave up waiting on a semaphore or a sentinel: the outputs of that run are
+ * not valid) or DEVICE.  After an error the chain's synchronisation state is reset, so
+ * the next run starts clean.  If code/detail are non-NULL they receive the raw error
+ * word and its detail (tile and k-block of the failing wait). */
+cusync_status_t cusync_chain_check(cusync_chain_t chain, cusync_stream_t stream, uint32_t* code, uint32_t* detail);
+
+/* Clear the chain's semaphores, tile counters and error word (stream-ordered). */
+cusync_status_t cusync_chain_reset(cusync_chain_t chain, cusync_stream_t stream);
+
+/* Geometry the chain described by *d would use (tiles, semaphores, grids on
+ * d->num_sms SMs, or the current device's count when 0).  Pure host computation. */
+cusync_status_t cusync_plan_info(const cusync_chain_desc_t* d, cusync_chain_info_t* out);
+
+/* The semaphore waits the consumer performs for row tile m_tile of the chain described
+ * by *d, in issue order: entry i is (kb[i], flag[i], per_run[i]): before loading A
+ * k-block kb[i] it waits until semaphore flag[i] has received per_run[i] posts in the
+ * current run.  Writes at most max entries and the total count to *n_out.  Pure host
+ * computation with the same code the device runs. */
+cusync_status_t cusync_consumer_waits(const cusync_chain_desc_t* d, int32_t m_tile, int32_t* kb, int32_t* flag,
+                                      uint32_t* per_run, int32_t max, int32_t* n_out);
+
+/* The semaphore producer tile (m_tile, n_tile) posts (-1 if the policy posts none), and
+ * the producer column visited at position y of a row (the policy's tile order).  Pure
+ * host computation. */
+cusync_status_t cusync_producer_flag(const cusync_chain_desc_t* d, int32_t m_tile, int32_t n_tile, int32_t* flag);
+cusync_status_t cusync_producer_col(const cusync_chain_desc_t* d, int32_t y, int32_t* col);
+
+/* Release the chain's device state.  NULL is accepted. */
+cusync_status_t cusync_destroy_chain(cusync_chain_t chain);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CUSYNC_H_ */

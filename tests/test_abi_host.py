@@ -1,0 +1,213 @@
+"""CPU tests of the C-ABI library: it builds, loads and exports every function the public
+header declares; its host-side planner matches the oracle (and through it the tables of
+[cuSync]); and the dependency logic the kernels execute (the same code, called on the
+host) matches the oracle's brute-force dependency sets for every policy."""
+
+import os
+import re
+
+import pytest
+
+import tile_level_sync_gb300 as cs
+from oracle import deps, planner
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for fn in os.listdir(inc):
+        if fn.endswith(".h"):
+            src = open(os.path.join(inc, fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(cusync_\w+)\s*\(", src))
+    return names
+
+
+def test_library_exports_every_declared_function():
+    lib = cs.load()
+    names = _declared_functions()
+    assert len(names) >= 13
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings():
+    assert cs.status_string(cs.OK) == "CUSYNC_OK"
+    assert cs.status_string(cs.ERR_TIMEOUT) == "CUSYNC_ERR_TIMEOUT"
+
+
+@pytest.mark.parametrize("tbs0,tbs1,occ,sms", [
+    (192, 384, 2, 80), (72, 48, 3, 80), (6, 6, 1, 4), (240, 0, 2, 80), (0, 0, 1, 148),
+    (48, 96, 1, 148), (384, 768, 1, 148), (1536, 3072, 1, 148), (296, 148, 1, 148), (1, 1, 1, 1),
+])
+def test_wave_stats_matches_oracle(tbs0, tbs1, occ, sms):
+    r = cs.cusync_wave_stats(tbs0, tbs1, occ, sms)
+    cap = planner.wave_capacity(occ, sms)
+    o = planner.chain_waves([tbs0, tbs1], cap)
+    assert r.cap == cap
+    assert list(r.tbs) == [tbs0, tbs1]
+    assert list(r.waves_ceil) == list(o.waves_ceil)
+    assert list(r.waves) == pytest.approx(list(o.waves_frac), abs=1e-15)
+    assert list(r.util) == pytest.approx(list(o.util), abs=1e-15)
+    assert r.stream_waves == o.stream_waves
+    assert r.fused_waves == o.fused_waves
+    assert r.fused_waves_frac == pytest.approx(o.fused_waves_frac, abs=1e-15)
+    assert r.last_wave_tbs == o.last_wave_tbs
+
+
+def test_wave_stats_invalid():
+    lib = cs.load()
+    rep = cs.cusync_wave_report_t()
+    import ctypes
+    assert lib.cusync_wave_stats(-1, 0, 1, 1, ctypes.byref(rep)) == cs.ERR_INVALID_ARG
+    assert lib.cusync_wave_stats(1, 0, 0, 1, ctypes.byref(rep)) == cs.ERR_INVALID_ARG
+    assert lib.cusync_wave_stats(1, 0, 1, 0, ctypes.byref(rep)) == cs.ERR_INVALID_ARG
+    assert lib.cusync_wave_stats(1, 0, 1, 1, None) == cs.ERR_INVALID_ARG
+
+
+GPT = dict(K=12288, N1=6144, N2=12288)
+
+
+@pytest.mark.parametrize("M,tile_n,prod,cons,stream,fused", [
+    (64, 256, 4, 1, 2, 1),
+    (256, 256, 48, 96, 2, 1),
+    (512, 256, 96, 192, 3, 2),
+    (1024, 256, 192, 384, 5, 4),
+    (2048, 256, 384, 768, 9, 8),
+    (4096, 256, 768, 1536, 17, 16),
+    (256, 128, 96, 192, 3, 2),
+    (1024, 128, 384, 768, 9, 8),
+])
+def test_plan_waves_gpt_mlp(M, tile_n, prod, cons, stream, fused):
+    dims = dict(K=256, N1=1024, N2=256) if M == 64 else GPT
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, tile_n=tile_n, num_sms=148, **dims)
+    r = cs.cusync_plan_waves(d)
+    assert (r.tbs[0], r.tbs[1]) == (prod, cons)
+    assert r.tbs[0] == planner.gemm_tiles(M, dims["N1"], 128, tile_n)
+    assert (r.stream_waves, r.fused_waves) == (stream, fused)
+    assert (r.tile_m, r.tile_n, r.tile_k) == (128, tile_n, 64)
+
+
+def test_plan_swiglu_and_conv():
+    d = cs.make_desc(cs.CHAIN_MLP_SWIGLU, "TILE", M=256, K=8192, N1=3584, N2=8192, tile_n=256, num_sms=148)
+    r = cs.cusync_plan_waves(d)
+    assert (r.tbs[0], r.tbs[1]) == (2 * 28, 2 * 32)
+    d = cs.make_desc(cs.CHAIN_CONV_RELU, "TILE", n=32, h=14, w=14, c=256, k_out=256, tile_n=256, num_sms=148)
+    info = cs.cusync_plan_info(d)
+    assert info.conv_rows_per_tile == 7
+    assert list(info.m_tiles) == [64, 64] and list(info.k_blocks) == [36, 36]
+    r = cs.cusync_plan_waves(d)
+    assert (r.tbs[0], r.tbs[1], r.stream_waves, r.fused_waves) == (64, 64, 2, 1)
+
+
+def test_invalid_and_unsupported_descriptors():
+    bad = [
+        (cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=0, K=64, N1=64, N2=64, num_sms=148), cs.ERR_INVALID_ARG),
+        (cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=8, K=60, N1=64, N2=64, num_sms=148), cs.ERR_UNSUPPORTED),
+        (cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=8, K=64, N1=64, N2=64, tile_n=64, num_sms=148),
+         cs.ERR_UNSUPPORTED),
+        (cs.make_desc(cs.CHAIN_MLP_GELU, 9, M=8, K=64, N1=64, N2=64, num_sms=148), cs.ERR_INVALID_ARG),
+        (cs.make_desc(cs.CHAIN_MLP_GELU, "STRIDED", M=8, K=64, N1=768, N2=64, tile_n=256, strided_group=2,
+                      num_sms=148), cs.ERR_UNSUPPORTED),   # 3 column tiles, G = 2
+        (cs.make_desc(cs.CHAIN_CONV_RELU, "ROW", n=1, h=14, w=14, c=96, k_out=128, num_sms=148),
+         cs.ERR_UNSUPPORTED),
+        (cs.make_desc(cs.CHAIN_CONV_RELU, "ROW", n=1, h=4, w=200, c=64, k_out=64, num_sms=148),
+         cs.ERR_UNSUPPORTED),
+    ]
+    for d, want in bad:
+        with pytest.raises(cs.CusyncError) as e:
+            cs.cusync_plan_waves(d)
+        assert e.value.status == want
+
+
+# ------------------------------------------------------------------ dependency logic
+
+
+def _members(policy, flag, nt, D, G):
+    if policy == "TILE":
+        return {(flag // nt, flag % nt)}
+    if policy == "ROW":
+        return {(flag, c) for c in range(nt)}
+    if policy == "STRIDED":
+        m, g = divmod(flag, D)
+        return {(m, g + j * D) for j in range(G)}
+    raise ValueError(policy)
+
+
+def _oracle_chain(desc, info):
+    if desc.kind == cs.CHAIN_CONV_RELU:
+        return deps.ConvChain(N=desc.n, P=desc.h, Q=desc.w, C=desc.k_out, TH=info.conv_rows_per_tile,
+                              BNo=info.n_out[0], BK=info.tile_k)
+    return deps.GemmChain(M=desc.M, N1=desc.N1, BM=info.tile_m, BNo=info.n_out[0], BK=info.tile_k)
+
+
+CASES = [
+    dict(kind=cs.CHAIN_MLP_GELU, M=300, K=128, N1=1024, N2=256, tile_n=256),
+    dict(kind=cs.CHAIN_MLP_GELU, M=256, K=128, N1=1536, N2=256, tile_n=128),
+    dict(kind=cs.CHAIN_MLP_GELU, M=130, K=64, N1=640, N2=64, tile_n=128),           # ragged M and N1
+    dict(kind=cs.CHAIN_MLP_SWIGLU, M=200, K=64, N1=512, N2=64, tile_n=256),
+    dict(kind=cs.CHAIN_CONV_RELU, n=2, h=14, w=14, c=64, k_out=256, tile_n=128),
+    dict(kind=cs.CHAIN_CONV_RELU, n=2, h=9, w=30, c=64, k_out=128, tile_n=128),     # 4 rows per tile
+    dict(kind=cs.CHAIN_CONV_RELU, n=1, h=5, w=100, c=128, k_out=128, tile_n=128),   # 1 row per tile
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+@pytest.mark.parametrize("policy,G", [("TILE", 1), ("ROW", 1), ("STRIDED", 2), ("STRIDED", 1)])
+def test_consumer_waits_match_oracle(case, policy, G):
+    desc = cs.make_desc(policy=policy, strided_group=G, num_sms=148, **case)
+    try:
+        info = cs.cusync_plan_info(desc)
+    except cs.CusyncError as e:
+        assert policy == "STRIDED" and e.status == cs.ERR_UNSUPPORTED
+        return
+    ch = _oracle_chain(desc, info)
+    nt = info.n_tiles[0]
+    assert ch.n_tiles == nt and ch.m_tiles == info.m_tiles[1] and ch.k_blocks == info.k_blocks[1]
+    D, Gc = info.strided_distance, info.strided_group
+    for m in range(ch.m_tiles):
+        got = [set() for _ in range(ch.k_blocks)]
+        for kb, flag, per_run in cs.cusync_consumer_waits(desc, m):
+            mem = _members(policy, flag, nt, D, Gc)
+            assert per_run == len(mem)
+            assert 0 <= flag < info.num_flags
+            got[kb] |= mem
+        want = deps.wait_sets(ch, policy, m, Gc)
+        assert got == want, (policy, m)
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_sentinel_and_stream_wait_on_no_semaphore(case):
+    for pol in ("SENTINEL", "STREAM"):
+        desc = cs.make_desc(policy=pol, num_sms=148, **case)
+        info = cs.cusync_plan_info(desc)
+        assert info.num_flags == 0
+        for m in range(info.m_tiles[1]):
+            assert cs.cusync_consumer_waits(desc, m) == []
+        assert cs.cusync_producer_flag(desc, 0, 0) == -1
+
+
+@pytest.mark.parametrize("case", CASES)
+@pytest.mark.parametrize("policy,G", [("TILE", 1), ("ROW", 1), ("STRIDED", 2)])
+def test_producer_posts_and_order(case, policy, G):
+    desc = cs.make_desc(policy=policy, strided_group=G, num_sms=148, **case)
+    try:
+        info = cs.cusync_plan_info(desc)
+    except cs.CusyncError:
+        return
+    nt, D, Gc = info.n_tiles[0], info.strided_distance, info.strided_group
+    posts = {}
+    for m in range(info.m_tiles[0]):
+        for c in range(nt):
+            f = cs.cusync_producer_flag(desc, m, c)
+            assert (m, c) in _members(policy, f, nt, D, Gc)
+            posts[f] = posts.get(f, 0) + 1
+    for f, n in posts.items():
+        assert n == len(_members(policy, f, nt, D, Gc))
+    order = [cs.cusync_producer_col(desc, y) for y in range(nt)]
+    if policy == "STRIDED":
+        assert order == deps.strided_producer_order(nt, Gc)
+    else:
+        assert order == list(range(nt))

@@ -1,0 +1,170 @@
+"""GPU parity: every chain, policy and launch mode against the oracle, element by element,
+on seeded inputs; byte identity of H and Y across policies and the stream-serialised
+baseline; device waits that expire report a status instead of hanging."""
+
+import numpy as np
+import pytest
+import torch
+
+import tile_level_sync_gb300 as cs
+from oracle import chains
+from tile_level_sync_gb300 import synth
+
+from gpu_helpers import assert_within_tol, bits, device_mlp_operands, f64, run_conv, run_mlp
+
+pytestmark = pytest.mark.gpu
+
+POLICIES = ["STREAM", "ROW", "TILE", "STRIDED", "SENTINEL"]
+LAUNCHES = [cs.LAUNCH_PERSISTENT, cs.LAUNCH_PDL]
+
+
+def _mlp_case(M, K, N1, N2, seed=0):
+    X, W1, W2 = synth.mlp_gelu_inputs(M, K, N1, N2, seed)
+    H_ref, Y_ref = chains.mlp_gelu(f64(X), f64(W1), f64(W2))
+    return (X, W1, W2), (H_ref, Y_ref)
+
+
+@pytest.mark.parametrize("tile_n", [256, 128])
+def test_tiny_mlp_all_policies_bit_identical(tile_n):
+    """64x256 . 256x1024 . 1024x256 (the tiny MLP configuration)."""
+    (X, W1, W2), (H_ref, Y_ref) = _mlp_case(64, 256, 1024, 256)
+    ops = device_mlp_operands(X, W1, W2)
+    ref_bits = None
+    for pol in POLICIES:
+        for launch in LAUNCHES:
+            if pol == "STREAM" and launch != cs.LAUNCH_PERSISTENT:
+                continue
+            d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, launch, M=64, K=256, N1=1024, N2=256, tile_n=tile_n)
+            H, Y, _ = run_mlp(d, *ops, runs=2)
+            assert_within_tol(f64(H), H_ref, f"H {pol} {launch}")
+            assert_within_tol(f64(Y), Y_ref, f"Y {pol} {launch}")
+            b = (bits(H), bits(Y))
+            if ref_bits is None:
+                ref_bits = b
+            else:
+                assert np.array_equal(b[0], ref_bits[0]) and np.array_equal(b[1], ref_bits[1]), (pol, launch)
+
+
+@pytest.mark.parametrize("M,K,N1,N2,tile_n", [
+    (200, 384, 640, 264, 256),     # ragged M, N1 (H columns) and N2
+    (384, 1024, 2048, 1024, 128),  # several row and column tiles, longer K
+    (1, 64, 512, 128, 256),        # a single token
+    (520, 512, 1536, 512, 256),    # more tiles than a persistent CTA's ring holds
+])
+def test_mlp_shapes_all_policies(M, K, N1, N2, tile_n):
+    (X, W1, W2), (H_ref, Y_ref) = _mlp_case(M, K, N1, N2, seed=1)
+    ops = device_mlp_operands(X, W1, W2)
+    ref_bits = None
+    for pol in POLICIES:
+        d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, cs.LAUNCH_PERSISTENT, M=M, K=K, N1=N1, N2=N2, tile_n=tile_n)
+        try:
+            cs.cusync_plan_info(d)
+        except cs.CusyncError as e:   # StridedSync needs a column-tile count divisible by G
+            assert pol == "STRIDED" and e.status == cs.ERR_UNSUPPORTED
+            continue
+        H, Y, _ = run_mlp(d, *ops, runs=3)
+        assert_within_tol(f64(H), H_ref, f"H {pol}")
+        assert_within_tol(f64(Y), Y_ref, f"Y {pol}")
+        b = (bits(H), bits(Y))
+        if ref_bits is None:
+            ref_bits = b
+        else:
+            assert np.array_equal(b[0], ref_bits[0]) and np.array_equal(b[1], ref_bits[1]), pol
+
+
+def test_intermediate_never_holds_negative_zero():
+    (X, W1, W2), _ = _mlp_case(256, 512, 1024, 256, seed=2)
+    ops = device_mlp_operands(X, W1, W2)
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "SENTINEL", M=256, K=512, N1=1024, N2=256)
+    H, _, _ = run_mlp(d, *ops)
+    assert not np.any(bits(H).view(np.uint16) == 0x8000)
+
+
+@pytest.mark.parametrize("M,K,N1,N2,tile_n", [(64, 256, 512, 256, 256), (200, 512, 384, 264, 256),
+                                               (130, 256, 640, 128, 128)])
+def test_swiglu_all_policies(M, K, N1, N2, tile_n):
+    X, Wg, Wu, Wd = synth.mlp_swiglu_inputs(M, K, N1, N2, seed=3)
+    H_ref, Y_ref = chains.mlp_swiglu(f64(X), f64(Wg), f64(Wu), f64(Wd))
+    ops = device_mlp_operands(X, Wg, Wd, Wup=Wu)
+    ref_bits = None
+    for pol in POLICIES:
+        d = cs.make_desc(cs.CHAIN_MLP_SWIGLU, pol, cs.LAUNCH_PERSISTENT, M=M, K=K, N1=N1, N2=N2, tile_n=tile_n)
+        try:
+            cs.cusync_plan_info(d)
+        except cs.CusyncError as e:
+            assert pol == "STRIDED" and e.status == cs.ERR_UNSUPPORTED
+            continue
+        H, Y, _ = run_mlp(d, *ops, runs=2)
+        assert_within_tol(f64(H), H_ref, f"H {pol}")
+        assert_within_tol(f64(Y), Y_ref, f"Y {pol}")
+        b = (bits(H), bits(Y))
+        if ref_bits is None:
+            ref_bits = b
+        else:
+            assert np.array_equal(b[0], ref_bits[0]) and np.array_equal(b[1], ref_bits[1]), pol
+
+
+@pytest.mark.parametrize("n,h,w,c,k,tile_n", [(2, 14, 14, 128, 128, 128), (3, 14, 14, 64, 256, 256),
+                                              (2, 9, 30, 64, 128, 128), (1, 5, 100, 128, 64, 128)])
+def test_conv_chain_all_policies(n, h, w, c, k, tile_n):
+    x, w1, w2 = synth.conv_inputs(n, h, w, c, k, seed=4)
+    H_ref, Y_ref = chains.conv_relu_chain(f64(x), f64(w1), f64(w2))
+    ref_bits = None
+    for pol in POLICIES:
+        for launch in LAUNCHES:
+            if pol == "STREAM" and launch != cs.LAUNCH_PERSISTENT:
+                continue
+            d = cs.make_desc(cs.CHAIN_CONV_RELU, pol, launch, n=n, h=h, w=w, c=c, k_out=k, tile_n=tile_n)
+            try:
+                cs.cusync_plan_info(d)
+            except cs.CusyncError as e:
+                assert pol == "STRIDED" and e.status == cs.ERR_UNSUPPORTED
+                continue
+            y1, y2, _ = run_conv(d, x, w1, w2, runs=2)
+            assert_within_tol(f64(y1), H_ref, f"y1 {pol} {launch}")
+            assert_within_tol(f64(y2), Y_ref, f"y2 {pol} {launch}")
+            b = (bits(y1), bits(y2))
+            if ref_bits is None:
+                ref_bits = b
+            else:
+                assert np.array_equal(b[0], ref_bits[0]) and np.array_equal(b[1], ref_bits[1]), (pol, launch)
+
+
+def test_skipped_post_times_out_and_recovers():
+    """A producer tile that never posts makes the consumer's bounded wait expire: the run
+    reports CUSYNC_ERR_TIMEOUT (no hang, no trap), and the chain works again afterwards."""
+    (X, W1, W2), (H_ref, Y_ref) = _mlp_case(256, 256, 1024, 256, seed=5)
+    ops = device_mlp_operands(X, W1, W2)
+    for pol in ("ROW", "TILE"):
+        d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, M=256, K=256, N1=1024, N2=256, flags=cs.DEBUG_SKIP_POST,
+                         timeout_ns=20_000_000)
+        _, _, st = run_mlp(d, *ops, check=False)
+        assert st == cs.ERR_TIMEOUT
+        d.flags = 0
+        H, Y, st = run_mlp(d, *ops)
+        assert_within_tol(f64(Y), Y_ref, f"Y after timeout {pol}")
+    # the same chain object, across the failure
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "TILE", M=256, K=256, N1=1024, N2=256, flags=cs.DEBUG_SKIP_POST,
+                     timeout_ns=20_000_000)
+    ch = cs.Chain(d)
+    Hd = torch.empty((256, 1024), dtype=torch.bfloat16, device="cuda")
+    Yd = torch.empty((256, 256), dtype=torch.bfloat16, device="cuda")
+    ch.run(*ops, Hd, Yd)
+    st, code, detail = ch.check()
+    assert st == cs.ERR_TIMEOUT and (code >> 24) == 1
+    ch.close()
+
+
+def test_invalid_pointers_rejected():
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=64, K=256, N1=1024, N2=256)
+    ch = cs.Chain(d)
+    try:
+        t = torch.empty(64 * 1024 + 8, dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(cs.CusyncError) as e:
+            ch.run(t.data_ptr() + 2, t, t, t, t)   # misaligned
+        assert e.value.status == cs.ERR_INVALID_ARG
+        with pytest.raises(cs.CusyncError) as e:
+            ch.run(0, t, t, t, t)
+        assert e.value.status == cs.ERR_INVALID_ARG
+    finally:
+        ch.close()

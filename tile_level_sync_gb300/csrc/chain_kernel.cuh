@@ -1,0 +1,573 @@
+// The chain kernel: a persistent, warp-specialised tcgen05 GEMM that runs producer
+// tiles, consumer tiles, or both from one tile queue, with the synchronisation of
+// "A Framework for Fine-Grained Synchronization of Dependent GPU Kernels" (cuSync)
+// and of the CUDA Programming Guide §4.6 "Fine-Grained Synchronization" (CUDA-FGS).
+//
+// Roles inside one CTA (192 threads, one CTA per SM):
+//   warp 0, lane 0  scheduler + TMA issuer.  Claims tiles from a global counter in
+//                   queue order (cuSync §IV-C: stage.tile() = atomicAdd on a per-stage
+//                   counter), hands each tile to the other roles through a shared-memory
+//                   ring, and streams the A and B k-blocks into a multi-stage
+//                   shared-memory ring with TMA.  For a consumer tile it issues the
+//                   weight (B) loads of the next stages first and only then waits on the
+//                   producer's semaphores before each A load (cuSync §V, "Reorder Tile
+//                   Loads and Synchronization").
+//   warp 1          TMEM owner and MMA issuer.  Lane 0 issues tcgen05.mma (128 x BN x 16,
+//                   bf16 in, fp32 accumulate into TMEM) and commits each stage back to
+//                   the loader.  Under the sentinel policy the warp also scans every
+//                   landed A stage for the 0x8000 pattern and re-issues its load while
+//                   the pattern is present (CUDA-FGS §4.6.4.4 and §4.6.7, with a software
+//                   check because sm_103a has no copy-time validity report).
+//   warps 2..5      epilogue.  tcgen05.ld the fp32 accumulator (double-buffered in TMEM
+//                   so the next tile's mainloop overlaps this epilogue), apply GeLU /
+//                   SwiGLU / ReLU, round to bf16 (round-to-nearest-even), replace -0 by
+//                   +0 (CUDA-FGS §4.6.4.3), write whole 16-byte chunks with one 128-bit
+//                   store each, and for a producer tile post its semaphore after all of
+//                   the tile's stores (cuSync §IV-E "Post": barrier, device-scope fence,
+//                   atomic increment).
+//
+// The pipelining follows the load-compute rules of "ALCOP: Automatic Load-COmpute
+// Pipelining in Deep Learning Compiler for AI-GPUs" (§ pipelining rules): only buffers
+// filled by asynchronous copies in a sequential k-loop are multi-buffered, each with its
+// own barrier.
+//
+// Every wait is bounded by %globaltimer.  A semaphore or sentinel wait that expires
+// records an error word and lets the CTA run to completion on whatever data is present;
+// a pipeline (mbarrier) wait that expires also raises a CTA-local abort so the other
+// roles drain.  Nothing traps.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "geometry.h"
+#include "ptx.cuh"
+
+namespace cusync {
+
+// Control words in front of the semaphore array.
+enum : int { CTRL_ERR = 0, CTRL_ERR_DETAIL = 1, CTRL_COUNTER = 2, CTRL_EXIT = 4, CTRL_WORDS = 16 };
+// Error classes (bits 31..24 of the error word; bits 23..0 hold the tile index).
+enum : uint32_t { ERRC_FLAG_TIMEOUT = 1, ERRC_SENTINEL_TIMEOUT = 2, ERRC_PIPELINE = 3 };
+// Flag bits shared with cusync.h.
+constexpr uint32_t kFlagNoReorder = 1u << 0;
+constexpr uint32_t kDebugSkipPost = 1u << 8;
+
+struct StageArgs {
+  CUtensorMap tmA;       // activations: 2-D [M, K] or 4-D NHWC image
+  CUtensorMap tmB;       // weights [N (or 2*N1), K]
+  void* out;             // bf16 [M, N] row-major (conv: [pixels, channels])
+  StageGeo g;
+  int32_t b_half_rows;   // SwiGLU: row offset of the up-projection half of B
+};
+
+struct ChainArgs {
+  StageArgs st[2];       // 0 = producer, 1 = consumer
+  DepCfg dep;
+  uint32_t* flags;       // semaphores
+  uint32_t* ctrl;        // CTRL_* words
+  int32_t queue;         // tile counter slot used by this launch
+  int32_t first_stage;   // stages served by this launch: [first_stage, last_stage]
+  int32_t last_stage;
+  int32_t tiles0, tiles1;
+  uint32_t epoch;        // run number (semaphores count up across runs)
+  uint32_t flags_bits;
+  int32_t pdl_role;      // 1: trigger dependents at start; 2: wait on the primary at exit
+  int32_t sentinel_check;
+  int32_t _pad;
+  uint64_t timeout_ns;       // semaphore / sentinel waits
+  uint64_t pipe_timeout_ns;  // shared-memory pipeline waits
+};
+
+template <int BN>
+struct KCfg {
+  static constexpr int kStages = (BN == 256) ? 4 : 6;
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;  // two fp32 accumulators of BN columns
+  static constexpr int kSlots = 4;          // tile hand-off ring
+  static constexpr int kThreads = 192;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 1024;
+};
+
+struct TileRef {
+  int32_t s, m, c;
+};
+
+__device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
+  int32_t s, u;
+  if (a.first_stage == a.last_stage) {
+    s = a.first_stage;
+    u = t;
+  } else if (t < a.tiles0) {
+    s = 0;
+    u = t;
+  } else {
+    s = 1;
+    u = t - a.tiles0;
+  }
+  const StageGeo& g = a.st[s].g;
+  const int32_t m = u / g.n_tiles, y = u % g.n_tiles;
+  const int32_t c = (s == 0) ? producer_col(a.dep, y) : y;
+  return TileRef{s, m, c};
+}
+
+__device__ __forceinline__ uint32_t a_tile_bytes(const StageGeo& g) {
+  return g.a_mode == AMODE_GEMM ? (uint32_t)(kBM * kBK * 2) : (uint32_t)(g.img_w * g.th * kBK * 2);
+}
+
+__device__ __forceinline__ void issue_a(const ChainArgs& a, const TileRef& tr, int32_t kb, void* dst, uint64_t* bar,
+                                        uint64_t pol) {
+  const StageArgs& S = a.st[tr.s];
+  if (S.g.a_mode == AMODE_GEMM) {
+    ptx::tma_load_2d(dst, &S.tmA, bar, kb * kBK, tr.m * kBM, pol);
+  } else {
+    // implicit im2col: filter tap (r, s), channel block cb; the box is TH image rows of
+    // one image shifted by (r-1, s-1); rows or columns outside the image are zero-filled.
+    const int32_t tap = kb / S.g.cblocks, cb = kb % S.g.cblocks;
+    const int32_t r = tap / 3, s = tap % 3;
+    const int32_t n = tr.m / S.g.tpi, hb = tr.m % S.g.tpi;
+    ptx::tma_load_4d(dst, &S.tmA, bar, cb * kBK, s - 1, hb * S.g.th + r - 1, n, pol);
+  }
+}
+
+template <int BN>
+__device__ __forceinline__ void issue_b(const ChainArgs& a, const TileRef& tr, int32_t kb, uint8_t* dst,
+                                        uint64_t* bar, uint64_t pol) {
+  const StageArgs& S = a.st[tr.s];
+  if (S.g.epi == EPI_SWIGLU) {
+    // gate rows then up rows of the same BN/2 output columns, stacked in one B tile
+    const int32_t row0 = tr.c * (BN / 2);
+    ptx::tma_load_2d(dst, &S.tmB, bar, kb * kBK, row0, pol);
+    ptx::tma_load_2d(dst + (BN / 2) * 128, &S.tmB, bar, kb * kBK, S.b_half_rows + row0, pol);
+  } else {
+    ptx::tma_load_2d(dst, &S.tmB, bar, kb * kBK, tr.c * BN, pol);
+  }
+}
+
+__device__ __forceinline__ void record_error(const ChainArgs& a, uint32_t cls, int32_t tile, int32_t detail) {
+  const uint32_t w = (cls << 24) | ((uint32_t)tile & 0xFFFFFFu);
+  if (atomicCAS(a.ctrl + CTRL_ERR, 0u, w) == 0u) atomicExch(a.ctrl + CTRL_ERR_DETAIL, (uint32_t)detail);
+}
+
+// Bounded acquire-poll of one semaphore ([cuSync] §IV-E "Wait"; CUDA-FGS §4.6.2 flag
+// protocol).  Gives up when the deadline passes or another wait has already failed.
+__device__ __forceinline__ void wait_flag(const ChainArgs& a, int32_t flag, uint32_t target, int32_t tile,
+                                          int32_t kb) {
+  const uint32_t* f = a.flags + flag;
+  if ((int32_t)(ptx::ld_acquire_gpu(f) - target) >= 0) return;
+  const uint64_t t0 = ptx::globaltimer();
+  uint32_t iter = 0;
+  while (true) {
+    __nanosleep(32);
+    if ((int32_t)(ptx::ld_acquire_gpu(f) - target) >= 0) return;
+    if ((++iter & 63u) == 0) {
+      if (ptx::ld_relaxed_gpu(a.ctrl + CTRL_ERR) != 0u) return;
+      if (ptx::globaltimer() - t0 > a.timeout_ns) {
+        record_error(a, ERRC_FLAG_TIMEOUT, tile, (kb << 16) | (flag & 0xFFFF));
+        return;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ bool has_sentinel_bf16x2(uint32_t x) {
+  return ((x & 0xFFFFu) == 0x8000u) | ((x >> 16) == 0x8000u);
+}
+
+__device__ __forceinline__ uint32_t canon_bf16x2(uint32_t x) {
+  uint32_t lo = x & 0xFFFFu, hi = x >> 16;
+  lo = (lo == 0x8000u) ? 0u : lo;
+  hi = (hi == 0x8000u) ? 0u : hi;
+  return lo | (hi << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // round to nearest even; a -> low half
+  return canon_bf16x2(*reinterpret_cast<uint32_t*>(&v));
+}
+
+// tanh-GeLU written as z * sigmoid(2u), u = sqrt(2/pi) (z + 0.044715 z^3), which equals
+// 0.5 z (1 + tanh u).
+__device__ __forceinline__ float gelu_f(float z) {
+  const float u = 0.7978845608028654f * (z + 0.044715f * z * z * z);
+  return __fdividef(z, 1.0f + __expf(-2.0f * u));
+}
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ ChainArgs args) {
+  using C = KCfg<BN>;
+  constexpr int S = C::kStages;
+  constexpr uint32_t FULL = 0xFFFFFFFFu;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_base = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+  uint64_t* full = bars;                  // [S]   A+B (or A retry) landed
+  uint64_t* empty = full + S;             // [S]   MMA finished reading the stage
+  uint64_t* tfull = empty + S;            // [2]   accumulator ready
+  uint64_t* tempty = tfull + 2;           // [2]   accumulator drained
+  uint64_t* qfull = tempty + 2;           // [slots] tile index published
+  uint64_t* qempty = qfull + C::kSlots;   // [slots] tile index consumed
+  uint64_t* mma_done = qempty + C::kSlots;
+  uint64_t* epi_done = mma_done + 1;      // [2]   all epilogue threads stored the tile
+  int32_t* qtile = reinterpret_cast<int32_t*>(epi_done + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qtile + C::kSlots);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+  volatile int32_t* it_issued = abort_flag + 1;
+
+  auto smem_a = [&](int st) { return stage_base + st * C::kStageBytes; };
+  auto smem_b = [&](int st) { return stage_base + st * C::kStageBytes + C::kABytes; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (args.pdl_role == 1) ptx::pdl_launch_dependents();
+
+  if (warp == 1) {
+    if (lane == 0) {
+      for (int i = 0; i < S; ++i) {
+        ptx::mbar_init(&full[i], 1);
+        ptx::mbar_init(&empty[i], 1);
+      }
+      for (int i = 0; i < 2; ++i) {
+        ptx::mbar_init(&tfull[i], 1);
+        ptx::mbar_init(&tempty[i], 128);
+        ptx::mbar_init(&epi_done[i], 128);
+      }
+      for (int i = 0; i < C::kSlots; ++i) {
+        ptx::mbar_init(&qfull[i], 1);
+        ptx::mbar_init(&qempty[i], 1 + 4);
+      }
+      ptx::mbar_init(mma_done, 1);
+      *abort_flag = 0;
+      *it_issued = 0;
+      ptx::mbar_init_fence();
+    }
+    __syncwarp();
+    ptx::tmem_alloc(tmem_slot, C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int s = args.first_stage; s <= args.last_stage; ++s) {
+      ptx::prefetch_tmap(&args.st[s].tmA);
+      ptx::prefetch_tmap(&args.st[s].tmB);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int32_t total = (args.first_stage == args.last_stage) ? (args.first_stage == 0 ? args.tiles0 : args.tiles1)
+                                                              : args.tiles0 + args.tiles1;
+  const uint64_t pto = args.pipe_timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ scheduler + TMA
+    if (lane == 0) {
+      const uint64_t pol_a = ptx::l2_policy_evict_last();
+      const uint64_t pol_b = ptx::l2_policy_evict_normal();
+      const bool reorder = !(args.flags_bits & kFlagNoReorder);
+      uint32_t it = 0, tcount = 0;
+      bool ok = true;
+      while (true) {
+        int32_t t = (int32_t)atomicAdd(args.ctrl + CTRL_COUNTER + args.queue, 1u);
+        bool done = t >= total || !ok || *abort_flag;
+        const int slot = tcount % C::kSlots;
+        if (!ptx::mbar_wait_bounded(&qempty[slot], ((tcount / C::kSlots) & 1u) ^ 1u, pto)) {
+          record_error(args, ERRC_PIPELINE, 0xFFFFFF, 1);
+          *abort_flag = 1;
+          done = true;
+        }
+        qtile[slot] = done ? -1 : t;
+        ptx::mbar_arrive(&qfull[slot]);
+        ++tcount;
+        if (done) break;
+
+        const TileRef tr = decode_tile(args, t);
+        const StageArgs& SA = args.st[tr.s];
+        const int32_t KB = SA.g.k_blocks;
+        const uint32_t tx = a_tile_bytes(SA.g) + (uint32_t)C::kBBytes;
+        const bool cons = (tr.s == 1);
+        DepTracker dt;
+        dt.reset();
+        int32_t bnext = 0;
+        auto do_waits = [&](int32_t kb) {
+          if (!cons) return;
+          Wait w[kMaxWaits];
+          const int n = dt.next(SA.g, args.dep, tr.m, kb, w);
+          for (int i = 0; i < n; ++i) wait_flag(args, w[i].flag, args.epoch * w[i].per_run, t, kb);
+          if (n > 0) ptx::fence_proxy_async_global();
+        };
+        for (int32_t kb = 0; kb < KB && ok; ++kb) {
+          if (!reorder) do_waits(kb);
+          const int32_t blimit = reorder ? min(KB, kb + S) : kb + 1;
+          while (bnext < blimit) {
+            const uint32_t j = it + (uint32_t)bnext;
+            const int st = (int)(j % S);
+            if (!ptx::mbar_wait_bounded(&empty[st], ((j / S) & 1u) ^ 1u, pto) || *abort_flag) {
+              record_error(args, ERRC_PIPELINE, t, 2);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&full[st], tx);
+            issue_b<BN>(args, tr, bnext, smem_b(st), &full[st], pol_b);
+            ++bnext;
+          }
+          if (!ok) break;
+          if (reorder) do_waits(kb);
+          const int st = (int)((it + (uint32_t)kb) % S);
+          issue_a(args, tr, kb, smem_a(st), &full[st], pol_a);
+        }
+        it += (uint32_t)bnext;
+        *it_issued = (int32_t)it;
+        if (!ok) {
+          // hand a terminator to the other roles so that they stop
+          const int slot2 = tcount % C::kSlots;
+          if (ptx::mbar_wait_bounded(&qempty[slot2], ((tcount / C::kSlots) & 1u) ^ 1u, pto)) {
+            qtile[slot2] = -1;
+            ptx::mbar_arrive(&qfull[slot2]);
+          }
+          break;
+        }
+      }
+      // The last CTA to finish claiming resets this launch's tile counter for the next run.
+      __threadfence();
+      const uint32_t prev = atomicAdd(args.ctrl + CTRL_EXIT + args.queue, 1u);
+      if (prev == gridDim.x - 1) {
+        atomicExch(args.ctrl + CTRL_COUNTER + args.queue, 0u);
+        atomicExch(args.ctrl + CTRL_EXIT + args.queue, 0u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint64_t pol_a = ptx::l2_policy_evict_last();
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, BN);
+    uint32_t it = 0, tcount = 0, acount = 0, fpar = 0;
+    bool ok = true;
+    while (ok) {
+      const int slot = tcount % C::kSlots;
+      if (!ptx::mbar_wait_bounded(&qfull[slot], (tcount / C::kSlots) & 1u, pto)) {
+        ok = false;
+        break;
+      }
+      const int32_t t = qtile[slot];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&qempty[slot]);
+      ++tcount;
+      if (t < 0) break;
+      const TileRef tr = decode_tile(args, t);
+      const StageGeo& g = args.st[tr.s].g;
+      const int acc = acount & 1;
+      const uint32_t apar = ((acount >> 1) & 1u) ^ 1u;
+      ++acount;
+      if (!ptx::mbar_wait_bounded(&tempty[acc], apar, pto)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      const bool check = args.sentinel_check && tr.s == 1;
+      const uint32_t abytes = a_tile_bytes(g);
+      for (int32_t kb = 0; kb < g.k_blocks; ++kb, ++it) {
+        const int st = (int)(it % S);
+        if (!ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto)) {
+          ok = false;
+          break;
+        }
+        fpar ^= 1u << st;
+        if (check) {
+          // Software validity check of the landed A tile: every bf16 element is compared
+          // with the sentinel; while any still holds it, the A load is issued again.
+          uint64_t t0 = 0;
+          while (true) {
+            bool bad = false;
+            const uint8_t* base = smem_a(st);
+            for (uint32_t off = (uint32_t)lane * 16u; off < abytes; off += 512u) {
+              const uint4 v = ptx::ld_shared_v4(base + off);
+              bad |= has_sentinel_bf16x2(v.x) | has_sentinel_bf16x2(v.y) | has_sentinel_bf16x2(v.z) |
+                     has_sentinel_bf16x2(v.w);
+            }
+            if (!__any_sync(FULL, bad)) break;
+            if (ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u) break;
+            const uint64_t now = ptx::globaltimer();
+            if (t0 == 0) t0 = now;
+            if (now - t0 > args.timeout_ns) {
+              if (lane == 0) record_error(args, ERRC_SENTINEL_TIMEOUT, t, kb);
+              break;
+            }
+            if (lane == 0) {
+              __nanosleep(128);
+              ptx::fence_proxy_async_smem();
+              ptx::mbar_arrive_expect_tx(&full[st], abytes);
+              issue_a(args, tr, kb, smem_a(st), &full[st], pol_a);
+            }
+            __syncwarp();
+            if (!ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto)) {
+              ok = false;
+              break;
+            }
+            fpar ^= 1u << st;
+          }
+          if (!ok) break;
+        }
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t a0 = ptx::smem_u32(smem_a(st));
+          const uint32_t b0 = ptx::smem_u32(smem_b(st));
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            ptx::umma_bf16(d_tmem, ptx::smem_desc_k128(a0 + 32u * k), ptx::smem_desc_k128(b0 + 32u * k), idesc,
+                           (kb | k) != 0 ? 1u : 0u);
+          }
+          ptx::umma_commit(&empty[st]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) ptx::umma_commit(&tfull[acc]);
+      __syncwarp();
+    }
+    if (!ok) {
+      record_error(args, ERRC_PIPELINE, 0xFFFFFF, 3);
+      *abort_flag = 1;
+    }
+    if (lane == 0) {
+      // every MMA this thread issued has completed once mma_done flips
+      ptx::umma_commit(mma_done);
+      ptx::mbar_wait_bounded(mma_done, 0, pto);
+    }
+    __syncwarp();
+    // Abnormal exit only: wait (bounded) for copies the loader issued but nobody consumed.
+    if (lane == 0 && !ok) {
+      const uint32_t issued = (uint32_t)*it_issued;
+      for (uint32_t j = it; j < issued && j < it + S; ++j) {
+        const int st = (int)(j % S);
+        ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto);
+        fpar ^= 1u << st;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    uint32_t tcount = 0, acount = 0;
+    while (true) {
+      const int slot = tcount % C::kSlots;
+      if (!ptx::mbar_wait_bounded(&qfull[slot], (tcount / C::kSlots) & 1u, pto)) break;
+      const int32_t t = qtile[slot];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&qempty[slot]);
+      ++tcount;
+      if (t < 0) break;
+      const TileRef tr = decode_tile(args, t);
+      const StageArgs& SA = args.st[tr.s];
+      const StageGeo& g = SA.g;
+      const int acc = acount & 1;
+      const uint32_t apar = (acount >> 1) & 1u;
+      ++acount;
+      if (!ptx::mbar_wait_bounded(&tfull[acc], apar, pto)) {
+        record_error(args, ERRC_PIPELINE, t, 4);
+        *abort_flag = 1;
+        break;
+      }
+      ptx::tc_fence_after();
+
+      int64_t grow;
+      bool valid;
+      if (g.a_mode == AMODE_GEMM) {
+        grow = (int64_t)tr.m * kBM + row;
+        valid = grow < g.M;
+      } else {
+        const int32_t n = tr.m / g.tpi, hb = tr.m % g.tpi;
+        const int32_t hl = row / g.img_w, w = row % g.img_w;
+        const int32_t h = hb * g.th + hl;
+        valid = (hl < g.th) && (h < g.img_h);
+        grow = ((int64_t)n * g.img_h + h) * g.img_w + w;
+      }
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(SA.out) + (valid ? grow * (int64_t)g.N : 0);
+      const int32_t col0 = tr.c * g.n_out;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const int nchunks = g.n_out / 32;
+      for (int j = 0; j < nchunks; ++j) {
+        uint32_t v[32];
+        float f[32];
+        if (g.epi == EPI_SWIGLU) {
+          uint32_t u[32];
+          ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(j * 32), v);
+          ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(BN / 2 + j * 32), u);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) f[i] = silu_f(__uint_as_float(v[i])) * __uint_as_float(u[i]);
+        } else {
+          ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(j * 32), v);
+          ptx::tmem_ld_wait();
+          if (g.epi == EPI_GELU) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = gelu_f(__uint_as_float(v[i]));
+          } else if (g.epi == EPI_RELU) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = fmaxf(__uint_as_float(v[i]), 0.0f);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+          }
+        }
+        uint32_t p[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+        if (valid) {
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const int32_t col = col0 + j * 32 + ch * 8;
+            if (col < g.N) ptx::st_relaxed_gpu_b128(orow + col, p[4 * ch], p[4 * ch + 1], p[4 * ch + 2], p[4 * ch + 3]);
+          }
+        }
+      }
+      // Arrive on epi_done before releasing the accumulator: a thread can reach this
+      // accumulator's next tile only after every thread released it, so each phase of
+      // epi_done[acc] counts the arrivals of exactly one tile.
+      ptx::mbar_arrive(&epi_done[acc]);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tempty[acc]);
+      if (tr.s == 0 && threadIdx.x == 64) {
+        const int32_t flag = producer_flag(args.dep, tr.m, tr.c);
+        if (flag >= 0) {
+          // cuSync §IV-E "Post": after all of the tile's stores (the epi_done barrier
+          // orders the 128 threads' stores before this thread), one device-scope release.
+          if (!ptx::mbar_wait_bounded(&epi_done[acc], apar, pto)) {
+            record_error(args, ERRC_PIPELINE, t, 5);
+            *abort_flag = 1;
+          } else if (!((args.flags_bits & kDebugSkipPost) && tr.m == 0 && tr.c == 0)) {
+            ptx::fence_acq_rel_gpu();
+            ptx::red_release_gpu_add(args.flags + flag, 1u);
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+  if (args.pdl_role == 2 && threadIdx.x == 0) ptx::pdl_wait();
+}
+
+// Fill a buffer with the bf16 sentinel 0x8000 using 16-byte stores (CUDA-FGS §4.6.4.2,
+// initialisation "in a separate kernel").
+__global__ void sentinel_fill_kernel(uint4* buf, int64_t n16) {
+  const uint4 s = make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
+    buf[i] = s;
+}
+
+}  // namespace cusync

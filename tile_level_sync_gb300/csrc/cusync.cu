@@ -1,0 +1,604 @@
+// Host side of the C ABI declared in include/cusync.h: argument validation, the wave
+// planner, chain state, TMA descriptors and kernel launches.
+//
+// Sources: "A Framework for Fine-Grained Synchronization of Dependent GPU Kernels"
+// (cuSync) §II-A (waves), §III-A (fused waves), §IV-A..C (launch on separate streams,
+// stage processing order, tile processing order), §V (optimisations); CUDA Programming
+// Guide §4.6 (sentinel protocol, programmatic dependent launch, §4.6.5 progress).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "../../include/cusync.h"
+#include "chain_kernel.cuh"
+#include "geometry.h"
+
+using namespace cusync;
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // one second
+
+bool log_enabled() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = std::getenv("CUSYNC_LOG");
+    v = (e && e[0] == '1') ? 1 : 0;
+  }
+  return v == 1;
+}
+
+#define CUSYNC_LOG(...)                          \
+  do {                                           \
+    if (log_enabled()) {                         \
+      std::fprintf(stderr, "[cusync] " __VA_ARGS__); \
+      std::fprintf(stderr, "\n");                \
+    }                                            \
+  } while (0)
+
+cusync_status_t cuda_fail(cudaError_t e, const char* what) {
+  CUSYNC_LOG("%s: %s", what, cudaGetErrorString(e));
+  return CUSYNC_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------- planning
+
+struct Plan {
+  int32_t bn;           // accumulator tile width (UMMA N)
+  StageGeo geo[2];
+  DepCfg dep;
+  int64_t num_flags;
+};
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Image rows per row tile of a convolution: the fewest tiles per image whose rows fit
+// the 128-row UMMA tile, then the rows spread evenly over them.
+int32_t conv_rows_per_tile(int32_t h, int32_t w) {
+  const int32_t max_rows = kBM / w;
+  const int32_t tpi = (int32_t)ceil_div(h, max_rows);
+  return (int32_t)ceil_div(h, tpi);
+}
+
+int32_t default_tile_n(const cusync_chain_desc_t& d) {
+  if (d.tile_n) return d.tile_n;
+  return 256;
+}
+
+cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
+  if (d.kind < CUSYNC_CHAIN_MLP_GELU || d.kind > CUSYNC_CHAIN_CONV_RELU) return CUSYNC_ERR_INVALID_ARG;
+  if (d.policy < CUSYNC_POLICY_STREAM || d.policy > CUSYNC_POLICY_SENTINEL) return CUSYNC_ERR_INVALID_ARG;
+  if (d.launch != CUSYNC_LAUNCH_PERSISTENT && d.launch != CUSYNC_LAUNCH_PDL) return CUSYNC_ERR_INVALID_ARG;
+  const int32_t bn = default_tile_n(d);
+  if (bn != 128 && bn != 256) return CUSYNC_ERR_UNSUPPORTED;
+  std::memset(p, 0, sizeof(*p));
+  p->bn = bn;
+  StageGeo& g0 = p->geo[0];
+  StageGeo& g1 = p->geo[1];
+  if (d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU) {
+    if (d.M < 1 || d.K < 1 || d.N1 < 1 || d.N2 < 1) return CUSYNC_ERR_INVALID_ARG;
+    // TMA row strides and 16-byte output chunks need multiples of 8 bf16 elements.
+    if (d.K % 8 || d.N1 % 8 || d.N2 % 8) return CUSYNC_ERR_UNSUPPORTED;
+    if (d.M > (1ll << 30) || d.K > (1ll << 30) || d.N1 > (1ll << 30) || d.N2 > (1ll << 30))
+      return CUSYNC_ERR_UNSUPPORTED;
+    const bool swiglu = d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
+    g0.a_mode = AMODE_GEMM;
+    g0.epi = swiglu ? EPI_SWIGLU : EPI_GELU;
+    g0.M = (int32_t)d.M;
+    g0.N = (int32_t)d.N1;
+    g0.K = (int32_t)d.K;
+    g0.n_out = swiglu ? bn / 2 : bn;
+    g1.a_mode = AMODE_GEMM;
+    g1.epi = EPI_NONE;
+    g1.M = (int32_t)d.M;
+    g1.N = (int32_t)d.N2;
+    g1.K = (int32_t)d.N1;
+    g1.n_out = bn;
+    for (StageGeo* g : {&g0, &g1}) {
+      g->m_tiles = (int32_t)ceil_div(g->M, kBM);
+      g->n_tiles = (int32_t)ceil_div(g->N, g->n_out);
+      g->k_blocks = (int32_t)ceil_div(g->K, kBK);
+    }
+  } else {
+    if (d.n < 1 || d.h < 1 || d.w < 1 || d.c < 1 || d.k_out < 1) return CUSYNC_ERR_INVALID_ARG;
+    if (d.c % kBK || d.k_out % kBK) return CUSYNC_ERR_UNSUPPORTED;  // whole channel blocks per tap
+    if (d.w > kBM || d.w > 256) return CUSYNC_ERR_UNSUPPORTED;       // one image row per box row run
+    if ((int64_t)d.n * d.h * d.w > (1ll << 30)) return CUSYNC_ERR_UNSUPPORTED;
+    if (ceil_div(d.k_out, bn) > kMaxConvColTiles) return CUSYNC_ERR_UNSUPPORTED;
+    const int32_t th = conv_rows_per_tile(d.h, d.w);
+    const int32_t tpi = (int32_t)ceil_div(d.h, th);
+    const int32_t cins[2] = {d.c, d.k_out};
+    for (int s = 0; s < 2; ++s) {
+      StageGeo& g = p->geo[s];
+      g.a_mode = AMODE_CONV;
+      g.epi = s == 0 ? EPI_RELU : EPI_NONE;
+      g.M = d.n * d.h * d.w;
+      g.N = d.k_out;
+      g.K = 9 * cins[s];
+      g.n_out = bn;
+      g.img_n = d.n;
+      g.img_h = d.h;
+      g.img_w = d.w;
+      g.cin = cins[s];
+      g.th = th;
+      g.tpi = tpi;
+      g.cblocks = cins[s] / kBK;
+      g.m_tiles = d.n * tpi;
+      g.n_tiles = (int32_t)ceil_div(d.k_out, bn);
+      g.k_blocks = 9 * g.cblocks;
+    }
+  }
+  DepCfg& dep = p->dep;
+  dep.policy = d.policy;
+  dep.prod_m_tiles = g0.m_tiles;
+  dep.prod_n_tiles = g0.n_tiles;
+  dep.prod_n_out = g0.n_out;
+  dep.G = 1;
+  dep.D = g0.n_tiles;
+  if (d.policy == CUSYNC_POLICY_STRIDED_TILE) {
+    const int32_t G = d.strided_group ? d.strided_group : 2;
+    if (G < 1 || g0.n_tiles % G) return CUSYNC_ERR_UNSUPPORTED;
+    dep.G = G;
+    dep.D = g0.n_tiles / G;
+  }
+  p->num_flags = num_flags(dep);
+  if (p->num_flags > (1ll << 24)) return CUSYNC_ERR_UNSUPPORTED;
+  return CUSYNC_OK;
+}
+
+int query_num_sms(int32_t requested, int* out) {
+  if (requested > 0) {
+    *out = requested;
+    return 0;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  *out = sms;
+  return 0;
+}
+
+// ----------------------------------------------------------------------------- TMA maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_encode_mu;
+
+bool load_encoder() {
+  std::lock_guard<std::mutex> lk(g_encode_mu);
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// 2-D row-major bf16 [rows, cols] with a [box_rows, 64] box, 128-byte swizzle.
+bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 4-D NHWC bf16 image [n, h, w, c] with a [1, th, w, 64] box (all of an image row run,
+// one 64-channel block), 128-byte swizzle; out-of-image elements read as zero.
+bool encode_nhwc(CUtensorMap* m, const void* ptr, uint64_t n, uint64_t h, uint64_t w, uint64_t c, uint32_t th) {
+  cuuint64_t dims[4] = {c, w, h, n};
+  cuuint64_t strides[3] = {c * 2, w * c * 2, h * w * c * 2};
+  cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)w, th, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <int BN>
+cudaError_t set_kernel_attrs() {
+  cudaError_t e = cudaFuncSetAttribute(chain_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       KCfg<BN>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(chain_kernel<BN>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
+}  // namespace
+
+// ----------------------------------------------------------------------------- chain
+
+struct cusync_chain {
+  cusync_chain_desc_t d;
+  Plan plan;
+  int device;
+  int num_sms;
+  uint32_t* state;       // CTRL_WORDS control words, then the semaphores
+  uint32_t epoch;
+  int32_t grid_fused, grid_prod, grid_cons;
+  // TMA descriptors cached by operand pointers
+  const void* cached[5];
+  bool maps_valid;
+  ChainArgs args;
+};
+
+namespace {
+
+template <int BN>
+cudaError_t launch_chain(const ChainArgs& a, int grid, bool cooperative, bool pdl_secondary, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(KCfg<BN>::kThreads);
+  cfg.dynamicSmemBytes = KCfg<BN>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  int na = 0;
+  if (cooperative) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  } else if (pdl_secondary) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, chain_kernel<BN>, a);
+}
+
+cudaError_t launch_any(int bn, const ChainArgs& a, int grid, bool coop, bool pdl2, cudaStream_t s) {
+  return bn == 256 ? launch_chain<256>(a, grid, coop, pdl2, s) : launch_chain<128>(a, grid, coop, pdl2, s);
+}
+
+cusync_status_t run_chain(cusync_chain* ch, const void* a0, const void* b0, const void* b1, void* h, void* y,
+                          cudaStream_t stream) {
+  const cusync_chain_desc_t& d = ch->d;
+  const Plan& p = ch->plan;
+  if (!aligned16(a0) || !aligned16(b0) || !aligned16(b1) || !aligned16(h) || !aligned16(y))
+    return CUSYNC_ERR_INVALID_ARG;
+  if (h == y || h == a0 || y == a0) return CUSYNC_ERR_INVALID_ARG;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != ch->device) return CUSYNC_ERR_INVALID_ARG;
+  ChainArgs& A = ch->args;
+  const void* ptrs[5] = {a0, b0, b1, h, y};
+  if (!ch->maps_valid || std::memcmp(ptrs, ch->cached, sizeof(ptrs)) != 0) {
+    bool ok = true;
+    if (d.kind == CUSYNC_CHAIN_CONV_RELU) {
+      const StageGeo& g0 = p.geo[0];
+      ok &= encode_nhwc(&A.st[0].tmA, a0, d.n, d.h, d.w, d.c, (uint32_t)g0.th);
+      ok &= encode_2d(&A.st[0].tmB, b0, (uint64_t)d.k_out, (uint64_t)9 * d.c, (uint32_t)p.bn);
+      ok &= encode_nhwc(&A.st[1].tmA, h, d.n, d.h, d.w, d.k_out, (uint32_t)g0.th);
+      ok &= encode_2d(&A.st[1].tmB, b1, (uint64_t)d.k_out, (uint64_t)9 * d.k_out, (uint32_t)p.bn);
+    } else {
+      const bool swiglu = d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
+      ok &= encode_2d(&A.st[0].tmA, a0, (uint64_t)d.M, (uint64_t)d.K, (uint32_t)kBM);
+      ok &= encode_2d(&A.st[0].tmB, b0, (uint64_t)(swiglu ? 2 * d.N1 : d.N1), (uint64_t)d.K,
+                      (uint32_t)(swiglu ? p.bn / 2 : p.bn));
+      ok &= encode_2d(&A.st[1].tmA, h, (uint64_t)d.M, (uint64_t)d.N1, (uint32_t)kBM);
+      ok &= encode_2d(&A.st[1].tmB, b1, (uint64_t)d.N2, (uint64_t)d.N1, (uint32_t)p.bn);
+    }
+    if (!ok) {
+      ch->maps_valid = false;
+      return CUSYNC_ERR_INVALID_ARG;
+    }
+    std::memcpy(ch->cached, ptrs, sizeof(ptrs));
+    ch->maps_valid = true;
+  }
+  A.st[0].out = h;
+  A.st[1].out = y;
+  A.epoch = ++ch->epoch;
+
+  cudaError_t e;
+  if (d.policy == CUSYNC_POLICY_SENTINEL && !(d.flags & CUSYNC_DEBUG_SKIP_INIT)) {
+    const int64_t bytes = (int64_t)p.geo[0].M * p.geo[0].N * 2;
+    const int64_t n16 = bytes / 16;
+    int blocks = (int)std::min<int64_t>(ceil_div(n16, 256), (int64_t)ch->num_sms * 8);
+    if (blocks < 1) blocks = 1;
+    sentinel_fill_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<uint4*>(h), n16);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "sentinel fill launch");
+  }
+  const bool two_kernels = d.policy == CUSYNC_POLICY_STREAM || d.launch == CUSYNC_LAUNCH_PDL;
+  if (!two_kernels) {
+    ChainArgs a = A;
+    a.queue = 0;
+    a.first_stage = 0;
+    a.last_stage = 1;
+    a.pdl_role = 0;
+    e = launch_any(p.bn, a, ch->grid_fused, /*coop=*/true, false, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fused chain launch");
+    return CUSYNC_OK;
+  }
+  const bool pdl = d.policy != CUSYNC_POLICY_STREAM;
+  ChainArgs a = A;
+  a.queue = 0;
+  a.first_stage = 0;
+  a.last_stage = 0;
+  a.pdl_role = pdl ? 1 : 0;
+  e = launch_any(p.bn, a, ch->grid_prod, false, false, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "producer launch");
+  a.queue = 1;
+  a.first_stage = 1;
+  a.last_stage = 1;
+  a.pdl_role = pdl ? 2 : 0;
+  e = launch_any(p.bn, a, ch->grid_cons, false, pdl, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "consumer launch");
+  return CUSYNC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* cusync_status_string(cusync_status_t s) {
+  switch (s) {
+    case CUSYNC_OK: return "CUSYNC_OK";
+    case CUSYNC_ERR_INVALID_ARG: return "CUSYNC_ERR_INVALID_ARG";
+    case CUSYNC_ERR_UNSUPPORTED: return "CUSYNC_ERR_UNSUPPORTED";
+    case CUSYNC_ERR_CUDA: return "CUSYNC_ERR_CUDA";
+    case CUSYNC_ERR_NOMEM: return "CUSYNC_ERR_NOMEM";
+    case CUSYNC_ERR_TIMEOUT: return "CUSYNC_ERR_TIMEOUT";
+    case CUSYNC_ERR_DEVICE: return "CUSYNC_ERR_DEVICE";
+  }
+  return "CUSYNC_ERR_UNKNOWN";
+}
+
+// [cuSync] §II-A "Thread block Wave Execution" and §III-A.
+cusync_status_t cusync_wave_stats(int64_t tbs0, int64_t tbs1, int32_t occupancy, int32_t num_sms,
+                                  cusync_wave_report_t* out) {
+  if (!out || tbs0 < 0 || tbs1 < 0 || occupancy < 1 || num_sms < 1) return CUSYNC_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  const int64_t cap = (int64_t)occupancy * num_sms;
+  const int64_t tbs[2] = {tbs0, tbs1};
+  int32_t stream = 0;
+  for (int i = 0; i < 2; ++i) {
+    out->tbs[i] = tbs[i];
+    out->waves[i] = (double)tbs[i] / (double)cap;
+    out->waves_ceil[i] = (int32_t)ceil_div(tbs[i], cap);
+    out->util[i] = out->waves_ceil[i] ? (double)tbs[i] / ((double)out->waves_ceil[i] * (double)cap) : 0.0;
+    stream += out->waves_ceil[i];
+  }
+  const int64_t total = tbs0 + tbs1;
+  out->stream_waves = stream;
+  out->fused_waves = (int32_t)ceil_div(total, cap);
+  out->fused_waves_frac = (double)total / (double)cap;
+  out->last_wave_tbs = total == 0 ? 0 : (total % cap == 0 ? cap : total % cap);
+  out->cap = (int32_t)cap;
+  out->occupancy = occupancy;
+  out->num_sms = num_sms;
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_plan_waves(const cusync_chain_desc_t* d, cusync_wave_report_t* out) {
+  if (!d || !out) return CUSYNC_ERR_INVALID_ARG;
+  Plan p;
+  cusync_status_t st = make_plan(*d, &p);
+  if (st != CUSYNC_OK) return st;
+  int sms = 0;
+  if (query_num_sms(d->num_sms, &sms) != 0) return CUSYNC_ERR_CUDA;
+  const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
+  const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
+  st = cusync_wave_stats(t0, t1, 1, sms, out);
+  if (st != CUSYNC_OK) return st;
+  out->tile_m = kBM;
+  out->tile_n = p.bn;
+  out->tile_k = kBK;
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t* out) {
+  if (!d || !out) return CUSYNC_ERR_INVALID_ARG;
+  *out = nullptr;
+  Plan p;
+  cusync_status_t st = make_plan(*d, &p);
+  if (st != CUSYNC_OK) return st;
+  if (!load_encoder()) return CUSYNC_ERR_CUDA;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) {
+    CUSYNC_LOG("device compute capability %d.%d; this library is built for sm_103a", major, minor);
+    return CUSYNC_ERR_UNSUPPORTED;
+  }
+  int dev_sms = 0;
+  if (query_num_sms(0, &dev_sms) != 0) return CUSYNC_ERR_CUDA;
+  const int sms = d->num_sms > 0 ? std::min(d->num_sms, dev_sms) : dev_sms;
+  if ((e = set_kernel_attrs<256>()) != cudaSuccess) return cuda_fail(e, "kernel attributes (256)");
+  if ((e = set_kernel_attrs<128>()) != cudaSuccess) return cuda_fail(e, "kernel attributes (128)");
+  // Load the kernels now rather than at their first launch (CUDA-FGS §4.6.5, "Overlap").
+  cudaFuncAttributes fa;
+  cudaFuncGetAttributes(&fa, chain_kernel<256>);
+  cudaFuncGetAttributes(&fa, chain_kernel<128>);
+  cudaFuncGetAttributes(&fa, sentinel_fill_kernel);
+
+  cusync_chain* ch = new (std::nothrow) cusync_chain();
+  if (!ch) return CUSYNC_ERR_NOMEM;
+  ch->d = *d;
+  if (ch->d.timeout_ns == 0) ch->d.timeout_ns = kDefaultTimeoutNs;
+  ch->plan = p;
+  ch->device = dev;
+  ch->num_sms = sms;
+  const size_t words = CTRL_WORDS + (size_t)p.num_flags;
+  if (cudaMalloc(&ch->state, words * sizeof(uint32_t)) != cudaSuccess) {
+    delete ch;
+    return CUSYNC_ERR_NOMEM;
+  }
+  if ((e = cudaMemset(ch->state, 0, words * sizeof(uint32_t))) != cudaSuccess) {
+    cudaFree(ch->state);
+    delete ch;
+    return cuda_fail(e, "state clear");
+  }
+  ch->epoch = 0;
+  const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
+  const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
+  ch->grid_fused = (int32_t)std::min<int64_t>(sms, t0 + t1);
+  ch->grid_prod = (int32_t)std::min<int64_t>(sms, t0);
+  ch->grid_cons = (int32_t)std::min<int64_t>(sms, t1);
+
+  ChainArgs& A = ch->args;
+  std::memset(&A, 0, sizeof(A));
+  A.st[0].g = p.geo[0];
+  A.st[1].g = p.geo[1];
+  A.st[0].b_half_rows = d->kind == CUSYNC_CHAIN_MLP_SWIGLU ? (int32_t)d->N1 : 0;
+  A.dep = p.dep;
+  A.ctrl = ch->state;
+  A.flags = ch->state + CTRL_WORDS;
+  A.tiles0 = (int32_t)t0;
+  A.tiles1 = (int32_t)t1;
+  A.flags_bits = d->flags;
+  A.sentinel_check = d->policy == CUSYNC_POLICY_SENTINEL ? 1 : 0;
+  A.timeout_ns = ch->d.timeout_ns;
+  A.pipe_timeout_ns = std::max<uint64_t>(4 * ch->d.timeout_ns, 2000000000ull);
+  ch->maps_valid = false;
+  *out = ch;
+  CUSYNC_LOG("chain kind=%d policy=%d launch=%d tiles=%lld+%lld bn=%d sms=%d flags=%lld", d->kind, d->policy,
+             d->launch, (long long)t0, (long long)t1, p.bn, sms, (long long)p.num_flags);
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_run_mlp(cusync_chain_t ch, const void* X, const void* W1t, const void* W2t, void* H, void* Y,
+                               cusync_stream_t stream) {
+  if (!ch) return CUSYNC_ERR_INVALID_ARG;
+  if (ch->d.kind != CUSYNC_CHAIN_MLP_GELU && ch->d.kind != CUSYNC_CHAIN_MLP_SWIGLU) return CUSYNC_ERR_INVALID_ARG;
+  return run_chain(ch, X, W1t, W2t, H, Y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+cusync_status_t cusync_run_conv_chain(cusync_chain_t ch, const void* x, const void* w1, const void* w2, void* y1,
+                                      void* y2, cusync_stream_t stream) {
+  if (!ch) return CUSYNC_ERR_INVALID_ARG;
+  if (ch->d.kind != CUSYNC_CHAIN_CONV_RELU) return CUSYNC_ERR_INVALID_ARG;
+  return run_chain(ch, x, w1, w2, y1, y2, reinterpret_cast<cudaStream_t>(stream));
+}
+
+cusync_status_t cusync_chain_reset(cusync_chain_t ch, cusync_stream_t stream) {
+  if (!ch) return CUSYNC_ERR_INVALID_ARG;
+  const size_t words = CTRL_WORDS + (size_t)ch->plan.num_flags;
+  cudaError_t e = cudaMemsetAsync(ch->state, 0, words * sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "state reset");
+  ch->epoch = 0;
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_chain_check(cusync_chain_t ch, cusync_stream_t stream, uint32_t* code, uint32_t* detail) {
+  if (!ch) return CUSYNC_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  uint32_t w[2] = {0, 0};
+  e = cudaMemcpy(w, ch->state, sizeof(w), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "error word read");
+  if (code) *code = w[0];
+  if (detail) *detail = w[1];
+  if (w[0] == 0) return CUSYNC_OK;
+  const uint32_t cls = w[0] >> 24;
+  CUSYNC_LOG("device error class %u tile %u detail 0x%x", cls, w[0] & 0xFFFFFFu, w[1]);
+  cusync_status_t r = CUSYNC_ERR_DEVICE;
+  if (cls == ERRC_FLAG_TIMEOUT || cls == ERRC_SENTINEL_TIMEOUT) r = CUSYNC_ERR_TIMEOUT;
+  if (cusync_chain_reset(ch, stream) != CUSYNC_OK) return CUSYNC_ERR_CUDA;
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  return r;
+}
+
+cusync_status_t cusync_plan_info(const cusync_chain_desc_t* d, cusync_chain_info_t* out) {
+  if (!d || !out) return CUSYNC_ERR_INVALID_ARG;
+  Plan p;
+  cusync_status_t st = make_plan(*d, &p);
+  if (st != CUSYNC_OK) return st;
+  int sms = 0;
+  if (query_num_sms(d->num_sms, &sms) != 0) return CUSYNC_ERR_CUDA;
+  std::memset(out, 0, sizeof(*out));
+  for (int s = 0; s < 2; ++s) {
+    out->m_tiles[s] = p.geo[s].m_tiles;
+    out->n_tiles[s] = p.geo[s].n_tiles;
+    out->k_blocks[s] = p.geo[s].k_blocks;
+    out->n_out[s] = p.geo[s].n_out;
+  }
+  out->tile_m = kBM;
+  out->tile_n = p.bn;
+  out->tile_k = kBK;
+  out->strided_group = p.dep.G;
+  out->strided_distance = p.dep.D;
+  out->num_flags = (int32_t)p.num_flags;
+  const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
+  const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
+  const bool two = d->policy == CUSYNC_POLICY_STREAM || d->launch == CUSYNC_LAUNCH_PDL;
+  out->grid[0] = (int32_t)std::min<int64_t>(sms, two ? t0 : t0 + t1);
+  out->grid[1] = two ? (int32_t)std::min<int64_t>(sms, t1) : 0;
+  out->num_sms = sms;
+  out->conv_rows_per_tile = d->kind == CUSYNC_CHAIN_CONV_RELU ? p.geo[0].th : 0;
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_consumer_waits(const cusync_chain_desc_t* d, int32_t m_tile, int32_t* kb, int32_t* flag,
+                                      uint32_t* per_run, int32_t max, int32_t* n_out) {
+  if (!d || !n_out || max < 0) return CUSYNC_ERR_INVALID_ARG;
+  Plan p;
+  cusync_status_t st = make_plan(*d, &p);
+  if (st != CUSYNC_OK) return st;
+  const StageGeo& g = p.geo[1];
+  if (m_tile < 0 || m_tile >= g.m_tiles) return CUSYNC_ERR_INVALID_ARG;
+  if (max > 0 && (!kb || !flag || !per_run)) return CUSYNC_ERR_INVALID_ARG;
+  DepTracker dt;
+  dt.reset();
+  int32_t n = 0;
+  for (int32_t k = 0; k < g.k_blocks; ++k) {
+    Wait w[kMaxWaits];
+    const int c = dt.next(g, p.dep, m_tile, k, w);
+    for (int i = 0; i < c; ++i, ++n) {
+      if (n < max) {
+        kb[n] = k;
+        flag[n] = w[i].flag;
+        per_run[n] = w[i].per_run;
+      }
+    }
+  }
+  *n_out = n;
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_producer_flag(const cusync_chain_desc_t* d, int32_t m_tile, int32_t n_tile, int32_t* flag) {
+  if (!d || !flag) return CUSYNC_ERR_INVALID_ARG;
+  Plan p;
+  cusync_status_t st = make_plan(*d, &p);
+  if (st != CUSYNC_OK) return st;
+  const StageGeo& g = p.geo[0];
+  if (m_tile < 0 || m_tile >= g.m_tiles || n_tile < 0 || n_tile >= g.n_tiles) return CUSYNC_ERR_INVALID_ARG;
+  *flag = producer_flag(p.dep, m_tile, n_tile);
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_producer_col(const cusync_chain_desc_t* d, int32_t y, int32_t* col) {
+  if (!d || !col) return CUSYNC_ERR_INVALID_ARG;
+  Plan p;
+  cusync_status_t st = make_plan(*d, &p);
+  if (st != CUSYNC_OK) return st;
+  if (y < 0 || y >= p.geo[0].n_tiles) return CUSYNC_ERR_INVALID_ARG;
+  *col = producer_col(p.dep, y);
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_destroy_chain(cusync_chain_t ch) {
+  if (!ch) return CUSYNC_OK;
+  cudaError_t e = cudaSuccess;
+  if (ch->state) e = cudaFree(ch->state);
+  delete ch;
+  return e == cudaSuccess ? CUSYNC_OK : CUSYNC_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,192 @@
+// Tile geometry, tile order and dependency tracking of a producer -> consumer chain.
+//
+// Everything here is plain integer logic compiled for both the host and the device:
+// the chain kernel calls it to decide which semaphores to wait on and to post, and the
+// host library exposes the same functions (cusync_consumer_waits,
+// cusync_producer_flag) so that the dependency logic the GPU executes can be checked
+// on a CPU.
+//
+// Sources:
+//  * "A Framework for Fine-Grained Synchronization of Dependent GPU Kernels" (cuSync),
+//    §II-C (tiled GEMM: tile C^{xy} reads a row of A tiles), §IV-C (tile processing
+//    order), §IV-E (TileSync, RowSync, StridedSync, Conv2DTileSync; Fig. fig:ex and
+//    Fig. fig:use-case:self-attention:strided).
+#pragma once
+#include <cstdint>
+
+#if defined(__CUDACC__)
+#define CUSYNC_HD __host__ __device__ __forceinline__
+#else
+#define CUSYNC_HD inline
+#endif
+
+namespace cusync {
+
+// Policy and epilogue codes (same values as the public enums in cusync.h).
+enum : int32_t { POL_STREAM = 0, POL_ROW = 1, POL_TILE = 2, POL_STRIDED = 3, POL_SENTINEL = 4 };
+enum : int32_t { EPI_NONE = 0, EPI_GELU = 1, EPI_SWIGLU = 2, EPI_RELU = 3 };
+enum : int32_t { AMODE_GEMM = 0, AMODE_CONV = 1 };
+
+constexpr int32_t kBM = 128;  // output rows (tokens / pixels) per tile: UMMA M
+constexpr int32_t kBK = 64;   // reduction elements per k-block: one 128-byte swizzle row of bf16
+constexpr int32_t kMaxConvColTiles = 16;
+constexpr int32_t kMaxWaits = 4;
+
+// One GEMM stage of the chain: out[M, N] = act(A[M, K] x B[N, K]^T).
+// For a convolution stage, A is the implicit im2col matrix of an NHWC image and the
+// M rows of a tile are `th` whole image rows of one image (th * img_w <= 128).
+struct StageGeo {
+  int32_t a_mode;    // AMODE_*
+  int32_t epi;       // EPI_*
+  int32_t M;         // output rows: tokens, or pixels N*P*Q
+  int32_t N;         // output columns (channels)
+  int32_t K;         // reduction length (conv: 9 * input channels)
+  int32_t m_tiles;   // row tiles
+  int32_t n_tiles;   // column tiles
+  int32_t k_blocks;  // ceil(K / kBK)
+  int32_t n_out;     // output columns written per tile (BN, or BN/2 for SwiGLU)
+  // convolution only
+  int32_t img_n, img_h, img_w, cin;  // input image (= output image: 3x3, stride 1, pad 1)
+  int32_t th;                        // image rows per row tile
+  int32_t tpi;                       // row tiles per image = ceil(img_h / th)
+  int32_t cblocks;                   // cin / kBK channel blocks per filter tap
+};
+
+// Consumer-side view of the producer's semaphores.
+struct DepCfg {
+  int32_t policy;        // POL_*
+  int32_t prod_m_tiles;  // producer row tiles
+  int32_t prod_n_tiles;  // producer column tiles (nt)
+  int32_t prod_n_out;    // H columns per producer tile
+  int32_t G;             // StridedSync group size (tiles sharing one semaphore)
+  int32_t D;             // StridedSync distance = nt / G
+};
+
+struct Wait {
+  int32_t flag;      // semaphore index
+  uint32_t per_run;  // posts the semaphore receives per chain run
+};
+
+// Number of semaphores the policy needs.
+CUSYNC_HD int64_t num_flags(const DepCfg& d) {
+  switch (d.policy) {
+    case POL_TILE: return (int64_t)d.prod_m_tiles * d.prod_n_tiles;
+    case POL_ROW: return d.prod_m_tiles;
+    case POL_STRIDED: return (int64_t)d.prod_m_tiles * d.D;
+    default: return 0;
+  }
+}
+
+// Producer column tile visited at position y of a row.  RowMajor for every policy but
+// StridedSync, whose prodOrder visits the G members of group 0 (columns 0, D, 2D, ...)
+// first, then those of group 1, and so on.
+CUSYNC_HD int32_t producer_col(const DepCfg& d, int32_t y) {
+  if (d.policy == POL_STRIDED) return (y % d.G) * d.D + y / d.G;
+  return y;
+}
+
+// Semaphore the producer posts after finishing tile (m, c); -1 if the policy posts none.
+CUSYNC_HD int32_t producer_flag(const DepCfg& d, int32_t m, int32_t c) {
+  switch (d.policy) {
+    case POL_TILE: return m * d.prod_n_tiles + c;
+    case POL_ROW: return m;
+    case POL_STRIDED: return m * d.D + (c % d.D);
+    default: return -1;
+  }
+}
+
+// Image-row range (in producer row tiles) read by consumer row tile m for filter row r.
+CUSYNC_HD void conv_row_tiles(const StageGeo& g, int32_t m, int32_t r, int32_t* lo_tile, int32_t* hi_tile) {
+  const int32_t n = m / g.tpi, hb = m % g.tpi;
+  const int32_t p0 = hb * g.th;
+  int32_t p1 = p0 + g.th - 1;
+  if (p1 > g.img_h - 1) p1 = g.img_h - 1;
+  int32_t lo = p0 + r - 1, hi = p1 + r - 1;  // 3x3, pad 1
+  if (lo < 0) lo = 0;
+  if (hi > g.img_h - 1) hi = g.img_h - 1;
+  if (hi < lo) {  // a tile whose shifted window lies wholly outside the image
+    *lo_tile = 0;
+    *hi_tile = -1;
+    return;
+  }
+  *lo_tile = n * g.tpi + lo / g.th;
+  *hi_tile = n * g.tpi + hi / g.th;
+}
+
+// Tracks which producer tiles a consumer row tile has already waited for, and yields
+// the semaphore waits needed before each A k-block, in the consumer's fixed natural
+// k order.  Each producer tile is waited for once, when a k-block first reads it
+// (TileSync), or with its whole group (StridedSync), or all rows up front before the
+// first k-block (RowSync).  Sentinel and stream-ordered chains wait on no semaphore.
+struct DepTracker {
+  int32_t last_c;                      // GEMM: last producer column tile waited
+  int32_t lo[kMaxConvColTiles];        // conv: waited producer row-tile interval per column tile
+  int32_t hi[kMaxConvColTiles];
+
+  CUSYNC_HD void reset() {
+    last_c = -1;
+    for (int i = 0; i < kMaxConvColTiles; ++i) {
+      lo[i] = 1;
+      hi[i] = 0;  // empty interval
+    }
+  }
+
+  CUSYNC_HD int next(const StageGeo& cons, const DepCfg& d, int32_t m, int32_t kb, Wait* out) {
+    const int32_t pol = d.policy;
+    if (pol != POL_TILE && pol != POL_ROW && pol != POL_STRIDED) return 0;
+    int n = 0;
+    if (cons.a_mode == AMODE_GEMM) {
+      const int32_t c = (kb * kBK) / d.prod_n_out;
+      if (pol == POL_ROW) {
+        if (kb == 0) out[n++] = Wait{m, (uint32_t)d.prod_n_tiles};
+        return n;
+      }
+      if (c == last_c) return 0;
+      last_c = c;
+      if (pol == POL_TILE) {
+        out[n++] = Wait{m * d.prod_n_tiles + c, 1u};
+      } else if (c < d.D) {  // StridedSync: group c is first touched at column c
+        out[n++] = Wait{m * d.D + c, (uint32_t)d.G};
+      }
+      return n;
+    }
+    // convolution: k = (r*3 + s)*cin + channel
+    const int32_t tap = kb / cons.cblocks, cb = kb % cons.cblocks;
+    const int32_t r = tap / 3;
+    if (pol == POL_ROW) {
+      if (kb != 0) return 0;
+      // union over the three filter rows (consecutive windows overlap or touch, so the
+      // union is one interval of row tiles)
+      int32_t a = 0x7FFFFFFF, b = -1;
+      for (int32_t rr = 0; rr < 3; ++rr) {
+        int32_t lo_t, hi_t;
+        conv_row_tiles(cons, m, rr, &lo_t, &hi_t);
+        if (hi_t < lo_t) continue;
+        if (lo_t < a) a = lo_t;
+        if (hi_t > b) b = hi_t;
+      }
+      for (int32_t mp = a; mp <= b && n < kMaxWaits; ++mp) out[n++] = Wait{mp, (uint32_t)d.prod_n_tiles};
+      return n;
+    }
+    const int32_t c = (cb * kBK) / d.prod_n_out;
+    int32_t a, b;
+    conv_row_tiles(cons, m, r, &a, &b);
+    for (int32_t mp = a; mp <= b && n < kMaxWaits; ++mp) {
+      if (lo[c] <= mp && mp <= hi[c]) continue;
+      if (pol == POL_TILE) {
+        out[n++] = Wait{mp * d.prod_n_tiles + c, 1u};
+        if (lo[c] > hi[c]) { lo[c] = mp; hi[c] = mp; }
+        else { if (mp < lo[c]) lo[c] = mp; if (mp > hi[c]) hi[c] = mp; }
+      } else {  // StridedSync: the whole group of column c, for row tile mp
+        out[n++] = Wait{mp * d.D + (c % d.D), (uint32_t)d.G};
+        for (int32_t cc = c % d.D; cc < d.prod_n_tiles; cc += d.D) {
+          if (lo[cc] > hi[cc]) { lo[cc] = mp; hi[cc] = mp; }
+          else { if (mp < lo[cc]) lo[cc] = mp; if (mp > hi[cc]) hi[cc] = mp; }
+        }
+      }
+    }
+    return n;
+  }
+};
+
+}  // namespace cusync
