@@ -1,0 +1,620 @@
+#!/usr/bin/env python3
+"""Benchmark of the tile-synchronised dependent GEMM chain on GB300.
+
+One step = one run of the whole hot path on one batch of synthetic input: the
+chain's tile-counter/semaphore state carried by epoch, the producer GEMM with its
+fused GeLU epilogue publishing tiles, and the consumer GEMM waiting on them -- one
+persistent kernel launch (plus the sentinel fill under the sentinel policy).  The
+headline workload is the GPT-3-shaped MLP slice X[256,12288] . W1[12288,6144] ->
+GeLU -> . W2[6144,12288] (bf16, fp32 accumulation), timed with CUDA events on the
+launching stream for the best tile-synchronisation policy, next to the
+stream-serialised two-kernel chain.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead
+(on the host cores, a bounded sample of the same workload per step).
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs and TFLOP/s per dependent GEMM chain vs stream-serialised; % of BF16 peak"
+UNIT = "TFLOP/s"
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Pages' own number for this workload: MLP, batch 256, TileSync, 840 us per chain on a
+# Tesla V100 in fp16 ([cuSync] Table tab:waves:mlp).  Context on other hardware.
+PAGES_US_B256 = 840.0
+# DRAM bytes (read + write) per launch of the fused chain kernel from one ncu capture
+# (profiles/chain_kernel_full_<workload>_row.md), valid only for the kernel sources the
+# capture was taken on (sha256 of tile_level_sync_gb300/csrc/*).
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tile_level_sync_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload, policy, launch, tile_n):
+    rec = NCU_TRAFFIC.get((workload, policy, launch, tile_n))
+    if rec and rec[1] == kernel_source_hash():
+        return rec[0]
+    return None
+
+
+def reduce_max(value, device):
+    """Max of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step, world, ms_per_step):
+    """Whole-job TFLOP/s: every rank ran the same step; time is the slowest rank's."""
+    return world * flops_per_step / (ms_per_step * 1e-3) / 1e12
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=50)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="gpt3_mlp_m256")
+    p.add_argument("--policies", default="ROW,TILE,STRIDED,SENTINEL")
+    p.add_argument("--launch", default="persistent", choices=["persistent", "pdl"])
+    p.add_argument("--tile-n", type=int, default=0)
+    p.add_argument("--raster", type=int, default=0)
+    p.add_argument("--l2-prefetch", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sweep-out", default="", help="also time every policy/launch/tile of each workload "
+                   "in the comma list --sweep and write the results to this JSON file")
+    p.add_argument("--sweep", default="")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) with host timestamps, for the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_id), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inwin = [p for (t, p) in self.samples if t0 <= t <= t1]
+        used = inwin
+        note = "samples inside the timed region"
+        if len(inwin) < 1 and self.samples:
+            # region shorter than the sampling period: nearest samples around it
+            near = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:2]
+            used = [p for (_, p) in near]
+            note = "timed region shorter than the 200 ms sampling period: nearest samples"
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in used if num(p[1]) is not None]
+        smax = [num(p[2]) for p in used if num(p[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in used:
+            for name, v in zip(names, p[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(used), "note": note,
+                "power_w_max": max([num(p[3]) or 0.0 for p in used])}
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+
+
+def cpu_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count() or 1
+
+
+def oracle_sample_runner(wl, inputs):
+    """Return (fn(rows) -> flops, rows_total): the oracle on a subset of token rows."""
+    from oracle import chains
+    from tile_level_sync_gb300 import synth
+
+    d = wl.dims
+    if wl.kind == "mlp_gelu":
+        X, W1, W2 = (synth.f64(t) for t in inputs)
+
+        def fn(rows):
+            chains.mlp_gelu_rows(X, W1, W2, rows)
+            return 2.0 * len(rows) * d["K"] * d["N1"] + 2.0 * len(rows) * d["N1"] * d["N2"]
+        return fn, d["M"]
+    if wl.kind == "mlp_swiglu":
+        X, Wg, Wu, Wd = (synth.f64(t) for t in inputs)
+
+        def fn(rows):
+            chains.mlp_swiglu_rows(X, Wg, Wu, Wd, rows)
+            return 2.0 * len(rows) * d["K"] * 2 * d["N1"] + 2.0 * len(rows) * d["N1"] * d["N2"]
+        return fn, d["M"]
+    x, w1, w2 = (synth.f64(t) for t in inputs)
+
+    def fn(rows):  # rows = images
+        chains.conv_relu_chain(x[rows], w1, w2)
+        return wl.gemm_flops() * len(rows) / d["N"]
+    return fn, d["N"]
+
+
+def time_oracle(wl, inputs, budget_s=12.0):
+    fn, total = oracle_sample_runner(wl, inputs)
+    import numpy as np
+    rows = list(range(total))
+    t0 = time.perf_counter()
+    flops = fn(rows[:1])
+    t1 = time.perf_counter() - t0
+    n = int(max(1, min(total, budget_s / max(t1, 1e-6))))
+    sel = list(np.linspace(0, total - 1, n).astype(int))
+    t0 = time.perf_counter()
+    flops = fn(sel)
+    dt = time.perf_counter() - t0
+    unit = "images" if wl.kind == "conv_relu" else "token rows"
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{n} of {total} {unit} of {wl.name}, fp64 numpy oracle, {dt:.2f} s"}
+
+
+def run_reference(a):
+    """The CPU oracle as the reference arm: each step a bounded sample of the workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from tile_level_sync_gb300 import synth
+    import numpy as np
+    wl = synth.WORKLOADS[a.workload]
+    inputs = synth.workload_inputs(wl, seed=0)
+    fn, total = oracle_sample_runner(wl, inputs)
+    t0 = time.perf_counter()
+    fn([0])
+    t_row = max(time.perf_counter() - t0, 1e-6)
+    budget = 90.0
+    per_step = int(max(1, min(total, budget / ((a.steps + a.warmup) * t_row))))
+    sel = list(np.linspace(0, total - 1, per_step).astype(int))
+    for _ in range(a.warmup):
+        fn(sel)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(a.steps):
+        flops += fn(sel)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    unit_name = "images" if wl.kind == "conv_relu" else "token rows"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": dt / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, **wl.dims, "parallelism": "replicas only"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{per_step} of {total} {unit_name} of {wl.name} per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+
+class Setup:
+    """Device operands and chains of one workload."""
+
+    def __init__(self, wl, inputs, tile_n, launch, raster=0, l2_prefetch=0):
+        import torch
+        import tile_level_sync_gb300 as cs
+        self.cs = cs
+        self.wl = wl
+        d = wl.dims
+        dev = "cuda"
+        if wl.kind == "conv_relu":
+            x, w1, w2 = inputs
+            self.a = x.to(dev)
+            self.b0 = w1.contiguous().to(dev)
+            self.b1 = w2.contiguous().to(dev)
+            self.h = torch.empty((d["N"], d["H"], d["W"], d["K"]), dtype=torch.bfloat16, device=dev)
+            self.y = torch.empty_like(self.h)
+            self.x_host = x
+            self.base = dict(kind=cs.CHAIN_CONV_RELU, n=d["N"], h=d["H"], w=d["W"], c=d["C"], k_out=d["K"])
+        else:
+            if wl.kind == "mlp_gelu":
+                X, W1, W2 = inputs
+                W1t = W1.t().contiguous()
+                kind = cs.CHAIN_MLP_GELU
+            else:
+                X, Wg, Wu, W2 = inputs
+                W1t = torch.cat([Wg.t(), Wu.t()], 0).contiguous()
+                kind = cs.CHAIN_MLP_SWIGLU
+            self.a = X.to(dev)
+            self.b0 = W1t.to(dev)
+            self.b1 = W2.t().contiguous().to(dev)
+            self.h = torch.empty((d["M"], d["N1"]), dtype=torch.bfloat16, device=dev)
+            self.y = torch.empty((d["M"], d["N2"]), dtype=torch.bfloat16, device=dev)
+            self.x_host = X
+            self.base = dict(kind=kind, M=d["M"], K=d["K"], N1=d["N1"], N2=d["N2"])
+        self.tile_n = tile_n
+        self.launch = launch
+        self.raster = raster
+        self.l2_prefetch = l2_prefetch
+        self.chains = {}
+
+    def chain(self, policy, launch=None, tile_n=None, raster=None, l2_prefetch=None):
+        cs = self.cs
+        launch = self.launch if launch is None else launch
+        tile_n = self.tile_n if tile_n is None else tile_n
+        raster = self.raster if raster is None else raster
+        l2_prefetch = self.l2_prefetch if l2_prefetch is None else l2_prefetch
+        key = (policy, launch, tile_n, raster, l2_prefetch)
+        if key not in self.chains:
+            self.chains[key] = cs.Chain(cs.make_desc(policy=policy, launch=launch, tile_n=tile_n, raster_rows=raster,
+                                                     l2_prefetch=l2_prefetch, **self.base))
+        return self.chains[key]
+
+    def run(self, ch):
+        ch.run(self.a, self.b0, self.b1, self.h, self.y)
+
+    def kernels_per_run(self, policy, launch):
+        n = 2 if (policy == "STREAM" or launch == self.cs.LAUNCH_PDL) else 1
+        return n + (1 if policy == "SENTINEL" else 0)
+
+
+def time_runs(torch, setup, ch, n):
+    """Mean ms per run over n back-to-back runs (events on the launching stream)."""
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for _ in range(n):
+        setup.run(ch)
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def per_launch_ms(torch, setup, ch, n):
+    """Mean device duration of a single run, each bracketed by its own events."""
+    s = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(s)
+        setup.run(ch)
+        b.record(s)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def info_tile_n(setup, policy):
+    return setup.chain(policy).info().tile_n
+
+
+def algorithmic_bytes(wl):
+    d = wl.dims
+    if wl.kind == "conv_relu":
+        pix = d["N"] * d["H"] * d["W"]
+        return 2 * (pix * d["C"] + 9 * d["C"] * d["K"] + 2 * pix * d["K"] + 9 * d["K"] * d["K"] + pix * d["K"])
+    n1w = 2 * d["N1"] if wl.kind == "mlp_swiglu" else d["N1"]
+    return 2 * (d["M"] * d["K"] + d["K"] * n1w + 2 * d["M"] * d["N1"] + d["N1"] * d["N2"] + d["M"] * d["N2"])
+
+
+def check_output(setup, wl, inputs):
+    """Sampled rows of the timed workload's output against the oracle."""
+    import numpy as np
+    from oracle import chains
+    from tile_level_sync_gb300 import synth
+    d = wl.dims
+    Y = setup.y.float().cpu().double().numpy()
+    if wl.kind == "conv_relu":
+        x, w1, w2 = (synth.f64(t) for t in inputs)
+        imgs = [0, d["N"] - 1]
+        _, ref = chains.conv_relu_chain(x[imgs], w1, w2)
+        got = Y[imgs]
+    else:
+        rows = sorted(set([0, 1, d["M"] // 2, d["M"] - 1]))
+        if wl.kind == "mlp_gelu":
+            _, ref = chains.mlp_gelu_rows(*(synth.f64(t) for t in inputs), rows)
+        else:
+            _, ref = chains.mlp_swiglu_rows(*(synth.f64(t) for t in inputs), rows)
+        got = Y[rows]
+    bound = 2e-2 * np.maximum(1.0, np.abs(ref))
+    return bool(np.all(np.abs(got - ref) <= bound))
+
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        return run_reference(a)
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import tile_level_sync_gb300 as cs
+    from tile_level_sync_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    cs.load()
+
+    wl = synth.WORKLOADS[a.workload]
+    inputs = synth.workload_inputs(wl, seed=0)
+    launch = cs.LAUNCH_PDL if a.launch == "pdl" else cs.LAUNCH_PERSISTENT
+    setup = Setup(wl, inputs, a.tile_n, launch, a.raster, a.l2_prefetch)
+    flops = wl.gemm_flops()
+    peaks, peak_src = load_peaks()
+
+    # warm every policy, then choose the fastest tile-synchronised one
+    pols = [p.strip().upper() for p in a.policies.split(",") if p.strip()]
+    per_policy = {}
+    for pol in pols + ["STREAM"]:
+        try:
+            ch = setup.chain(pol)
+        except cs.CusyncError:        # e.g. StridedSync needs n_tiles divisible by G
+            pols = [p for p in pols if p != pol]
+            continue
+        for _ in range(max(3, a.warmup)):
+            setup.run(ch)
+        st, code, detail = ch.check()
+        if st != cs.OK:
+            raise RuntimeError(f"{pol}: {cs.status_string(st)} 0x{code:08x}")
+        per_policy[pol] = time_runs(torch, setup, ch, min(200, max(5, a.steps)))
+    best = min(pols, key=lambda p: per_policy[p])
+    ch = setup.chain(best)
+
+    # ---- timed region: exactly K steps, barrier + synchronize on both sides
+    for _ in range(a.warmup):
+        setup.run(ch)
+    sampler = ClockSampler(torch.cuda.current_device() if world > 1 else 0)
+    sampler.start()
+    time.sleep(0.5)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    e0.record(s)
+    for _ in range(a.steps):
+        setup.run(ch)
+    e1.record(s)
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    if world > 1:
+        dist.barrier()
+    time.sleep(0.3)
+    sampler.stop()
+    ms = reduce_max(e0.elapsed_time(e1), "cuda")
+    ms_step = ms / a.steps
+    st, code, _ = ch.check()
+    if st != cs.OK:
+        raise RuntimeError(f"timed run reported {cs.status_string(st)} 0x{code:08x}")
+    parity_ok = check_output(setup, wl, inputs) if rank == 0 else None
+
+    # ---- stream-serialised baseline, same tiles and k order, same number of steps
+    ch_stream = setup.chain("STREAM")
+    for _ in range(a.warmup):
+        setup.run(ch_stream)
+    stream_ms = time_runs(torch, setup, ch_stream, a.steps)
+
+    # ---- dominant kernel: the fused chain kernel, per-launch events
+    kern_ms = per_launch_ms(torch, setup, ch, min(a.steps, 500))
+    alg_bytes = algorithmic_bytes(wl)
+    hbm_gbs = alg_bytes / (kern_ms * 1e-3) / 1e9
+    tflops_kernel = flops / (kern_ms * 1e-3) / 1e12
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    bound = "hbm" if flops / alg_bytes < ridge else "tensor"
+    traffic = measured_traffic(wl.name, best, a.launch, info_tile_n(setup, best))
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": hbm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": hbm_gbs / peaks["hbm_gbs"], "traffic": traffic}
+    else:
+        roof = {"bound": "tensor", "achieved": tflops_kernel, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": tflops_kernel / peaks["bf16_tflops"], "traffic": traffic}
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+    roof["algorithmic_bytes"] = alg_bytes
+    roof["kernel_ms"] = kern_ms
+    roof["tensor_frac_of_measured"] = tflops_kernel / peaks["bf16_tflops"]
+
+    # ---- end to end through the public API: H2D of X, the chain, D2H of Y
+    x_pin = setup.x_host.pin_memory()
+    y_pin = torch.empty(setup.y.shape, dtype=torch.bfloat16).pin_memory()
+    k_e2e = min(a.steps, 2000)
+    for _ in range(3):
+        setup.a.copy_(x_pin, non_blocking=True)
+        setup.run(ch)
+        y_pin.copy_(setup.y, non_blocking=True)
+    torch.cuda.synchronize()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(s)
+    for _ in range(k_e2e):
+        setup.a.copy_(x_pin, non_blocking=True)
+        setup.run(ch)
+        y_pin.copy_(setup.y, non_blocking=True)
+    e3.record(s)
+    torch.cuda.synchronize()
+    e2e_ms = e2.elapsed_time(e3) / k_e2e
+    h2d = x_pin.numel() * 2
+    d2h = y_pin.numel() * 2
+
+    plan = cs.cusync_plan_waves(setup.chain(best).desc)
+    plan148 = cs.cusync_plan_waves(cs.make_desc(policy=best, launch=launch, tile_n=a.tile_n, num_sms=148,
+                                                **setup.base))
+    info = setup.chain(best).info()
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu = time_oracle(wl, inputs)
+
+    clocks = sampler.summary(t_host0 - 0.05, t_host1 + 0.05)
+    value = job_throughput(flops, world, ms_step)
+    us = ms_step * 1e3
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / (flops / (PAGES_US_B256 * 1e-6) / 1e12) if wl.name == "gpt3_mlp_m256" else None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, **wl.dims, "policy": best, "launch": a.launch,
+                   "tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "parallelism": "replicas only",
+                   "l2": f"inputs {alg_bytes / 1e6:.0f} MB of operands > 129 MB L2; no flush between steps"
+                   if alg_bytes > 129e6 else "inputs smaller than L2",
+                   "vs_baseline_note": "pages' TileSync B=256 chain (840 us) on a V100 in fp16; context only"},
+        "us_per_chain": us,
+        "stream_us_per_chain": stream_ms * 1e3,
+        "speedup_vs_stream": stream_ms / ms_step,
+        "policies_us": {k: v * 1e3 for k, v in per_policy.items()},
+        "pct_bf16_peak": {"measured": value / world / peaks["bf16_tflops"] * 100,
+                          "nominal": value / world / NOMINAL_BF16_TFLOPS * 100},
+        "hbm_gbs_chain": alg_bytes / (ms_step * 1e-3) / 1e9,
+        "waves": {"device_sms": plan.num_sms, "tbs": list(plan.tbs), "stream_waves": plan.stream_waves,
+                  "fused_waves": plan.fused_waves, "last_wave_tbs": plan.last_wave_tbs,
+                  "util": list(plan.util),
+                  "sms148": {"stream_waves": plan148.stream_waves, "fused_waves": plan148.fused_waves,
+                             "last_wave_tbs": plan148.last_wave_tbs, "util": list(plan148.util)}},
+        "roofline": roof,
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "note": "X copied in from pinned host memory and Y read back every step; weights resident"},
+        "gpu_launches": a.steps * setup.kernels_per_run(best, launch),
+        "clocks": clocks,
+        "parity_sampled_rows": parity_ok,
+        "cpu_baseline": cpu,
+    }
+    if a.sweep_out and rank == 0:
+        line["sweep_file"] = a.sweep_out
+        sweep(a, torch, cs, synth, a.sweep_out)
+    for c in setup.chains.values():
+        c.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def sweep(a, torch, cs, synth, out_path):
+    """Every listed workload x tile width x (raster, L2 prefetch) x policy: us per chain.
+
+    Written to a file; not a bench line."""
+    names = [n for n in a.sweep.split(",") if n] or list(synth.WORKLOADS)
+    results = []
+    variants = [(16, 8), (1, -1), (16, -1), (1, 8)]
+    for name in names:
+        wl = synth.WORKLOADS[name]
+        inputs = synth.workload_inputs(wl, seed=0)
+        for tile_n in (256, 128):
+            setup = Setup(wl, inputs, tile_n, cs.LAUNCH_PERSISTENT)
+            row = {"workload": name, "tile_n": tile_n, "gflop": wl.gemm_flops() / 1e9, "us": {}}
+            for vi, (raster, pf) in enumerate(variants):
+                pols = ["STREAM", "ROW", "TILE", "STRIDED", "SENTINEL"] if vi == 0 else ["STREAM", "ROW", "TILE"]
+                for pol in pols:
+                    for launch in (cs.LAUNCH_PERSISTENT, cs.LAUNCH_PDL):
+                        if launch == cs.LAUNCH_PDL and (pol == "STREAM" or vi != 0):
+                            continue
+                        key = f"{pol}/{'pdl' if launch else 'pers'}/r{raster}/pf{pf}"
+                        try:
+                            ch = setup.chain(pol, launch=launch, raster=raster, l2_prefetch=pf)
+                        except cs.CusyncError as e:
+                            row["us"][key] = str(e)
+                            continue
+                        for _ in range(5):
+                            setup.run(ch)
+                        st, code, _ = ch.check()
+                        n = 50 if wl.gemm_flops() > 1e11 else 200
+                        ms = time_runs(torch, setup, ch, n)
+                        row["us"][key] = ms * 1e3 if st == cs.OK else f"status {st}"
+                for c in list(setup.chains.values()):
+                    c.close()
+                setup.chains = {}
+            plan = cs.cusync_plan_waves(setup.chain("ROW").desc)
+            row["waves"] = {"tbs": list(plan.tbs), "stream": plan.stream_waves, "fused": plan.fused_waves,
+                            "last_wave_tbs": plan.last_wave_tbs, "sms": plan.num_sms}
+            for c in setup.chains.values():
+                c.close()
+            results.append(row)
+            print(json.dumps(row), file=sys.stderr, flush=True)
+    with open(out_path, "w") as f:
+        json.dump(results, f, indent=1)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -117,9 +117,14 @@ typedef struct {
   int32_t strided_group;             /* G for STRIDED_TILE; 0 = 2 */
   uint32_t flags;                    /* CUSYNC_FLAG_* | CUSYNC_DEBUG_* */
   int32_t num_sms;                   /* SMs the kernels may use; 0 = all of the device */
-  int32_t _pad1;
+  int32_t raster_rows;               /* tile order: row tiles per raster group (columns
+                                        outer, rows inner within a group); 0 or 1 =
+                                        plain row-major */
   uint64_t timeout_ns;               /* bound of every device wait on a semaphore or a
                                         sentinel; 0 = 1e9 (one second) */
+  int32_t l2_prefetch;               /* weight k-blocks prefetched into L2 ahead of the
+                                        shared-memory ring; 0 or -1 = none */
+  int32_t _pad2;
 } cusync_chain_desc_t;
 
 /* Wave arithmetic of a two-kernel chain ([cuSync] §II-A "Thread block Wave Execution",
@@ -214,6 +219,12 @@ cusync_status_t cusync_consumer_waits(const cusync_chain_desc_t* d, int32_t m_ti
  * host computation. */
 cusync_status_t cusync_producer_flag(const cusync_chain_desc_t* d, int32_t m_tile, int32_t n_tile, int32_t* flag);
 cusync_status_t cusync_producer_col(const cusync_chain_desc_t* d, int32_t y, int32_t* col);
+
+/* (row tile, column tile) at position u of stage `stage`'s tile queue (0 = producer,
+ * 1 = consumer): the order in which the persistent CTAs claim tiles.  Pure host
+ * computation. */
+cusync_status_t cusync_tile_at(const cusync_chain_desc_t* d, int32_t stage, int32_t u, int32_t* m_tile,
+                               int32_t* n_tile);
 
 /* Release the chain's device state.  NULL is accepted. */
 cusync_status_t cusync_destroy_chain(cusync_chain_t chain);

@@ -211,3 +211,27 @@ def test_producer_posts_and_order(case, policy, G):
         assert order == deps.strided_producer_order(nt, Gc)
     else:
         assert order == list(range(nt))
+
+
+@pytest.mark.parametrize("case", CASES)
+@pytest.mark.parametrize("policy,G", [("ROW", 1), ("STRIDED", 2), ("SENTINEL", 1)])
+@pytest.mark.parametrize("raster", [1, 3, 16])
+def test_tile_order_is_a_permutation(case, policy, G, raster):
+    desc = cs.make_desc(policy=policy, strided_group=G, num_sms=148, raster_rows=raster, **case)
+    try:
+        info = cs.cusync_plan_info(desc)
+    except cs.CusyncError:
+        return
+    for stage in (0, 1):
+        mt, nt = info.m_tiles[stage], info.n_tiles[stage]
+        seen = [cs.cusync_tile_at(desc, stage, u) for u in range(mt * nt)]
+        assert sorted(seen) == [(m, n) for m in range(mt) for n in range(nt)]
+        # rows are finished group by group: every tile of row group g precedes group g+1
+        pos = {t: u for u, t in enumerate(seen)}
+        for m in range(mt - 1):
+            if (m // raster) != ((m + 1) // raster):
+                assert max(pos[(m, n)] for n in range(nt)) < min(pos[(m + 1, n)] for n in range(nt))
+        if raster == 1:
+            order = deps.strided_producer_order(nt, info.strided_group) if (stage == 0 and policy == "STRIDED") \
+                else list(range(nt))
+            assert seen == [(m, order[y]) for m in range(mt) for y in range(nt)]

@@ -168,3 +168,21 @@ def test_invalid_pointers_rejected():
         assert e.value.status == cs.ERR_INVALID_ARG
     finally:
         ch.close()
+
+
+def test_tile_order_and_prefetch_do_not_change_results():
+    """The raster group size and the L2 prefetch distance only change when and in which
+    order tiles are computed, never a byte of H or Y."""
+    (X, W1, W2), (H_ref, Y_ref) = _mlp_case(520, 512, 1536, 512, seed=6)
+    ops = device_mlp_operands(X, W1, W2)
+    ref = None
+    for pol in ("STREAM", "ROW", "TILE"):
+        for raster, pf in ((1, -1), (3, 8), (16, 2), (16, -1)):
+            d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, M=520, K=512, N1=1536, N2=512, tile_n=256,
+                             raster_rows=raster, l2_prefetch=pf)
+            H, Y, _ = run_mlp(d, *ops, runs=2)
+            b = (bits(H), bits(Y))
+            if ref is None:
+                assert_within_tol(f64(Y), Y_ref, "Y")
+                ref = b
+            assert np.array_equal(b[0], ref[0]) and np.array_equal(b[1], ref[1]), (pol, raster, pf)

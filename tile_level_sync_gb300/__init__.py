@@ -33,8 +33,8 @@ class cusync_chain_desc_t(ctypes.Structure):
         ("kind", c_i32), ("policy", c_i32), ("launch", c_i32), ("_pad0", c_i32),
         ("M", c_i64), ("K", c_i64), ("N1", c_i64), ("N2", c_i64),
         ("n", c_i32), ("h", c_i32), ("w", c_i32), ("c", c_i32), ("k_out", c_i32),
-        ("tile_n", c_i32), ("strided_group", c_i32), ("flags", c_u32), ("num_sms", c_i32), ("_pad1", c_i32),
-        ("timeout_ns", c_u64),
+        ("tile_n", c_i32), ("strided_group", c_i32), ("flags", c_u32), ("num_sms", c_i32), ("raster_rows", c_i32),
+        ("timeout_ns", c_u64), ("l2_prefetch", c_i32), ("_pad2", c_i32),
     ]
 
 
@@ -71,6 +71,8 @@ _SIGNATURES = {
                                       ctypes.POINTER(c_i32), ctypes.POINTER(c_u32), c_i32, ctypes.POINTER(c_i32)]),
     "cusync_producer_flag": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), c_i32, c_i32, ctypes.POINTER(c_i32)]),
     "cusync_producer_col": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), c_i32, ctypes.POINTER(c_i32)]),
+    "cusync_tile_at": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), c_i32, c_i32, ctypes.POINTER(c_i32),
+                               ctypes.POINTER(c_i32)]),
     "cusync_destroy_chain": (c_i32, [_VP]),
 }
 
@@ -133,12 +135,14 @@ def status_string(status):
 
 
 def make_desc(kind=CHAIN_MLP_GELU, policy=POLICY_ROW, launch=LAUNCH_PERSISTENT, M=0, K=0, N1=0, N2=0,
-              n=0, h=0, w=0, c=0, k_out=0, tile_n=0, strided_group=0, flags=0, num_sms=0, timeout_ns=0):
+              n=0, h=0, w=0, c=0, k_out=0, tile_n=0, strided_group=0, flags=0, num_sms=0, timeout_ns=0,
+              raster_rows=0, l2_prefetch=0):
     if isinstance(policy, str):
         policy = POLICY_NAMES[policy]
     return cusync_chain_desc_t(kind=kind, policy=policy, launch=launch, M=M, K=K, N1=N1, N2=N2, n=n, h=h, w=w,
                                c=c, k_out=k_out, tile_n=tile_n, strided_group=strided_group, flags=flags,
-                               num_sms=num_sms, timeout_ns=timeout_ns)
+                               num_sms=num_sms, timeout_ns=timeout_ns, raster_rows=raster_rows,
+                               l2_prefetch=l2_prefetch)
 
 
 # ---------------------------------------------------------------- the C functions
@@ -184,6 +188,12 @@ def cusync_producer_col(desc, y):
     c = c_i32()
     _check(load().cusync_producer_col(ctypes.byref(desc), y, ctypes.byref(c)), "cusync_producer_col")
     return c.value
+
+
+def cusync_tile_at(desc, stage, u):
+    m, n = c_i32(), c_i32()
+    _check(load().cusync_tile_at(ctypes.byref(desc), stage, u, ctypes.byref(m), ctypes.byref(n)), "cusync_tile_at")
+    return m.value, n.value
 
 
 def cusync_create_chain(desc):

@@ -50,6 +50,8 @@ enum : uint32_t { ERRC_FLAG_TIMEOUT = 1, ERRC_SENTINEL_TIMEOUT = 2, ERRC_PIPELIN
 // Flag bits shared with cusync.h.
 constexpr uint32_t kFlagNoReorder = 1u << 0;
 constexpr uint32_t kDebugSkipPost = 1u << 8;
+// Semaphores read in one round trip when a wait finds its semaphore not yet known ready.
+constexpr int kProbe = 32;
 
 struct StageArgs {
   CUtensorMap tmA;       // activations: 2-D [M, K] or 4-D NHWC image
@@ -72,6 +74,8 @@ struct ChainArgs {
   uint32_t flags_bits;
   int32_t pdl_role;      // 1: trigger dependents at start; 2: wait on the primary at exit
   int32_t sentinel_check;
+  int32_t num_flags;     // semaphores in `flags`
+  int32_t l2_prefetch;   // weight k-blocks prefetched into L2 ahead of the B loads (0: none)
   int32_t _pad;
   uint64_t timeout_ns;       // semaphore / sentinel waits
   uint64_t pipe_timeout_ns;  // shared-memory pipeline waits
@@ -105,8 +109,8 @@ __device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
     s = 1;
     u = t - a.tiles0;
   }
-  const StageGeo& g = a.st[s].g;
-  const int32_t m = u / g.n_tiles, y = u % g.n_tiles;
+  int32_t m, y;
+  tile_at(a.st[s].g, u, &m, &y);
   const int32_t c = (s == 0) ? producer_col(a.dep, y) : y;
   return TileRef{s, m, c};
 }
@@ -144,30 +148,21 @@ __device__ __forceinline__ void issue_b(const ChainArgs& a, const TileRef& tr, i
   }
 }
 
+template <int BN>
+__device__ __forceinline__ void prefetch_b(const ChainArgs& a, const TileRef& tr, int32_t kb) {
+  const StageArgs& S = a.st[tr.s];
+  if (S.g.epi == EPI_SWIGLU) {
+    const int32_t row0 = tr.c * (BN / 2);
+    ptx::tma_prefetch_2d(&S.tmB, kb * kBK, row0);
+    ptx::tma_prefetch_2d(&S.tmB, kb * kBK, S.b_half_rows + row0);
+  } else {
+    ptx::tma_prefetch_2d(&S.tmB, kb * kBK, tr.c * BN);
+  }
+}
+
 __device__ __forceinline__ void record_error(const ChainArgs& a, uint32_t cls, int32_t tile, int32_t detail) {
   const uint32_t w = (cls << 24) | ((uint32_t)tile & 0xFFFFFFu);
   if (atomicCAS(a.ctrl + CTRL_ERR, 0u, w) == 0u) atomicExch(a.ctrl + CTRL_ERR_DETAIL, (uint32_t)detail);
-}
-
-// Bounded acquire-poll of one semaphore ([cuSync] §IV-E "Wait"; CUDA-FGS §4.6.2 flag
-// protocol).  Gives up when the deadline passes or another wait has already failed.
-__device__ __forceinline__ void wait_flag(const ChainArgs& a, int32_t flag, uint32_t target, int32_t tile,
-                                          int32_t kb) {
-  const uint32_t* f = a.flags + flag;
-  if ((int32_t)(ptx::ld_acquire_gpu(f) - target) >= 0) return;
-  const uint64_t t0 = ptx::globaltimer();
-  uint32_t iter = 0;
-  while (true) {
-    __nanosleep(32);
-    if ((int32_t)(ptx::ld_acquire_gpu(f) - target) >= 0) return;
-    if ((++iter & 63u) == 0) {
-      if (ptx::ld_relaxed_gpu(a.ctrl + CTRL_ERR) != 0u) return;
-      if (ptx::globaltimer() - t0 > a.timeout_ns) {
-        record_error(a, ERRC_FLAG_TIMEOUT, tile, (kb << 16) | (flag & 0xFFFF));
-        return;
-      }
-    }
-  }
 }
 
 __device__ __forceinline__ bool has_sentinel_bf16x2(uint32_t x) {
@@ -293,32 +288,101 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
         const bool cons = (tr.s == 1);
         DepTracker dt;
         dt.reset();
-        int32_t bnext = 0;
-        auto do_waits = [&](int32_t kb) {
-          if (!cons) return;
+        int32_t bnext = 0;  // next k-block whose stage slot is armed and whose B load is issued
+        int32_t pfnext = 0; // next k-block whose weights are prefetched into L2
+        const int32_t pfd = (SA.g.a_mode == AMODE_GEMM) ? args.l2_prefetch : 0;
+        // Arm the stage slot of k-block kbb and issue its weight (B) load, after prefetching
+        // the weights of later k-blocks into L2.  Blocking waits for the slot to drain;
+        // non-blocking returns 0 if it has not drained yet.
+        auto arm_b = [&](int32_t kbb, bool blocking) -> int {
+          const uint32_t j = it + (uint32_t)kbb;
+          const int st = (int)(j % S);
+          const uint32_t par = ((j / S) & 1u) ^ 1u;
+          if (blocking) {
+            if (!ptx::mbar_wait_bounded(&empty[st], par, pto) || *abort_flag) return -1;
+          } else if (!ptx::mbar_test_wait(&empty[st], par)) {
+            return 0;
+          }
+          if (pfd > 0) {
+            const int32_t lim = min(KB, kbb + S + pfd);
+            if (pfnext < kbb + S) pfnext = min(KB, kbb + S);
+            for (; pfnext < lim; ++pfnext) prefetch_b<BN>(args, tr, pfnext);
+          }
+          ptx::mbar_arrive_expect_tx(&full[st], tx);
+          issue_b<BN>(args, tr, kbb, smem_b(st), &full[st], pol_b);
+          return 1;
+        };
+        // Semaphores already seen at their target during this tile: [rc_lo, rc_hi).
+        int32_t rc_lo = 0, rc_hi = 0;
+        uint32_t rc_target = 0;
+        // Semaphore waits before A k-block kb (cuSync §IV-E "Wait", bounded).  A wait
+        // first probes a run of up to kProbe consecutive semaphores with relaxed loads (one
+        // round trip) and remembers which already reached the target; only a semaphore
+        // still short of its target is polled.  While polling, the weight loads of the
+        // following stages are issued as their slots drain (cuSync §V "Reorder Tile Loads
+        // and Synchronization").  One acquire fence after the observations orders the
+        // A-tile reads after the producer's releases.
+        auto wait_deps = [&](int32_t kb) {
           Wait w[kMaxWaits];
           const int n = dt.next(SA.g, args.dep, tr.m, kb, w);
-          for (int i = 0; i < n; ++i) wait_flag(args, w[i].flag, args.epoch * w[i].per_run, t, kb);
-          if (n > 0) ptx::fence_proxy_async_global();
+          bool observed = false;
+          for (int i = 0; i < n; ++i) {
+            const int32_t f = w[i].flag;
+            const uint32_t target = args.epoch * w[i].per_run;
+            if (target == rc_target && rc_lo <= f && f < rc_hi) continue;
+            uint32_t v[kProbe];
+            const int32_t cnt = min(kProbe, args.num_flags - f);
+#pragma unroll
+            for (int q = 0; q < kProbe; ++q) v[q] = q < cnt ? ptx::ld_relaxed_gpu(args.flags + f + q) : 0u;
+            int32_t ready = 0;
+#pragma unroll
+            for (int q = 0; q < kProbe; ++q)
+              if (ready == q && q < cnt && (int32_t)(v[q] - target) >= 0) ready = q + 1;
+            observed = true;
+            if (ready > 0) {
+              rc_lo = f;
+              rc_hi = f + ready;
+              rc_target = target;
+              continue;
+            }
+            const uint64_t t0 = ptx::globaltimer();
+            uint32_t iter = 0;
+            while (true) {
+              if (reorder && bnext < min(KB, kb + S) && arm_b(bnext, false) > 0) {
+                ++bnext;
+              } else {
+                __nanosleep(64);
+              }
+              if ((int32_t)(ptx::ld_relaxed_gpu(args.flags + f) - target) >= 0) break;
+              if ((++iter & 63u) == 0) {
+                if (ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u) break;
+                if (ptx::globaltimer() - t0 > args.timeout_ns) {
+                  record_error(args, ERRC_FLAG_TIMEOUT, t, (kb << 16) | (f & 0xFFFF));
+                  break;
+                }
+              }
+            }
+            rc_lo = f;
+            rc_hi = f + 1;
+            rc_target = target;
+          }
+          if (observed) {
+            ptx::fence_acq_rel_gpu();
+            ptx::fence_proxy_async_global();
+          }
         };
-        for (int32_t kb = 0; kb < KB && ok; ++kb) {
-          if (!reorder) do_waits(kb);
-          const int32_t blimit = reorder ? min(KB, kb + S) : kb + 1;
-          while (bnext < blimit) {
-            const uint32_t j = it + (uint32_t)bnext;
-            const int st = (int)(j % S);
-            if (!ptx::mbar_wait_bounded(&empty[st], ((j / S) & 1u) ^ 1u, pto) || *abort_flag) {
+        for (int32_t kb = 0; kb < KB; ++kb) {
+          if (cons && !reorder) wait_deps(kb);
+          if (bnext == kb) {
+            if (arm_b(kb, true) < 0) {
               record_error(args, ERRC_PIPELINE, t, 2);
               *abort_flag = 1;
               ok = false;
               break;
             }
-            ptx::mbar_arrive_expect_tx(&full[st], tx);
-            issue_b<BN>(args, tr, bnext, smem_b(st), &full[st], pol_b);
             ++bnext;
           }
-          if (!ok) break;
-          if (reorder) do_waits(kb);
+          if (cons && reorder) wait_deps(kb);
           const int st = (int)((it + (uint32_t)kb) % S);
           issue_a(args, tr, kb, smem_a(st), &full[st], pol_a);
         }

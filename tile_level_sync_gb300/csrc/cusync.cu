@@ -135,6 +135,10 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
       g.k_blocks = 9 * g.cblocks;
     }
   }
+  const int32_t raster = d.raster_rows > 0 ? d.raster_rows : 1;
+  g0.raster = raster < g0.m_tiles ? raster : g0.m_tiles;
+  g1.raster = raster < g1.m_tiles ? raster : g1.m_tiles;
+  if (d.l2_prefetch < -1 || d.l2_prefetch > 64) return CUSYNC_ERR_INVALID_ARG;
   DepCfg& dep = p->dep;
   dep.policy = d.policy;
   dep.prod_m_tiles = g0.m_tiles;
@@ -463,6 +467,8 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
   A.tiles1 = (int32_t)t1;
   A.flags_bits = d->flags;
   A.sentinel_check = d->policy == CUSYNC_POLICY_SENTINEL ? 1 : 0;
+  A.num_flags = (int32_t)p.num_flags;
+  A.l2_prefetch = d->l2_prefetch <= 0 ? 0 : d->l2_prefetch;
   A.timeout_ns = ch->d.timeout_ns;
   A.pipe_timeout_ns = std::max<uint64_t>(4 * ch->d.timeout_ns, 2000000000ull);
   ch->maps_valid = false;
@@ -580,6 +586,21 @@ cusync_status_t cusync_producer_flag(const cusync_chain_desc_t* d, int32_t m_til
   const StageGeo& g = p.geo[0];
   if (m_tile < 0 || m_tile >= g.m_tiles || n_tile < 0 || n_tile >= g.n_tiles) return CUSYNC_ERR_INVALID_ARG;
   *flag = producer_flag(p.dep, m_tile, n_tile);
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_tile_at(const cusync_chain_desc_t* d, int32_t stage, int32_t u, int32_t* m_tile,
+                               int32_t* n_tile) {
+  if (!d || !m_tile || !n_tile || stage < 0 || stage > 1) return CUSYNC_ERR_INVALID_ARG;
+  Plan p;
+  cusync_status_t st = make_plan(*d, &p);
+  if (st != CUSYNC_OK) return st;
+  const StageGeo& g = p.geo[stage];
+  if (u < 0 || u >= g.m_tiles * g.n_tiles) return CUSYNC_ERR_INVALID_ARG;
+  int32_t m, y;
+  tile_at(g, u, &m, &y);
+  *m_tile = m;
+  *n_tile = stage == 0 ? producer_col(p.dep, y) : y;
   return CUSYNC_OK;
 }
 

@@ -45,6 +45,7 @@ struct StageGeo {
   int32_t n_tiles;   // column tiles
   int32_t k_blocks;  // ceil(K / kBK)
   int32_t n_out;     // output columns written per tile (BN, or BN/2 for SwiGLU)
+  int32_t raster;    // row tiles per raster group (see tile_at)
   // convolution only
   int32_t img_n, img_h, img_w, cin;  // input image (= output image: 3x3, stride 1, pad 1)
   int32_t th;                        // image rows per row tile
@@ -83,6 +84,22 @@ CUSYNC_HD int64_t num_flags(const DepCfg& d) {
 CUSYNC_HD int32_t producer_col(const DepCfg& d, int32_t y) {
   if (d.policy == POL_STRIDED) return (y % d.G) * d.D + y / d.G;
   return y;
+}
+
+// Tile at position u of a stage's queue.  Row tiles are taken in groups of `raster`
+// rows; inside a group the column position is the outer index and the row the inner
+// one, so the CTAs working at the same time share a few weight column tiles and a few
+// activation row tiles in L2.  raster = 1 is the RowMajor order of cuSync §IV-C;
+// within every group the rows still complete in order.  Writes the row tile and the
+// column position (which a policy may permute, see producer_col).
+CUSYNC_HD void tile_at(const StageGeo& g, int32_t u, int32_t* m, int32_t* y) {
+  const int32_t gm = g.raster < 1 ? 1 : g.raster;
+  const int32_t per_group = gm * g.n_tiles;
+  const int32_t grp = u / per_group;
+  const int32_t rows = (g.m_tiles - grp * gm) < gm ? (g.m_tiles - grp * gm) : gm;
+  const int32_t idx = u - grp * per_group;
+  *y = idx / rows;
+  *m = grp * gm + idx % rows;
 }
 
 // Semaphore the producer posts after finishing tile (m, c); -1 if the policy posts none.
