@@ -226,6 +226,28 @@ cusync_status_t cusync_producer_col(const cusync_chain_desc_t* d, int32_t y, int
 cusync_status_t cusync_tile_at(const cusync_chain_desc_t* d, int32_t stage, int32_t u, int32_t* m_tile,
                                int32_t* n_tile);
 
+/* Allocation-free variant of cusync_run_mlp, for callers that cannot allocate device
+ * memory themselves (for example an operator running inside a runtime that owns the
+ * device memory pool, or a serving loop that must avoid cudaMalloc's synchronisation).
+ * The pages have no counterpart: it exists for such callers only.
+ *
+ * It needs no chain object: it plans the chain described by *d and runs it with the same
+ * kernels, keeping the synchronisation state (error word, tile counters, semaphores) in a
+ * fixed 64 KiB array inside the library (16368 semaphores at most; larger plans return
+ * CUSYNC_ERR_UNSUPPORTED).  It calls no cudaMalloc or cudaFree.  Inputs and outputs are
+ * as for cusync_run_mlp.
+ *  - The first call on each device looks up the array's device address and prepares the
+ *    kernels for that device; make that first call before any stream capture.
+ *  - Every call clears the part of the array it uses on `stream`, then launches; the
+ *    array keeps the last call's contents.  Calls whose work may overlap on the GPU
+ *    (e.g. on two unordered streams) race on the array: order them.
+ *  - If error_word is non-NULL the call waits for the chain to finish and stores the
+ *    device error word there (0 = no wait expired), returning CUSYNC_ERR_TIMEOUT or
+ *    CUSYNC_ERR_DEVICE when it is set.  With NULL it returns after the launches. */
+cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, const void* X, const void* W1t,
+                                       const void* W2t, void* H, void* Y, cusync_stream_t stream,
+                                       uint32_t* error_word);
+
 /* Release the chain's device state.  NULL is accepted. */
 cusync_status_t cusync_destroy_chain(cusync_chain_t chain);
 

@@ -73,6 +73,8 @@ _SIGNATURES = {
     "cusync_producer_col": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), c_i32, ctypes.POINTER(c_i32)]),
     "cusync_tile_at": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), c_i32, c_i32, ctypes.POINTER(c_i32),
                                ctypes.POINTER(c_i32)]),
+    "cusync_run_mlp_noalloc": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), _VP, _VP, _VP, _VP, _VP, _VP,
+                                       ctypes.POINTER(c_u32)]),
     "cusync_destroy_chain": (c_i32, [_VP]),
 }
 
@@ -210,6 +212,17 @@ def cusync_run_mlp(chain, X, W1t, W2t, H, Y, stream=None):
 def cusync_run_conv_chain(chain, x, w1, w2, y1, y2, stream=None):
     _check(load().cusync_run_conv_chain(chain, _ptr(x), _ptr(w1), _ptr(w2), _ptr(y1), _ptr(y2), _stream(stream)),
            "cusync_run_conv_chain")
+
+
+def cusync_run_mlp_noalloc(desc, X, W1t, W2t, H, Y, stream=None, wait=False):
+    """Allocation-free MLP chain run (see include/cusync.h).  With wait=True it returns
+    (status, device error word) after the chain finished; else it returns after launching."""
+    err = c_u32() if wait else None
+    st = load().cusync_run_mlp_noalloc(ctypes.byref(desc), _ptr(X), _ptr(W1t), _ptr(W2t), _ptr(H), _ptr(Y),
+                                       _stream(stream), ctypes.byref(err) if wait else None)
+    if st not in (OK, ERR_TIMEOUT, ERR_DEVICE):
+        raise CusyncError(st, "cusync_run_mlp_noalloc")
+    return st, (err.value if wait else None)
 
 
 def cusync_chain_check(chain, stream=None):

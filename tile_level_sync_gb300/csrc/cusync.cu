@@ -623,3 +623,152 @@ cusync_status_t cusync_destroy_chain(cusync_chain_t ch) {
 }
 
 }  // extern "C"
+
+// ----------------------------------------------------------------------------- no-alloc entry
+//
+// Some callers of this library may not allocate device memory themselves: a plugin or
+// operator running inside an inference runtime whose device memory is owned by the
+// runtime's own pool, or a latency-critical serving loop where cudaMalloc / cudaFree
+// would add device-wide synchronisation.  cusync_run_mlp_noalloc serves them: it runs
+// the same chain kernel as cusync_run_mlp, but keeps the chain's synchronisation state
+// (error word, tile counters, semaphores) in the fixed array below instead of in memory
+// allocated by cusync_create_chain.  It allocates nothing.
+//
+// The array lives in every device that loads this library, until the process exits.
+// All calls share it and it keeps the last call's contents, so every call clears the
+// part it uses on its stream before launching; two calls whose work overlaps on the GPU
+// (different streams, no ordering between them) race on it and must not be issued.
+
+namespace {
+
+constexpr int kNoAllocWords = 16384;  // 64 KiB: CTRL_WORDS control words + semaphores
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocWords];
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch array and the kernels' attributes for the current device,
+// set up on the first call made with that device current.
+cusync_status_t noalloc_setup(int dev, uint32_t** out) {
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (dev < 0 || dev >= kMaxDevices) return CUSYNC_ERR_UNSUPPORTED;
+  if (g_noalloc_ptr[dev] == nullptr) {
+    if (!load_encoder()) return CUSYNC_ERR_CUDA;
+    cudaError_t e = set_kernel_attrs<256>();
+    if (e == cudaSuccess) e = set_kernel_attrs<128>();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel attributes (no-alloc)");
+    uint32_t* p = nullptr;
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return CUSYNC_OK;
+}
+
+}  // namespace
+
+extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, const void* X, const void* W1t,
+                                                  const void* W2t, void* H, void* Y, cusync_stream_t stream,
+                                                  uint32_t* error_word) {
+  if (!d) return CUSYNC_ERR_INVALID_ARG;
+  if (d->kind != CUSYNC_CHAIN_MLP_GELU && d->kind != CUSYNC_CHAIN_MLP_SWIGLU) return CUSYNC_ERR_INVALID_ARG;
+  Plan p;
+  cusync_status_t st = make_plan(*d, &p);
+  if (st != CUSYNC_OK) return st;
+  // The fixed array bounds the number of semaphores this entry point can use.
+  if ((int64_t)CTRL_WORDS + p.num_flags > kNoAllocWords) {
+    CUSYNC_LOG("no-alloc run needs %lld semaphores; the fixed scratch holds %d", (long long)p.num_flags,
+               kNoAllocWords - CTRL_WORDS);
+    return CUSYNC_ERR_UNSUPPORTED;
+  }
+  if (!aligned16(X) || !aligned16(W1t) || !aligned16(W2t) || !aligned16(H) || !aligned16(Y))
+    return CUSYNC_ERR_INVALID_ARG;
+  if (H == Y || H == X || Y == X) return CUSYNC_ERR_INVALID_ARG;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3) return CUSYNC_ERR_UNSUPPORTED;
+  uint32_t* scratch = nullptr;
+  if ((st = noalloc_setup(dev, &scratch)) != CUSYNC_OK) return st;
+  int dev_sms = 0;
+  if (query_num_sms(0, &dev_sms) != 0) return CUSYNC_ERR_CUDA;
+  const int sms = d->num_sms > 0 ? std::min(d->num_sms, dev_sms) : dev_sms;
+
+  ChainArgs A;
+  std::memset(&A, 0, sizeof(A));
+  const bool swiglu = d->kind == CUSYNC_CHAIN_MLP_SWIGLU;
+  bool ok = true;
+  ok &= encode_2d(&A.st[0].tmA, X, (uint64_t)d->M, (uint64_t)d->K, (uint32_t)kBM);
+  ok &= encode_2d(&A.st[0].tmB, W1t, (uint64_t)(swiglu ? 2 * d->N1 : d->N1), (uint64_t)d->K,
+                  (uint32_t)(swiglu ? p.bn / 2 : p.bn));
+  ok &= encode_2d(&A.st[1].tmA, H, (uint64_t)d->M, (uint64_t)d->N1, (uint32_t)kBM);
+  ok &= encode_2d(&A.st[1].tmB, W2t, (uint64_t)d->N2, (uint64_t)d->N1, (uint32_t)p.bn);
+  if (!ok) return CUSYNC_ERR_INVALID_ARG;
+  const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
+  const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
+  const uint64_t timeout = d->timeout_ns ? d->timeout_ns : kDefaultTimeoutNs;
+  A.st[0].g = p.geo[0];
+  A.st[1].g = p.geo[1];
+  A.st[0].out = H;
+  A.st[1].out = Y;
+  A.st[0].b_half_rows = swiglu ? (int32_t)d->N1 : 0;
+  A.dep = p.dep;
+  A.ctrl = scratch;
+  A.flags = scratch + CTRL_WORDS;
+  A.tiles0 = (int32_t)t0;
+  A.tiles1 = (int32_t)t1;
+  A.epoch = 1;  // the semaphores are cleared below, so every call is run number one
+  A.flags_bits = d->flags;
+  A.sentinel_check = d->policy == CUSYNC_POLICY_SENTINEL ? 1 : 0;
+  A.num_flags = (int32_t)p.num_flags;
+  A.l2_prefetch = d->l2_prefetch <= 0 ? 0 : d->l2_prefetch;
+  A.timeout_ns = timeout;
+  A.pipe_timeout_ns = std::max<uint64_t>(4 * timeout, 2000000000ull);
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // Clear what must start at zero: error word, tile counters, semaphores.
+  e = cudaMemsetAsync(scratch, 0, ((size_t)CTRL_WORDS + (size_t)p.num_flags) * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e, "no-alloc scratch clear");
+  if (d->policy == CUSYNC_POLICY_SENTINEL && !(d->flags & CUSYNC_DEBUG_SKIP_INIT)) {
+    const int64_t n16 = (int64_t)p.geo[0].M * p.geo[0].N * 2 / 16;
+    int blocks = (int)std::min<int64_t>(ceil_div(n16, 256), (int64_t)sms * 8);
+    if (blocks < 1) blocks = 1;
+    sentinel_fill_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<uint4*>(H), n16);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "sentinel fill launch");
+  }
+  const bool two_kernels = d->policy == CUSYNC_POLICY_STREAM || d->launch == CUSYNC_LAUNCH_PDL;
+  if (!two_kernels) {
+    A.queue = 0;
+    A.first_stage = 0;
+    A.last_stage = 1;
+    A.pdl_role = 0;
+    e = launch_any(p.bn, A, (int)std::min<int64_t>(sms, t0 + t1), /*coop=*/true, false, s);
+    if (e != cudaSuccess) return cuda_fail(e, "no-alloc fused launch");
+  } else {
+    const bool pdl = d->policy != CUSYNC_POLICY_STREAM;
+    A.queue = 0;
+    A.first_stage = 0;
+    A.last_stage = 0;
+    A.pdl_role = pdl ? 1 : 0;
+    e = launch_any(p.bn, A, (int)std::min<int64_t>(sms, t0), false, false, s);
+    if (e != cudaSuccess) return cuda_fail(e, "no-alloc producer launch");
+    A.queue = 1;
+    A.first_stage = 1;
+    A.last_stage = 1;
+    A.pdl_role = pdl ? 2 : 0;
+    e = launch_any(p.bn, A, (int)std::min<int64_t>(sms, t1), false, pdl, s);
+    if (e != cudaSuccess) return cuda_fail(e, "no-alloc consumer launch");
+  }
+  if (error_word) {
+    if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
+    if ((e = cudaMemcpy(error_word, scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost)) != cudaSuccess)
+      return cuda_fail(e, "error word read");
+    if (*error_word != 0) return (*error_word >> 24) == ERRC_PIPELINE ? CUSYNC_ERR_DEVICE : CUSYNC_ERR_TIMEOUT;
+  }
+  return CUSYNC_OK;
+}
