@@ -2,7 +2,7 @@
 
 [cuSync] §II-C (Tile based Computations): the producer's output H is cut
 into tiles, each written by one thread block; a consumer tile of a GEMM
-reads a row of H tiles ("tile C^{xy} needs rows x of A").  §IV-D
+reads the whole row band of H its output rows belong to.  §IV-D
 (Synchronizing Dependent Tiles): before the consumer loads a tile of its A
 input it waits for the producer tiles that write it.  This module derives,
 by brute force over the elements of H, exactly which producer tiles write
@@ -36,8 +36,9 @@ Two geometries are modelled:
   channel blocks per filter tap, so k-block kb reads, for tap (r, s) and
   channel block cb, H[n, p + r - pad, q + s - pad, cb*BK:(cb+1)*BK] for the
   tile's output pixels (p, q) that fall inside the image.  This is the
-  halo-aware form of [cuSync] §IV-E "Conv2DTileSync", whose printed mapping
-  ("[i, j] waits on [i, j/(KxK)]") omits the spatial halo.
+  halo-aware form of [cuSync] §IV-E "Conv2DTileSync", whose mapping from an output
+  tile to the input-image tile it waits on divides the column index by the filter
+  area and leaves out the spatial halo.
 """
 
 import math

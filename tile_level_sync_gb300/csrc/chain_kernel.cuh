@@ -5,7 +5,7 @@
 //
 // Roles inside one CTA (192 threads, one CTA per SM):
 //   warp 0, lane 0  scheduler + TMA issuer.  Claims tiles from a global counter in
-//                   queue order (cuSync §IV-C: stage.tile() = atomicAdd on a per-stage
+//                   queue order (cuSync §IV-C: each kernel takes its next tile from a per-stage
 //                   counter), hands each tile to the other roles through a shared-memory
 //                   ring, and streams the A and B k-blocks into a multi-stage
 //                   shared-memory ring with TMA.  For a consumer tile it issues the
