@@ -87,6 +87,7 @@ def parse():
     p.add_argument("--tile-n", type=int, default=0)
     p.add_argument("--raster", type=int, default=0)
     p.add_argument("--l2-prefetch", type=int, default=0)
+    p.add_argument("--cta-pair", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--sweep-out", default="", help="also time every policy/launch/tile of each workload "
                    "in the comma list --sweep and write the results to this JSON file")
@@ -276,7 +277,7 @@ def run_reference(a):
 class Setup:
     """Device operands and chains of one workload."""
 
-    def __init__(self, wl, inputs, tile_n, launch, raster=0, l2_prefetch=0):
+    def __init__(self, wl, inputs, tile_n, launch, raster=0, l2_prefetch=0, cta_pair=0):
         import torch
         import tile_level_sync_gb300 as cs
         self.cs = cs
@@ -312,18 +313,20 @@ class Setup:
         self.launch = launch
         self.raster = raster
         self.l2_prefetch = l2_prefetch
+        self.cta_pair = cta_pair
         self.chains = {}
 
-    def chain(self, policy, launch=None, tile_n=None, raster=None, l2_prefetch=None):
+    def chain(self, policy, launch=None, tile_n=None, raster=None, l2_prefetch=None, cta_pair=None):
         cs = self.cs
         launch = self.launch if launch is None else launch
         tile_n = self.tile_n if tile_n is None else tile_n
         raster = self.raster if raster is None else raster
         l2_prefetch = self.l2_prefetch if l2_prefetch is None else l2_prefetch
-        key = (policy, launch, tile_n, raster, l2_prefetch)
+        cta_pair = self.cta_pair if cta_pair is None else cta_pair
+        key = (policy, launch, tile_n, raster, l2_prefetch, cta_pair)
         if key not in self.chains:
             self.chains[key] = cs.Chain(cs.make_desc(policy=policy, launch=launch, tile_n=tile_n, raster_rows=raster,
-                                                     l2_prefetch=l2_prefetch, **self.base))
+                                                     l2_prefetch=l2_prefetch, cta_pair=cta_pair, **self.base))
         return self.chains[key]
 
     def run(self, ch):
@@ -419,7 +422,7 @@ def main():
     wl = synth.WORKLOADS[a.workload]
     inputs = synth.workload_inputs(wl, seed=0)
     launch = cs.LAUNCH_PDL if a.launch == "pdl" else cs.LAUNCH_PERSISTENT
-    setup = Setup(wl, inputs, a.tile_n, launch, a.raster, a.l2_prefetch)
+    setup = Setup(wl, inputs, a.tile_n, launch, a.raster, a.l2_prefetch, a.cta_pair)
     flops = wl.gemm_flops()
     peaks, peak_src = load_peaks()
 
@@ -518,7 +521,7 @@ def main():
 
     plan = cs.cusync_plan_waves(setup.chain(best).desc)
     plan148 = cs.cusync_plan_waves(cs.make_desc(policy=best, launch=launch, tile_n=a.tile_n, num_sms=148,
-                                                **setup.base))
+                                                cta_pair=a.cta_pair, **setup.base))
     info = setup.chain(best).info()
 
     cpu = None
@@ -534,7 +537,8 @@ def main():
         "vs_baseline": value / (flops / (PAGES_US_B256 * 1e-6) / 1e12) if wl.name == "gpt3_mlp_m256" else None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, **wl.dims, "policy": best, "launch": a.launch,
-                   "tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "parallelism": "replicas only",
+                   "tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "cta_pair": info.cta_pair,
+                   "parallelism": "replicas only",
                    "l2": f"inputs {alg_bytes / 1e6:.0f} MB of operands > 129 MB L2; no flush between steps"
                    if alg_bytes > 129e6 else "inputs smaller than L2",
                    "vs_baseline_note": "pages' TileSync B=256 chain (840 us) on a V100 in fp16; context only"},
@@ -577,22 +581,22 @@ def sweep(a, torch, cs, synth, out_path):
     Written to a file; not a bench line."""
     names = [n for n in a.sweep.split(",") if n] or list(synth.WORKLOADS)
     results = []
-    variants = [(16, 8), (1, -1), (16, -1), (1, 8)]
+    variants = [(1, -1, 2), (1, -1, 1), (16, -1, 2)]
     for name in names:
         wl = synth.WORKLOADS[name]
         inputs = synth.workload_inputs(wl, seed=0)
         for tile_n in (256, 128):
             setup = Setup(wl, inputs, tile_n, cs.LAUNCH_PERSISTENT)
             row = {"workload": name, "tile_n": tile_n, "gflop": wl.gemm_flops() / 1e9, "us": {}}
-            for vi, (raster, pf) in enumerate(variants):
+            for vi, (raster, pf, pair) in enumerate(variants):
                 pols = ["STREAM", "ROW", "TILE", "STRIDED", "SENTINEL"] if vi == 0 else ["STREAM", "ROW", "TILE"]
                 for pol in pols:
                     for launch in (cs.LAUNCH_PERSISTENT, cs.LAUNCH_PDL):
                         if launch == cs.LAUNCH_PDL and (pol == "STREAM" or vi != 0):
                             continue
-                        key = f"{pol}/{'pdl' if launch else 'pers'}/r{raster}/pf{pf}"
+                        key = f"{pol}/{'pdl' if launch else 'pers'}/r{raster}/p{pair}"
                         try:
-                            ch = setup.chain(pol, launch=launch, raster=raster, l2_prefetch=pf)
+                            ch = setup.chain(pol, launch=launch, raster=raster, l2_prefetch=pf, cta_pair=pair)
                         except cs.CusyncError as e:
                             row["us"][key] = str(e)
                             continue

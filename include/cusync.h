@@ -124,7 +124,10 @@ typedef struct {
                                         sentinel; 0 = 1e9 (one second) */
   int32_t l2_prefetch;               /* weight k-blocks prefetched into L2 ahead of the
                                         shared-memory ring; 0 or -1 = none */
-  int32_t _pad2;
+  int32_t cta_pair;                  /* CTAs per tile: 1, or 2 = a CTA pair (cluster of
+                                        two) computes a 256-row tile with cta_group::2
+                                        MMAs, each CTA loading half of the weight tile
+                                        (MLP chains only); 0 = 1 */
 } cusync_chain_desc_t;
 
 /* Wave arithmetic of a two-kernel chain ([cuSync] §II-A "Thread block Wave Execution",
@@ -155,6 +158,7 @@ typedef struct {
   int32_t grid[2];         /* CTAs of the producer / consumer launch (fused: grid[0]) */
   int32_t num_sms;
   int32_t conv_rows_per_tile; /* CONV_RELU: image rows per row tile */
+  int32_t cta_pair;           /* CTAs per tile (1 or 2); each posts its tile's semaphore */
 } cusync_chain_info_t;
 
 /* Status code as a static string. */

@@ -82,7 +82,7 @@ GPT = dict(K=12288, N1=6144, N2=12288)
 ])
 def test_plan_waves_gpt_mlp(M, tile_n, prod, cons, stream, fused):
     dims = dict(K=256, N1=1024, N2=256) if M == 64 else GPT
-    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, tile_n=tile_n, num_sms=148, **dims)
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, tile_n=tile_n, num_sms=148, cta_pair=1, **dims)
     r = cs.cusync_plan_waves(d)
     assert (r.tbs[0], r.tbs[1]) == (prod, cons)
     assert r.tbs[0] == planner.gemm_tiles(M, dims["N1"], 128, tile_n)
@@ -90,8 +90,41 @@ def test_plan_waves_gpt_mlp(M, tile_n, prod, cons, stream, fused):
     assert (r.tile_m, r.tile_n, r.tile_k) == (128, tile_n, 64)
 
 
+@pytest.mark.parametrize("M,prod,cons,stream,fused", [
+    (256, 24, 48, 2, 1),
+    (1024, 96, 192, 5, 4),
+    (4096, 384, 768, 17, 16),
+])
+def test_plan_waves_cta_pairs(M, prod, cons, stream, fused):
+    # a CTA pair computes a 256 x 256 tile and occupies two SMs: 74 pairs on 148 SMs
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, tile_n=256, num_sms=148, cta_pair=2, **GPT)
+    r = cs.cusync_plan_waves(d)
+    assert (r.tbs[0], r.tbs[1]) == (prod, cons)
+    assert r.cap == 74
+    assert (r.stream_waves, r.fused_waves) == (stream, fused)
+    assert (r.tile_m, r.tile_n) == (256, 256)
+    o = planner.chain_waves([prod, cons], 74)
+    assert (o.stream_waves, o.fused_waves) == (stream, fused)
+    info = cs.cusync_plan_info(d)
+    assert info.cta_pair == 2 and info.grid[0] == 2 * min(74, prod + cons)
+
+
+def test_cta_pair_only_for_mlp_chains():
+    d = cs.make_desc(cs.CHAIN_CONV_RELU, "ROW", n=1, h=14, w=14, c=64, k_out=64, num_sms=148, cta_pair=2)
+    with pytest.raises(cs.CusyncError) as e:
+        cs.cusync_plan_info(d)
+    assert e.value.status == cs.ERR_UNSUPPORTED
+    d.cta_pair = 0
+    assert cs.cusync_plan_info(d).cta_pair == 1
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=64, K=64, N1=256, N2=64, num_sms=148)
+    assert cs.cusync_plan_info(d).cta_pair == 1
+    d.cta_pair = 2
+    assert cs.cusync_plan_info(d).cta_pair == 2
+
+
 def test_plan_swiglu_and_conv():
-    d = cs.make_desc(cs.CHAIN_MLP_SWIGLU, "TILE", M=256, K=8192, N1=3584, N2=8192, tile_n=256, num_sms=148)
+    d = cs.make_desc(cs.CHAIN_MLP_SWIGLU, "TILE", M=256, K=8192, N1=3584, N2=8192, tile_n=256, num_sms=148,
+                     cta_pair=1)
     r = cs.cusync_plan_waves(d)
     assert (r.tbs[0], r.tbs[1]) == (2 * 28, 2 * 32)
     d = cs.make_desc(cs.CHAIN_CONV_RELU, "TILE", n=32, h=14, w=14, c=256, k_out=256, tile_n=256, num_sms=148)
@@ -156,8 +189,11 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES)
 @pytest.mark.parametrize("policy,G", [("TILE", 1), ("ROW", 1), ("STRIDED", 2), ("STRIDED", 1)])
-def test_consumer_waits_match_oracle(case, policy, G):
-    desc = cs.make_desc(policy=policy, strided_group=G, num_sms=148, **case)
+@pytest.mark.parametrize("pair", [1, 2])
+def test_consumer_waits_match_oracle(case, policy, G, pair):
+    if pair == 2 and case["kind"] == cs.CHAIN_CONV_RELU:
+        pytest.skip("CTA pairs are for the MLP chains")
+    desc = cs.make_desc(policy=policy, strided_group=G, num_sms=148, cta_pair=pair, **case)
     try:
         info = cs.cusync_plan_info(desc)
     except cs.CusyncError as e:
@@ -171,7 +207,7 @@ def test_consumer_waits_match_oracle(case, policy, G):
         got = [set() for _ in range(ch.k_blocks)]
         for kb, flag, per_run in cs.cusync_consumer_waits(desc, m):
             mem = _members(policy, flag, nt, D, Gc)
-            assert per_run == len(mem)
+            assert per_run == len(mem) * info.cta_pair   # every CTA of a tile posts
             assert 0 <= flag < info.num_flags
             got[kb] |= mem
         want = deps.wait_sets(ch, policy, m, Gc)
@@ -191,8 +227,11 @@ def test_sentinel_and_stream_wait_on_no_semaphore(case):
 
 @pytest.mark.parametrize("case", CASES)
 @pytest.mark.parametrize("policy,G", [("TILE", 1), ("ROW", 1), ("STRIDED", 2)])
-def test_producer_posts_and_order(case, policy, G):
-    desc = cs.make_desc(policy=policy, strided_group=G, num_sms=148, **case)
+@pytest.mark.parametrize("pair", [1, 2])
+def test_producer_posts_and_order(case, policy, G, pair):
+    if pair == 2 and case["kind"] == cs.CHAIN_CONV_RELU:
+        pytest.skip("CTA pairs are for the MLP chains")
+    desc = cs.make_desc(policy=policy, strided_group=G, num_sms=148, cta_pair=pair, **case)
     try:
         info = cs.cusync_plan_info(desc)
     except cs.CusyncError:

@@ -25,7 +25,8 @@ def _mlp_case(M, K, N1, N2, seed=0):
 
 
 @pytest.mark.parametrize("tile_n", [256, 128])
-def test_tiny_mlp_all_policies_bit_identical(tile_n):
+@pytest.mark.parametrize("pair", [1, 2])
+def test_tiny_mlp_all_policies_bit_identical(tile_n, pair):
     """64x256 . 256x1024 . 1024x256 (the tiny MLP configuration)."""
     (X, W1, W2), (H_ref, Y_ref) = _mlp_case(64, 256, 1024, 256)
     ops = device_mlp_operands(X, W1, W2)
@@ -34,7 +35,8 @@ def test_tiny_mlp_all_policies_bit_identical(tile_n):
         for launch in LAUNCHES:
             if pol == "STREAM" and launch != cs.LAUNCH_PERSISTENT:
                 continue
-            d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, launch, M=64, K=256, N1=1024, N2=256, tile_n=tile_n)
+            d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, launch, M=64, K=256, N1=1024, N2=256, tile_n=tile_n,
+                             cta_pair=pair)
             H, Y, _ = run_mlp(d, *ops, runs=2)
             assert_within_tol(f64(H), H_ref, f"H {pol} {launch}")
             assert_within_tol(f64(Y), Y_ref, f"Y {pol} {launch}")
@@ -51,12 +53,14 @@ def test_tiny_mlp_all_policies_bit_identical(tile_n):
     (1, 64, 512, 128, 256),        # a single token
     (520, 512, 1536, 512, 256),    # more tiles than a persistent CTA's ring holds
 ])
-def test_mlp_shapes_all_policies(M, K, N1, N2, tile_n):
+@pytest.mark.parametrize("pair", [1, 2])
+def test_mlp_shapes_all_policies(M, K, N1, N2, tile_n, pair):
     (X, W1, W2), (H_ref, Y_ref) = _mlp_case(M, K, N1, N2, seed=1)
     ops = device_mlp_operands(X, W1, W2)
     ref_bits = None
     for pol in POLICIES:
-        d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, cs.LAUNCH_PERSISTENT, M=M, K=K, N1=N1, N2=N2, tile_n=tile_n)
+        d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, cs.LAUNCH_PERSISTENT, M=M, K=K, N1=N1, N2=N2, tile_n=tile_n,
+                         cta_pair=pair)
         try:
             cs.cusync_plan_info(d)
         except cs.CusyncError as e:   # StridedSync needs a column-tile count divisible by G
@@ -82,13 +86,15 @@ def test_intermediate_never_holds_negative_zero():
 
 @pytest.mark.parametrize("M,K,N1,N2,tile_n", [(64, 256, 512, 256, 256), (200, 512, 384, 264, 256),
                                                (130, 256, 640, 128, 128)])
-def test_swiglu_all_policies(M, K, N1, N2, tile_n):
+@pytest.mark.parametrize("pair", [1, 2])
+def test_swiglu_all_policies(M, K, N1, N2, tile_n, pair):
     X, Wg, Wu, Wd = synth.mlp_swiglu_inputs(M, K, N1, N2, seed=3)
     H_ref, Y_ref = chains.mlp_swiglu(f64(X), f64(Wg), f64(Wu), f64(Wd))
     ops = device_mlp_operands(X, Wg, Wd, Wup=Wu)
     ref_bits = None
     for pol in POLICIES:
-        d = cs.make_desc(cs.CHAIN_MLP_SWIGLU, pol, cs.LAUNCH_PERSISTENT, M=M, K=K, N1=N1, N2=N2, tile_n=tile_n)
+        d = cs.make_desc(cs.CHAIN_MLP_SWIGLU, pol, cs.LAUNCH_PERSISTENT, M=M, K=K, N1=N1, N2=N2, tile_n=tile_n,
+                         cta_pair=pair)
         try:
             cs.cusync_plan_info(d)
         except cs.CusyncError as e:

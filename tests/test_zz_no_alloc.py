@@ -35,8 +35,8 @@ def test_noalloc_matches_regular_entry_point_twice(policy, launch):
 
 
 def test_noalloc_rejects_plans_beyond_the_fixed_scratch():
-    # 16384 row tiles of RowSync semaphores do not fit the 16368 the array holds
-    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=128 * 16384, K=64, N1=64, N2=64)
+    # 16384 single-CTA row tiles of RowSync semaphores do not fit the 16368 the array holds
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=128 * 16384, K=64, N1=64, N2=64, cta_pair=1)
     lib = cs.load()
     import ctypes
     st = lib.cusync_run_mlp_noalloc(ctypes.byref(d), None, None, None, None, None, None, None)

@@ -3,31 +3,38 @@
 // "A Framework for Fine-Grained Synchronization of Dependent GPU Kernels" (cuSync)
 // and of the CUDA Programming Guide §4.6 "Fine-Grained Synchronization" (CUDA-FGS).
 //
-// Roles inside one CTA (192 threads, one CTA per SM):
-//   warp 0, lane 0  scheduler + TMA issuer.  Claims tiles from a global counter in
-//                   queue order (cuSync §IV-C: each kernel takes its next tile from a per-stage
-//                   counter), hands each tile to the other roles through a shared-memory
-//                   ring, and streams the A and B k-blocks into a multi-stage
-//                   shared-memory ring with TMA.  For a consumer tile it issues the
-//                   weight (B) loads of the next stages first and only then waits on the
-//                   producer's semaphores before each A load (cuSync §V, "Reorder Tile
-//                   Loads and Synchronization").
-//   warp 1          TMEM owner and MMA issuer.  Lane 0 issues tcgen05.mma (128 x BN x 16,
-//                   bf16 in, fp32 accumulate into TMEM) and commits each stage back to
-//                   the loader.  Under the sentinel policy the warp also scans every
-//                   landed A stage for the 0x8000 pattern and re-issues its load while
-//                   the pattern is present (CUDA-FGS §4.6.4.4 and §4.6.7, with a software
-//                   check because sm_103a has no copy-time validity report).
-//   warps 2..5      epilogue.  tcgen05.ld the fp32 accumulator (double-buffered in TMEM
-//                   so the next tile's mainloop overlaps this epilogue), apply GeLU /
-//                   SwiGLU / ReLU, round to bf16 (round-to-nearest-even), replace -0 by
-//                   +0 (CUDA-FGS §4.6.4.3), write whole 16-byte chunks with one 128-bit
-//                   store each, and for a producer tile post its semaphore after all of
-//                   the tile's stores (cuSync §IV-E "Post": barrier, device-scope fence,
-//                   atomic increment).
+// One CTA per SM (PAIR = 1) or one CTA pair per two SMs in a cluster of 2 (PAIR = 2).
+// Roles inside each CTA (192 threads):
+//   warp 0, lane 0  TMA issuer (+ scheduler in the leader CTA).  The scheduler claims
+//                   tiles from a global counter in queue order (cuSync §IV-C: each
+//                   kernel takes its next tile from a per-stage counter) and hands them
+//                   to every role of the CTA (and of the peer CTA) through a
+//                   shared-memory ring.  The loader streams this CTA's rows of A and its
+//                   share of B into a multi-stage shared-memory ring with TMA.  For a
+//                   consumer tile it waits on the producer's semaphores before each A
+//                   load and, while a semaphore is still short, issues the weight (B)
+//                   loads of the next stages (cuSync §V, "Reorder Tile Loads and
+//                   Synchronization").
+//   warp 1          TMEM owner, stage checker and (leader) MMA issuer.  It waits for
+//                   each stage of this CTA to land; under the sentinel policy it scans
+//                   every A element for the 0x8000 pattern and re-issues the A load while
+//                   the pattern is present (CUDA-FGS §4.6.4.4 and §4.6.7, in software:
+//                   sm_103a has no copy-time validity report).  In a pair the peer's
+//                   checker then arrives on the leader's `ready` barrier; the leader's
+//                   lane 0 issues tcgen05.mma (128 x BN x 16 per CTA, or 256 x BN x 16
+//                   across the pair with cta_group::2, bf16 in, fp32 accumulate into
+//                   TMEM) and commits each stage back to the loaders of both CTAs.
+//   warps 2..5      epilogue.  tcgen05.ld of this CTA's 128 accumulator rows
+//                   (double-buffered in TMEM so the next tile's mainloop overlaps this
+//                   epilogue), GeLU / SwiGLU / ReLU, bf16 round-to-nearest-even, -0 -> +0
+//                   (CUDA-FGS §4.6.4.3), whole 16-byte chunks written with one 128-bit
+//                   store each; for a producer tile one thread posts the tile's semaphore
+//                   after all of the CTA's stores (cuSync §IV-E "Post": barrier,
+//                   device-scope fence, atomic increment).  Each CTA of a pair posts its
+//                   own half, so a pair tile's semaphore receives two posts.
 //
 // The pipelining follows the load-compute rules of "ALCOP: Automatic Load-COmpute
-// Pipelining in Deep Learning Compiler for AI-GPUs" (§ pipelining rules): only buffers
+// Pipelining in Deep Learning Compiler for AI-GPUs" (pipelining rules): only buffers
 // filled by asynchronous copies in a sequential k-loop are multi-buffered, each with its
 // own barrier.
 //
@@ -81,14 +88,16 @@ struct ChainArgs {
   uint64_t pipe_timeout_ns;  // shared-memory pipeline waits
 };
 
-template <int BN>
+template <int BN, int PAIR>
 struct KCfg {
-  static constexpr int kStages = (BN == 256) ? 4 : 6;
-  static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kTileM = 128 * PAIR;          // output rows per tile (pair tile)
+  static constexpr int kBRows = BN / PAIR;           // B rows held by each CTA
+  static constexpr int kABytes = 128 * kBK * 2;      // this CTA's 128 rows of A
+  static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = 2 * BN;  // two fp32 accumulators of BN columns
-  static constexpr int kSlots = 4;          // tile hand-off ring
+  static constexpr int kStages = (192 * 1024) / kStageBytes;  // 4, 6 or 8
+  static constexpr int kTmemCols = 2 * BN;           // two fp32 accumulators of BN columns
+  static constexpr int kSlots = 4;                   // tile hand-off ring
   static constexpr int kThreads = 192;
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 1024;
 };
@@ -116,14 +125,19 @@ __device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
 }
 
 __device__ __forceinline__ uint32_t a_tile_bytes(const StageGeo& g) {
-  return g.a_mode == AMODE_GEMM ? (uint32_t)(kBM * kBK * 2) : (uint32_t)(g.img_w * g.th * kBK * 2);
+  return g.a_mode == AMODE_GEMM ? (uint32_t)(128 * kBK * 2) : (uint32_t)(g.img_w * g.th * kBK * 2);
 }
 
-__device__ __forceinline__ void issue_a(const ChainArgs& a, const TileRef& tr, int32_t kb, void* dst, uint64_t* bar,
-                                        uint64_t pol) {
+// This CTA's A k-block: rows [m*tile_m + rank*128, +128) of a GEMM, or the conv box.
+// With to_leader, the copy's completion is counted on the pair leader's barrier `bar`.
+template <int PAIR>
+__device__ __forceinline__ void issue_a(const ChainArgs& a, const TileRef& tr, int32_t kb, uint32_t rank, void* dst,
+                                        uint64_t* bar, uint64_t pol, bool to_leader = false) {
   const StageArgs& S = a.st[tr.s];
   if (S.g.a_mode == AMODE_GEMM) {
-    ptx::tma_load_2d(dst, &S.tmA, bar, kb * kBK, tr.m * kBM, pol);
+    const int32_t row = tr.m * (128 * PAIR) + (int32_t)rank * 128;
+    if (PAIR == 2 && to_leader) ptx::tma_load_2d_to_leader(dst, &S.tmA, ptx::mapa(bar, 0), kb * kBK, row, pol);
+    else ptx::tma_load_2d(dst, &S.tmA, bar, kb * kBK, row, pol);
   } else {
     // implicit im2col: filter tap (r, s), channel block cb; the box is TH image rows of
     // one image shifted by (r-1, s-1); rows or columns outside the image are zero-filled.
@@ -134,30 +148,39 @@ __device__ __forceinline__ void issue_a(const ChainArgs& a, const TileRef& tr, i
   }
 }
 
-template <int BN>
-__device__ __forceinline__ void issue_b(const ChainArgs& a, const TileRef& tr, int32_t kb, uint8_t* dst,
-                                        uint64_t* bar, uint64_t pol) {
-  const StageArgs& S = a.st[tr.s];
+// Row of B where this CTA's share of the weight tile starts.  A single CTA holds the BN
+// rows of its column tile (SwiGLU: BN/2 gate rows then BN/2 up rows); in a pair the
+// leader holds the first half and the peer the second, which for SwiGLU are the gate
+// and up rows.
+template <int BN, int PAIR>
+__device__ __forceinline__ int32_t b_row(const StageArgs& S, const TileRef& tr, uint32_t rank, int half) {
   if (S.g.epi == EPI_SWIGLU) {
-    // gate rows then up rows of the same BN/2 output columns, stacked in one B tile
     const int32_t row0 = tr.c * (BN / 2);
-    ptx::tma_load_2d(dst, &S.tmB, bar, kb * kBK, row0, pol);
-    ptx::tma_load_2d(dst + (BN / 2) * 128, &S.tmB, bar, kb * kBK, S.b_half_rows + row0, pol);
+    const int which = PAIR == 2 ? (int)rank : half;
+    return which == 0 ? row0 : S.b_half_rows + row0;
+  }
+  return tr.c * BN + (PAIR == 2 ? (int32_t)rank * (BN / 2) : 0);
+}
+
+template <int BN, int PAIR>
+__device__ __forceinline__ void issue_b(const ChainArgs& a, const TileRef& tr, int32_t kb, uint32_t rank, uint8_t* dst,
+                                        uint64_t* bar, uint64_t pol, bool to_leader = false) {
+  const StageArgs& S = a.st[tr.s];
+  if (PAIR == 1 && S.g.epi == EPI_SWIGLU) {
+    ptx::tma_load_2d(dst, &S.tmB, bar, kb * kBK, b_row<BN, PAIR>(S, tr, rank, 0), pol);
+    ptx::tma_load_2d(dst + (BN / 2) * 128, &S.tmB, bar, kb * kBK, b_row<BN, PAIR>(S, tr, rank, 1), pol);
+  } else if (PAIR == 2 && to_leader) {
+    ptx::tma_load_2d_to_leader(dst, &S.tmB, ptx::mapa(bar, 0), kb * kBK, b_row<BN, PAIR>(S, tr, rank, 0), pol);
   } else {
-    ptx::tma_load_2d(dst, &S.tmB, bar, kb * kBK, tr.c * BN, pol);
+    ptx::tma_load_2d(dst, &S.tmB, bar, kb * kBK, b_row<BN, PAIR>(S, tr, rank, 0), pol);
   }
 }
 
-template <int BN>
-__device__ __forceinline__ void prefetch_b(const ChainArgs& a, const TileRef& tr, int32_t kb) {
+template <int BN, int PAIR>
+__device__ __forceinline__ void prefetch_b(const ChainArgs& a, const TileRef& tr, int32_t kb, uint32_t rank) {
   const StageArgs& S = a.st[tr.s];
-  if (S.g.epi == EPI_SWIGLU) {
-    const int32_t row0 = tr.c * (BN / 2);
-    ptx::tma_prefetch_2d(&S.tmB, kb * kBK, row0);
-    ptx::tma_prefetch_2d(&S.tmB, kb * kBK, S.b_half_rows + row0);
-  } else {
-    ptx::tma_prefetch_2d(&S.tmB, kb * kBK, tr.c * BN);
-  }
+  ptx::tma_prefetch_2d(&S.tmB, kb * kBK, b_row<BN, PAIR>(S, tr, rank, 0));
+  if (PAIR == 1 && S.g.epi == EPI_SWIGLU) ptx::tma_prefetch_2d(&S.tmB, kb * kBK, b_row<BN, PAIR>(S, tr, rank, 1));
 }
 
 __device__ __forceinline__ void record_error(const ChainArgs& a, uint32_t cls, int32_t tile, int32_t detail) {
@@ -189,25 +212,35 @@ __device__ __forceinline__ float gelu_f(float z) {
 }
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
-template <int BN>
+// Bounded waits on barriers that may receive arrivals from the other CTA of a pair use
+// cluster-scope acquire.
+template <int PAIR>
+__device__ __forceinline__ bool xwait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+  if (PAIR == 2) return ptx::mbar_wait_bounded_cluster(bar, parity, timeout_ns);
+  return ptx::mbar_wait_bounded(bar, parity, timeout_ns);
+}
+
+template <int BN, int PAIR>
 __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ ChainArgs args) {
-  using C = KCfg<BN>;
+  using C = KCfg<BN, PAIR>;
   constexpr int S = C::kStages;
   constexpr uint32_t FULL = 0xFFFFFFFFu;
+  constexpr bool kPair = PAIR == 2;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
-  uint64_t* full = bars;                  // [S]   A+B (or A retry) landed
-  uint64_t* empty = full + S;             // [S]   MMA finished reading the stage
-  uint64_t* tfull = empty + S;            // [2]   accumulator ready
-  uint64_t* tempty = tfull + 2;           // [2]   accumulator drained
-  uint64_t* qfull = tempty + 2;           // [slots] tile index published
-  uint64_t* qempty = qfull + C::kSlots;   // [slots] tile index consumed
+  uint64_t* full = bars;                  // [S]   this CTA's A+B (or A retry) landed
+  uint64_t* empty = full + S;             // [S]   the MMA finished reading the stage
+  uint64_t* ready = empty + S;            // [S]   pair: both CTAs' stages checked (leader)
+  uint64_t* tfull = ready + S;            // [2]   accumulator ready
+  uint64_t* tempty = tfull + 2;           // [2]   accumulator drained (leader in a pair)
+  uint64_t* epi_done = tempty + 2;        // [2]   all epilogue threads of this CTA stored the tile
+  uint64_t* qfull = epi_done + 2;         // [slots] tile index published
+  uint64_t* qempty = qfull + C::kSlots;   // [slots] tile index consumed (leader in a pair)
   uint64_t* mma_done = qempty + C::kSlots;
-  uint64_t* epi_done = mma_done + 1;      // [2]   all epilogue threads stored the tile
-  int32_t* qtile = reinterpret_cast<int32_t*>(epi_done + 2);
+  int32_t* qtile = reinterpret_cast<int32_t*>(mma_done + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qtile + C::kSlots);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   volatile int32_t* it_issued = abort_flag + 1;
@@ -217,6 +250,13 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  // Pair without the sentinel check: the peer's copies complete on the leader's `full`
+  // barriers, which count the bytes of both CTAs.  With the check, each CTA's copies
+  // complete locally, its checker validates them and arrives on the leader's `ready`.
+  const bool direct = kPair && !args.sentinel_check;
+  const bool to_leader = direct && !leader;
 
   if (args.pdl_role == 1) ptx::pdl_launch_dependents();
 
@@ -225,15 +265,18 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
       for (int i = 0; i < S; ++i) {
         ptx::mbar_init(&full[i], 1);
         ptx::mbar_init(&empty[i], 1);
+        ptx::mbar_init(&ready[i], 2);
       }
       for (int i = 0; i < 2; ++i) {
         ptx::mbar_init(&tfull[i], 1);
-        ptx::mbar_init(&tempty[i], 128);
+        ptx::mbar_init(&tempty[i], kPair ? 8 : 128);
         ptx::mbar_init(&epi_done[i], 128);
       }
       for (int i = 0; i < C::kSlots; ++i) {
         ptx::mbar_init(&qfull[i], 1);
-        ptx::mbar_init(&qempty[i], 1 + 4);
+        // consumers of a slot: MMA warp + 4 epilogue warps (+ the peer's loader, checker
+        // and 4 epilogue warps in a pair)
+        ptx::mbar_init(&qempty[i], kPair ? 5 + 6 : 5);
       }
       ptx::mbar_init(mma_done, 1);
       *abort_flag = 0;
@@ -241,8 +284,13 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
       ptx::mbar_init_fence();
     }
     __syncwarp();
-    ptx::tmem_alloc(tmem_slot, C::kTmemCols);
-    ptx::tmem_relinquish();
+    if (kPair) {
+      ptx::tmem_alloc_pair(tmem_slot, C::kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(tmem_slot, C::kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     for (int s = args.first_stage; s <= args.last_stage; ++s) {
@@ -252,12 +300,19 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (kPair) ptx::cluster_sync();  // the peer's barriers exist before any remote arrive
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   const int32_t total = (args.first_stage == args.last_stage) ? (args.first_stage == 0 ? args.tiles0 : args.tiles1)
                                                               : args.tiles0 + args.tiles1;
   const uint64_t pto = args.pipe_timeout_ns;
+
+  // Arrive on "consumed" for ring slot `slot` (the leader's barrier in a pair).
+  auto ring_release = [&](int slot) {
+    if (kPair && !leader) ptx::mbar_arrive_cluster(ptx::mapa(&qempty[slot], 0));
+    else ptx::mbar_arrive(&qempty[slot]);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ scheduler + TMA
@@ -268,16 +323,35 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
       uint32_t it = 0, tcount = 0;
       bool ok = true;
       while (true) {
-        int32_t t = (int32_t)atomicAdd(args.ctrl + CTRL_COUNTER + args.queue, 1u);
-        bool done = t >= total || !ok || *abort_flag;
         const int slot = tcount % C::kSlots;
-        if (!ptx::mbar_wait_bounded(&qempty[slot], ((tcount / C::kSlots) & 1u) ^ 1u, pto)) {
-          record_error(args, ERRC_PIPELINE, 0xFFFFFF, 1);
-          *abort_flag = 1;
-          done = true;
+        const uint32_t tpar = (tcount / C::kSlots) & 1u;
+        int32_t t;
+        bool done;
+        if (leader) {
+          t = (int32_t)atomicAdd(args.ctrl + CTRL_COUNTER + args.queue, 1u);
+          done = t >= total || !ok || *abort_flag;
+          if (!xwait<PAIR>(&qempty[slot], tpar ^ 1u, pto)) {
+            record_error(args, ERRC_PIPELINE, 0xFFFFFF, 1);
+            *abort_flag = 1;
+            done = true;
+          }
+          qtile[slot] = done ? -1 : t;
+          if (kPair) {
+            ptx::st_cluster_u32(ptx::mapa(&qtile[slot], 1), (uint32_t)(done ? -1 : t));
+            ptx::mbar_arrive_cluster(ptx::mapa(&qfull[slot], 1));
+          }
+          ptx::mbar_arrive(&qfull[slot]);
+        } else {
+          if (!xwait<PAIR>(&qfull[slot], tpar, pto)) {
+            record_error(args, ERRC_PIPELINE, 0xFFFFFF, 6);
+            *abort_flag = 1;
+            t = -1;
+          } else {
+            t = qtile[slot];
+          }
+          done = t < 0;
+          ring_release(slot);
         }
-        qtile[slot] = done ? -1 : t;
-        ptx::mbar_arrive(&qfull[slot]);
         ++tcount;
         if (done) break;
 
@@ -288,8 +362,8 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
         const bool cons = (tr.s == 1);
         DepTracker dt;
         dt.reset();
-        int32_t bnext = 0;  // next k-block whose stage slot is armed and whose B load is issued
-        int32_t pfnext = 0; // next k-block whose weights are prefetched into L2
+        int32_t bnext = 0;   // next k-block whose stage slot is armed and whose B load is issued
+        int32_t pfnext = 0;  // next k-block whose weights are prefetched into L2
         const int32_t pfd = (SA.g.a_mode == AMODE_GEMM) ? args.l2_prefetch : 0;
         // Arm the stage slot of k-block kbb and issue its weight (B) load, after prefetching
         // the weights of later k-blocks into L2.  Blocking waits for the slot to drain;
@@ -306,22 +380,23 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
           if (pfd > 0) {
             const int32_t lim = min(KB, kbb + S + pfd);
             if (pfnext < kbb + S) pfnext = min(KB, kbb + S);
-            for (; pfnext < lim; ++pfnext) prefetch_b<BN>(args, tr, pfnext);
+            for (; pfnext < lim; ++pfnext) prefetch_b<BN, PAIR>(args, tr, pfnext, rank);
           }
-          ptx::mbar_arrive_expect_tx(&full[st], tx);
-          issue_b<BN>(args, tr, kbb, smem_b(st), &full[st], pol_b);
+          if (!to_leader) ptx::mbar_arrive_expect_tx(&full[st], direct ? 2 * tx : tx);
+          issue_b<BN, PAIR>(args, tr, kbb, rank, smem_b(st), &full[st], pol_b, to_leader);
           return 1;
         };
         // Semaphores already seen at their target during this tile: [rc_lo, rc_hi).
         int32_t rc_lo = 0, rc_hi = 0;
         uint32_t rc_target = 0;
         // Semaphore waits before A k-block kb (cuSync §IV-E "Wait", bounded).  A wait
-        // first probes a run of up to kProbe consecutive semaphores with relaxed loads (one
-        // round trip) and remembers which already reached the target; only a semaphore
-        // still short of its target is polled.  While polling, the weight loads of the
-        // following stages are issued as their slots drain (cuSync §V "Reorder Tile Loads
-        // and Synchronization").  One acquire fence after the observations orders the
-        // A-tile reads after the producer's releases.
+        // first probes a run of up to kProbe consecutive semaphores with relaxed loads
+        // (one round trip) and remembers which already reached the target; only a
+        // semaphore still short of its target is polled, with exponential back-off.
+        // While polling, the weight loads of the following stages are issued as their
+        // slots drain (cuSync §V "Reorder Tile Loads and Synchronization").  One acquire
+        // fence after the observations orders the A-tile reads after the producer's
+        // releases, and a proxy fence orders them for the TMA (async proxy).
         auto wait_deps = [&](int32_t kb) {
           Wait w[kMaxWaits];
           const int n = dt.next(SA.g, args.dep, tr.m, kb, w);
@@ -334,27 +409,28 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
             const int32_t cnt = min(kProbe, args.num_flags - f);
 #pragma unroll
             for (int q = 0; q < kProbe; ++q) v[q] = q < cnt ? ptx::ld_relaxed_gpu(args.flags + f + q) : 0u;
-            int32_t ready = 0;
+            int32_t nready = 0;
 #pragma unroll
             for (int q = 0; q < kProbe; ++q)
-              if (ready == q && q < cnt && (int32_t)(v[q] - target) >= 0) ready = q + 1;
+              if (nready == q && q < cnt && (int32_t)(v[q] - target) >= 0) nready = q + 1;
             observed = true;
-            if (ready > 0) {
+            if (nready > 0) {
               rc_lo = f;
-              rc_hi = f + ready;
+              rc_hi = f + nready;
               rc_target = target;
               continue;
             }
             const uint64_t t0 = ptx::globaltimer();
-            uint32_t iter = 0;
+            uint32_t iter = 0, backoff = 64;
             while (true) {
               if (reorder && bnext < min(KB, kb + S) && arm_b(bnext, false) > 0) {
                 ++bnext;
               } else {
-                __nanosleep(64);
+                __nanosleep(backoff);
+                if (backoff < 1024) backoff <<= 1;
               }
               if ((int32_t)(ptx::ld_relaxed_gpu(args.flags + f) - target) >= 0) break;
-              if ((++iter & 63u) == 0) {
+              if ((++iter & 15u) == 0) {
                 if (ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u) break;
                 if (ptx::globaltimer() - t0 > args.timeout_ns) {
                   record_error(args, ERRC_FLAG_TIMEOUT, t, (kb << 16) | (f & 0xFFFF));
@@ -384,44 +460,51 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
           }
           if (cons && reorder) wait_deps(kb);
           const int st = (int)((it + (uint32_t)kb) % S);
-          issue_a(args, tr, kb, smem_a(st), &full[st], pol_a);
+          issue_a<PAIR>(args, tr, kb, rank, smem_a(st), &full[st], pol_a, to_leader);
         }
         it += (uint32_t)bnext;
         *it_issued = (int32_t)it;
-        if (!ok) {
+        if (!ok && leader) {
           // hand a terminator to the other roles so that they stop
           const int slot2 = tcount % C::kSlots;
-          if (ptx::mbar_wait_bounded(&qempty[slot2], ((tcount / C::kSlots) & 1u) ^ 1u, pto)) {
+          if (xwait<PAIR>(&qempty[slot2], ((tcount / C::kSlots) & 1u) ^ 1u, pto)) {
             qtile[slot2] = -1;
+            if (kPair) {
+              ptx::st_cluster_u32(ptx::mapa(&qtile[slot2], 1), (uint32_t)-1);
+              ptx::mbar_arrive_cluster(ptx::mapa(&qfull[slot2], 1));
+            }
             ptx::mbar_arrive(&qfull[slot2]);
           }
           break;
         }
+        if (!ok) break;
       }
-      // The last CTA to finish claiming resets this launch's tile counter for the next run.
-      __threadfence();
-      const uint32_t prev = atomicAdd(args.ctrl + CTRL_EXIT + args.queue, 1u);
-      if (prev == gridDim.x - 1) {
-        atomicExch(args.ctrl + CTRL_COUNTER + args.queue, 0u);
-        atomicExch(args.ctrl + CTRL_EXIT + args.queue, 0u);
+      if (leader) {
+        // The last CTA (pair) to finish claiming resets this launch's tile counter.
+        __threadfence();
+        const uint32_t prev = atomicAdd(args.ctrl + CTRL_EXIT + args.queue, 1u);
+        if (prev == gridDim.x / PAIR - 1) {
+          atomicExch(args.ctrl + CTRL_COUNTER + args.queue, 0u);
+          atomicExch(args.ctrl + CTRL_EXIT + args.queue, 0u);
+        }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ checker + MMA issuer
     const uint64_t pol_a = ptx::l2_policy_evict_last();
-    constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, BN);
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(128 * PAIR, BN);
     uint32_t it = 0, tcount = 0, acount = 0, fpar = 0;
     bool ok = true;
     while (ok) {
       const int slot = tcount % C::kSlots;
-      if (!ptx::mbar_wait_bounded(&qfull[slot], (tcount / C::kSlots) & 1u, pto)) {
+      if (!xwait<PAIR>(&qfull[slot], (tcount / C::kSlots) & 1u, pto)) {
         ok = false;
         break;
       }
       const int32_t t = qtile[slot];
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&qempty[slot]);
+      if (lane == 0) ring_release(slot);
       ++tcount;
       if (t < 0) break;
       const TileRef tr = decode_tile(args, t);
@@ -429,24 +512,28 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
       const int acc = acount & 1;
       const uint32_t apar = ((acount >> 1) & 1u) ^ 1u;
       ++acount;
-      if (!ptx::mbar_wait_bounded(&tempty[acc], apar, pto)) {
-        ok = false;
-        break;
+      if (leader) {
+        if (!xwait<PAIR>(&tempty[acc], apar, pto)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
       }
-      ptx::tc_fence_after();
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       const bool check = args.sentinel_check && tr.s == 1;
       const uint32_t abytes = a_tile_bytes(g);
       for (int32_t kb = 0; kb < g.k_blocks; ++kb, ++it) {
         const int st = (int)(it % S);
+        if (to_leader) continue;  // this CTA's stages are counted on the leader's barriers
         if (!ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto)) {
           ok = false;
           break;
         }
         fpar ^= 1u << st;
         if (check) {
-          // Software validity check of the landed A tile: every bf16 element is compared
-          // with the sentinel; while any still holds it, the A load is issued again.
+          // Software validity check of this CTA's landed A tile: every bf16 element is
+          // compared with the sentinel; while any still holds it, the A load is issued
+          // again.
           uint64_t t0 = 0;
           while (true) {
             bool bad = false;
@@ -468,7 +555,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
               __nanosleep(128);
               ptx::fence_proxy_async_smem();
               ptx::mbar_arrive_expect_tx(&full[st], abytes);
-              issue_a(args, tr, kb, smem_a(st), &full[st], pol_a);
+              issue_a<PAIR>(args, tr, kb, rank, smem_a(st), &full[st], pol_a);
             }
             __syncwarp();
             if (!ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto)) {
@@ -479,30 +566,57 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
           }
           if (!ok) break;
         }
-        ptx::tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = ptx::smem_u32(smem_a(st));
-          const uint32_t b0 = ptx::smem_u32(smem_b(st));
-#pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            ptx::umma_bf16(d_tmem, ptx::smem_desc_k128(a0 + 32u * k), ptx::smem_desc_k128(b0 + 32u * k), idesc,
-                           (kb | k) != 0 ? 1u : 0u);
+        if (kPair && !direct) {
+          // both CTAs' shares of this stage are checked before the pair MMA reads them
+          bool rok = true;
+          if (lane == 0) {
+            if (leader) {
+              ptx::mbar_arrive(&ready[st]);
+              rok = ptx::mbar_wait_bounded_cluster(&ready[st], (it / S) & 1u, pto);
+            } else {
+              ptx::mbar_arrive_cluster(ptx::mapa(&ready[st], 0));
+            }
           }
-          ptx::umma_commit(&empty[st]);
+          if (!__shfl_sync(FULL, rok ? 1 : 0, 0)) {
+            ok = false;
+            break;
+          }
+        }
+        if (leader) {
+          ptx::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a0 = ptx::smem_u32(smem_a(st));
+            const uint32_t b0 = ptx::smem_u32(smem_b(st));
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              if (kPair)
+                ptx::umma_bf16_pair(d_tmem, ptx::smem_desc_k128(a0 + 32u * k), ptx::smem_desc_k128(b0 + 32u * k),
+                                    idesc, (kb | k) != 0 ? 1u : 0u);
+              else
+                ptx::umma_bf16(d_tmem, ptx::smem_desc_k128(a0 + 32u * k), ptx::smem_desc_k128(b0 + 32u * k), idesc,
+                               (kb | k) != 0 ? 1u : 0u);
+            }
+            if (kPair) ptx::umma_commit_pair_multicast(&empty[st], 0x3);
+            else ptx::umma_commit(&empty[st]);
+          }
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) ptx::umma_commit(&tfull[acc]);
+      if (leader && lane == 0) {
+        if (kPair) ptx::umma_commit_pair_multicast(&tfull[acc], 0x3);
+        else ptx::umma_commit(&tfull[acc]);
+      }
       __syncwarp();
     }
     if (!ok) {
       record_error(args, ERRC_PIPELINE, 0xFFFFFF, 3);
       *abort_flag = 1;
     }
-    if (lane == 0) {
+    if (leader && lane == 0) {
       // every MMA this thread issued has completed once mma_done flips
-      ptx::umma_commit(mma_done);
+      if (kPair) ptx::umma_commit_pair_multicast(mma_done, 0x1);
+      else ptx::umma_commit(mma_done);
       ptx::mbar_wait_bounded(mma_done, 0, pto);
     }
     __syncwarp();
@@ -523,10 +637,10 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
     uint32_t tcount = 0, acount = 0;
     while (true) {
       const int slot = tcount % C::kSlots;
-      if (!ptx::mbar_wait_bounded(&qfull[slot], (tcount / C::kSlots) & 1u, pto)) break;
+      if (!xwait<PAIR>(&qfull[slot], (tcount / C::kSlots) & 1u, pto)) break;
       const int32_t t = qtile[slot];
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&qempty[slot]);
+      if (lane == 0) ring_release(slot);
       ++tcount;
       if (t < 0) break;
       const TileRef tr = decode_tile(args, t);
@@ -545,7 +659,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
       int64_t grow;
       bool valid;
       if (g.a_mode == AMODE_GEMM) {
-        grow = (int64_t)tr.m * kBM + row;
+        grow = (int64_t)tr.m * (128 * PAIR) + (int64_t)rank * 128 + row;
         valid = grow < g.M;
       } else {
         const int32_t n = tr.m / g.tpi, hb = tr.m % g.tpi;
@@ -598,13 +712,22 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
       // epi_done[acc] counts the arrivals of exactly one tile.
       ptx::mbar_arrive(&epi_done[acc]);
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&tempty[acc]);
+      if (kPair) {
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) ptx::mbar_arrive(&tempty[acc]);
+          else ptx::mbar_arrive_cluster(ptx::mapa(&tempty[acc], 0));
+        }
+      } else {
+        ptx::mbar_arrive(&tempty[acc]);
+      }
       if (tr.s == 0 && threadIdx.x == 64) {
         const int32_t flag = producer_flag(args.dep, tr.m, tr.c);
         if (flag >= 0) {
-          // cuSync §IV-E "Post": after all of the tile's stores (the epi_done barrier
-          // orders the 128 threads' stores before this thread), one device-scope release.
-          if (!ptx::mbar_wait_bounded(&epi_done[acc], apar, pto)) {
+          // cuSync §IV-E "Post": after all of this CTA's stores of the tile (the epi_done
+          // barrier orders its 128 threads' stores before this thread), one device-scope
+          // release.
+          if (!ptx::mbar_wait_sleepy(&epi_done[acc], apar, pto)) {
             record_error(args, ERRC_PIPELINE, t, 5);
             *abort_flag = 1;
           } else if (!((args.flags_bits & kDebugSkipPost) && tr.m == 0 && tr.c == 0)) {
@@ -619,9 +742,11 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
 
   ptx::tc_fence_before();
   __syncthreads();
+  if (kPair) ptx::cluster_sync();  // both CTAs are done with the pair's TMEM and barriers
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+    if (kPair) ptx::tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
   if (args.pdl_role == 2 && threadIdx.x == 0) ptx::pdl_wait();
 }

@@ -52,6 +52,7 @@ cusync_status_t cuda_fail(cudaError_t e, const char* what) {
 
 struct Plan {
   int32_t bn;           // accumulator tile width (UMMA N)
+  int32_t pair;         // CTAs per tile: 1, or 2 (a CTA pair computing a 256-row tile)
   StageGeo geo[2];
   DepCfg dep;
   int64_t num_flags;
@@ -78,8 +79,15 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   if (d.launch != CUSYNC_LAUNCH_PERSISTENT && d.launch != CUSYNC_LAUNCH_PDL) return CUSYNC_ERR_INVALID_ARG;
   const int32_t bn = default_tile_n(d);
   if (bn != 128 && bn != 256) return CUSYNC_ERR_UNSUPPORTED;
+  const bool mlp = d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
+  // Single-CTA tiles by default (they measured faster than CTA pairs on GB300); CTA pairs
+  // (cta_group::2) on request for the GEMM chains.
+  const int32_t pair = d.cta_pair ? d.cta_pair : 1;
+  if (pair != 1 && pair != 2) return CUSYNC_ERR_INVALID_ARG;
+  if (pair == 2 && !mlp) return CUSYNC_ERR_UNSUPPORTED;
   std::memset(p, 0, sizeof(*p));
   p->bn = bn;
+  p->pair = pair;
   StageGeo& g0 = p->geo[0];
   StageGeo& g1 = p->geo[1];
   if (d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU) {
@@ -102,7 +110,7 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
     g1.K = (int32_t)d.N1;
     g1.n_out = bn;
     for (StageGeo* g : {&g0, &g1}) {
-      g->m_tiles = (int32_t)ceil_div(g->M, kBM);
+      g->m_tiles = (int32_t)ceil_div(g->M, (int64_t)kBM * pair);
       g->n_tiles = (int32_t)ceil_div(g->N, g->n_out);
       g->k_blocks = (int32_t)ceil_div(g->K, kBK);
     }
@@ -146,6 +154,7 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   dep.prod_n_out = g0.n_out;
   dep.G = 1;
   dep.D = g0.n_tiles;
+  dep.posts = pair;
   if (d.policy == CUSYNC_POLICY_STRIDED_TILE) {
     const int32_t G = d.strided_group ? d.strided_group : 2;
     if (G < 1 || g0.n_tiles % G) return CUSYNC_ERR_UNSUPPORTED;
@@ -212,14 +221,75 @@ bool encode_nhwc(CUtensorMap* m, const void* ptr, uint64_t n, uint64_t h, uint64
 
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int BN>
+template <int BN, int PAIR>
 cudaError_t set_kernel_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(chain_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       KCfg<BN>::kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(chain_kernel<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       KCfg<BN, PAIR>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(chain_kernel<BN>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                              cudaSharedmemCarveoutMaxShared);
+  e = cudaFuncSetAttribute(chain_kernel<BN, PAIR>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  // Load the kernel now rather than at its first launch (CUDA-FGS §4.6.5, "Overlap").
+  cudaFuncAttributes fa;
+  return cudaFuncGetAttributes(&fa, chain_kernel<BN, PAIR>);
 }
+
+cudaError_t set_all_kernel_attrs() {
+  cudaError_t e = set_kernel_attrs<256, 1>();
+  if (e == cudaSuccess) e = set_kernel_attrs<128, 1>();
+  if (e == cudaSuccess) e = set_kernel_attrs<256, 2>();
+  if (e == cudaSuccess) e = set_kernel_attrs<128, 2>();
+  cudaFuncAttributes fa;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, sentinel_fill_kernel);
+  return e;
+}
+
+// Clusters of two CTAs that can be resident at once (pair kernels), for the current device.
+template <int BN>
+int max_pair_clusters() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(KCfg<BN, 2>::kThreads);
+  cfg.dynamicSmemBytes = KCfg<BN, 2>::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, chain_kernel<BN, 2>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// Grid sizes (CTAs) of the fused launch and of the two separate launches.
+struct Grids {
+  int32_t fused, prod, cons;
+};
+
+Grids make_grids(const Plan& p, int sms, int max_clusters) {
+  const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
+  const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
+  Grids g;
+  if (p.pair == 2) {
+    const int64_t cl = std::max<int64_t>(1, std::min<int64_t>(sms / 2, max_clusters > 0 ? max_clusters : sms / 2));
+    g.fused = (int32_t)(2 * std::min<int64_t>(cl, t0 + t1));
+    g.prod = (int32_t)(2 * std::min<int64_t>(cl, t0));
+    g.cons = (int32_t)(2 * std::min<int64_t>(cl, t1));
+  } else {
+    g.fused = (int32_t)std::min<int64_t>(sms, t0 + t1);
+    g.prod = (int32_t)std::min<int64_t>(sms, t0);
+    g.cons = (int32_t)std::min<int64_t>(sms, t1);
+  }
+  return g;
+}
+
+// B box rows per CTA: BN (single), BN/2 (pair, or either SwiGLU half).
+uint32_t b_box_rows(const Plan& p, bool swiglu) { return (uint32_t)((swiglu || p.pair == 2) ? p.bn / 2 : p.bn); }
 
 }  // namespace
 
@@ -232,7 +302,7 @@ struct cusync_chain {
   int num_sms;
   uint32_t* state;       // CTRL_WORDS control words, then the semaphores
   uint32_t epoch;
-  int32_t grid_fused, grid_prod, grid_cons;
+  Grids grids;
   // TMA descriptors cached by operand pointers
   const void* cached[5];
   bool maps_valid;
@@ -241,31 +311,130 @@ struct cusync_chain {
 
 namespace {
 
-template <int BN>
+template <int BN, int PAIR>
 cudaError_t launch_chain(const ChainArgs& a, int grid, bool cooperative, bool pdl_secondary, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(KCfg<BN>::kThreads);
-  cfg.dynamicSmemBytes = KCfg<BN>::kSmemBytes;
+  cfg.blockDim = dim3(KCfg<BN, PAIR>::kThreads);
+  cfg.dynamicSmemBytes = KCfg<BN, PAIR>::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[3];
   int na = 0;
-  if (cooperative) {
-    attr[na].id = cudaLaunchAttributeCooperative;
-    attr[na].val.cooperative = 1;
+  if (PAIR == 2) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
     ++na;
-  } else if (pdl_secondary) {
+  }
+  if (pdl_secondary) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
+  if (cooperative) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    ++na;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, chain_kernel<BN>, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, chain_kernel<BN, PAIR>, a);
+  if (e != cudaSuccess && cooperative && PAIR == 2) {
+    // Cooperative cluster launches may be refused; the grid is already sized to the
+    // clusters that can be resident at once, so launch without the attribute.
+    cudaGetLastError();
+    CUSYNC_LOG("cooperative cluster launch refused (%s); launching without it", cudaGetErrorString(e));
+    cfg.numAttrs = na - 1;
+    e = cudaLaunchKernelEx(&cfg, chain_kernel<BN, PAIR>, a);
+  }
+  return e;
 }
 
-cudaError_t launch_any(int bn, const ChainArgs& a, int grid, bool coop, bool pdl2, cudaStream_t s) {
-  return bn == 256 ? launch_chain<256>(a, grid, coop, pdl2, s) : launch_chain<128>(a, grid, coop, pdl2, s);
+cudaError_t launch_any(const Plan& p, const ChainArgs& a, int grid, bool coop, bool pdl2, cudaStream_t s) {
+  if (p.pair == 2)
+    return p.bn == 256 ? launch_chain<256, 2>(a, grid, coop, pdl2, s) : launch_chain<128, 2>(a, grid, coop, pdl2, s);
+  return p.bn == 256 ? launch_chain<256, 1>(a, grid, coop, pdl2, s) : launch_chain<128, 1>(a, grid, coop, pdl2, s);
+}
+
+// The launches of one chain run: sentinel fill, then one fused persistent kernel or the
+// producer and consumer kernels (stream order, or programmatic dependent launch).
+cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArgs A, const Grids& g, void* h,
+                           int sms, cudaStream_t stream) {
+  cudaError_t e;
+  if (d.policy == CUSYNC_POLICY_SENTINEL && !(d.flags & CUSYNC_DEBUG_SKIP_INIT)) {
+    const int64_t bytes = (int64_t)p.geo[0].M * p.geo[0].N * 2;
+    const int64_t n16 = bytes / 16;
+    int blocks = (int)std::min<int64_t>(ceil_div(n16, 256), (int64_t)sms * 8);
+    if (blocks < 1) blocks = 1;
+    sentinel_fill_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<uint4*>(h), n16);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "sentinel fill launch");
+  }
+  const bool two_kernels = d.policy == CUSYNC_POLICY_STREAM || d.launch == CUSYNC_LAUNCH_PDL;
+  if (!two_kernels) {
+    A.queue = 0;
+    A.first_stage = 0;
+    A.last_stage = 1;
+    A.pdl_role = 0;
+    e = launch_any(p, A, g.fused, /*coop=*/true, false, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fused chain launch");
+    return CUSYNC_OK;
+  }
+  const bool pdl = d.policy != CUSYNC_POLICY_STREAM;
+  A.queue = 0;
+  A.first_stage = 0;
+  A.last_stage = 0;
+  A.pdl_role = pdl ? 1 : 0;
+  e = launch_any(p, A, g.prod, false, false, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "producer launch");
+  A.queue = 1;
+  A.first_stage = 1;
+  A.last_stage = 1;
+  A.pdl_role = pdl ? 2 : 0;
+  e = launch_any(p, A, g.cons, false, pdl, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "consumer launch");
+  return CUSYNC_OK;
+}
+
+// TMA descriptors of a run: 2-D maps for GEMM operands, 4-D NHWC maps for conv images.
+bool encode_maps(const cusync_chain_desc_t& d, const Plan& p, ChainArgs& A, const void* a0, const void* b0,
+                 const void* b1, const void* h) {
+  bool ok = true;
+  if (d.kind == CUSYNC_CHAIN_CONV_RELU) {
+    const StageGeo& g0 = p.geo[0];
+    ok &= encode_nhwc(&A.st[0].tmA, a0, d.n, d.h, d.w, d.c, (uint32_t)g0.th);
+    ok &= encode_2d(&A.st[0].tmB, b0, (uint64_t)d.k_out, (uint64_t)9 * d.c, b_box_rows(p, false));
+    ok &= encode_nhwc(&A.st[1].tmA, h, d.n, d.h, d.w, d.k_out, (uint32_t)g0.th);
+    ok &= encode_2d(&A.st[1].tmB, b1, (uint64_t)d.k_out, (uint64_t)9 * d.k_out, b_box_rows(p, false));
+  } else {
+    const bool swiglu = d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
+    ok &= encode_2d(&A.st[0].tmA, a0, (uint64_t)d.M, (uint64_t)d.K, 128u);
+    ok &= encode_2d(&A.st[0].tmB, b0, (uint64_t)(swiglu ? 2 * d.N1 : d.N1), (uint64_t)d.K, b_box_rows(p, swiglu));
+    ok &= encode_2d(&A.st[1].tmA, h, (uint64_t)d.M, (uint64_t)d.N1, 128u);
+    ok &= encode_2d(&A.st[1].tmB, b1, (uint64_t)d.N2, (uint64_t)d.N1, b_box_rows(p, false));
+  }
+  return ok;
+}
+
+// Kernel arguments that do not depend on the operand pointers.
+void fill_static_args(const cusync_chain_desc_t& d, const Plan& p, uint32_t* state, ChainArgs& A) {
+  const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
+  const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
+  const uint64_t timeout = d.timeout_ns ? d.timeout_ns : kDefaultTimeoutNs;
+  A.st[0].g = p.geo[0];
+  A.st[1].g = p.geo[1];
+  A.st[0].b_half_rows = d.kind == CUSYNC_CHAIN_MLP_SWIGLU ? (int32_t)d.N1 : 0;
+  A.dep = p.dep;
+  A.ctrl = state;
+  A.flags = state + CTRL_WORDS;
+  A.tiles0 = (int32_t)t0;
+  A.tiles1 = (int32_t)t1;
+  A.flags_bits = d.flags;
+  A.sentinel_check = d.policy == CUSYNC_POLICY_SENTINEL ? 1 : 0;
+  A.num_flags = (int32_t)p.num_flags;
+  A.l2_prefetch = d.l2_prefetch <= 0 ? 0 : d.l2_prefetch;
+  A.timeout_ns = timeout;
+  A.pipe_timeout_ns = std::max<uint64_t>(4 * timeout, 2000000000ull);
 }
 
 cusync_status_t run_chain(cusync_chain* ch, const void* a0, const void* b0, const void* b1, void* h, void* y,
@@ -280,22 +449,7 @@ cusync_status_t run_chain(cusync_chain* ch, const void* a0, const void* b0, cons
   ChainArgs& A = ch->args;
   const void* ptrs[5] = {a0, b0, b1, h, y};
   if (!ch->maps_valid || std::memcmp(ptrs, ch->cached, sizeof(ptrs)) != 0) {
-    bool ok = true;
-    if (d.kind == CUSYNC_CHAIN_CONV_RELU) {
-      const StageGeo& g0 = p.geo[0];
-      ok &= encode_nhwc(&A.st[0].tmA, a0, d.n, d.h, d.w, d.c, (uint32_t)g0.th);
-      ok &= encode_2d(&A.st[0].tmB, b0, (uint64_t)d.k_out, (uint64_t)9 * d.c, (uint32_t)p.bn);
-      ok &= encode_nhwc(&A.st[1].tmA, h, d.n, d.h, d.w, d.k_out, (uint32_t)g0.th);
-      ok &= encode_2d(&A.st[1].tmB, b1, (uint64_t)d.k_out, (uint64_t)9 * d.k_out, (uint32_t)p.bn);
-    } else {
-      const bool swiglu = d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
-      ok &= encode_2d(&A.st[0].tmA, a0, (uint64_t)d.M, (uint64_t)d.K, (uint32_t)kBM);
-      ok &= encode_2d(&A.st[0].tmB, b0, (uint64_t)(swiglu ? 2 * d.N1 : d.N1), (uint64_t)d.K,
-                      (uint32_t)(swiglu ? p.bn / 2 : p.bn));
-      ok &= encode_2d(&A.st[1].tmA, h, (uint64_t)d.M, (uint64_t)d.N1, (uint32_t)kBM);
-      ok &= encode_2d(&A.st[1].tmB, b1, (uint64_t)d.N2, (uint64_t)d.N1, (uint32_t)p.bn);
-    }
-    if (!ok) {
+    if (!encode_maps(d, p, A, a0, b0, b1, h)) {
       ch->maps_valid = false;
       return CUSYNC_ERR_INVALID_ARG;
     }
@@ -305,42 +459,7 @@ cusync_status_t run_chain(cusync_chain* ch, const void* a0, const void* b0, cons
   A.st[0].out = h;
   A.st[1].out = y;
   A.epoch = ++ch->epoch;
-
-  cudaError_t e;
-  if (d.policy == CUSYNC_POLICY_SENTINEL && !(d.flags & CUSYNC_DEBUG_SKIP_INIT)) {
-    const int64_t bytes = (int64_t)p.geo[0].M * p.geo[0].N * 2;
-    const int64_t n16 = bytes / 16;
-    int blocks = (int)std::min<int64_t>(ceil_div(n16, 256), (int64_t)ch->num_sms * 8);
-    if (blocks < 1) blocks = 1;
-    sentinel_fill_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<uint4*>(h), n16);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "sentinel fill launch");
-  }
-  const bool two_kernels = d.policy == CUSYNC_POLICY_STREAM || d.launch == CUSYNC_LAUNCH_PDL;
-  if (!two_kernels) {
-    ChainArgs a = A;
-    a.queue = 0;
-    a.first_stage = 0;
-    a.last_stage = 1;
-    a.pdl_role = 0;
-    e = launch_any(p.bn, a, ch->grid_fused, /*coop=*/true, false, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "fused chain launch");
-    return CUSYNC_OK;
-  }
-  const bool pdl = d.policy != CUSYNC_POLICY_STREAM;
-  ChainArgs a = A;
-  a.queue = 0;
-  a.first_stage = 0;
-  a.last_stage = 0;
-  a.pdl_role = pdl ? 1 : 0;
-  e = launch_any(p.bn, a, ch->grid_prod, false, false, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "producer launch");
-  a.queue = 1;
-  a.first_stage = 1;
-  a.last_stage = 1;
-  a.pdl_role = pdl ? 2 : 0;
-  e = launch_any(p.bn, a, ch->grid_cons, false, pdl, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "consumer launch");
-  return CUSYNC_OK;
+  return launch_run(d, p, A, ch->grids, h, ch->num_sms, stream);
 }
 
 }  // namespace
@@ -395,9 +514,11 @@ cusync_status_t cusync_plan_waves(const cusync_chain_desc_t* d, cusync_wave_repo
   if (query_num_sms(d->num_sms, &sms) != 0) return CUSYNC_ERR_CUDA;
   const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
   const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
-  st = cusync_wave_stats(t0, t1, 1, sms, out);
+  // one tile per CTA, or per CTA pair: a pair occupies two SMs
+  st = cusync_wave_stats(t0, t1, 1, p.pair == 2 ? sms / 2 : sms, out);
   if (st != CUSYNC_OK) return st;
-  out->tile_m = kBM;
+  out->num_sms = sms;
+  out->tile_m = kBM * p.pair;
   out->tile_n = p.bn;
   out->tile_k = kBK;
   return CUSYNC_OK;
@@ -423,13 +544,12 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
   int dev_sms = 0;
   if (query_num_sms(0, &dev_sms) != 0) return CUSYNC_ERR_CUDA;
   const int sms = d->num_sms > 0 ? std::min(d->num_sms, dev_sms) : dev_sms;
-  if ((e = set_kernel_attrs<256>()) != cudaSuccess) return cuda_fail(e, "kernel attributes (256)");
-  if ((e = set_kernel_attrs<128>()) != cudaSuccess) return cuda_fail(e, "kernel attributes (128)");
-  // Load the kernels now rather than at their first launch (CUDA-FGS §4.6.5, "Overlap").
-  cudaFuncAttributes fa;
-  cudaFuncGetAttributes(&fa, chain_kernel<256>);
-  cudaFuncGetAttributes(&fa, chain_kernel<128>);
-  cudaFuncGetAttributes(&fa, sentinel_fill_kernel);
+  if ((e = set_all_kernel_attrs()) != cudaSuccess) return cuda_fail(e, "kernel attributes");
+  const int max_clusters = p.pair == 2 ? (p.bn == 256 ? max_pair_clusters<256>() : max_pair_clusters<128>()) : 0;
+  if (p.pair == 2 && max_clusters < 1) {
+    CUSYNC_LOG("no CTA-pair cluster can be resident on this device");
+    return CUSYNC_ERR_UNSUPPORTED;
+  }
 
   cusync_chain* ch = new (std::nothrow) cusync_chain();
   if (!ch) return CUSYNC_ERR_NOMEM;
@@ -449,32 +569,14 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
     return cuda_fail(e, "state clear");
   }
   ch->epoch = 0;
-  const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
-  const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
-  ch->grid_fused = (int32_t)std::min<int64_t>(sms, t0 + t1);
-  ch->grid_prod = (int32_t)std::min<int64_t>(sms, t0);
-  ch->grid_cons = (int32_t)std::min<int64_t>(sms, t1);
-
+  ch->grids = make_grids(p, sms, max_clusters);
   ChainArgs& A = ch->args;
   std::memset(&A, 0, sizeof(A));
-  A.st[0].g = p.geo[0];
-  A.st[1].g = p.geo[1];
-  A.st[0].b_half_rows = d->kind == CUSYNC_CHAIN_MLP_SWIGLU ? (int32_t)d->N1 : 0;
-  A.dep = p.dep;
-  A.ctrl = ch->state;
-  A.flags = ch->state + CTRL_WORDS;
-  A.tiles0 = (int32_t)t0;
-  A.tiles1 = (int32_t)t1;
-  A.flags_bits = d->flags;
-  A.sentinel_check = d->policy == CUSYNC_POLICY_SENTINEL ? 1 : 0;
-  A.num_flags = (int32_t)p.num_flags;
-  A.l2_prefetch = d->l2_prefetch <= 0 ? 0 : d->l2_prefetch;
-  A.timeout_ns = ch->d.timeout_ns;
-  A.pipe_timeout_ns = std::max<uint64_t>(4 * ch->d.timeout_ns, 2000000000ull);
+  fill_static_args(ch->d, p, ch->state, A);
   ch->maps_valid = false;
   *out = ch;
-  CUSYNC_LOG("chain kind=%d policy=%d launch=%d tiles=%lld+%lld bn=%d sms=%d flags=%lld", d->kind, d->policy,
-             d->launch, (long long)t0, (long long)t1, p.bn, sms, (long long)p.num_flags);
+  CUSYNC_LOG("chain kind=%d policy=%d launch=%d tiles=%d+%d bn=%d pair=%d sms=%d clusters=%d flags=%lld", d->kind,
+             d->policy, d->launch, A.tiles0, A.tiles1, p.bn, p.pair, sms, max_clusters, (long long)p.num_flags);
   return CUSYNC_OK;
 }
 
@@ -535,17 +637,17 @@ cusync_status_t cusync_plan_info(const cusync_chain_desc_t* d, cusync_chain_info
     out->k_blocks[s] = p.geo[s].k_blocks;
     out->n_out[s] = p.geo[s].n_out;
   }
-  out->tile_m = kBM;
+  out->tile_m = kBM * p.pair;
   out->tile_n = p.bn;
   out->tile_k = kBK;
   out->strided_group = p.dep.G;
   out->strided_distance = p.dep.D;
   out->num_flags = (int32_t)p.num_flags;
-  const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
-  const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
+  const Grids g = make_grids(p, sms, 0);
   const bool two = d->policy == CUSYNC_POLICY_STREAM || d->launch == CUSYNC_LAUNCH_PDL;
-  out->grid[0] = (int32_t)std::min<int64_t>(sms, two ? t0 : t0 + t1);
-  out->grid[1] = two ? (int32_t)std::min<int64_t>(sms, t1) : 0;
+  out->grid[0] = two ? g.prod : g.fused;
+  out->grid[1] = two ? g.cons : 0;
+  out->cta_pair = p.pair;
   out->num_sms = sms;
   out->conv_rows_per_tile = d->kind == CUSYNC_CHAIN_CONV_RELU ? p.geo[0].th : 0;
   return CUSYNC_OK;
@@ -646,6 +748,7 @@ static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocWords];
 
 constexpr int kMaxDevices = 64;
 uint32_t* g_noalloc_ptr[kMaxDevices] = {};
+int g_noalloc_clusters[kMaxDevices][2] = {};  // co-resident CTA-pair clusters (BN 256, 128)
 std::mutex g_noalloc_mu;
 
 // Device address of the scratch array and the kernels' attributes for the current device,
@@ -655,12 +758,13 @@ cusync_status_t noalloc_setup(int dev, uint32_t** out) {
   if (dev < 0 || dev >= kMaxDevices) return CUSYNC_ERR_UNSUPPORTED;
   if (g_noalloc_ptr[dev] == nullptr) {
     if (!load_encoder()) return CUSYNC_ERR_CUDA;
-    cudaError_t e = set_kernel_attrs<256>();
-    if (e == cudaSuccess) e = set_kernel_attrs<128>();
+    cudaError_t e = set_all_kernel_attrs();
     if (e != cudaSuccess) return cuda_fail(e, "kernel attributes (no-alloc)");
     uint32_t* p = nullptr;
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    g_noalloc_clusters[dev][0] = max_pair_clusters<256>();
+    g_noalloc_clusters[dev][1] = max_pair_clusters<128>();
     g_noalloc_ptr[dev] = p;
   }
   *out = g_noalloc_ptr[dev];
@@ -701,69 +805,20 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
 
   ChainArgs A;
   std::memset(&A, 0, sizeof(A));
-  const bool swiglu = d->kind == CUSYNC_CHAIN_MLP_SWIGLU;
-  bool ok = true;
-  ok &= encode_2d(&A.st[0].tmA, X, (uint64_t)d->M, (uint64_t)d->K, (uint32_t)kBM);
-  ok &= encode_2d(&A.st[0].tmB, W1t, (uint64_t)(swiglu ? 2 * d->N1 : d->N1), (uint64_t)d->K,
-                  (uint32_t)(swiglu ? p.bn / 2 : p.bn));
-  ok &= encode_2d(&A.st[1].tmA, H, (uint64_t)d->M, (uint64_t)d->N1, (uint32_t)kBM);
-  ok &= encode_2d(&A.st[1].tmB, W2t, (uint64_t)d->N2, (uint64_t)d->N1, (uint32_t)p.bn);
-  if (!ok) return CUSYNC_ERR_INVALID_ARG;
-  const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
-  const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
-  const uint64_t timeout = d->timeout_ns ? d->timeout_ns : kDefaultTimeoutNs;
-  A.st[0].g = p.geo[0];
-  A.st[1].g = p.geo[1];
+  if (!encode_maps(*d, p, A, X, W1t, W2t, H)) return CUSYNC_ERR_INVALID_ARG;
+  fill_static_args(*d, p, scratch, A);
   A.st[0].out = H;
   A.st[1].out = Y;
-  A.st[0].b_half_rows = swiglu ? (int32_t)d->N1 : 0;
-  A.dep = p.dep;
-  A.ctrl = scratch;
-  A.flags = scratch + CTRL_WORDS;
-  A.tiles0 = (int32_t)t0;
-  A.tiles1 = (int32_t)t1;
   A.epoch = 1;  // the semaphores are cleared below, so every call is run number one
-  A.flags_bits = d->flags;
-  A.sentinel_check = d->policy == CUSYNC_POLICY_SENTINEL ? 1 : 0;
-  A.num_flags = (int32_t)p.num_flags;
-  A.l2_prefetch = d->l2_prefetch <= 0 ? 0 : d->l2_prefetch;
-  A.timeout_ns = timeout;
-  A.pipe_timeout_ns = std::max<uint64_t>(4 * timeout, 2000000000ull);
+  const int max_clusters = g_noalloc_clusters[dev][p.bn == 256 ? 0 : 1];
+  if (p.pair == 2 && max_clusters < 1) return CUSYNC_ERR_UNSUPPORTED;
+  const Grids grids = make_grids(p, sms, max_clusters);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // Clear what must start at zero: error word, tile counters, semaphores.
   e = cudaMemsetAsync(scratch, 0, ((size_t)CTRL_WORDS + (size_t)p.num_flags) * sizeof(uint32_t), s);
   if (e != cudaSuccess) return cuda_fail(e, "no-alloc scratch clear");
-  if (d->policy == CUSYNC_POLICY_SENTINEL && !(d->flags & CUSYNC_DEBUG_SKIP_INIT)) {
-    const int64_t n16 = (int64_t)p.geo[0].M * p.geo[0].N * 2 / 16;
-    int blocks = (int)std::min<int64_t>(ceil_div(n16, 256), (int64_t)sms * 8);
-    if (blocks < 1) blocks = 1;
-    sentinel_fill_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<uint4*>(H), n16);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "sentinel fill launch");
-  }
-  const bool two_kernels = d->policy == CUSYNC_POLICY_STREAM || d->launch == CUSYNC_LAUNCH_PDL;
-  if (!two_kernels) {
-    A.queue = 0;
-    A.first_stage = 0;
-    A.last_stage = 1;
-    A.pdl_role = 0;
-    e = launch_any(p.bn, A, (int)std::min<int64_t>(sms, t0 + t1), /*coop=*/true, false, s);
-    if (e != cudaSuccess) return cuda_fail(e, "no-alloc fused launch");
-  } else {
-    const bool pdl = d->policy != CUSYNC_POLICY_STREAM;
-    A.queue = 0;
-    A.first_stage = 0;
-    A.last_stage = 0;
-    A.pdl_role = pdl ? 1 : 0;
-    e = launch_any(p.bn, A, (int)std::min<int64_t>(sms, t0), false, false, s);
-    if (e != cudaSuccess) return cuda_fail(e, "no-alloc producer launch");
-    A.queue = 1;
-    A.first_stage = 1;
-    A.last_stage = 1;
-    A.pdl_role = pdl ? 2 : 0;
-    e = launch_any(p.bn, A, (int)std::min<int64_t>(sms, t1), false, pdl, s);
-    if (e != cudaSuccess) return cuda_fail(e, "no-alloc consumer launch");
-  }
+  if ((st = launch_run(*d, p, A, grids, H, sms, s)) != CUSYNC_OK) return st;
   if (error_word) {
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
     if ((e = cudaMemcpy(error_word, scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost)) != cudaSuccess)

@@ -61,6 +61,7 @@ struct DepCfg {
   int32_t prod_n_out;    // H columns per producer tile
   int32_t G;             // StridedSync group size (tiles sharing one semaphore)
   int32_t D;             // StridedSync distance = nt / G
+  int32_t posts;         // posts per producer tile (one per CTA computing it: 1 or 2)
 };
 
 struct Wait {
@@ -154,16 +155,17 @@ struct DepTracker {
     int n = 0;
     if (cons.a_mode == AMODE_GEMM) {
       const int32_t c = (kb * kBK) / d.prod_n_out;
+      const uint32_t pp = (uint32_t)d.posts;
       if (pol == POL_ROW) {
-        if (kb == 0) out[n++] = Wait{m, (uint32_t)d.prod_n_tiles};
+        if (kb == 0) out[n++] = Wait{m, (uint32_t)d.prod_n_tiles * pp};
         return n;
       }
       if (c == last_c) return 0;
       last_c = c;
       if (pol == POL_TILE) {
-        out[n++] = Wait{m * d.prod_n_tiles + c, 1u};
+        out[n++] = Wait{m * d.prod_n_tiles + c, pp};
       } else if (c < d.D) {  // StridedSync: group c is first touched at column c
-        out[n++] = Wait{m * d.D + c, (uint32_t)d.G};
+        out[n++] = Wait{m * d.D + c, (uint32_t)d.G * pp};
       }
       return n;
     }
@@ -182,7 +184,8 @@ struct DepTracker {
         if (lo_t < a) a = lo_t;
         if (hi_t > b) b = hi_t;
       }
-      for (int32_t mp = a; mp <= b && n < kMaxWaits; ++mp) out[n++] = Wait{mp, (uint32_t)d.prod_n_tiles};
+      for (int32_t mp = a; mp <= b && n < kMaxWaits; ++mp)
+        out[n++] = Wait{mp, (uint32_t)(d.prod_n_tiles * d.posts)};
       return n;
     }
     const int32_t c = (cb * kBK) / d.prod_n_out;
@@ -191,11 +194,11 @@ struct DepTracker {
     for (int32_t mp = a; mp <= b && n < kMaxWaits; ++mp) {
       if (lo[c] <= mp && mp <= hi[c]) continue;
       if (pol == POL_TILE) {
-        out[n++] = Wait{mp * d.prod_n_tiles + c, 1u};
+        out[n++] = Wait{mp * d.prod_n_tiles + c, (uint32_t)d.posts};
         if (lo[c] > hi[c]) { lo[c] = mp; hi[c] = mp; }
         else { if (mp < lo[c]) lo[c] = mp; if (mp > hi[c]) hi[c] = mp; }
       } else {  // StridedSync: the whole group of column c, for row tile mp
-        out[n++] = Wait{mp * d.D + (c % d.D), (uint32_t)d.G};
+        out[n++] = Wait{mp * d.D + (c % d.D), (uint32_t)(d.G * d.posts)};
         for (int32_t cc = c % d.D; cc < d.prod_n_tiles; cc += d.D) {
           if (lo[cc] > hi[cc]) { lo[cc] = mp; hi[cc] = mp; }
           else { if (mp < lo[cc]) lo[cc] = mp; if (mp > hi[cc]) hi[cc] = mp; }
