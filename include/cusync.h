@@ -102,6 +102,7 @@ typedef enum {
 #define CUSYNC_FLAG_NO_REORDER (1u << 0)  /* disable [cuSync] §V "Reorder Tile Loads and
                                              Synchronization": weight tiles are then
                                              loaded only after the A-tile wait */
+#define CUSYNC_FLAG_TRACE (1u << 1)       /* record a per-tile timeline (cusync_chain_trace) */
 /* Fault injection for tests; each makes a device wait expire, never a GPU fault. */
 #define CUSYNC_DEBUG_SKIP_POST (1u << 8)     /* the producer never posts tile (0,0) */
 #define CUSYNC_DEBUG_SKIP_INIT (1u << 9)     /* SENTINEL: skip the sentinel fill */
@@ -122,12 +123,14 @@ typedef struct {
                                         plain row-major */
   uint64_t timeout_ns;               /* bound of every device wait on a semaphore or a
                                         sentinel; 0 = 1e9 (one second) */
-  int32_t l2_prefetch;               /* weight k-blocks prefetched into L2 ahead of the
-                                        shared-memory ring; 0 or -1 = none */
+  int32_t l2_prefetch;               /* k-blocks a prefetch warp runs ahead of the TMA
+                                        loader, prefetching weight (and producer
+                                        activation) rows into L2; 0 or -1 = none */
   int32_t cta_pair;                  /* CTAs per tile: 1, or 2 = a CTA pair (cluster of
                                         two) computes a 256-row tile with cta_group::2
                                         MMAs, each CTA loading half of the weight tile
-                                        (MLP chains only); 0 = 1 */
+                                        (MLP chains only); 0 = 2 for MLP chains with
+                                        M >= 1024, else 1 */
 } cusync_chain_desc_t;
 
 /* Wave arithmetic of a two-kernel chain ([cuSync] §II-A "Thread block Wave Execution",
@@ -147,6 +150,21 @@ typedef struct {
   int32_t tile_m, tile_n, tile_k; /* tile chosen by cusync_plan_waves (0 from
                                      cusync_wave_stats) */
 } cusync_wave_report_t;
+
+/* One tile of a traced run (CUSYNC_FLAG_TRACE): %globaltimer stamps in nanoseconds taken
+ * by the roles of the CTA that ran it.  Producer tiles come first (index < tbs[0]). */
+typedef struct {
+  uint32_t tile;      /* tile index in the chain (producer tiles, then consumer tiles) */
+  uint32_t smid;      /* SM the tile ran on */
+  uint32_t cta;       /* CTA (blockIdx.x) */
+  uint32_t stage;     /* 0 producer, 1 consumer */
+  uint64_t t_claim;   /* the scheduler claimed the tile */
+  uint64_t t_ready;   /* the loader passed the waits before k-block 0 */
+  uint64_t t_mma0;    /* the first stage of the tile landed */
+  uint64_t t_mma1;    /* the last MMA of the tile was committed */
+  uint64_t t_epi;     /* the epilogue finished the tile's stores */
+  uint64_t t_post;    /* producer: the tile's semaphore was posted (0 if none) */
+} cusync_trace_rec_t;
 
 /* Geometry of a chain (for tests and introspection). */
 typedef struct {
@@ -251,6 +269,12 @@ cusync_status_t cusync_tile_at(const cusync_chain_desc_t* d, int32_t stage, int3
 cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, const void* X, const void* W1t,
                                        const void* W2t, void* H, void* Y, cusync_stream_t stream,
                                        uint32_t* error_word);
+
+/* Copy the timeline of the last traced run into out[0..max) (one record per tile, in tile
+ * order) after synchronising `stream`; *n_out receives the number of tiles.  INVALID_ARG
+ * if the chain was created without CUSYNC_FLAG_TRACE. */
+cusync_status_t cusync_chain_trace(cusync_chain_t chain, cusync_stream_t stream, cusync_trace_rec_t* out,
+                                   int32_t max, int32_t* n_out);
 
 /* Release the chain's device state.  NULL is accepted. */
 cusync_status_t cusync_destroy_chain(cusync_chain_t chain);

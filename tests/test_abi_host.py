@@ -118,6 +118,9 @@ def test_cta_pair_only_for_mlp_chains():
     assert cs.cusync_plan_info(d).cta_pair == 1
     d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=64, K=64, N1=256, N2=64, num_sms=148)
     assert cs.cusync_plan_info(d).cta_pair == 1
+    d.M = 1024
+    assert cs.cusync_plan_info(d).cta_pair == 2
+    d.M = 64
     d.cta_pair = 2
     assert cs.cusync_plan_info(d).cta_pair == 2
 

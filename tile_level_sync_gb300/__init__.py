@@ -21,6 +21,7 @@ CHAIN_MLP_GELU, CHAIN_MLP_SWIGLU, CHAIN_CONV_RELU = range(3)
 LAUNCH_PERSISTENT, LAUNCH_PDL = range(2)
 (OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NOMEM, ERR_TIMEOUT, ERR_DEVICE) = range(7)
 FLAG_NO_REORDER = 1 << 0
+FLAG_TRACE = 1 << 1
 DEBUG_SKIP_POST = 1 << 8
 DEBUG_SKIP_INIT = 1 << 9
 
@@ -45,6 +46,12 @@ class cusync_wave_report_t(ctypes.Structure):
         ("last_wave_tbs", c_i64), ("cap", c_i32), ("occupancy", c_i32), ("num_sms", c_i32),
         ("tile_m", c_i32), ("tile_n", c_i32), ("tile_k", c_i32),
     ]
+
+
+class cusync_trace_rec_t(ctypes.Structure):
+    _fields_ = [("tile", c_u32), ("smid", c_u32), ("cta", c_u32), ("stage", c_u32),
+                ("t_claim", c_u64), ("t_ready", c_u64), ("t_mma0", c_u64), ("t_mma1", c_u64),
+                ("t_epi", c_u64), ("t_post", c_u64)]
 
 
 class cusync_chain_info_t(ctypes.Structure):
@@ -75,6 +82,7 @@ _SIGNATURES = {
                                ctypes.POINTER(c_i32)]),
     "cusync_run_mlp_noalloc": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), _VP, _VP, _VP, _VP, _VP, _VP,
                                        ctypes.POINTER(c_u32)]),
+    "cusync_chain_trace": (c_i32, [_VP, _VP, ctypes.POINTER(cusync_trace_rec_t), c_i32, ctypes.POINTER(c_i32)]),
     "cusync_destroy_chain": (c_i32, [_VP]),
 }
 
@@ -238,6 +246,16 @@ def cusync_chain_reset(chain, stream=None):
     _check(load().cusync_chain_reset(chain, _stream(stream)), "cusync_chain_reset")
 
 
+def cusync_chain_trace(chain, stream=None, max_records=1 << 20):
+    """Per-tile timeline of the last traced run, as a list of dicts."""
+    n = c_i32()
+    _check(load().cusync_chain_trace(chain, _stream(stream), None, 0, ctypes.byref(n)), "cusync_chain_trace")
+    k = min(n.value, max_records)
+    buf = (cusync_trace_rec_t * k)()
+    _check(load().cusync_chain_trace(chain, _stream(stream), buf, k, ctypes.byref(n)), "cusync_chain_trace")
+    return [{f: getattr(r, f) for f, _ in cusync_trace_rec_t._fields_} for r in buf]
+
+
 def cusync_destroy_chain(chain):
     _check(load().cusync_destroy_chain(chain), "cusync_destroy_chain")
 
@@ -263,6 +281,9 @@ class Chain:
 
     def info(self):
         return cusync_plan_info(self.desc)
+
+    def trace(self, stream=None):
+        return cusync_chain_trace(self.handle, stream)
 
     def close(self):
         if self.handle is not None:

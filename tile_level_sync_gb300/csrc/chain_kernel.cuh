@@ -64,8 +64,17 @@ struct StageArgs {
   CUtensorMap tmA;       // activations: 2-D [M, K] or 4-D NHWC image
   CUtensorMap tmB;       // weights [N (or 2*N1), K]
   void* out;             // bf16 [M, N] row-major (conv: [pixels, channels])
+  const uint16_t* a_ptr; // GEMM activations [a_rows, K] row-major, for L2 prefetch
+  const uint16_t* b_ptr; // weights [b_rows, K] row-major, for L2 prefetch
+  int32_t a_rows, b_rows;
   StageGeo g;
   int32_t b_half_rows;   // SwiGLU: row offset of the up-projection half of B
+};
+
+// One tile of a traced run (same layout as cusync_trace_rec_t).
+struct TraceRec {
+  uint32_t tile, smid, cta, stage;
+  uint64_t t_claim, t_ready, t_mma0, t_mma1, t_epi, t_post;
 };
 
 struct ChainArgs {
@@ -73,6 +82,7 @@ struct ChainArgs {
   DepCfg dep;
   uint32_t* flags;       // semaphores
   uint32_t* ctrl;        // CTRL_* words
+  TraceRec* trace;       // per-tile timeline, or null
   int32_t queue;         // tile counter slot used by this launch
   int32_t first_stage;   // stages served by this launch: [first_stage, last_stage]
   int32_t last_stage;
@@ -82,7 +92,7 @@ struct ChainArgs {
   int32_t pdl_role;      // 1: trigger dependents at start; 2: wait on the primary at exit
   int32_t sentinel_check;
   int32_t num_flags;     // semaphores in `flags`
-  int32_t l2_prefetch;   // weight k-blocks prefetched into L2 ahead of the B loads (0: none)
+  int32_t l2_prefetch;   // k-blocks the prefetch warp runs ahead of the loader (0: none)
   int32_t _pad;
   uint64_t timeout_ns;       // semaphore / sentinel waits
   uint64_t pipe_timeout_ns;  // shared-memory pipeline waits
@@ -98,7 +108,7 @@ struct KCfg {
   static constexpr int kStages = (192 * 1024) / kStageBytes;  // 4, 6 or 8
   static constexpr int kTmemCols = 2 * BN;           // two fp32 accumulators of BN columns
   static constexpr int kSlots = 4;                   // tile hand-off ring
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 224;              // 7 warps: loader, MMA, 4 epilogue, prefetch
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 1024;
 };
 
@@ -122,6 +132,11 @@ __device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
   tile_at(a.st[s].g, u, &m, &y);
   const int32_t c = (s == 0) ? producer_col(a.dep, y) : y;
   return TileRef{s, m, c};
+}
+
+// Index of queue position t in the chain's tile numbering (producer tiles first).
+__device__ __forceinline__ int32_t chain_tile(const ChainArgs& a, int32_t t) {
+  return a.first_stage == 1 ? a.tiles0 + t : t;
 }
 
 __device__ __forceinline__ uint32_t a_tile_bytes(const StageGeo& g) {
@@ -176,11 +191,18 @@ __device__ __forceinline__ void issue_b(const ChainArgs& a, const TileRef& tr, i
   }
 }
 
-template <int BN, int PAIR>
-__device__ __forceinline__ void prefetch_b(const ChainArgs& a, const TileRef& tr, int32_t kb, uint32_t rank) {
-  const StageArgs& S = a.st[tr.s];
-  ptx::tma_prefetch_2d(&S.tmB, kb * kBK, b_row<BN, PAIR>(S, tr, rank, 0));
-  if (PAIR == 1 && S.g.epi == EPI_SWIGLU) ptx::tma_prefetch_2d(&S.tmB, kb * kBK, b_row<BN, PAIR>(S, tr, rank, 1));
+// Prefetch into L2, one 128-byte line per row, the k-block kb of `rows` rows starting at
+// `row0` of a row-major bf16 matrix with `nrows` rows and K columns; rows are spread over
+// the warp's lanes.  Lines that would reach past the end of the matrix are skipped.
+__device__ __forceinline__ void prefetch_rows(const uint16_t* base, int32_t nrows, int32_t K, int32_t row0,
+                                              int32_t rows, int32_t kb, int lane) {
+  const int32_t col = kb * kBK;
+  if (base == nullptr || col >= K) return;
+  for (int32_t r = lane; r < rows; r += 32) {
+    const int32_t row = row0 + r;
+    if (row >= nrows || (row == nrows - 1 && col + kBK > K)) continue;
+    ptx::prefetch_l2(base + (int64_t)row * K + col);
+  }
 }
 
 __device__ __forceinline__ void record_error(const ChainArgs& a, uint32_t cls, int32_t tile, int32_t detail) {
@@ -221,7 +243,7 @@ __device__ __forceinline__ bool xwait(uint64_t* bar, uint32_t parity, uint64_t t
 }
 
 template <int BN, int PAIR>
-__global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ ChainArgs args) {
+__global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ ChainArgs args) {
   using C = KCfg<BN, PAIR>;
   constexpr int S = C::kStages;
   constexpr uint32_t FULL = 0xFFFFFFFFu;
@@ -244,6 +266,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qtile + C::kSlots);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   volatile int32_t* it_issued = abort_flag + 1;
+  volatile uint32_t* progress = reinterpret_cast<volatile uint32_t*>(it_issued + 1);  // k-blocks issued
 
   auto smem_a = [&](int st) { return stage_base + st * C::kStageBytes; };
   auto smem_b = [&](int st) { return stage_base + st * C::kStageBytes + C::kABytes; };
@@ -274,13 +297,14 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
       }
       for (int i = 0; i < C::kSlots; ++i) {
         ptx::mbar_init(&qfull[i], 1);
-        // consumers of a slot: MMA warp + 4 epilogue warps (+ the peer's loader, checker
-        // and 4 epilogue warps in a pair)
-        ptx::mbar_init(&qempty[i], kPair ? 5 + 6 : 5);
+        // consumers of a slot: MMA warp, 4 epilogue warps and the prefetch warp (+ the
+        // peer's loader, checker, 4 epilogue warps and prefetch warp in a pair)
+        ptx::mbar_init(&qempty[i], kPair ? 6 + 7 : 6);
       }
       ptx::mbar_init(mma_done, 1);
       *abort_flag = 0;
       *it_issued = 0;
+      *progress = 0;
       ptx::mbar_init_fence();
     }
     __syncwarp();
@@ -359,15 +383,41 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
         const StageArgs& SA = args.st[tr.s];
         const int32_t KB = SA.g.k_blocks;
         const uint32_t tx = a_tile_bytes(SA.g) + (uint32_t)C::kBBytes;
+        TraceRec* trec = (args.trace && leader) ? args.trace + chain_tile(args, t) : nullptr;
+        if (trec) {
+          trec->tile = (uint32_t)chain_tile(args, t);
+          trec->smid = ptx::smid();
+          trec->cta = blockIdx.x;
+          trec->stage = (uint32_t)tr.s;
+          trec->t_claim = ptx::globaltimer();
+          trec->t_post = 0;
+        }
         const bool cons = (tr.s == 1);
-        DepTracker dt;
-        dt.reset();
+        GemmDepTracker gdt;
+        gdt.reset();
+        ConvDepTracker cdt;  // touched (stack arrays) only by convolution tiles
+        if (SA.g.a_mode != AMODE_GEMM) cdt.reset();
         int32_t bnext = 0;   // next k-block whose stage slot is armed and whose B load is issued
-        int32_t pfnext = 0;  // next k-block whose weights are prefetched into L2
-        const int32_t pfd = (SA.g.a_mode == AMODE_GEMM) ? args.l2_prefetch : 0;
-        // Arm the stage slot of k-block kbb and issue its weight (B) load, after prefetching
-        // the weights of later k-blocks into L2.  Blocking waits for the slot to drain;
-        // non-blocking returns 0 if it has not drained yet.
+        // Per-tile invariants of the k-loop, so that the single loader thread spends as few
+        // instructions per k-block as possible (its latency is on the critical path).
+        const bool gemm = SA.g.a_mode == AMODE_GEMM;
+        const CUtensorMap* tmA = &SA.tmA;
+        const CUtensorMap* tmB = &SA.tmB;
+        const int32_t a_row = tr.m * (128 * PAIR) + (int32_t)rank * 128;
+        const int32_t brow0 = b_row<BN, PAIR>(SA, tr, rank, 0);
+        const int32_t brow1 = (PAIR == 1 && SA.g.epi == EPI_SWIGLU) ? b_row<BN, PAIR>(SA, tr, rank, 1) : -1;
+        const uint32_t txs = direct ? 2 * tx : tx;
+        // k-blocks at which the consumer may have to wait: only where a k-block starts
+        // reading a producer tile it has not read before (GEMM), every k-block (conv).
+        const int32_t pol = args.dep.policy;
+        int32_t dep_every = 0;
+        if (cons && (pol == POL_ROW || pol == POL_TILE || pol == POL_STRIDED)) {
+          if (!gemm) dep_every = 1;
+          else if (pol == POL_ROW) dep_every = KB + 1;
+          else dep_every = max(1, args.dep.prod_n_out / kBK);
+        }
+        // Arm the stage slot of k-block kbb and issue its weight (B) load.  Blocking waits
+        // for the slot to drain; non-blocking returns 0 if it has not drained yet.
         auto arm_b = [&](int32_t kbb, bool blocking) -> int {
           const uint32_t j = it + (uint32_t)kbb;
           const int st = (int)(j % S);
@@ -377,13 +427,14 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
           } else if (!ptx::mbar_test_wait(&empty[st], par)) {
             return 0;
           }
-          if (pfd > 0) {
-            const int32_t lim = min(KB, kbb + S + pfd);
-            if (pfnext < kbb + S) pfnext = min(KB, kbb + S);
-            for (; pfnext < lim; ++pfnext) prefetch_b<BN, PAIR>(args, tr, pfnext, rank);
+          uint8_t* dst = smem_b(st);
+          if (to_leader) {
+            ptx::tma_load_2d_to_leader(dst, tmB, ptx::mapa(&full[st], 0), kbb * kBK, brow0, pol_b);
+          } else {
+            ptx::mbar_arrive_expect_tx(&full[st], txs);
+            ptx::tma_load_2d(dst, tmB, &full[st], kbb * kBK, brow0, pol_b);
+            if (brow1 >= 0) ptx::tma_load_2d(dst + (BN / 2) * 128, tmB, &full[st], kbb * kBK, brow1, pol_b);
           }
-          if (!to_leader) ptx::mbar_arrive_expect_tx(&full[st], direct ? 2 * tx : tx);
-          issue_b<BN, PAIR>(args, tr, kbb, rank, smem_b(st), &full[st], pol_b, to_leader);
           return 1;
         };
         // Semaphores already seen at their target during this tile: [rc_lo, rc_hi).
@@ -399,7 +450,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
         // releases, and a proxy fence orders them for the TMA (async proxy).
         auto wait_deps = [&](int32_t kb) {
           Wait w[kMaxWaits];
-          const int n = dt.next(SA.g, args.dep, tr.m, kb, w);
+          const int n = gemm ? gdt.next(args.dep, tr.m, kb, w) : cdt.next(SA.g, args.dep, tr.m, kb, w);
           bool observed = false;
           for (int i = 0; i < n; ++i) {
             const int32_t f = w[i].flag;
@@ -448,7 +499,8 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
           }
         };
         for (int32_t kb = 0; kb < KB; ++kb) {
-          if (cons && !reorder) wait_deps(kb);
+          const bool dep_kb = dep_every > 0 && (kb % dep_every) == 0;
+          if (dep_kb && !reorder) wait_deps(kb);
           if (bnext == kb) {
             if (arm_b(kb, true) < 0) {
               record_error(args, ERRC_PIPELINE, t, 2);
@@ -458,9 +510,16 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
             }
             ++bnext;
           }
-          if (cons && reorder) wait_deps(kb);
+          if (dep_kb && reorder) wait_deps(kb);
+          if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
           const int st = (int)((it + (uint32_t)kb) % S);
-          issue_a<PAIR>(args, tr, kb, rank, smem_a(st), &full[st], pol_a, to_leader);
+          if (gemm) {
+            if (to_leader) ptx::tma_load_2d_to_leader(smem_a(st), tmA, ptx::mapa(&full[st], 0), kb * kBK, a_row, pol_a);
+            else ptx::tma_load_2d(smem_a(st), tmA, &full[st], kb * kBK, a_row, pol_a);
+          } else {
+            issue_a<PAIR>(args, tr, kb, rank, smem_a(st), &full[st], pol_a, to_leader);
+          }
+          *progress = it + (uint32_t)kb + 1u;
         }
         it += (uint32_t)bnext;
         *it_issued = (int32_t)it;
@@ -584,6 +643,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
         }
         if (leader) {
           ptx::tc_fence_after();
+          if (lane == 0 && kb == 0 && args.trace) args.trace[chain_tile(args, t)].t_mma0 = ptx::globaltimer();
           if (lane == 0) {
             const uint32_t a0 = ptx::smem_u32(smem_a(st));
             const uint32_t b0 = ptx::smem_u32(smem_b(st));
@@ -606,6 +666,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
       if (leader && lane == 0) {
         if (kPair) ptx::umma_commit_pair_multicast(&tfull[acc], 0x3);
         else ptx::umma_commit(&tfull[acc]);
+        if (args.trace) args.trace[chain_tile(args, t)].t_mma1 = ptx::globaltimer();
       }
       __syncwarp();
     }
@@ -628,6 +689,55 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
         ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto);
         fpar ^= 1u << st;
       }
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ L2 prefetch warp
+    // Follows the tile ring and, paced by the loader's progress counter, prefetches the
+    // k-blocks up to l2_prefetch ahead of the loader into L2 with plain prefetch
+    // instructions: this CTA's weight rows for every GEMM tile and its activation rows
+    // for producer tiles.  The TMA loads that follow then hit L2 instead of waiting for
+    // HBM, which the shared-memory ring alone cannot hide.
+    const int32_t pd = args.l2_prefetch;
+    uint32_t tcount = 0, it0 = 0;
+    while (true) {
+      const int slot = tcount % C::kSlots;
+      if (!xwait<PAIR>(&qfull[slot], (tcount / C::kSlots) & 1u, pto)) break;
+      const int32_t t = qtile[slot];
+      __syncwarp();
+      if (lane == 0) ring_release(slot);
+      ++tcount;
+      if (t < 0) break;
+      const TileRef tr = decode_tile(args, t);
+      const StageArgs& SA = args.st[tr.s];
+      const StageGeo& g = SA.g;
+      const int32_t KB = g.k_blocks;
+      if (pd > 0 && g.a_mode == AMODE_GEMM) {
+        const int32_t a_row0 = tr.m * (128 * PAIR) + (int32_t)rank * 128;
+        const int32_t b_rows = (PAIR == 1 && g.epi == EPI_SWIGLU) ? BN / 2 : BN / PAIR;
+        const int32_t b0 = b_row<BN, PAIR>(SA, tr, rank, 0);
+        const int32_t b1 = (PAIR == 1 && g.epi == EPI_SWIGLU) ? b_row<BN, PAIR>(SA, tr, rank, 1) : -1;
+        bool live = true;
+        for (int32_t kb = 0; kb < KB && live; ++kb) {
+          const uint32_t j = it0 + (uint32_t)kb;
+          if (lane == 0) {
+            const uint64_t t0 = ptx::globaltimer();
+            while ((int32_t)(j - *progress) >= pd) {
+              __nanosleep(64);
+              if (*abort_flag || ptx::globaltimer() - t0 > pto) {
+                live = false;
+                break;
+              }
+            }
+          }
+          live = __shfl_sync(FULL, live ? 1 : 0, 0) != 0;
+          if (!live) break;
+          prefetch_rows(SA.b_ptr, SA.b_rows, g.K, b0, b_rows, kb, lane);
+          if (b1 >= 0) prefetch_rows(SA.b_ptr, SA.b_rows, g.K, b1, b_rows, kb, lane);
+          if (tr.s == 0) prefetch_rows(SA.a_ptr, SA.a_rows, g.K, a_row0, 128, kb, lane);
+        }
+      }
+      it0 += (uint32_t)KB;
     }
     __syncwarp();
   } else {
@@ -721,6 +831,10 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
       } else {
         ptx::mbar_arrive(&tempty[acc]);
       }
+      if (args.trace && leader && threadIdx.x == 64) {
+        if (ptx::mbar_wait_bounded(&epi_done[acc], apar, pto))
+          args.trace[chain_tile(args, t)].t_epi = ptx::globaltimer();
+      }
       if (tr.s == 0 && threadIdx.x == 64) {
         const int32_t flag = producer_flag(args.dep, tr.m, tr.c);
         if (flag >= 0) {
@@ -733,6 +847,7 @@ __global__ void __launch_bounds__(192, 1) chain_kernel(const __grid_constant__ C
           } else if (!((args.flags_bits & kDebugSkipPost) && tr.m == 0 && tr.c == 0)) {
             ptx::fence_acq_rel_gpu();
             ptx::red_release_gpu_add(args.flags + flag, 1u);
+            if (args.trace && leader) args.trace[chain_tile(args, t)].t_post = ptx::globaltimer();
           }
         }
       }

@@ -25,6 +25,7 @@ using namespace cusync;
 namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // one second
+constexpr int32_t kDefaultPrefetch = 0;                // L2 prefetch lead (off: it measured slower)
 
 bool log_enabled() {
   static int v = -1;
@@ -80,9 +81,9 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   const int32_t bn = default_tile_n(d);
   if (bn != 128 && bn != 256) return CUSYNC_ERR_UNSUPPORTED;
   const bool mlp = d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
-  // Single-CTA tiles by default (they measured faster than CTA pairs on GB300); CTA pairs
-  // (cta_group::2) on request for the GEMM chains.
-  const int32_t pair = d.cta_pair ? d.cta_pair : 1;
+  // CTA pairs (cta_group::2, 256-row tiles) for MLP chains with at least 1024 tokens,
+  // where they measured faster on GB300; single-CTA 128-row tiles otherwise.
+  const int32_t pair = d.cta_pair ? d.cta_pair : ((mlp && d.M >= 1024) ? 2 : 1);
   if (pair != 1 && pair != 2) return CUSYNC_ERR_INVALID_ARG;
   if (pair == 2 && !mlp) return CUSYNC_ERR_UNSUPPORTED;
   std::memset(p, 0, sizeof(*p));
@@ -301,6 +302,7 @@ struct cusync_chain {
   int device;
   int num_sms;
   uint32_t* state;       // CTRL_WORDS control words, then the semaphores
+  TraceRec* trace;       // per-tile timeline (CUSYNC_FLAG_TRACE), or null
   uint32_t epoch;
   Grids grids;
   // TMA descriptors cached by operand pointers
@@ -408,6 +410,14 @@ bool encode_maps(const cusync_chain_desc_t& d, const Plan& p, ChainArgs& A, cons
     ok &= encode_2d(&A.st[1].tmB, b1, (uint64_t)d.k_out, (uint64_t)9 * d.k_out, b_box_rows(p, false));
   } else {
     const bool swiglu = d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
+    A.st[0].a_ptr = static_cast<const uint16_t*>(a0);
+    A.st[0].a_rows = (int32_t)d.M;
+    A.st[0].b_ptr = static_cast<const uint16_t*>(b0);
+    A.st[0].b_rows = (int32_t)(swiglu ? 2 * d.N1 : d.N1);
+    A.st[1].a_ptr = static_cast<const uint16_t*>(h);
+    A.st[1].a_rows = (int32_t)d.M;
+    A.st[1].b_ptr = static_cast<const uint16_t*>(b1);
+    A.st[1].b_rows = (int32_t)d.N2;
     ok &= encode_2d(&A.st[0].tmA, a0, (uint64_t)d.M, (uint64_t)d.K, 128u);
     ok &= encode_2d(&A.st[0].tmB, b0, (uint64_t)(swiglu ? 2 * d.N1 : d.N1), (uint64_t)d.K, b_box_rows(p, swiglu));
     ok &= encode_2d(&A.st[1].tmA, h, (uint64_t)d.M, (uint64_t)d.N1, 128u);
@@ -432,7 +442,7 @@ void fill_static_args(const cusync_chain_desc_t& d, const Plan& p, uint32_t* sta
   A.flags_bits = d.flags;
   A.sentinel_check = d.policy == CUSYNC_POLICY_SENTINEL ? 1 : 0;
   A.num_flags = (int32_t)p.num_flags;
-  A.l2_prefetch = d.l2_prefetch <= 0 ? 0 : d.l2_prefetch;
+  A.l2_prefetch = d.l2_prefetch < 0 ? 0 : (d.l2_prefetch == 0 ? kDefaultPrefetch : d.l2_prefetch);
   A.timeout_ns = timeout;
   A.pipe_timeout_ns = std::max<uint64_t>(4 * timeout, 2000000000ull);
 }
@@ -569,10 +579,22 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
     return cuda_fail(e, "state clear");
   }
   ch->epoch = 0;
+  ch->trace = nullptr;
+  if (d->flags & CUSYNC_FLAG_TRACE) {
+    const size_t n = (size_t)p.geo[0].m_tiles * p.geo[0].n_tiles + (size_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
+    if (cudaMalloc(&ch->trace, n * sizeof(TraceRec)) != cudaSuccess ||
+        cudaMemset(ch->trace, 0, n * sizeof(TraceRec)) != cudaSuccess) {
+      if (ch->trace) cudaFree(ch->trace);
+      cudaFree(ch->state);
+      delete ch;
+      return CUSYNC_ERR_NOMEM;
+    }
+  }
   ch->grids = make_grids(p, sms, max_clusters);
   ChainArgs& A = ch->args;
   std::memset(&A, 0, sizeof(A));
   fill_static_args(ch->d, p, ch->state, A);
+  A.trace = ch->trace;
   ch->maps_valid = false;
   *out = ch;
   CUSYNC_LOG("chain kind=%d policy=%d launch=%d tiles=%d+%d bn=%d pair=%d sms=%d clusters=%d flags=%lld", d->kind,
@@ -716,9 +738,24 @@ cusync_status_t cusync_producer_col(const cusync_chain_desc_t* d, int32_t y, int
   return CUSYNC_OK;
 }
 
+cusync_status_t cusync_chain_trace(cusync_chain_t ch, cusync_stream_t stream, cusync_trace_rec_t* out, int32_t max,
+                                   int32_t* n_out) {
+  static_assert(sizeof(cusync_trace_rec_t) == sizeof(TraceRec), "trace record layout");
+  if (!ch || !n_out || max < 0 || (max > 0 && !out) || !ch->trace) return CUSYNC_ERR_INVALID_ARG;
+  const int32_t n = ch->args.tiles0 + ch->args.tiles1;
+  *n_out = n;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  const int32_t k = std::min(n, max);
+  if (k > 0 && (e = cudaMemcpy(out, ch->trace, (size_t)k * sizeof(TraceRec), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "trace read");
+  return CUSYNC_OK;
+}
+
 cusync_status_t cusync_destroy_chain(cusync_chain_t ch) {
   if (!ch) return CUSYNC_OK;
   cudaError_t e = cudaSuccess;
+  if (ch->trace) cudaFree(ch->trace);
   if (ch->state) e = cudaFree(ch->state);
   delete ch;
   return e == cudaSuccess ? CUSYNC_OK : CUSYNC_ERR_CUDA;

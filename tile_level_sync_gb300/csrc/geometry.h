@@ -136,13 +136,44 @@ CUSYNC_HD void conv_row_tiles(const StageGeo& g, int32_t m, int32_t r, int32_t* 
 // k order.  Each producer tile is waited for once, when a k-block first reads it
 // (TileSync), or with its whole group (StridedSync), or all rows up front before the
 // first k-block (RowSync).  Sentinel and stream-ordered chains wait on no semaphore.
-struct DepTracker {
-  int32_t last_c;                      // GEMM: last producer column tile waited
-  int32_t lo[kMaxConvColTiles];        // conv: waited producer row-tile interval per column tile
+//
+// GEMM chains: consumer k-block kb reads producer column tile c = kb*kBK / prod_n_out
+// of its own row tile, so at most one wait per k-block and only the last column waited
+// needs remembering (register state only).
+struct GemmDepTracker {
+  int32_t last_c;
+  CUSYNC_HD void reset() { last_c = -1; }
+  CUSYNC_HD int next(const DepCfg& d, int32_t m, int32_t kb, Wait* out) {
+    const int32_t pol = d.policy;
+    const uint32_t pp = (uint32_t)d.posts;
+    if (pol == POL_ROW) {
+      if (kb != 0) return 0;
+      out[0] = Wait{m, (uint32_t)d.prod_n_tiles * pp};
+      return 1;
+    }
+    if (pol != POL_TILE && pol != POL_STRIDED) return 0;
+    const int32_t c = (kb * kBK) / d.prod_n_out;
+    if (c == last_c) return 0;
+    last_c = c;
+    if (pol == POL_TILE) {
+      out[0] = Wait{m * d.prod_n_tiles + c, pp};
+      return 1;
+    }
+    if (c < d.D) {  // StridedSync: group c is first touched at column c
+      out[0] = Wait{m * d.D + c, (uint32_t)d.G * pp};
+      return 1;
+    }
+    return 0;
+  }
+};
+
+// Convolution chains (halo): the producer row tiles a k-block reads depend on its filter
+// row; per producer column tile, the row tiles already waited for form one interval.
+struct ConvDepTracker {
+  int32_t lo[kMaxConvColTiles];  // waited producer row-tile interval per column tile
   int32_t hi[kMaxConvColTiles];
 
   CUSYNC_HD void reset() {
-    last_c = -1;
     for (int i = 0; i < kMaxConvColTiles; ++i) {
       lo[i] = 1;
       hi[i] = 0;  // empty interval
@@ -153,23 +184,7 @@ struct DepTracker {
     const int32_t pol = d.policy;
     if (pol != POL_TILE && pol != POL_ROW && pol != POL_STRIDED) return 0;
     int n = 0;
-    if (cons.a_mode == AMODE_GEMM) {
-      const int32_t c = (kb * kBK) / d.prod_n_out;
-      const uint32_t pp = (uint32_t)d.posts;
-      if (pol == POL_ROW) {
-        if (kb == 0) out[n++] = Wait{m, (uint32_t)d.prod_n_tiles * pp};
-        return n;
-      }
-      if (c == last_c) return 0;
-      last_c = c;
-      if (pol == POL_TILE) {
-        out[n++] = Wait{m * d.prod_n_tiles + c, pp};
-      } else if (c < d.D) {  // StridedSync: group c is first touched at column c
-        out[n++] = Wait{m * d.D + c, (uint32_t)d.G * pp};
-      }
-      return n;
-    }
-    // convolution: k = (r*3 + s)*cin + channel
+    // k = (r*3 + s)*cin + channel
     const int32_t tap = kb / cons.cblocks, cb = kb % cons.cblocks;
     const int32_t r = tap / 3;
     if (pol == POL_ROW) {
@@ -206,6 +221,19 @@ struct DepTracker {
       }
     }
     return n;
+  }
+};
+
+// Either tracker, chosen by the consumer's A operand (used by the host introspection).
+struct DepTracker {
+  GemmDepTracker gemm;
+  ConvDepTracker conv;
+  CUSYNC_HD void reset() {
+    gemm.reset();
+    conv.reset();
+  }
+  CUSYNC_HD int next(const StageGeo& cons, const DepCfg& d, int32_t m, int32_t kb, Wait* out) {
+    return cons.a_mode == AMODE_GEMM ? gemm.next(d, m, kb, out) : conv.next(cons, d, m, kb, out);
   }
 };
 
