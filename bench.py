@@ -2,13 +2,14 @@
 """Benchmark of the tile-synchronised dependent GEMM chain on GB300.
 
 One step = one run of the whole hot path on one batch of synthetic input: the
-chain's tile-counter/semaphore state carried by epoch, the producer GEMM with its
-fused GeLU epilogue publishing tiles, and the consumer GEMM waiting on them -- one
-persistent kernel launch (plus the sentinel fill under the sentinel policy).  The
-headline workload is the GPT-3-shaped MLP slice X[256,12288] . W1[12288,6144] ->
-GeLU -> . W2[6144,12288] (bf16, fp32 accumulation), timed with CUDA events on the
-launching stream for the best tile-synchronisation policy, next to the
-stream-serialised two-kernel chain.
+chain's semaphores counting up by one run, the producer GEMM with its fused GeLU
+epilogue publishing tiles, and the consumer GEMM waiting on them -- one persistent
+kernel launch (plus the sentinel fill under the sentinel policy).  The headline
+workload is the GPT-3-shaped MLP slice X[256,12288] . W1[12288,6144] -> GeLU ->
+. W2[6144,12288] (bf16, fp32 accumulation), timed with CUDA events on the launching
+stream for the best tile-synchronisation policy, next to the stream-serialised
+two-kernel chain.  The timed runs are replayed from CUDA graphs (captured library
+calls) unless --no-graph is given; the end-to-end figure calls the library directly.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead
 (on the host cores, a bounded sample of the same workload per step).
@@ -89,6 +90,8 @@ def parse():
     p.add_argument("--l2-prefetch", type=int, default=0)
     p.add_argument("--cta-pair", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graph", action="store_true", help="one library call per run in the timed loops "
+                   "instead of replaying the runs from CUDA graphs")
     p.add_argument("--sweep-out", default="", help="also time every policy/launch/tile of each workload "
                    "in the comma list --sweep and write the results to this JSON file")
     p.add_argument("--sweep", default="")
@@ -337,14 +340,49 @@ class Setup:
         return n + (1 if policy == "SENTINEL" else 0)
 
 
-def time_runs(torch, setup, ch, n):
+class ChainGraph:
+    """n runs of one chain recorded by CUDA stream capture (groups of up to `group` runs
+    per graph), so that replaying them costs one graph launch per group instead of one
+    library call and two or three kernel launches per run from the host."""
+
+    def __init__(self, torch, setup, ch, n, group=50):
+        self.torch = torch
+        self.graphs = []
+        left = n
+        while left > 0:
+            k = min(group, left)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(k):
+                    setup.run(ch)
+            self.graphs.append(g)
+            left -= k
+        torch.cuda.synchronize()
+
+    def replay(self):
+        for g in self.graphs:
+            g.replay()
+
+
+def run_steps(torch, setup, ch, n, graph):
+    """Enqueue n runs: from a captured graph, or one library call per run."""
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(n):
+            setup.run(ch)
+
+
+def time_runs(torch, setup, ch, n, use_graph=True):
     """Mean ms per run over n back-to-back runs (events on the launching stream)."""
+    graph = ChainGraph(torch, setup, ch, n) if use_graph else None
+    if graph is not None:
+        graph.replay()          # warm the instantiated graphs
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record(s)
-    for _ in range(n):
-        setup.run(ch)
+    run_steps(torch, setup, ch, n, graph)
     e1.record(s)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / n
@@ -440,11 +478,12 @@ def main():
         st, code, detail = ch.check()
         if st != cs.OK:
             raise RuntimeError(f"{pol}: {cs.status_string(st)} 0x{code:08x}")
-        per_policy[pol] = time_runs(torch, setup, ch, min(200, max(5, a.steps)))
+        per_policy[pol] = time_runs(torch, setup, ch, min(200, max(5, a.steps)), not a.no_graph)
     best = min(pols, key=lambda p: per_policy[p])
     ch = setup.chain(best)
 
     # ---- timed region: exactly K steps, barrier + synchronize on both sides
+    graph = None if a.no_graph else ChainGraph(torch, setup, ch, a.steps)
     for _ in range(a.warmup):
         setup.run(ch)
     sampler = ClockSampler(torch.cuda.current_device() if world > 1 else 0)
@@ -457,11 +496,11 @@ def main():
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_host0 = time.time()
     e0.record(s)
-    for _ in range(a.steps):
-        setup.run(ch)
+    run_steps(torch, setup, ch, a.steps, graph)
     e1.record(s)
     torch.cuda.synchronize()
     t_host1 = time.time()
+    del graph
     if world > 1:
         dist.barrier()
     time.sleep(0.3)
@@ -477,7 +516,7 @@ def main():
     ch_stream = setup.chain("STREAM")
     for _ in range(a.warmup):
         setup.run(ch_stream)
-    stream_ms = time_runs(torch, setup, ch_stream, a.steps)
+    stream_ms = time_runs(torch, setup, ch_stream, a.steps, not a.no_graph)
 
     # ---- dominant kernel: the fused chain kernel, per-launch events
     kern_ms = per_launch_ms(torch, setup, ch, min(a.steps, 500))
@@ -539,6 +578,7 @@ def main():
         "config": {"workload": wl.name, **wl.dims, "policy": best, "launch": a.launch,
                    "tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "cta_pair": info.cta_pair,
                    "parallelism": "replicas only",
+                   "enqueue": "library call per run" if a.no_graph else "CUDA-graph replay, 50 captured runs per graph",
                    "l2": f"inputs {alg_bytes / 1e6:.0f} MB of operands > 129 MB L2; no flush between steps"
                    if alg_bytes > 129e6 else "inputs smaller than L2",
                    "vs_baseline_note": "pages' TileSync B=256 chain (840 us) on a V100 in fp16; context only"},
@@ -604,7 +644,7 @@ def sweep(a, torch, cs, synth, out_path):
                             setup.run(ch)
                         st, code, _ = ch.check()
                         n = 50 if wl.gemm_flops() > 1e11 else 200
-                        ms = time_runs(torch, setup, ch, n)
+                        ms = time_runs(torch, setup, ch, n, not a.no_graph)
                         row["us"][key] = ms * 1e3 if st == cs.OK else f"status {st}"
                 for c in list(setup.chains.values()):
                     c.close()

@@ -204,7 +204,11 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
  * intermediate, caller-owned scratch of M*N1 bf16 that holds the producer's output on
  * return) and Y.  Pointers: X [M,K], W1t [N1,K] (SwiGLU: [2*N1,K]), W2t [N2,N1],
  * H [M,N1], Y [M,N2]; device memory, 16-byte aligned, not overlapping H or Y.
- * Asynchronous; INVALID_ARG / UNSUPPORTED / CUDA on launch-time errors. */
+ * Asynchronous; INVALID_ARG / UNSUPPORTED / CUDA on launch-time errors.
+ * Only kernel launches are enqueued on `stream`, so the call can be recorded by CUDA
+ * stream capture; the run count that the semaphores are compared against lives in the
+ * chain's device state, so each replay of a captured run is a new run.  Runs of one
+ * chain must not overlap (one stream, or ordered streams). */
 cusync_status_t cusync_run_mlp(cusync_chain_t chain, const void* X, const void* W1t, const void* W2t, void* H,
                                void* Y, cusync_stream_t stream);
 

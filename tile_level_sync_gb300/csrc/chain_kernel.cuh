@@ -51,7 +51,7 @@
 namespace cusync {
 
 // Control words in front of the semaphore array.
-enum : int { CTRL_ERR = 0, CTRL_ERR_DETAIL = 1, CTRL_COUNTER = 2, CTRL_EXIT = 4, CTRL_WORDS = 16 };
+enum : int { CTRL_ERR = 0, CTRL_ERR_DETAIL = 1, CTRL_COUNTER = 2, CTRL_EXIT = 4, CTRL_RUNS = 6, CTRL_WORDS = 16 };
 // Error classes (bits 31..24 of the error word; bits 23..0 hold the tile index).
 enum : uint32_t { ERRC_FLAG_TIMEOUT = 1, ERRC_SENTINEL_TIMEOUT = 2, ERRC_PIPELINE = 3 };
 // Flag bits shared with cusync.h.
@@ -87,7 +87,6 @@ struct ChainArgs {
   int32_t first_stage;   // stages served by this launch: [first_stage, last_stage]
   int32_t last_stage;
   int32_t tiles0, tiles1;
-  uint32_t epoch;        // run number (semaphores count up across runs)
   uint32_t flags_bits;
   int32_t pdl_role;      // 1: trigger dependents at start; 2: wait on the primary at exit
   int32_t sentinel_check;
@@ -210,8 +209,14 @@ __device__ __forceinline__ void record_error(const ChainArgs& a, uint32_t cls, i
   if (atomicCAS(a.ctrl + CTRL_ERR, 0u, w) == 0u) atomicExch(a.ctrl + CTRL_ERR_DETAIL, (uint32_t)detail);
 }
 
-__device__ __forceinline__ bool has_sentinel_bf16x2(uint32_t x) {
-  return ((x & 0xFFFFu) == 0x8000u) | ((x >> 16) == 0x8000u);
+// Bit 15 (bit 31) of the result is set when the low (high) bf16 half of x is the sentinel
+// 0x8000; the other bits are don't-care.  x ^ 0x80008000 turns a sentinel half into a zero
+// half, and (t - 0x00010001) & ~t has the top bit of a half set exactly when some half is
+// zero (a borrow out of a zero low half can only add a flag when one is already raised).
+// Three integer operations per word, so results can be OR-ed together and tested once.
+__device__ __forceinline__ uint32_t sentinel_bits_bf16x2(uint32_t x) {
+  const uint32_t t = x ^ 0x80008000u;
+  return (t - 0x00010001u) & ~t;
 }
 
 __device__ __forceinline__ uint32_t canon_bf16x2(uint32_t x) {
@@ -282,6 +287,11 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
   const bool to_leader = direct && !leader;
 
   if (args.pdl_role == 1) ptx::pdl_launch_dependents();
+  // Run number of this launch.  Semaphores count up across runs (run r waits for r times
+  // the posts of one run), and the count of finished runs lives in device memory, so the
+  // same launch can be replayed from a CUDA graph.  Read before the first barrier: the
+  // launch that increments it (below) does so only after every CTA has passed that point.
+  uint32_t epoch = 0;
 
   if (warp == 1) {
     if (lane == 0) {
@@ -317,6 +327,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
     }
   }
   if (warp == 0 && lane == 0) {
+    epoch = ptx::ld_relaxed_gpu(args.ctrl + CTRL_RUNS) + 1u;
     for (int s = args.first_stage; s <= args.last_stage; ++s) {
       ptx::prefetch_tmap(&args.st[s].tmA);
       ptx::prefetch_tmap(&args.st[s].tmB);
@@ -407,14 +418,27 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
         const int32_t brow0 = b_row<BN, PAIR>(SA, tr, rank, 0);
         const int32_t brow1 = (PAIR == 1 && SA.g.epi == EPI_SWIGLU) ? b_row<BN, PAIR>(SA, tr, rank, 1) : -1;
         const uint32_t txs = direct ? 2 * tx : tx;
-        // k-blocks at which the consumer may have to wait: only where a k-block starts
-        // reading a producer tile it has not read before (GEMM), every k-block (conv).
+        // k-blocks at which the consumer may have to wait (dep_kblock): every dep_every-th
+        // k-block of a GEMM; for a convolution the first 64 k-blocks by a bit mask, every
+        // later one by dep_every = 1.
         const int32_t pol = args.dep.policy;
         int32_t dep_every = 0;
+        uint64_t dep_mask = 0;
         if (cons && (pol == POL_ROW || pol == POL_TILE || pol == POL_STRIDED)) {
-          if (!gemm) dep_every = 1;
-          else if (pol == POL_ROW) dep_every = KB + 1;
-          else dep_every = max(1, args.dep.prod_n_out / kBK);
+          if (gemm) {
+            dep_every = pol == POL_ROW ? KB + 1 : max(1, args.dep.prod_n_out / kBK);
+          } else {
+            for (int32_t k = 0; k < KB && k < 64; ++k)
+              if (dep_kblock(SA.g, args.dep, k)) dep_mask |= 1ull << k;
+            dep_every = 1;
+          }
+        }
+        // convolution A coordinates of k-block kb, advanced incrementally: channel block,
+        // filter column s and filter row r; image and first image row of the tile
+        int32_t cv_cb = 0, cv_s = 0, cv_r = 0, cv_img = 0, cv_h0 = 0;
+        if (!gemm) {
+          cv_img = tr.m / SA.g.tpi;
+          cv_h0 = (tr.m % SA.g.tpi) * SA.g.th - 1;
         }
         // Arm the stage slot of k-block kbb and issue its weight (B) load.  Blocking waits
         // for the slot to drain; non-blocking returns 0 if it has not drained yet.
@@ -454,7 +478,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
           bool observed = false;
           for (int i = 0; i < n; ++i) {
             const int32_t f = w[i].flag;
-            const uint32_t target = args.epoch * w[i].per_run;
+            const uint32_t target = epoch * w[i].per_run;
             if (target == rc_target && rc_lo <= f && f < rc_hi) continue;
             uint32_t v[kProbe];
             const int32_t cnt = min(kProbe, args.num_flags - f);
@@ -498,28 +522,54 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
             ptx::fence_proxy_async_global();
           }
         };
-        for (int32_t kb = 0; kb < KB; ++kb) {
-          const bool dep_kb = dep_every > 0 && (kb % dep_every) == 0;
-          if (dep_kb && !reorder) wait_deps(kb);
-          if (bnext == kb) {
-            if (arm_b(kb, true) < 0) {
-              record_error(args, ERRC_PIPELINE, t, 2);
-              *abort_flag = 1;
-              ok = false;
-              break;
+        // The GEMM and convolution k-loops are kept apart: the single loader thread's
+        // instruction latency per k-block is on the critical path of the GEMM mainloop.
+        if (gemm) {
+          for (int32_t kb = 0; kb < KB; ++kb) {
+            const bool dep_kb = dep_every > 0 && (kb % dep_every) == 0;
+            if (dep_kb && !reorder) wait_deps(kb);
+            if (bnext == kb) {
+              if (arm_b(kb, true) < 0) {
+                record_error(args, ERRC_PIPELINE, t, 2);
+                *abort_flag = 1;
+                ok = false;
+                break;
+              }
+              ++bnext;
             }
-            ++bnext;
-          }
-          if (dep_kb && reorder) wait_deps(kb);
-          if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
-          const int st = (int)((it + (uint32_t)kb) % S);
-          if (gemm) {
+            if (dep_kb && reorder) wait_deps(kb);
+            if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
+            const int st = (int)((it + (uint32_t)kb) % S);
             if (to_leader) ptx::tma_load_2d_to_leader(smem_a(st), tmA, ptx::mapa(&full[st], 0), kb * kBK, a_row, pol_a);
             else ptx::tma_load_2d(smem_a(st), tmA, &full[st], kb * kBK, a_row, pol_a);
-          } else {
-            issue_a<PAIR>(args, tr, kb, rank, smem_a(st), &full[st], pol_a, to_leader);
+            *progress = it + (uint32_t)kb + 1u;
           }
-          *progress = it + (uint32_t)kb + 1u;
+        } else {
+          for (int32_t kb = 0; kb < KB; ++kb) {
+            const bool dep_kb = kb < 64 ? ((dep_mask >> kb) & 1ull) != 0 : dep_every > 0;
+            if (dep_kb && !reorder) wait_deps(kb);
+            if (bnext == kb) {
+              if (arm_b(kb, true) < 0) {
+                record_error(args, ERRC_PIPELINE, t, 2);
+                *abort_flag = 1;
+                ok = false;
+                break;
+              }
+              ++bnext;
+            }
+            if (dep_kb && reorder) wait_deps(kb);
+            if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
+            const int st = (int)((it + (uint32_t)kb) % S);
+            ptx::tma_load_4d(smem_a(st), tmA, &full[st], cv_cb * kBK, cv_s - 1, cv_h0 + cv_r, cv_img, pol_a);
+            if (++cv_cb == SA.g.cblocks) {
+              cv_cb = 0;
+              if (++cv_s == 3) {
+                cv_s = 0;
+                ++cv_r;
+              }
+            }
+            *progress = it + (uint32_t)kb + 1u;
+          }
         }
         it += (uint32_t)bnext;
         *it_issued = (int32_t)it;
@@ -545,6 +595,11 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
         if (prev == gridDim.x / PAIR - 1) {
           atomicExch(args.ctrl + CTRL_COUNTER + args.queue, 0u);
           atomicExch(args.ctrl + CTRL_EXIT + args.queue, 0u);
+          // Every CTA of the launch that serves the consumer has read the run number by now.
+          if (args.last_stage == 1) {
+            __threadfence();
+            atomicAdd(args.ctrl + CTRL_RUNS, 1u);
+          }
         }
       }
     }
@@ -554,6 +609,9 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
     const uint64_t pol_a = ptx::l2_policy_evict_last();
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(128 * PAIR, BN);
     uint32_t it = 0, tcount = 0, acount = 0, fpar = 0;
+    // Stages of later k-blocks of the current tile that the sentinel check already found
+    // landed and clean (their barrier phase is consumed).
+    uint32_t clean_ahead = 0;
     bool ok = true;
     while (ok) {
       const int slot = tcount % C::kSlots;
@@ -581,28 +639,49 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       const bool check = args.sentinel_check && tr.s == 1;
       const uint32_t abytes = a_tile_bytes(g);
+      // Whether the A tile in stage sx still holds the sentinel anywhere (all lanes).
+      auto stage_has_sentinel = [&](int sx, uint32_t nbytes) -> bool {
+        uint32_t sbits = 0;
+        const uint8_t* base = smem_a(sx);
+        // eight 16-byte loads in flight per lane before any of them is tested
+        for (uint32_t off0 = (uint32_t)lane * 16u; off0 < nbytes; off0 += 8u * 512u) {
+          uint4 v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t off = off0 + (uint32_t)j * 512u;
+            v[j] = off < nbytes ? ptx::ld_shared_v4(base + off) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            sbits |= sentinel_bits_bf16x2(v[j].x) | sentinel_bits_bf16x2(v[j].y) | sentinel_bits_bf16x2(v[j].z) |
+                     sentinel_bits_bf16x2(v[j].w);
+        }
+        return __any_sync(FULL, (sbits & 0x80008000u) != 0u);
+      };
       for (int32_t kb = 0; kb < g.k_blocks; ++kb, ++it) {
         const int st = (int)(it % S);
         if (to_leader) continue;  // this CTA's stages are counted on the leader's barriers
-        if (!ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto)) {
-          ok = false;
-          break;
-        }
-        fpar ^= 1u << st;
-        if (check) {
+        if (!check) {
+          if (!ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto)) {
+            ok = false;
+            break;
+          }
+          fpar ^= 1u << st;
+        } else if ((clean_ahead >> st) & 1u) {
+          clean_ahead &= ~(1u << st);  // landed and checked clean while an earlier stage was reloaded
+        } else {
+          if (!ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto)) {
+            ok = false;
+            break;
+          }
+          fpar ^= 1u << st;
           // Software validity check of this CTA's landed A tile: every bf16 element is
           // compared with the sentinel; while any still holds it, the A load is issued
           // again.
           uint64_t t0 = 0;
+          bool reloaded = false;
           while (true) {
-            bool bad = false;
-            const uint8_t* base = smem_a(st);
-            for (uint32_t off = (uint32_t)lane * 16u; off < abytes; off += 512u) {
-              const uint4 v = ptx::ld_shared_v4(base + off);
-              bad |= has_sentinel_bf16x2(v.x) | has_sentinel_bf16x2(v.y) | has_sentinel_bf16x2(v.z) |
-                     has_sentinel_bf16x2(v.w);
-            }
-            if (!__any_sync(FULL, bad)) break;
+            if (!stage_has_sentinel(st, abytes)) break;
             if (ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u) break;
             const uint64_t now = ptx::globaltimer();
             if (t0 == 0) t0 = now;
@@ -622,8 +701,33 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
               break;
             }
             fpar ^= 1u << st;
+            reloaded = true;
           }
           if (!ok) break;
+          if (reloaded) {
+            // This k-block's data has just become valid.  The A tiles of the following
+            // k-blocks of this tile that landed meanwhile were most likely copied before
+            // their data was written too: check them now and issue the stale ones again
+            // at once, so that their reloads overlap instead of following one another.
+            for (int j = 1; j < S && kb + j < g.k_blocks; ++j) {
+              const int sj = (int)((it + (uint32_t)j) % S);
+              if ((clean_ahead >> sj) & 1u) continue;
+              bool landed = false;
+              if (lane == 0) landed = ptx::mbar_test_wait(&full[sj], (fpar >> sj) & 1u);
+              if (!__shfl_sync(FULL, landed ? 1 : 0, 0)) continue;
+              fpar ^= 1u << sj;
+              if (stage_has_sentinel(sj, abytes)) {
+                if (lane == 0) {
+                  ptx::fence_proxy_async_smem();
+                  ptx::mbar_arrive_expect_tx(&full[sj], abytes);
+                  issue_a<PAIR>(args, tr, kb + j, rank, smem_a(sj), &full[sj], pol_a);
+                }
+              } else {
+                clean_ahead |= 1u << sj;
+              }
+            }
+            __syncwarp();
+          }
         }
         if (kPair && !direct) {
           // both CTAs' shares of this stage are checked before the pair MMA reads them
@@ -686,6 +790,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       const uint32_t issued = (uint32_t)*it_issued;
       for (uint32_t j = it; j < issued && j < it + S; ++j) {
         const int st = (int)(j % S);
+        if ((clean_ahead >> st) & 1u) continue;  // landed, phase already consumed
         ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto);
         fpar ^= 1u << st;
       }

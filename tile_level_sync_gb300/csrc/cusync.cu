@@ -303,7 +303,6 @@ struct cusync_chain {
   int num_sms;
   uint32_t* state;       // CTRL_WORDS control words, then the semaphores
   TraceRec* trace;       // per-tile timeline (CUSYNC_FLAG_TRACE), or null
-  uint32_t epoch;
   Grids grids;
   // TMA descriptors cached by operand pointers
   const void* cached[5];
@@ -468,7 +467,6 @@ cusync_status_t run_chain(cusync_chain* ch, const void* a0, const void* b0, cons
   }
   A.st[0].out = h;
   A.st[1].out = y;
-  A.epoch = ++ch->epoch;
   return launch_run(d, p, A, ch->grids, h, ch->num_sms, stream);
 }
 
@@ -578,7 +576,6 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
     delete ch;
     return cuda_fail(e, "state clear");
   }
-  ch->epoch = 0;
   ch->trace = nullptr;
   if (d->flags & CUSYNC_FLAG_TRACE) {
     const size_t n = (size_t)p.geo[0].m_tiles * p.geo[0].n_tiles + (size_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
@@ -621,7 +618,6 @@ cusync_status_t cusync_chain_reset(cusync_chain_t ch, cusync_stream_t stream) {
   const size_t words = CTRL_WORDS + (size_t)ch->plan.num_flags;
   cudaError_t e = cudaMemsetAsync(ch->state, 0, words * sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "state reset");
-  ch->epoch = 0;
   return CUSYNC_OK;
 }
 
@@ -688,6 +684,7 @@ cusync_status_t cusync_consumer_waits(const cusync_chain_desc_t* d, int32_t m_ti
   dt.reset();
   int32_t n = 0;
   for (int32_t k = 0; k < g.k_blocks; ++k) {
+    if (!dep_kblock(g, p.dep, k)) continue;
     Wait w[kMaxWaits];
     const int c = dt.next(g, p.dep, m_tile, k, w);
     for (int i = 0; i < c; ++i, ++n) {
@@ -846,13 +843,12 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
   fill_static_args(*d, p, scratch, A);
   A.st[0].out = H;
   A.st[1].out = Y;
-  A.epoch = 1;  // the semaphores are cleared below, so every call is run number one
   const int max_clusters = g_noalloc_clusters[dev][p.bn == 256 ? 0 : 1];
   if (p.pair == 2 && max_clusters < 1) return CUSYNC_ERR_UNSUPPORTED;
   const Grids grids = make_grids(p, sms, max_clusters);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // Clear what must start at zero: error word, tile counters, semaphores.
+  // Clear what must start at zero: error word, tile counters, run count, semaphores.
   e = cudaMemsetAsync(scratch, 0, ((size_t)CTRL_WORDS + (size_t)p.num_flags) * sizeof(uint32_t), s);
   if (e != cudaSuccess) return cuda_fail(e, "no-alloc scratch clear");
   if ((st = launch_run(*d, p, A, grids, H, sms, s)) != CUSYNC_OK) return st;

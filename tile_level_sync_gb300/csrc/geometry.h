@@ -224,6 +224,23 @@ struct ConvDepTracker {
   }
 };
 
+// Whether consumer k-block kb can need a semaphore that no earlier k-block of its tile
+// needed; the trackers are consulted only at these k-blocks (on the device and in the
+// host introspection alike).  RowSync waits once, before k-block 0.  A GEMM k-block
+// starts reading a new producer column tile every prod_n_out / kBK k-blocks.  A conv
+// k-block (filter tap r*3+s, channel block cb) reads the producer row tiles of filter
+// row r, which change only when s returns to 0, and producer column tile
+// cb*kBK / prod_n_out, which changes every prod_n_out / kBK channel blocks.
+CUSYNC_HD bool dep_kblock(const StageGeo& cons, const DepCfg& d, int32_t kb) {
+  const int32_t pol = d.policy;
+  if (pol != POL_TILE && pol != POL_ROW && pol != POL_STRIDED) return false;
+  if (pol == POL_ROW) return kb == 0;
+  const int32_t per_col = d.prod_n_out / kBK > 1 ? d.prod_n_out / kBK : 1;
+  if (cons.a_mode == AMODE_GEMM) return kb % per_col == 0;
+  const int32_t tap = kb / cons.cblocks, cb = kb % cons.cblocks;
+  return tap % 3 == 0 && cb % per_col == 0;
+}
+
 // Either tracker, chosen by the consumer's A operand (used by the host introspection).
 struct DepTracker {
   GemmDepTracker gemm;
