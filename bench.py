@@ -40,7 +40,11 @@ PAGES_US_B256 = 840.0
 # DRAM bytes (read + write) per launch of the fused chain kernel from one ncu capture
 # (profiles/chain_kernel_full_<workload>_row.md), valid only for the kernel sources the
 # capture was taken on (sha256 of tile_level_sync_gb300/csrc/*).
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # (workload, policy, launch, tile_n): (dram__bytes_read.sum + dram__bytes_write.sum per
+    # launch of the chain kernel, hash of the kernel sources the capture was taken with)
+    ("gpt3_mlp_m256", "ROW", "persistent", 256): (309942528 + 4713984, "19d876437095d7b3"),
+}
 
 
 def kernel_source_hash():
@@ -95,6 +99,10 @@ def parse():
     p.add_argument("--sweep-out", default="", help="also time every policy/launch/tile of each workload "
                    "in the comma list --sweep and write the results to this JSON file")
     p.add_argument("--sweep", default="")
+    p.add_argument("--trace-out", default="", help="also run STREAM and each listed policy once with the "
+                   "in-kernel per-tile trace and write timeline statistics to this JSON file")
+    p.add_argument("--profile-runs", type=int, default=0, help="only run the first policy of --policies this many "
+                   "times after 3 warm-up runs (for a profiler), then exit without a bench line")
     return p.parse_args()
 
 
@@ -401,6 +409,65 @@ def per_launch_ms(torch, setup, ch, n):
     return statistics.mean(a.elapsed_time(b) for a, b in evs)
 
 
+def trace_stats(torch, setup, policy, launch):
+    """One traced run of `policy`: the per-tile timeline (claim, dependencies met, first
+    and last MMA, epilogue done) reduced to the figures that explain a chain's time.
+
+    * mainloop ns per k-block (median over tiles) and epilogue us, per stage;
+    * consumer wait: dependencies met minus claim, per consumer tile (us);
+    * SM activity: SMs with a tile in flight, sampled every 0.5 us over the run, as a
+      fraction of the SMs the plan uses; and the same fraction inside the last-wave window,
+      from the last tile claim to the end of the run (the tail that wave quantisation
+      leaves idle).
+    """
+    import numpy as np
+    cs = setup.cs
+    d = cs.make_desc(policy=policy, launch=launch, tile_n=setup.tile_n, raster_rows=setup.raster,
+                     l2_prefetch=setup.l2_prefetch, cta_pair=setup.cta_pair, flags=cs.FLAG_TRACE, **setup.base)
+    ch = cs.Chain(d)
+    try:
+        for _ in range(3):
+            setup.run(ch)
+        torch.cuda.synchronize()
+        setup.run(ch)
+        torch.cuda.synchronize()
+        st, code, _ = ch.check()
+        if st != cs.OK:
+            raise RuntimeError(f"traced {policy}: {cs.status_string(st)} 0x{code:08x}")
+        recs = ch.trace()
+        info = ch.info()
+    finally:
+        ch.close()
+    stage = np.array([r["stage"] for r in recs])
+    t0 = min(r["t_claim"] for r in recs)
+    T = {k: (np.array([r[k] for r in recs], dtype=np.float64) - t0) / 1e3
+         for k in ("t_claim", "t_ready", "t_mma0", "t_mma1", "t_epi")}
+    end = float(T["t_epi"].max())
+    sms = int(info.num_sms)
+    ts = np.arange(0.0, end, 0.5)
+    per_sm = {}
+    for r, a, b in zip(recs, T["t_claim"], T["t_epi"]):
+        m = per_sm.setdefault(r["smid"], np.zeros(len(ts), dtype=bool))
+        m |= (ts >= a) & (ts < b)    # an SM is busy while any of its tiles is in flight
+    busy = np.sum(list(per_sm.values()), axis=0).astype(np.float64) if per_sm else np.zeros(len(ts))
+    busy *= info.cta_pair            # a pair tile is recorded by its leader and occupies two SMs
+    tail = ts >= float(T["t_claim"].max())
+    out = {"policy": policy, "launch": "pdl" if launch == cs.LAUNCH_PDL else "persistent", "span_us": end,
+           "tiles": [int((stage == 0).sum()), int((stage == 1).sum())], "sms": sms, "cta_pair": int(info.cta_pair),
+           "sm_active_frac": float(busy.mean() / sms) if len(ts) else None,
+           "last_wave_window_us": float(end - T["t_claim"].max()),
+           "sm_active_frac_last_wave": float(busy[tail].mean() / sms) if tail.any() else None}
+    for s in (0, 1):
+        sel = stage == s
+        kb = info.k_blocks[s]
+        out[f"stage{s}"] = {"ns_per_kblock": float(np.median((T["t_mma1"] - T["t_mma0"])[sel] / kb * 1e3)),
+                            "epilogue_us": float(np.median((T["t_epi"] - T["t_mma1"])[sel]))}
+    w = (T["t_ready"] - T["t_claim"])[stage == 1]
+    out["consumer_wait_us"] = {"median": float(np.median(w)), "p90": float(np.percentile(w, 90)),
+                               "max": float(w.max())}
+    return out
+
+
 def info_tile_n(setup, policy):
     return setup.chain(policy).info().tile_n
 
@@ -464,8 +531,18 @@ def main():
     flops = wl.gemm_flops()
     peaks, peak_src = load_peaks()
 
-    # warm every policy, then choose the fastest tile-synchronised one
     pols = [p.strip().upper() for p in a.policies.split(",") if p.strip()]
+    if a.profile_runs > 0:
+        ch = setup.chain(pols[0])
+        for _ in range(3 + a.profile_runs):
+            setup.run(ch)
+        st, code, _ = ch.check()
+        ch.close()
+        if st != cs.OK:
+            raise RuntimeError(f"{pols[0]}: {cs.status_string(st)} 0x{code:08x}")
+        return 0
+
+    # warm every policy, then choose the fastest tile-synchronised one
     per_policy = {}
     for pol in pols + ["STREAM"]:
         try:
@@ -603,6 +680,13 @@ def main():
         "parity_sampled_rows": parity_ok,
         "cpu_baseline": cpu,
     }
+    if a.trace_out and rank == 0:
+        traces = [trace_stats(torch, setup, "STREAM", cs.LAUNCH_PERSISTENT)]
+        for pol in pols:
+            traces.append(trace_stats(torch, setup, pol, launch))
+        with open(a.trace_out, "w") as f:
+            json.dump({"workload": wl.name, "traces": traces}, f, indent=1)
+        line["trace_file"] = a.trace_out
     if a.sweep_out and rank == 0:
         line["sweep_file"] = a.sweep_out
         sweep(a, torch, cs, synth, a.sweep_out)

@@ -63,6 +63,7 @@ constexpr int kProbe = 32;
 struct StageArgs {
   CUtensorMap tmA;       // activations: 2-D [M, K] or 4-D NHWC image
   CUtensorMap tmB;       // weights [N (or 2*N1), K]
+  CUtensorMap tmO;       // GEMM output [M, N]: 64-column x 32-row store boxes, 128-byte swizzle
   void* out;             // bf16 [M, N] row-major (conv: [pixels, channels])
   const uint16_t* a_ptr; // GEMM activations [a_rows, K] row-major, for L2 prefetch
   const uint16_t* b_ptr; // weights [b_rows, K] row-major, for L2 prefetch
@@ -108,7 +109,10 @@ struct KCfg {
   static constexpr int kTmemCols = 2 * BN;           // two fp32 accumulators of BN columns
   static constexpr int kSlots = 4;                   // tile hand-off ring
   static constexpr int kThreads = 224;              // 7 warps: loader, MMA, 4 epilogue, prefetch
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 1024;
+  // epilogue staging for TMA stores: per epilogue warp two 32-row x 64-column bf16 boxes
+  static constexpr int kEpiBufBytes = 32 * 64 * 2;
+  static constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 1024 + kEpiBytes;
 };
 
 struct TileRef {
@@ -272,6 +276,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   volatile int32_t* it_issued = abort_flag + 1;
   volatile uint32_t* progress = reinterpret_cast<volatile uint32_t*>(it_issued + 1);  // k-blocks issued
+  uint8_t* epi_stage = smem + S * C::kStageBytes + 1024;  // 1024-byte aligned TMA store boxes
 
   auto smem_a = [&](int st) { return stage_base + st * C::kStageBytes; };
   auto smem_b = [&](int st) { return stage_base + st * C::kStageBytes + C::kABytes; };
@@ -280,11 +285,11 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
   const bool leader = rank == 0;
-  // Pair without the sentinel check: the peer's copies complete on the leader's `full`
-  // barriers, which count the bytes of both CTAs.  With the check, each CTA's copies
-  // complete locally, its checker validates them and arrives on the leader's `ready`.
-  const bool direct = kPair && !args.sentinel_check;
-  const bool to_leader = direct && !leader;
+  // A pair tile without the sentinel check is loaded "direct": the peer's copies complete
+  // on the leader's `full` barriers, which count the bytes of both CTAs.  A consumer tile
+  // under the sentinel policy is not: each CTA's copies complete locally, its checker
+  // validates them and arrives on the leader's `ready` barrier.
+  auto direct_tile = [&](const TileRef& tr) { return kPair && !(args.sentinel_check && tr.s == 1); };
 
   if (args.pdl_role == 1) ptx::pdl_launch_dependents();
   // Run number of this launch.  Semaphores count up across runs (run r waits for r times
@@ -331,6 +336,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
     for (int s = args.first_stage; s <= args.last_stage; ++s) {
       ptx::prefetch_tmap(&args.st[s].tmA);
       ptx::prefetch_tmap(&args.st[s].tmB);
+      if (args.st[s].g.a_mode == AMODE_GEMM) ptx::prefetch_tmap(&args.st[s].tmO);
     }
   }
   ptx::tc_fence_before();
@@ -363,7 +369,12 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
         int32_t t;
         bool done;
         if (leader) {
-          t = (int32_t)atomicAdd(args.ctrl + CTRL_COUNTER + args.queue, 1u);
+          // The first tile of each CTA (pair) is its own index, so the first wave is placed
+          // on SMs the way the block scheduler places a plain grid; later tiles come from
+          // the launch's counter, offset by the number of CTAs (pairs).
+          const int32_t nctas = (int32_t)(gridDim.x / PAIR);
+          t = tcount == 0 ? (int32_t)(blockIdx.x / PAIR)
+                          : nctas + (int32_t)atomicAdd(args.ctrl + CTRL_COUNTER + args.queue, 1u);
           done = t >= total || !ok || *abort_flag;
           if (!xwait<PAIR>(&qempty[slot], tpar ^ 1u, pto)) {
             record_error(args, ERRC_PIPELINE, 0xFFFFFF, 1);
@@ -417,6 +428,8 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
         const int32_t a_row = tr.m * (128 * PAIR) + (int32_t)rank * 128;
         const int32_t brow0 = b_row<BN, PAIR>(SA, tr, rank, 0);
         const int32_t brow1 = (PAIR == 1 && SA.g.epi == EPI_SWIGLU) ? b_row<BN, PAIR>(SA, tr, rank, 1) : -1;
+        const bool direct = direct_tile(tr);
+        const bool to_leader = direct && !leader;
         const uint32_t txs = direct ? 2 * tx : tx;
         // k-blocks at which the consumer may have to wait (dep_kblock): every dep_every-th
         // k-block of a GEMM; for a convolution the first 64 k-blocks by a bit mask, every
@@ -502,7 +515,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
                 ++bnext;
               } else {
                 __nanosleep(backoff);
-                if (backoff < 1024) backoff <<= 1;
+                if (backoff < 256) backoff <<= 1;
               }
               if ((int32_t)(ptx::ld_relaxed_gpu(args.flags + f) - target) >= 0) break;
               if ((++iter & 15u) == 0) {
@@ -612,6 +625,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
     // Stages of later k-blocks of the current tile that the sentinel check already found
     // landed and clean (their barrier phase is consumed).
     uint32_t clean_ahead = 0;
+    uint32_t rpar = 0;  // leader: parity of each stage's next `ready` phase
     bool ok = true;
     while (ok) {
       const int slot = tcount % C::kSlots;
@@ -638,6 +652,8 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       }
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
       const bool check = args.sentinel_check && tr.s == 1;
+      const bool direct = direct_tile(tr);
+      const bool to_leader = direct && !leader;
       const uint32_t abytes = a_tile_bytes(g);
       // Whether the A tile in stage sx still holds the sentinel anywhere (all lanes).
       auto stage_has_sentinel = [&](int sx, uint32_t nbytes) -> bool {
@@ -735,7 +751,8 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
           if (lane == 0) {
             if (leader) {
               ptx::mbar_arrive(&ready[st]);
-              rok = ptx::mbar_wait_bounded_cluster(&ready[st], (it / S) & 1u, pto);
+              rok = ptx::mbar_wait_bounded_cluster(&ready[st], (rpar >> st) & 1u, pto);
+              rpar ^= 1u << st;
             } else {
               ptx::mbar_arrive_cluster(ptx::mapa(&ready[st], 0));
             }
@@ -887,6 +904,12 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       const int32_t col0 = tr.c * g.n_out;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const int nchunks = g.n_out / 32;
+      // GEMM outputs leave through TMA stores of 32-row x 64-column boxes staged in this
+      // warp's two shared-memory buffers; convolution outputs (a tile's pixels are not a
+      // box of the output tensor) through 16-byte stores from registers.
+      const bool tma_out = g.a_mode == AMODE_GEMM;
+      uint8_t* ebuf = epi_stage + (q * 2) * C::kEpiBufBytes;
+      const int32_t row_w0 = tr.m * (128 * PAIR) + (int32_t)rank * 128 + q * 32;
       for (int j = 0; j < nchunks; ++j) {
         uint32_t v[32];
         float f[32];
@@ -914,13 +937,47 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
         uint32_t p[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) p[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-        if (valid) {
+        if (tma_out) {
+          // Two 32-column chunks fill one 64-column box; each lane writes its row (128
+          // bytes) with the 16-byte units permuted as the 128-byte swizzle expects, which
+          // also spreads a warp's stores over all banks.
+          const int box = j >> 1;
+          uint8_t* buf = ebuf + (box & 1) * C::kEpiBufBytes;
+          if ((j & 1) == 0 && box >= 2) {
+            if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last read `buf`
+            __syncwarp();
+          }
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const int u = (j & 1) * 4 + ch;
+            ptx::st_shared_v4(buf + lane * 128 + ((u ^ (lane & 7)) << 4), p[4 * ch], p[4 * ch + 1], p[4 * ch + 2],
+                              p[4 * ch + 3]);
+          }
+          if ((j & 1) == 1 || j == nchunks - 1) {
+            ptx::fence_proxy_async_smem();  // this thread's writes before the async-proxy read
+            __syncwarp();
+            // boxes that start past the tensor's last row or column hold nothing to store
+            if (lane == 0 && row_w0 < g.M && col0 + box * 64 < g.N) {
+              ptx::tma_store_2d(&SA.tmO, buf, col0 + box * 64, row_w0);
+              ptx::bulk_commit_group();
+            }
+          }
+        } else if (valid) {
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             const int32_t col = col0 + j * 32 + ch * 8;
             if (col < g.N) ptx::st_relaxed_gpu_b128(orow + col, p[4 * ch], p[4 * ch + 1], p[4 * ch + 2], p[4 * ch + 3]);
           }
         }
+      }
+      if (tma_out) {
+        // The tile's stores have completed (not only read their source) before this warp
+        // reports them done: the semaphore post below may follow right after.
+        if (lane == 0) {
+          ptx::bulk_wait_group_all();
+          ptx::fence_proxy_async_global();
+        }
+        __syncwarp();
       }
       // Arrive on epi_done before releasing the accumulator: a thread can reach this
       // accumulator's next tile only after every thread released it, so each phase of

@@ -399,7 +399,7 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
 
 // TMA descriptors of a run: 2-D maps for GEMM operands, 4-D NHWC maps for conv images.
 bool encode_maps(const cusync_chain_desc_t& d, const Plan& p, ChainArgs& A, const void* a0, const void* b0,
-                 const void* b1, const void* h) {
+                 const void* b1, const void* h, const void* y) {
   bool ok = true;
   if (d.kind == CUSYNC_CHAIN_CONV_RELU) {
     const StageGeo& g0 = p.geo[0];
@@ -421,6 +421,8 @@ bool encode_maps(const cusync_chain_desc_t& d, const Plan& p, ChainArgs& A, cons
     ok &= encode_2d(&A.st[0].tmB, b0, (uint64_t)(swiglu ? 2 * d.N1 : d.N1), (uint64_t)d.K, b_box_rows(p, swiglu));
     ok &= encode_2d(&A.st[1].tmA, h, (uint64_t)d.M, (uint64_t)d.N1, 128u);
     ok &= encode_2d(&A.st[1].tmB, b1, (uint64_t)d.N2, (uint64_t)d.N1, b_box_rows(p, false));
+    ok &= encode_2d(&A.st[0].tmO, h, (uint64_t)d.M, (uint64_t)d.N1, 32u);
+    ok &= encode_2d(&A.st[1].tmO, y, (uint64_t)d.M, (uint64_t)d.N2, 32u);
   }
   return ok;
 }
@@ -458,7 +460,7 @@ cusync_status_t run_chain(cusync_chain* ch, const void* a0, const void* b0, cons
   ChainArgs& A = ch->args;
   const void* ptrs[5] = {a0, b0, b1, h, y};
   if (!ch->maps_valid || std::memcmp(ptrs, ch->cached, sizeof(ptrs)) != 0) {
-    if (!encode_maps(d, p, A, a0, b0, b1, h)) {
+    if (!encode_maps(d, p, A, a0, b0, b1, h, y)) {
       ch->maps_valid = false;
       return CUSYNC_ERR_INVALID_ARG;
     }
@@ -839,7 +841,7 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
 
   ChainArgs A;
   std::memset(&A, 0, sizeof(A));
-  if (!encode_maps(*d, p, A, X, W1t, W2t, H)) return CUSYNC_ERR_INVALID_ARG;
+  if (!encode_maps(*d, p, A, X, W1t, W2t, H, Y)) return CUSYNC_ERR_INVALID_ARG;
   fill_static_args(*d, p, scratch, A);
   A.st[0].out = H;
   A.st[1].out = Y;
