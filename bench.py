@@ -730,6 +730,10 @@ def sweep(a, torch, cs, synth, out_path):
                         n = 50 if wl.gemm_flops() > 1e11 else 200
                         ms = time_runs(torch, setup, ch, n, not a.no_graph)
                         row["us"][key] = ms * 1e3 if st == cs.OK else f"status {st}"
+                        pk = f"r{raster}/p{pair}"
+                        if pk not in row.setdefault("predicted_us", {}):
+                            pred = cs.cusync_predict_policies(ch.desc)
+                            row["predicted_us"][pk] = {n_: pred.us[i] for n_, i in cs.POLICY_NAMES.items() if i < 5}
                 for c in list(setup.chains.values()):
                     c.close()
                 setup.chains = {}

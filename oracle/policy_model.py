@@ -1,0 +1,170 @@
+"""Latency model of one chain run under each synchronisation policy (oracle; test
+infrastructure only).
+
+[ALCOP] "ALCOP: Automatic Load-COmpute Pipelining in Deep Learning Compiler for
+AI-GPUs", analytical model (Table I): the thread blocks of a kernel run in
+threadblock batches that occupy all SMs, so a kernel takes (number of batches) x
+(threadblock latency), and a threadblock's latency is the sum of an initial phase
+(T_init, the first data requested and awaited), a steady main loop (T_main_loop) and
+an epilogue (T_epilogue).
+
+[cuSync] "A Framework for Fine-Grained Synchronization of Dependent GPU Kernels",
+§III: with stream synchronisation the consumer kernel starts after the producer
+kernel's last wave; with tile synchronisation consumer thread blocks share the waves of
+the producer and each consumer tile only waits (§IV-E) for the producer tiles its policy
+names.
+
+The model written out here, step by step:
+
+* a tile of stage s costs T_init (start_ns) when it is its CTA's first tile, then
+  k_blocks(s) x kblock_ns[s] of main loop, then epilogue_ns[s]; a persistent CTA starts
+  its next tile's main loop when the previous one ends, and a tile's epilogue starts
+  after both its main loop and the CTA's previous epilogue have finished;
+* the queue holds the producer tiles (row-major; StridedSync visits each group's
+  columns one after another) before the consumer tiles (row-major); CTA q takes tile q
+  first, and every later tile goes to the CTA whose main loop frees up first (the lowest
+  index on a tie);
+* a producer tile's post is seen post_ns after its epilogue; before consumer k-block kb
+  the tile waits for the producer tiles its policy waits for there (``deps.wait_sets``);
+  if they are posted later than the k-block could start, the k-block starts start_ns
+  after the last post (the copy pipeline refills); a k-block that waited on anything
+  costs wait_kblock_ns more (TileSync, StridedSync, RowSync's first k-block);
+* the sentinel policy waits on exactly the producer tiles each k-block reads (the
+  TileSync sets), costs sentinel_kblock_ns per consumer k-block and starts after the
+  intermediate is filled (fill_ns_per_mb per MB);
+* stream order runs the producer tiles as one launch, then, gap_ns after its last
+  epilogue, the consumer tiles as a second launch with no waits.
+"""
+
+from dataclasses import dataclass
+
+from oracle import deps
+
+
+@dataclass
+class Model:
+    kblock_ns: tuple
+    wait_kblock_ns: float
+    sentinel_kblock_ns: float
+    start_ns: float
+    epilogue_ns: tuple
+    post_ns: float
+    gap_ns: float
+    fill_ns_per_mb: float
+
+
+@dataclass
+class Chain:
+    """A chain's tiles: producer tiles (m, c) in queue order with k_blocks[0] each, consumer
+    row tiles (m) in queue order with k_blocks[1] each, and the dependency geometry."""
+    prod_tiles: list      # [(m, c)] in queue order
+    cons_rows: list       # [m] in queue order
+    k_blocks: tuple
+    dep_chain: object     # deps.GemmChain / deps.ConvChain
+    G: int = 1
+    h_mb: float = 0.0
+
+
+def play(tiles, slots, t0, model, cost):
+    """Run `tiles` (each passed to cost(tile, t_start) -> main-loop end) on `slots` CTAs
+    from time t0.  Returns [(tile, main_end, done)] in queue order."""
+    ctas = [{"free": t0, "last_done": t0, "used": False} for _ in range(max(1, min(slots, len(tiles))))]
+    out = []
+    for q, tile in enumerate(tiles):
+        if q < len(ctas):
+            k = q
+        else:
+            k = min(range(len(ctas)), key=lambda i: (ctas[i]["free"], i))
+        c = ctas[k]
+        start = c["free"] if c["used"] else c["free"] + model.start_ns
+        c["used"] = True
+        main_end = cost(tile, start)
+        done = max(main_end, c["last_done"]) + model.epilogue_ns[tile[0]]
+        c["free"] = main_end
+        c["last_done"] = done
+        out.append((tile, main_end, done))
+    return out
+
+
+def predict_stream(chain, slots0, slots1, model):
+    """Stream order: two launches, the second gap_ns after the first's last epilogue."""
+    kb0, kb1 = chain.k_blocks
+    r0 = play([(0, t) for t in chain.prod_tiles], slots0, 0.0, model,
+              lambda tile, s: s + kb0 * model.kblock_ns[0])
+    end0 = max(d for _, _, d in r0) if r0 else 0.0
+    r1 = play([(1, m) for m in chain.cons_rows], slots1, end0 + model.gap_ns, model,
+              lambda tile, s: s + kb1 * model.kblock_ns[1])
+    return max(d for _, _, d in r1) if r1 else end0 + model.gap_ns
+
+
+def predict_fused(chain, policy, slots, model):
+    """One persistent launch: producer tiles, then consumer tiles that wait per policy."""
+    kb0, kb1 = chain.k_blocks
+    sentinel = policy == "SENTINEL"
+    wait_policy = "TILE" if sentinel else policy
+    posted = {}
+    wait_cache = {}
+
+    def cost(tile, start):
+        stage, what = tile
+        if stage == 0:
+            return start + kb0 * model.kblock_ns[0]
+        m = what
+        if m not in wait_cache:
+            wait_cache[m] = deps.wait_sets(chain.dep_chain, wait_policy, m, chain.G)
+        t = start
+        for kb in range(kb1):
+            need = wait_cache[m][kb]
+            if need:
+                ready = max(posted[p] for p in need)
+                if ready > t:
+                    t = ready + model.start_ns
+            if sentinel:
+                t += model.sentinel_kblock_ns
+            else:
+                t += model.kblock_ns[1] + (model.wait_kblock_ns if need else 0.0)
+        return t
+
+    tiles = [(0, t) for t in chain.prod_tiles] + [(1, m) for m in chain.cons_rows]
+    t0 = chain.h_mb * model.fill_ns_per_mb if sentinel else 0.0
+    # the tiles are taken in queue order, so every producer tile's post time is known
+    # before the first consumer tile asks for it
+    ctas = [{"free": t0, "last_done": t0, "used": False} for _ in range(max(1, min(slots, len(tiles))))]
+    end = t0
+    for q, tile in enumerate(tiles):
+        k = q if q < len(ctas) else min(range(len(ctas)), key=lambda i: (ctas[i]["free"], i))
+        c = ctas[k]
+        start = c["free"] if c["used"] else c["free"] + model.start_ns
+        c["used"] = True
+        main_end = cost(tile, start)
+        done = max(main_end, c["last_done"]) + model.epilogue_ns[tile[0]]
+        c["free"] = main_end
+        c["last_done"] = done
+        end = max(end, done)
+        if tile[0] == 0:
+            posted[tile[1]] = done + model.post_ns
+    return end
+
+
+def gemm_chain(M, N1, N2, tile_n, n_out, pair, policy, G=2):
+    """Queue order of an MLP chain's tiles ([cuSync] §IV-C row-major; StridedSync's
+    producer order) and its dependency geometry."""
+    bm = 128 * pair
+    mt = -(-M // bm)
+    nt0 = -(-N1 // n_out)
+    nt1 = -(-N2 // tile_n)
+    order = deps.strided_producer_order(nt0, G) if policy == "STRIDED" else list(range(nt0))
+    prod = [(m, order[y]) for m in range(mt) for y in range(nt0)]
+    cons = [m for m in range(mt) for _ in range(nt1)]
+    return prod, cons, deps.GemmChain(M=M, N1=N1, BM=bm, BNo=n_out, BK=64)
+
+
+def conv_chain(n, h, w, c, k, tile_n, th):
+    """Queue order of a conv chain's tiles (row tiles of th image rows; row-major) and its
+    halo-aware dependency geometry; th is the tiling's rows per tile."""
+    tpi = -(-h // th)
+    mt = n * tpi
+    nt = -(-k // tile_n)
+    prod = [(m, y) for m in range(mt) for y in range(nt)]
+    cons = [m for m in range(mt) for _ in range(nt)]
+    return prod, cons, deps.ConvChain(N=n, P=h, Q=w, C=k, TH=th, BNo=tile_n, BK=64)

@@ -192,3 +192,18 @@ def test_tile_order_and_prefetch_do_not_change_results():
                 assert_within_tol(f64(Y), Y_ref, "Y")
                 ref = b
             assert np.array_equal(b[0], ref[0]) and np.array_equal(b[1], ref[1]), (pol, raster, pf)
+
+
+def test_auto_policy_runs_the_predicted_policy():
+    """CUSYNC_POLICY_AUTO creates the chain with the policy the latency model predicts
+    fastest; its output is byte-identical to that policy's."""
+    (X, W1, W2), (H_ref, Y_ref) = _mlp_case(520, 512, 1536, 512, seed=7)
+    ops = device_mlp_operands(X, W1, W2)
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "AUTO", M=520, K=512, N1=1536, N2=512)
+    chosen = cs.cusync_plan_info(d).policy
+    assert chosen == cs.cusync_predict_policies(d).best
+    H, Y, _ = run_mlp(d, *ops, runs=2)
+    assert_within_tol(f64(Y), Y_ref, "Y auto")
+    d2 = cs.make_desc(cs.CHAIN_MLP_GELU, chosen, M=520, K=512, N1=1536, N2=512)
+    H2, Y2, _ = run_mlp(d2, *ops, runs=1)
+    assert np.array_equal(bits(Y), bits(Y2)) and np.array_equal(bits(H), bits(H2))

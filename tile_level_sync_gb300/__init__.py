@@ -16,7 +16,7 @@ from . import _build
 c_i32, c_i64, c_u32, c_u64, c_dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_double
 
 # ---------------------------------------------------------------- enums (cusync.h)
-POLICY_STREAM, POLICY_ROW, POLICY_TILE, POLICY_STRIDED_TILE, POLICY_SENTINEL = range(5)
+POLICY_STREAM, POLICY_ROW, POLICY_TILE, POLICY_STRIDED_TILE, POLICY_SENTINEL, POLICY_AUTO = range(6)
 CHAIN_MLP_GELU, CHAIN_MLP_SWIGLU, CHAIN_CONV_RELU = range(3)
 LAUNCH_PERSISTENT, LAUNCH_PDL = range(2)
 (OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NOMEM, ERR_TIMEOUT, ERR_DEVICE) = range(7)
@@ -26,7 +26,7 @@ DEBUG_SKIP_POST = 1 << 8
 DEBUG_SKIP_INIT = 1 << 9
 
 POLICY_NAMES = {"STREAM": POLICY_STREAM, "ROW": POLICY_ROW, "TILE": POLICY_TILE,
-                "STRIDED": POLICY_STRIDED_TILE, "SENTINEL": POLICY_SENTINEL}
+                "STRIDED": POLICY_STRIDED_TILE, "SENTINEL": POLICY_SENTINEL, "AUTO": POLICY_AUTO}
 
 
 class cusync_chain_desc_t(ctypes.Structure):
@@ -60,7 +60,18 @@ class cusync_chain_info_t(ctypes.Structure):
         ("tile_m", c_i32), ("tile_n", c_i32), ("tile_k", c_i32),
         ("strided_group", c_i32), ("strided_distance", c_i32), ("num_flags", c_i32),
         ("grid", c_i32 * 2), ("num_sms", c_i32), ("conv_rows_per_tile", c_i32), ("cta_pair", c_i32),
+        ("policy", c_i32),
     ]
+
+
+class cusync_latency_model_t(ctypes.Structure):
+    _fields_ = [("kblock_ns", c_dbl * 2), ("wait_kblock_ns", c_dbl), ("sentinel_kblock_ns", c_dbl),
+                ("start_ns", c_dbl), ("epilogue_ns", c_dbl * 2), ("post_ns", c_dbl), ("gap_ns", c_dbl),
+                ("fill_ns_per_mb", c_dbl)]
+
+
+class cusync_policy_prediction_t(ctypes.Structure):
+    _fields_ = [("us", c_dbl * 5), ("best_sync", c_i32), ("best", c_i32), ("num_sms", c_i32)]
 
 
 _VP = ctypes.c_void_p
@@ -83,6 +94,10 @@ _SIGNATURES = {
     "cusync_run_mlp_noalloc": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), _VP, _VP, _VP, _VP, _VP, _VP,
                                        ctypes.POINTER(c_u32)]),
     "cusync_chain_trace": (c_i32, [_VP, _VP, ctypes.POINTER(cusync_trace_rec_t), c_i32, ctypes.POINTER(c_i32)]),
+    "cusync_default_latency_model": (c_i32, [ctypes.POINTER(cusync_chain_desc_t),
+                                             ctypes.POINTER(cusync_latency_model_t)]),
+    "cusync_predict_policies": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), ctypes.POINTER(cusync_latency_model_t),
+                                        ctypes.POINTER(cusync_policy_prediction_t)]),
     "cusync_destroy_chain": (c_i32, [_VP]),
 }
 
@@ -173,6 +188,21 @@ def cusync_plan_waves(desc):
 def cusync_plan_info(desc):
     r = cusync_chain_info_t()
     _check(load().cusync_plan_info(ctypes.byref(desc), ctypes.byref(r)), "cusync_plan_info")
+    return r
+
+
+def cusync_default_latency_model(desc):
+    r = cusync_latency_model_t()
+    _check(load().cusync_default_latency_model(ctypes.byref(desc), ctypes.byref(r)), "cusync_default_latency_model")
+    return r
+
+
+def cusync_predict_policies(desc, model=None):
+    """Predicted microseconds per policy (indexed by POLICY_*; -1 where a policy does not
+    apply), plus the fastest tile-synchronised policy and the fastest overall."""
+    r = cusync_policy_prediction_t()
+    m = ctypes.byref(model) if model is not None else None
+    _check(load().cusync_predict_policies(ctypes.byref(desc), m, ctypes.byref(r)), "cusync_predict_policies")
     return r
 
 

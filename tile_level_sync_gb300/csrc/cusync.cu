@@ -19,6 +19,7 @@
 #include "../../include/cusync.h"
 #include "chain_kernel.cuh"
 #include "geometry.h"
+#include "policy_model.h"
 
 using namespace cusync;
 
@@ -74,8 +75,15 @@ int32_t default_tile_n(const cusync_chain_desc_t& d) {
   return 256;
 }
 
+cusync_status_t resolve_auto(const cusync_chain_desc_t& d, cusync_chain_desc_t* out);
+
 cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   if (d.kind < CUSYNC_CHAIN_MLP_GELU || d.kind > CUSYNC_CHAIN_CONV_RELU) return CUSYNC_ERR_INVALID_ARG;
+  if (d.policy == CUSYNC_POLICY_AUTO) {
+    cusync_chain_desc_t r;
+    cusync_status_t st = resolve_auto(d, &r);
+    return st != CUSYNC_OK ? st : make_plan(r, p);
+  }
   if (d.policy < CUSYNC_POLICY_STREAM || d.policy > CUSYNC_POLICY_SENTINEL) return CUSYNC_ERR_INVALID_ARG;
   if (d.launch != CUSYNC_LAUNCH_PERSISTENT && d.launch != CUSYNC_LAUNCH_PDL) return CUSYNC_ERR_INVALID_ARG;
   const int32_t bn = default_tile_n(d);
@@ -287,6 +295,89 @@ Grids make_grids(const Plan& p, int sms, int max_clusters) {
     g.cons = (int32_t)std::min<int64_t>(sms, t1);
   }
   return g;
+}
+
+// ----------------------------------------------------------------------------- latency model
+
+// GB300 constants of the latency model for plan p, from the in-kernel trace of the bench
+// workloads: mainloop ns per k-block (single CTAs 345-375, CTA pairs 390-420 per pair
+// k-block, convolutions 355-400, consumers slightly slower than producers), the sentinel
+// check's k-block (about 1.0 us, 1.5 us with pairs), a tile's first copy about 1 us,
+// the post seen by a consumer about 1.5 us after the stores, 2 us between stream-ordered
+// kernels, and epilogue time per output column by activation (tanh-GeLU 22 ns, SwiGLU
+// 26 ns, ReLU 22 ns, none 17 ns for a 128-row tile).
+LatencyModel default_model(const Plan& p) {
+  LatencyModel m;
+  const bool conv = p.geo[0].a_mode == AMODE_CONV;
+  if (conv) {
+    m.kblock_ns[0] = 365.0;
+    m.kblock_ns[1] = 360.0;
+    m.sentinel_kblock_ns = 990.0;
+  } else if (p.pair == 2) {
+    m.kblock_ns[0] = 395.0;
+    m.kblock_ns[1] = 415.0;
+    m.sentinel_kblock_ns = 1480.0;
+  } else {
+    m.kblock_ns[0] = p.bn == 128 ? 355.0 : 350.0;
+    m.kblock_ns[1] = p.bn == 128 ? 365.0 : 370.0;
+    m.sentinel_kblock_ns = 1000.0;
+  }
+  m.wait_kblock_ns = 150.0;
+  m.start_ns = 1000.0;
+  for (int s = 0; s < 2; ++s) {
+    double per_col = 17.0;
+    switch (p.geo[s].epi) {
+      case EPI_GELU: per_col = 22.0; break;
+      case EPI_SWIGLU: per_col = 26.0; break;
+      case EPI_RELU: per_col = 22.0; break;
+      default: break;
+    }
+    m.epilogue_ns[s] = per_col * p.geo[s].n_out;
+  }
+  m.post_ns = 1500.0;
+  m.gap_ns = 2000.0;
+  m.fill_ns_per_mb = 350.0;
+  return m;
+}
+
+// Predicted us of one run under each policy (-1 where the plan is refused).
+void predict_all(const cusync_chain_desc_t& d, const cusync_latency_model_t* model, int sms, double us[5]) {
+  for (int pol = CUSYNC_POLICY_STREAM; pol <= CUSYNC_POLICY_SENTINEL; ++pol) {
+    cusync_chain_desc_t c = d;
+    c.policy = (cusync_policy_t)pol;
+    Plan q;
+    if (make_plan(c, &q) != CUSYNC_OK) {
+      us[pol] = -1.0;
+      continue;
+    }
+    LatencyModel lm;
+    if (model) std::memcpy(&lm, model, sizeof(lm));
+    else lm = default_model(q);
+    const Grids g = make_grids(q, sms, 0);
+    ModelChain mc;
+    mc.geo[0] = q.geo[0];
+    mc.geo[1] = q.geo[1];
+    mc.dep = q.dep;
+    mc.slots_fused = g.fused / q.pair;
+    mc.slots[0] = g.prod / q.pair;
+    mc.slots[1] = g.cons / q.pair;
+    mc.h_mb = (double)q.geo[0].M * (double)q.geo[0].N * 2.0 / 1e6;
+    us[pol] = predict_chain_ns(mc, lm) / 1000.0;
+  }
+}
+
+cusync_status_t resolve_auto(const cusync_chain_desc_t& d, cusync_chain_desc_t* out) {
+  int sms = 0;
+  if (query_num_sms(d.num_sms, &sms) != 0) return CUSYNC_ERR_CUDA;
+  double us[5];
+  predict_all(d, nullptr, sms, us);
+  int best = -1;
+  for (int pol = CUSYNC_POLICY_STREAM; pol <= CUSYNC_POLICY_SENTINEL; ++pol)
+    if (us[pol] >= 0.0 && (best < 0 || us[pol] < us[best])) best = pol;
+  if (best < 0) return CUSYNC_ERR_UNSUPPORTED;
+  *out = d;
+  out->policy = (cusync_policy_t)best;
+  return CUSYNC_OK;
 }
 
 // B box rows per CTA: BN (single), BN/2 (pair, or either SwiGLU half).
@@ -564,6 +655,7 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
   cusync_chain* ch = new (std::nothrow) cusync_chain();
   if (!ch) return CUSYNC_ERR_NOMEM;
   ch->d = *d;
+  ch->d.policy = (cusync_policy_t)p.dep.policy;  // CUSYNC_POLICY_AUTO resolved
   if (ch->d.timeout_ns == 0) ch->d.timeout_ns = kDefaultTimeoutNs;
   ch->plan = p;
   ch->device = dev;
@@ -664,13 +756,46 @@ cusync_status_t cusync_plan_info(const cusync_chain_desc_t* d, cusync_chain_info
   out->strided_distance = p.dep.D;
   out->num_flags = (int32_t)p.num_flags;
   const Grids g = make_grids(p, sms, 0);
-  const bool two = d->policy == CUSYNC_POLICY_STREAM || d->launch == CUSYNC_LAUNCH_PDL;
+  const bool two = p.dep.policy == POL_STREAM || d->launch == CUSYNC_LAUNCH_PDL;
   out->grid[0] = two ? g.prod : g.fused;
   out->grid[1] = two ? g.cons : 0;
   out->cta_pair = p.pair;
   out->num_sms = sms;
   out->conv_rows_per_tile = d->kind == CUSYNC_CHAIN_CONV_RELU ? p.geo[0].th : 0;
+  out->policy = p.dep.policy;
   return CUSYNC_OK;
+}
+
+cusync_status_t cusync_default_latency_model(const cusync_chain_desc_t* d, cusync_latency_model_t* out) {
+  if (!d || !out) return CUSYNC_ERR_INVALID_ARG;
+  cusync_chain_desc_t c = *d;
+  if (c.policy == CUSYNC_POLICY_AUTO) c.policy = CUSYNC_POLICY_STREAM;  // the constants do not depend on it
+  Plan p;
+  cusync_status_t st = make_plan(c, &p);
+  if (st != CUSYNC_OK) return st;
+  const LatencyModel m = default_model(p);
+  static_assert(sizeof(LatencyModel) == sizeof(cusync_latency_model_t), "latency model layout");
+  std::memcpy(out, &m, sizeof(m));
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_predict_policies(const cusync_chain_desc_t* d, const cusync_latency_model_t* model,
+                                        cusync_policy_prediction_t* out) {
+  if (!d || !out) return CUSYNC_ERR_INVALID_ARG;
+  int sms = 0;
+  if (query_num_sms(d->num_sms, &sms) != 0) return CUSYNC_ERR_CUDA;
+  std::memset(out, 0, sizeof(*out));
+  predict_all(*d, model, sms, out->us);
+  out->best = -1;
+  out->best_sync = -1;
+  for (int pol = CUSYNC_POLICY_STREAM; pol <= CUSYNC_POLICY_SENTINEL; ++pol) {
+    if (out->us[pol] < 0.0) continue;
+    if (out->best < 0 || out->us[pol] < out->us[out->best]) out->best = pol;
+    if (pol != CUSYNC_POLICY_STREAM && (out->best_sync < 0 || out->us[pol] < out->us[out->best_sync]))
+      out->best_sync = pol;
+  }
+  out->num_sms = sms;
+  return out->best < 0 ? CUSYNC_ERR_UNSUPPORTED : CUSYNC_OK;
 }
 
 cusync_status_t cusync_consumer_waits(const cusync_chain_desc_t* d, int32_t m_tile, int32_t* kb, int32_t* flag,
@@ -817,6 +942,8 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
   Plan p;
   cusync_status_t st = make_plan(*d, &p);
   if (st != CUSYNC_OK) return st;
+  cusync_chain_desc_t dd = *d;
+  dd.policy = (cusync_policy_t)p.dep.policy;  // CUSYNC_POLICY_AUTO resolved
   // The fixed array bounds the number of semaphores this entry point can use.
   if ((int64_t)CTRL_WORDS + p.num_flags > kNoAllocWords) {
     CUSYNC_LOG("no-alloc run needs %lld semaphores; the fixed scratch holds %d", (long long)p.num_flags,
@@ -841,8 +968,8 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
 
   ChainArgs A;
   std::memset(&A, 0, sizeof(A));
-  if (!encode_maps(*d, p, A, X, W1t, W2t, H, Y)) return CUSYNC_ERR_INVALID_ARG;
-  fill_static_args(*d, p, scratch, A);
+  if (!encode_maps(dd, p, A, X, W1t, W2t, H, Y)) return CUSYNC_ERR_INVALID_ARG;
+  fill_static_args(dd, p, scratch, A);
   A.st[0].out = H;
   A.st[1].out = Y;
   const int max_clusters = g_noalloc_clusters[dev][p.bn == 256 ? 0 : 1];
@@ -853,7 +980,7 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
   // Clear what must start at zero: error word, tile counters, run count, semaphores.
   e = cudaMemsetAsync(scratch, 0, ((size_t)CTRL_WORDS + (size_t)p.num_flags) * sizeof(uint32_t), s);
   if (e != cudaSuccess) return cuda_fail(e, "no-alloc scratch clear");
-  if ((st = launch_run(*d, p, A, grids, H, sms, s)) != CUSYNC_OK) return st;
+  if ((st = launch_run(dd, p, A, grids, H, sms, s)) != CUSYNC_OK) return st;
   if (error_word) {
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "stream synchronize");
     if ((e = cudaMemcpy(error_word, scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost)) != cudaSuccess)
