@@ -134,7 +134,19 @@ typedef struct {
                                         two) computes a 256-row tile with cta_group::2
                                         MMAs, each CTA loading half of the weight tile
                                         (MLP chains only); 0 = 2 for MLP chains with
-                                        M >= 1024, else 1 */
+                                        M >= 512, else 1 */
+  int32_t ksplit;                    /* K split of the producer GEMM (MLP chains): each
+                                        producer tile is computed by this many work units
+                                        over consecutive k-block ranges, whose fp32 partial
+                                        sums are added in unit order (deterministic) before
+                                        the last unit applies the epilogue and posts -- the
+                                        z dimension of the first GEMM's grid in [cuSync]
+                                        Table tab:waves:mlp.  0 = planner: when the
+                                        producer tiles fill at most half of a wave, the
+                                        largest split that keeps all units in it (at
+                                        most 4); when they fill more than half of one
+                                        wave, 2; else none; never fewer than 16 k-blocks
+                                        per unit.  1 = none */
 } cusync_chain_desc_t;
 
 /* Wave arithmetic of a two-kernel chain ([cuSync] §II-A "Thread block Wave Execution",
@@ -182,6 +194,9 @@ typedef struct {
   int32_t conv_rows_per_tile; /* CONV_RELU: image rows per row tile */
   int32_t cta_pair;           /* CTAs per tile (1 or 2); each posts its tile's semaphore */
   int32_t policy;             /* the policy the plan uses (CUSYNC_POLICY_AUTO resolved) */
+  int32_t ksplit;             /* K-split units per producer tile (1 = none); the
+                                 producer launch has m_tiles*n_tiles*ksplit units */
+  int32_t kb_per_split;       /* k-blocks per unit */
 } cusync_chain_info_t;
 
 /* Latency model of one chain run, in nanoseconds (cusync_predict_policies).  A tile

@@ -24,6 +24,10 @@ The model written out here, step by step:
   columns one after another) before the consumer tiles (row-major); CTA q takes tile q
   first, and every later tile goes to the CTA whose main loop frees up first (the lowest
   index on a tie);
+* with a K split of S, each producer tile is S consecutive queue entries; entry k runs
+  k-blocks [k * kb_per_split, min((k + 1) * kb_per_split, k_blocks)); the last entry's
+  epilogue (adding the others' partial sums) also waits for all the others' epilogues;
+  only the last entry posts;
 * a producer tile's post is seen post_ns after its epilogue; before consumer k-block kb
   the tile waits for the producer tiles its policy waits for there (``deps.wait_sets``);
   if they are posted later than the k-block could start, the k-block starts start_ns
@@ -63,6 +67,8 @@ class Chain:
     dep_chain: object     # deps.GemmChain / deps.ConvChain
     G: int = 1
     h_mb: float = 0.0
+    ksplit: int = 1       # producer units per tile (K split), each over consecutive k-blocks
+    kb_per_split: int = 0
 
 
 def play(tiles, slots, t0, model, cost):
@@ -86,33 +92,74 @@ def play(tiles, slots, t0, model, cost):
     return out
 
 
+def _units(chain):
+    """Producer queue entries (tile, unit, k-blocks)."""
+    S = max(1, chain.ksplit)
+    kb0 = chain.k_blocks[0]
+    per = chain.kb_per_split if S > 1 else kb0
+    return [(t, k, min(per, kb0 - k * per)) for t in chain.prod_tiles for k in range(S)]
+
+
+def _play_producers(chain, slots, t0, model, ctas=None):
+    """The producer entries on `slots` CTAs (or on the given CTA states); returns the
+    CTA states, each tile's done time (its last unit's) and the latest done time."""
+    S = max(1, chain.ksplit)
+    units = _units(chain)
+    if ctas is None:
+        ctas = [{"free": t0, "last_done": t0, "used": False} for _ in range(max(1, min(slots, len(units))))]
+    prev_done = {}
+    tile_done = {}
+    end = t0
+    for q, (tile, k, nkb) in enumerate(units):
+        i = q if q < len(ctas) else min(range(len(ctas)), key=lambda j: (ctas[j]["free"], j))
+        c = ctas[i]
+        start = c["free"] if c["used"] else c["free"] + model.start_ns
+        c["used"] = True
+        main_end = start + nkb * model.kblock_ns[0]
+        ready = max(main_end, c["last_done"])
+        if S > 1 and k == S - 1:
+            ready = max(ready, prev_done[tile])
+        done = ready + model.epilogue_ns[0]
+        if k < S - 1:
+            prev_done[tile] = max(prev_done.get(tile, done), done)
+        c["free"] = main_end
+        c["last_done"] = done
+        end = max(end, done)
+        if k == S - 1:
+            tile_done[tile] = done
+    return ctas, tile_done, end
+
+
 def predict_stream(chain, slots0, slots1, model):
     """Stream order: two launches, the second gap_ns after the first's last epilogue."""
     kb0, kb1 = chain.k_blocks
-    r0 = play([(0, t) for t in chain.prod_tiles], slots0, 0.0, model,
-              lambda tile, s: s + kb0 * model.kblock_ns[0])
-    end0 = max(d for _, _, d in r0) if r0 else 0.0
+    _, _, end0 = _play_producers(chain, slots0, 0.0, model)
     r1 = play([(1, m) for m in chain.cons_rows], slots1, end0 + model.gap_ns, model,
               lambda tile, s: s + kb1 * model.kblock_ns[1])
     return max(d for _, _, d in r1) if r1 else end0 + model.gap_ns
 
 
 def predict_fused(chain, policy, slots, model):
-    """One persistent launch: producer tiles, then consumer tiles that wait per policy."""
-    kb0, kb1 = chain.k_blocks
+    """One persistent launch: producer entries, then consumer tiles that wait per policy."""
+    kb1 = chain.k_blocks[1]
     sentinel = policy == "SENTINEL"
     wait_policy = "TILE" if sentinel else policy
-    posted = {}
+    t0 = chain.h_mb * model.fill_ns_per_mb if sentinel else 0.0
+    n_units = len(_units(chain))
+    total = n_units + len(chain.cons_rows)
+    ctas = [{"free": t0, "last_done": t0, "used": False} for _ in range(max(1, min(slots, total)))]
+    # the producer entries come first in the queue, so every producer tile's post time
+    # is known before the first consumer tile asks for it
+    ctas, tile_done, end = _play_producers(chain, slots, t0, model, ctas)
+    posted = {tile: d + model.post_ns for tile, d in tile_done.items()}
     wait_cache = {}
-
-    def cost(tile, start):
-        stage, what = tile
-        if stage == 0:
-            return start + kb0 * model.kblock_ns[0]
-        m = what
+    for q, m in enumerate(chain.cons_rows, start=n_units):
+        i = q if q < len(ctas) else min(range(len(ctas)), key=lambda j: (ctas[j]["free"], j))
+        c = ctas[i]
+        t = c["free"] if c["used"] else c["free"] + model.start_ns
+        c["used"] = True
         if m not in wait_cache:
             wait_cache[m] = deps.wait_sets(chain.dep_chain, wait_policy, m, chain.G)
-        t = start
         for kb in range(kb1):
             need = wait_cache[m][kb]
             if need:
@@ -123,26 +170,10 @@ def predict_fused(chain, policy, slots, model):
                 t += model.sentinel_kblock_ns
             else:
                 t += model.kblock_ns[1] + (model.wait_kblock_ns if need else 0.0)
-        return t
-
-    tiles = [(0, t) for t in chain.prod_tiles] + [(1, m) for m in chain.cons_rows]
-    t0 = chain.h_mb * model.fill_ns_per_mb if sentinel else 0.0
-    # the tiles are taken in queue order, so every producer tile's post time is known
-    # before the first consumer tile asks for it
-    ctas = [{"free": t0, "last_done": t0, "used": False} for _ in range(max(1, min(slots, len(tiles))))]
-    end = t0
-    for q, tile in enumerate(tiles):
-        k = q if q < len(ctas) else min(range(len(ctas)), key=lambda i: (ctas[i]["free"], i))
-        c = ctas[k]
-        start = c["free"] if c["used"] else c["free"] + model.start_ns
-        c["used"] = True
-        main_end = cost(tile, start)
-        done = max(main_end, c["last_done"]) + model.epilogue_ns[tile[0]]
-        c["free"] = main_end
+        done = max(t, c["last_done"]) + model.epilogue_ns[1]
+        c["free"] = t
         c["last_done"] = done
         end = max(end, done)
-        if tile[0] == 0:
-            posted[tile[1]] = done + model.post_ns
     return end
 
 

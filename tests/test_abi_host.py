@@ -82,7 +82,7 @@ GPT = dict(K=12288, N1=6144, N2=12288)
 ])
 def test_plan_waves_gpt_mlp(M, tile_n, prod, cons, stream, fused):
     dims = dict(K=256, N1=1024, N2=256) if M == 64 else GPT
-    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, tile_n=tile_n, num_sms=148, cta_pair=1, **dims)
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, tile_n=tile_n, num_sms=148, cta_pair=1, ksplit=1, **dims)
     r = cs.cusync_plan_waves(d)
     assert (r.tbs[0], r.tbs[1]) == (prod, cons)
     assert r.tbs[0] == planner.gemm_tiles(M, dims["N1"], 128, tile_n)
@@ -97,7 +97,7 @@ def test_plan_waves_gpt_mlp(M, tile_n, prod, cons, stream, fused):
 ])
 def test_plan_waves_cta_pairs(M, prod, cons, stream, fused):
     # a CTA pair computes a 256 x 256 tile and occupies two SMs: 74 pairs on 148 SMs
-    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, tile_n=256, num_sms=148, cta_pair=2, **GPT)
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, tile_n=256, num_sms=148, cta_pair=2, ksplit=1, **GPT)
     r = cs.cusync_plan_waves(d)
     assert (r.tbs[0], r.tbs[1]) == (prod, cons)
     assert r.cap == 74
@@ -120,6 +120,10 @@ def test_cta_pair_only_for_mlp_chains():
     assert cs.cusync_plan_info(d).cta_pair == 1
     d.M = 1024
     assert cs.cusync_plan_info(d).cta_pair == 2
+    d.M = 512
+    assert cs.cusync_plan_info(d).cta_pair == 2
+    d.M = 256
+    assert cs.cusync_plan_info(d).cta_pair == 1
     d.M = 64
     d.cta_pair = 2
     assert cs.cusync_plan_info(d).cta_pair == 2
@@ -127,7 +131,7 @@ def test_cta_pair_only_for_mlp_chains():
 
 def test_plan_swiglu_and_conv():
     d = cs.make_desc(cs.CHAIN_MLP_SWIGLU, "TILE", M=256, K=8192, N1=3584, N2=8192, tile_n=256, num_sms=148,
-                     cta_pair=1)
+                     cta_pair=1, ksplit=1)
     r = cs.cusync_plan_waves(d)
     assert (r.tbs[0], r.tbs[1]) == (2 * 28, 2 * 32)
     d = cs.make_desc(cs.CHAIN_CONV_RELU, "TILE", n=32, h=14, w=14, c=256, k_out=256, tile_n=256, num_sms=148)
@@ -277,3 +281,43 @@ def test_tile_order_is_a_permutation(case, policy, G, raster):
             order = deps.strided_producer_order(nt, info.strided_group) if (stage == 0 and policy == "STRIDED") \
                 else list(range(nt))
             assert seen == [(m, order[y]) for m in range(mt) for y in range(nt)]
+
+
+@pytest.mark.parametrize("kind,dims,pair,want", [
+    (cs.CHAIN_MLP_GELU, dict(M=256, **GPT), 1, 3),            # 48 tiles on 152 SMs: 3 units each
+    (cs.CHAIN_MLP_GELU, dict(M=512, **GPT), 1, 2),            # 96 tiles fill more than half a wave
+    (cs.CHAIN_MLP_GELU, dict(M=1024, **GPT), 1, 1),           # 192 tiles: more than a wave
+    (cs.CHAIN_MLP_GELU, dict(M=64, K=256, N1=1024, N2=256), 1, 1),   # 4 k-blocks: nothing to split
+    (cs.CHAIN_MLP_GELU, dict(M=64, K=12288, N1=6144, N2=12288), 1, 4),  # 24 tiles: at most 4 units
+    (cs.CHAIN_MLP_SWIGLU, dict(M=256, K=8192, N1=3584, N2=8192), 1, 2),
+    (cs.CHAIN_MLP_GELU, dict(M=256, **GPT), 2, 3),            # 24 pair tiles on 76 pairs
+])
+def test_planner_k_split(kind, dims, pair, want):
+    d = cs.make_desc(kind, "ROW", num_sms=152, cta_pair=pair, tile_n=256, **dims)
+    info = cs.cusync_plan_info(d)
+    assert info.ksplit == want
+    assert info.kb_per_split * want >= info.k_blocks[0] > info.kb_per_split * (want - 1)
+    r = cs.cusync_plan_waves(d)
+    assert r.tbs[0] == info.m_tiles[0] * info.n_tiles[0] * want   # the producer launch runs units
+    assert r.tbs[0] * pair <= 2 * 152
+
+
+def test_k_split_requests():
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=256, num_sms=152, ksplit=5, tile_n=256, **GPT)
+    info = cs.cusync_plan_info(d)
+    assert info.ksplit == 5 and info.kb_per_split == 39            # 192 k-blocks in 5 units
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=64, K=320, N1=512, N2=256, ksplit=4, num_sms=152)
+    info = cs.cusync_plan_info(d)
+    assert (info.ksplit, info.kb_per_split) == (3, 2)              # 5 k-blocks: no empty unit
+    with pytest.raises(cs.CusyncError) as e:                       # more units than k-blocks
+        cs.cusync_plan_info(cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=64, K=128, N1=512, N2=256, ksplit=3,
+                                         num_sms=152))
+    assert e.value.status == cs.ERR_UNSUPPORTED
+    d = cs.make_desc(cs.CHAIN_CONV_RELU, "ROW", n=1, h=14, w=14, c=64, k_out=128, ksplit=2, num_sms=152)
+    with pytest.raises(cs.CusyncError) as e:
+        cs.cusync_plan_info(d)
+    assert e.value.status == cs.ERR_UNSUPPORTED
+    with pytest.raises(cs.CusyncError) as e:
+        cs.cusync_plan_info(cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=64, K=64, N1=256, N2=64, ksplit=-1,
+                                         num_sms=152))
+    assert e.value.status == cs.ERR_INVALID_ARG

@@ -207,3 +207,47 @@ def test_auto_policy_runs_the_predicted_policy():
     d2 = cs.make_desc(cs.CHAIN_MLP_GELU, chosen, M=520, K=512, N1=1536, N2=512)
     H2, Y2, _ = run_mlp(d2, *ops, runs=1)
     assert np.array_equal(bits(Y), bits(Y2)) and np.array_equal(bits(H), bits(H2))
+
+
+@pytest.mark.parametrize("ksplit", [0, 2, 3, 5])
+@pytest.mark.parametrize("pair", [1, 2])
+def test_k_split_producer_all_policies(ksplit, pair):
+    """Producer tiles computed as K-split units (partial sums added in unit order by the
+    tile's units, the last one applying GeLU and posting): every policy and launch mode
+    within tolerance of the oracle and byte-identical to one another; ksplit 0 lets the
+    planner choose (2 here)."""
+    M, K, N1, N2 = 264, 2048, 1024, 512
+    (X, W1, W2), (H_ref, Y_ref) = _mlp_case(M, K, N1, N2, seed=8)
+    ops = device_mlp_operands(X, W1, W2)
+    ref_bits = None
+    for pol in POLICIES:
+        for launch in LAUNCHES:
+            if pol == "STREAM" and launch != cs.LAUNCH_PERSISTENT:
+                continue
+            d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, launch, M=M, K=K, N1=N1, N2=N2, tile_n=256, cta_pair=pair,
+                             ksplit=ksplit)
+            assert cs.cusync_plan_info(d).ksplit == (ksplit or 2)
+            H, Y, _ = run_mlp(d, *ops, runs=3)
+            assert_within_tol(f64(H), H_ref, f"H {pol} {launch} ksplit={ksplit}")
+            assert_within_tol(f64(Y), Y_ref, f"Y {pol} {launch} ksplit={ksplit}")
+            b = (bits(H), bits(Y))
+            if ref_bits is None:
+                ref_bits = b
+            else:
+                assert np.array_equal(b[0], ref_bits[0]) and np.array_equal(b[1], ref_bits[1]), (pol, launch)
+
+
+def test_k_split_swiglu():
+    M, K, N1, N2 = 200, 1024, 512, 256
+    X, Wg, Wu, Wd = synth.mlp_swiglu_inputs(M, K, N1, N2, seed=9)
+    H_ref, Y_ref = chains.mlp_swiglu(f64(X), f64(Wg), f64(Wu), f64(Wd))
+    ops = device_mlp_operands(X, Wg, Wd, Wup=Wu)
+    ref = None
+    for pol in ("STREAM", "ROW", "TILE", "SENTINEL"):
+        d = cs.make_desc(cs.CHAIN_MLP_SWIGLU, pol, M=M, K=K, N1=N1, N2=N2, tile_n=256, ksplit=3)
+        H, Y, _ = run_mlp(d, *ops, runs=2)
+        assert_within_tol(f64(H), H_ref, f"H {pol}")
+        assert_within_tol(f64(Y), Y_ref, f"Y {pol}")
+        b = (bits(H), bits(Y))
+        ref = ref or b
+        assert np.array_equal(b[0], ref[0]) and np.array_equal(b[1], ref[1]), pol

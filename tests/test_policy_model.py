@@ -93,16 +93,17 @@ def _oracle_predict(desc, info, model, policy):
                                        G=info.strided_group if policy == "STRIDED" else 2)
         h_mb = desc.M * desc.N1 * 2 / 1e6
     G = info.strided_group if policy == "STRIDED" else 1
-    ch = pm.Chain(prod, cons, tuple(info.k_blocks), dc, G=G, h_mb=h_mb)
+    ch = pm.Chain(prod, cons, tuple(info.k_blocks), dc, G=G, h_mb=h_mb, ksplit=info.ksplit,
+                  kb_per_split=info.kb_per_split)
     mo = pm.Model(kblock_ns=tuple(model.kblock_ns), wait_kblock_ns=model.wait_kblock_ns,
                   sentinel_kblock_ns=model.sentinel_kblock_ns, start_ns=model.start_ns,
                   epilogue_ns=tuple(model.epilogue_ns), post_ns=model.post_ns, gap_ns=model.gap_ns,
                   fill_ns_per_mb=model.fill_ns_per_mb)
     slots = info.num_sms // info.cta_pair
-    nt = len(prod) + len(cons)
+    units = len(prod) * info.ksplit
     if policy == "STREAM":
-        return pm.predict_stream(ch, min(slots, len(prod)), min(slots, len(cons)), mo) / 1e3
-    return pm.predict_fused(ch, policy, min(slots, nt), mo) / 1e3
+        return pm.predict_stream(ch, min(slots, units), min(slots, len(cons)), mo) / 1e3
+    return pm.predict_fused(ch, policy, min(slots, units + len(cons)), mo) / 1e3
 
 
 CASES = [
@@ -111,6 +112,9 @@ CASES = [
     dict(kind=cs.CHAIN_MLP_GELU, M=1024, K=256, N1=1024, N2=512, tile_n=256, cta_pair=2, num_sms=20),
     dict(kind=cs.CHAIN_MLP_SWIGLU, M=256, K=256, N1=512, N2=256, tile_n=256, cta_pair=1, num_sms=12),
     dict(kind=cs.CHAIN_CONV_RELU, n=2, h=14, w=14, c=64, k_out=256, tile_n=128, num_sms=6),
+    # K split: 2 x 2 producer tiles on 16 CTAs -> 4 units each (4 k-blocks per unit)
+    dict(kind=cs.CHAIN_MLP_GELU, M=256, K=1024, N1=512, N2=512, tile_n=256, cta_pair=1, num_sms=16),
+    dict(kind=cs.CHAIN_MLP_GELU, M=256, K=1024, N1=512, N2=512, tile_n=256, cta_pair=1, num_sms=40, ksplit=3),
 ]
 
 
@@ -169,3 +173,17 @@ def test_default_model_is_calibrated_per_tiling():
     assert conv.epilogue_ns[0] == pytest.approx(conv.epilogue_ns[1] * 22.0 / 17.0)
     for m in (gelu, pair, conv):
         assert m.sentinel_kblock_ns > m.kblock_ns[1] and m.start_ns > 0 and m.post_ns > 0
+
+
+def test_k_split_closed_form():
+    """Two units of one tile on two CTAs: each runs half of the k-blocks; the second
+    unit's epilogue follows the first's; the consumer refills after the post."""
+    prod, cons, dc = pm.gemm_chain(128, 256, 128, 256, 256, 1, "ROW")
+    ch = pm.Chain(prod, cons, (8, 4), dc, ksplit=2, kb_per_split=4)
+    m = _model()
+    u0 = 100 + 4 * 10 + 30
+    u1 = max(100 + 4 * 10, u0) + 30
+    cons_start = 100 + 4 * 10             # CTA 0 frees up first and takes the consumer tile
+    want = max(u1 + 7 + 100, cons_start) + 4 * 20 + 3
+    want = max(want, u0) + 40
+    assert pm.predict_fused(ch, "ROW", 2, m) == pytest.approx(want, rel=1e-12)

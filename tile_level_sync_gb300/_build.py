@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(PKG, "libcusync.so")
 
 SOURCES = [os.path.join(CSRC, "cusync.cu")]
 DEPS = SOURCES + [
-    os.path.join(CSRC, f) for f in ("chain_kernel.cuh", "geometry.h", "ptx.cuh")
+    os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC)) if f.endswith((".h", ".cuh"))
 ] + [os.path.join(INCLUDE, "cusync.h")]
 
 NVCC_FLAGS = [

@@ -84,6 +84,8 @@ struct ChainArgs {
   uint32_t* flags;       // semaphores
   uint32_t* ctrl;        // CTRL_* words
   TraceRec* trace;       // per-tile timeline, or null
+  float* split_ws;       // K split: fp32 partial sums, per (tile, pair rank) ksplit-1 slots of 128 x BN
+  uint32_t* split_turn;  // K split: units of a tile's rows that have stored their sums
   int32_t queue;         // tile counter slot used by this launch
   int32_t first_stage;   // stages served by this launch: [first_stage, last_stage]
   int32_t last_stage;
@@ -117,6 +119,9 @@ struct KCfg {
 
 struct TileRef {
   int32_t s, m, c;
+  int32_t ks;   // K-split unit of the tile (0 without a split)
+  int32_t kb0;  // first k-block of the unit
+  int32_t nkb;  // k-blocks of the unit
 };
 
 __device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
@@ -131,10 +136,18 @@ __device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
     s = 1;
     u = t - a.tiles0;
   }
+  const StageGeo& g = a.st[s].g;
+  int32_t ks = 0, kb0 = 0, nkb = g.k_blocks;
+  if (g.ksplit > 1) {
+    ks = u % g.ksplit;
+    u /= g.ksplit;
+    kb0 = ks * g.kb_per_split;
+    nkb = min(g.kb_per_split, g.k_blocks - kb0);
+  }
   int32_t m, y;
-  tile_at(a.st[s].g, u, &m, &y);
+  tile_at(g, u, &m, &y);
   const int32_t c = (s == 0) ? producer_col(a.dep, y) : y;
-  return TileRef{s, m, c};
+  return TileRef{s, m, c, ks, kb0, nkb};
 }
 
 // Index of queue position t in the chain's tile numbering (producer tiles first).
@@ -235,13 +248,24 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return canon_bf16x2(*reinterpret_cast<uint32_t*>(&v));
 }
 
-// tanh-GeLU written as z * sigmoid(2u), u = sqrt(2/pi) (z + 0.044715 z^3), which equals
-// 0.5 z (1 + tanh u).
-__device__ __forceinline__ float gelu_f(float z) {
-  const float u = 0.7978845608028654f * (z + 0.044715f * z * z * z);
-  return __fdividef(z, 1.0f + __expf(-2.0f * u));
+// The activations use the hardware tanh approximation (PTX tanh.approx.f32, one MUFU
+// operation; relative error about 2^-11, far below a bf16 half-ulp of 2^-9):
+// tanh-GeLU 0.5 z (1 + tanh u) with u = sqrt(2/pi) (z + 0.044715 z^3), and
+// silu(g) = g sigmoid(g) = 0.5 g (1 + tanh(g / 2)).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
-__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float gelu_f(float z) {
+  const float u = 0.7978845608028654f * fmaf(0.044715f * z, z * z, z);
+  const float h = 0.5f * z;
+  return fmaf(h, tanh_approx(u), h);
+}
+__device__ __forceinline__ float silu_f(float g) {
+  const float h = 0.5f * g;
+  return fmaf(h, tanh_approx(h), h);
+}
 
 // Bounded waits on barriers that may receive arrivals from the other CTA of a pair use
 // cluster-scope acquire.
@@ -276,6 +300,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   volatile int32_t* it_issued = abort_flag + 1;
   volatile uint32_t* progress = reinterpret_cast<volatile uint32_t*>(it_issued + 1);  // k-blocks issued
+  volatile uint32_t* run_no = progress + 1;  // this launch's run number, for every role
   uint8_t* epi_stage = smem + S * C::kStageBytes + 1024;  // 1024-byte aligned TMA store boxes
 
   auto smem_a = [&](int st) { return stage_base + st * C::kStageBytes; };
@@ -333,6 +358,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
   }
   if (warp == 0 && lane == 0) {
     epoch = ptx::ld_relaxed_gpu(args.ctrl + CTRL_RUNS) + 1u;
+    *run_no = epoch;
     for (int s = args.first_stage; s <= args.last_stage; ++s) {
       ptx::prefetch_tmap(&args.st[s].tmA);
       ptx::prefetch_tmap(&args.st[s].tmB);
@@ -403,7 +429,8 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
 
         const TileRef tr = decode_tile(args, t);
         const StageArgs& SA = args.st[tr.s];
-        const int32_t KB = SA.g.k_blocks;
+        const int32_t KB = tr.nkb;            // k-blocks of this work unit
+        const int32_t kx0 = tr.kb0 * kBK;     // its first reduction coordinate
         const uint32_t tx = a_tile_bytes(SA.g) + (uint32_t)C::kBBytes;
         TraceRec* trec = (args.trace && leader) ? args.trace + chain_tile(args, t) : nullptr;
         if (trec) {
@@ -466,11 +493,11 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
           }
           uint8_t* dst = smem_b(st);
           if (to_leader) {
-            ptx::tma_load_2d_to_leader(dst, tmB, ptx::mapa(&full[st], 0), kbb * kBK, brow0, pol_b);
+            ptx::tma_load_2d_to_leader(dst, tmB, ptx::mapa(&full[st], 0), kx0 + kbb * kBK, brow0, pol_b);
           } else {
             ptx::mbar_arrive_expect_tx(&full[st], txs);
-            ptx::tma_load_2d(dst, tmB, &full[st], kbb * kBK, brow0, pol_b);
-            if (brow1 >= 0) ptx::tma_load_2d(dst + (BN / 2) * 128, tmB, &full[st], kbb * kBK, brow1, pol_b);
+            ptx::tma_load_2d(dst, tmB, &full[st], kx0 + kbb * kBK, brow0, pol_b);
+            if (brow1 >= 0) ptx::tma_load_2d(dst + (BN / 2) * 128, tmB, &full[st], kx0 + kbb * kBK, brow1, pol_b);
           }
           return 1;
         };
@@ -553,8 +580,8 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
             if (dep_kb && reorder) wait_deps(kb);
             if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
             const int st = (int)((it + (uint32_t)kb) % S);
-            if (to_leader) ptx::tma_load_2d_to_leader(smem_a(st), tmA, ptx::mapa(&full[st], 0), kb * kBK, a_row, pol_a);
-            else ptx::tma_load_2d(smem_a(st), tmA, &full[st], kb * kBK, a_row, pol_a);
+            if (to_leader) ptx::tma_load_2d_to_leader(smem_a(st), tmA, ptx::mapa(&full[st], 0), kx0 + kb * kBK, a_row, pol_a);
+            else ptx::tma_load_2d(smem_a(st), tmA, &full[st], kx0 + kb * kBK, a_row, pol_a);
             *progress = it + (uint32_t)kb + 1u;
           }
         } else {
@@ -674,7 +701,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
         }
         return __any_sync(FULL, (sbits & 0x80008000u) != 0u);
       };
-      for (int32_t kb = 0; kb < g.k_blocks; ++kb, ++it) {
+      for (int32_t kb = 0; kb < tr.nkb; ++kb, ++it) {
         const int st = (int)(it % S);
         if (to_leader) continue;  // this CTA's stages are counted on the leader's barriers
         if (!check) {
@@ -725,7 +752,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
             // k-blocks of this tile that landed meanwhile were most likely copied before
             // their data was written too: check them now and issue the stale ones again
             // at once, so that their reloads overlap instead of following one another.
-            for (int j = 1; j < S && kb + j < g.k_blocks; ++j) {
+            for (int j = 1; j < S && kb + j < tr.nkb; ++j) {
               const int sj = (int)((it + (uint32_t)j) % S);
               if ((clean_ahead >> sj) & 1u) continue;
               bool landed = false;
@@ -833,7 +860,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       const TileRef tr = decode_tile(args, t);
       const StageArgs& SA = args.st[tr.s];
       const StageGeo& g = SA.g;
-      const int32_t KB = g.k_blocks;
+      const int32_t KB = tr.nkb;
       if (pd > 0 && g.a_mode == AMODE_GEMM) {
         const int32_t a_row0 = tr.m * (128 * PAIR) + (int32_t)rank * 128;
         const int32_t b_rows = (PAIR == 1 && g.epi == EPI_SWIGLU) ? BN / 2 : BN / PAIR;
@@ -854,9 +881,9 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
           }
           live = __shfl_sync(FULL, live ? 1 : 0, 0) != 0;
           if (!live) break;
-          prefetch_rows(SA.b_ptr, SA.b_rows, g.K, b0, b_rows, kb, lane);
-          if (b1 >= 0) prefetch_rows(SA.b_ptr, SA.b_rows, g.K, b1, b_rows, kb, lane);
-          if (tr.s == 0) prefetch_rows(SA.a_ptr, SA.a_rows, g.K, a_row0, 128, kb, lane);
+          prefetch_rows(SA.b_ptr, SA.b_rows, g.K, b0, b_rows, tr.kb0 + kb, lane);
+          if (b1 >= 0) prefetch_rows(SA.b_ptr, SA.b_rows, g.K, b1, b_rows, tr.kb0 + kb, lane);
+          if (tr.s == 0) prefetch_rows(SA.a_ptr, SA.a_rows, g.K, a_row0, 128, tr.kb0 + kb, lane);
         }
       }
       it0 += (uint32_t)KB;
@@ -910,6 +937,70 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       const bool tma_out = g.a_mode == AMODE_GEMM;
       uint8_t* ebuf = epi_stage + (q * 2) * C::kEpiBufBytes;
       const int32_t row_w0 = tr.m * (128 * PAIR) + (int32_t)rank * 128 + q * 32;
+      // K split: the units of a tile other than the last store their fp32 partial sums
+      // in their own workspace slot and count themselves done; the last unit waits for
+      // all of them, adds the slots in unit order and then its own sums (the same
+      // association for every run and policy), and applies the epilogue to the total.
+      const bool split = g.ksplit > 1;
+      const bool last_unit = !split || tr.ks == g.ksplit - 1;
+      // Workspace layout per slot of a 128-row block: groups of 4 columns, then rows,
+      // then the 4 columns -- a warp's 32 rows of one column group are 512 contiguous
+      // bytes, so the float4 accesses below are fully coalesced.
+      constexpr int kSlotF4 = 128 * BN / 4;  // float4s per slot
+      float4* ws_row = nullptr;
+      if (split) {
+        const int64_t tile_id = ((int64_t)tr.m * g.n_tiles + tr.c) * PAIR + (int64_t)rank;
+        ws_row = reinterpret_cast<float4*>(args.split_ws) + tile_id * (g.ksplit - 1) * kSlotF4 + row;
+        if (last_unit) {
+          const uint32_t* turn = args.split_turn + tile_id;
+          const uint32_t target = *run_no * (uint32_t)(g.ksplit - 1);
+          const uint64_t t0 = ptx::globaltimer();
+          while ((int32_t)(ptx::ld_acquire_gpu(turn) - target) < 0) {
+            __nanosleep(64);
+            if (ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u) break;
+            if (ptx::globaltimer() - t0 > args.timeout_ns) {
+              record_error(args, ERRC_FLAG_TIMEOUT, t, 0xFFFF);
+              break;
+            }
+          }
+        }
+      }
+      // 32 accumulator columns from `col` on: a unit that is not the last stores them in
+      // its slot; the last one replaces them by slot 0 + slot 1 + ... + its own.  Through
+      // L2, not L1: the workspace is written and read by different CTAs.
+      auto split_add = [&](uint32_t (&x)[32], int col) {
+        float4* w = ws_row + (col / 4) * 128;  // column group col/4 + i is at w + i * 128
+        if (!last_unit) {
+          float4* ws = w + tr.ks * kSlotF4;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            __stcg(ws + i * 128, make_float4(__uint_as_float(x[4 * i]), __uint_as_float(x[4 * i + 1]),
+                                             __uint_as_float(x[4 * i + 2]), __uint_as_float(x[4 * i + 3])));
+          return;
+        }
+        float4 a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = __ldcg(w + i * 128);  // eight loads in flight per slot
+        for (int k = 1; k < g.ksplit - 1; ++k) {
+          float4 b[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) b[i] = __ldcg(w + k * kSlotF4 + i * 128);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            a[i].x += b[i].x;
+            a[i].y += b[i].y;
+            a[i].z += b[i].z;
+            a[i].w += b[i].w;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          x[4 * i + 0] = __float_as_uint(a[i].x + __uint_as_float(x[4 * i + 0]));
+          x[4 * i + 1] = __float_as_uint(a[i].y + __uint_as_float(x[4 * i + 1]));
+          x[4 * i + 2] = __float_as_uint(a[i].z + __uint_as_float(x[4 * i + 2]));
+          x[4 * i + 3] = __float_as_uint(a[i].w + __uint_as_float(x[4 * i + 3]));
+        }
+      };
       for (int j = 0; j < nchunks; ++j) {
         uint32_t v[32];
         float f[32];
@@ -918,11 +1009,20 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
           ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(j * 32), v);
           ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(BN / 2 + j * 32), u);
           ptx::tmem_ld_wait();
+          if (split) {
+            split_add(v, j * 32);
+            split_add(u, BN / 2 + j * 32);
+            if (!last_unit) continue;
+          }
 #pragma unroll
           for (int i = 0; i < 32; ++i) f[i] = silu_f(__uint_as_float(v[i])) * __uint_as_float(u[i]);
         } else {
           ptx::tmem_ld_32x32b_x32(tbase + (uint32_t)(j * 32), v);
           ptx::tmem_ld_wait();
+          if (split) {
+            split_add(v, j * 32);
+            if (!last_unit) continue;
+          }
           if (g.epi == EPI_GELU) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = gelu_f(__uint_as_float(v[i]));
@@ -997,13 +1097,24 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
         if (ptx::mbar_wait_bounded(&epi_done[acc], apar, pto))
           args.trace[chain_tile(args, t)].t_epi = ptx::globaltimer();
       }
-      if (tr.s == 0 && threadIdx.x == 64) {
+      if (tr.s == 0 && threadIdx.x == 64 && !last_unit) {
+        // K split: this unit's sums are in its workspace slot (the epi_done barrier orders
+        // the 128 threads' stores before this thread); count it for the tile's last unit.
+        if (!ptx::mbar_wait_bounded(&epi_done[acc], apar, pto)) {
+          record_error(args, ERRC_PIPELINE, t, 7);
+          *abort_flag = 1;
+        } else {
+          const int64_t tile_id = ((int64_t)tr.m * g.n_tiles + tr.c) * PAIR + (int64_t)rank;
+          ptx::fence_acq_rel_gpu();
+          ptx::red_release_gpu_add(args.split_turn + tile_id, 1u);
+        }
+      } else if (tr.s == 0 && threadIdx.x == 64) {
         const int32_t flag = producer_flag(args.dep, tr.m, tr.c);
         if (flag >= 0) {
           // cuSync §IV-E "Post": after all of this CTA's stores of the tile (the epi_done
           // barrier orders its 128 threads' stores before this thread), one device-scope
           // release.
-          if (!ptx::mbar_wait_sleepy(&epi_done[acc], apar, pto)) {
+          if (!ptx::mbar_wait_bounded(&epi_done[acc], apar, pto)) {
             record_error(args, ERRC_PIPELINE, t, 5);
             *abort_flag = 1;
           } else if (!((args.flags_bits & kDebugSkipPost) && tr.m == 0 && tr.c == 0)) {

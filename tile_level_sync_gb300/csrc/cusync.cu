@@ -58,7 +58,16 @@ struct Plan {
   StageGeo geo[2];
   DepCfg dep;
   int64_t num_flags;
+  int64_t split_rows;   // K split: workspace row blocks (producer tiles x pair), else 0
 };
+
+// Words of a chain's device state: control words, semaphores, K-split turn counters.
+int64_t state_words(const Plan& p) { return CTRL_WORDS + p.num_flags + p.split_rows; }
+// fp32 elements of the K-split workspace: ksplit - 1 slots of a 128-row accumulator per
+// row block.
+int64_t split_ws_floats(const Plan& p) {
+  return p.split_rows * (int64_t)(p.geo[0].ksplit - 1) * 128 * (int64_t)p.bn;
+}
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -76,6 +85,7 @@ int32_t default_tile_n(const cusync_chain_desc_t& d) {
 }
 
 cusync_status_t resolve_auto(const cusync_chain_desc_t& d, cusync_chain_desc_t* out);
+int query_num_sms(int32_t requested, int* out);
 
 cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   if (d.kind < CUSYNC_CHAIN_MLP_GELU || d.kind > CUSYNC_CHAIN_CONV_RELU) return CUSYNC_ERR_INVALID_ARG;
@@ -89,9 +99,9 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   const int32_t bn = default_tile_n(d);
   if (bn != 128 && bn != 256) return CUSYNC_ERR_UNSUPPORTED;
   const bool mlp = d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
-  // CTA pairs (cta_group::2, 256-row tiles) for MLP chains with at least 1024 tokens,
+  // CTA pairs (cta_group::2, 256-row tiles) for MLP chains with at least 512 tokens,
   // where they measured faster on GB300; single-CTA 128-row tiles otherwise.
-  const int32_t pair = d.cta_pair ? d.cta_pair : ((mlp && d.M >= 1024) ? 2 : 1);
+  const int32_t pair = d.cta_pair ? d.cta_pair : ((mlp && d.M >= 512) ? 2 : 1);
   if (pair != 1 && pair != 2) return CUSYNC_ERR_INVALID_ARG;
   if (pair == 2 && !mlp) return CUSYNC_ERR_UNSUPPORTED;
   std::memset(p, 0, sizeof(*p));
@@ -155,6 +165,33 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   const int32_t raster = d.raster_rows > 0 ? d.raster_rows : 1;
   g0.raster = raster < g0.m_tiles ? raster : g0.m_tiles;
   g1.raster = raster < g1.m_tiles ? raster : g1.m_tiles;
+  // K split of the producer GEMM (see cusync_chain_desc_t::ksplit)
+  if (d.ksplit < 0 || d.ksplit > 16) return CUSYNC_ERR_INVALID_ARG;
+  int32_t ks = d.ksplit;
+  if (ks == 0) {
+    ks = 1;
+    if (mlp) {
+      int sms = 0;
+      if (query_num_sms(d.num_sms, &sms) != 0) sms = 148;
+      // Producer tiles that fill at most half of a wave: as many units per tile as fit in
+      // the wave (at most 4, at least 16 k-blocks each).  Tiles that fill more than half
+      // of it: 2 units per tile, whose second wave the fused queue fills with consumer
+      // tiles (measured faster on GB300, e.g. the M=512 GPT-3 MLP slice).
+      const int64_t slots = sms / pair;
+      const int64_t t0 = (int64_t)g0.m_tiles * g0.n_tiles;
+      int64_t want = 1;
+      if (t0 > 0 && 2 * t0 <= slots) want = std::min<int64_t>(slots / t0, 4);
+      else if (t0 > 0 && t0 <= slots) want = 2;
+      ks = (int32_t)std::max<int64_t>(1, std::min<int64_t>(want, g0.k_blocks / 16));
+    }
+  }
+  if (ks > 1 && !mlp) return CUSYNC_ERR_UNSUPPORTED;
+  if (ks > g0.k_blocks) return CUSYNC_ERR_UNSUPPORTED;
+  g0.ksplit = ks;
+  g0.kb_per_split = (int32_t)ceil_div(g0.k_blocks, ks);
+  g0.ksplit = (int32_t)ceil_div(g0.k_blocks, g0.kb_per_split);  // no empty unit
+  g1.ksplit = 1;
+  g1.kb_per_split = g1.k_blocks;
   if (d.l2_prefetch < -1 || d.l2_prefetch > 64) return CUSYNC_ERR_INVALID_ARG;
   DepCfg& dep = p->dep;
   dep.policy = d.policy;
@@ -172,6 +209,7 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   }
   p->num_flags = num_flags(dep);
   if (p->num_flags > (1ll << 24)) return CUSYNC_ERR_UNSUPPORTED;
+  p->split_rows = g0.ksplit > 1 ? (int64_t)g0.m_tiles * g0.n_tiles * pair : 0;
   return CUSYNC_OK;
 }
 
@@ -281,8 +319,8 @@ struct Grids {
 };
 
 Grids make_grids(const Plan& p, int sms, int max_clusters) {
-  const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
-  const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
+  const int64_t t0 = stage_units(p.geo[0]);
+  const int64_t t1 = stage_units(p.geo[1]);
   Grids g;
   if (p.pair == 2) {
     const int64_t cl = std::max<int64_t>(1, std::min<int64_t>(sms / 2, max_clusters > 0 ? max_clusters : sms / 2));
@@ -392,7 +430,8 @@ struct cusync_chain {
   Plan plan;
   int device;
   int num_sms;
-  uint32_t* state;       // CTRL_WORDS control words, then the semaphores
+  uint32_t* state;       // CTRL_WORDS control words, the semaphores, K-split turn counters
+  float* split_ws;       // K-split fp32 workspace, or null
   TraceRec* trace;       // per-tile timeline (CUSYNC_FLAG_TRACE), or null
   Grids grids;
   // TMA descriptors cached by operand pointers
@@ -477,7 +516,8 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
   A.first_stage = 0;
   A.last_stage = 0;
   A.pdl_role = pdl ? 1 : 0;
-  e = launch_any(p, A, g.prod, false, false, stream);
+  // K-split units wait for the tile's earlier units: the producer CTAs must all be resident.
+  e = launch_any(p, A, g.prod, /*coop=*/p.geo[0].ksplit > 1, false, stream);
   if (e != cudaSuccess) return cuda_fail(e, "producer launch");
   A.queue = 1;
   A.first_stage = 1;
@@ -519,9 +559,9 @@ bool encode_maps(const cusync_chain_desc_t& d, const Plan& p, ChainArgs& A, cons
 }
 
 // Kernel arguments that do not depend on the operand pointers.
-void fill_static_args(const cusync_chain_desc_t& d, const Plan& p, uint32_t* state, ChainArgs& A) {
-  const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
-  const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
+void fill_static_args(const cusync_chain_desc_t& d, const Plan& p, uint32_t* state, float* split_ws, ChainArgs& A) {
+  const int64_t t0 = stage_units(p.geo[0]);
+  const int64_t t1 = stage_units(p.geo[1]);
   const uint64_t timeout = d.timeout_ns ? d.timeout_ns : kDefaultTimeoutNs;
   A.st[0].g = p.geo[0];
   A.st[1].g = p.geo[1];
@@ -529,6 +569,8 @@ void fill_static_args(const cusync_chain_desc_t& d, const Plan& p, uint32_t* sta
   A.dep = p.dep;
   A.ctrl = state;
   A.flags = state + CTRL_WORDS;
+  A.split_turn = p.split_rows > 0 ? state + CTRL_WORDS + p.num_flags : nullptr;
+  A.split_ws = split_ws;
   A.tiles0 = (int32_t)t0;
   A.tiles1 = (int32_t)t1;
   A.flags_bits = d.flags;
@@ -613,8 +655,8 @@ cusync_status_t cusync_plan_waves(const cusync_chain_desc_t* d, cusync_wave_repo
   if (st != CUSYNC_OK) return st;
   int sms = 0;
   if (query_num_sms(d->num_sms, &sms) != 0) return CUSYNC_ERR_CUDA;
-  const int64_t t0 = (int64_t)p.geo[0].m_tiles * p.geo[0].n_tiles;
-  const int64_t t1 = (int64_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
+  const int64_t t0 = stage_units(p.geo[0]);
+  const int64_t t1 = stage_units(p.geo[1]);
   // one tile per CTA, or per CTA pair: a pair occupies two SMs
   st = cusync_wave_stats(t0, t1, 1, p.pair == 2 ? sms / 2 : sms, out);
   if (st != CUSYNC_OK) return st;
@@ -660,7 +702,10 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
   ch->plan = p;
   ch->device = dev;
   ch->num_sms = sms;
-  const size_t words = CTRL_WORDS + (size_t)p.num_flags;
+  const size_t words = (size_t)state_words(p);
+  ch->state = nullptr;
+  ch->split_ws = nullptr;
+  ch->trace = nullptr;
   if (cudaMalloc(&ch->state, words * sizeof(uint32_t)) != cudaSuccess) {
     delete ch;
     return CUSYNC_ERR_NOMEM;
@@ -670,12 +715,17 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
     delete ch;
     return cuda_fail(e, "state clear");
   }
-  ch->trace = nullptr;
+  if (p.split_rows > 0 && cudaMalloc(&ch->split_ws, (size_t)split_ws_floats(p) * sizeof(float)) != cudaSuccess) {
+    cudaFree(ch->state);
+    delete ch;
+    return CUSYNC_ERR_NOMEM;
+  }
   if (d->flags & CUSYNC_FLAG_TRACE) {
-    const size_t n = (size_t)p.geo[0].m_tiles * p.geo[0].n_tiles + (size_t)p.geo[1].m_tiles * p.geo[1].n_tiles;
+    const size_t n = (size_t)stage_units(p.geo[0]) + (size_t)stage_units(p.geo[1]);
     if (cudaMalloc(&ch->trace, n * sizeof(TraceRec)) != cudaSuccess ||
         cudaMemset(ch->trace, 0, n * sizeof(TraceRec)) != cudaSuccess) {
       if (ch->trace) cudaFree(ch->trace);
+      if (ch->split_ws) cudaFree(ch->split_ws);
       cudaFree(ch->state);
       delete ch;
       return CUSYNC_ERR_NOMEM;
@@ -684,7 +734,7 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
   ch->grids = make_grids(p, sms, max_clusters);
   ChainArgs& A = ch->args;
   std::memset(&A, 0, sizeof(A));
-  fill_static_args(ch->d, p, ch->state, A);
+  fill_static_args(ch->d, p, ch->state, ch->split_ws, A);
   A.trace = ch->trace;
   ch->maps_valid = false;
   *out = ch;
@@ -709,7 +759,7 @@ cusync_status_t cusync_run_conv_chain(cusync_chain_t ch, const void* x, const vo
 
 cusync_status_t cusync_chain_reset(cusync_chain_t ch, cusync_stream_t stream) {
   if (!ch) return CUSYNC_ERR_INVALID_ARG;
-  const size_t words = CTRL_WORDS + (size_t)ch->plan.num_flags;
+  const size_t words = (size_t)state_words(ch->plan);
   cudaError_t e = cudaMemsetAsync(ch->state, 0, words * sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "state reset");
   return CUSYNC_OK;
@@ -763,6 +813,8 @@ cusync_status_t cusync_plan_info(const cusync_chain_desc_t* d, cusync_chain_info
   out->num_sms = sms;
   out->conv_rows_per_tile = d->kind == CUSYNC_CHAIN_CONV_RELU ? p.geo[0].th : 0;
   out->policy = p.dep.policy;
+  out->ksplit = p.geo[0].ksplit;
+  out->kb_per_split = p.geo[0].kb_per_split;
   return CUSYNC_OK;
 }
 
@@ -880,6 +932,7 @@ cusync_status_t cusync_destroy_chain(cusync_chain_t ch) {
   if (!ch) return CUSYNC_OK;
   cudaError_t e = cudaSuccess;
   if (ch->trace) cudaFree(ch->trace);
+  if (ch->split_ws) cudaFree(ch->split_ws);
   if (ch->state) e = cudaFree(ch->state);
   delete ch;
   return e == cudaSuccess ? CUSYNC_OK : CUSYNC_ERR_CUDA;
@@ -939,10 +992,13 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
                                                   uint32_t* error_word) {
   if (!d) return CUSYNC_ERR_INVALID_ARG;
   if (d->kind != CUSYNC_CHAIN_MLP_GELU && d->kind != CUSYNC_CHAIN_MLP_SWIGLU) return CUSYNC_ERR_INVALID_ARG;
-  Plan p;
-  cusync_status_t st = make_plan(*d, &p);
-  if (st != CUSYNC_OK) return st;
+  // No workspace to hold K-split partial sums: the producer tiles are not split.
+  if (d->ksplit > 1) return CUSYNC_ERR_UNSUPPORTED;
   cusync_chain_desc_t dd = *d;
+  dd.ksplit = 1;
+  Plan p;
+  cusync_status_t st = make_plan(dd, &p);
+  if (st != CUSYNC_OK) return st;
   dd.policy = (cusync_policy_t)p.dep.policy;  // CUSYNC_POLICY_AUTO resolved
   // The fixed array bounds the number of semaphores this entry point can use.
   if ((int64_t)CTRL_WORDS + p.num_flags > kNoAllocWords) {
@@ -969,7 +1025,7 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
   ChainArgs A;
   std::memset(&A, 0, sizeof(A));
   if (!encode_maps(dd, p, A, X, W1t, W2t, H, Y)) return CUSYNC_ERR_INVALID_ARG;
-  fill_static_args(dd, p, scratch, A);
+  fill_static_args(dd, p, scratch, nullptr, A);
   A.st[0].out = H;
   A.st[1].out = Y;
   const int max_clusters = g_noalloc_clusters[dev][p.bn == 256 ? 0 : 1];

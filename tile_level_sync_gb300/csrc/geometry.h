@@ -51,7 +51,18 @@ struct StageGeo {
   int32_t th;                        // image rows per row tile
   int32_t tpi;                       // row tiles per image = ceil(img_h / th)
   int32_t cblocks;                   // cin / kBK channel blocks per filter tap
+  // K split (GEMM producers): each tile is computed by ksplit work units, unit k taking
+  // k-blocks [k * kb_per_split, (k + 1) * kb_per_split); their fp32 partial sums are added
+  // in unit order and the last unit applies the epilogue.  1 = no split.
+  int32_t ksplit;
+  int32_t kb_per_split;
 };
+
+// Work units of a stage's queue: tiles x K-split units (the split units of one tile are
+// consecutive in the queue).
+CUSYNC_HD int64_t stage_units(const StageGeo& g) {
+  return (int64_t)g.m_tiles * g.n_tiles * (g.ksplit > 1 ? g.ksplit : 1);
+}
 
 // Consumer-side view of the producer's semaphores.
 struct DepCfg {

@@ -12,7 +12,9 @@
 //    consumer tile waits for under each policy), §VI-B ("no one policy" is best for
 //    every shape).
 //
-// Here a tile's latency is T_start + (k-blocks x per-k-block time) + T_epilogue, and the
+// Here a tile's latency is T_start + (k-blocks x per-k-block time) + T_epilogue (with a
+// K split, each unit of a producer tile runs its share of the k-blocks, and the last
+// unit's epilogue -- adding the others' partial sums -- follows all of theirs), and the
 // threadblock batches are not assumed but played out: a persistent CTA takes the next
 // tile of the queue as soon as its mainloop finishes (its epilogue overlaps the next
 // tile's mainloop), the first tile of each CTA is its own index, later tiles go to the
@@ -73,8 +75,11 @@ struct SimCta {
 // (all producer tiles precede consumer tiles in the queue, so they are filled first).
 inline double play_queue(const ModelChain& c, const LatencyModel& lm, int s0, int s1, int32_t slots, double t0,
                          bool sentinel, std::vector<double>* flag_ready) {
-  const int64_t n0 = (int64_t)c.geo[0].m_tiles * c.geo[0].n_tiles;
-  const int64_t n1 = (int64_t)c.geo[1].m_tiles * c.geo[1].n_tiles;
+  const int64_t n0 = stage_units(c.geo[0]);
+  const int64_t n1 = stage_units(c.geo[1]);
+  const int32_t S = c.geo[0].ksplit > 1 ? c.geo[0].ksplit : 1;
+  // K split: when the other units of each producer tile have all stored their sums
+  std::vector<double> unit_done(S > 1 ? (size_t)(n0 / S) : 0, 0.0);
   const int64_t total = (s0 == 0 ? n0 : 0) + (s1 == 1 ? n1 : 0);
   if (total == 0) return t0;
   std::vector<SimCta> cta((size_t)std::max<int64_t>(1, std::min<int64_t>(slots, total)));
@@ -84,7 +89,13 @@ inline double play_queue(const ModelChain& c, const LatencyModel& lm, int s0, in
   std::vector<std::vector<int32_t>> wl;
   for (int64_t q = 0; q < total; ++q) {
     const int s = (s0 == 0 && q < n0) ? 0 : 1;
-    const int64_t u = (s == 0) ? q : (s0 == 0 ? q - n0 : q);
+    int64_t u = (s == 0) ? q : (s0 == 0 ? q - n0 : q);
+    int32_t ks = 0, nkb = c.geo[s].k_blocks;
+    if (s == 0 && S > 1) {
+      ks = (int32_t)(u % S);
+      u /= S;
+      nkb = std::min(c.geo[0].kb_per_split, c.geo[0].k_blocks - ks * c.geo[0].kb_per_split);
+    }
     int32_t m, y;
     tile_at(c.geo[s], (int32_t)u, &m, &y);
     const int32_t col = (s == 0) ? producer_col(c.dep, y) : y;
@@ -101,7 +112,7 @@ inline double play_queue(const ModelChain& c, const LatencyModel& lm, int s0, in
     x.used = true;
     const StageGeo& g = c.geo[s];
     if (s == 0 || !waits) {
-      t += (double)g.k_blocks * lm.kblock_ns[s];
+      t += (double)nkb * lm.kblock_ns[s];
     } else {
       consumer_wait_lists(c, m, &wl);
       const double kb_ns = sentinel ? lm.sentinel_kblock_ns : lm.kblock_ns[1];
@@ -112,11 +123,15 @@ inline double play_queue(const ModelChain& c, const LatencyModel& lm, int s0, in
         t += kb_ns + ((!sentinel && !wl[kb].empty()) ? lm.wait_kblock_ns : 0.0);
       }
     }
-    const double done = std::max(t, x.last_done) + lm.epilogue_ns[s];
+    double ready = std::max(t, x.last_done);
+    const bool last = s != 0 || ks == S - 1;
+    if (s == 0 && S > 1 && last) ready = std::max(ready, unit_done[(size_t)u]);  // all other units stored
+    const double done = ready + lm.epilogue_ns[s];
+    if (s == 0 && S > 1 && !last) unit_done[(size_t)u] = std::max(unit_done[(size_t)u], done);
     x.free_main = t;
     x.last_done = done;
     end = std::max(end, done);
-    if (s == 0 && flag_ready) {
+    if (s == 0 && flag_ready && ks == S - 1) {
       const int32_t f = producer_flag(c.dep, m, col);
       if (f >= 0) (*flag_ready)[(size_t)f] = std::max((*flag_ready)[(size_t)f], done + lm.post_ns);
     }
