@@ -219,6 +219,13 @@ def oracle_sample_runner(wl, inputs):
             chains.mlp_swiglu_rows(X, Wg, Wu, Wd, rows)
             return 2.0 * len(rows) * d["K"] * 2 * d["N1"] + 2.0 * len(rows) * d["N1"] * d["N2"]
         return fn, d["M"]
+    if wl.kind == "attention":
+        X, Wqkv, W2 = (synth.f64(t) for t in inputs)
+
+        def fn(rows):
+            chains.attention_rows(X, Wqkv, W2, rows)
+            return 2.0 * len(rows) * d["K"] * 3 * d["N1"] + 2.0 * len(rows) * d["N1"] * d["N2"]
+        return fn, d["M"]
     x, w1, w2 = (synth.f64(t) for t in inputs)
 
     def fn(rows):  # rows = images
@@ -304,6 +311,16 @@ class Setup:
             self.y = torch.empty_like(self.h)
             self.x_host = x
             self.base = dict(kind=cs.CHAIN_CONV_RELU, n=d["N"], h=d["H"], w=d["W"], c=d["C"], k_out=d["K"])
+        elif wl.kind == "attention":
+            X, Wqkv, W2 = inputs
+            self.a = X.to(dev)
+            self.b0 = Wqkv.t().contiguous().to(dev)
+            self.b1 = W2.t().contiguous().to(dev)
+            self.h = torch.empty((d["M"], 3 * d["N1"]), dtype=torch.bfloat16, device=dev)
+            self.h2 = torch.empty((d["M"], d["N1"]), dtype=torch.bfloat16, device=dev)
+            self.y = torch.empty((d["M"], d["N2"]), dtype=torch.bfloat16, device=dev)
+            self.x_host = X
+            self.base = dict(kind=cs.CHAIN_ATTENTION, M=d["M"], K=d["K"], N1=d["N1"], N2=d["N2"])
         else:
             if wl.kind == "mlp_gelu":
                 X, W1, W2 = inputs
@@ -341,10 +358,11 @@ class Setup:
         return self.chains[key]
 
     def run(self, ch):
-        ch.run(self.a, self.b0, self.b1, self.h, self.y)
+        ch.run(self.a, self.b0, self.b1, self.h, self.y, h2=getattr(self, "h2", None))
 
     def kernels_per_run(self, policy, launch):
-        n = 2 if (policy == "STREAM" or launch == self.cs.LAUNCH_PDL) else 1
+        stages = 3 if self.base["kind"] == self.cs.CHAIN_ATTENTION else 2
+        n = stages if (policy == "STREAM" or launch == self.cs.LAUNCH_PDL) else 1
         return n + (1 if policy == "SENTINEL" else 0)
 
 
@@ -477,6 +495,9 @@ def algorithmic_bytes(wl):
     if wl.kind == "conv_relu":
         pix = d["N"] * d["H"] * d["W"]
         return 2 * (pix * d["C"] + 9 * d["C"] * d["K"] + 2 * pix * d["K"] + 9 * d["K"] * d["K"] + pix * d["K"])
+    if wl.kind == "attention":   # XQKV and XDot each written once and read once
+        return 2 * (d["M"] * d["K"] + d["K"] * 3 * d["N1"] + 2 * d["M"] * 3 * d["N1"] + 2 * d["M"] * d["N1"]
+                    + d["N1"] * d["N2"] + d["M"] * d["N2"])
     n1w = 2 * d["N1"] if wl.kind == "mlp_swiglu" else d["N1"]
     return 2 * (d["M"] * d["K"] + d["K"] * n1w + 2 * d["M"] * d["N1"] + d["N1"] * d["N2"] + d["M"] * d["N2"])
 
@@ -497,6 +518,8 @@ def check_output(setup, wl, inputs):
         rows = sorted(set([0, 1, d["M"] // 2, d["M"] - 1]))
         if wl.kind == "mlp_gelu":
             _, ref = chains.mlp_gelu_rows(*(synth.f64(t) for t in inputs), rows)
+        elif wl.kind == "attention":
+            _, _, ref = chains.attention_rows(*(synth.f64(t) for t in inputs), rows)
         else:
             _, ref = chains.mlp_swiglu_rows(*(synth.f64(t) for t in inputs), rows)
         got = Y[rows]
@@ -732,8 +755,12 @@ def sweep(a, torch, cs, synth, out_path):
                         row["us"][key] = ms * 1e3 if st == cs.OK else f"status {st}"
                         pk = f"r{raster}/p{pair}"
                         if pk not in row.setdefault("predicted_us", {}):
-                            pred = cs.cusync_predict_policies(ch.desc)
-                            row["predicted_us"][pk] = {n_: pred.us[i] for n_, i in cs.POLICY_NAMES.items() if i < 5}
+                            try:
+                                pred = cs.cusync_predict_policies(ch.desc)
+                                row["predicted_us"][pk] = {n_: pred.us[i] for n_, i in cs.POLICY_NAMES.items()
+                                                           if i < 5}
+                            except cs.CusyncError:   # the model covers two-stage chains
+                                row["predicted_us"][pk] = None
                 for c in list(setup.chains.values()):
                     c.close()
                 setup.chains = {}

@@ -78,7 +78,17 @@ typedef enum {
   /* H = ReLU(conv3x3(x, w1)) (bf16), y = conv3x3(H, w2); stride 1, pad 1, NHWC images
    * x [n,h,w,c], H and y [n,h,w,k_out], KRSC weights w1 [k_out,3,3,c] and
    * w2 [k_out,3,3,k_out]. */
-  CUSYNC_CHAIN_CONV_RELU = 2
+  CUSYNC_CHAIN_CONV_RELU = 2,
+  /* Self-attention block of [cuSync] Fig. fig:gpt-3:attention, three dependent kernels:
+   * XQKV = X x QKV (X [M,K]; W1t = QKV^T [3*N1, K], rows 0..N1-1 the XQ block, N1..2N1-1
+   * the XV block, 2N1..3N1-1 the XK block, as the figure slices XQKV); then per head of
+   * 128 columns and token row, XDot = softmax(XQ * XV) * XK (element-wise products,
+   * softmax over the head's 128 values; dropout is the identity of inference); then
+   * Y = XDot x W2 (W2t [N2, N1]).  Policies: ROW or TILE between both pairs of kernels,
+   * STRIDED_TILE = StridedSync (G = 3: a head's Q, V and K tiles share one semaphore)
+   * then TileSync, STREAM = three stream-ordered kernels; SENTINEL is not offered.
+   * N1 must be a multiple of the tile width and of 128. */
+  CUSYNC_CHAIN_ATTENTION = 3
 } cusync_chain_kind_t;
 
 /* How the two grids are made co-resident so that a waiting consumer can never starve
@@ -197,6 +207,11 @@ typedef struct {
   int32_t ksplit;             /* K-split units per producer tile (1 = none); the
                                  producer launch has m_tiles*n_tiles*ksplit units */
   int32_t kb_per_split;       /* k-blocks per unit */
+  /* ATTENTION (three stages): stage 1 is the pointwise kernel, stage 2 the output GEMM */
+  int32_t nst;                /* stages of the chain: 2, or 3 */
+  int32_t m_tiles2, n_tiles2, k_blocks2, n_out2, grid2;
+  int32_t num_flags_pw;       /* semaphores the pointwise stage waits on */
+  int32_t strided_group_pw, strided_distance_pw;
 } cusync_chain_info_t;
 
 /* Latency model of one chain run, in nanoseconds (cusync_predict_policies).  A tile
@@ -276,6 +291,15 @@ cusync_status_t cusync_run_mlp(cusync_chain_t chain, const void* X, const void* 
 cusync_status_t cusync_run_conv_chain(cusync_chain_t chain, const void* x, const void* w1, const void* w2, void* y1,
                                       void* y2, cusync_stream_t stream);
 
+/* Run an ATTENTION chain on `stream` ([cuSync] Fig. fig:gpt-3:attention): writes XQKV
+ * (first intermediate, [M, 3*N1] bf16: the XQ, XV and XK blocks side by side), XDot
+ * (second intermediate, [M, N1] bf16) and Y [M, N2].  Inputs: X [M,K], Wqkv_t [3*N1,K]
+ * (QKV^T, K contiguous), W2t [N2,N1].  Device memory, 16-byte aligned, caller-owned, the
+ * outputs distinct from one another and from X.  Asynchronous, capturable like
+ * cusync_run_mlp; INVALID_ARG / UNSUPPORTED / CUDA on launch-time errors. */
+cusync_status_t cusync_run_attention(cusync_chain_t chain, const void* X, const void* Wqkv_t, const void* W2t,
+                                     void* XQKV, void* XDot, void* Y, cusync_stream_t stream);
+
 /* Synchronise `stream` and read the chain's device error word.  Returns OK, TIMEOUT (a
  * consumer gave up waiting on a semaphore or a sentinel: the outputs of that run are
  * not valid) or DEVICE.  After an error the chain's synchronisation state is reset, so
@@ -297,6 +321,14 @@ cusync_status_t cusync_plan_info(const cusync_chain_desc_t* d, cusync_chain_info
  * computation with the same code the device runs. */
 cusync_status_t cusync_consumer_waits(const cusync_chain_desc_t* d, int32_t m_tile, int32_t* kb, int32_t* flag,
                                       uint32_t* per_run, int32_t max, int32_t* n_out);
+
+/* ATTENTION chains: the semaphore waits of pointwise tile (m_tile, head) on the QKV GEMM
+ * ([cuSync] §IV-E; Fig. fig:use-case:self-attention:strided for StridedSync): entry i
+ * is (flag[i], per_run[i]) -- semaphore flag[i] must have received per_run[i] posts in
+ * the current run before the head is computed.  Writes at most max entries and the
+ * count to *n_out.  Pure host computation with the code the device runs. */
+cusync_status_t cusync_pointwise_waits(const cusync_chain_desc_t* d, int32_t m_tile, int32_t head, int32_t* flag,
+                                       uint32_t* per_run, int32_t max, int32_t* n_out);
 
 /* The semaphore producer tile (m_tile, n_tile) posts (-1 if the policy posts none), and
  * the producer column visited at position y of a row (the policy's tile order).  Pure

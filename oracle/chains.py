@@ -23,6 +23,18 @@ the GPU receives:
                                            q*stride + s - pad, c] * w[o,r,s,c]
   No bias, no activation after the second convolution, no residual add.
 
+* Self-attention block ([cuSync] §II-B, Fig. ``fig:gpt-3:attention``):
+      XQKV = X x QKV               QKV [K, 3*N1]; stored in bf16
+      XQ, XV, XK = the column blocks [0,N1), [N1,2N1), [2N1,3N1) of XQKV
+                                   (in the figure's order: the second block is XV)
+      XDot = Dropout(Softmax(XQ . XV)) . XK, stored in bf16
+      Y    = XDot x W2             W2 [N1, N2]
+  Reading: "." is the element-wise product (the figure's fused dot-product
+  kernel), and the softmax runs over the columns of one head (``head``
+  columns), because the pages' tile dependencies have a column tile of XDot
+  read only the same column tiles of XQ, XV and XK; dropout is the identity
+  (inference).
+
 All inputs are fp64 arrays whose values are exactly representable in bf16.
 """
 
@@ -107,3 +119,28 @@ def mlp_swiglu_rows(X, Wgate, Wup, Wdown, rows):
     """(H[rows], Y[rows]) of ``mlp_swiglu`` for a subset of token rows."""
     X = _as64(X)[np.asarray(rows)]
     return mlp_swiglu(X, Wgate, Wup, Wdown)
+
+
+def softmax_heads(s, head):
+    """Softmax of each row of s [M, N] over consecutive groups of ``head`` columns."""
+    M, N = s.shape
+    g = s.reshape(M, N // head, head)
+    e = np.exp(g - g.max(axis=2, keepdims=True))
+    return (e / e.sum(axis=2, keepdims=True)).reshape(M, N)
+
+
+def attention(X, Wqkv, W2, head=128):
+    """(XQKV, XDot, Y) of the self-attention block; XQKV and XDot as stored (bf16 values)."""
+    X, Wqkv, W2 = _as64(X), _as64(Wqkv), _as64(W2)
+    n1 = Wqkv.shape[1] // 3
+    xqkv = bf16_intermediate(X @ Wqkv)
+    xq, xv, xk = xqkv[:, :n1], xqkv[:, n1:2 * n1], xqkv[:, 2 * n1:]
+    xdot = bf16_intermediate(softmax_heads(xq * xv, head) * xk)
+    return xqkv, xdot, xdot @ W2
+
+
+def attention_rows(X, Wqkv, W2, rows, head=128):
+    """(XQKV, XDot, Y) of ``attention`` for a subset of token rows (each output row
+    depends only on the same input row)."""
+    X = _as64(X)[np.asarray(rows)]
+    return attention(X, Wqkv, W2, head)

@@ -198,3 +198,47 @@ def wait_sets(chain, policy, m, G=2):
     else:
         raise ValueError(policy)
     return out
+
+
+@dataclass(frozen=True)
+class QkvChain:
+    """The QKV GEMM -> pointwise step of the attention block ([cuSync] Fig.
+    ``fig:use-case:self-attention:dependencies``): XQKV [M, 3*N1] is written in [BM, BNo]
+    tiles; pointwise tile (m, i) reads rows m*BM.. and the columns of head i
+    ([i*head, (i+1)*head)) of each of the three blocks."""
+    M: int
+    N1: int
+    BM: int
+    BNo: int
+    head: int = 128
+
+    @property
+    def n_tiles(self):
+        return math.ceil(3 * self.N1 / self.BNo)
+
+    def writes(self, m, c):
+        mask = np.zeros((self.M, 3 * self.N1), dtype=bool)
+        mask[m * self.BM:(m + 1) * self.BM, c * self.BNo:(c + 1) * self.BNo] = True
+        return mask
+
+    def reads(self, m, i):
+        mask = np.zeros((self.M, 3 * self.N1), dtype=bool)
+        for b in range(3):
+            c0 = b * self.N1 + i * self.head
+            mask[m * self.BM:(m + 1) * self.BM, c0:c0 + self.head] = True
+        return mask
+
+
+def pointwise_wait_set(chain, policy, m, i):
+    """Producer tiles a pointwise tile waits for: its data dependencies (TileSync), the
+    whole row(s) of tiles (RowSync), or the StridedSync(G = 3) groups of its columns."""
+    rd = chain.reads(m, i)
+    data = {(mp, c) for mp in range(math.ceil(chain.M / chain.BM)) for c in range(chain.n_tiles)
+            if np.any(chain.writes(mp, c) & rd)}
+    if policy == "TILE":
+        return data
+    if policy == "ROW":
+        return {(mp, c) for (mp, _) in data for c in range(chain.n_tiles)}
+    if policy == "STRIDED":
+        return {(mp, cc) for (mp, c) in data for cc in strided_members(chain, 3, c)}
+    raise ValueError(policy)

@@ -321,3 +321,74 @@ def test_k_split_requests():
         cs.cusync_plan_info(cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=64, K=64, N1=256, N2=64, ksplit=-1,
                                          num_sms=152))
     assert e.value.status == cs.ERR_INVALID_ARG
+
+
+# ----------------------------------------------------------------- attention chain
+
+ATTN_CASES = [
+    dict(M=200, K=512, N1=512, N2=384, tile_n=256),     # ragged M; 6 QKV column tiles, 4 heads
+    dict(M=256, K=256, N1=768, N2=256, tile_n=128),     # 18 QKV column tiles, 6 heads
+    dict(M=64, K=128, N1=256, N2=128, tile_n=256),
+]
+
+
+@pytest.mark.parametrize("case", ATTN_CASES)
+@pytest.mark.parametrize("policy", ["ROW", "TILE", "STRIDED"])
+def test_attention_plan_and_pointwise_waits_match_oracle(case, policy):
+    d = cs.make_desc(cs.CHAIN_ATTENTION, policy, num_sms=148, cta_pair=1, ksplit=1, **case)
+    info = cs.cusync_plan_info(d)
+    M, N1, tn = case["M"], case["N1"], case["tile_n"]
+    assert info.nst == 3 and info.cta_pair == 1
+    assert (info.n_tiles[0], info.n_tiles[1], info.n_tiles2) == (3 * N1 // tn, N1 // 128, -(-case["N2"] // tn))
+    assert info.k_blocks[1] == 0 and info.n_out[1] == 128
+    qc = deps.QkvChain(M=M, N1=N1, BM=128, BNo=tn)
+    nt = info.n_tiles[0]
+    for m in range(info.m_tiles[1]):
+        for i in range(info.n_tiles[1]):
+            got = set()
+            for flag, per_run in cs.cusync_pointwise_waits(d, m, i):
+                if policy == "TILE":
+                    mem = {divmod(flag, nt)}
+                    assert per_run == 1
+                elif policy == "ROW":
+                    mem = {(flag, c) for c in range(nt)}
+                    assert per_run == nt
+                else:
+                    D = info.strided_distance_pw
+                    assert info.strided_group_pw == 3 and D * 3 == nt
+                    mp, g = divmod(flag, D)
+                    mem = {(mp, g + j * D) for j in range(3)}
+                    assert per_run == 3
+                got |= mem
+            assert got == deps.pointwise_wait_set(qc, policy, m, i), (m, i)
+
+
+@pytest.mark.parametrize("case", ATTN_CASES)
+@pytest.mark.parametrize("policy", ["ROW", "TILE", "STRIDED"])
+def test_attention_output_gemm_waits_match_oracle(case, policy):
+    """The output GEMM reads XDot: TileSync on the pointwise tiles (also under StridedSync,
+    as in the pages' Strided+TileSync), or RowSync."""
+    d = cs.make_desc(cs.CHAIN_ATTENTION, policy, num_sms=148, cta_pair=1, ksplit=1, **case)
+    info = cs.cusync_plan_info(d)
+    gc = deps.GemmChain(M=case["M"], N1=case["N1"], BM=128, BNo=128, BK=64)
+    want_pol = "ROW" if policy == "ROW" else "TILE"
+    nt = info.n_tiles[1]
+    for m in range(info.m_tiles2):
+        got = [set() for _ in range(info.k_blocks2)]
+        for kb, flag, per_run in cs.cusync_consumer_waits(d, m):
+            got[kb] |= {(flag, c) for c in range(nt)} if want_pol == "ROW" else {divmod(flag, nt)}
+        assert got == deps.wait_sets(gc, want_pol, m), m
+
+
+def test_attention_refusals():
+    base = dict(M=64, K=128, N1=256, N2=128, tile_n=256, num_sms=148)
+    for kw, status in [(dict(policy="SENTINEL"), cs.ERR_UNSUPPORTED), (dict(policy="ROW", N1=192), cs.ERR_UNSUPPORTED),
+                       (dict(policy="ROW", cta_pair=2), cs.ERR_UNSUPPORTED)]:
+        args = dict(base, **kw)
+        pol = args.pop("policy")
+        with pytest.raises(cs.CusyncError) as e:
+            cs.cusync_plan_info(cs.make_desc(cs.CHAIN_ATTENTION, pol, **args))
+        assert e.value.status == status, kw
+    # the latency model covers the two-stage chains only
+    with pytest.raises(cs.CusyncError):
+        cs.cusync_predict_policies(cs.make_desc(cs.CHAIN_ATTENTION, "ROW", **base))

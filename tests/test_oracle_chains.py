@@ -167,3 +167,54 @@ def test_conv_chain_relu_and_rounding():
     Hb = bf16.canonicalize_zero(bf16.round_to_bf16(np.maximum(y1, 0.0)))
     np.testing.assert_array_equal(H, Hb)
     np.testing.assert_allclose(Y, _loop_conv(Hb, w2), rtol=1e-15, atol=1e-15)
+
+
+# ----------------------------------------------------------------- self-attention block
+
+def bf16_vals(a):
+    """Round an fp64 array to bf16 values with the oracle's (separately pinned) rounding."""
+    return bf16.round_to_bf16(np.asarray(a, dtype=np.float64))
+
+def test_attention_brute_force_small():
+    """Python loops over every element on a 2-token, 2-head example."""
+    import math
+    rng = np.random.default_rng(21)
+    M, K, N1, N2, head = 2, 3, 4, 5, 2
+    X = bf16_vals(rng.standard_normal((M, K)))
+    W = bf16_vals(0.5 * rng.standard_normal((K, 3 * N1)))
+    W2 = bf16_vals(rng.standard_normal((N1, N2)))
+    xqkv, xdot, y = chains.attention(X, W, W2, head=head)
+    for r in range(M):
+        row = [sum(X[r, k] * W[k, j] for k in range(K)) for j in range(3 * N1)]
+        row = [float(chains.bf16_intermediate(np.array([v]))[0]) for v in row]
+        assert np.allclose(xqkv[r], row, rtol=0, atol=0)
+        for h in range(N1 // head):
+            cols = range(h * head, (h + 1) * head)
+            s = [row[j] * row[N1 + j] for j in cols]
+            mx = max(s)
+            e = [math.exp(v - mx) for v in s]
+            for t, j in enumerate(cols):
+                want = float(chains.bf16_intermediate(np.array([e[t] / sum(e) * row[2 * N1 + j]]))[0])
+                assert xdot[r, j] == want
+        for o in range(N2):
+            assert y[r, o] == pytest.approx(sum(xdot[r, j] * W2[j, o] for j in range(N1)), rel=1e-12, abs=1e-12)
+
+
+def test_attention_uniform_softmax_when_q_is_zero():
+    """XQ = 0 makes every product 0, so each head's softmax is uniform: XDot = XK / head."""
+    rng = np.random.default_rng(22)
+    M, K, N1, head = 3, 8, 256, 128
+    X = bf16_vals(rng.standard_normal((M, K)))
+    W = bf16_vals(0.1 * rng.standard_normal((K, 3 * N1)))
+    W[:, :N1] = 0.0
+    xqkv, xdot, _ = chains.attention(X, W, np.eye(N1), head=head)
+    assert np.array_equal(xdot, chains.bf16_intermediate(xqkv[:, 2 * N1:] / head))
+
+
+def test_softmax_heads_sums_and_shift():
+    rng = np.random.default_rng(23)
+    s = rng.standard_normal((4, 512)) * 3
+    p = chains.softmax_heads(s, 128)
+    assert np.allclose(p.reshape(4, 4, 128).sum(axis=2), 1.0, rtol=0, atol=1e-12)
+    shift = np.repeat(rng.standard_normal((4, 4)), 128, axis=1)
+    assert np.allclose(chains.softmax_heads(s + shift, 128), p, rtol=0, atol=1e-12)

@@ -17,7 +17,7 @@ c_i32, c_i64, c_u32, c_u64, c_dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_uin
 
 # ---------------------------------------------------------------- enums (cusync.h)
 POLICY_STREAM, POLICY_ROW, POLICY_TILE, POLICY_STRIDED_TILE, POLICY_SENTINEL, POLICY_AUTO = range(6)
-CHAIN_MLP_GELU, CHAIN_MLP_SWIGLU, CHAIN_CONV_RELU = range(3)
+CHAIN_MLP_GELU, CHAIN_MLP_SWIGLU, CHAIN_CONV_RELU, CHAIN_ATTENTION = range(4)
 LAUNCH_PERSISTENT, LAUNCH_PDL = range(2)
 (OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NOMEM, ERR_TIMEOUT, ERR_DEVICE) = range(7)
 FLAG_NO_REORDER = 1 << 0
@@ -61,6 +61,8 @@ class cusync_chain_info_t(ctypes.Structure):
         ("strided_group", c_i32), ("strided_distance", c_i32), ("num_flags", c_i32),
         ("grid", c_i32 * 2), ("num_sms", c_i32), ("conv_rows_per_tile", c_i32), ("cta_pair", c_i32),
         ("policy", c_i32), ("ksplit", c_i32), ("kb_per_split", c_i32),
+        ("nst", c_i32), ("m_tiles2", c_i32), ("n_tiles2", c_i32), ("k_blocks2", c_i32), ("n_out2", c_i32),
+        ("grid2", c_i32), ("num_flags_pw", c_i32), ("strided_group_pw", c_i32), ("strided_distance_pw", c_i32),
     ]
 
 
@@ -82,12 +84,15 @@ _SIGNATURES = {
     "cusync_create_chain": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), ctypes.POINTER(_VP)]),
     "cusync_run_mlp": (c_i32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "cusync_run_conv_chain": (c_i32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "cusync_run_attention": (c_i32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "cusync_chain_check": (c_i32, [_VP, _VP, ctypes.POINTER(c_u32), ctypes.POINTER(c_u32)]),
     "cusync_chain_reset": (c_i32, [_VP, _VP]),
     "cusync_plan_info": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), ctypes.POINTER(cusync_chain_info_t)]),
     "cusync_consumer_waits": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), c_i32, ctypes.POINTER(c_i32),
                                       ctypes.POINTER(c_i32), ctypes.POINTER(c_u32), c_i32, ctypes.POINTER(c_i32)]),
     "cusync_producer_flag": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), c_i32, c_i32, ctypes.POINTER(c_i32)]),
+    "cusync_pointwise_waits": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), c_i32, c_i32, ctypes.POINTER(c_i32),
+                                       ctypes.POINTER(c_u32), c_i32, ctypes.POINTER(c_i32)]),
     "cusync_producer_col": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), c_i32, ctypes.POINTER(c_i32)]),
     "cusync_tile_at": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), c_i32, c_i32, ctypes.POINTER(c_i32),
                                ctypes.POINTER(c_i32)]),
@@ -206,6 +211,15 @@ def cusync_predict_policies(desc, model=None):
     return r
 
 
+def cusync_pointwise_waits(desc, m_tile, head):
+    fl = (c_i32 * 3)()
+    pr = (c_u32 * 3)()
+    n = c_i32()
+    _check(load().cusync_pointwise_waits(ctypes.byref(desc), m_tile, head, fl, pr, 3, ctypes.byref(n)),
+           "cusync_pointwise_waits")
+    return [(fl[i], pr[i]) for i in range(n.value)]
+
+
 def cusync_consumer_waits(desc, m_tile, max_entries=4096):
     kb = (c_i32 * max_entries)()
     fl = (c_i32 * max_entries)()
@@ -250,6 +264,11 @@ def cusync_run_mlp(chain, X, W1t, W2t, H, Y, stream=None):
 def cusync_run_conv_chain(chain, x, w1, w2, y1, y2, stream=None):
     _check(load().cusync_run_conv_chain(chain, _ptr(x), _ptr(w1), _ptr(w2), _ptr(y1), _ptr(y2), _stream(stream)),
            "cusync_run_conv_chain")
+
+
+def cusync_run_attention(chain, X, Wqkv_t, W2t, XQKV, XDot, Y, stream=None):
+    _check(load().cusync_run_attention(chain, _ptr(X), _ptr(Wqkv_t), _ptr(W2t), _ptr(XQKV), _ptr(XDot), _ptr(Y),
+                                       _stream(stream)), "cusync_run_attention")
 
 
 def cusync_run_mlp_noalloc(desc, X, W1t, W2t, H, Y, stream=None, wait=False):
@@ -297,9 +316,12 @@ class Chain:
         self.desc = desc
         self.handle = cusync_create_chain(desc)
 
-    def run(self, a, w1, w2, h, y, stream=None):
+    def run(self, a, w1, w2, h, y, stream=None, h2=None):
+        """Run the chain; h2 is the second intermediate (XDot) of an attention chain."""
         if self.desc.kind == CHAIN_CONV_RELU:
             cusync_run_conv_chain(self.handle, a, w1, w2, h, y, stream)
+        elif self.desc.kind == CHAIN_ATTENTION:
+            cusync_run_attention(self.handle, a, w1, w2, h, h2, y, stream)
         else:
             cusync_run_mlp(self.handle, a, w1, w2, h, y, stream)
 

@@ -51,7 +51,8 @@
 namespace cusync {
 
 // Control words in front of the semaphore array.
-enum : int { CTRL_ERR = 0, CTRL_ERR_DETAIL = 1, CTRL_COUNTER = 2, CTRL_EXIT = 4, CTRL_RUNS = 6, CTRL_WORDS = 16 };
+// Tile counters and exit counters: one per launch of a chain run (queue 0..2).
+enum : int { CTRL_ERR = 0, CTRL_ERR_DETAIL = 1, CTRL_COUNTER = 2, CTRL_EXIT = 5, CTRL_RUNS = 8, CTRL_WORDS = 16 };
 // Error classes (bits 31..24 of the error word; bits 23..0 hold the tile index).
 enum : uint32_t { ERRC_FLAG_TIMEOUT = 1, ERRC_SENTINEL_TIMEOUT = 2, ERRC_PIPELINE = 3 };
 // Flag bits shared with cusync.h.
@@ -79,9 +80,11 @@ struct TraceRec {
 };
 
 struct ChainArgs {
-  StageArgs st[2];       // 0 = producer, 1 = consumer
-  DepCfg dep;
-  uint32_t* flags;       // semaphores
+  StageArgs st[3];       // 0 = producer, nst - 1 = the GEMM consumer (attention: 1 = pointwise)
+  DepCfg dep;            // what the last stage waits for on the stage before it
+  DepCfg dep_pw;         // attention: what the pointwise stage waits for on stage 0
+  uint32_t* flags;       // semaphores of `dep`
+  uint32_t* flags_pw;    // semaphores of `dep_pw`
   uint32_t* ctrl;        // CTRL_* words
   TraceRec* trace;       // per-tile timeline, or null
   float* split_ws;       // K split: fp32 partial sums, per (tile, pair rank) ksplit-1 slots of 128 x BN
@@ -89,9 +92,10 @@ struct ChainArgs {
   int32_t queue;         // tile counter slot used by this launch
   int32_t first_stage;   // stages served by this launch: [first_stage, last_stage]
   int32_t last_stage;
-  int32_t tiles0, tiles1;
+  int32_t tiles0, tiles1, tiles2;
+  int32_t nst;           // stages in the chain: 2, or 3 (attention)
   uint32_t flags_bits;
-  int32_t pdl_role;      // 1: trigger dependents at start; 2: wait on the primary at exit
+  int32_t pdl_role;      // bit 0: trigger dependents at start; bit 1: wait on the primary at exit
   int32_t sentinel_check;
   int32_t num_flags;     // semaphores in `flags`
   int32_t l2_prefetch;   // k-blocks the prefetch warp runs ahead of the loader (0: none)
@@ -125,16 +129,13 @@ struct TileRef {
 };
 
 __device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
-  int32_t s, u;
-  if (a.first_stage == a.last_stage) {
-    s = a.first_stage;
-    u = t;
-  } else if (t < a.tiles0) {
-    s = 0;
-    u = t;
-  } else {
-    s = 1;
-    u = t - a.tiles0;
+  // the launch serves stages [first_stage, last_stage], their work units in that order
+  int32_t s = a.first_stage, u = t;
+  while (s < a.last_stage) {
+    const int32_t n = s == 0 ? a.tiles0 : (s == 1 ? a.tiles1 : a.tiles2);
+    if (u < n) break;
+    u -= n;
+    ++s;
   }
   const StageGeo& g = a.st[s].g;
   int32_t ks = 0, kb0 = 0, nkb = g.k_blocks;
@@ -146,13 +147,15 @@ __device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
   }
   int32_t m, y;
   tile_at(g, u, &m, &y);
-  const int32_t c = (s == 0) ? producer_col(a.dep, y) : y;
+  // StridedSync's producer order applies to the stage whose semaphores it groups
+  const DepCfg& pd = (a.nst == 3) ? a.dep_pw : a.dep;
+  const int32_t c = (s == 0) ? producer_col(pd, y) : y;
   return TileRef{s, m, c, ks, kb0, nkb};
 }
 
 // Index of queue position t in the chain's tile numbering (producer tiles first).
 __device__ __forceinline__ int32_t chain_tile(const ChainArgs& a, int32_t t) {
-  return a.first_stage == 1 ? a.tiles0 + t : t;
+  return t + (a.first_stage >= 1 ? a.tiles0 : 0) + (a.first_stage >= 2 ? a.tiles1 : 0);
 }
 
 __device__ __forceinline__ uint32_t a_tile_bytes(const StageGeo& g) {
@@ -267,6 +270,92 @@ __device__ __forceinline__ float silu_f(float g) {
   return fmaf(h, tanh_approx(h), h);
 }
 
+// Attention chain, pointwise tile (m, head i), run by the 128 epilogue threads (one token
+// row each): once the QKV GEMM's tiles it reads are posted (cuSync §IV-E waits on the
+// semaphores of the policy -- StridedSync groups a head's three Q/V/K tiles), each thread
+// computes s_j = q_j v_j over the head's kHead columns, p = softmax(s) over the head, and
+// XDot_j = p_j k_j ("A Framework for Fine-Grained Synchronization of Dependent GPU
+// Kernels", Fig. fig:gpt-3:attention, fused dot-product kernel; dropout is the identity
+// of inference).  Two passes over the row: an online maximum and sum of exponentials,
+// then the outputs.  Then cuSync §IV-E "Post" for the GEMM that reads XDot.
+__device__ __noinline__ void pointwise_tile(const ChainArgs& args, const TileRef& tr, int32_t t, int row,
+                                            uint64_t* pw_done, uint32_t pw_parity, uint32_t runs, bool leader,
+                                            uint64_t pto, volatile int32_t* abort_flag) {
+  const StageArgs& SA = args.st[tr.s];
+  const StageGeo& g = SA.g;
+  Wait w[3];
+  const int nw = pointwise_waits(args.dep_pw, tr.m, tr.c, w);
+  for (int i = 0; i < nw; ++i) {
+    const uint32_t target = runs * w[i].per_run;
+    const uint64_t t0 = ptx::globaltimer();
+    while ((int32_t)(ptx::ld_acquire_gpu(args.flags_pw + w[i].flag) - target) < 0) {
+      __nanosleep(64);
+      if (ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u) break;
+      if (ptx::globaltimer() - t0 > args.timeout_ns) {
+        record_error(args, ERRC_FLAG_TIMEOUT, t, w[i].flag & 0xFFFF);
+        break;
+      }
+    }
+  }
+  const int64_t grow = (int64_t)tr.m * 128 + row;
+  if (grow < g.M) {
+    const int32_t n1 = g.N;
+    const uint16_t* xr = SA.a_ptr + grow * (int64_t)g.K + (int64_t)tr.c * kHead;  // XQKV row: Q | V | K
+    const uint4* qp = reinterpret_cast<const uint4*>(xr);
+    const uint4* vp = reinterpret_cast<const uint4*>(xr + n1);
+    const uint4* kp = reinterpret_cast<const uint4*>(xr + 2 * n1);
+    auto lo = [](uint32_t x) { return __uint_as_float(x << 16); };
+    auto hi = [](uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); };
+    float mx = -INFINITY, sum = 0.0f;
+    for (int j = 0; j < kHead / 8; ++j) {
+      const uint4 a = __ldcg(qp + j), b = __ldcg(vp + j);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float sv = (e & 1) ? hi(av[e / 2]) * hi(bv[e / 2]) : lo(av[e / 2]) * lo(bv[e / 2]);
+        if (sv > mx) {
+          sum = sum * __expf(mx - sv) + 1.0f;
+          mx = sv;
+        } else {
+          sum += __expf(sv - mx);
+        }
+      }
+    }
+    const float inv = 1.0f / sum;
+    __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(SA.out) + grow * (int64_t)n1 + (int64_t)tr.c * kHead;
+    for (int j = 0; j < kHead / 8; ++j) {
+      const uint4 a = __ldcg(qp + j), b = __ldcg(vp + j), c = __ldcg(kp + j);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w}, cv[4] = {c.x, c.y, c.z, c.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p0 = __expf(lo(av[e]) * lo(bv[e]) - mx) * inv;
+        const float p1 = __expf(hi(av[e]) * hi(bv[e]) - mx) * inv;
+        o[e] = pack_bf16x2(p0 * lo(cv[e]), p1 * hi(cv[e]));
+      }
+      ptx::st_relaxed_gpu_b128(orow + j * 8, o[0], o[1], o[2], o[3]);
+    }
+  }
+  ptx::mbar_arrive(pw_done);
+  if (threadIdx.x == 64) {
+    if (!ptx::mbar_wait_bounded(pw_done, pw_parity, pto)) {
+      record_error(args, ERRC_PIPELINE, t, 8);
+      *abort_flag = 1;
+    } else {
+      const int32_t flag = producer_flag(args.dep, tr.m, tr.c);
+      if (flag >= 0) {
+        ptx::fence_acq_rel_gpu();
+        ptx::red_release_gpu_add(args.flags + flag, 1u);
+      }
+      if (args.trace && leader) {
+        args.trace[chain_tile(args, t)].t_epi = ptx::globaltimer();
+        args.trace[chain_tile(args, t)].t_post = ptx::globaltimer();
+      }
+    }
+  }
+  __syncwarp();
+}
+
 // Bounded waits on barriers that may receive arrivals from the other CTA of a pair use
 // cluster-scope acquire.
 template <int PAIR>
@@ -295,7 +384,8 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
   uint64_t* qfull = epi_done + 2;         // [slots] tile index published
   uint64_t* qempty = qfull + C::kSlots;   // [slots] tile index consumed (leader in a pair)
   uint64_t* mma_done = qempty + C::kSlots;
-  int32_t* qtile = reinterpret_cast<int32_t*>(mma_done + 1);
+  uint64_t* pw_done = mma_done + 1;       // attention: all epilogue threads stored a pointwise tile
+  int32_t* qtile = reinterpret_cast<int32_t*>(pw_done + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qtile + C::kSlots);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   volatile int32_t* it_issued = abort_flag + 1;
@@ -314,9 +404,9 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
   // on the leader's `full` barriers, which count the bytes of both CTAs.  A consumer tile
   // under the sentinel policy is not: each CTA's copies complete locally, its checker
   // validates them and arrives on the leader's `ready` barrier.
-  auto direct_tile = [&](const TileRef& tr) { return kPair && !(args.sentinel_check && tr.s == 1); };
+  auto direct_tile = [&](const TileRef& tr) { return kPair && !(args.sentinel_check && tr.s == args.nst - 1); };
 
-  if (args.pdl_role == 1) ptx::pdl_launch_dependents();
+  if (args.pdl_role & 1) ptx::pdl_launch_dependents();
   // Run number of this launch.  Semaphores count up across runs (run r waits for r times
   // the posts of one run), and the count of finished runs lives in device memory, so the
   // same launch can be replayed from a CUDA graph.  Read before the first barrier: the
@@ -342,6 +432,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
         ptx::mbar_init(&qempty[i], kPair ? 6 + 7 : 6);
       }
       ptx::mbar_init(mma_done, 1);
+      ptx::mbar_init(pw_done, 128);
       *abort_flag = 0;
       *it_issued = 0;
       *progress = 0;
@@ -371,8 +462,8 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int32_t total = (args.first_stage == args.last_stage) ? (args.first_stage == 0 ? args.tiles0 : args.tiles1)
-                                                              : args.tiles0 + args.tiles1;
+  int32_t total = 0;
+  for (int s = args.first_stage; s <= args.last_stage; ++s) total += s == 0 ? args.tiles0 : (s == 1 ? args.tiles1 : args.tiles2);
   const uint64_t pto = args.pipe_timeout_ns;
 
   // Arrive on "consumed" for ring slot `slot` (the leader's barrier in a pair).
@@ -441,7 +532,8 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
           trec->t_claim = ptx::globaltimer();
           trec->t_post = 0;
         }
-        const bool cons = (tr.s == 1);
+        if (SA.g.a_mode == AMODE_POINTWISE) continue;  // computed by the epilogue warps; nothing to load
+        const bool cons = (tr.s == args.nst - 1);
         GemmDepTracker gdt;
         gdt.reset();
         ConvDepTracker cdt;  // touched (stack arrays) only by convolution tiles
@@ -636,7 +728,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
           atomicExch(args.ctrl + CTRL_COUNTER + args.queue, 0u);
           atomicExch(args.ctrl + CTRL_EXIT + args.queue, 0u);
           // Every CTA of the launch that serves the consumer has read the run number by now.
-          if (args.last_stage == 1) {
+          if (args.last_stage == args.nst - 1) {
             __threadfence();
             atomicAdd(args.ctrl + CTRL_RUNS, 1u);
           }
@@ -667,6 +759,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       if (t < 0) break;
       const TileRef tr = decode_tile(args, t);
       const StageGeo& g = args.st[tr.s].g;
+      if (g.a_mode == AMODE_POINTWISE) continue;  // no MMA
       const int acc = acount & 1;
       const uint32_t apar = ((acount >> 1) & 1u) ^ 1u;
       ++acount;
@@ -678,7 +771,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
         ptx::tc_fence_after();
       }
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-      const bool check = args.sentinel_check && tr.s == 1;
+      const bool check = args.sentinel_check && tr.s == args.nst - 1;
       const bool direct = direct_tile(tr);
       const bool to_leader = direct && !leader;
       const uint32_t abytes = a_tile_bytes(g);
@@ -893,7 +986,10 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
-    uint32_t tcount = 0, acount = 0;
+    uint32_t tcount = 0, acount = 0, pwcount = 0;  // pwcount: pointwise tiles done
+    // Attention chain: a pointwise tile (see pointwise_tile) -- out of line, so that its
+    // registers do not weigh on the GEMM epilogue.
+
     while (true) {
       const int slot = tcount % C::kSlots;
       if (!xwait<PAIR>(&qfull[slot], (tcount / C::kSlots) & 1u, pto)) break;
@@ -905,6 +1001,11 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       const TileRef tr = decode_tile(args, t);
       const StageArgs& SA = args.st[tr.s];
       const StageGeo& g = SA.g;
+      if (g.a_mode == AMODE_POINTWISE) {
+        pointwise_tile(args, tr, t, row, pw_done, pwcount & 1u, *run_no, leader, pto, abort_flag);
+        ++pwcount;
+        continue;
+      }
       const int acc = acount & 1;
       const uint32_t apar = (acount >> 1) & 1u;
       ++acount;
@@ -1109,7 +1210,10 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
           ptx::red_release_gpu_add(args.split_turn + tile_id, 1u);
         }
       } else if (tr.s == 0 && threadIdx.x == 64) {
-        const int32_t flag = producer_flag(args.dep, tr.m, tr.c);
+        // stage 0 feeds the last stage (two-stage chains) or the pointwise stage (attention)
+        const bool to_pw = args.nst == 3;
+        const int32_t flag = producer_flag(to_pw ? args.dep_pw : args.dep, tr.m, tr.c);
+        uint32_t* const fl = to_pw ? args.flags_pw : args.flags;
         if (flag >= 0) {
           // cuSync §IV-E "Post": after all of this CTA's stores of the tile (the epi_done
           // barrier orders its 128 threads' stores before this thread), one device-scope
@@ -1119,7 +1223,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
             *abort_flag = 1;
           } else if (!((args.flags_bits & kDebugSkipPost) && tr.m == 0 && tr.c == 0)) {
             ptx::fence_acq_rel_gpu();
-            ptx::red_release_gpu_add(args.flags + flag, 1u);
+            ptx::red_release_gpu_add(fl + flag, 1u);
             if (args.trace && leader) args.trace[chain_tile(args, t)].t_post = ptx::globaltimer();
           }
         }
@@ -1136,7 +1240,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
     if (kPair) ptx::tmem_dealloc_pair(tmem_base, C::kTmemCols);
     else ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
-  if (args.pdl_role == 2 && threadIdx.x == 0) ptx::pdl_wait();
+  if ((args.pdl_role & 2) && threadIdx.x == 0) ptx::pdl_wait();
 }
 
 // Fill a buffer with the bf16 sentinel 0x8000 using 16-byte stores (CUDA-FGS §4.6.4.2,

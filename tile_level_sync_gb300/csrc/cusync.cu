@@ -55,14 +55,17 @@ cusync_status_t cuda_fail(cudaError_t e, const char* what) {
 struct Plan {
   int32_t bn;           // accumulator tile width (UMMA N)
   int32_t pair;         // CTAs per tile: 1, or 2 (a CTA pair computing a 256-row tile)
-  StageGeo geo[2];
-  DepCfg dep;
+  int32_t nst;          // stages: 2, or 3 (attention: QKV GEMM, pointwise, output GEMM)
+  StageGeo geo[3];
+  DepCfg dep;           // the last stage's waits on the stage before it
+  DepCfg dep_pw;        // attention: the pointwise stage's waits on the QKV GEMM
   int64_t num_flags;
+  int64_t num_flags_pw;
   int64_t split_rows;   // K split: workspace row blocks (producer tiles x pair), else 0
 };
 
 // Words of a chain's device state: control words, semaphores, K-split turn counters.
-int64_t state_words(const Plan& p) { return CTRL_WORDS + p.num_flags + p.split_rows; }
+int64_t state_words(const Plan& p) { return CTRL_WORDS + p.num_flags + p.num_flags_pw + p.split_rows; }
 // fp32 elements of the K-split workspace: ksplit - 1 slots of a 128-row accumulator per
 // row block.
 int64_t split_ws_floats(const Plan& p) {
@@ -88,7 +91,7 @@ cusync_status_t resolve_auto(const cusync_chain_desc_t& d, cusync_chain_desc_t* 
 int query_num_sms(int32_t requested, int* out);
 
 cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
-  if (d.kind < CUSYNC_CHAIN_MLP_GELU || d.kind > CUSYNC_CHAIN_CONV_RELU) return CUSYNC_ERR_INVALID_ARG;
+  if (d.kind < CUSYNC_CHAIN_MLP_GELU || d.kind > CUSYNC_CHAIN_ATTENTION) return CUSYNC_ERR_INVALID_ARG;
   if (d.policy == CUSYNC_POLICY_AUTO) {
     cusync_chain_desc_t r;
     cusync_status_t st = resolve_auto(d, &r);
@@ -99,6 +102,7 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   const int32_t bn = default_tile_n(d);
   if (bn != 128 && bn != 256) return CUSYNC_ERR_UNSUPPORTED;
   const bool mlp = d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
+  const bool attn = d.kind == CUSYNC_CHAIN_ATTENTION;
   // CTA pairs (cta_group::2, 256-row tiles) for MLP chains with at least 512 tokens,
   // where they measured faster on GB300; single-CTA 128-row tiles otherwise.
   const int32_t pair = d.cta_pair ? d.cta_pair : ((mlp && d.M >= 512) ? 2 : 1);
@@ -109,7 +113,41 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   p->pair = pair;
   StageGeo& g0 = p->geo[0];
   StageGeo& g1 = p->geo[1];
-  if (d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU) {
+  StageGeo& g2 = p->geo[2];
+  p->nst = attn ? 3 : 2;
+  if (attn) {
+    // "A Framework for Fine-Grained Synchronization of Dependent GPU Kernels",
+    // Fig. fig:gpt-3:attention: XQKV = X x QKV (one GEMM for the three blocks), the
+    // pointwise dot-product kernel per head, XW2 = XDot x W2.
+    if (d.M < 1 || d.K < 1 || d.N1 < 1 || d.N2 < 1) return CUSYNC_ERR_INVALID_ARG;
+    if (d.K % 8 || d.N2 % 8 || d.N1 % bn || d.N1 % kHead) return CUSYNC_ERR_UNSUPPORTED;
+    if (d.policy == CUSYNC_POLICY_SENTINEL) return CUSYNC_ERR_UNSUPPORTED;
+    if (d.M > (1ll << 30) || d.K > (1ll << 30) || 3 * d.N1 > (1ll << 30) || d.N2 > (1ll << 30))
+      return CUSYNC_ERR_UNSUPPORTED;
+    g0.a_mode = AMODE_GEMM;
+    g0.epi = EPI_NONE;
+    g0.M = (int32_t)d.M;
+    g0.N = (int32_t)(3 * d.N1);
+    g0.K = (int32_t)d.K;
+    g0.n_out = bn;
+    g1.a_mode = AMODE_POINTWISE;
+    g1.epi = EPI_NONE;
+    g1.M = (int32_t)d.M;
+    g1.N = (int32_t)d.N1;
+    g1.K = (int32_t)(3 * d.N1);  // row length of the XQKV input
+    g1.n_out = kHead;
+    g2.a_mode = AMODE_GEMM;
+    g2.epi = EPI_NONE;
+    g2.M = (int32_t)d.M;
+    g2.N = (int32_t)d.N2;
+    g2.K = (int32_t)d.N1;
+    g2.n_out = bn;
+    for (StageGeo* g : {&g0, &g1, &g2}) {
+      g->m_tiles = (int32_t)ceil_div(g->M, (int64_t)kBM * pair);
+      g->n_tiles = (int32_t)ceil_div(g->N, g->n_out);
+      g->k_blocks = g->a_mode == AMODE_POINTWISE ? 0 : (int32_t)ceil_div(g->K, kBK);
+    }
+  } else if (d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU) {
     if (d.M < 1 || d.K < 1 || d.N1 < 1 || d.N2 < 1) return CUSYNC_ERR_INVALID_ARG;
     // TMA row strides and 16-byte output chunks need multiples of 8 bf16 elements.
     if (d.K % 8 || d.N1 % 8 || d.N2 % 8) return CUSYNC_ERR_UNSUPPORTED;
@@ -165,12 +203,13 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   const int32_t raster = d.raster_rows > 0 ? d.raster_rows : 1;
   g0.raster = raster < g0.m_tiles ? raster : g0.m_tiles;
   g1.raster = raster < g1.m_tiles ? raster : g1.m_tiles;
+  g2.raster = raster < g2.m_tiles ? raster : g2.m_tiles;
   // K split of the producer GEMM (see cusync_chain_desc_t::ksplit)
   if (d.ksplit < 0 || d.ksplit > 16) return CUSYNC_ERR_INVALID_ARG;
   int32_t ks = d.ksplit;
   if (ks == 0) {
     ks = 1;
-    if (mlp) {
+    if (mlp || attn) {
       int sms = 0;
       if (query_num_sms(d.num_sms, &sms) != 0) sms = 148;
       // Producer tiles that fill at most half of a wave: as many units per tile as fit in
@@ -185,14 +224,48 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
       ks = (int32_t)std::max<int64_t>(1, std::min<int64_t>(want, g0.k_blocks / 16));
     }
   }
-  if (ks > 1 && !mlp) return CUSYNC_ERR_UNSUPPORTED;
+  if (ks > 1 && !mlp && !attn) return CUSYNC_ERR_UNSUPPORTED;
   if (ks > g0.k_blocks) return CUSYNC_ERR_UNSUPPORTED;
   g0.ksplit = ks;
   g0.kb_per_split = (int32_t)ceil_div(g0.k_blocks, ks);
   g0.ksplit = (int32_t)ceil_div(g0.k_blocks, g0.kb_per_split);  // no empty unit
   g1.ksplit = 1;
   g1.kb_per_split = g1.k_blocks;
+  g2.ksplit = 1;
+  g2.kb_per_split = g2.k_blocks;
   if (d.l2_prefetch < -1 || d.l2_prefetch > 64) return CUSYNC_ERR_INVALID_ARG;
+  if (attn) {
+    // the pointwise stage waits on the QKV GEMM: StridedSync with G = 3 (the Q, V and K
+    // tiles of a head share one semaphore), or RowSync / TileSync; the output GEMM waits on
+    // the pointwise stage: TileSync (also under StridedSync, as in the pages'
+    // Strided+TileSync), or RowSync
+    DepCfg& dp = p->dep_pw;
+    dp.policy = d.policy;
+    dp.prod_m_tiles = g0.m_tiles;
+    dp.prod_n_tiles = g0.n_tiles;
+    dp.prod_n_out = g0.n_out;
+    dp.G = 1;
+    dp.D = g0.n_tiles;
+    dp.posts = pair;
+    if (d.policy == CUSYNC_POLICY_STRIDED_TILE) {
+      if (g0.n_tiles % 3) return CUSYNC_ERR_UNSUPPORTED;
+      dp.G = 3;
+      dp.D = g0.n_tiles / 3;
+    }
+    DepCfg& dep = p->dep;
+    dep.policy = d.policy == CUSYNC_POLICY_STRIDED_TILE ? CUSYNC_POLICY_TILE : d.policy;
+    dep.prod_m_tiles = g1.m_tiles;
+    dep.prod_n_tiles = g1.n_tiles;
+    dep.prod_n_out = g1.n_out;
+    dep.G = 1;
+    dep.D = g1.n_tiles;
+    dep.posts = 1;
+    p->num_flags = num_flags(dep);
+    p->num_flags_pw = num_flags(dp);
+    if (p->num_flags + p->num_flags_pw > (1ll << 24)) return CUSYNC_ERR_UNSUPPORTED;
+    p->split_rows = g0.ksplit > 1 ? (int64_t)g0.m_tiles * g0.n_tiles * pair : 0;
+    return CUSYNC_OK;
+  }
   DepCfg& dep = p->dep;
   dep.policy = d.policy;
   dep.prod_m_tiles = g0.m_tiles;
@@ -315,23 +388,20 @@ int max_pair_clusters() {
 
 // Grid sizes (CTAs) of the fused launch and of the two separate launches.
 struct Grids {
-  int32_t fused, prod, cons;
+  int32_t fused;     // the one persistent launch of all stages
+  int32_t stage[3];  // one launch per stage (stream order or programmatic dependent launch)
 };
 
 Grids make_grids(const Plan& p, int sms, int max_clusters) {
-  const int64_t t0 = stage_units(p.geo[0]);
-  const int64_t t1 = stage_units(p.geo[1]);
+  int64_t t[3] = {0, 0, 0}, total = 0;
+  for (int s = 0; s < p.nst; ++s) total += (t[s] = stage_units(p.geo[s]));
+  // one tile per CTA, or per CTA pair (cluster of two) resident at once
+  const int64_t slots = p.pair == 2 ? std::max<int64_t>(1, std::min<int64_t>(sms / 2, max_clusters > 0 ? max_clusters
+                                                                                                       : sms / 2))
+                                    : sms;
   Grids g;
-  if (p.pair == 2) {
-    const int64_t cl = std::max<int64_t>(1, std::min<int64_t>(sms / 2, max_clusters > 0 ? max_clusters : sms / 2));
-    g.fused = (int32_t)(2 * std::min<int64_t>(cl, t0 + t1));
-    g.prod = (int32_t)(2 * std::min<int64_t>(cl, t0));
-    g.cons = (int32_t)(2 * std::min<int64_t>(cl, t1));
-  } else {
-    g.fused = (int32_t)std::min<int64_t>(sms, t0 + t1);
-    g.prod = (int32_t)std::min<int64_t>(sms, t0);
-    g.cons = (int32_t)std::min<int64_t>(sms, t1);
-  }
+  g.fused = (int32_t)(p.pair * std::min<int64_t>(slots, total));
+  for (int s = 0; s < 3; ++s) g.stage[s] = (int32_t)(p.pair * std::min<int64_t>(slots, t[s]));
   return g;
 }
 
@@ -384,7 +454,7 @@ void predict_all(const cusync_chain_desc_t& d, const cusync_latency_model_t* mod
     cusync_chain_desc_t c = d;
     c.policy = (cusync_policy_t)pol;
     Plan q;
-    if (make_plan(c, &q) != CUSYNC_OK) {
+    if (make_plan(c, &q) != CUSYNC_OK || q.nst != 2) {  // the model covers two-stage chains
       us[pol] = -1.0;
       continue;
     }
@@ -397,8 +467,8 @@ void predict_all(const cusync_chain_desc_t& d, const cusync_latency_model_t* mod
     mc.geo[1] = q.geo[1];
     mc.dep = q.dep;
     mc.slots_fused = g.fused / q.pair;
-    mc.slots[0] = g.prod / q.pair;
-    mc.slots[1] = g.cons / q.pair;
+    mc.slots[0] = g.stage[0] / q.pair;
+    mc.slots[1] = g.stage[1] / q.pair;
     mc.h_mb = (double)q.geo[0].M * (double)q.geo[0].N * 2.0 / 1e6;
     us[pol] = predict_chain_ns(mc, lm) / 1000.0;
   }
@@ -435,7 +505,7 @@ struct cusync_chain {
   TraceRec* trace;       // per-tile timeline (CUSYNC_FLAG_TRACE), or null
   Grids grids;
   // TMA descriptors cached by operand pointers
-  const void* cached[5];
+  const void* cached[6];
   bool maps_valid;
   ChainArgs args;
 };
@@ -501,38 +571,57 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
     sentinel_fill_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<uint4*>(h), n16);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "sentinel fill launch");
   }
-  const bool two_kernels = d.policy == CUSYNC_POLICY_STREAM || d.launch == CUSYNC_LAUNCH_PDL;
-  if (!two_kernels) {
+  const bool per_stage = d.policy == CUSYNC_POLICY_STREAM || d.launch == CUSYNC_LAUNCH_PDL;
+  if (!per_stage) {
     A.queue = 0;
     A.first_stage = 0;
-    A.last_stage = 1;
+    A.last_stage = p.nst - 1;
     A.pdl_role = 0;
     e = launch_any(p, A, g.fused, /*coop=*/true, false, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fused chain launch");
     return CUSYNC_OK;
   }
+  // One launch per stage; with programmatic dependent launch each one after the first is
+  // a secondary of the one before it (triggered at that one's start).
   const bool pdl = d.policy != CUSYNC_POLICY_STREAM;
-  A.queue = 0;
-  A.first_stage = 0;
-  A.last_stage = 0;
-  A.pdl_role = pdl ? 1 : 0;
-  // K-split units wait for the tile's earlier units: the producer CTAs must all be resident.
-  e = launch_any(p, A, g.prod, /*coop=*/p.geo[0].ksplit > 1, false, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "producer launch");
-  A.queue = 1;
-  A.first_stage = 1;
-  A.last_stage = 1;
-  A.pdl_role = pdl ? 2 : 0;
-  e = launch_any(p, A, g.cons, false, pdl, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "consumer launch");
+  for (int s = 0; s < p.nst; ++s) {
+    A.queue = s;
+    A.first_stage = s;
+    A.last_stage = s;
+    A.pdl_role = pdl ? ((s + 1 < p.nst ? 1 : 0) | (s > 0 ? 2 : 0)) : 0;
+    // K-split units of the first stage wait for one another: its CTAs must all be resident.
+    e = launch_any(p, A, g.stage[s], /*coop=*/s == 0 && p.geo[0].ksplit > 1, /*pdl2=*/pdl && s > 0, stream);
+    if (e != cudaSuccess) return cuda_fail(e, s == 0 ? "producer launch" : "consumer launch");
+  }
   return CUSYNC_OK;
 }
 
 // TMA descriptors of a run: 2-D maps for GEMM operands, 4-D NHWC maps for conv images.
 bool encode_maps(const cusync_chain_desc_t& d, const Plan& p, ChainArgs& A, const void* a0, const void* b0,
-                 const void* b1, const void* h, const void* y) {
+                 const void* b1, const void* h, const void* y, const void* h2 = nullptr) {
   bool ok = true;
-  if (d.kind == CUSYNC_CHAIN_CONV_RELU) {
+  if (d.kind == CUSYNC_CHAIN_ATTENTION) {
+    // stage 0: XQKV = X x QKV; stage 1 reads XQKV and writes XDot (no maps);
+    // stage 2: Y = XDot x W2
+    const uint64_t n3 = (uint64_t)(3 * d.N1);
+    A.st[0].a_ptr = static_cast<const uint16_t*>(a0);
+    A.st[0].a_rows = (int32_t)d.M;
+    A.st[0].b_ptr = static_cast<const uint16_t*>(b0);
+    A.st[0].b_rows = (int32_t)n3;
+    A.st[1].a_ptr = static_cast<const uint16_t*>(h);
+    A.st[1].a_rows = (int32_t)d.M;
+    A.st[2].a_ptr = static_cast<const uint16_t*>(h2);
+    A.st[2].a_rows = (int32_t)d.M;
+    A.st[2].b_ptr = static_cast<const uint16_t*>(b1);
+    A.st[2].b_rows = (int32_t)d.N2;
+    ok &= h2 != nullptr;
+    ok &= encode_2d(&A.st[0].tmA, a0, (uint64_t)d.M, (uint64_t)d.K, 128u);
+    ok &= encode_2d(&A.st[0].tmB, b0, n3, (uint64_t)d.K, b_box_rows(p, false));
+    ok &= encode_2d(&A.st[0].tmO, h, (uint64_t)d.M, n3, 32u);
+    ok &= encode_2d(&A.st[2].tmA, h2, (uint64_t)d.M, (uint64_t)d.N1, 128u);
+    ok &= encode_2d(&A.st[2].tmB, b1, (uint64_t)d.N2, (uint64_t)d.N1, b_box_rows(p, false));
+    ok &= encode_2d(&A.st[2].tmO, y, (uint64_t)d.M, (uint64_t)d.N2, 32u);
+  } else if (d.kind == CUSYNC_CHAIN_CONV_RELU) {
     const StageGeo& g0 = p.geo[0];
     ok &= encode_nhwc(&A.st[0].tmA, a0, d.n, d.h, d.w, d.c, (uint32_t)g0.th);
     ok &= encode_2d(&A.st[0].tmB, b0, (uint64_t)d.k_out, (uint64_t)9 * d.c, b_box_rows(p, false));
@@ -565,14 +654,19 @@ void fill_static_args(const cusync_chain_desc_t& d, const Plan& p, uint32_t* sta
   const uint64_t timeout = d.timeout_ns ? d.timeout_ns : kDefaultTimeoutNs;
   A.st[0].g = p.geo[0];
   A.st[1].g = p.geo[1];
+  A.st[2].g = p.geo[2];
   A.st[0].b_half_rows = d.kind == CUSYNC_CHAIN_MLP_SWIGLU ? (int32_t)d.N1 : 0;
+  A.nst = p.nst;
   A.dep = p.dep;
+  A.dep_pw = p.dep_pw;
   A.ctrl = state;
   A.flags = state + CTRL_WORDS;
-  A.split_turn = p.split_rows > 0 ? state + CTRL_WORDS + p.num_flags : nullptr;
+  A.flags_pw = state + CTRL_WORDS + p.num_flags;
+  A.split_turn = p.split_rows > 0 ? state + CTRL_WORDS + p.num_flags + p.num_flags_pw : nullptr;
   A.split_ws = split_ws;
   A.tiles0 = (int32_t)t0;
   A.tiles1 = (int32_t)t1;
+  A.tiles2 = (int32_t)stage_units(p.geo[2]);
   A.flags_bits = d.flags;
   A.sentinel_check = d.policy == CUSYNC_POLICY_SENTINEL ? 1 : 0;
   A.num_flags = (int32_t)p.num_flags;
@@ -581,19 +675,20 @@ void fill_static_args(const cusync_chain_desc_t& d, const Plan& p, uint32_t* sta
   A.pipe_timeout_ns = std::max<uint64_t>(4 * timeout, 2000000000ull);
 }
 
-cusync_status_t run_chain(cusync_chain* ch, const void* a0, const void* b0, const void* b1, void* h, void* y,
-                          cudaStream_t stream) {
+cusync_status_t run_chain(cusync_chain* ch, const void* a0, const void* b0, const void* b1, void* h, void* h2,
+                          void* y, cudaStream_t stream) {
   const cusync_chain_desc_t& d = ch->d;
   const Plan& p = ch->plan;
   if (!aligned16(a0) || !aligned16(b0) || !aligned16(b1) || !aligned16(h) || !aligned16(y))
     return CUSYNC_ERR_INVALID_ARG;
   if (h == y || h == a0 || y == a0) return CUSYNC_ERR_INVALID_ARG;
+  if (p.nst == 3 && (!aligned16(h2) || h2 == h || h2 == y || h2 == a0)) return CUSYNC_ERR_INVALID_ARG;
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess || cur != ch->device) return CUSYNC_ERR_INVALID_ARG;
   ChainArgs& A = ch->args;
-  const void* ptrs[5] = {a0, b0, b1, h, y};
+  const void* ptrs[6] = {a0, b0, b1, h, y, h2};
   if (!ch->maps_valid || std::memcmp(ptrs, ch->cached, sizeof(ptrs)) != 0) {
-    if (!encode_maps(d, p, A, a0, b0, b1, h, y)) {
+    if (!encode_maps(d, p, A, a0, b0, b1, h, y, h2)) {
       ch->maps_valid = false;
       return CUSYNC_ERR_INVALID_ARG;
     }
@@ -601,7 +696,8 @@ cusync_status_t run_chain(cusync_chain* ch, const void* a0, const void* b0, cons
     ch->maps_valid = true;
   }
   A.st[0].out = h;
-  A.st[1].out = y;
+  A.st[1].out = p.nst == 3 ? h2 : y;
+  A.st[2].out = p.nst == 3 ? y : nullptr;
   return launch_run(d, p, A, ch->grids, h, ch->num_sms, stream);
 }
 
@@ -721,7 +817,7 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
     return CUSYNC_ERR_NOMEM;
   }
   if (d->flags & CUSYNC_FLAG_TRACE) {
-    const size_t n = (size_t)stage_units(p.geo[0]) + (size_t)stage_units(p.geo[1]);
+    const size_t n = (size_t)stage_units(p.geo[0]) + (size_t)stage_units(p.geo[1]) + (size_t)stage_units(p.geo[2]);
     if (cudaMalloc(&ch->trace, n * sizeof(TraceRec)) != cudaSuccess ||
         cudaMemset(ch->trace, 0, n * sizeof(TraceRec)) != cudaSuccess) {
       if (ch->trace) cudaFree(ch->trace);
@@ -747,14 +843,21 @@ cusync_status_t cusync_run_mlp(cusync_chain_t ch, const void* X, const void* W1t
                                cusync_stream_t stream) {
   if (!ch) return CUSYNC_ERR_INVALID_ARG;
   if (ch->d.kind != CUSYNC_CHAIN_MLP_GELU && ch->d.kind != CUSYNC_CHAIN_MLP_SWIGLU) return CUSYNC_ERR_INVALID_ARG;
-  return run_chain(ch, X, W1t, W2t, H, Y, reinterpret_cast<cudaStream_t>(stream));
+  return run_chain(ch, X, W1t, W2t, H, nullptr, Y, reinterpret_cast<cudaStream_t>(stream));
 }
 
 cusync_status_t cusync_run_conv_chain(cusync_chain_t ch, const void* x, const void* w1, const void* w2, void* y1,
                                       void* y2, cusync_stream_t stream) {
   if (!ch) return CUSYNC_ERR_INVALID_ARG;
   if (ch->d.kind != CUSYNC_CHAIN_CONV_RELU) return CUSYNC_ERR_INVALID_ARG;
-  return run_chain(ch, x, w1, w2, y1, y2, reinterpret_cast<cudaStream_t>(stream));
+  return run_chain(ch, x, w1, w2, y1, nullptr, y2, reinterpret_cast<cudaStream_t>(stream));
+}
+
+cusync_status_t cusync_run_attention(cusync_chain_t ch, const void* X, const void* Wqkv_t, const void* W2t,
+                                     void* XQKV, void* XDot, void* Y, cusync_stream_t stream) {
+  if (!ch) return CUSYNC_ERR_INVALID_ARG;
+  if (ch->d.kind != CUSYNC_CHAIN_ATTENTION) return CUSYNC_ERR_INVALID_ARG;
+  return run_chain(ch, X, Wqkv_t, W2t, XQKV, XDot, Y, reinterpret_cast<cudaStream_t>(stream));
 }
 
 cusync_status_t cusync_chain_reset(cusync_chain_t ch, cusync_stream_t stream) {
@@ -807,14 +910,41 @@ cusync_status_t cusync_plan_info(const cusync_chain_desc_t* d, cusync_chain_info
   out->num_flags = (int32_t)p.num_flags;
   const Grids g = make_grids(p, sms, 0);
   const bool two = p.dep.policy == POL_STREAM || d->launch == CUSYNC_LAUNCH_PDL;
-  out->grid[0] = two ? g.prod : g.fused;
-  out->grid[1] = two ? g.cons : 0;
+  out->grid[0] = two ? g.stage[0] : g.fused;
+  out->grid[1] = two ? g.stage[1] : 0;
+  out->grid2 = two ? g.stage[2] : 0;
   out->cta_pair = p.pair;
   out->num_sms = sms;
   out->conv_rows_per_tile = d->kind == CUSYNC_CHAIN_CONV_RELU ? p.geo[0].th : 0;
-  out->policy = p.dep.policy;
+  out->policy = p.nst == 3 ? p.dep_pw.policy : p.dep.policy;
   out->ksplit = p.geo[0].ksplit;
   out->kb_per_split = p.geo[0].kb_per_split;
+  out->nst = p.nst;
+  out->m_tiles2 = p.geo[2].m_tiles;
+  out->n_tiles2 = p.geo[2].n_tiles;
+  out->k_blocks2 = p.geo[2].k_blocks;
+  out->n_out2 = p.geo[2].n_out;
+  out->num_flags_pw = (int32_t)p.num_flags_pw;
+  out->strided_group_pw = p.dep_pw.G;
+  out->strided_distance_pw = p.dep_pw.D;
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_pointwise_waits(const cusync_chain_desc_t* d, int32_t m_tile, int32_t head, int32_t* flag,
+                                       uint32_t* per_run, int32_t max, int32_t* n_out) {
+  if (!d || !n_out || max < 0 || (max > 0 && (!flag || !per_run))) return CUSYNC_ERR_INVALID_ARG;
+  Plan p;
+  cusync_status_t st = make_plan(*d, &p);
+  if (st != CUSYNC_OK) return st;
+  if (p.nst != 3) return CUSYNC_ERR_INVALID_ARG;
+  if (m_tile < 0 || m_tile >= p.geo[1].m_tiles || head < 0 || head >= p.geo[1].n_tiles) return CUSYNC_ERR_INVALID_ARG;
+  Wait w[3];
+  const int n = pointwise_waits(p.dep_pw, m_tile, head, w);
+  for (int i = 0; i < n && i < max; ++i) {
+    flag[i] = w[i].flag;
+    per_run[i] = w[i].per_run;
+  }
+  *n_out = n;
   return CUSYNC_OK;
 }
 
@@ -856,7 +986,7 @@ cusync_status_t cusync_consumer_waits(const cusync_chain_desc_t* d, int32_t m_ti
   Plan p;
   cusync_status_t st = make_plan(*d, &p);
   if (st != CUSYNC_OK) return st;
-  const StageGeo& g = p.geo[1];
+  const StageGeo& g = p.geo[p.nst - 1];  // the stage that waits on `dep`
   if (m_tile < 0 || m_tile >= g.m_tiles) return CUSYNC_ERR_INVALID_ARG;
   if (max > 0 && (!kb || !flag || !per_run)) return CUSYNC_ERR_INVALID_ARG;
   DepTracker dt;
@@ -918,7 +1048,7 @@ cusync_status_t cusync_chain_trace(cusync_chain_t ch, cusync_stream_t stream, cu
                                    int32_t* n_out) {
   static_assert(sizeof(cusync_trace_rec_t) == sizeof(TraceRec), "trace record layout");
   if (!ch || !n_out || max < 0 || (max > 0 && !out) || !ch->trace) return CUSYNC_ERR_INVALID_ARG;
-  const int32_t n = ch->args.tiles0 + ch->args.tiles1;
+  const int32_t n = ch->args.tiles0 + ch->args.tiles1 + ch->args.tiles2;
   *n_out = n;
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");

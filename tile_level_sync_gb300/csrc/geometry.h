@@ -25,7 +25,11 @@ namespace cusync {
 // Policy and epilogue codes (same values as the public enums in cusync.h).
 enum : int32_t { POL_STREAM = 0, POL_ROW = 1, POL_TILE = 2, POL_STRIDED = 3, POL_SENTINEL = 4 };
 enum : int32_t { EPI_NONE = 0, EPI_GELU = 1, EPI_SWIGLU = 2, EPI_RELU = 3 };
-enum : int32_t { AMODE_GEMM = 0, AMODE_CONV = 1 };
+// A operand of a stage: a GEMM, an implicit-GEMM convolution, or no GEMM at all (the
+// attention chain's pointwise stage, computed by the epilogue warps).
+enum : int32_t { AMODE_GEMM = 0, AMODE_CONV = 1, AMODE_POINTWISE = 2 };
+// Width of a pointwise tile of the attention chain (one attention head).
+constexpr int32_t kHead = 128;
 
 constexpr int32_t kBM = 128;  // output rows (tokens / pixels) per tile: UMMA M
 constexpr int32_t kBK = 64;   // reduction elements per k-block: one 128-byte swizzle row of bf16
@@ -250,6 +254,29 @@ CUSYNC_HD bool dep_kblock(const StageGeo& cons, const DepCfg& d, int32_t kb) {
   if (cons.a_mode == AMODE_GEMM) return kb % per_col == 0;
   const int32_t tap = kb / cons.cblocks, cb = kb % cons.cblocks;
   return tap % 3 == 0 && cb % per_col == 0;
+}
+
+// Semaphore waits of the attention chain's pointwise tile (m, i) (head i of row tile m) on
+// the QKV GEMM, whose output row holds the Q, V and K blocks of width nq = 3 * D column
+// tiles apart (D = producer column tiles per block): the head reads column tile
+// c = i * kHead / prod_n_out of each block.  RowSync: the whole row tile; TileSync: the
+// three tiles; StridedSync (G = 3, distance D): the one semaphore the three share.
+CUSYNC_HD int pointwise_waits(const DepCfg& d, int32_t m, int32_t i, Wait* out) {
+  const int32_t c = i * kHead / d.prod_n_out;
+  const int32_t third = d.prod_n_tiles / 3;
+  switch (d.policy) {
+    case POL_ROW:
+      out[0] = Wait{m, (uint32_t)(d.prod_n_tiles * d.posts)};
+      return 1;
+    case POL_TILE:
+      for (int j = 0; j < 3; ++j) out[j] = Wait{m * d.prod_n_tiles + c + j * third, (uint32_t)d.posts};
+      return 3;
+    case POL_STRIDED:
+      out[0] = Wait{m * d.D + (c % d.D), (uint32_t)(d.G * d.posts)};
+      return 1;
+    default:
+      return 0;
+  }
 }
 
 // Either tracker, chosen by the consumer's A operand (used by the host introspection).

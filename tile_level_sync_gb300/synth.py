@@ -11,12 +11,14 @@ order listed, each array rounded to bf16 with round-to-nearest-even):
 * GeLU MLP:   X [M,K] ~ N(0,1); W1 [K,N1] ~ N(0,0.02); W2 [N1,N2] ~ N(0,0.02)
 * SwiGLU MLP: X [M,K] ~ N(0,1); Wgate, Wup [K,N1] ~ N(0,0.02); Wdown [N1,N2] ~ N(0,0.02)
 * conv pair:  x [N,H,W,C] ~ N(0,1) (NHWC); w1, w2 [K,3,3,C] ~ N(0,0.03) (KRSC)
+* attention:  X [M,K] ~ N(0,1); QKV [K,3*N1] ~ N(0,0.02); W2 [N1,N2] ~ N(0,0.02)
 
 N(mu, sigma) takes sigma as the standard deviation.  Shapes follow the
 GPT-3 145B MLP shard of [cuSync] §II-B / §III-A (H = 12288, one of 8
 tensor-parallel shards: X [B,12288], W1 [12288,6144], W2 [6144,12288]) and
-the 14x14x256 ResNet-38 layer of Table ``tab:resnet-sizes``; no dataset or
-trained weights are involved.
+the 14x14x256 ResNet-38 layer of Table ``tab:resnet-sizes``; the self-attention
+block of Fig. ``fig:gpt-3:attention`` takes the same shard (QKV [12288, 3*1536],
+W2 [1536, 12288]); no dataset or trained weights are involved.
 """
 
 from dataclasses import dataclass, field
@@ -28,7 +30,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                  # "mlp_gelu" | "mlp_swiglu" | "conv_relu"
+    kind: str                  # "mlp_gelu" | "mlp_swiglu" | "conv_relu" | "attention"
     dims: dict = field(default_factory=dict)
 
     def gemm_flops(self):
@@ -40,6 +42,8 @@ class Workload:
         if self.kind == "conv_relu":
             pix = d["N"] * d["H"] * d["W"]
             return 2 * pix * d["K"] * 9 * d["C"] + 2 * pix * d["K"] * 9 * d["K"]
+        if self.kind == "attention":   # the two GEMMs; the pointwise stage has no tensor work
+            return 2 * d["M"] * d["K"] * (3 * d["N1"]) + 2 * d["M"] * d["N1"] * d["N2"]
         raise ValueError(self.kind)
 
 
@@ -59,6 +63,8 @@ WORKLOADS = {
         Workload("swiglu_m256", "mlp_swiglu", dict(M=256, K=8192, N1=3584, N2=8192)),
         Workload("swiglu_m1024", "mlp_swiglu", dict(M=1024, K=8192, N1=3584, N2=8192)),
         Workload("conv_resnet14_n32", "conv_relu", dict(N=32, H=14, W=14, C=256, K=256)),
+        Workload("gpt3_attn_m256", "attention", dict(M=256, K=12288, N1=1536, N2=12288)),
+        Workload("gpt3_attn_m1024", "attention", dict(M=1024, K=12288, N1=1536, N2=12288)),
     ]
 }
 
@@ -100,6 +106,16 @@ def conv_inputs(N, H, W, C, K, seed=0):
     return x, w1, w2
 
 
+def attention_inputs(M, K, N1, N2, seed=0):
+    """(X [M,K], QKV [K,3*N1] -- the XQ, XV, XK column blocks --, W2 [N1,N2]) as CPU bf16
+    tensors."""
+    rng = np.random.default_rng(seed)
+    X = to_bf16(_normal(rng, (M, K), 1.0))
+    Wqkv = to_bf16(_normal(rng, (K, 3 * N1), 0.02))
+    W2 = to_bf16(_normal(rng, (N1, N2), 0.02))
+    return X, Wqkv, W2
+
+
 def workload_inputs(w: Workload, seed=0):
     d = w.dims
     if w.kind == "mlp_gelu":
@@ -108,6 +124,8 @@ def workload_inputs(w: Workload, seed=0):
         return mlp_swiglu_inputs(d["M"], d["K"], d["N1"], d["N2"], seed)
     if w.kind == "conv_relu":
         return conv_inputs(d["N"], d["H"], d["W"], d["C"], d["K"], seed)
+    if w.kind == "attention":
+        return attention_inputs(d["M"], d["K"], d["N1"], d["N2"], seed)
     raise ValueError(w.kind)
 
 
