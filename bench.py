@@ -737,9 +737,11 @@ def sweep(a, torch, cs, synth, out_path):
             row = {"workload": name, "tile_n": tile_n, "gflop": wl.gemm_flops() / 1e9, "us": {}}
             for vi, (raster, pf, pair) in enumerate(variants):
                 pols = ["STREAM", "ROW", "TILE", "STRIDED", "SENTINEL"] if vi == 0 else ["STREAM", "ROW", "TILE"]
+                if wl.kind == "attention":   # single CTAs only; its policies are Row, Tile, Strided+Tile
+                    pols = ["STREAM", "ROW", "TILE", "STRIDED"]
                 for pol in pols:
                     for launch in (cs.LAUNCH_PERSISTENT, cs.LAUNCH_PDL):
-                        if launch == cs.LAUNCH_PDL and (pol == "STREAM" or vi != 0):
+                        if launch == cs.LAUNCH_PDL and (pol == "STREAM" or (vi != 0 and wl.kind != "attention")):
                             continue
                         key = f"{pol}/{'pdl' if launch else 'pers'}/r{raster}/p{pair}"
                         try:

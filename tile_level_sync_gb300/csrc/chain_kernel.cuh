@@ -478,7 +478,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       const uint64_t pol_a = ptx::l2_policy_evict_last();
       const uint64_t pol_b = ptx::l2_policy_evict_normal();
       const bool reorder = !(args.flags_bits & kFlagNoReorder);
-      uint32_t it = 0, tcount = 0;
+      uint32_t it = 0, tcount = 0, pw_seen = 0;
       bool ok = true;
       while (true) {
         const int slot = tcount % C::kSlots;
@@ -532,7 +532,18 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
           trec->t_claim = ptx::globaltimer();
           trec->t_post = 0;
         }
-        if (SA.g.a_mode == AMODE_POINTWISE) continue;  // computed by the epilogue warps; nothing to load
+        if (SA.g.a_mode == AMODE_POINTWISE) {
+          // Computed by this CTA's epilogue warps; nothing to load.  The next claim waits
+          // until they are done, so that the pointwise tiles spread over the CTAs instead
+          // of queueing behind one CTA's epilogue.
+          if (!ptx::mbar_wait_bounded(pw_done, pw_seen & 1u, pto) || *abort_flag) {
+            record_error(args, ERRC_PIPELINE, t, 9);
+            *abort_flag = 1;
+            ok = false;
+          }
+          ++pw_seen;
+          continue;
+        }
         const bool cons = (tr.s == args.nst - 1);
         GemmDepTracker gdt;
         gdt.reset();
