@@ -190,6 +190,8 @@ typedef struct {
   uint64_t t_mma1;    /* the last MMA of the tile was committed */
   uint64_t t_epi;     /* the epilogue finished the tile's stores */
   uint64_t t_post;    /* producer: the tile's semaphore was posted (0 if none) */
+  uint32_t polls;     /* consumer: semaphore reads its waits took (probes and polls) */
+  uint32_t reloads;   /* consumer, sentinel policy: A k-blocks loaded again */
 } cusync_trace_rec_t;
 
 /* Geometry of a chain (for tests and introspection). */

@@ -77,6 +77,7 @@ struct StageArgs {
 struct TraceRec {
   uint32_t tile, smid, cta, stage;
   uint64_t t_claim, t_ready, t_mma0, t_mma1, t_epi, t_post;
+  uint32_t polls, reloads;
 };
 
 struct ChainArgs {
@@ -531,6 +532,8 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
           trec->stage = (uint32_t)tr.s;
           trec->t_claim = ptx::globaltimer();
           trec->t_post = 0;
+          trec->polls = 0;
+          trec->reloads = 0;
         }
         if (SA.g.a_mode == AMODE_POINTWISE) {
           // Computed by this CTA's epilogue warps; nothing to load.  The next claim waits
@@ -659,6 +662,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
             rc_lo = f;
             rc_hi = f + 1;
             rc_target = target;
+            if (trec) trec->polls += iter + 1u;
           }
           if (observed) {
             ptx::fence_acq_rel_gpu();
@@ -787,21 +791,26 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       const bool to_leader = direct && !leader;
       const uint32_t abytes = a_tile_bytes(g);
       // Whether the A tile in stage sx still holds the sentinel anywhere (all lanes).
+      // The sentinel check inspects one 32-bit word (two bf16 elements) of every aligned
+      // 16-byte chunk, the granularity of CUDA-FGS's per-16-byte validity report: the
+      // producer writes each chunk with one 128-bit store under this policy, so a chunk is
+      // either all sentinel or all data.  Lane l reads word (c / 8) % 4 of chunk c = 32 i + l,
+      // which puts a warp's 32 reads in 32 different banks.
       auto stage_has_sentinel = [&](int sx, uint32_t nbytes) -> bool {
         uint32_t sbits = 0;
         const uint8_t* base = smem_a(sx);
-        // eight 16-byte loads in flight per lane before any of them is tested
-        for (uint32_t off0 = (uint32_t)lane * 16u; off0 < nbytes; off0 += 8u * 512u) {
-          uint4 v[8];
+        const uint32_t nchunks = nbytes / 16u;
+        const uint32_t word = ((uint32_t)lane >> 3) & 3u;
+        // eight loads in flight per lane before any of them is tested
+        for (uint32_t c0 = (uint32_t)lane; c0 < nchunks; c0 += 8u * 32u) {
+          uint32_t v[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const uint32_t off = off0 + (uint32_t)j * 512u;
-            v[j] = off < nbytes ? ptx::ld_shared_v4(base + off) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t c = c0 + (uint32_t)j * 32u;
+            v[j] = c < nchunks ? ptx::ld_shared_u32(base + c * 16u + word * 4u) : 0u;
           }
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            sbits |= sentinel_bits_bf16x2(v[j].x) | sentinel_bits_bf16x2(v[j].y) | sentinel_bits_bf16x2(v[j].z) |
-                     sentinel_bits_bf16x2(v[j].w);
+          for (int j = 0; j < 8; ++j) sbits |= sentinel_bits_bf16x2(v[j]);
         }
         return __any_sync(FULL, (sbits & 0x80008000u) != 0u);
       };
@@ -841,6 +850,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
               ptx::fence_proxy_async_smem();
               ptx::mbar_arrive_expect_tx(&full[st], abytes);
               issue_a<PAIR>(args, tr, kb, rank, smem_a(st), &full[st], pol_a);
+              if (args.trace && leader) args.trace[chain_tile(args, t)].reloads += 1u;
             }
             __syncwarp();
             if (!ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto)) {
@@ -868,6 +878,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
                   ptx::fence_proxy_async_smem();
                   ptx::mbar_arrive_expect_tx(&full[sj], abytes);
                   issue_a<PAIR>(args, tr, kb + j, rank, smem_a(sj), &full[sj], pol_a);
+                  if (args.trace && leader) args.trace[chain_tile(args, t)].reloads += 1u;
                 }
               } else {
                 clean_ahead |= 1u << sj;
@@ -1046,7 +1057,9 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       // GEMM outputs leave through TMA stores of 32-row x 64-column boxes staged in this
       // warp's two shared-memory buffers; convolution outputs (a tile's pixels are not a
       // box of the output tensor) through 16-byte stores from registers.
-      const bool tma_out = g.a_mode == AMODE_GEMM;
+      // (under the sentinel policy the tile that the consumer checks is written with one
+      // 128-bit store per 16-byte chunk, as the per-chunk check requires)
+      const bool tma_out = g.a_mode == AMODE_GEMM && !(args.sentinel_check && tr.s == args.nst - 2);
       uint8_t* ebuf = epi_stage + (q * 2) * C::kEpiBufBytes;
       const int32_t row_w0 = tr.m * (128 * PAIR) + (int32_t)rank * 128 + q * 32;
       // K split: the units of a tile other than the last store their fp32 partial sums

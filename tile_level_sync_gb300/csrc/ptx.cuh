@@ -318,6 +318,12 @@ __device__ __forceinline__ void st_relaxed_gpu_b128(void* p, uint32_t a, uint32_
       : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_shared_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
