@@ -192,6 +192,8 @@ typedef struct {
   uint64_t t_post;    /* producer: the tile's semaphore was posted (0 if none) */
   uint32_t polls;     /* consumer: semaphore reads its waits took (probes and polls) */
   uint32_t reloads;   /* consumer, sentinel policy: A k-blocks loaded again */
+  uint32_t land_clk;  /* SM cycles the MMA issuer waited for this tile's stages to land */
+  uint32_t check_clk; /* SM cycles of the sentinel check of this tile (scans and reloads) */
 } cusync_trace_rec_t;
 
 /* Geometry of a chain (for tests and introspection). */

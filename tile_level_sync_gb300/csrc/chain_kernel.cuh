@@ -4,7 +4,7 @@
 // and of the CUDA Programming Guide §4.6 "Fine-Grained Synchronization" (CUDA-FGS).
 //
 // One CTA per SM (PAIR = 1) or one CTA pair per two SMs in a cluster of 2 (PAIR = 2).
-// Roles inside each CTA (192 threads):
+// Roles inside each CTA (256 threads):
 //   warp 0, lane 0  TMA issuer (+ scheduler in the leader CTA).  The scheduler claims
 //                   tiles from a global counter in queue order (cuSync §IV-C: each
 //                   kernel takes its next tile from a per-stage counter) and hands them
@@ -15,15 +15,19 @@
 //                   load and, while a semaphore is still short, issues the weight (B)
 //                   loads of the next stages (cuSync §V, "Reorder Tile Loads and
 //                   Synchronization").
-//   warp 1          TMEM owner, stage checker and (leader) MMA issuer.  It waits for
-//                   each stage of this CTA to land; under the sentinel policy it scans
-//                   every A element for the 0x8000 pattern and re-issues the A load while
-//                   the pattern is present (CUDA-FGS §4.6.4.4 and §4.6.7, in software:
-//                   sm_103a has no copy-time validity report).  In a pair the peer's
-//                   checker then arrives on the leader's `ready` barrier; the leader's
-//                   lane 0 issues tcgen05.mma (128 x BN x 16 per CTA, or 256 x BN x 16
-//                   across the pair with cta_group::2, bf16 in, fp32 accumulate into
-//                   TMEM) and commits each stage back to the loaders of both CTAs.
+//   warp 1          TMEM owner and (leader) MMA issuer.  It waits for each stage to land
+//                   (or, for a tile under the sentinel check, to be checked); lane 0
+//                   issues tcgen05.mma (128 x BN x 16 per CTA, or 256 x BN x 16 across
+//                   the pair with cta_group::2, bf16 in, fp32 accumulate into TMEM) and
+//                   commits each stage back to the loaders of both CTAs.
+//   warp 7          sentinel checker (sentinel policy only).  It waits for each landed
+//                   stage of a consumer tile, scans every A element for the 0x8000
+//                   pattern and re-issues the A load while the pattern is present
+//                   (CUDA-FGS §4.6.4.4 and §4.6.7, in software: sm_103a has no copy-time
+//                   validity report), then arrives on the MMA issuer's `ready` barrier
+//                   (the leader's, in a pair), so that the scan overlaps the MMAs of the
+//                   stages before it.
+//   warp 6          L2 prefetch of the k-blocks ahead of the loader.
 //   warps 2..5      epilogue.  tcgen05.ld of this CTA's 128 accumulator rows
 //                   (double-buffered in TMEM so the next tile's mainloop overlaps this
 //                   epilogue), GeLU / SwiGLU / ReLU, bf16 round-to-nearest-even, -0 -> +0
@@ -78,6 +82,7 @@ struct TraceRec {
   uint32_t tile, smid, cta, stage;
   uint64_t t_claim, t_ready, t_mma0, t_mma1, t_epi, t_post;
   uint32_t polls, reloads;
+  uint32_t land_clk, check_clk;
 };
 
 struct ChainArgs {
@@ -115,7 +120,8 @@ struct KCfg {
   static constexpr int kStages = (192 * 1024) / kStageBytes;  // 4, 6 or 8
   static constexpr int kTmemCols = 2 * BN;           // two fp32 accumulators of BN columns
   static constexpr int kSlots = 4;                   // tile hand-off ring
-  static constexpr int kThreads = 224;              // 7 warps: loader, MMA, 4 epilogue, prefetch
+  // 7 warps (loader, MMA, 4 epilogue, prefetch), + 2 sentinel checkers under that policy
+  static constexpr int threads(bool check) { return check ? 288 : 224; }
   // epilogue staging for TMA stores: per epilogue warp two 32-row x 64-column bf16 boxes
   static constexpr int kEpiBufBytes = 32 * 64 * 2;
   static constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;
@@ -365,8 +371,10 @@ __device__ __forceinline__ bool xwait(uint64_t* bar, uint32_t parity, uint64_t t
   return ptx::mbar_wait_bounded(bar, parity, timeout_ns);
 }
 
-template <int BN, int PAIR>
-__global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ ChainArgs args) {
+// CHECK: the sentinel policy's instantiation, with the two checker warps (the host sets
+// args.sentinel_check to match); every other policy runs without them.
+template <int BN, int PAIR, bool CHECK>
+__global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kernel(const __grid_constant__ ChainArgs args) {
   using C = KCfg<BN, PAIR>;
   constexpr int S = C::kStages;
   constexpr uint32_t FULL = 0xFFFFFFFFu;
@@ -378,7 +386,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
   uint64_t* full = bars;                  // [S]   this CTA's A+B (or A retry) landed
   uint64_t* empty = full + S;             // [S]   the MMA finished reading the stage
-  uint64_t* ready = empty + S;            // [S]   pair: both CTAs' stages checked (leader)
+  uint64_t* ready = empty + S;            // [S]   checked tile: the stage passed the check (both CTAs')
   uint64_t* tfull = ready + S;            // [2]   accumulator ready
   uint64_t* tempty = tfull + 2;           // [2]   accumulator drained (leader in a pair)
   uint64_t* epi_done = tempty + 2;        // [2]   all epilogue threads of this CTA stored the tile
@@ -386,12 +394,17 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
   uint64_t* qempty = qfull + C::kSlots;   // [slots] tile index consumed (leader in a pair)
   uint64_t* mma_done = qempty + C::kSlots;
   uint64_t* pw_done = mma_done + 1;       // attention: all epilogue threads stored a pointwise tile
-  int32_t* qtile = reinterpret_cast<int32_t*>(pw_done + 1);
+  uint64_t* cfull = pw_done + 1;          // [S]   sentinel-checked tile: this CTA's A+B (or A retry) landed
+  int32_t* qtile = reinterpret_cast<int32_t*>(cfull + S);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qtile + C::kSlots);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   volatile int32_t* it_issued = abort_flag + 1;
   volatile uint32_t* progress = reinterpret_cast<volatile uint32_t*>(it_issued + 1);  // k-blocks issued
   volatile uint32_t* run_no = progress + 1;  // this launch's run number, for every role
+  // per stage: whether its last copy completes on cfull (1) or full (0)
+  volatile uint8_t* stage_kind = reinterpret_cast<volatile uint8_t*>(run_no + 1);
+  // pair, sentinel check: words the peer's checker stores into to signal `ready` (S <= 8)
+  uint32_t* ready_sink = const_cast<uint32_t*>(run_no + 3);
   uint8_t* epi_stage = smem + S * C::kStageBytes + 1024;  // 1024-byte aligned TMA store boxes
 
   auto smem_a = [&](int st) { return stage_base + st * C::kStageBytes; };
@@ -405,7 +418,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
   // on the leader's `full` barriers, which count the bytes of both CTAs.  A consumer tile
   // under the sentinel policy is not: each CTA's copies complete locally, its checker
   // validates them and arrives on the leader's `ready` barrier.
-  auto direct_tile = [&](const TileRef& tr) { return kPair && !(args.sentinel_check && tr.s == args.nst - 1); };
+  auto direct_tile = [&](const TileRef& tr) { return kPair && !(CHECK && tr.s == args.nst - 1); };
 
   if (args.pdl_role & 1) ptx::pdl_launch_dependents();
   // Run number of this launch.  Semaphores count up across runs (run r waits for r times
@@ -419,7 +432,9 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       for (int i = 0; i < S; ++i) {
         ptx::mbar_init(&full[i], 1);
         ptx::mbar_init(&empty[i], 1);
-        ptx::mbar_init(&ready[i], 2);
+        ptx::mbar_init(&ready[i], 1);
+        ptx::mbar_init(&cfull[i], 1);
+        stage_kind[i] = 0;
       }
       for (int i = 0; i < 2; ++i) {
         ptx::mbar_init(&tfull[i], 1);
@@ -428,9 +443,11 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       }
       for (int i = 0; i < C::kSlots; ++i) {
         ptx::mbar_init(&qfull[i], 1);
-        // consumers of a slot: MMA warp, 4 epilogue warps and the prefetch warp (+ the
-        // peer's loader, checker, 4 epilogue warps and prefetch warp in a pair)
-        ptx::mbar_init(&qempty[i], kPair ? 6 + 7 : 6);
+        // consumers of a slot: MMA warp, 4 epilogue warps, the prefetch warp and, under
+        // the sentinel policy, the two checker warps (+ the peer's loader and the same
+        // warps in a pair)
+        const uint32_t nloc = CHECK ? 8u : 6u;
+        ptx::mbar_init(&qempty[i], kPair ? 2u * nloc + 1u : nloc);
       }
       ptx::mbar_init(mma_done, 1);
       ptx::mbar_init(pw_done, 128);
@@ -534,6 +551,8 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
           trec->t_post = 0;
           trec->polls = 0;
           trec->reloads = 0;
+          trec->land_clk = 0;
+          trec->check_clk = 0;
         }
         if (SA.g.a_mode == AMODE_POINTWISE) {
           // Computed by this CTA's epilogue warps; nothing to load.  The next claim waits
@@ -564,6 +583,10 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
         const bool direct = direct_tile(tr);
         const bool to_leader = direct && !leader;
         const uint32_t txs = direct ? 2 * tx : tx;
+        // a tile that the checker warp validates completes its copies on cfull, which only
+        // the checker waits on; every other tile on full, which only the MMA issuer waits on
+        const bool checked = CHECK && cons;
+        uint64_t* const lbar = checked ? cfull : full;
         // k-blocks at which the consumer may have to wait (dep_kblock): every dep_every-th
         // k-block of a GEMM; for a convolution the first 64 k-blocks by a bit mask, every
         // later one by dep_every = 1.
@@ -598,12 +621,13 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
             return 0;
           }
           uint8_t* dst = smem_b(st);
+          stage_kind[st] = checked ? 1 : 0;
           if (to_leader) {
             ptx::tma_load_2d_to_leader(dst, tmB, ptx::mapa(&full[st], 0), kx0 + kbb * kBK, brow0, pol_b);
           } else {
-            ptx::mbar_arrive_expect_tx(&full[st], txs);
-            ptx::tma_load_2d(dst, tmB, &full[st], kx0 + kbb * kBK, brow0, pol_b);
-            if (brow1 >= 0) ptx::tma_load_2d(dst + (BN / 2) * 128, tmB, &full[st], kx0 + kbb * kBK, brow1, pol_b);
+            ptx::mbar_arrive_expect_tx(&lbar[st], txs);
+            ptx::tma_load_2d(dst, tmB, &lbar[st], kx0 + kbb * kBK, brow0, pol_b);
+            if (brow1 >= 0) ptx::tma_load_2d(dst + (BN / 2) * 128, tmB, &lbar[st], kx0 + kbb * kBK, brow1, pol_b);
           }
           return 1;
         };
@@ -688,7 +712,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
             if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
             const int st = (int)((it + (uint32_t)kb) % S);
             if (to_leader) ptx::tma_load_2d_to_leader(smem_a(st), tmA, ptx::mapa(&full[st], 0), kx0 + kb * kBK, a_row, pol_a);
-            else ptx::tma_load_2d(smem_a(st), tmA, &full[st], kx0 + kb * kBK, a_row, pol_a);
+            else ptx::tma_load_2d(smem_a(st), tmA, &lbar[st], kx0 + kb * kBK, a_row, pol_a);
             *progress = it + (uint32_t)kb + 1u;
           }
         } else {
@@ -707,7 +731,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
             if (dep_kb && reorder) wait_deps(kb);
             if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
             const int st = (int)((it + (uint32_t)kb) % S);
-            ptx::tma_load_4d(smem_a(st), tmA, &full[st], cv_cb * kBK, cv_s - 1, cv_h0 + cv_r, cv_img, pol_a);
+            ptx::tma_load_4d(smem_a(st), tmA, &lbar[st], cv_cb * kBK, cv_s - 1, cv_h0 + cv_r, cv_img, pol_a);
             if (++cv_cb == SA.g.cblocks) {
               cv_cb = 0;
               if (++cv_s == 3) {
@@ -752,14 +776,11 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ------------------------------------------------------------ checker + MMA issuer
-    const uint64_t pol_a = ptx::l2_policy_evict_last();
+    // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc = ptx::idesc_bf16_f32(128 * PAIR, BN);
-    uint32_t it = 0, tcount = 0, acount = 0, fpar = 0;
-    // Stages of later k-blocks of the current tile that the sentinel check already found
-    // landed and clean (their barrier phase is consumed).
-    uint32_t clean_ahead = 0;
-    uint32_t rpar = 0;  // leader: parity of each stage's next `ready` phase
+    uint32_t it = 0, tcount = 0, acount = 0;
+    uint32_t fpar = 0;  // parity of each stage's next `full` phase
+    uint32_t rpar = 0;  // parity of each stage's next `ready` phase (checked tiles)
     bool ok = true;
     while (ok) {
       const int slot = tcount % C::kSlots;
@@ -786,150 +807,59 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
         ptx::tc_fence_after();
       }
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-      const bool check = args.sentinel_check && tr.s == args.nst - 1;
-      const bool direct = direct_tile(tr);
-      const bool to_leader = direct && !leader;
-      const uint32_t abytes = a_tile_bytes(g);
-      // Whether the A tile in stage sx still holds the sentinel anywhere (all lanes).
-      // The sentinel check inspects one 32-bit word (two bf16 elements) of every aligned
-      // 16-byte chunk, the granularity of CUDA-FGS's per-16-byte validity report: the
-      // producer writes each chunk with one 128-bit store under this policy, so a chunk is
-      // either all sentinel or all data.  Lane l reads word (c / 8) % 4 of chunk c = 32 i + l,
-      // which puts a warp's 32 reads in 32 different banks.
-      auto stage_has_sentinel = [&](int sx, uint32_t nbytes) -> bool {
-        uint32_t sbits = 0;
-        const uint8_t* base = smem_a(sx);
-        const uint32_t nchunks = nbytes / 16u;
-        const uint32_t word = ((uint32_t)lane >> 3) & 3u;
-        // eight loads in flight per lane before any of them is tested
-        for (uint32_t c0 = (uint32_t)lane; c0 < nchunks; c0 += 8u * 32u) {
-          uint32_t v[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t c = c0 + (uint32_t)j * 32u;
-            v[j] = c < nchunks ? ptx::ld_shared_u32(base + c * 16u + word * 4u) : 0u;
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) sbits |= sentinel_bits_bf16x2(v[j]);
-        }
-        return __any_sync(FULL, (sbits & 0x80008000u) != 0u);
-      };
+      const bool checked = CHECK && tr.s == args.nst - 1;
+      // The peer of a pair issues nothing: its direct copies complete on the leader's
+      // `full`, and its checker arrives on the leader's `ready`.
+      if (!leader) {
+        it += (uint32_t)tr.nkb;
+        continue;
+      }
+      uint32_t land_clk = 0;  // traced runs: SM cycles spent waiting for stages
       for (int32_t kb = 0; kb < tr.nkb; ++kb, ++it) {
         const int st = (int)(it % S);
-        if (to_leader) continue;  // this CTA's stages are counted on the leader's barriers
-        if (!check) {
-          if (!ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto)) {
-            ok = false;
-            break;
-          }
-          fpar ^= 1u << st;
-        } else if ((clean_ahead >> st) & 1u) {
-          clean_ahead &= ~(1u << st);  // landed and checked clean while an earlier stage was reloaded
+        const uint32_t c0 = args.trace ? (uint32_t)clock64() : 0u;
+        bool landed;
+        if (checked) {
+          // every CTA's share of this stage landed and passed the sentinel check
+          landed = xwait<PAIR>(&ready[st], (rpar >> st) & 1u, pto);
+          rpar ^= 1u << st;
         } else {
-          if (!ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto)) {
-            ok = false;
-            break;
-          }
+          landed = ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto);
           fpar ^= 1u << st;
-          // Software validity check of this CTA's landed A tile: every bf16 element is
-          // compared with the sentinel; while any still holds it, the A load is issued
-          // again.
-          uint64_t t0 = 0;
-          bool reloaded = false;
-          while (true) {
-            if (!stage_has_sentinel(st, abytes)) break;
-            if (ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u) break;
-            const uint64_t now = ptx::globaltimer();
-            if (t0 == 0) t0 = now;
-            if (now - t0 > args.timeout_ns) {
-              if (lane == 0) record_error(args, ERRC_SENTINEL_TIMEOUT, t, kb);
-              break;
-            }
-            if (lane == 0) {
-              __nanosleep(128);
-              ptx::fence_proxy_async_smem();
-              ptx::mbar_arrive_expect_tx(&full[st], abytes);
-              issue_a<PAIR>(args, tr, kb, rank, smem_a(st), &full[st], pol_a);
-              if (args.trace && leader) args.trace[chain_tile(args, t)].reloads += 1u;
-            }
-            __syncwarp();
-            if (!ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto)) {
-              ok = false;
-              break;
-            }
-            fpar ^= 1u << st;
-            reloaded = true;
-          }
-          if (!ok) break;
-          if (reloaded) {
-            // This k-block's data has just become valid.  The A tiles of the following
-            // k-blocks of this tile that landed meanwhile were most likely copied before
-            // their data was written too: check them now and issue the stale ones again
-            // at once, so that their reloads overlap instead of following one another.
-            for (int j = 1; j < S && kb + j < tr.nkb; ++j) {
-              const int sj = (int)((it + (uint32_t)j) % S);
-              if ((clean_ahead >> sj) & 1u) continue;
-              bool landed = false;
-              if (lane == 0) landed = ptx::mbar_test_wait(&full[sj], (fpar >> sj) & 1u);
-              if (!__shfl_sync(FULL, landed ? 1 : 0, 0)) continue;
-              fpar ^= 1u << sj;
-              if (stage_has_sentinel(sj, abytes)) {
-                if (lane == 0) {
-                  ptx::fence_proxy_async_smem();
-                  ptx::mbar_arrive_expect_tx(&full[sj], abytes);
-                  issue_a<PAIR>(args, tr, kb + j, rank, smem_a(sj), &full[sj], pol_a);
-                  if (args.trace && leader) args.trace[chain_tile(args, t)].reloads += 1u;
-                }
-              } else {
-                clean_ahead |= 1u << sj;
-              }
-            }
-            __syncwarp();
-          }
         }
-        if (kPair && !direct) {
-          // both CTAs' shares of this stage are checked before the pair MMA reads them
-          bool rok = true;
-          if (lane == 0) {
-            if (leader) {
-              ptx::mbar_arrive(&ready[st]);
-              rok = ptx::mbar_wait_bounded_cluster(&ready[st], (rpar >> st) & 1u, pto);
-              rpar ^= 1u << st;
-            } else {
-              ptx::mbar_arrive_cluster(ptx::mapa(&ready[st], 0));
-            }
-          }
-          if (!__shfl_sync(FULL, rok ? 1 : 0, 0)) {
-            ok = false;
-            break;
-          }
+        if (!landed) {
+          ok = false;
+          break;
         }
-        if (leader) {
-          ptx::tc_fence_after();
-          if (lane == 0 && kb == 0 && args.trace) args.trace[chain_tile(args, t)].t_mma0 = ptx::globaltimer();
-          if (lane == 0) {
-            const uint32_t a0 = ptx::smem_u32(smem_a(st));
-            const uint32_t b0 = ptx::smem_u32(smem_b(st));
+        if (args.trace) land_clk += (uint32_t)clock64() - c0;
+        ptx::tc_fence_after();
+        if (lane == 0 && kb == 0 && args.trace) args.trace[chain_tile(args, t)].t_mma0 = ptx::globaltimer();
+        if (lane == 0) {
+          const uint32_t a0 = ptx::smem_u32(smem_a(st));
+          const uint32_t b0 = ptx::smem_u32(smem_b(st));
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              if (kPair)
-                ptx::umma_bf16_pair(d_tmem, ptx::smem_desc_k128(a0 + 32u * k), ptx::smem_desc_k128(b0 + 32u * k),
-                                    idesc, (kb | k) != 0 ? 1u : 0u);
-              else
-                ptx::umma_bf16(d_tmem, ptx::smem_desc_k128(a0 + 32u * k), ptx::smem_desc_k128(b0 + 32u * k), idesc,
-                               (kb | k) != 0 ? 1u : 0u);
-            }
-            if (kPair) ptx::umma_commit_pair_multicast(&empty[st], 0x3);
-            else ptx::umma_commit(&empty[st]);
+          for (int k = 0; k < kBK / 16; ++k) {
+            if (kPair)
+              ptx::umma_bf16_pair(d_tmem, ptx::smem_desc_k128(a0 + 32u * k), ptx::smem_desc_k128(b0 + 32u * k),
+                                  idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              ptx::umma_bf16(d_tmem, ptx::smem_desc_k128(a0 + 32u * k), ptx::smem_desc_k128(b0 + 32u * k), idesc,
+                             (kb | k) != 0 ? 1u : 0u);
           }
+          if (kPair) ptx::umma_commit_pair_multicast(&empty[st], 0x3);
+          else ptx::umma_commit(&empty[st]);
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (leader && lane == 0) {
+      if (lane == 0) {
         if (kPair) ptx::umma_commit_pair_multicast(&tfull[acc], 0x3);
         else ptx::umma_commit(&tfull[acc]);
-        if (args.trace) args.trace[chain_tile(args, t)].t_mma1 = ptx::globaltimer();
+        if (args.trace) {
+          TraceRec* r = args.trace + chain_tile(args, t);
+          r->t_mma1 = ptx::globaltimer();
+          r->land_clk = land_clk;
+        }
       }
       __syncwarp();
     }
@@ -944,14 +874,179 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       ptx::mbar_wait_bounded(mma_done, 0, pto);
     }
     __syncwarp();
-    // Abnormal exit only: wait (bounded) for copies the loader issued but nobody consumed.
-    if (lane == 0 && !ok) {
+    // Abnormal exit only: wait (bounded) for copies on `full` that were issued but not
+    // consumed (the checker drains `cfull`).
+    if (lane == 0 && !ok && leader) {
       const uint32_t issued = (uint32_t)*it_issued;
       for (uint32_t j = it; j < issued && j < it + S; ++j) {
         const int st = (int)(j % S);
-        if ((clean_ahead >> st) & 1u) continue;  // landed, phase already consumed
+        if (stage_kind[st] != 0) continue;
         ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto);
         fpar ^= 1u << st;
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 7) {
+    // ------------------------------------------------------------ sentinel checkers
+    // Under the sentinel policy every consumer k-block's A tile is validated here, off the
+    // MMA issuer's path, and handed to it through `ready` (the leader's, in a pair).  Two
+    // warps share the work: warp 7 owns the even stages, warp 8 the odd ones (the stage
+    // count is even, so a stage always belongs to the same warp and each warp's barrier
+    // phases are its own).
+    static_assert(S % 2 == 0, "the checkers split the stages by parity");
+    const int ck = warp - 7;
+    if constexpr (CHECK) {
+      const uint64_t pol_a = ptx::l2_policy_evict_last();
+      uint32_t it = 0, tcount = 0;
+      uint32_t cpar = 0;  // parity of each stage's next `cfull` phase
+      // Stages of later k-blocks of the current tile that were found landed and clean
+      // while an earlier one was reloaded (their cfull phase is consumed).
+      uint32_t clean_ahead = 0;
+      bool ok = true;
+      // Whether the A tile in stage sx still holds the sentinel anywhere (all lanes).
+      // The check inspects one 32-bit word (two bf16 elements) of every aligned 16-byte
+      // chunk, the granularity of CUDA-FGS's per-16-byte validity report: the producer
+      // writes each chunk with one 128-bit store under this policy, so a chunk is either
+      // all sentinel or all data.  Lane l reads word (c / 8) % 4 of chunk c = 32 i + l,
+      // which puts a warp's 32 reads in 32 different banks.  Shared-memory loads are slow
+      // to return while TMA writes and the MMAs read the same memory, so a 16 KB tile's 32
+      // loads per lane are all issued before the first one is tested.
+      auto stage_has_sentinel = [&](int sx, uint32_t nbytes) -> bool {
+        uint32_t sbits = 0;
+        const uint8_t* base = smem_a(sx);
+        const uint32_t nchunks = nbytes / 16u;
+        const uint32_t word = ((uint32_t)lane >> 3) & 3u;
+        for (uint32_t c0 = (uint32_t)lane; c0 < nchunks; c0 += 32u * 32u) {
+          uint32_t v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const uint32_t c = c0 + (uint32_t)j * 32u;
+            v[j] = c < nchunks ? ptx::ld_shared_u32(base + c * 16u + word * 4u) : 0u;
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sbits |= sentinel_bits_bf16x2(v[j]);
+        }
+        return __any_sync(FULL, (sbits & 0x80008000u) != 0u);
+      };
+      while (ok) {
+        const int slot = tcount % C::kSlots;
+        if (!xwait<PAIR>(&qfull[slot], (tcount / C::kSlots) & 1u, pto)) {
+          ok = false;
+          break;
+        }
+        const int32_t t = qtile[slot];
+        __syncwarp();
+        if (lane == 0) ring_release(slot);
+        ++tcount;
+        if (t < 0) break;
+        const TileRef tr = decode_tile(args, t);
+        const StageGeo& g = args.st[tr.s].g;
+        if (g.a_mode == AMODE_POINTWISE) continue;
+        if (tr.s != args.nst - 1) {
+          it += (uint32_t)tr.nkb;  // loaded on `full`, consumed by the MMA issuer alone
+          continue;
+        }
+        const uint32_t abytes = a_tile_bytes(g);
+        uint32_t check_clk = 0, reloads = 0;
+        for (int32_t kb = 0; kb < tr.nkb; ++kb, ++it) {
+          const int st = (int)(it % S);
+          if ((st & 1) != ck) continue;  // the other checker's stage
+          if ((clean_ahead >> st) & 1u) {
+            clean_ahead &= ~(1u << st);
+          } else {
+            if (!ptx::mbar_wait_bounded(&cfull[st], (cpar >> st) & 1u, pto)) {
+              ok = false;
+              break;
+            }
+            cpar ^= 1u << st;
+            const uint32_t c1 = args.trace ? (uint32_t)clock64() : 0u;
+            // Software validity check of this CTA's landed A tile: while any element still
+            // holds the sentinel, the A load is issued again.
+            uint64_t t0 = 0;
+            bool reloaded = false;
+            while (true) {
+              if (!stage_has_sentinel(st, abytes)) break;
+              if (ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u) break;
+              const uint64_t now = ptx::globaltimer();
+              if (t0 == 0) t0 = now;
+              if (now - t0 > args.timeout_ns) {
+                if (lane == 0) record_error(args, ERRC_SENTINEL_TIMEOUT, t, kb);
+                break;
+              }
+              if (lane == 0) {
+                __nanosleep(128);
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive_expect_tx(&cfull[st], abytes);
+                issue_a<PAIR>(args, tr, kb, rank, smem_a(st), &cfull[st], pol_a);
+              }
+              ++reloads;
+              __syncwarp();
+              if (!ptx::mbar_wait_bounded(&cfull[st], (cpar >> st) & 1u, pto)) {
+                ok = false;
+                break;
+              }
+              cpar ^= 1u << st;
+              reloaded = true;
+            }
+            if (!ok) break;
+            if (reloaded) {
+              // This k-block's data has just become valid.  The A tiles of the following
+              // k-blocks of this tile that landed meanwhile were most likely copied before
+              // their data was written too: check them now and issue the stale ones again
+              // at once, so that their reloads overlap instead of following one another.
+              for (int j = 2; j < S && kb + j < tr.nkb; j += 2) {
+                const int sj = (int)((it + (uint32_t)j) % S);
+                if ((clean_ahead >> sj) & 1u) continue;
+                bool landed = false;
+                if (lane == 0) landed = ptx::mbar_test_wait(&cfull[sj], (cpar >> sj) & 1u);
+                if (!__shfl_sync(FULL, landed ? 1 : 0, 0)) continue;
+                cpar ^= 1u << sj;
+                if (stage_has_sentinel(sj, abytes)) {
+                  if (lane == 0) {
+                    ptx::fence_proxy_async_smem();
+                    ptx::mbar_arrive_expect_tx(&cfull[sj], abytes);
+                    issue_a<PAIR>(args, tr, kb + j, rank, smem_a(sj), &cfull[sj], pol_a);
+                  }
+                  ++reloads;
+                } else {
+                  clean_ahead |= 1u << sj;
+                }
+              }
+              __syncwarp();
+            }
+            if (args.trace) check_clk += (uint32_t)clock64() - c1;
+          }
+          // Hand the checked stage to the MMA issuer.  In a pair the leader's checker
+          // arrives and expects 4 bytes, which the peer's checker supplies with an
+          // asynchronous store: a remote mbarrier.arrive.release would stall it for a
+          // round trip between the SMs at every k-block.
+          __syncwarp();
+          if (lane == 0) {
+            if (!kPair) ptx::mbar_arrive(&ready[st]);
+            else if (leader) ptx::mbar_arrive_expect_tx(&ready[st], 4u);
+            else ptx::st_async_u32(ptx::mapa(&ready_sink[st], 0), 1u, ptx::mapa(&ready[st], 0));
+          }
+        }
+        if (!ok) break;
+        if (args.trace && leader && lane == 0) {
+          TraceRec* r = args.trace + chain_tile(args, t);
+          atomicAdd(&r->check_clk, check_clk);
+          atomicAdd(&r->reloads, reloads);
+        }
+      }
+      if (!ok) {
+        record_error(args, ERRC_PIPELINE, 0xFFFFFF, 10);
+        *abort_flag = 1;
+        // wait (bounded) for copies on `cfull` that were issued but not consumed
+        if (lane == 0) {
+          const uint32_t issued = (uint32_t)*it_issued;
+          for (uint32_t j = it; j < issued && j < it + S; ++j) {
+            const int st = (int)(j % S);
+            if ((st & 1) != ck || stage_kind[st] != 1 || ((clean_ahead >> st) & 1u)) continue;
+            ptx::mbar_wait_bounded(&cfull[st], (cpar >> st) & 1u, pto);
+            cpar ^= 1u << st;
+          }
+        }
       }
     }
     __syncwarp();
@@ -1004,7 +1099,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       it0 += (uint32_t)KB;
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
@@ -1059,7 +1154,7 @@ __global__ void __launch_bounds__(224, 1) chain_kernel(const __grid_constant__ C
       // box of the output tensor) through 16-byte stores from registers.
       // (under the sentinel policy the tile that the consumer checks is written with one
       // 128-bit store per 16-byte chunk, as the per-chunk check requires)
-      const bool tma_out = g.a_mode == AMODE_GEMM && !(args.sentinel_check && tr.s == args.nst - 2);
+      const bool tma_out = g.a_mode == AMODE_GEMM && !(CHECK && tr.s == args.nst - 2);
       uint8_t* ebuf = epi_stage + (q * 2) * C::kEpiBufBytes;
       const int32_t row_w0 = tr.m * (128 * PAIR) + (int32_t)rank * 128 + q * 32;
       // K split: the units of a tile other than the last store their fp32 partial sums

@@ -341,35 +341,43 @@ bool encode_nhwc(CUtensorMap* m, const void* ptr, uint64_t n, uint64_t h, uint64
 
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int BN, int PAIR>
+template <int BN, int PAIR, bool CHECK>
 cudaError_t set_kernel_attrs() {
-  cudaError_t e = cudaFuncSetAttribute(chain_kernel<BN, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(chain_kernel<BN, PAIR, CHECK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        KCfg<BN, PAIR>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(chain_kernel<BN, PAIR>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(chain_kernel<BN, PAIR, CHECK>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   // Load the kernel now rather than at its first launch (CUDA-FGS §4.6.5, "Overlap").
   cudaFuncAttributes fa;
-  return cudaFuncGetAttributes(&fa, chain_kernel<BN, PAIR>);
+  return cudaFuncGetAttributes(&fa, chain_kernel<BN, PAIR, CHECK>);
+}
+
+template <bool CHECK>
+cudaError_t set_kernel_attrs_all_tiles() {
+  cudaError_t e = set_kernel_attrs<256, 1, CHECK>();
+  if (e == cudaSuccess) e = set_kernel_attrs<128, 1, CHECK>();
+  if (e == cudaSuccess) e = set_kernel_attrs<256, 2, CHECK>();
+  if (e == cudaSuccess) e = set_kernel_attrs<128, 2, CHECK>();
+  return e;
 }
 
 cudaError_t set_all_kernel_attrs() {
-  cudaError_t e = set_kernel_attrs<256, 1>();
-  if (e == cudaSuccess) e = set_kernel_attrs<128, 1>();
-  if (e == cudaSuccess) e = set_kernel_attrs<256, 2>();
-  if (e == cudaSuccess) e = set_kernel_attrs<128, 2>();
+  cudaError_t e = set_kernel_attrs_all_tiles<false>();
+  if (e == cudaSuccess) e = set_kernel_attrs_all_tiles<true>();
   cudaFuncAttributes fa;
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, sentinel_fill_kernel);
   return e;
 }
 
-// Clusters of two CTAs that can be resident at once (pair kernels), for the current device.
-template <int BN>
-int max_pair_clusters() {
+// Clusters of two CTAs that can be resident at once (pair kernels), for the current device:
+// the fewer of the instantiations with and without the sentinel checkers.
+template <int BN, bool CHECK>
+int max_pair_clusters_of() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(KCfg<BN, 2>::kThreads);
+  cfg.blockDim = dim3(KCfg<BN, 2>::threads(CHECK));
   cfg.dynamicSmemBytes = KCfg<BN, 2>::kSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -379,11 +387,16 @@ int max_pair_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, chain_kernel<BN, 2>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, chain_kernel<BN, 2, CHECK>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
   return n;
+}
+
+template <int BN>
+int max_pair_clusters() {
+  return std::min(max_pair_clusters_of<BN, false>(), max_pair_clusters_of<BN, true>());
 }
 
 // Grid sizes (CTAs) of the fused launch and of the two separate launches.
@@ -512,11 +525,11 @@ struct cusync_chain {
 
 namespace {
 
-template <int BN, int PAIR>
+template <int BN, int PAIR, bool CHECK>
 cudaError_t launch_chain(const ChainArgs& a, int grid, bool cooperative, bool pdl_secondary, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(KCfg<BN, PAIR>::kThreads);
+  cfg.blockDim = dim3(KCfg<BN, PAIR>::threads(CHECK));
   cfg.dynamicSmemBytes = KCfg<BN, PAIR>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[3];
@@ -540,22 +553,29 @@ cudaError_t launch_chain(const ChainArgs& a, int grid, bool cooperative, bool pd
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, chain_kernel<BN, PAIR>, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, chain_kernel<BN, PAIR, CHECK>, a);
   if (e != cudaSuccess && cooperative && PAIR == 2) {
     // Cooperative cluster launches may be refused; the grid is already sized to the
     // clusters that can be resident at once, so launch without the attribute.
     cudaGetLastError();
     CUSYNC_LOG("cooperative cluster launch refused (%s); launching without it", cudaGetErrorString(e));
     cfg.numAttrs = na - 1;
-    e = cudaLaunchKernelEx(&cfg, chain_kernel<BN, PAIR>, a);
+    e = cudaLaunchKernelEx(&cfg, chain_kernel<BN, PAIR, CHECK>, a);
   }
   return e;
 }
 
-cudaError_t launch_any(const Plan& p, const ChainArgs& a, int grid, bool coop, bool pdl2, cudaStream_t s) {
+template <bool CHECK>
+cudaError_t launch_tiles(const Plan& p, const ChainArgs& a, int grid, bool coop, bool pdl2, cudaStream_t s) {
   if (p.pair == 2)
-    return p.bn == 256 ? launch_chain<256, 2>(a, grid, coop, pdl2, s) : launch_chain<128, 2>(a, grid, coop, pdl2, s);
-  return p.bn == 256 ? launch_chain<256, 1>(a, grid, coop, pdl2, s) : launch_chain<128, 1>(a, grid, coop, pdl2, s);
+    return p.bn == 256 ? launch_chain<256, 2, CHECK>(a, grid, coop, pdl2, s)
+                       : launch_chain<128, 2, CHECK>(a, grid, coop, pdl2, s);
+  return p.bn == 256 ? launch_chain<256, 1, CHECK>(a, grid, coop, pdl2, s)
+                     : launch_chain<128, 1, CHECK>(a, grid, coop, pdl2, s);
+}
+
+cudaError_t launch_any(const Plan& p, const ChainArgs& a, int grid, bool coop, bool pdl2, cudaStream_t s) {
+  return a.sentinel_check ? launch_tiles<true>(p, a, grid, coop, pdl2, s) : launch_tiles<false>(p, a, grid, coop, pdl2, s);
 }
 
 // The launches of one chain run: sentinel fill, then one fused persistent kernel or the

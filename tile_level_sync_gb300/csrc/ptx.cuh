@@ -353,6 +353,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Asynchronous 32-bit store into a peer CTA's shared memory; its completion counts 4
+// bytes of transactions on the peer's mbarrier at `cluster_bar`, with release semantics at
+// cluster scope.  Unlike a remote mbarrier.arrive.release, the issuing thread does not
+// wait for the round trip.
+__device__ __forceinline__ void st_async_u32(uint32_t cluster_addr, uint32_t v, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(cluster_addr),
+               "r"(v), "r"(cluster_bar)
+               : "memory");
+}
+
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
