@@ -144,7 +144,7 @@ typedef struct {
                                         two) computes a 256-row tile with cta_group::2
                                         MMAs, each CTA loading half of the weight tile
                                         (MLP chains only); 0 = 2 for MLP chains with
-                                        M >= 512, else 1 */
+                                        M >= 256, else 1 */
   int32_t ksplit;                    /* K split of the producer GEMM (MLP chains): each
                                         producer tile is computed by this many work units
                                         over consecutive k-block ranges, whose fp32 partial

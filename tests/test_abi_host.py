@@ -123,6 +123,8 @@ def test_cta_pair_only_for_mlp_chains():
     d.M = 512
     assert cs.cusync_plan_info(d).cta_pair == 2
     d.M = 256
+    assert cs.cusync_plan_info(d).cta_pair == 2
+    d.M = 255
     assert cs.cusync_plan_info(d).cta_pair == 1
     d.M = 64
     d.cta_pair = 2

@@ -164,7 +164,8 @@ def test_auto_policy_resolves_to_the_predicted_best(case):
 
 
 def test_default_model_is_calibrated_per_tiling():
-    gelu = cs.cusync_default_latency_model(cs.make_desc(policy="ROW", M=256, K=256, N1=512, N2=256, tile_n=256))
+    gelu = cs.cusync_default_latency_model(cs.make_desc(policy="ROW", M=256, K=256, N1=512, N2=256, tile_n=256,
+                                                        cta_pair=1))
     pair = cs.cusync_default_latency_model(cs.make_desc(policy="ROW", M=1024, K=256, N1=512, N2=256, tile_n=256))
     conv = cs.cusync_default_latency_model(cs.make_desc(cs.CHAIN_CONV_RELU, "ROW", n=1, h=14, w=14, c=64,
                                                         k_out=128, tile_n=128))

@@ -103,9 +103,10 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   if (bn != 128 && bn != 256) return CUSYNC_ERR_UNSUPPORTED;
   const bool mlp = d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
   const bool attn = d.kind == CUSYNC_CHAIN_ATTENTION;
-  // CTA pairs (cta_group::2, 256-row tiles) for MLP chains with at least 512 tokens,
-  // where they measured faster on GB300; single-CTA 128-row tiles otherwise.
-  const int32_t pair = d.cta_pair ? d.cta_pair : ((mlp && d.M >= 512) ? 2 : 1);
+  // CTA pairs (cta_group::2, 256-row tiles) for MLP chains with at least 256 tokens,
+  // where they measured faster on GB300 (GPT-3 M=256: 91 against 97 us; SwiGLU M=256
+  // even); single-CTA 128-row tiles otherwise.
+  const int32_t pair = d.cta_pair ? d.cta_pair : ((mlp && d.M >= 256) ? 2 : 1);
   if (pair != 1 && pair != 2) return CUSYNC_ERR_INVALID_ARG;
   if (pair == 2 && !mlp) return CUSYNC_ERR_UNSUPPORTED;
   std::memset(p, 0, sizeof(*p));
@@ -422,8 +423,9 @@ Grids make_grids(const Plan& p, int sms, int max_clusters) {
 
 // GB300 constants of the latency model for plan p, from the in-kernel trace of the bench
 // workloads: mainloop ns per k-block (single CTAs 345-375, CTA pairs 390-420 per pair
-// k-block, convolutions 355-400, consumers slightly slower than producers), the sentinel
-// check's k-block (about 1.0 us, 1.5 us with pairs), a tile's first copy about 1 us,
+// k-block, convolutions 355-400, consumers slightly slower than producers), a consumer
+// k-block under the sentinel check once its data is valid (420-440 ns: two checker warps
+// scan alternate stages), a tile's first copy about 1 us,
 // the post seen by a consumer about 1.5 us after the stores, 2 us between stream-ordered
 // kernels, and epilogue time per output column by activation (tanh-GeLU 22 ns, SwiGLU
 // 26 ns, ReLU 22 ns, none 17 ns for a 128-row tile).
@@ -433,15 +435,15 @@ LatencyModel default_model(const Plan& p) {
   if (conv) {
     m.kblock_ns[0] = 365.0;
     m.kblock_ns[1] = 360.0;
-    m.sentinel_kblock_ns = 990.0;
+    m.sentinel_kblock_ns = 420.0;
   } else if (p.pair == 2) {
     m.kblock_ns[0] = 395.0;
     m.kblock_ns[1] = 415.0;
-    m.sentinel_kblock_ns = 1480.0;
+    m.sentinel_kblock_ns = 435.0;
   } else {
     m.kblock_ns[0] = p.bn == 128 ? 355.0 : 350.0;
     m.kblock_ns[1] = p.bn == 128 ? 365.0 : 370.0;
-    m.sentinel_kblock_ns = 1000.0;
+    m.sentinel_kblock_ns = 440.0;
   }
   m.wait_kblock_ns = 150.0;
   m.start_ns = 1000.0;
