@@ -41,9 +41,10 @@ PAGES_US_B256 = 840.0
 # (profiles/chain_kernel_full_<workload>_row.md), valid only for the kernel sources the
 # capture was taken on (sha256 of tile_level_sync_gb300/csrc/*).
 NCU_TRAFFIC = {
-    # (workload, policy, launch, tile_n): (dram__bytes_read.sum + dram__bytes_write.sum per
-    # launch of the chain kernel, hash of the kernel sources the capture was taken with)
-    ("gpt3_mlp_m256", "ROW", "persistent", 256): (311041024 + 17731072, "8885eca9a8acb357"),
+    # (workload, policy, launch, tile_n, CTAs per tile): (dram__bytes_read.sum +
+    # dram__bytes_write.sum per launch of the chain kernel, hash of the kernel sources the
+    # capture was taken with)
+    ("gpt3_mlp_m256", "ROW", "persistent", 256, 2): (309524736 + 17603840, "facbce89ed376179"),
 }
 
 
@@ -57,8 +58,8 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def measured_traffic(workload, policy, launch, tile_n):
-    rec = NCU_TRAFFIC.get((workload, policy, launch, tile_n))
+def measured_traffic(workload, policy, launch, tile_n, pair):
+    rec = NCU_TRAFFIC.get((workload, policy, launch, tile_n, pair))
     if rec and rec[1] == kernel_source_hash():
         return rec[0]
     return None
@@ -102,7 +103,8 @@ def parse():
     p.add_argument("--trace-out", default="", help="also run STREAM and each listed policy once with the "
                    "in-kernel per-tile trace and write timeline statistics to this JSON file")
     p.add_argument("--profile-runs", type=int, default=0, help="only run the first policy of --policies this many "
-                   "times after 3 warm-up runs (for a profiler), then exit without a bench line")
+                   "times after 3 warm-up runs (for a profiler; launched without the cooperative attribute), "
+                   "then exit without a bench line")
     return p.parse_args()
 
 
@@ -344,17 +346,18 @@ class Setup:
         self.cta_pair = cta_pair
         self.chains = {}
 
-    def chain(self, policy, launch=None, tile_n=None, raster=None, l2_prefetch=None, cta_pair=None):
+    def chain(self, policy, launch=None, tile_n=None, raster=None, l2_prefetch=None, cta_pair=None, flags=0):
         cs = self.cs
         launch = self.launch if launch is None else launch
         tile_n = self.tile_n if tile_n is None else tile_n
         raster = self.raster if raster is None else raster
         l2_prefetch = self.l2_prefetch if l2_prefetch is None else l2_prefetch
         cta_pair = self.cta_pair if cta_pair is None else cta_pair
-        key = (policy, launch, tile_n, raster, l2_prefetch, cta_pair)
+        key = (policy, launch, tile_n, raster, l2_prefetch, cta_pair, flags)
         if key not in self.chains:
             self.chains[key] = cs.Chain(cs.make_desc(policy=policy, launch=launch, tile_n=tile_n, raster_rows=raster,
-                                                     l2_prefetch=l2_prefetch, cta_pair=cta_pair, **self.base))
+                                                     l2_prefetch=l2_prefetch, cta_pair=cta_pair, flags=flags,
+                                                     **self.base))
         return self.chains[key]
 
     def run(self, ch):
@@ -486,10 +489,6 @@ def trace_stats(torch, setup, policy, launch):
     return out
 
 
-def info_tile_n(setup, policy):
-    return setup.chain(policy).info().tile_n
-
-
 def algorithmic_bytes(wl):
     d = wl.dims
     if wl.kind == "conv_relu":
@@ -556,7 +555,9 @@ def main():
 
     pols = [p.strip().upper() for p in a.policies.split(",") if p.strip()]
     if a.profile_runs > 0:
-        ch = setup.chain(pols[0])
+        # ncu cannot replay a cooperative cluster launch; the grid is sized to the resident
+        # CTAs (pairs) either way, and under the profiler nothing else runs on the GPU
+        ch = setup.chain(pols[0], flags=cs.FLAG_NO_COOPERATIVE)
         for _ in range(3 + a.profile_runs):
             setup.run(ch)
         st, code, _ = ch.check()
@@ -625,7 +626,8 @@ def main():
     tflops_kernel = flops / (kern_ms * 1e-3) / 1e12
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     bound = "hbm" if flops / alg_bytes < ridge else "tensor"
-    traffic = measured_traffic(wl.name, best, a.launch, info_tile_n(setup, best))
+    best_info = setup.chain(best).info()
+    traffic = measured_traffic(wl.name, best, a.launch, best_info.tile_n, best_info.cta_pair)
     if bound == "hbm":
         roof = {"bound": "hbm", "achieved": hbm_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": hbm_gbs / peaks["hbm_gbs"], "traffic": traffic}

@@ -117,6 +117,12 @@ typedef enum {
                                              Synchronization": weight tiles are then
                                              loaded only after the A-tile wait */
 #define CUSYNC_FLAG_TRACE (1u << 1)       /* record a per-tile timeline (cusync_chain_trace) */
+#define CUSYNC_FLAG_NO_COOPERATIVE (1u << 2) /* launch persistent grids without the cooperative
+                                             attribute (for profilers that cannot replay a
+                                             cooperative cluster launch); co-residency then
+                                             rests on the grid being sized to the CTAs or
+                                             pairs that can be resident, on an otherwise idle
+                                             GPU */
 /* Fault injection for tests; each makes a device wait expire, never a GPU fault. */
 #define CUSYNC_DEBUG_SKIP_POST (1u << 8)     /* the producer never posts tile (0,0) */
 #define CUSYNC_DEBUG_SKIP_INIT (1u << 9)     /* SENTINEL: skip the sentinel fill */

@@ -33,6 +33,28 @@ def test_library_exports_every_declared_function():
     assert not missing, missing
 
 
+def _header_constants():
+    """CUSYNC_* enumerators (explicit values) and #define flags of the public header."""
+    src = open(os.path.join(ROOT, "include", "cusync.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    vals = {k: int(v) for k, v in re.findall(r"\b(CUSYNC_[A-Z0-9_]+)\s*=\s*(\d+)", src)}
+    for k, sh in re.findall(r"#define\s+(CUSYNC_[A-Z0-9_]+)\s+\(1u\s*<<\s*(\d+)\)", src):
+        vals[k] = 1 << int(sh)
+    return vals
+
+
+def test_binding_constants_match_header():
+    vals = _header_constants()
+    assert len(vals) >= 20
+    for name, v in vals.items():
+        py = name[len("CUSYNC_"):]
+        if py.startswith("POLICY_") or py.startswith("CHAIN_") or py.startswith("LAUNCH_") or \
+                py.startswith("FLAG_") or py.startswith("DEBUG_"):
+            assert getattr(cs, py) == v, name
+        elif py == "OK" or py.startswith("ERR_"):
+            assert getattr(cs, py) == v, name
+
+
 def test_status_strings():
     assert cs.status_string(cs.OK) == "CUSYNC_OK"
     assert cs.status_string(cs.ERR_TIMEOUT) == "CUSYNC_ERR_TIMEOUT"

@@ -599,7 +599,8 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
     A.first_stage = 0;
     A.last_stage = p.nst - 1;
     A.pdl_role = 0;
-    e = launch_any(p, A, g.fused, /*coop=*/true, false, stream);
+    const bool coop = !(d.flags & CUSYNC_FLAG_NO_COOPERATIVE);
+    e = launch_any(p, A, g.fused, coop, false, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fused chain launch");
     return CUSYNC_OK;
   }
@@ -612,7 +613,8 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
     A.last_stage = s;
     A.pdl_role = pdl ? ((s + 1 < p.nst ? 1 : 0) | (s > 0 ? 2 : 0)) : 0;
     // K-split units of the first stage wait for one another: its CTAs must all be resident.
-    e = launch_any(p, A, g.stage[s], /*coop=*/s == 0 && p.geo[0].ksplit > 1, /*pdl2=*/pdl && s > 0, stream);
+    const bool coop = s == 0 && p.geo[0].ksplit > 1 && !(d.flags & CUSYNC_FLAG_NO_COOPERATIVE);
+    e = launch_any(p, A, g.stage[s], coop, /*pdl2=*/pdl && s > 0, stream);
     if (e != cudaSuccess) return cuda_fail(e, s == 0 ? "producer launch" : "consumer launch");
   }
   return CUSYNC_OK;
