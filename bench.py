@@ -44,7 +44,7 @@ NCU_TRAFFIC = {
     # (workload, policy, launch, tile_n, CTAs per tile): (dram__bytes_read.sum +
     # dram__bytes_write.sum per launch of the chain kernel, hash of the kernel sources the
     # capture was taken with)
-    ("gpt3_mlp_m256", "ROW", "persistent", 256, 2): (309524736 + 17603840, "facbce89ed376179"),
+    ("gpt3_mlp_m256", "ROW", "persistent", 256, 2): (309555712 + 17315072, "6b5a162c4dd8b4f0"),
 }
 
 
@@ -103,8 +103,7 @@ def parse():
     p.add_argument("--trace-out", default="", help="also run STREAM and each listed policy once with the "
                    "in-kernel per-tile trace and write timeline statistics to this JSON file")
     p.add_argument("--profile-runs", type=int, default=0, help="only run the first policy of --policies this many "
-                   "times after 3 warm-up runs (for a profiler; launched without the cooperative attribute), "
-                   "then exit without a bench line")
+                   "times after 3 warm-up runs (for a profiler), then exit without a bench line")
     return p.parse_args()
 
 
@@ -555,9 +554,7 @@ def main():
 
     pols = [p.strip().upper() for p in a.policies.split(",") if p.strip()]
     if a.profile_runs > 0:
-        # ncu cannot replay a cooperative cluster launch; the grid is sized to the resident
-        # CTAs (pairs) either way, and under the profiler nothing else runs on the GPU
-        ch = setup.chain(pols[0], flags=cs.FLAG_NO_COOPERATIVE)
+        ch = setup.chain(pols[0])
         for _ in range(3 + a.profile_runs):
             setup.run(ch)
         st, code, _ = ch.check()

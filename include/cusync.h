@@ -91,11 +91,12 @@ typedef enum {
   CUSYNC_CHAIN_ATTENTION = 3
 } cusync_chain_kind_t;
 
-/* How the two grids are made co-resident so that a waiting consumer can never starve
- * the producer ([cuSync] §IV-B "Stage Processing Order"; [CUDA-FGS] §4.6.5). */
+/* How the stages are launched so that a waiting consumer can never starve the producer
+ * ([cuSync] §IV-B "Stage Processing Order"; [CUDA-FGS] §4.6.5). */
 typedef enum {
-  /* One persistent kernel (cooperative launch: every CTA resident) with a single tile
-   * queue holding all producer tiles before all consumer tiles. */
+  /* One persistent kernel with a single tile queue holding all producer tiles before all
+   * consumer tiles; every tile is claimed from a counter by a running CTA, so every tile
+   * a consumer waits on is already held by a running CTA (no co-residency needed). */
   CUSYNC_LAUNCH_PERSISTENT = 0,
   /* Two persistent kernels on one stream; the consumer is launched with programmatic
    * stream serialisation and the producer triggers its dependents at its start. */
@@ -117,12 +118,6 @@ typedef enum {
                                              Synchronization": weight tiles are then
                                              loaded only after the A-tile wait */
 #define CUSYNC_FLAG_TRACE (1u << 1)       /* record a per-tile timeline (cusync_chain_trace) */
-#define CUSYNC_FLAG_NO_COOPERATIVE (1u << 2) /* launch persistent grids without the cooperative
-                                             attribute (for profilers that cannot replay a
-                                             cooperative cluster launch); co-residency then
-                                             rests on the grid being sized to the CTAs or
-                                             pairs that can be resident, on an otherwise idle
-                                             GPU */
 /* Fault injection for tests; each makes a device wait expire, never a GPU fault. */
 #define CUSYNC_DEBUG_SKIP_POST (1u << 8)     /* the producer never posts tile (0,0) */
 #define CUSYNC_DEBUG_SKIP_INIT (1u << 9)     /* SENTINEL: skip the sentinel fill */

@@ -22,7 +22,6 @@ LAUNCH_PERSISTENT, LAUNCH_PDL = range(2)
 (OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NOMEM, ERR_TIMEOUT, ERR_DEVICE) = range(7)
 FLAG_NO_REORDER = 1 << 0
 FLAG_TRACE = 1 << 1
-FLAG_NO_COOPERATIVE = 1 << 2
 DEBUG_SKIP_POST = 1 << 8
 DEBUG_SKIP_INIT = 1 << 9
 

@@ -528,13 +528,13 @@ struct cusync_chain {
 namespace {
 
 template <int BN, int PAIR, bool CHECK>
-cudaError_t launch_chain(const ChainArgs& a, int grid, bool cooperative, bool pdl_secondary, cudaStream_t stream) {
+cudaError_t launch_chain(const ChainArgs& a, int grid, bool pdl_secondary, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(KCfg<BN, PAIR>::threads(CHECK));
   cfg.dynamicSmemBytes = KCfg<BN, PAIR>::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[3];
+  cudaLaunchAttribute attr[2];
   int na = 0;
   if (PAIR == 2) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
@@ -548,36 +548,20 @@ cudaError_t launch_chain(const ChainArgs& a, int grid, bool cooperative, bool pd
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
   }
-  if (cooperative) {
-    attr[na].id = cudaLaunchAttributeCooperative;
-    attr[na].val.cooperative = 1;
-    ++na;
-  }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, chain_kernel<BN, PAIR, CHECK>, a);
-  if (e != cudaSuccess && cooperative && PAIR == 2) {
-    // Cooperative cluster launches may be refused; the grid is already sized to the
-    // clusters that can be resident at once, so launch without the attribute.
-    cudaGetLastError();
-    CUSYNC_LOG("cooperative cluster launch refused (%s); launching without it", cudaGetErrorString(e));
-    cfg.numAttrs = na - 1;
-    e = cudaLaunchKernelEx(&cfg, chain_kernel<BN, PAIR, CHECK>, a);
-  }
-  return e;
+  return cudaLaunchKernelEx(&cfg, chain_kernel<BN, PAIR, CHECK>, a);
 }
 
 template <bool CHECK>
-cudaError_t launch_tiles(const Plan& p, const ChainArgs& a, int grid, bool coop, bool pdl2, cudaStream_t s) {
+cudaError_t launch_tiles(const Plan& p, const ChainArgs& a, int grid, bool pdl2, cudaStream_t s) {
   if (p.pair == 2)
-    return p.bn == 256 ? launch_chain<256, 2, CHECK>(a, grid, coop, pdl2, s)
-                       : launch_chain<128, 2, CHECK>(a, grid, coop, pdl2, s);
-  return p.bn == 256 ? launch_chain<256, 1, CHECK>(a, grid, coop, pdl2, s)
-                     : launch_chain<128, 1, CHECK>(a, grid, coop, pdl2, s);
+    return p.bn == 256 ? launch_chain<256, 2, CHECK>(a, grid, pdl2, s) : launch_chain<128, 2, CHECK>(a, grid, pdl2, s);
+  return p.bn == 256 ? launch_chain<256, 1, CHECK>(a, grid, pdl2, s) : launch_chain<128, 1, CHECK>(a, grid, pdl2, s);
 }
 
-cudaError_t launch_any(const Plan& p, const ChainArgs& a, int grid, bool coop, bool pdl2, cudaStream_t s) {
-  return a.sentinel_check ? launch_tiles<true>(p, a, grid, coop, pdl2, s) : launch_tiles<false>(p, a, grid, coop, pdl2, s);
+cudaError_t launch_any(const Plan& p, const ChainArgs& a, int grid, bool pdl2, cudaStream_t s) {
+  return a.sentinel_check ? launch_tiles<true>(p, a, grid, pdl2, s) : launch_tiles<false>(p, a, grid, pdl2, s);
 }
 
 // The launches of one chain run: sentinel fill, then one fused persistent kernel or the
@@ -599,8 +583,7 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
     A.first_stage = 0;
     A.last_stage = p.nst - 1;
     A.pdl_role = 0;
-    const bool coop = !(d.flags & CUSYNC_FLAG_NO_COOPERATIVE);
-    e = launch_any(p, A, g.fused, coop, false, stream);
+    e = launch_any(p, A, g.fused, false, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fused chain launch");
     return CUSYNC_OK;
   }
@@ -612,9 +595,7 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
     A.first_stage = s;
     A.last_stage = s;
     A.pdl_role = pdl ? ((s + 1 < p.nst ? 1 : 0) | (s > 0 ? 2 : 0)) : 0;
-    // K-split units of the first stage wait for one another: its CTAs must all be resident.
-    const bool coop = s == 0 && p.geo[0].ksplit > 1 && !(d.flags & CUSYNC_FLAG_NO_COOPERATIVE);
-    e = launch_any(p, A, g.stage[s], coop, /*pdl2=*/pdl && s > 0, stream);
+    e = launch_any(p, A, g.stage[s], /*pdl2=*/pdl && s > 0, stream);
     if (e != cudaSuccess) return cuda_fail(e, s == 0 ? "producer launch" : "consumer launch");
   }
   return CUSYNC_OK;
