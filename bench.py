@@ -727,7 +727,9 @@ def sweep(a, torch, cs, synth, out_path):
     Written to a file; not a bench line."""
     names = [n for n in a.sweep.split(",") if n] or list(synth.WORKLOADS)
     results = []
-    variants = [(1, -1, 2), (1, -1, 1), (16, -1, 2)]
+    # (raster rows, L2 prefetch, CTAs per tile; 0 = the planner's choice): every policy and
+    # launch mode on the planner's tiling, Stream/Row/Tile on the others
+    variants = [(1, -1, 0), (1, -1, 1), (1, -1, 2), (16, -1, 0)]
     for name in names:
         wl = synth.WORKLOADS[name]
         inputs = synth.workload_inputs(wl, seed=0)
