@@ -485,6 +485,18 @@ def trace_stats(torch, setup, policy, launch):
     w = (T["t_ready"] - T["t_claim"])[stage == 1]
     out["consumer_wait_us"] = {"median": float(np.median(w)), "p90": float(np.percentile(w, 90)),
                                "max": float(w.max())}
+    # debug counters per consumer tile: semaphore reads of its waits (probes and polls),
+    # A k-blocks loaded again under the sentinel check, and the MMA issuer's SM cycles
+    # spent waiting for stages (landed, or checked) and the checkers' cycles, per k-block
+    cons = [r for r in recs if r["stage"] == 1]
+    kb1 = max(1, info.k_blocks[1])
+    polls = np.array([r["polls"] for r in cons], dtype=np.float64)
+    out["consumer_polls"] = {"median": float(np.median(polls)), "max": float(polls.max())}
+    out["sentinel_reloads"] = {"total": int(sum(r["reloads"] for r in cons)),
+                               "max_per_tile": int(max(r["reloads"] for r in cons))}
+    out["consumer_clk_per_kblock"] = {
+        "mma_wait": float(np.median([r["land_clk"] / kb1 for r in cons])),
+        "check": float(np.median([r["check_clk"] / kb1 for r in cons]))}
     return out
 
 
