@@ -23,6 +23,14 @@ the GPU receives:
                                            q*stride + s - pad, c] * w[o,r,s,c]
   No bias, no activation after the second convolution, no residual add.
 
+* Convolution stack ([cuSync] §II-B "ResNet", Table ``tab:resnet-sizes``: each layer of
+  ResNet-38 is a pair of 3x3 convolutions with the same kernel size and channels, and a
+  group of layers repeats that pair): N convolutions in a row,
+      h_0 = x,  h_s = bf16(relu(conv(h_{s-1}, w_s)))  for s = 1 .. N-1,
+      y = conv(h_{N-1}, w_N)
+  so a stack of two is the conv pair above.  Same reading as the pair: ReLU after every
+  convolution but the last, no bias, no residual add.
+
 * Self-attention block ([cuSync] §II-B, Fig. ``fig:gpt-3:attention``):
       XQKV = X x QKV               QKV [K, 3*N1]; stored in bf16
       XQ, XV, XK = the column blocks [0,N1), [N1,2N1), [2N1,3N1) of XQKV
@@ -103,6 +111,20 @@ def conv_relu_chain(x, w1, w2, stride=1, pad=1):
     H = bf16_intermediate(relu(y1))
     Y = conv2d_nhwc(H, w2, stride, pad)
     return H, Y
+
+
+def conv_stack(x, ws, stride=1, pad=1):
+    """Return (hs, y) of the convolution stack: hs[s] is the bf16 intermediate written by
+    stage s (s = 0 .. N-2), y = the last convolution in fp64.  ws is a sequence of KRSC
+    weight tensors, one per stage."""
+    if len(ws) < 1:
+        raise ValueError("a stack needs at least one convolution")
+    h = _as64(x)
+    hs = []
+    for w in ws[:-1]:
+        h = bf16_intermediate(relu(conv2d_nhwc(h, w, stride, pad)))
+        hs.append(h)
+    return hs, conv2d_nhwc(h, ws[-1], stride, pad)
 
 
 def mlp_gelu_rows(X, W1, W2, rows):

@@ -153,6 +153,20 @@ def data_deps(chain, m, kb):
     return out
 
 
+def war_readers(chain, m, c):
+    """Buffer rotation: the tiles (m', c') of the stage that reads a buffer which stage
+    s + 2 overwrites with its tile (m, c).  In a stack whose intermediates alternate
+    between two buffers, stage s + 2 writes the buffer that stage s wrote and stage s + 1
+    read; every consumer tile (m', c') reads all channels of its input rows, so it is a
+    reader of the region when any of its k-blocks reads an element that (m, c) writes."""
+    w = chain.writes(m, c)
+    readers = set()
+    for mp in range(chain.m_tiles):
+        if any((chain.reads(mp, kb) & w).any() for kb in range(chain.k_blocks)):
+            readers |= {(mp, cp) for cp in range(chain.n_tiles)}
+    return readers
+
+
 def strided_members(chain, G, c):
     """Producer column tiles sharing column c's StridedSync semaphore (distance D = n_tiles / G)."""
     if chain.n_tiles % G:

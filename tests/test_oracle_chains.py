@@ -169,6 +169,72 @@ def test_conv_chain_relu_and_rounding():
     np.testing.assert_allclose(Y, _loop_conv(Hb, w2), rtol=1e-15, atol=1e-15)
 
 
+# ----------------------------------------------------------------- convolution stack
+
+def _delta(c, r=1, s=1, scale=1.0):
+    w = np.zeros((c, 3, 3, c))
+    for i in range(c):
+        w[i, r, s, i] = scale
+    return w
+
+
+def test_conv_stack_brute_force_three_stages():
+    """Every stage by explicit loops: conv, ReLU and bf16 rounding after the first two,
+    nothing after the last."""
+    rng = np.random.default_rng(13)
+    x = _bf16_ints(rng, (1, 4, 3, 2))
+    ws = [_bf16_ints(rng, (2, 3, 3, 2)) / 8 for _ in range(3)]
+    hs, y = chains.conv_stack(x, ws)
+    h = x
+    for s in range(2):
+        h = bf16.canonicalize_zero(bf16.round_to_bf16(np.maximum(_loop_conv(h, ws[s]), 0.0)))
+        np.testing.assert_array_equal(hs[s], h)
+    np.testing.assert_allclose(y, _loop_conv(h, ws[2]), rtol=1e-15, atol=1e-15)
+    assert len(hs) == 2
+
+
+def test_conv_stack_of_two_is_the_pair():
+    rng = np.random.default_rng(14)
+    x = bf16.round_to_bf16(rng.standard_normal((2, 5, 4, 3)))
+    w1 = bf16.round_to_bf16(rng.standard_normal((3, 3, 3, 3)) * 0.2)
+    w2 = bf16.round_to_bf16(rng.standard_normal((3, 3, 3, 3)) * 0.2)
+    hs, y = chains.conv_stack(x, [w1, w2])
+    H, Y = chains.conv_relu_chain(x, w1, w2)
+    np.testing.assert_array_equal(hs[0], H)
+    np.testing.assert_array_equal(y, Y)
+
+
+def test_conv_stack_identity_kernels():
+    """Centre-delta kernels: every convolution is the identity, so every intermediate and
+    the output are relu(x)."""
+    rng = np.random.default_rng(15)
+    x = bf16.round_to_bf16(rng.standard_normal((2, 4, 4, 3)))
+    hs, y = chains.conv_stack(x, [_delta(3)] * 5)
+    for h in hs:
+        np.testing.assert_array_equal(h, np.maximum(x, 0.0))
+    np.testing.assert_array_equal(y, np.maximum(x, 0.0))
+
+
+def test_conv_stack_shifts_accumulate():
+    """Tap (r=1, s=2) moves the image one column left with a zero column entering on the
+    right; on a non-negative image N stages move it N columns."""
+    rng = np.random.default_rng(16)
+    x = np.abs(bf16.round_to_bf16(rng.standard_normal((1, 3, 7, 2))))
+    for n in (2, 3, 4):
+        _, y = chains.conv_stack(x, [_delta(2, r=1, s=2)] * n)
+        np.testing.assert_array_equal(y[:, :, :7 - n], x[:, :, n:])
+        np.testing.assert_array_equal(y[:, :, 7 - n:], 0.0)
+
+
+def test_conv_stack_scales_multiply():
+    """Centre taps of 2 (exact in bf16): N stages multiply a non-negative image by 2^N."""
+    rng = np.random.default_rng(17)
+    x = np.abs(bf16.round_to_bf16(rng.standard_normal((1, 3, 3, 4))))
+    hs, y = chains.conv_stack(x, [_delta(4, scale=2.0)] * 4)
+    np.testing.assert_array_equal(y, 16.0 * x)
+    np.testing.assert_array_equal(hs[1], 4.0 * x)
+
+
 # ----------------------------------------------------------------- self-attention block
 
 def bf16_vals(a):

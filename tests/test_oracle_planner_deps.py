@@ -165,3 +165,33 @@ def test_sentinel_example_closed_form():
     # element 1023 - 5 of tile 0 came from the -0.0 input and must be +0.0
     assert out[1018] == 0.0 and not np.signbit(out[1018])
     assert out[511] == 0.0 and not np.signbit(out[511])
+
+
+@pytest.mark.parametrize("chain", [
+    deps.ConvChain(N=2, P=6, Q=5, C=128, TH=2, BNo=64, BK=64),
+    deps.ConvChain(N=1, P=7, Q=3, C=128, TH=3, BNo=128, BK=64),
+    deps.ConvChain(N=1, P=5, Q=4, C=64, TH=1, BNo=64, BK=64),
+])
+@pytest.mark.parametrize("policy", ["ROW", "TILE"])
+def test_two_buffer_rotation_is_covered_by_the_waits(chain, policy):
+    """A stack whose intermediates alternate between two buffers overwrites, in stage
+    s + 2, the buffer that stage s + 1 reads.  Before a stage-(s + 2) tile stores (after
+    its last k-block) it has waited for every stage-(s + 1) tile its policy names; those
+    must include every tile that reads the region it overwrites (a tile posts only after
+    its own k-blocks have read their input)."""
+    for m in range(chain.m_tiles):
+        waited = set().union(*deps.wait_sets(chain, policy, m))
+        for c in range(chain.n_tiles):
+            readers = deps.war_readers(chain, m, c)
+            assert readers, (m, c)
+            assert readers <= waited, (m, c, sorted(readers - waited))
+
+
+def test_two_buffer_rotation_needs_every_k_block_of_waits():
+    """The property above holds only once all of a tile's k-blocks have waited: the
+    TileSync waits before the first k-block alone miss readers (rows below the tile), so
+    the store must follow the last wait."""
+    chain = deps.ConvChain(N=1, P=6, Q=4, C=128, TH=2, BNo=64, BK=64)
+    first = deps.wait_sets(chain, "TILE", 1)[0]
+    assert not deps.war_readers(chain, 1, 0) <= first
+
