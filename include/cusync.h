@@ -88,7 +88,18 @@ typedef enum {
    * STRIDED_TILE = StridedSync (G = 3: a head's Q, V and K tiles share one semaphore)
    * then TileSync, STREAM = three stream-ordered kernels; SENTINEL is not offered.
    * N1 must be a multiple of the tile width and of 128. */
-  CUSYNC_CHAIN_ATTENTION = 3
+  CUSYNC_CHAIN_ATTENTION = 3,
+  /* A stack of `stages` 3x3 convolutions ([cuSync] Table tab:resnet-sizes: a ResNet-38
+   * layer group repeats pairs of convolutions with equal channels): h_1 =
+   * ReLU(conv(x, w_1)) (bf16), h_s = ReLU(conv(h_{s-1}, w_s)), y = conv(h_{N-1}, w_N);
+   * stride 1, pad 1, NHWC images of c channels throughout (c == k_out), all in one
+   * persistent kernel (or one kernel per stage under STREAM and PDL).  Every stage waits
+   * on the one before it with the chain's policy (ROW, TILE or SENTINEL).  The
+   * intermediates live in a caller-owned workspace (cusync_chain_info_t::work_bytes):
+   * two buffers used in turn under ROW, TILE and STREAM (a stage overwrites the input of
+   * the stage before it only after its own waits have covered every reader), one per
+   * intermediate under SENTINEL (the sentinel fill precedes the run). */
+  CUSYNC_CHAIN_CONV_STACK = 4
 } cusync_chain_kind_t;
 
 /* How the stages are launched so that a waiting consumer can never starve the producer
@@ -158,6 +169,8 @@ typedef struct {
                                         most 4); when they fill more than half of one
                                         wave, 2; else none; never fewer than 16 k-blocks
                                         per unit.  1 = none */
+  int32_t stages;                    /* CONV_STACK: convolutions in the stack, 2..16 */
+  int32_t _pad1;
 } cusync_chain_desc_t;
 
 /* Wave arithmetic of a two-kernel chain ([cuSync] §II-A "Thread block Wave Execution",
@@ -217,6 +230,9 @@ typedef struct {
   int32_t m_tiles2, n_tiles2, k_blocks2, n_out2, grid2;
   int32_t num_flags_pw;       /* semaphores the pointwise stage waits on */
   int32_t strided_group_pw, strided_distance_pw;
+  int32_t work_buffers;       /* CONV_STACK: intermediate buffers in the workspace */
+  int64_t work_bytes;         /* CONV_STACK: bytes of the caller's workspace (n*h*w*c
+                                 bf16 per buffer) */
 } cusync_chain_info_t;
 
 /* Latency model of one chain run, in nanoseconds (cusync_predict_policies).  A tile
@@ -295,6 +311,13 @@ cusync_status_t cusync_run_mlp(cusync_chain_t chain, const void* X, const void* 
  * cusync_run_mlp. */
 cusync_status_t cusync_run_conv_chain(cusync_chain_t chain, const void* x, const void* w1, const void* w2, void* y1,
                                       void* y2, cusync_stream_t stream);
+
+/* Run a CONV_STACK chain: x [n,h,w,c], w [stages][c,3,3,c] (the stages' KRSC weights one
+ * after the other), work (caller-owned workspace of cusync_chain_info_t::work_bytes, which
+ * receives the intermediates; its contents on return are unspecified) and y
+ * ([n,h,w,c], the last convolution).  Same rules as cusync_run_mlp. */
+cusync_status_t cusync_run_conv_stack(cusync_chain_t chain, const void* x, const void* w, void* work, void* y,
+                                      cusync_stream_t stream);
 
 /* Run an ATTENTION chain on `stream` ([cuSync] Fig. fig:gpt-3:attention): writes XQKV
  * (first intermediate, [M, 3*N1] bf16: the XQ, XV and XK blocks side by side), XDot

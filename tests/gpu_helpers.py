@@ -9,17 +9,17 @@ from tile_level_sync_gb300 import synth
 RTOL_ABS = 2e-2   # |gpu - ref| <= 2e-2 * max(1, |ref|)
 
 
-def within_tol(gpu, ref):
+def within_tol(gpu, ref, scale=1.0):
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     err = np.abs(gpu - ref)
-    bound = RTOL_ABS * np.maximum(1.0, np.abs(ref))
+    bound = scale * RTOL_ABS * np.maximum(1.0, np.abs(ref))
     bad = err > bound
     return (not np.any(bad)), float(np.max(err / bound)) if err.size else 0.0
 
 
-def assert_within_tol(gpu, ref, what):
-    ok, worst = within_tol(gpu, ref)
+def assert_within_tol(gpu, ref, what, scale=1.0):
+    ok, worst = within_tol(gpu, ref, scale)
     assert ok, f"{what}: worst error / bound = {worst:.3f}"
 
 

@@ -416,3 +416,70 @@ def test_attention_refusals():
     # the latency model covers the two-stage chains only
     with pytest.raises(cs.CusyncError):
         cs.cusync_predict_policies(cs.make_desc(cs.CHAIN_ATTENTION, "ROW", **base))
+
+
+STACK_CASES = [
+    dict(n=2, h=14, w=14, c=128, stages=4, tile_n=128),   # two row tiles per image
+    dict(n=1, h=9, w=30, c=64, stages=3, tile_n=128),     # 4 image rows per tile, ragged columns
+    dict(n=1, h=5, w=100, c=128, stages=5, tile_n=256),   # 1 image row per tile
+]
+
+
+@pytest.mark.parametrize("case", STACK_CASES)
+@pytest.mark.parametrize("policy", ["ROW", "TILE"])
+def test_stack_waits_match_oracle_and_cover_rotation(case, policy):
+    """Every stage of a convolution stack waits on the one before it exactly as the
+    oracle's Conv2DTileSync sets say (one set of semaphores per boundary), and the union
+    of a tile's waits covers every tile that reads what it overwrites when the
+    intermediates alternate between two buffers."""
+    desc = cs.make_desc(cs.CHAIN_CONV_STACK, policy, num_sms=148, **case)
+    info = cs.cusync_plan_info(desc)
+    stages = case["stages"]
+    assert info.nst == stages and info.work_buffers == min(2, stages - 1)
+    assert info.work_bytes == info.work_buffers * case["n"] * case["h"] * case["w"] * case["c"] * 2
+    ch = deps.ConvChain(N=case["n"], P=case["h"], Q=case["w"], C=case["c"], TH=info.conv_rows_per_tile,
+                        BNo=info.n_out[0], BK=info.tile_k)
+    nt = info.n_tiles[0]
+    assert ch.n_tiles == nt and ch.m_tiles == info.m_tiles[1] and ch.k_blocks == info.k_blocks[1]
+    assert info.num_flags % (stages - 1) == 0
+    stride = info.num_flags // (stages - 1)
+    for m in range(ch.m_tiles):
+        got = [set() for _ in range(ch.k_blocks)]
+        for kb, flag, per_run in cs.cusync_consumer_waits(desc, m):
+            mem = _members(policy, flag, nt, info.strided_distance, info.strided_group)
+            assert per_run == len(mem) and 0 <= flag < stride
+            got[kb] |= mem
+        assert got == deps.wait_sets(ch, policy, m), (policy, m)
+        waited = set().union(*got)
+        for c in range(nt):
+            assert deps.war_readers(ch, m, c) <= waited, (m, c)
+
+
+def test_stack_plan_and_refusals():
+    base = dict(n=2, h=14, w=14, c=256, num_sms=152)
+    act = 2 * 14 * 14 * 256 * 2
+    for pol, nbuf in (("ROW", 2), ("TILE", 2), ("STREAM", 2), ("SENTINEL", 11)):
+        info = cs.cusync_plan_info(cs.make_desc(cs.CHAIN_CONV_STACK, pol, stages=12, **base))
+        assert info.nst == 12 and info.work_buffers == nbuf and info.work_bytes == nbuf * act
+        assert info.m_tiles[0] == info.m_tiles[1] and info.k_blocks[0] == info.k_blocks[1]  # uniform stages
+        per = {"ROW": info.m_tiles[0], "TILE": info.m_tiles[0] * info.n_tiles[0]}.get(pol, 0)
+        assert info.num_flags == per * 11
+    info = cs.cusync_plan_info(cs.make_desc(cs.CHAIN_CONV_STACK, "ROW", stages=2, **base))
+    assert info.work_buffers == 1 and info.work_bytes == act
+    bad = [
+        (dict(stages=1), cs.ERR_UNSUPPORTED), (dict(stages=17), cs.ERR_UNSUPPORTED),
+        (dict(stages=4, k_out=128), cs.ERR_UNSUPPORTED),             # channels must stay equal
+        (dict(stages=4, cta_pair=2), cs.ERR_UNSUPPORTED),
+        (dict(stages=4, policy=cs.POLICY_STRIDED_TILE), cs.ERR_UNSUPPORTED),
+        (dict(stages=4, ksplit=2), cs.ERR_UNSUPPORTED),
+    ]
+    for extra, status in bad:
+        kw = dict(base)
+        pol = extra.pop("policy", cs.POLICY_ROW)
+        kw.update(extra)
+        with pytest.raises(cs.CusyncError) as e:
+            cs.cusync_plan_info(cs.make_desc(cs.CHAIN_CONV_STACK, pol, **kw))
+        assert e.value.status == status, extra
+    with pytest.raises(cs.CusyncError) as e:
+        cs.cusync_plan_info(cs.make_desc(cs.CHAIN_CONV_STACK, "ROW", n=1, h=8, w=8, c=96, stages=3, num_sms=152))
+    assert e.value.status == cs.ERR_UNSUPPORTED

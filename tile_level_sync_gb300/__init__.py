@@ -17,7 +17,7 @@ c_i32, c_i64, c_u32, c_u64, c_dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_uin
 
 # ---------------------------------------------------------------- enums (cusync.h)
 POLICY_STREAM, POLICY_ROW, POLICY_TILE, POLICY_STRIDED_TILE, POLICY_SENTINEL, POLICY_AUTO = range(6)
-CHAIN_MLP_GELU, CHAIN_MLP_SWIGLU, CHAIN_CONV_RELU, CHAIN_ATTENTION = range(4)
+CHAIN_MLP_GELU, CHAIN_MLP_SWIGLU, CHAIN_CONV_RELU, CHAIN_ATTENTION, CHAIN_CONV_STACK = range(5)
 LAUNCH_PERSISTENT, LAUNCH_PDL = range(2)
 (OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NOMEM, ERR_TIMEOUT, ERR_DEVICE) = range(7)
 FLAG_NO_REORDER = 1 << 0
@@ -36,6 +36,7 @@ class cusync_chain_desc_t(ctypes.Structure):
         ("n", c_i32), ("h", c_i32), ("w", c_i32), ("c", c_i32), ("k_out", c_i32),
         ("tile_n", c_i32), ("strided_group", c_i32), ("flags", c_u32), ("num_sms", c_i32), ("raster_rows", c_i32),
         ("timeout_ns", c_u64), ("l2_prefetch", c_i32), ("cta_pair", c_i32), ("ksplit", c_i32),
+        ("stages", c_i32), ("_pad1", c_i32),
     ]
 
 
@@ -64,6 +65,7 @@ class cusync_chain_info_t(ctypes.Structure):
         ("policy", c_i32), ("ksplit", c_i32), ("kb_per_split", c_i32),
         ("nst", c_i32), ("m_tiles2", c_i32), ("n_tiles2", c_i32), ("k_blocks2", c_i32), ("n_out2", c_i32),
         ("grid2", c_i32), ("num_flags_pw", c_i32), ("strided_group_pw", c_i32), ("strided_distance_pw", c_i32),
+        ("work_buffers", c_i32), ("work_bytes", c_i64),
     ]
 
 
@@ -85,6 +87,7 @@ _SIGNATURES = {
     "cusync_create_chain": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), ctypes.POINTER(_VP)]),
     "cusync_run_mlp": (c_i32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "cusync_run_conv_chain": (c_i32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "cusync_run_conv_stack": (c_i32, [_VP, _VP, _VP, _VP, _VP, _VP]),
     "cusync_run_attention": (c_i32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
     "cusync_chain_check": (c_i32, [_VP, _VP, ctypes.POINTER(c_u32), ctypes.POINTER(c_u32)]),
     "cusync_chain_reset": (c_i32, [_VP, _VP]),
@@ -167,13 +170,13 @@ def status_string(status):
 
 def make_desc(kind=CHAIN_MLP_GELU, policy=POLICY_ROW, launch=LAUNCH_PERSISTENT, M=0, K=0, N1=0, N2=0,
               n=0, h=0, w=0, c=0, k_out=0, tile_n=0, strided_group=0, flags=0, num_sms=0, timeout_ns=0,
-              raster_rows=0, l2_prefetch=0, cta_pair=0, ksplit=0):
+              raster_rows=0, l2_prefetch=0, cta_pair=0, ksplit=0, stages=0):
     if isinstance(policy, str):
         policy = POLICY_NAMES[policy]
     return cusync_chain_desc_t(kind=kind, policy=policy, launch=launch, M=M, K=K, N1=N1, N2=N2, n=n, h=h, w=w,
                                c=c, k_out=k_out, tile_n=tile_n, strided_group=strided_group, flags=flags,
                                num_sms=num_sms, timeout_ns=timeout_ns, raster_rows=raster_rows,
-                               l2_prefetch=l2_prefetch, cta_pair=cta_pair, ksplit=ksplit)
+                               l2_prefetch=l2_prefetch, cta_pair=cta_pair, ksplit=ksplit, stages=stages)
 
 
 # ---------------------------------------------------------------- the C functions
@@ -267,6 +270,11 @@ def cusync_run_conv_chain(chain, x, w1, w2, y1, y2, stream=None):
            "cusync_run_conv_chain")
 
 
+def cusync_run_conv_stack(chain, x, w, work, y, stream=None):
+    _check(load().cusync_run_conv_stack(chain, _ptr(x), _ptr(w), _ptr(work), _ptr(y), _stream(stream)),
+           "cusync_run_conv_stack")
+
+
 def cusync_run_attention(chain, X, Wqkv_t, W2t, XQKV, XDot, Y, stream=None):
     _check(load().cusync_run_attention(chain, _ptr(X), _ptr(Wqkv_t), _ptr(W2t), _ptr(XQKV), _ptr(XDot), _ptr(Y),
                                        _stream(stream)), "cusync_run_attention")
@@ -318,8 +326,12 @@ class Chain:
         self.handle = cusync_create_chain(desc)
 
     def run(self, a, w1, w2, h, y, stream=None, h2=None):
-        """Run the chain; h2 is the second intermediate (XDot) of an attention chain."""
-        if self.desc.kind == CHAIN_CONV_RELU:
+        """Run the chain; h2 is the second intermediate (XDot) of an attention chain.  A
+        convolution stack takes its stacked weights as w1 and its workspace as h (w2
+        unused)."""
+        if self.desc.kind == CHAIN_CONV_STACK:
+            cusync_run_conv_stack(self.handle, a, w1, h, y, stream)
+        elif self.desc.kind == CHAIN_CONV_RELU:
             cusync_run_conv_chain(self.handle, a, w1, w2, h, y, stream)
         elif self.desc.kind == CHAIN_ATTENTION:
             cusync_run_attention(self.handle, a, w1, w2, h, h2, y, stream)

@@ -55,8 +55,17 @@
 namespace cusync {
 
 // Control words in front of the semaphore array.
-// Tile counters and exit counters: one per launch of a chain run (queue 0..2).
-enum : int { CTRL_ERR = 0, CTRL_ERR_DETAIL = 1, CTRL_COUNTER = 2, CTRL_EXIT = 5, CTRL_RUNS = 8, CTRL_WORDS = 16 };
+// Tile counters and exit counters: one per launch of a chain run (queue 0 .. kMaxQueues-1;
+// a run launches at most one kernel per stage).
+constexpr int kMaxQueues = 16;
+enum : int {
+  CTRL_ERR = 0,
+  CTRL_ERR_DETAIL = 1,
+  CTRL_RUNS = 8,
+  CTRL_COUNTER = 16,
+  CTRL_EXIT = CTRL_COUNTER + kMaxQueues,
+  CTRL_WORDS = CTRL_EXIT + kMaxQueues
+};
 // Error classes (bits 31..24 of the error word; bits 23..0 hold the tile index).
 enum : uint32_t { ERRC_FLAG_TIMEOUT = 1, ERRC_SENTINEL_TIMEOUT = 2, ERRC_PIPELINE = 3 };
 // Flag bits shared with cusync.h.
@@ -86,7 +95,8 @@ struct TraceRec {
 };
 
 struct ChainArgs {
-  StageArgs st[3];       // 0 = producer, nst - 1 = the GEMM consumer (attention: 1 = pointwise)
+  StageArgs st[3];       // 0 = producer, nst - 1 = the GEMM consumer (attention: 1 = pointwise);
+                         // convolution stack: 0 = the first stage, 1 = every later stage
   DepCfg dep;            // what the last stage waits for on the stage before it
   DepCfg dep_pw;         // attention: what the pointwise stage waits for on stage 0
   uint32_t* flags;       // semaphores of `dep`
@@ -99,7 +109,12 @@ struct ChainArgs {
   int32_t first_stage;   // stages served by this launch: [first_stage, last_stage]
   int32_t last_stage;
   int32_t tiles0, tiles1, tiles2;
-  int32_t nst;           // stages in the chain: 2, or 3 (attention)
+  int32_t nst;           // stages in the chain: 2, 3 (attention), or a stack's depth
+  int32_t stack;         // convolution stack: stages 1 .. nst-1 share st[1], read the
+                         // intermediate of the stage before them and write their own
+  int32_t nbuf;          // stack: intermediate buffers in st[0].out; stage s writes s % nbuf
+  int32_t flags_stride;  // stack: semaphores per stage boundary (boundary s at s * stride)
+  int64_t buf_elems;     // stack: elements of one intermediate buffer
   uint32_t flags_bits;
   int32_t pdl_role;      // bit 0: trigger dependents at start; bit 1: wait on the primary at exit
   int32_t sentinel_check;
@@ -135,16 +150,37 @@ struct TileRef {
   int32_t nkb;  // k-blocks of the unit
 };
 
+// Work units of stage s.
+__device__ __forceinline__ int32_t stage_tiles(const ChainArgs& a, int32_t s) {
+  return a.stack ? a.tiles0 : (s == 0 ? a.tiles0 : (s == 1 ? a.tiles1 : a.tiles2));
+}
+
+// Operands and geometry of stage s.
+__device__ __forceinline__ const StageArgs& stage_args(const ChainArgs& a, int32_t s) {
+  return a.st[a.stack ? (s > 0 ? 1 : 0) : s];
+}
+
+// Whether stage s reads the output of the stage before it (waits on it, or checks it).
+__device__ __forceinline__ bool stage_consumes(const ChainArgs& a, int32_t s) {
+  return a.stack ? s > 0 : s == a.nst - 1;
+}
+
+// Stack: the intermediate buffer that stage s (< nst - 1) writes.  With two buffers a
+// stage overwrites the input of the stage before it; the tile's own waits have covered
+// every reader of what it overwrites by the time it stores (it stores after its last
+// k-block, and each semaphore it waited on was posted after that tile's reads).
+__device__ __forceinline__ int32_t stack_buf(const ChainArgs& a, int32_t s) { return s % a.nbuf; }
+
 __device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
   // the launch serves stages [first_stage, last_stage], their work units in that order
   int32_t s = a.first_stage, u = t;
   while (s < a.last_stage) {
-    const int32_t n = s == 0 ? a.tiles0 : (s == 1 ? a.tiles1 : a.tiles2);
+    const int32_t n = stage_tiles(a, s);
     if (u < n) break;
     u -= n;
     ++s;
   }
-  const StageGeo& g = a.st[s].g;
+  const StageGeo& g = stage_args(a, s).g;
   int32_t ks = 0, kb0 = 0, nkb = g.k_blocks;
   if (g.ksplit > 1) {
     ks = u % g.ksplit;
@@ -162,7 +198,8 @@ __device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
 
 // Index of queue position t in the chain's tile numbering (producer tiles first).
 __device__ __forceinline__ int32_t chain_tile(const ChainArgs& a, int32_t t) {
-  return t + (a.first_stage >= 1 ? a.tiles0 : 0) + (a.first_stage >= 2 ? a.tiles1 : 0);
+  for (int32_t s = 0; s < a.first_stage; ++s) t += stage_tiles(a, s);
+  return t;
 }
 
 __device__ __forceinline__ uint32_t a_tile_bytes(const StageGeo& g) {
@@ -174,7 +211,7 @@ __device__ __forceinline__ uint32_t a_tile_bytes(const StageGeo& g) {
 template <int PAIR>
 __device__ __forceinline__ void issue_a(const ChainArgs& a, const TileRef& tr, int32_t kb, uint32_t rank, void* dst,
                                         uint64_t* bar, uint64_t pol, bool to_leader = false) {
-  const StageArgs& S = a.st[tr.s];
+  const StageArgs& S = stage_args(a, tr.s);
   if (S.g.a_mode == AMODE_GEMM) {
     const int32_t row = tr.m * (128 * PAIR) + (int32_t)rank * 128;
     if (PAIR == 2 && to_leader) ptx::tma_load_2d_to_leader(dst, &S.tmA, ptx::mapa(bar, 0), kb * kBK, row, pol);
@@ -185,7 +222,10 @@ __device__ __forceinline__ void issue_a(const ChainArgs& a, const TileRef& tr, i
     const int32_t tap = kb / S.g.cblocks, cb = kb % S.g.cblocks;
     const int32_t r = tap / 3, s = tap % 3;
     const int32_t n = tr.m / S.g.tpi, hb = tr.m % S.g.tpi;
-    ptx::tma_load_4d(dst, &S.tmA, bar, cb * kBK, s - 1, hb * S.g.th + r - 1, n, pol);
+    if (a.stack && tr.s > 0)  // the stack's intermediates: one more coordinate, the buffer
+      ptx::tma_load_5d(dst, &S.tmA, bar, cb * kBK, s - 1, hb * S.g.th + r - 1, n, stack_buf(a, tr.s - 1), pol);
+    else
+      ptx::tma_load_4d(dst, &S.tmA, bar, cb * kBK, s - 1, hb * S.g.th + r - 1, n, pol);
   }
 }
 
@@ -201,20 +241,6 @@ __device__ __forceinline__ int32_t b_row(const StageArgs& S, const TileRef& tr, 
     return which == 0 ? row0 : S.b_half_rows + row0;
   }
   return tr.c * BN + (PAIR == 2 ? (int32_t)rank * (BN / 2) : 0);
-}
-
-template <int BN, int PAIR>
-__device__ __forceinline__ void issue_b(const ChainArgs& a, const TileRef& tr, int32_t kb, uint32_t rank, uint8_t* dst,
-                                        uint64_t* bar, uint64_t pol, bool to_leader = false) {
-  const StageArgs& S = a.st[tr.s];
-  if (PAIR == 1 && S.g.epi == EPI_SWIGLU) {
-    ptx::tma_load_2d(dst, &S.tmB, bar, kb * kBK, b_row<BN, PAIR>(S, tr, rank, 0), pol);
-    ptx::tma_load_2d(dst + (BN / 2) * 128, &S.tmB, bar, kb * kBK, b_row<BN, PAIR>(S, tr, rank, 1), pol);
-  } else if (PAIR == 2 && to_leader) {
-    ptx::tma_load_2d_to_leader(dst, &S.tmB, ptx::mapa(bar, 0), kb * kBK, b_row<BN, PAIR>(S, tr, rank, 0), pol);
-  } else {
-    ptx::tma_load_2d(dst, &S.tmB, bar, kb * kBK, b_row<BN, PAIR>(S, tr, rank, 0), pol);
-  }
 }
 
 // Prefetch into L2, one 128-byte line per row, the k-block kb of `rows` rows starting at
@@ -288,7 +314,7 @@ __device__ __forceinline__ float silu_f(float g) {
 __device__ __noinline__ void pointwise_tile(const ChainArgs& args, const TileRef& tr, int32_t t, int row,
                                             uint64_t* pw_done, uint32_t pw_parity, uint32_t runs, bool leader,
                                             uint64_t pto, volatile int32_t* abort_flag) {
-  const StageArgs& SA = args.st[tr.s];
+  const StageArgs& SA = stage_args(args, tr.s);
   const StageGeo& g = SA.g;
   Wait w[3];
   const int nw = pointwise_waits(args.dep_pw, tr.m, tr.c, w);
@@ -418,13 +444,15 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
   // on the leader's `full` barriers, which count the bytes of both CTAs.  A consumer tile
   // under the sentinel policy is not: each CTA's copies complete locally, its checker
   // validates them and arrives on the leader's `ready` barrier.
-  auto direct_tile = [&](const TileRef& tr) { return kPair && !(CHECK && tr.s == args.nst - 1); };
+  auto direct_tile = [&](const TileRef& tr) { return kPair && !(CHECK && stage_consumes(args, tr.s)); };
 
-  if (args.pdl_role & 1) ptx::pdl_launch_dependents();
   // Run number of this launch.  Semaphores count up across runs (run r waits for r times
   // the posts of one run), and the count of finished runs lives in device memory, so the
   // same launch can be replayed from a CUDA graph.  Read before the first barrier: the
-  // launch that increments it (below) does so only after every CTA has passed that point.
+  // launch that increments it (below: the last stage's, once all of its CTAs have claimed
+  // their last tile) does so only after every CTA of its own launch has passed that point,
+  // and a later stage's launch starts only after every CTA of this one has triggered its
+  // dependents, which it does after that barrier.
   uint32_t epoch = 0;
 
   if (warp == 1) {
@@ -469,19 +497,22 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
     epoch = ptx::ld_relaxed_gpu(args.ctrl + CTRL_RUNS) + 1u;
     *run_no = epoch;
     for (int s = args.first_stage; s <= args.last_stage; ++s) {
-      ptx::prefetch_tmap(&args.st[s].tmA);
-      ptx::prefetch_tmap(&args.st[s].tmB);
-      if (args.st[s].g.a_mode == AMODE_GEMM) ptx::prefetch_tmap(&args.st[s].tmO);
+      const StageArgs& S = stage_args(args, s);
+      ptx::prefetch_tmap(&S.tmA);
+      ptx::prefetch_tmap(&S.tmB);
+      if (S.g.a_mode == AMODE_GEMM) ptx::prefetch_tmap(&S.tmO);
+      if (args.stack && s >= 1) break;  // the later stages of a stack share these maps
     }
   }
   ptx::tc_fence_before();
   __syncthreads();
   if (kPair) ptx::cluster_sync();  // the peer's barriers exist before any remote arrive
   ptx::tc_fence_after();
+  if (args.pdl_role & 1) ptx::pdl_launch_dependents();  // after this CTA read the run number
   const uint32_t tmem_base = *tmem_slot;
 
   int32_t total = 0;
-  for (int s = args.first_stage; s <= args.last_stage; ++s) total += s == 0 ? args.tiles0 : (s == 1 ? args.tiles1 : args.tiles2);
+  for (int s = args.first_stage; s <= args.last_stage; ++s) total += stage_tiles(args, s);
   const uint64_t pto = args.pipe_timeout_ns;
 
   // Arrive on "consumed" for ring slot `slot` (the leader's barrier in a pair).
@@ -538,7 +569,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         if (done) break;
 
         const TileRef tr = decode_tile(args, t);
-        const StageArgs& SA = args.st[tr.s];
+        const StageArgs& SA = stage_args(args, tr.s);
         const int32_t KB = tr.nkb;            // k-blocks of this work unit
         const int32_t kx0 = tr.kb0 * kBK;     // its first reduction coordinate
         const uint32_t tx = a_tile_bytes(SA.g) + (uint32_t)C::kBBytes;
@@ -567,7 +598,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           ++pw_seen;
           continue;
         }
-        const bool cons = (tr.s == args.nst - 1);
+        const bool cons = stage_consumes(args, tr.s);
         GemmDepTracker gdt;
         gdt.reset();
         ConvDepTracker cdt;  // touched (stack arrays) only by convolution tiles
@@ -588,6 +619,13 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         // the checker waits on; every other tile on full, which only the MMA issuer waits on
         const bool checked = CHECK && cons;
         uint64_t* const lbar = checked ? cfull : full;
+        // Stack: stage s waits on the semaphores of the boundary it consumes (s - 1), reads
+        // its input from that stage's buffer (the fifth coordinate of the intermediates'
+        // map) and its weights from slice s of the stacked weights (the third coordinate).
+        const bool stacked = args.stack != 0;
+        const uint32_t* const wflags = args.flags + (stacked && tr.s > 0 ? (tr.s - 1) * args.flags_stride : 0);
+        const int32_t wnflags = stacked ? args.flags_stride : args.num_flags;
+        const int32_t a_buf = stacked && tr.s > 0 ? stack_buf(args, tr.s - 1) : -1;
         // k-blocks at which the consumer may have to wait (dep_kblock): every dep_every-th
         // k-block of a GEMM; for a convolution the first 64 k-blocks by a bit mask, every
         // later one by dep_every = 1.
@@ -623,7 +661,10 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           }
           uint8_t* dst = smem_b(st);
           stage_kind[st] = checked ? 1 : 0;
-          if (to_leader) {
+          if (stacked) {
+            ptx::mbar_arrive_expect_tx(&lbar[st], txs);
+            ptx::tma_load_3d(dst, tmB, &lbar[st], kx0 + kbb * kBK, brow0, tr.s, pol_b);
+          } else if (to_leader) {
             ptx::tma_load_2d_to_leader(dst, tmB, ptx::mapa(&full[st], 0), kx0 + kbb * kBK, brow0, pol_b);
           } else {
             ptx::mbar_arrive_expect_tx(&lbar[st], txs);
@@ -652,9 +693,9 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
             const uint32_t target = epoch * w[i].per_run;
             if (target == rc_target && rc_lo <= f && f < rc_hi) continue;
             uint32_t v[kProbe];
-            const int32_t cnt = min(kProbe, args.num_flags - f);
+            const int32_t cnt = min(kProbe, wnflags - f);
 #pragma unroll
-            for (int q = 0; q < kProbe; ++q) v[q] = q < cnt ? ptx::ld_relaxed_gpu(args.flags + f + q) : 0u;
+            for (int q = 0; q < kProbe; ++q) v[q] = q < cnt ? ptx::ld_relaxed_gpu(wflags + f + q) : 0u;
             int32_t nready = 0;
 #pragma unroll
             for (int q = 0; q < kProbe; ++q)
@@ -675,7 +716,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
                 __nanosleep(backoff);
                 if (backoff < 256) backoff <<= 1;
               }
-              if ((int32_t)(ptx::ld_relaxed_gpu(args.flags + f) - target) >= 0) break;
+              if ((int32_t)(ptx::ld_relaxed_gpu(wflags + f) - target) >= 0) break;
               if ((++iter & 15u) == 0) {
                 if (ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u) break;
                 if (ptx::globaltimer() - t0 > args.timeout_ns) {
@@ -732,7 +773,10 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
             if (dep_kb && reorder) wait_deps(kb);
             if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
             const int st = (int)((it + (uint32_t)kb) % S);
-            ptx::tma_load_4d(smem_a(st), tmA, &lbar[st], cv_cb * kBK, cv_s - 1, cv_h0 + cv_r, cv_img, pol_a);
+            if (a_buf >= 0)
+              ptx::tma_load_5d(smem_a(st), tmA, &lbar[st], cv_cb * kBK, cv_s - 1, cv_h0 + cv_r, cv_img, a_buf, pol_a);
+            else
+              ptx::tma_load_4d(smem_a(st), tmA, &lbar[st], cv_cb * kBK, cv_s - 1, cv_h0 + cv_r, cv_img, pol_a);
             if (++cv_cb == SA.g.cblocks) {
               cv_cb = 0;
               if (++cv_s == 3) {
@@ -795,7 +839,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       ++tcount;
       if (t < 0) break;
       const TileRef tr = decode_tile(args, t);
-      const StageGeo& g = args.st[tr.s].g;
+      const StageGeo& g = stage_args(args, tr.s).g;
       if (g.a_mode == AMODE_POINTWISE) continue;  // no MMA
       const int acc = acount & 1;
       const uint32_t apar = ((acount >> 1) & 1u) ^ 1u;
@@ -808,7 +852,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         ptx::tc_fence_after();
       }
       const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-      const bool checked = CHECK && tr.s == args.nst - 1;
+      const bool checked = CHECK && stage_consumes(args, tr.s);
       // The peer of a pair issues nothing: its direct copies complete on the leader's
       // `full`, and its checker arrives on the leader's `ready`.
       if (!leader) {
@@ -941,9 +985,9 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         ++tcount;
         if (t < 0) break;
         const TileRef tr = decode_tile(args, t);
-        const StageGeo& g = args.st[tr.s].g;
+        const StageGeo& g = stage_args(args, tr.s).g;
         if (g.a_mode == AMODE_POINTWISE) continue;
-        if (tr.s != args.nst - 1) {
+        if (!stage_consumes(args, tr.s)) {
           it += (uint32_t)tr.nkb;  // loaded on `full`, consumed by the MMA issuer alone
           continue;
         }
@@ -1069,7 +1113,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       ++tcount;
       if (t < 0) break;
       const TileRef tr = decode_tile(args, t);
-      const StageArgs& SA = args.st[tr.s];
+      const StageArgs& SA = stage_args(args, tr.s);
       const StageGeo& g = SA.g;
       const int32_t KB = tr.nkb;
       if (pd > 0 && g.a_mode == AMODE_GEMM) {
@@ -1117,7 +1161,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       ++tcount;
       if (t < 0) break;
       const TileRef tr = decode_tile(args, t);
-      const StageArgs& SA = args.st[tr.s];
+      const StageArgs& SA = stage_args(args, tr.s);
       const StageGeo& g = SA.g;
       if (g.a_mode == AMODE_POINTWISE) {
         pointwise_tile(args, tr, t, row, pw_done, pwcount & 1u, *run_no, leader, pto, abort_flag);
@@ -1146,7 +1190,14 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         valid = (hl < g.th) && (h < g.img_h);
         grow = ((int64_t)n * g.img_h + h) * g.img_w + w;
       }
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(SA.out) + (valid ? grow * (int64_t)g.N : 0);
+      // a stack's stage writes its intermediate buffer (the last stage: the output) and
+      // applies no activation after the last convolution
+      const bool stack_mid = args.stack && tr.s < args.nst - 1;
+      const int32_t epi = (args.stack && !stack_mid) ? EPI_NONE : g.epi;
+      __nv_bfloat16* const obase = stack_mid ? reinterpret_cast<__nv_bfloat16*>(args.st[0].out) +
+                                                   (int64_t)stack_buf(args, tr.s) * args.buf_elems
+                                             : reinterpret_cast<__nv_bfloat16*>(SA.out);
+      __nv_bfloat16* orow = obase + (valid ? grow * (int64_t)g.N : 0);
       const int32_t col0 = tr.c * g.n_out;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       const int nchunks = g.n_out / 32;
@@ -1244,10 +1295,10 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
             split_add(v, j * 32);
             if (!last_unit) continue;
           }
-          if (g.epi == EPI_GELU) {
+          if (epi == EPI_GELU) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = gelu_f(__uint_as_float(v[i]));
-          } else if (g.epi == EPI_RELU) {
+          } else if (epi == EPI_RELU) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = fmaxf(__uint_as_float(v[i]), 0.0f);
           } else {
@@ -1329,11 +1380,12 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           ptx::fence_acq_rel_gpu();
           ptx::red_release_gpu_add(args.split_turn + tile_id, 1u);
         }
-      } else if (tr.s == 0 && threadIdx.x == 64) {
-        // stage 0 feeds the last stage (two-stage chains) or the pointwise stage (attention)
-        const bool to_pw = args.nst == 3;
+      } else if ((args.stack ? stack_mid : tr.s == 0) && threadIdx.x == 64) {
+        // stage 0 feeds the last stage (two-stage chains) or the pointwise stage (attention);
+        // a stack's stage s feeds stage s + 1 through the semaphores of boundary s
+        const bool to_pw = args.nst == 3 && !args.stack;
         const int32_t flag = producer_flag(to_pw ? args.dep_pw : args.dep, tr.m, tr.c);
-        uint32_t* const fl = to_pw ? args.flags_pw : args.flags;
+        uint32_t* const fl = to_pw ? args.flags_pw : args.flags + (args.stack ? tr.s * args.flags_stride : 0);
         if (flag >= 0) {
           // cuSync §IV-E "Post": after all of this CTA's stores of the tile (the epi_done
           // barrier orders its 128 threads' stores before this thread), one device-scope

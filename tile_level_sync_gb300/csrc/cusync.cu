@@ -55,14 +55,31 @@ cusync_status_t cuda_fail(cudaError_t e, const char* what) {
 struct Plan {
   int32_t bn;           // accumulator tile width (UMMA N)
   int32_t pair;         // CTAs per tile: 1, or 2 (a CTA pair computing a 256-row tile)
-  int32_t nst;          // stages: 2, or 3 (attention: QKV GEMM, pointwise, output GEMM)
-  StageGeo geo[3];
-  DepCfg dep;           // the last stage's waits on the stage before it
+  int32_t nst;          // stages: 2, 3 (attention: QKV GEMM, pointwise, output GEMM), or
+                        // a convolution stack's depth
+  StageGeo geo[3];      // per stage; a stack: geo[0] its first stage, geo[1] every later one
+  int32_t stack;        // convolution stack (stages 1 .. nst-1 share geo[1] and `dep`)
+  int32_t nbuf;         // stack: intermediate buffers in the workspace
+  int64_t flags_stride; // stack: semaphores per stage boundary
+  DepCfg dep;           // the last stage's waits on the stage before it (a stack: every stage's)
   DepCfg dep_pw;        // attention: the pointwise stage's waits on the QKV GEMM
   int64_t num_flags;
   int64_t num_flags_pw;
   int64_t split_rows;   // K split: workspace row blocks (producer tiles x pair), else 0
 };
+
+// Geometry of stage s.
+const StageGeo& sgeo(const Plan& p, int s) { return p.geo[p.stack ? (s > 0 ? 1 : 0) : s]; }
+
+// Work units of all stages (trace records of a run).
+int64_t total_units(const Plan& p) {
+  int64_t n = 0;
+  for (int s = 0; s < p.nst; ++s) n += stage_units(sgeo(p, s));
+  return n;
+}
+
+// Elements of one intermediate of a convolution stack.
+int64_t stack_buf_elems(const cusync_chain_desc_t& d) { return (int64_t)d.n * d.h * d.w * d.c; }
 
 // Words of a chain's device state: control words, semaphores, K-split turn counters.
 int64_t state_words(const Plan& p) { return CTRL_WORDS + p.num_flags + p.num_flags_pw + p.split_rows; }
@@ -91,7 +108,7 @@ cusync_status_t resolve_auto(const cusync_chain_desc_t& d, cusync_chain_desc_t* 
 int query_num_sms(int32_t requested, int* out);
 
 cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
-  if (d.kind < CUSYNC_CHAIN_MLP_GELU || d.kind > CUSYNC_CHAIN_ATTENTION) return CUSYNC_ERR_INVALID_ARG;
+  if (d.kind < CUSYNC_CHAIN_MLP_GELU || d.kind > CUSYNC_CHAIN_CONV_STACK) return CUSYNC_ERR_INVALID_ARG;
   if (d.policy == CUSYNC_POLICY_AUTO) {
     cusync_chain_desc_t r;
     cusync_status_t st = resolve_auto(d, &r);
@@ -103,6 +120,7 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   if (bn != 128 && bn != 256) return CUSYNC_ERR_UNSUPPORTED;
   const bool mlp = d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
   const bool attn = d.kind == CUSYNC_CHAIN_ATTENTION;
+  const bool stack = d.kind == CUSYNC_CHAIN_CONV_STACK;
   // CTA pairs (cta_group::2, 256-row tiles) for MLP chains with at least 256 tokens,
   // where they measured faster on GB300 (GPT-3 M=256: 91 against 97 us; SwiGLU M=256
   // even); single-CTA 128-row tiles otherwise.
@@ -116,7 +134,40 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   StageGeo& g1 = p->geo[1];
   StageGeo& g2 = p->geo[2];
   p->nst = attn ? 3 : 2;
-  if (attn) {
+  if (stack) {
+    // [cuSync] Table tab:resnet-sizes: a ResNet-38 layer group is a run of 3x3
+    // convolutions of equal channels; here `stages` of them in one chain
+    if (d.n < 1 || d.h < 1 || d.w < 1 || d.c < 1 || d.stages < 1) return CUSYNC_ERR_INVALID_ARG;
+    if (d.stages < 2 || d.stages > kMaxQueues) return CUSYNC_ERR_UNSUPPORTED;
+    if (d.k_out != 0 && d.k_out != d.c) return CUSYNC_ERR_UNSUPPORTED;   // equal channels
+    if (d.policy == CUSYNC_POLICY_STRIDED_TILE) return CUSYNC_ERR_UNSUPPORTED;
+    if (d.c % kBK) return CUSYNC_ERR_UNSUPPORTED;
+    if (d.w > kBM || d.w > 256) return CUSYNC_ERR_UNSUPPORTED;
+    if ((int64_t)d.n * d.h * d.w > (1ll << 30)) return CUSYNC_ERR_UNSUPPORTED;
+    if (ceil_div(d.c, bn) > kMaxConvColTiles) return CUSYNC_ERR_UNSUPPORTED;
+    const int32_t th = conv_rows_per_tile(d.h, d.w);
+    for (int s = 0; s < 2; ++s) {
+      StageGeo& g = p->geo[s];
+      g.a_mode = AMODE_CONV;
+      g.epi = EPI_RELU;  // the kernel applies none after the last convolution
+      g.M = d.n * d.h * d.w;
+      g.N = d.c;
+      g.K = 9 * d.c;
+      g.n_out = bn;
+      g.img_n = d.n;
+      g.img_h = d.h;
+      g.img_w = d.w;
+      g.cin = d.c;
+      g.th = th;
+      g.tpi = (int32_t)ceil_div(d.h, th);
+      g.cblocks = d.c / kBK;
+      g.m_tiles = d.n * g.tpi;
+      g.n_tiles = (int32_t)ceil_div(d.c, bn);
+      g.k_blocks = 9 * g.cblocks;
+    }
+    p->nst = d.stages;
+    p->stack = 1;
+  } else if (attn) {
     // "A Framework for Fine-Grained Synchronization of Dependent GPU Kernels",
     // Fig. fig:gpt-3:attention: XQKV = X x QKV (one GEMM for the three blocks), the
     // pointwise dot-product kernel per head, XW2 = XDot x W2.
@@ -282,6 +333,13 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
     dep.D = g0.n_tiles / G;
   }
   p->num_flags = num_flags(dep);
+  if (stack) {
+    // one set of semaphores per stage boundary; the intermediates alternate between two
+    // buffers, except under the sentinel policy (one buffer each, filled before the run)
+    p->flags_stride = p->num_flags;
+    p->num_flags = p->flags_stride * (p->nst - 1);
+    p->nbuf = d.policy == CUSYNC_POLICY_SENTINEL ? p->nst - 1 : std::min(2, p->nst - 1);
+  }
   if (p->num_flags > (1ll << 24)) return CUSYNC_ERR_UNSUPPORTED;
   p->split_rows = g0.ksplit > 1 ? (int64_t)g0.m_tiles * g0.n_tiles * pair : 0;
   return CUSYNC_OK;
@@ -336,6 +394,31 @@ bool encode_nhwc(CUtensorMap* m, const void* ptr, uint64_t n, uint64_t h, uint64
   cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)w, th, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A convolution stack's intermediates: `nbuf` NHWC images one after the other, as a 5-D
+// map [nbuf, n, h, w, c] whose outermost coordinate selects the buffer; same box.
+bool encode_nhwc_bufs(CUtensorMap* m, const void* ptr, uint64_t nbuf, uint64_t n, uint64_t h, uint64_t w, uint64_t c,
+                      uint32_t th) {
+  cuuint64_t dims[5] = {c, w, h, n, nbuf};
+  cuuint64_t strides[4] = {c * 2, w * c * 2, h * w * c * 2, n * h * w * c * 2};
+  cuuint32_t box[5] = {(cuuint32_t)kBK, (cuuint32_t)w, th, 1, 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A convolution stack's weights: `depth` row-major [rows, cols] matrices one after the
+// other, as a 3-D map whose outermost coordinate selects the stage; [box_rows, 64] box.
+bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t depth, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  cuuint64_t dims[3] = {cols, rows, depth};
+  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kBK, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -403,19 +486,19 @@ int max_pair_clusters() {
 // Grid sizes (CTAs) of the fused launch and of the two separate launches.
 struct Grids {
   int32_t fused;     // the one persistent launch of all stages
-  int32_t stage[3];  // one launch per stage (stream order or programmatic dependent launch)
+  int32_t stage[kMaxQueues];  // one launch per stage (stream order or programmatic dependent launch)
 };
 
 Grids make_grids(const Plan& p, int sms, int max_clusters) {
-  int64_t t[3] = {0, 0, 0}, total = 0;
-  for (int s = 0; s < p.nst; ++s) total += (t[s] = stage_units(p.geo[s]));
+  int64_t t[kMaxQueues] = {}, total = 0;
+  for (int s = 0; s < p.nst; ++s) total += (t[s] = stage_units(sgeo(p, s)));
   // one tile per CTA, or per CTA pair (cluster of two) resident at once
   const int64_t slots = p.pair == 2 ? std::max<int64_t>(1, std::min<int64_t>(sms / 2, max_clusters > 0 ? max_clusters
                                                                                                        : sms / 2))
                                     : sms;
   Grids g;
   g.fused = (int32_t)(p.pair * std::min<int64_t>(slots, total));
-  for (int s = 0; s < 3; ++s) g.stage[s] = (int32_t)(p.pair * std::min<int64_t>(slots, t[s]));
+  for (int s = 0; s < kMaxQueues; ++s) g.stage[s] = (int32_t)(p.pair * std::min<int64_t>(slots, t[s]));
   return g;
 }
 
@@ -570,7 +653,8 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
                            int sms, cudaStream_t stream) {
   cudaError_t e;
   if (d.policy == CUSYNC_POLICY_SENTINEL && !(d.flags & CUSYNC_DEBUG_SKIP_INIT)) {
-    const int64_t bytes = (int64_t)p.geo[0].M * p.geo[0].N * 2;
+    // the intermediate (a stack: all of its intermediates, one buffer each)
+    const int64_t bytes = (int64_t)p.geo[0].M * p.geo[0].N * 2 * (p.stack ? p.nbuf : 1);
     const int64_t n16 = bytes / 16;
     int blocks = (int)std::min<int64_t>(ceil_div(n16, 256), (int64_t)sms * 8);
     if (blocks < 1) blocks = 1;
@@ -596,7 +680,7 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
     A.last_stage = s;
     A.pdl_role = pdl ? ((s + 1 < p.nst ? 1 : 0) | (s > 0 ? 2 : 0)) : 0;
     e = launch_any(p, A, g.stage[s], /*pdl2=*/pdl && s > 0, stream);
-    if (e != cudaSuccess) return cuda_fail(e, s == 0 ? "producer launch" : "consumer launch");
+    if (e != cudaSuccess) return cuda_fail(e, s == 0 ? "producer launch" : "later stage launch");
   }
   return CUSYNC_OK;
 }
@@ -626,6 +710,14 @@ bool encode_maps(const cusync_chain_desc_t& d, const Plan& p, ChainArgs& A, cons
     ok &= encode_2d(&A.st[2].tmA, h2, (uint64_t)d.M, (uint64_t)d.N1, 128u);
     ok &= encode_2d(&A.st[2].tmB, b1, (uint64_t)d.N2, (uint64_t)d.N1, b_box_rows(p, false));
     ok &= encode_2d(&A.st[2].tmO, y, (uint64_t)d.M, (uint64_t)d.N2, 32u);
+  } else if (d.kind == CUSYNC_CHAIN_CONV_STACK) {
+    // stage 0 reads x, every later stage one of the workspace's buffers; all stages take
+    // their weights from the stacked weights (a0 = x, b0 = weights, h = workspace)
+    const StageGeo& g0 = p.geo[0];
+    ok &= encode_nhwc(&A.st[0].tmA, a0, d.n, d.h, d.w, d.c, (uint32_t)g0.th);
+    ok &= encode_nhwc_bufs(&A.st[1].tmA, h, (uint64_t)p.nbuf, d.n, d.h, d.w, d.c, (uint32_t)g0.th);
+    ok &= encode_3d(&A.st[0].tmB, b0, (uint64_t)p.nst, (uint64_t)d.c, (uint64_t)9 * d.c, b_box_rows(p, false));
+    A.st[1].tmB = A.st[0].tmB;
   } else if (d.kind == CUSYNC_CHAIN_CONV_RELU) {
     const StageGeo& g0 = p.geo[0];
     ok &= encode_nhwc(&A.st[0].tmA, a0, d.n, d.h, d.w, d.c, (uint32_t)g0.th);
@@ -672,6 +764,10 @@ void fill_static_args(const cusync_chain_desc_t& d, const Plan& p, uint32_t* sta
   A.tiles0 = (int32_t)t0;
   A.tiles1 = (int32_t)t1;
   A.tiles2 = (int32_t)stage_units(p.geo[2]);
+  A.stack = p.stack;
+  A.nbuf = p.stack ? p.nbuf : 1;
+  A.flags_stride = (int32_t)p.flags_stride;
+  A.buf_elems = p.stack ? stack_buf_elems(d) : 0;
   A.flags_bits = d.flags;
   A.sentinel_check = d.policy == CUSYNC_POLICY_SENTINEL ? 1 : 0;
   A.num_flags = (int32_t)p.num_flags;
@@ -687,7 +783,7 @@ cusync_status_t run_chain(cusync_chain* ch, const void* a0, const void* b0, cons
   if (!aligned16(a0) || !aligned16(b0) || !aligned16(b1) || !aligned16(h) || !aligned16(y))
     return CUSYNC_ERR_INVALID_ARG;
   if (h == y || h == a0 || y == a0) return CUSYNC_ERR_INVALID_ARG;
-  if (p.nst == 3 && (!aligned16(h2) || h2 == h || h2 == y || h2 == a0)) return CUSYNC_ERR_INVALID_ARG;
+  if (p.nst == 3 && !p.stack && (!aligned16(h2) || h2 == h || h2 == y || h2 == a0)) return CUSYNC_ERR_INVALID_ARG;
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess || cur != ch->device) return CUSYNC_ERR_INVALID_ARG;
   ChainArgs& A = ch->args;
@@ -701,8 +797,8 @@ cusync_status_t run_chain(cusync_chain* ch, const void* a0, const void* b0, cons
     ch->maps_valid = true;
   }
   A.st[0].out = h;
-  A.st[1].out = p.nst == 3 ? h2 : y;
-  A.st[2].out = p.nst == 3 ? y : nullptr;
+  A.st[1].out = (p.nst == 3 && !p.stack) ? h2 : y;
+  A.st[2].out = (p.nst == 3 && !p.stack) ? y : nullptr;
   return launch_run(d, p, A, ch->grids, h, ch->num_sms, stream);
 }
 
@@ -822,7 +918,7 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
     return CUSYNC_ERR_NOMEM;
   }
   if (d->flags & CUSYNC_FLAG_TRACE) {
-    const size_t n = (size_t)stage_units(p.geo[0]) + (size_t)stage_units(p.geo[1]) + (size_t)stage_units(p.geo[2]);
+    const size_t n = (size_t)total_units(p);
     if (cudaMalloc(&ch->trace, n * sizeof(TraceRec)) != cudaSuccess ||
         cudaMemset(ch->trace, 0, n * sizeof(TraceRec)) != cudaSuccess) {
       if (ch->trace) cudaFree(ch->trace);
@@ -856,6 +952,14 @@ cusync_status_t cusync_run_conv_chain(cusync_chain_t ch, const void* x, const vo
   if (!ch) return CUSYNC_ERR_INVALID_ARG;
   if (ch->d.kind != CUSYNC_CHAIN_CONV_RELU) return CUSYNC_ERR_INVALID_ARG;
   return run_chain(ch, x, w1, w2, y1, nullptr, y2, reinterpret_cast<cudaStream_t>(stream));
+}
+
+cusync_status_t cusync_run_conv_stack(cusync_chain_t ch, const void* x, const void* w, void* work, void* y,
+                                      cusync_stream_t stream) {
+  if (!ch) return CUSYNC_ERR_INVALID_ARG;
+  if (ch->d.kind != CUSYNC_CHAIN_CONV_STACK) return CUSYNC_ERR_INVALID_ARG;
+  // the weights take the place of both weight operands (one stacked map serves all stages)
+  return run_chain(ch, x, w, w, work, nullptr, y, reinterpret_cast<cudaStream_t>(stream));
 }
 
 cusync_status_t cusync_run_attention(cusync_chain_t ch, const void* X, const void* Wqkv_t, const void* W2t,
@@ -932,6 +1036,12 @@ cusync_status_t cusync_plan_info(const cusync_chain_desc_t* d, cusync_chain_info
   out->num_flags_pw = (int32_t)p.num_flags_pw;
   out->strided_group_pw = p.dep_pw.G;
   out->strided_distance_pw = p.dep_pw.D;
+  if (p.stack) {
+    out->conv_rows_per_tile = p.geo[0].th;
+    out->work_buffers = p.nbuf;
+    out->work_bytes = (int64_t)p.nbuf * stack_buf_elems(*d) * 2;
+    out->m_tiles2 = out->n_tiles2 = out->k_blocks2 = out->n_out2 = out->grid2 = 0;
+  }
   return CUSYNC_OK;
 }
 
@@ -991,7 +1101,7 @@ cusync_status_t cusync_consumer_waits(const cusync_chain_desc_t* d, int32_t m_ti
   Plan p;
   cusync_status_t st = make_plan(*d, &p);
   if (st != CUSYNC_OK) return st;
-  const StageGeo& g = p.geo[p.nst - 1];  // the stage that waits on `dep`
+  const StageGeo& g = sgeo(p, p.nst - 1);  // the stage that waits on `dep`
   if (m_tile < 0 || m_tile >= g.m_tiles) return CUSYNC_ERR_INVALID_ARG;
   if (max > 0 && (!kb || !flag || !per_run)) return CUSYNC_ERR_INVALID_ARG;
   DepTracker dt;
@@ -1053,7 +1163,7 @@ cusync_status_t cusync_chain_trace(cusync_chain_t ch, cusync_stream_t stream, cu
                                    int32_t* n_out) {
   static_assert(sizeof(cusync_trace_rec_t) == sizeof(TraceRec), "trace record layout");
   if (!ch || !n_out || max < 0 || (max > 0 && !out) || !ch->trace) return CUSYNC_ERR_INVALID_ARG;
-  const int32_t n = ch->args.tiles0 + ch->args.tiles1 + ch->args.tiles2;
+  const int32_t n = (int32_t)total_units(ch->plan);
   *n_out = n;
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");

@@ -106,6 +106,18 @@ def conv_inputs(N, H, W, C, K, seed=0):
     return x, w1, w2
 
 
+def conv_stack_inputs(N, H, W, C, stages, seed=0):
+    """(x [N,H,W,C] NHWC, w [stages,C,3,3,C]: each stage's KRSC weights) as CPU bf16 tensors.
+
+    Weights ~ N(0, 2 / (9 C)) (He initialisation for a 3x3 convolution followed by ReLU),
+    so the activations keep their scale through a deep stack; for the 14x14x256 layer
+    group this is the 0.03 of the convolution pair."""
+    rng = np.random.default_rng(seed)
+    x = to_bf16(_normal(rng, (N, H, W, C), 1.0))
+    w = to_bf16(_normal(rng, (stages, C, 3, 3, C), float(np.sqrt(2.0 / (9 * C)))))
+    return x, w
+
+
 def attention_inputs(M, K, N1, N2, seed=0):
     """(X [M,K], QKV [K,3*N1] -- the XQ, XV, XK column blocks --, W2 [N1,N2]) as CPU bf16
     tensors."""
