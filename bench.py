@@ -227,6 +227,14 @@ def oracle_sample_runner(wl, inputs):
             chains.attention_rows(X, Wqkv, W2, rows)
             return 2.0 * len(rows) * d["K"] * 3 * d["N1"] + 2.0 * len(rows) * d["N1"] * d["N2"]
         return fn, d["M"]
+    if wl.kind == "conv_stack":
+        x, wt = (synth.f64(t) for t in inputs)
+        ws = [wt[s] for s in range(d["S"])]
+
+        def fn(rows):  # rows = images
+            chains.conv_stack(x[rows], ws)
+            return wl.gemm_flops() * len(rows) / d["N"]
+        return fn, d["N"]
     x, w1, w2 = (synth.f64(t) for t in inputs)
 
     def fn(rows):  # rows = images
@@ -247,7 +255,7 @@ def time_oracle(wl, inputs, budget_s=12.0):
     t0 = time.perf_counter()
     flops = fn(sel)
     dt = time.perf_counter() - t0
-    unit = "images" if wl.kind == "conv_relu" else "token rows"
+    unit = "images" if wl.kind in ("conv_relu", "conv_stack") else "token rows"
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
             "sample": f"{n} of {total} {unit} of {wl.name}, fp64 numpy oracle, {dt:.2f} s"}
 
@@ -276,7 +284,7 @@ def run_reference(a):
         flops += fn(sel)
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
-    unit_name = "images" if wl.kind == "conv_relu" else "token rows"
+    unit_name = "images" if wl.kind in ("conv_relu", "conv_stack") else "token rows"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": dt / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -303,7 +311,18 @@ class Setup:
         self.wl = wl
         d = wl.dims
         dev = "cuda"
-        if wl.kind == "conv_relu":
+        if wl.kind == "conv_stack":
+            x, wt = inputs
+            self.a = x.to(dev)
+            self.b0 = wt.contiguous().to(dev)
+            self.b1 = None
+            self.base = dict(kind=cs.CHAIN_CONV_STACK, n=d["N"], h=d["H"], w=d["W"], c=d["C"], stages=d["S"])
+            # a workspace for two buffers or, under the sentinel policy, one per intermediate
+            self.h = torch.empty(((d["S"] - 1) * d["N"] * d["H"] * d["W"] * d["C"],), dtype=torch.bfloat16,
+                                 device=dev)
+            self.y = torch.empty((d["N"], d["H"], d["W"], d["C"]), dtype=torch.bfloat16, device=dev)
+            self.x_host = x
+        elif wl.kind == "conv_relu":
             x, w1, w2 = inputs
             self.a = x.to(dev)
             self.b0 = w1.contiguous().to(dev)
@@ -363,7 +382,7 @@ class Setup:
         ch.run(self.a, self.b0, self.b1, self.h, self.y, h2=getattr(self, "h2", None))
 
     def kernels_per_run(self, policy, launch):
-        stages = 3 if self.base["kind"] == self.cs.CHAIN_ATTENTION else 2
+        stages = 3 if self.base["kind"] == self.cs.CHAIN_ATTENTION else self.base.get("stages", 2)
         n = stages if (policy == "STREAM" or launch == self.cs.LAUNCH_PDL) else 1
         return n + (1 if policy == "SENTINEL" else 0)
 
@@ -505,6 +524,9 @@ def algorithmic_bytes(wl):
     if wl.kind == "conv_relu":
         pix = d["N"] * d["H"] * d["W"]
         return 2 * (pix * d["C"] + 9 * d["C"] * d["K"] + 2 * pix * d["K"] + 9 * d["K"] * d["K"] + pix * d["K"])
+    if wl.kind == "conv_stack":   # x and y once, each intermediate written once and read once
+        act = d["N"] * d["H"] * d["W"] * d["C"]
+        return 2 * (2 * act + 2 * (d["S"] - 1) * act + d["S"] * 9 * d["C"] * d["C"])
     if wl.kind == "attention":   # XQKV and XDot each written once and read once
         return 2 * (d["M"] * d["K"] + d["K"] * 3 * d["N1"] + 2 * d["M"] * 3 * d["N1"] + 2 * d["M"] * d["N1"]
                     + d["N1"] * d["N2"] + d["M"] * d["N2"])
@@ -519,7 +541,15 @@ def check_output(setup, wl, inputs):
     from tile_level_sync_gb300 import synth
     d = wl.dims
     Y = setup.y.float().cpu().double().numpy()
-    if wl.kind == "conv_relu":
+    scale = 1.0
+    if wl.kind == "conv_stack":
+        # end to end through S bf16 roundings: the pair's bound times sqrt(S - 1)
+        x, wt = (synth.f64(t) for t in inputs)
+        imgs = [0, d["N"] - 1]
+        _, ref = chains.conv_stack(x[imgs], [wt[s] for s in range(d["S"])])
+        got = Y[imgs]
+        scale = float(np.sqrt(d["S"] - 1))
+    elif wl.kind == "conv_relu":
         x, w1, w2 = (synth.f64(t) for t in inputs)
         imgs = [0, d["N"] - 1]
         _, ref = chains.conv_relu_chain(x[imgs], w1, w2)
@@ -533,7 +563,7 @@ def check_output(setup, wl, inputs):
         else:
             _, ref = chains.mlp_swiglu_rows(*(synth.f64(t) for t in inputs), rows)
         got = Y[rows]
-    bound = 2e-2 * np.maximum(1.0, np.abs(ref))
+    bound = scale * 2e-2 * np.maximum(1.0, np.abs(ref))
     return bool(np.all(np.abs(got - ref) <= bound))
 
 

@@ -12,13 +12,17 @@ order listed, each array rounded to bf16 with round-to-nearest-even):
 * SwiGLU MLP: X [M,K] ~ N(0,1); Wgate, Wup [K,N1] ~ N(0,0.02); Wdown [N1,N2] ~ N(0,0.02)
 * conv pair:  x [N,H,W,C] ~ N(0,1) (NHWC); w1, w2 [K,3,3,C] ~ N(0,0.03) (KRSC)
 * attention:  X [M,K] ~ N(0,1); QKV [K,3*N1] ~ N(0,0.02); W2 [N1,N2] ~ N(0,0.02)
+* conv stack: x [N,H,W,C] ~ N(0,1); w [S,C,3,3,C] ~ N(0, 2/(9C)) (S stages' KRSC weights)
 
 N(mu, sigma) takes sigma as the standard deviation.  Shapes follow the
 GPT-3 145B MLP shard of [cuSync] §II-B / §III-A (H = 12288, one of 8
 tensor-parallel shards: X [B,12288], W1 [12288,6144], W2 [6144,12288]) and
 the 14x14x256 ResNet-38 layer of Table ``tab:resnet-sizes``; the self-attention
 block of Fig. ``fig:gpt-3:attention`` takes the same shard (QKV [12288, 3*1536],
-W2 [1536, 12288]); no dataset or trained weights are involved.
+W2 [1536, 12288]); the convolution stacks are the four layer groups of that table
+(56x56x64: 3 layers of two convolutions, 28x28x128: 4, 14x14x256: 6, 7x7x512: 3) at a
+batch of 32 images, the batch of the convolution pair; no dataset or trained weights
+are involved.
 """
 
 from dataclasses import dataclass, field
@@ -30,7 +34,7 @@ import torch
 @dataclass(frozen=True)
 class Workload:
     name: str
-    kind: str                  # "mlp_gelu" | "mlp_swiglu" | "conv_relu" | "attention"
+    kind: str                  # "mlp_gelu" | "mlp_swiglu" | "conv_relu" | "attention" | "conv_stack"
     dims: dict = field(default_factory=dict)
 
     def gemm_flops(self):
@@ -44,6 +48,8 @@ class Workload:
             return 2 * pix * d["K"] * 9 * d["C"] + 2 * pix * d["K"] * 9 * d["K"]
         if self.kind == "attention":   # the two GEMMs; the pointwise stage has no tensor work
             return 2 * d["M"] * d["K"] * (3 * d["N1"]) + 2 * d["M"] * d["N1"] * d["N2"]
+        if self.kind == "conv_stack":
+            return d["S"] * 2 * d["N"] * d["H"] * d["W"] * d["C"] * 9 * d["C"]
         raise ValueError(self.kind)
 
 
@@ -65,6 +71,10 @@ WORKLOADS = {
         Workload("conv_resnet14_n32", "conv_relu", dict(N=32, H=14, W=14, C=256, K=256)),
         Workload("gpt3_attn_m256", "attention", dict(M=256, K=12288, N1=1536, N2=12288)),
         Workload("gpt3_attn_m1024", "attention", dict(M=1024, K=12288, N1=1536, N2=12288)),
+        Workload("resnet38_56x56x64_n32", "conv_stack", dict(N=32, H=56, W=56, C=64, S=6)),
+        Workload("resnet38_28x28x128_n32", "conv_stack", dict(N=32, H=28, W=28, C=128, S=8)),
+        Workload("resnet38_14x14x256_n32", "conv_stack", dict(N=32, H=14, W=14, C=256, S=12)),
+        Workload("resnet38_7x7x512_n32", "conv_stack", dict(N=32, H=7, W=7, C=512, S=6)),
     ]
 }
 
@@ -138,6 +148,8 @@ def workload_inputs(w: Workload, seed=0):
         return conv_inputs(d["N"], d["H"], d["W"], d["C"], d["K"], seed)
     if w.kind == "attention":
         return attention_inputs(d["M"], d["K"], d["N1"], d["N2"], seed)
+    if w.kind == "conv_stack":
+        return conv_stack_inputs(d["N"], d["H"], d["W"], d["C"], d["S"], seed)
     raise ValueError(w.kind)
 
 
