@@ -317,8 +317,9 @@ class Setup:
             self.b0 = wt.contiguous().to(dev)
             self.b1 = None
             self.base = dict(kind=cs.CHAIN_CONV_STACK, n=d["N"], h=d["H"], w=d["W"], c=d["C"], stages=d["S"])
-            # a workspace for two buffers or, under the sentinel policy, one per intermediate
-            self.h = torch.empty(((d["S"] - 1) * d["N"] * d["H"] * d["W"] * d["C"],), dtype=torch.bfloat16,
+            # a workspace for the largest plan: under the sentinel policy two sets of one
+            # buffer per intermediate (cusync_chain_info_t::work_bytes)
+            self.h = torch.empty((2 * (d["S"] - 1) * d["N"] * d["H"] * d["W"] * d["C"],), dtype=torch.bfloat16,
                                  device=dev)
             self.y = torch.empty((d["N"], d["H"], d["W"], d["C"]), dtype=torch.bfloat16, device=dev)
             self.x_host = x

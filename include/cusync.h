@@ -97,8 +97,11 @@ typedef enum {
    * on the one before it with the chain's policy (ROW, TILE or SENTINEL).  The
    * intermediates live in a caller-owned workspace (cusync_chain_info_t::work_bytes):
    * two buffers used in turn under ROW, TILE and STREAM (a stage overwrites the input of
-   * the stage before it only after its own waits have covered every reader), one per
-   * intermediate under SENTINEL (the sentinel fill precedes the run). */
+   * the stage before it only after its own waits have covered every reader); under
+   * SENTINEL one buffer per intermediate in each of two sets: run r uses set r % 2 and
+   * its last launch writes the sentinel over the other set in its tail, so no fill
+   * precedes a run (both sets are filled before the first run on a workspace, and after
+   * cusync_chain_reset). */
   CUSYNC_CHAIN_CONV_STACK = 4
 } cusync_chain_kind_t;
 

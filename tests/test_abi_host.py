@@ -458,7 +458,7 @@ def test_stack_waits_match_oracle_and_cover_rotation(case, policy):
 def test_stack_plan_and_refusals():
     base = dict(n=2, h=14, w=14, c=256, num_sms=152)
     act = 2 * 14 * 14 * 256 * 2
-    for pol, nbuf in (("ROW", 2), ("TILE", 2), ("STREAM", 2), ("SENTINEL", 11)):
+    for pol, nbuf in (("ROW", 2), ("TILE", 2), ("STREAM", 2), ("SENTINEL", 22)):
         info = cs.cusync_plan_info(cs.make_desc(cs.CHAIN_CONV_STACK, pol, stages=12, **base))
         assert info.nst == 12 and info.work_buffers == nbuf and info.work_bytes == nbuf * act
         assert info.m_tiles[0] == info.m_tiles[1] and info.k_blocks[0] == info.k_blocks[1]  # uniform stages

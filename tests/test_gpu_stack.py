@@ -49,6 +49,19 @@ def _buffers(work, info, shape):
     return work.view(info.work_buffers, *shape)
 
 
+def sentinel_sets(work, info, shape, stages, runs):
+    """(the set of intermediates the last of `runs` runs used, the other set): run r of a
+    chain uses set r % 2, and fills the other one with the sentinel."""
+    bufs = _buffers(work, info, shape)
+    used = runs & 1
+    return bufs[used * (stages - 1):(used + 1) * (stages - 1)], bufs[(1 - used) * (stages - 1):(2 - used) * (stages - 1)]
+
+
+def assert_all_sentinel(bufs, what):
+    b = bufs.contiguous().view(torch.int16).numpy().astype(np.uint16)
+    assert np.all(b == 0x8000), f"{what}: {int((b != 0x8000).sum())} elements are not the sentinel"
+
+
 def depth_scale(stages):
     return float(np.sqrt(stages - 1))
 
@@ -85,9 +98,12 @@ def test_stack_all_policies(n, h, w, c, stages, tile_n):
             assert_within_tol(f64(y), y_ref, f"y {pol} {launch}", depth_scale(stages))
             bufs = _buffers(work, info, (n, h, w, c))
             if pol == "SENTINEL":
-                # one buffer per intermediate: each stage checked on its own input
-                assert info.work_buffers == stages - 1
-                check_stagewise(x, wt, bufs, y, stages, f"{pol} {launch}")
+                # one buffer per intermediate in each of two sets: each stage of the last run
+                # checked on its own input; its tail filled the other set with the sentinel
+                assert info.work_buffers == 2 * (stages - 1)
+                used, other = sentinel_sets(work, info, (n, h, w, c), stages, runs=2)
+                check_stagewise(x, wt, used, y, stages, f"{pol} {launch}")
+                assert_all_sentinel(other, f"{pol} {launch} next set")
             else:
                 # two buffers in turn: the last two intermediates remain
                 assert info.work_buffers == min(2, stages - 1)
@@ -115,19 +131,23 @@ def test_stack_resnet38_layer_groups(n, h, w, c, stages):
         work, y, info = run_stack(d, x, wt)
         assert_within_tol(f64(y), y_ref, f"y {pol}", depth_scale(stages))
         if pol == "SENTINEL":
-            check_stagewise(x, wt, _buffers(work, info, (n, h, w, c)), y, stages, pol)
+            used, other = sentinel_sets(work, info, (n, h, w, c), stages, runs=1)
+            check_stagewise(x, wt, used, y, stages, pol)
+            assert_all_sentinel(other, "next set")
         if ref_bits is None:
             ref_bits = bits(y)
         else:
             assert np.array_equal(bits(y), ref_bits), pol
 
 
-def test_stack_repeated_runs_and_graph_replay():
-    """Runs count up the semaphores across runs: several runs in a row, and the same run
-    replayed from a CUDA graph, all give the same bytes."""
+@pytest.mark.parametrize("policy", ["TILE", "SENTINEL"])
+def test_stack_repeated_runs_and_graph_replay(policy):
+    """Runs count up the semaphores across runs (and, under the sentinel policy, alternate
+    between the two sets of intermediates, each run filling the next one's): several runs
+    in a row, and runs replayed from a CUDA graph, all give the same bytes."""
     n, h, w, c, stages = 1, 14, 14, 128, 5
     x, wt = synth.conv_stack_inputs(n, h, w, c, stages, seed=23)
-    d = cs.make_desc(cs.CHAIN_CONV_STACK, "TILE", n=n, h=h, w=w, c=c, stages=stages)
+    d = cs.make_desc(cs.CHAIN_CONV_STACK, policy, n=n, h=h, w=w, c=c, stages=stages)
     _, y1, info = run_stack(d, x, wt, runs=1)
     work = torch.empty(info.work_bytes // 2, dtype=torch.bfloat16, device="cuda")
     y = torch.empty((n, h, w, c), dtype=torch.bfloat16, device="cuda")

@@ -115,6 +115,13 @@ struct ChainArgs {
   int32_t nbuf;          // stack: intermediate buffers in st[0].out; stage s writes s % nbuf
   int32_t flags_stride;  // stack: semaphores per stage boundary (boundary s at s * stride)
   int64_t buf_elems;     // stack: elements of one intermediate buffer
+  // Stack under the sentinel policy: two sets of nst - 1 buffers used in turn, run r in
+  // set r % 2; the launch that serves the last stage ends with fill units that write the
+  // sentinel over the other set, ready for the next run.
+  int32_t rotate;
+  int32_t fill_units;
+  int64_t fill_unit_chunks;  // 16-byte chunks per fill unit
+  int64_t set_chunks;        // 16-byte chunks of one set
   uint32_t flags_bits;
   int32_t pdl_role;      // bit 0: trigger dependents at start; bit 1: wait on the primary at exit
   int32_t sentinel_check;
@@ -148,6 +155,7 @@ struct TileRef {
   int32_t ks;   // K-split unit of the tile (0 without a split)
   int32_t kb0;  // first k-block of the unit
   int32_t nkb;  // k-blocks of the unit
+  int32_t q;    // the unit's position among the launch's work units (fill units not counted)
 };
 
 // Work units of stage s.
@@ -169,9 +177,24 @@ __device__ __forceinline__ bool stage_consumes(const ChainArgs& a, int32_t s) {
 // stage overwrites the input of the stage before it; the tile's own waits have covered
 // every reader of what it overwrites by the time it stores (it stores after its last
 // k-block, and each semaphore it waited on was posted after that tile's reads).
-__device__ __forceinline__ int32_t stack_buf(const ChainArgs& a, int32_t s) { return s % a.nbuf; }
+// Under the sentinel policy the run's set comes first: run r uses set r % 2.
+__device__ __forceinline__ int32_t stack_buf(const ChainArgs& a, int32_t s, uint32_t run) {
+  return a.rotate ? (int32_t)(run & 1u) * (a.nst - 1) + s : s % a.nbuf;
+}
+
+// Fill units (see ChainArgs::rotate) follow the work units in the queue of the launch that
+// serves the last stage, so the CTAs that run out of work in the last wave write them.
+// They wait on nothing, so the order of the work units, and with it the argument that no
+// wait can deadlock, is unchanged.
+constexpr int32_t kFillStage = -1;
 
 __device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
+  if (a.fill_units > 0 && a.last_stage == a.nst - 1) {
+    int32_t units = 0;
+    for (int32_t s = a.first_stage; s <= a.last_stage; ++s) units += stage_tiles(a, s);
+    if (t >= units) return TileRef{kFillStage, t - units, 0, 0, 0, 0, -1};
+  }
+  const int32_t q = t;
   // the launch serves stages [first_stage, last_stage], their work units in that order
   int32_t s = a.first_stage, u = t;
   while (s < a.last_stage) {
@@ -193,7 +216,7 @@ __device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
   // StridedSync's producer order applies to the stage whose semaphores it groups
   const DepCfg& pd = (a.nst == 3) ? a.dep_pw : a.dep;
   const int32_t c = (s == 0) ? producer_col(pd, y) : y;
-  return TileRef{s, m, c, ks, kb0, nkb};
+  return TileRef{s, m, c, ks, kb0, nkb, q};
 }
 
 // Index of queue position t in the chain's tile numbering (producer tiles first).
@@ -210,7 +233,7 @@ __device__ __forceinline__ uint32_t a_tile_bytes(const StageGeo& g) {
 // With to_leader, the copy's completion is counted on the pair leader's barrier `bar`.
 template <int PAIR>
 __device__ __forceinline__ void issue_a(const ChainArgs& a, const TileRef& tr, int32_t kb, uint32_t rank, void* dst,
-                                        uint64_t* bar, uint64_t pol, bool to_leader = false) {
+                                        uint64_t* bar, uint64_t pol, int32_t a_buf, bool to_leader = false) {
   const StageArgs& S = stage_args(a, tr.s);
   if (S.g.a_mode == AMODE_GEMM) {
     const int32_t row = tr.m * (128 * PAIR) + (int32_t)rank * 128;
@@ -222,8 +245,8 @@ __device__ __forceinline__ void issue_a(const ChainArgs& a, const TileRef& tr, i
     const int32_t tap = kb / S.g.cblocks, cb = kb % S.g.cblocks;
     const int32_t r = tap / 3, s = tap % 3;
     const int32_t n = tr.m / S.g.tpi, hb = tr.m % S.g.tpi;
-    if (a.stack && tr.s > 0)  // the stack's intermediates: one more coordinate, the buffer
-      ptx::tma_load_5d(dst, &S.tmA, bar, cb * kBK, s - 1, hb * S.g.th + r - 1, n, stack_buf(a, tr.s - 1), pol);
+    if (a_buf >= 0)  // the stack's intermediates: one more coordinate, the buffer
+      ptx::tma_load_5d(dst, &S.tmA, bar, cb * kBK, s - 1, hb * S.g.th + r - 1, n, a_buf, pol);
     else
       ptx::tma_load_4d(dst, &S.tmA, bar, cb * kBK, s - 1, hb * S.g.th + r - 1, n, pol);
   }
@@ -381,8 +404,8 @@ __device__ __noinline__ void pointwise_tile(const ChainArgs& args, const TileRef
         ptx::red_release_gpu_add(args.flags + flag, 1u);
       }
       if (args.trace && leader) {
-        args.trace[chain_tile(args, t)].t_epi = ptx::globaltimer();
-        args.trace[chain_tile(args, t)].t_post = ptx::globaltimer();
+        args.trace[chain_tile(args, tr.q)].t_epi = ptx::globaltimer();
+        args.trace[chain_tile(args, tr.q)].t_post = ptx::globaltimer();
       }
     }
   }
@@ -513,6 +536,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
 
   int32_t total = 0;
   for (int s = args.first_stage; s <= args.last_stage; ++s) total += stage_tiles(args, s);
+  if (args.last_stage == args.nst - 1) total += args.fill_units;
   const uint64_t pto = args.pipe_timeout_ns;
 
   // Arrive on "consumed" for ring slot `slot` (the leader's barrier in a pair).
@@ -569,13 +593,14 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         if (done) break;
 
         const TileRef tr = decode_tile(args, t);
+        if (tr.s == kFillStage) continue;  // written by this CTA's epilogue warps; nothing to load
         const StageArgs& SA = stage_args(args, tr.s);
         const int32_t KB = tr.nkb;            // k-blocks of this work unit
         const int32_t kx0 = tr.kb0 * kBK;     // its first reduction coordinate
         const uint32_t tx = a_tile_bytes(SA.g) + (uint32_t)C::kBBytes;
-        TraceRec* trec = (args.trace && leader) ? args.trace + chain_tile(args, t) : nullptr;
+        TraceRec* trec = (args.trace && leader) ? args.trace + chain_tile(args, tr.q) : nullptr;
         if (trec) {
-          trec->tile = (uint32_t)chain_tile(args, t);
+          trec->tile = (uint32_t)chain_tile(args, tr.q);
           trec->smid = ptx::smid();
           trec->cta = blockIdx.x;
           trec->stage = (uint32_t)tr.s;
@@ -625,7 +650,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         const bool stacked = args.stack != 0;
         const uint32_t* const wflags = args.flags + (stacked && tr.s > 0 ? (tr.s - 1) * args.flags_stride : 0);
         const int32_t wnflags = stacked ? args.flags_stride : args.num_flags;
-        const int32_t a_buf = stacked && tr.s > 0 ? stack_buf(args, tr.s - 1) : -1;
+        const int32_t a_buf = stacked && tr.s > 0 ? stack_buf(args, tr.s - 1, epoch) : -1;
         // k-blocks at which the consumer may have to wait (dep_kblock): every dep_every-th
         // k-block of a GEMM; for a convolution the first 64 k-blocks by a bit mask, every
         // later one by dep_every = 1.
@@ -839,6 +864,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       ++tcount;
       if (t < 0) break;
       const TileRef tr = decode_tile(args, t);
+      if (tr.s == kFillStage) continue;
       const StageGeo& g = stage_args(args, tr.s).g;
       if (g.a_mode == AMODE_POINTWISE) continue;  // no MMA
       const int acc = acount & 1;
@@ -878,7 +904,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         }
         if (args.trace) land_clk += (uint32_t)clock64() - c0;
         ptx::tc_fence_after();
-        if (lane == 0 && kb == 0 && args.trace) args.trace[chain_tile(args, t)].t_mma0 = ptx::globaltimer();
+        if (lane == 0 && kb == 0 && args.trace) args.trace[chain_tile(args, tr.q)].t_mma0 = ptx::globaltimer();
         if (lane == 0) {
           const uint32_t a0 = ptx::smem_u32(smem_a(st));
           const uint32_t b0 = ptx::smem_u32(smem_b(st));
@@ -901,7 +927,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         if (kPair) ptx::umma_commit_pair_multicast(&tfull[acc], 0x3);
         else ptx::umma_commit(&tfull[acc]);
         if (args.trace) {
-          TraceRec* r = args.trace + chain_tile(args, t);
+          TraceRec* r = args.trace + chain_tile(args, tr.q);
           r->t_mma1 = ptx::globaltimer();
           r->land_clk = land_clk;
         }
@@ -985,6 +1011,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         ++tcount;
         if (t < 0) break;
         const TileRef tr = decode_tile(args, t);
+        if (tr.s == kFillStage) continue;
         const StageGeo& g = stage_args(args, tr.s).g;
         if (g.a_mode == AMODE_POINTWISE) continue;
         if (!stage_consumes(args, tr.s)) {
@@ -992,6 +1019,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           continue;
         }
         const uint32_t abytes = a_tile_bytes(g);
+        const int32_t a_buf = args.stack ? stack_buf(args, tr.s - 1, *run_no) : -1;
         uint32_t check_clk = 0, reloads = 0;
         for (int32_t kb = 0; kb < tr.nkb; ++kb, ++it) {
           const int st = (int)(it % S);
@@ -1022,7 +1050,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
                 __nanosleep(128);
                 ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive_expect_tx(&cfull[st], abytes);
-                issue_a<PAIR>(args, tr, kb, rank, smem_a(st), &cfull[st], pol_a);
+                issue_a<PAIR>(args, tr, kb, rank, smem_a(st), &cfull[st], pol_a, a_buf);
               }
               ++reloads;
               __syncwarp();
@@ -1050,7 +1078,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
                   if (lane == 0) {
                     ptx::fence_proxy_async_smem();
                     ptx::mbar_arrive_expect_tx(&cfull[sj], abytes);
-                    issue_a<PAIR>(args, tr, kb + j, rank, smem_a(sj), &cfull[sj], pol_a);
+                    issue_a<PAIR>(args, tr, kb + j, rank, smem_a(sj), &cfull[sj], pol_a, a_buf);
                   }
                   ++reloads;
                 } else {
@@ -1074,7 +1102,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         }
         if (!ok) break;
         if (args.trace && leader && lane == 0) {
-          TraceRec* r = args.trace + chain_tile(args, t);
+          TraceRec* r = args.trace + chain_tile(args, tr.q);
           atomicAdd(&r->check_clk, check_clk);
           atomicAdd(&r->reloads, reloads);
         }
@@ -1113,6 +1141,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       ++tcount;
       if (t < 0) break;
       const TileRef tr = decode_tile(args, t);
+      if (tr.s == kFillStage) continue;
       const StageArgs& SA = stage_args(args, tr.s);
       const StageGeo& g = SA.g;
       const int32_t KB = tr.nkb;
@@ -1161,6 +1190,19 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       ++tcount;
       if (t < 0) break;
       const TileRef tr = decode_tile(args, t);
+      if (tr.s == kFillStage) {
+        // [CUDA-FGS] §4.6.4.5 "Buffer Reuse": the sentinel goes over the set of buffers
+        // the next run will use while this run's tail is still computing; that set was
+        // last read by the run before this one, which has finished.  Whole 16-byte chunks.
+        const uint32_t next = (*run_no + 1u) & 1u;
+        uint4* const base = reinterpret_cast<uint4*>(args.st[0].out) + (int64_t)next * args.set_chunks;
+        const int64_t c0 = (int64_t)tr.m * args.fill_unit_chunks;
+        const int64_t c1 = min(c0 + args.fill_unit_chunks, args.set_chunks);
+        const uint4 v = make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
+        // streaming stores: L2 keeps the lines of the stages still running, not these
+        for (int64_t c = c0 + (threadIdx.x - 64); c < c1; c += 128) __stcs(base + c, v);
+        continue;
+      }
       const StageArgs& SA = stage_args(args, tr.s);
       const StageGeo& g = SA.g;
       if (g.a_mode == AMODE_POINTWISE) {
@@ -1195,7 +1237,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       const bool stack_mid = args.stack && tr.s < args.nst - 1;
       const int32_t epi = (args.stack && !stack_mid) ? EPI_NONE : g.epi;
       __nv_bfloat16* const obase = stack_mid ? reinterpret_cast<__nv_bfloat16*>(args.st[0].out) +
-                                                   (int64_t)stack_buf(args, tr.s) * args.buf_elems
+                                                   (int64_t)stack_buf(args, tr.s, *run_no) * args.buf_elems
                                              : reinterpret_cast<__nv_bfloat16*>(SA.out);
       __nv_bfloat16* orow = obase + (valid ? grow * (int64_t)g.N : 0);
       const int32_t col0 = tr.c * g.n_out;
@@ -1367,7 +1409,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       }
       if (args.trace && leader && threadIdx.x == 64) {
         if (ptx::mbar_wait_bounded(&epi_done[acc], apar, pto))
-          args.trace[chain_tile(args, t)].t_epi = ptx::globaltimer();
+          args.trace[chain_tile(args, tr.q)].t_epi = ptx::globaltimer();
       }
       if (tr.s == 0 && threadIdx.x == 64 && !last_unit) {
         // K split: this unit's sums are in its workspace slot (the epi_done barrier orders
@@ -1396,7 +1438,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           } else if (!((args.flags_bits & kDebugSkipPost) && tr.m == 0 && tr.c == 0)) {
             ptx::fence_acq_rel_gpu();
             ptx::red_release_gpu_add(fl + flag, 1u);
-            if (args.trace && leader) args.trace[chain_tile(args, t)].t_post = ptx::globaltimer();
+            if (args.trace && leader) args.trace[chain_tile(args, tr.q)].t_post = ptx::globaltimer();
           }
         }
       }

@@ -60,6 +60,7 @@ struct Plan {
   StageGeo geo[3];      // per stage; a stack: geo[0] its first stage, geo[1] every later one
   int32_t stack;        // convolution stack (stages 1 .. nst-1 share geo[1] and `dep`)
   int32_t nbuf;         // stack: intermediate buffers in the workspace
+  int32_t rotate;       // stack under the sentinel policy: two sets of buffers used in turn
   int64_t flags_stride; // stack: semaphores per stage boundary
   DepCfg dep;           // the last stage's waits on the stage before it (a stack: every stage's)
   DepCfg dep_pw;        // attention: the pointwise stage's waits on the QKV GEMM
@@ -335,10 +336,14 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   p->num_flags = num_flags(dep);
   if (stack) {
     // one set of semaphores per stage boundary; the intermediates alternate between two
-    // buffers, except under the sentinel policy (one buffer each, filled before the run)
+    // buffers, except under the sentinel policy
     p->flags_stride = p->num_flags;
     p->num_flags = p->flags_stride * (p->nst - 1);
-    p->nbuf = d.policy == CUSYNC_POLICY_SENTINEL ? p->nst - 1 : std::min(2, p->nst - 1);
+    // under the sentinel policy one buffer per intermediate, in two sets that alternate
+    // between runs: each run's last launch writes the sentinel over the other set
+    // ([CUDA-FGS] §4.6.4.5 "Buffer Reuse"), so no fill precedes a run
+    p->rotate = d.policy == CUSYNC_POLICY_SENTINEL ? 1 : 0;
+    p->nbuf = p->rotate ? 2 * (p->nst - 1) : std::min(2, p->nst - 1);
   }
   if (p->num_flags > (1ll << 24)) return CUSYNC_ERR_UNSUPPORTED;
   p->split_rows = g0.ksplit > 1 ? (int64_t)g0.m_tiles * g0.n_tiles * pair : 0;
@@ -606,6 +611,8 @@ struct cusync_chain {
   const void* cached[6];
   bool maps_valid;
   ChainArgs args;
+  const void* filled_ws;  // rotating sentinel stack: the workspace whose sets hold the sentinel
+  bool need_fill;         // rotating sentinel stack: fill both sets before the next run
 };
 
 namespace {
@@ -650,9 +657,11 @@ cudaError_t launch_any(const Plan& p, const ChainArgs& a, int grid, bool pdl2, c
 // The launches of one chain run: sentinel fill, then one fused persistent kernel or the
 // producer and consumer kernels (stream order, or programmatic dependent launch).
 cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArgs A, const Grids& g, void* h,
-                           int sms, cudaStream_t stream) {
+                           int sms, cudaStream_t stream, bool fill_sets = false) {
   cudaError_t e;
-  if (d.policy == CUSYNC_POLICY_SENTINEL && !(d.flags & CUSYNC_DEBUG_SKIP_INIT)) {
+  // Sentinel fill before the run; a rotating stack fills both of its sets only when asked
+  // (a new workspace, or after a reset), its runs otherwise fill the next run's set.
+  if (d.policy == CUSYNC_POLICY_SENTINEL && !(d.flags & CUSYNC_DEBUG_SKIP_INIT) && (!p.rotate || fill_sets)) {
     // the intermediate (a stack: all of its intermediates, one buffer each)
     const int64_t bytes = (int64_t)p.geo[0].M * p.geo[0].N * 2 * (p.stack ? p.nbuf : 1);
     const int64_t n16 = bytes / 16;
@@ -768,6 +777,12 @@ void fill_static_args(const cusync_chain_desc_t& d, const Plan& p, uint32_t* sta
   A.nbuf = p.stack ? p.nbuf : 1;
   A.flags_stride = (int32_t)p.flags_stride;
   A.buf_elems = p.stack ? stack_buf_elems(d) : 0;
+  A.rotate = p.rotate;
+  if (p.rotate) {
+    A.set_chunks = (int64_t)(p.nst - 1) * A.buf_elems / 8;
+    A.fill_unit_chunks = 4096;  // 64 KB per unit
+    A.fill_units = (int32_t)ceil_div(A.set_chunks, A.fill_unit_chunks);
+  }
   A.flags_bits = d.flags;
   A.sentinel_check = d.policy == CUSYNC_POLICY_SENTINEL ? 1 : 0;
   A.num_flags = (int32_t)p.num_flags;
@@ -799,7 +814,13 @@ cusync_status_t run_chain(cusync_chain* ch, const void* a0, const void* b0, cons
   A.st[0].out = h;
   A.st[1].out = (p.nst == 3 && !p.stack) ? h2 : y;
   A.st[2].out = (p.nst == 3 && !p.stack) ? y : nullptr;
-  return launch_run(d, p, A, ch->grids, h, ch->num_sms, stream);
+  const bool fill_sets = p.rotate && (h != ch->filled_ws || ch->need_fill);
+  const cusync_status_t st = launch_run(d, p, A, ch->grids, h, ch->num_sms, stream, fill_sets);
+  if (st == CUSYNC_OK && p.rotate) {
+    ch->filled_ws = h;
+    ch->need_fill = false;
+  }
+  return st;
 }
 
 }  // namespace
@@ -934,6 +955,8 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
   fill_static_args(ch->d, p, ch->state, ch->split_ws, A);
   A.trace = ch->trace;
   ch->maps_valid = false;
+  ch->filled_ws = nullptr;
+  ch->need_fill = true;
   *out = ch;
   CUSYNC_LOG("chain kind=%d policy=%d launch=%d tiles=%d+%d bn=%d pair=%d sms=%d clusters=%d flags=%lld", d->kind,
              d->policy, d->launch, A.tiles0, A.tiles1, p.bn, p.pair, sms, max_clusters, (long long)p.num_flags);
@@ -974,6 +997,7 @@ cusync_status_t cusync_chain_reset(cusync_chain_t ch, cusync_stream_t stream) {
   const size_t words = (size_t)state_words(ch->plan);
   cudaError_t e = cudaMemsetAsync(ch->state, 0, words * sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "state reset");
+  ch->need_fill = true;  // a run that stopped early may have left the next set unfilled
   return CUSYNC_OK;
 }
 
