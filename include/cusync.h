@@ -173,7 +173,14 @@ typedef struct {
                                         wave, 2; else none; never fewer than 16 k-blocks
                                         per unit.  1 = none */
   int32_t stages;                    /* CONV_STACK: convolutions in the stack, 2..16 */
-  int32_t _pad1;
+  int32_t ksplit_consumer;           /* K split of the consumer GEMM of an MLP chain, as
+                                        ksplit: each consumer tile computed by this many
+                                        units, added in unit order by the last.  0 =
+                                        planner: when the consumer tiles fill at most half
+                                        of a wave, as many units per tile as fit in one
+                                        wave (at most 4, at least 16 k-blocks each);
+                                        none under STRIDED_TILE with more than 64 groups.
+                                        1 = none */
 } cusync_chain_desc_t;
 
 /* Wave arithmetic of a two-kernel chain ([cuSync] §II-A "Thread block Wave Execution",
@@ -236,6 +243,8 @@ typedef struct {
   int32_t work_buffers;       /* CONV_STACK: intermediate buffers in the workspace */
   int64_t work_bytes;         /* CONV_STACK: bytes of the caller's workspace (n*h*w*c
                                  bf16 per buffer) */
+  int32_t ksplit_consumer;    /* K-split units per consumer tile (1 = none) */
+  int32_t kb_per_split_consumer;
 } cusync_chain_info_t;
 
 /* Latency model of one chain run, in nanoseconds (cusync_predict_policies).  A tile
@@ -352,6 +361,14 @@ cusync_status_t cusync_plan_info(const cusync_chain_desc_t* d, cusync_chain_info
  * computation with the same code the device runs. */
 cusync_status_t cusync_consumer_waits(const cusync_chain_desc_t* d, int32_t m_tile, int32_t* kb, int32_t* flag,
                                       uint32_t* per_run, int32_t max, int32_t* n_out);
+
+/* The waits of work unit `unit` (0 .. ksplit_consumer-1) of consumer tile m_tile of a
+ * two-stage GEMM chain whose consumer is K-split: the same triples as
+ * cusync_consumer_waits for the k-blocks the unit computes, as its loader performs them
+ * (a unit waits before its own first k-block for what it reads there).  INVALID_ARG for
+ * other chains or an out-of-range tile or unit. */
+cusync_status_t cusync_consumer_unit_waits(const cusync_chain_desc_t* d, int32_t m_tile, int32_t unit, int32_t* kb,
+                                           int32_t* flag, uint32_t* per_run, int32_t max, int32_t* n_out);
 
 /* ATTENTION chains: the semaphore waits of pointwise tile (m_tile, head) on the QKV GEMM
  * ([cuSync] §IV-E; Fig. fig:use-case:self-attention:strided for StridedSync): entry i

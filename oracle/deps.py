@@ -184,10 +184,13 @@ def strided_producer_order(n_tiles, G):
     return [(y % G) * D + y // G for y in range(n_tiles)]
 
 
-def wait_sets(chain, policy, m, G=2):
+def wait_sets(chain, policy, m, G=2, kbs=None):
     """For consumer row-tile m: list over k-blocks of the producer tiles newly waited for
-    before that k-block's A load (cumulatively these must cover every data dependency)."""
-    kbs = range(chain.k_blocks)
+    before that k-block's A load (cumulatively these must cover every data dependency).
+
+    kbs: the k-blocks a work unit computes, in order (default: all of the tile's); a
+    K-split unit of the consumer waits for what its own k-blocks read, from its first."""
+    kbs = range(chain.k_blocks) if kbs is None else kbs
     deps = [data_deps(chain, m, kb) for kb in kbs]
     waited = set()
     out = []

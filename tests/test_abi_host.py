@@ -104,7 +104,8 @@ GPT = dict(K=12288, N1=6144, N2=12288)
 ])
 def test_plan_waves_gpt_mlp(M, tile_n, prod, cons, stream, fused):
     dims = dict(K=256, N1=1024, N2=256) if M == 64 else GPT
-    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, tile_n=tile_n, num_sms=148, cta_pair=1, ksplit=1, **dims)
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, tile_n=tile_n, num_sms=148, cta_pair=1, ksplit=1,
+                     ksplit_consumer=1, **dims)
     r = cs.cusync_plan_waves(d)
     assert (r.tbs[0], r.tbs[1]) == (prod, cons)
     assert r.tbs[0] == planner.gemm_tiles(M, dims["N1"], 128, tile_n)
@@ -119,7 +120,7 @@ def test_plan_waves_gpt_mlp(M, tile_n, prod, cons, stream, fused):
 ])
 def test_plan_waves_cta_pairs(M, prod, cons, stream, fused):
     # a CTA pair computes a 256 x 256 tile and occupies two SMs: 74 pairs on 148 SMs
-    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, tile_n=256, num_sms=148, cta_pair=2, ksplit=1, **GPT)
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, tile_n=256, num_sms=148, cta_pair=2, ksplit=1, ksplit_consumer=1, **GPT)
     r = cs.cusync_plan_waves(d)
     assert (r.tbs[0], r.tbs[1]) == (prod, cons)
     assert r.cap == 74
@@ -155,7 +156,7 @@ def test_cta_pair_only_for_mlp_chains():
 
 def test_plan_swiglu_and_conv():
     d = cs.make_desc(cs.CHAIN_MLP_SWIGLU, "TILE", M=256, K=8192, N1=3584, N2=8192, tile_n=256, num_sms=148,
-                     cta_pair=1, ksplit=1)
+                     cta_pair=1, ksplit=1, ksplit_consumer=1)
     r = cs.cusync_plan_waves(d)
     assert (r.tbs[0], r.tbs[1]) == (2 * 28, 2 * 32)
     d = cs.make_desc(cs.CHAIN_CONV_RELU, "TILE", n=32, h=14, w=14, c=256, k_out=256, tile_n=256, num_sms=148)
@@ -483,3 +484,70 @@ def test_stack_plan_and_refusals():
     with pytest.raises(cs.CusyncError) as e:
         cs.cusync_plan_info(cs.make_desc(cs.CHAIN_CONV_STACK, "ROW", n=1, h=8, w=8, c=96, stages=3, num_sms=152))
     assert e.value.status == cs.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kind,dims,pair,want", [
+    (cs.CHAIN_MLP_GELU, dict(M=256, **GPT), 2, 1),      # 48 pair tiles: more than half of 76 pairs
+    (cs.CHAIN_MLP_GELU, dict(M=1024, **GPT), 2, 1),
+    (cs.CHAIN_MLP_SWIGLU, dict(M=256, K=8192, N1=3584, N2=8192), 2, 2),   # 32 pair tiles: 2 units fit
+    (cs.CHAIN_MLP_SWIGLU, dict(M=256, K=8192, N1=3584, N2=8192), 1, 2),   # 64 tiles on 152 SMs
+    (cs.CHAIN_MLP_GELU, dict(M=64, K=12288, N1=6144, N2=12288), 1, 3),    # 48 tiles: 3 units fit in a wave
+    (cs.CHAIN_MLP_GELU, dict(M=64, K=256, N1=1024, N2=256), 1, 1),        # 16 k-blocks: nothing to split
+])
+def test_planner_consumer_split(kind, dims, pair, want):
+    d = cs.make_desc(kind, "ROW", num_sms=152, cta_pair=pair, tile_n=256, **dims)
+    info = cs.cusync_plan_info(d)
+    assert info.ksplit_consumer == want
+    assert info.kb_per_split_consumer * want >= info.k_blocks[1] > info.kb_per_split_consumer * (want - 1)
+    # the model plays whole consumer tiles, so its prediction does not depend on the split
+    d1 = cs.make_desc(kind, "ROW", num_sms=152, cta_pair=pair, tile_n=256, ksplit_consumer=1, **dims)
+    assert cs.cusync_predict_policies(d).us[cs.POLICY_ROW] == cs.cusync_predict_policies(d1).us[cs.POLICY_ROW]
+
+
+def test_consumer_split_requests():
+    base = dict(num_sms=152, tile_n=256, M=256, **GPT)
+    assert cs.cusync_plan_info(cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", ksplit_consumer=2, **base)).ksplit_consumer == 2
+    assert cs.cusync_plan_info(cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", ksplit_consumer=1, **base)).ksplit_consumer == 1
+    for bad, status in ((dict(ksplit_consumer=-1), cs.ERR_INVALID_ARG), (dict(ksplit_consumer=17), cs.ERR_INVALID_ARG)):
+        with pytest.raises(cs.CusyncError) as e:
+            cs.cusync_plan_info(cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", **bad, **base))
+        assert e.value.status == status
+    # only the MLP chains split their consumer
+    conv = dict(n=2, h=14, w=14, c=128, k_out=128, num_sms=152)
+    assert cs.cusync_plan_info(cs.make_desc(cs.CHAIN_CONV_RELU, "ROW", **conv)).ksplit_consumer == 1
+    with pytest.raises(cs.CusyncError) as e:
+        cs.cusync_plan_info(cs.make_desc(cs.CHAIN_CONV_RELU, "ROW", ksplit_consumer=2, **conv))
+    assert e.value.status == cs.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("case", [
+    dict(M=300, K=128, N1=1024, N2=256, tile_n=256),
+    dict(M=256, K=128, N1=1536, N2=256, tile_n=128),
+    dict(M=130, K=64, N1=2304, N2=64, tile_n=128),
+])
+@pytest.mark.parametrize("policy,G", [("TILE", 1), ("ROW", 1), ("STRIDED", 2), ("STRIDED", 3)])
+@pytest.mark.parametrize("ks", [2, 3])
+def test_consumer_unit_waits_match_oracle(case, policy, G, ks):
+    """Every K-split unit of a consumer tile waits, from its own first k-block on, for the
+    producer tiles the oracle's policy sets name for exactly the k-blocks it computes."""
+    desc = cs.make_desc(cs.CHAIN_MLP_GELU, policy, strided_group=G, num_sms=148, cta_pair=1, ksplit_consumer=ks,
+                        **case)
+    try:
+        info = cs.cusync_plan_info(desc)
+    except cs.CusyncError as e:
+        assert policy == "STRIDED" and e.status == cs.ERR_UNSUPPORTED
+        return
+    ch = _oracle_chain(desc, info)
+    nt, D, Gc = info.n_tiles[0], info.strided_distance, info.strided_group
+    per = info.kb_per_split_consumer
+    # units start on producer column tiles, which may leave fewer units than asked for
+    assert 1 < info.ksplit_consumer <= ks and per % max(1, info.n_out[0] // 64) == 0
+    for m in range(ch.m_tiles):
+        for u in range(info.ksplit_consumer):
+            kbs = list(range(u * per, min((u + 1) * per, ch.k_blocks)))
+            got = {kb: set() for kb in kbs}
+            for kb, flag, per_run in cs.cusync_consumer_unit_waits(desc, m, u):
+                assert kb in got
+                got[kb] |= _members(policy, flag, nt, D, Gc)
+            want = deps.wait_sets(ch, policy, m, Gc, kbs=kbs)
+            assert [got[kb] for kb in kbs] == want, (policy, m, u)

@@ -237,6 +237,33 @@ def test_k_split_producer_all_policies(ksplit, pair):
                 assert np.array_equal(b[0], ref_bits[0]) and np.array_equal(b[1], ref_bits[1]), (pol, launch)
 
 
+@pytest.mark.parametrize("ks,ks_prod,pair", [(2, 1, 1), (3, 2, 1), (3, 1, 2), (4, 2, 2)])
+def test_k_split_consumer_all_policies(ks, ks_prod, pair):
+    """Consumer tiles computed as K-split units, each waiting from its own first k-block
+    for what it reads (StridedSync groups included): every policy and launch mode within
+    tolerance of the oracle and byte-identical to one another; with a split producer too."""
+    M, K, N1, N2 = 300, 1024, 2048, 512
+    (X, W1, W2), (H_ref, Y_ref) = _mlp_case(M, K, N1, N2, seed=12)
+    ops = device_mlp_operands(X, W1, W2)
+    ref_bits = None
+    for pol in POLICIES:
+        for launch in LAUNCHES:
+            if pol == "STREAM" and launch != cs.LAUNCH_PERSISTENT:
+                continue
+            d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, launch, M=M, K=K, N1=N1, N2=N2, tile_n=256, cta_pair=pair,
+                             ksplit=ks_prod, ksplit_consumer=ks)
+            info = cs.cusync_plan_info(d)
+            assert info.ksplit_consumer == ks and info.ksplit == ks_prod
+            H, Y, _ = run_mlp(d, *ops, runs=3)
+            assert_within_tol(f64(H), H_ref, f"H {pol} {launch}")
+            assert_within_tol(f64(Y), Y_ref, f"Y {pol} {launch}")
+            b = (bits(H), bits(Y))
+            if ref_bits is None:
+                ref_bits = b
+            else:
+                assert np.array_equal(b[0], ref_bits[0]) and np.array_equal(b[1], ref_bits[1]), (pol, launch)
+
+
 def test_k_split_swiglu():
     M, K, N1, N2 = 200, 1024, 512, 256
     X, Wg, Wu, Wd = synth.mlp_swiglu_inputs(M, K, N1, N2, seed=9)

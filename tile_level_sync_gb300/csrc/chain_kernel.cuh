@@ -105,6 +105,8 @@ struct ChainArgs {
   TraceRec* trace;       // per-tile timeline, or null
   float* split_ws;       // K split: fp32 partial sums, per (tile, pair rank) ksplit-1 slots of 128 x BN
   uint32_t* split_turn;  // K split: units of a tile's rows that have stored their sums
+  float* split_ws1;      // the same for a K-split consumer (stage 1 of a two-stage chain)
+  uint32_t* split_turn1;
   int32_t queue;         // tile counter slot used by this launch
   int32_t first_stage;   // stages served by this launch: [first_stage, last_stage]
   int32_t last_stage;
@@ -659,6 +661,8 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         uint64_t dep_mask = 0;
         if (cons && (pol == POL_ROW || pol == POL_TILE || pol == POL_STRIDED)) {
           if (gemm) {
+            // (a K-split unit of the consumer starts at a multiple of the period: the
+            // planner aligns kb_per_split, so the test below needs no offset)
             dep_every = pol == POL_ROW ? KB + 1 : max(1, args.dep.prod_n_out / kBK);
           } else {
             for (int32_t k = 0; k < KB && k < 64; ++k)
@@ -711,7 +715,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         // releases, and a proxy fence orders them for the TMA (async proxy).
         auto wait_deps = [&](int32_t kb) {
           Wait w[kMaxWaits];
-          const int n = gemm ? gdt.next(args.dep, tr.m, kb, w) : cdt.next(SA.g, args.dep, tr.m, kb, w);
+          const int n = gemm ? gdt.next(args.dep, tr.m, tr.kb0 + kb, w) : cdt.next(SA.g, args.dep, tr.m, kb, w);
           bool observed = false;
           for (int i = 0; i < n; ++i) {
             const int32_t f = w[i].flag;
@@ -764,6 +768,9 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         // instruction latency per k-block is on the critical path of the GEMM mainloop.
         if (gemm) {
           for (int32_t kb = 0; kb < KB; ++kb) {
+            // every dep_every-th k-block of the unit (unit_dep_kblock); one more term in this
+            // test measured 9-12% slower: the loader thread's latency per k-block is the
+            // mainloop's critical path
             const bool dep_kb = dep_every > 0 && (kb % dep_every) == 0;
             if (dep_kb && !reorder) wait_deps(kb);
             if (bnext == kb) {
@@ -1050,7 +1057,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
                 __nanosleep(128);
                 ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive_expect_tx(&cfull[st], abytes);
-                issue_a<PAIR>(args, tr, kb, rank, smem_a(st), &cfull[st], pol_a, a_buf);
+                issue_a<PAIR>(args, tr, tr.kb0 + kb, rank, smem_a(st), &cfull[st], pol_a, a_buf);
               }
               ++reloads;
               __syncwarp();
@@ -1078,7 +1085,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
                   if (lane == 0) {
                     ptx::fence_proxy_async_smem();
                     ptx::mbar_arrive_expect_tx(&cfull[sj], abytes);
-                    issue_a<PAIR>(args, tr, kb + j, rank, smem_a(sj), &cfull[sj], pol_a, a_buf);
+                    issue_a<PAIR>(args, tr, tr.kb0 + kb + j, rank, smem_a(sj), &cfull[sj], pol_a, a_buf);
                   }
                   ++reloads;
                 } else {
@@ -1257,6 +1264,8 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       // association for every run and policy), and applies the epilogue to the total.
       const bool split = g.ksplit > 1;
       const bool last_unit = !split || tr.ks == g.ksplit - 1;
+      float* const split_ws = tr.s == 0 ? args.split_ws : args.split_ws1;
+      uint32_t* const split_turn = tr.s == 0 ? args.split_turn : args.split_turn1;
       // Workspace layout per slot of a 128-row block: groups of 4 columns, then rows,
       // then the 4 columns -- a warp's 32 rows of one column group are 512 contiguous
       // bytes, so the float4 accesses below are fully coalesced.
@@ -1264,9 +1273,9 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       float4* ws_row = nullptr;
       if (split) {
         const int64_t tile_id = ((int64_t)tr.m * g.n_tiles + tr.c) * PAIR + (int64_t)rank;
-        ws_row = reinterpret_cast<float4*>(args.split_ws) + tile_id * (g.ksplit - 1) * kSlotF4 + row;
+        ws_row = reinterpret_cast<float4*>(split_ws) + tile_id * (g.ksplit - 1) * kSlotF4 + row;
         if (last_unit) {
-          const uint32_t* turn = args.split_turn + tile_id;
+          const uint32_t* turn = split_turn + tile_id;
           const uint32_t target = *run_no * (uint32_t)(g.ksplit - 1);
           const uint64_t t0 = ptx::globaltimer();
           while ((int32_t)(ptx::ld_acquire_gpu(turn) - target) < 0) {
@@ -1411,7 +1420,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         if (ptx::mbar_wait_bounded(&epi_done[acc], apar, pto))
           args.trace[chain_tile(args, tr.q)].t_epi = ptx::globaltimer();
       }
-      if (tr.s == 0 && threadIdx.x == 64 && !last_unit) {
+      if (threadIdx.x == 64 && !last_unit) {
         // K split: this unit's sums are in its workspace slot (the epi_done barrier orders
         // the 128 threads' stores before this thread); count it for the tile's last unit.
         if (!ptx::mbar_wait_bounded(&epi_done[acc], apar, pto)) {
@@ -1420,7 +1429,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         } else {
           const int64_t tile_id = ((int64_t)tr.m * g.n_tiles + tr.c) * PAIR + (int64_t)rank;
           ptx::fence_acq_rel_gpu();
-          ptx::red_release_gpu_add(args.split_turn + tile_id, 1u);
+          ptx::red_release_gpu_add(split_turn + tile_id, 1u);
         }
       } else if ((args.stack ? stack_mid : tr.s == 0) && threadIdx.x == 64) {
         // stage 0 feeds the last stage (two-stage chains) or the pointwise stage (attention);

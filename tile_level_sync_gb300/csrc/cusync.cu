@@ -67,6 +67,7 @@ struct Plan {
   int64_t num_flags;
   int64_t num_flags_pw;
   int64_t split_rows;   // K split: workspace row blocks (producer tiles x pair), else 0
+  int64_t split_rows1;  // K split of the consumer: its row blocks, else 0
 };
 
 // Geometry of stage s.
@@ -83,11 +84,14 @@ int64_t total_units(const Plan& p) {
 int64_t stack_buf_elems(const cusync_chain_desc_t& d) { return (int64_t)d.n * d.h * d.w * d.c; }
 
 // Words of a chain's device state: control words, semaphores, K-split turn counters.
-int64_t state_words(const Plan& p) { return CTRL_WORDS + p.num_flags + p.num_flags_pw + p.split_rows; }
+int64_t state_words(const Plan& p) {
+  return CTRL_WORDS + p.num_flags + p.num_flags_pw + p.split_rows + p.split_rows1;
+}
 // fp32 elements of the K-split workspace: ksplit - 1 slots of a 128-row accumulator per
 // row block.
+int64_t split_ws_floats0(const Plan& p) { return p.split_rows * (int64_t)(p.geo[0].ksplit - 1) * 128 * (int64_t)p.bn; }
 int64_t split_ws_floats(const Plan& p) {
-  return p.split_rows * (int64_t)(p.geo[0].ksplit - 1) * 128 * (int64_t)p.bn;
+  return split_ws_floats0(p) + p.split_rows1 * (int64_t)(p.geo[1].ksplit - 1) * 128 * (int64_t)p.bn;
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -282,8 +286,35 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   g0.ksplit = ks;
   g0.kb_per_split = (int32_t)ceil_div(g0.k_blocks, ks);
   g0.ksplit = (int32_t)ceil_div(g0.k_blocks, g0.kb_per_split);  // no empty unit
+  // K split of the consumer GEMM of an MLP chain (cusync_chain_desc_t::ksplit_consumer):
+  // consumer tiles that fill at most half of a wave get as many units per tile as fit in
+  // one wave (at most 4, at least 16 k-blocks each).  Measured on GB300: 5-10% faster for
+  // the SwiGLU M=256 slice (32 pair tiles of 56 k-blocks), but 4-9% slower for the GPT-3
+  // M=256 and M=512 slices (48 and 96 pair tiles of 96 k-blocks) with three units, whose
+  // consumers' partial sums cost more than the fuller waves gain.
+  if (d.ksplit_consumer < 0 || d.ksplit_consumer > 16) return CUSYNC_ERR_INVALID_ARG;
+  int32_t ks1 = d.ksplit_consumer;
+  if (ks1 == 0) {
+    ks1 = 1;
+    if (mlp) {
+      int sms = 0;
+      if (query_num_sms(d.num_sms, &sms) != 0) sms = 148;
+      const int64_t slots = std::max<int64_t>(1, sms / pair);
+      const int64_t t1 = (int64_t)g1.m_tiles * g1.n_tiles;
+      if (t1 > 0 && 2 * t1 <= slots)
+        ks1 = (int32_t)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(slots / t1, 4), g1.k_blocks / 16));
+    }
+  }
+  if (ks1 > 1 && !mlp) return CUSYNC_ERR_UNSUPPORTED;
+  if (ks1 > 1 && ks1 > g1.k_blocks) return CUSYNC_ERR_UNSUPPORTED;
   g1.ksplit = 1;
   g1.kb_per_split = g1.k_blocks;
+  if (ks1 > 1) {
+    // units start on producer column tiles (kb_per_split_alignment), no empty unit
+    const int32_t al = kb_per_split_alignment(g0.n_out);
+    g1.kb_per_split = (int32_t)(ceil_div(ceil_div(g1.k_blocks, ks1), al) * al);
+    g1.ksplit = (int32_t)ceil_div(g1.k_blocks, g1.kb_per_split);
+  }
   g2.ksplit = 1;
   g2.kb_per_split = g2.k_blocks;
   if (d.l2_prefetch < -1 || d.l2_prefetch > 64) return CUSYNC_ERR_INVALID_ARG;
@@ -333,6 +364,13 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
     dep.G = G;
     dep.D = g0.n_tiles / G;
   }
+  if (g1.ksplit > 1 && dep.policy == POL_STRIDED && dep.D > 64) {
+    // a StridedSync unit remembers its waited groups in 64 bits
+    if (d.ksplit_consumer > 1) return CUSYNC_ERR_UNSUPPORTED;
+    g1.ksplit = 1;
+    g1.kb_per_split = g1.k_blocks;
+  }
+  p->split_rows1 = g1.ksplit > 1 ? (int64_t)g1.m_tiles * g1.n_tiles * pair : 0;
   p->num_flags = num_flags(dep);
   if (stack) {
     // one set of semaphores per stage boundary; the intermediates alternate between two
@@ -556,6 +594,7 @@ void predict_all(const cusync_chain_desc_t& d, const cusync_latency_model_t* mod
   for (int pol = CUSYNC_POLICY_STREAM; pol <= CUSYNC_POLICY_SENTINEL; ++pol) {
     cusync_chain_desc_t c = d;
     c.policy = (cusync_policy_t)pol;
+    c.ksplit_consumer = 1;  // the model plays whole consumer tiles
     Plan q;
     if (make_plan(c, &q) != CUSYNC_OK || q.nst != 2) {  // the model covers two-stage chains
       us[pol] = -1.0;
@@ -769,7 +808,9 @@ void fill_static_args(const cusync_chain_desc_t& d, const Plan& p, uint32_t* sta
   A.flags = state + CTRL_WORDS;
   A.flags_pw = state + CTRL_WORDS + p.num_flags;
   A.split_turn = p.split_rows > 0 ? state + CTRL_WORDS + p.num_flags + p.num_flags_pw : nullptr;
-  A.split_ws = split_ws;
+  A.split_ws = p.split_rows > 0 ? split_ws : nullptr;
+  A.split_turn1 = p.split_rows1 > 0 ? state + CTRL_WORDS + p.num_flags + p.num_flags_pw + p.split_rows : nullptr;
+  A.split_ws1 = p.split_rows1 > 0 ? split_ws + split_ws_floats0(p) : nullptr;
   A.tiles0 = (int32_t)t0;
   A.tiles1 = (int32_t)t1;
   A.tiles2 = (int32_t)stage_units(p.geo[2]);
@@ -933,7 +974,8 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
     delete ch;
     return cuda_fail(e, "state clear");
   }
-  if (p.split_rows > 0 && cudaMalloc(&ch->split_ws, (size_t)split_ws_floats(p) * sizeof(float)) != cudaSuccess) {
+  if ((p.split_rows > 0 || p.split_rows1 > 0) &&
+      cudaMalloc(&ch->split_ws, (size_t)split_ws_floats(p) * sizeof(float)) != cudaSuccess) {
     cudaFree(ch->state);
     delete ch;
     return CUSYNC_ERR_NOMEM;
@@ -1052,6 +1094,8 @@ cusync_status_t cusync_plan_info(const cusync_chain_desc_t* d, cusync_chain_info
   out->policy = p.nst == 3 ? p.dep_pw.policy : p.dep.policy;
   out->ksplit = p.geo[0].ksplit;
   out->kb_per_split = p.geo[0].kb_per_split;
+  out->ksplit_consumer = p.geo[1].ksplit;
+  out->kb_per_split_consumer = p.geo[1].kb_per_split;
   out->nst = p.nst;
   out->m_tiles2 = p.geo[2].m_tiles;
   out->n_tiles2 = p.geo[2].n_tiles;
@@ -1138,6 +1182,38 @@ cusync_status_t cusync_consumer_waits(const cusync_chain_desc_t* d, int32_t m_ti
     for (int i = 0; i < c; ++i, ++n) {
       if (n < max) {
         kb[n] = k;
+        flag[n] = w[i].flag;
+        per_run[n] = w[i].per_run;
+      }
+    }
+  }
+  *n_out = n;
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_consumer_unit_waits(const cusync_chain_desc_t* d, int32_t m_tile, int32_t unit, int32_t* kb,
+                                           int32_t* flag, uint32_t* per_run, int32_t max, int32_t* n_out) {
+  if (!d || !n_out || max < 0) return CUSYNC_ERR_INVALID_ARG;
+  Plan p;
+  cusync_status_t st = make_plan(*d, &p);
+  if (st != CUSYNC_OK) return st;
+  if (p.stack || p.nst != 2) return CUSYNC_ERR_INVALID_ARG;
+  const StageGeo& g = p.geo[1];
+  if (g.a_mode != AMODE_GEMM) return CUSYNC_ERR_INVALID_ARG;
+  if (m_tile < 0 || m_tile >= g.m_tiles || unit < 0 || unit >= g.ksplit) return CUSYNC_ERR_INVALID_ARG;
+  if (max > 0 && (!kb || !flag || !per_run)) return CUSYNC_ERR_INVALID_ARG;
+  const int32_t kb0 = unit * g.kb_per_split;
+  const int32_t nkb = std::min(g.kb_per_split, g.k_blocks - kb0);
+  GemmDepTracker t;
+  t.reset();
+  int32_t n = 0;
+  for (int32_t k = 0; k < nkb; ++k) {
+    if (!unit_dep_kblock(p.dep, kb0, nkb, k)) continue;
+    Wait w[kMaxWaits];
+    const int c = t.next(p.dep, m_tile, kb0 + k, w);
+    for (int i = 0; i < c; ++i, ++n) {
+      if (n < max) {
+        kb[n] = kb0 + k;
         flag[n] = w[i].flag;
         per_run[n] = w[i].per_run;
       }
@@ -1265,6 +1341,7 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
   if (d->ksplit > 1) return CUSYNC_ERR_UNSUPPORTED;
   cusync_chain_desc_t dd = *d;
   dd.ksplit = 1;
+  dd.ksplit_consumer = 1;
   Plan p;
   cusync_status_t st = make_plan(dd, &p);
   if (st != CUSYNC_OK) return st;

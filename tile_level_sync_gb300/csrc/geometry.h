@@ -155,14 +155,21 @@ CUSYNC_HD void conv_row_tiles(const StageGeo& g, int32_t m, int32_t r, int32_t* 
 // GEMM chains: consumer k-block kb reads producer column tile c = kb*kBK / prod_n_out
 // of its own row tile, so at most one wait per k-block and only the last column waited
 // needs remembering (register state only).
+// A work unit's k-blocks are visited in increasing order from its first one (k-block 0 for
+// a whole tile, a later one for a K-split unit of a consumer tile).
 struct GemmDepTracker {
   int32_t last_c;
-  CUSYNC_HD void reset() { last_c = -1; }
+  uint64_t groups;  // StridedSync: groups already waited for (D <= 64)
+  CUSYNC_HD void reset() {
+    last_c = -1;
+    groups = 0;
+  }
   CUSYNC_HD int next(const DepCfg& d, int32_t m, int32_t kb, Wait* out) {
     const int32_t pol = d.policy;
     const uint32_t pp = (uint32_t)d.posts;
-    if (pol == POL_ROW) {
-      if (kb != 0) return 0;
+    if (pol == POL_ROW) {  // the whole row, before the unit's first k-block
+      if (last_c != -1) return 0;
+      last_c = 0;
       out[0] = Wait{m, (uint32_t)d.prod_n_tiles * pp};
       return 1;
     }
@@ -174,11 +181,17 @@ struct GemmDepTracker {
       out[0] = Wait{m * d.prod_n_tiles + c, pp};
       return 1;
     }
-    if (c < d.D) {  // StridedSync: group c is first touched at column c
-      out[0] = Wait{m * d.D + c, (uint32_t)d.G * pp};
-      return 1;
+    // StridedSync: column c belongs to group c mod D, waited for at its first touch (from
+    // column 0 on, group g is first touched at column g)
+    const int32_t grp = c % d.D;
+    if (d.D <= 64) {
+      if ((groups >> grp) & 1ull) return 0;
+      groups |= 1ull << grp;
+    } else if (c >= d.D) {
+      return 0;  // whole tiles only (a K split of the consumer needs D <= 64)
     }
-    return 0;
+    out[0] = Wait{m * d.D + grp, (uint32_t)d.G * pp};
+    return 1;
   }
 };
 
@@ -246,6 +259,7 @@ struct ConvDepTracker {
 // k-block (filter tap r*3+s, channel block cb) reads the producer row tiles of filter
 // row r, which change only when s returns to 0, and producer column tile
 // cb*kBK / prod_n_out, which changes every prod_n_out / kBK channel blocks.
+// (A K-split unit of a consumer tile also consults the tracker at its first k-block.)
 CUSYNC_HD bool dep_kblock(const StageGeo& cons, const DepCfg& d, int32_t kb) {
   const int32_t pol = d.policy;
   if (pol != POL_TILE && pol != POL_ROW && pol != POL_STRIDED) return false;
@@ -255,6 +269,24 @@ CUSYNC_HD bool dep_kblock(const StageGeo& cons, const DepCfg& d, int32_t kb) {
   const int32_t tap = kb / cons.cblocks, cb = kb % cons.cblocks;
   return tap % 3 == 0 && cb % per_col == 0;
 }
+
+// Whether a work unit of a GEMM consumer (KB k-blocks from k-block kb0 of its tile)
+// consults its tracker before its k-block kb (counted from the unit's first): RowSync at
+// the unit's first k-block, TileSync and StridedSync at every k-block that starts a
+// producer column tile.  The planner makes kb0 a multiple of that period
+// (kb_per_split_alignment), so the unit's first k-block is always one of them; the
+// loader evaluates the same test.
+CUSYNC_HD bool unit_dep_kblock(const DepCfg& d, int32_t kb0, int32_t KB, int32_t kb) {
+  const int32_t pol = d.policy;
+  if (pol != POL_TILE && pol != POL_ROW && pol != POL_STRIDED) return false;
+  (void)kb0;
+  const int32_t every = pol == POL_ROW ? KB + 1 : (d.prod_n_out / kBK > 1 ? d.prod_n_out / kBK : 1);
+  return (kb % every) == 0;
+}
+
+// K-block period that a consumer's K-split units must start on: the k-blocks of one
+// producer column tile.
+CUSYNC_HD int32_t kb_per_split_alignment(int32_t prod_n_out) { return prod_n_out / kBK > 1 ? prod_n_out / kBK : 1; }
 
 // Semaphore waits of the attention chain's pointwise tile (m, i) (head i of row tile m) on
 // the QKV GEMM, whose output row holds the Q, V and K blocks of width nq = 3 * D column
