@@ -103,10 +103,9 @@ struct ChainArgs {
   uint32_t* flags_pw;    // semaphores of `dep_pw`
   uint32_t* ctrl;        // CTRL_* words
   TraceRec* trace;       // per-tile timeline, or null
-  float* split_ws;       // K split: fp32 partial sums, per (tile, pair rank) ksplit-1 slots of 128 x BN
-  uint32_t* split_turn;  // K split: units of a tile's rows that have stored their sums
+  float* split_ws;       // K split: fp32 partial sums, per (tile, pair rank) ksplit-1 slots of 128 x BN;
+                         // every word not holding a sum holds kSplitEmpty
   float* split_ws1;      // the same for a K-split consumer (stage 1 of a two-stage chain)
-  uint32_t* split_turn1;
   int32_t queue;         // tile counter slot used by this launch
   int32_t first_stage;   // stages served by this launch: [first_stage, last_stage]
   int32_t last_stage;
@@ -295,6 +294,15 @@ __device__ __forceinline__ void record_error(const ChainArgs& a, uint32_t cls, i
 __device__ __forceinline__ uint32_t sentinel_bits_bf16x2(uint32_t x) {
   const uint32_t t = x ^ 0x80008000u;
   return (t - 0x00010001u) & ~t;
+}
+
+// K-split workspace words that hold no partial sum hold kSplitEmpty, a NaN (sign set,
+// all payload bits set); a unit stores a sum equal to it as the canonical NaN instead,
+// so a word holds either kSplitEmpty or a sum.
+constexpr uint32_t kSplitEmpty = 0xFFFFFFFFu;
+__device__ __forceinline__ uint32_t split_canon(uint32_t x) { return x == kSplitEmpty ? 0x7FFFFFFFu : x; }
+__device__ __forceinline__ bool split_empty(const uint4& v) {
+  return (v.x == kSplitEmpty) | (v.y == kSplitEmpty) | (v.z == kSplitEmpty) | (v.w == kSplitEmpty);
 }
 
 __device__ __forceinline__ uint32_t canon_bf16x2(uint32_t x) {
@@ -1259,69 +1267,99 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       uint8_t* ebuf = epi_stage + (q * 2) * C::kEpiBufBytes;
       const int32_t row_w0 = tr.m * (128 * PAIR) + (int32_t)rank * 128 + q * 32;
       // K split: the units of a tile other than the last store their fp32 partial sums
-      // in their own workspace slot and count themselves done; the last unit waits for
-      // all of them, adds the slots in unit order and then its own sums (the same
-      // association for every run and policy), and applies the epilogue to the total.
+      // in their own workspace slot; the last unit adds the slots in unit order and then
+      // its own sums (the same association for every run and policy), and applies the
+      // epilogue to the total.  The slots mark their own readiness: a word that holds no
+      // sum holds kSplitEmpty, a NaN that a sum never takes (the storing unit writes any
+      // such value as the canonical NaN), so the last unit re-reads a 16-byte word until
+      // it holds a sum, with no counter or fence between the units, and writes
+      // kSplitEmpty back once it has read it ([CUDA-FGS] §4.6.4 sentinel protocol, here
+      // for the partial sums rather than for the intermediate).
       const bool split = g.ksplit > 1;
       const bool last_unit = !split || tr.ks == g.ksplit - 1;
       float* const split_ws = tr.s == 0 ? args.split_ws : args.split_ws1;
-      uint32_t* const split_turn = tr.s == 0 ? args.split_turn : args.split_turn1;
       // Workspace layout per slot of a 128-row block: groups of 4 columns, then rows,
       // then the 4 columns -- a warp's 32 rows of one column group are 512 contiguous
-      // bytes, so the float4 accesses below are fully coalesced.
-      constexpr int kSlotF4 = 128 * BN / 4;  // float4s per slot
-      float4* ws_row = nullptr;
+      // bytes, so the 16-byte accesses below are fully coalesced.
+      constexpr int kSlotF4 = 128 * BN / 4;  // 16-byte words per slot
+      uint4* ws_row = nullptr;
       if (split) {
         const int64_t tile_id = ((int64_t)tr.m * g.n_tiles + tr.c) * PAIR + (int64_t)rank;
-        ws_row = reinterpret_cast<float4*>(split_ws) + tile_id * (g.ksplit - 1) * kSlotF4 + row;
-        if (last_unit) {
-          const uint32_t* turn = split_turn + tile_id;
-          const uint32_t target = *run_no * (uint32_t)(g.ksplit - 1);
-          const uint64_t t0 = ptx::globaltimer();
-          while ((int32_t)(ptx::ld_acquire_gpu(turn) - target) < 0) {
-            __nanosleep(64);
-            if (ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u) break;
-            if (ptx::globaltimer() - t0 > args.timeout_ns) {
-              record_error(args, ERRC_FLAG_TIMEOUT, t, 0xFFFF);
-              break;
-            }
-          }
-        }
+        ws_row = reinterpret_cast<uint4*>(split_ws) + tile_id * (g.ksplit - 1) * kSlotF4 + row;
       }
-      // 32 accumulator columns from `col` on: a unit that is not the last stores them in
-      // its slot; the last one replaces them by slot 0 + slot 1 + ... + its own.  Through
-      // L2, not L1: the workspace is written and read by different CTAs.
-      auto split_add = [&](uint32_t (&x)[32], int col) {
-        float4* w = ws_row + (col / 4) * 128;  // column group col/4 + i is at w + i * 128
-        if (!last_unit) {
-          float4* ws = w + tr.ks * kSlotF4;
+      const uint64_t split_t0 = (split && last_unit) ? ptx::globaltimer() : 0;
+      bool split_late = false;  // a slot word stayed empty past the timeout (error recorded)
+      // The 8 words of one slot at p (stride 128 words): split_issue loads them into v;
+      // split_settle re-reads those that still hold kSplitEmpty and then marks the 8
+      // words empty again for the next run.  Two slots are in flight at a time.
+      auto split_issue = [&](uint4 (&v)[8], const uint4* p) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = ptx::ld_relaxed_gpu_b128(p + i * 128);
+      };
+      auto split_settle = [&](uint4 (&v)[8], uint4* p) {
+        auto any_empty = [&]() {
+          bool e = false;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) e |= split_empty(v[i]);
+          return e;
+        };
+        uint32_t polls = 0;
+        while (!split_late && any_empty()) {
+          __nanosleep(128);
+          if ((++polls & 15u) == 0 && ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u) {
+            split_late = true;  // another wait already failed: stop polling
+            break;
+          }
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            __stcg(ws + i * 128, make_float4(__uint_as_float(x[4 * i]), __uint_as_float(x[4 * i + 1]),
-                                             __uint_as_float(x[4 * i + 2]), __uint_as_float(x[4 * i + 3])));
+            if (split_empty(v[i])) v[i] = ptx::ld_relaxed_gpu_b128(p + i * 128);
+          if (ptx::globaltimer() - split_t0 > args.timeout_ns && any_empty()) {
+            record_error(args, ERRC_FLAG_TIMEOUT, t, 0xFFFF);
+            split_late = true;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ptx::st_relaxed_gpu_b128(p + i * 128, kSplitEmpty, kSplitEmpty, kSplitEmpty, kSplitEmpty);
+      };
+      // 32 accumulator columns from `col` on: a unit that is not the last stores them in
+      // its slot; the last one replaces them by slot 0 + slot 1 + ... + its own.
+      auto split_add = [&](uint32_t (&x)[32], int col) {
+        uint4* w = ws_row + (col / 4) * 128;  // column group col/4 + i is at w + i * 128
+        if (!last_unit) {
+          uint4* ws = w + tr.ks * kSlotF4;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            ptx::st_relaxed_gpu_b128(ws + i * 128, split_canon(x[4 * i]), split_canon(x[4 * i + 1]),
+                                     split_canon(x[4 * i + 2]), split_canon(x[4 * i + 3]));
           return;
         }
-        float4 a[8];
+        uint4 a[8];
+        split_issue(a, w);
+        if (g.ksplit > 2) {
+          uint4 b[8];
+          split_issue(b, w + kSlotF4);
+          split_settle(a, w);
+          for (int k = 1;; ++k) {
+            split_settle(b, w + k * kSlotF4);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = __ldcg(w + i * 128);  // eight loads in flight per slot
-        for (int k = 1; k < g.ksplit - 1; ++k) {
-          float4 b[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) b[i] = __ldcg(w + k * kSlotF4 + i * 128);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            a[i].x += b[i].x;
-            a[i].y += b[i].y;
-            a[i].z += b[i].z;
-            a[i].w += b[i].w;
+            for (int i = 0; i < 8; ++i) {
+              a[i].x = __float_as_uint(__uint_as_float(a[i].x) + __uint_as_float(b[i].x));
+              a[i].y = __float_as_uint(__uint_as_float(a[i].y) + __uint_as_float(b[i].y));
+              a[i].z = __float_as_uint(__uint_as_float(a[i].z) + __uint_as_float(b[i].z));
+              a[i].w = __float_as_uint(__uint_as_float(a[i].w) + __uint_as_float(b[i].w));
+            }
+            if (k + 1 >= g.ksplit - 1) break;
+            split_issue(b, w + (k + 1) * kSlotF4);
           }
+        } else {
+          split_settle(a, w);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          x[4 * i + 0] = __float_as_uint(a[i].x + __uint_as_float(x[4 * i + 0]));
-          x[4 * i + 1] = __float_as_uint(a[i].y + __uint_as_float(x[4 * i + 1]));
-          x[4 * i + 2] = __float_as_uint(a[i].z + __uint_as_float(x[4 * i + 2]));
-          x[4 * i + 3] = __float_as_uint(a[i].w + __uint_as_float(x[4 * i + 3]));
+          x[4 * i + 0] = __float_as_uint(__uint_as_float(a[i].x) + __uint_as_float(x[4 * i + 0]));
+          x[4 * i + 1] = __float_as_uint(__uint_as_float(a[i].y) + __uint_as_float(x[4 * i + 1]));
+          x[4 * i + 2] = __float_as_uint(__uint_as_float(a[i].z) + __uint_as_float(x[4 * i + 2]));
+          x[4 * i + 3] = __float_as_uint(__uint_as_float(a[i].w) + __uint_as_float(x[4 * i + 3]));
         }
       };
       for (int j = 0; j < nchunks; ++j) {
@@ -1420,17 +1458,8 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         if (ptx::mbar_wait_bounded(&epi_done[acc], apar, pto))
           args.trace[chain_tile(args, tr.q)].t_epi = ptx::globaltimer();
       }
-      if (threadIdx.x == 64 && !last_unit) {
-        // K split: this unit's sums are in its workspace slot (the epi_done barrier orders
-        // the 128 threads' stores before this thread); count it for the tile's last unit.
-        if (!ptx::mbar_wait_bounded(&epi_done[acc], apar, pto)) {
-          record_error(args, ERRC_PIPELINE, t, 7);
-          *abort_flag = 1;
-        } else {
-          const int64_t tile_id = ((int64_t)tr.m * g.n_tiles + tr.c) * PAIR + (int64_t)rank;
-          ptx::fence_acq_rel_gpu();
-          ptx::red_release_gpu_add(split_turn + tile_id, 1u);
-        }
+      if (!last_unit) {
+        // K split: this unit's sums are in its workspace slot, which marks itself ready
       } else if ((args.stack ? stack_mid : tr.s == 0) && threadIdx.x == 64) {
         // stage 0 feeds the last stage (two-stage chains) or the pointwise stage (attention);
         // a stack's stage s feeds stage s + 1 through the semaphores of boundary s

@@ -83,9 +83,9 @@ int64_t total_units(const Plan& p) {
 // Elements of one intermediate of a convolution stack.
 int64_t stack_buf_elems(const cusync_chain_desc_t& d) { return (int64_t)d.n * d.h * d.w * d.c; }
 
-// Words of a chain's device state: control words, semaphores, K-split turn counters.
+// Words of a chain's device state: control words and semaphores.
 int64_t state_words(const Plan& p) {
-  return CTRL_WORDS + p.num_flags + p.num_flags_pw + p.split_rows + p.split_rows1;
+  return CTRL_WORDS + p.num_flags + p.num_flags_pw;
 }
 // fp32 elements of the K-split workspace: ksplit - 1 slots of a 128-row accumulator per
 // row block.
@@ -642,7 +642,7 @@ struct cusync_chain {
   Plan plan;
   int device;
   int num_sms;
-  uint32_t* state;       // CTRL_WORDS control words, the semaphores, K-split turn counters
+  uint32_t* state;       // CTRL_WORDS control words and the semaphores
   float* split_ws;       // K-split fp32 workspace, or null
   TraceRec* trace;       // per-tile timeline (CUSYNC_FLAG_TRACE), or null
   Grids grids;
@@ -807,9 +807,7 @@ void fill_static_args(const cusync_chain_desc_t& d, const Plan& p, uint32_t* sta
   A.ctrl = state;
   A.flags = state + CTRL_WORDS;
   A.flags_pw = state + CTRL_WORDS + p.num_flags;
-  A.split_turn = p.split_rows > 0 ? state + CTRL_WORDS + p.num_flags + p.num_flags_pw : nullptr;
   A.split_ws = p.split_rows > 0 ? split_ws : nullptr;
-  A.split_turn1 = p.split_rows1 > 0 ? state + CTRL_WORDS + p.num_flags + p.num_flags_pw + p.split_rows : nullptr;
   A.split_ws1 = p.split_rows1 > 0 ? split_ws + split_ws_floats0(p) : nullptr;
   A.tiles0 = (int32_t)t0;
   A.tiles1 = (int32_t)t1;
@@ -980,6 +978,13 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
     delete ch;
     return CUSYNC_ERR_NOMEM;
   }
+  // every K-split workspace word starts empty (all bits set: the kernel's empty mark)
+  if (ch->split_ws && (e = cudaMemset(ch->split_ws, 0xFF, (size_t)split_ws_floats(p) * sizeof(float))) != cudaSuccess) {
+    cudaFree(ch->split_ws);
+    cudaFree(ch->state);
+    delete ch;
+    return cuda_fail(e, "K-split workspace clear");
+  }
   if (d->flags & CUSYNC_FLAG_TRACE) {
     const size_t n = (size_t)total_units(p);
     if (cudaMalloc(&ch->trace, n * sizeof(TraceRec)) != cudaSuccess ||
@@ -1039,6 +1044,12 @@ cusync_status_t cusync_chain_reset(cusync_chain_t ch, cusync_stream_t stream) {
   const size_t words = (size_t)state_words(ch->plan);
   cudaError_t e = cudaMemsetAsync(ch->state, 0, words * sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "state reset");
+  // a run that stopped early may have left K-split sums unread: mark every word empty
+  if (ch->split_ws) {
+    e = cudaMemsetAsync(ch->split_ws, 0xFF, (size_t)split_ws_floats(ch->plan) * sizeof(float),
+                        reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "K-split workspace reset");
+  }
   ch->need_fill = true;  // a run that stopped early may have left the next set unfilled
   return CUSYNC_OK;
 }

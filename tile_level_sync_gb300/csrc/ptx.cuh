@@ -337,6 +337,21 @@ __device__ __forceinline__ void st_relaxed_gpu_b128(void* p, uint32_t a, uint32_
       : "memory");
 }
 
+// One naturally aligned 16-byte chunk read by a single 128-bit load at device scope.
+__device__ __forceinline__ uint4 ld_relaxed_gpu_b128(const void* p) {
+  uint4 r;
+  asm volatile(
+      "{\n\t.reg .b128 v;\n\t.reg .b64 lo, hi;\n\t"
+      "ld.relaxed.gpu.global.b128 v, [%4];\n\t"
+      "mov.b128 {lo, hi}, v;\n\t"
+      "mov.b64 {%0, %1}, lo;\n\t"
+      "mov.b64 {%2, %3}, hi;\n\t}"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p)
+      : "memory");
+  return r;
+}
+
 __device__ __forceinline__ uint32_t ld_shared_u32(const void* p) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
