@@ -1266,15 +1266,15 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       const bool tma_out = g.a_mode == AMODE_GEMM && !(CHECK && tr.s == args.nst - 2);
       uint8_t* ebuf = epi_stage + (q * 2) * C::kEpiBufBytes;
       const int32_t row_w0 = tr.m * (128 * PAIR) + (int32_t)rank * 128 + q * 32;
-      // K split: the units of a tile other than the last store their fp32 partial sums
-      // in their own workspace slot; the last unit adds the slots in unit order and then
-      // its own sums (the same association for every run and policy), and applies the
-      // epilogue to the total.  The slots mark their own readiness: a word that holds no
-      // sum holds kSplitEmpty, a NaN that a sum never takes (the storing unit writes any
-      // such value as the canonical NaN), so the last unit re-reads a 16-byte word until
-      // it holds a sum, with no counter or fence between the units, and writes
-      // kSplitEmpty back once it has read it ([CUDA-FGS] §4.6.4 sentinel protocol, here
-      // for the partial sums rather than for the intermediate).
+      // K split: unit k of a tile adds the running sum of units 0..k-1 to its fp32 partial
+      // sums; the units other than the last store the result in their workspace slot, and
+      // the last applies the epilogue to the total.  The slots mark their own readiness: a
+      // word that holds no sum holds kSplitEmpty, a NaN that a sum never takes (the storing
+      // unit writes any such value as the canonical NaN), so a unit re-reads a 16-byte
+      // word of its predecessor's slot until it holds a sum, with no counter or fence
+      // between the units, and writes kSplitEmpty back once it has read it ([CUDA-FGS]
+      // §4.6.4 sentinel protocol, here for the partial sums rather than the intermediate).
+      // A unit waits only on the unit before it in the queue, which is already running.
       const bool split = g.ksplit > 1;
       const bool last_unit = !split || tr.ks == g.ksplit - 1;
       float* const split_ws = tr.s == 0 ? args.split_ws : args.split_ws1;
@@ -1287,11 +1287,11 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         const int64_t tile_id = ((int64_t)tr.m * g.n_tiles + tr.c) * PAIR + (int64_t)rank;
         ws_row = reinterpret_cast<uint4*>(split_ws) + tile_id * (g.ksplit - 1) * kSlotF4 + row;
       }
-      const uint64_t split_t0 = (split && last_unit) ? ptx::globaltimer() : 0;
+      const uint64_t split_t0 = (split && tr.ks > 0) ? ptx::globaltimer() : 0;
       bool split_late = false;  // a slot word stayed empty past the timeout (error recorded)
       // The 8 words of one slot at p (stride 128 words): split_issue loads them into v;
       // split_settle re-reads those that still hold kSplitEmpty and then marks the 8
-      // words empty again for the next run.  Two slots are in flight at a time.
+      // words empty again for the next run.
       auto split_issue = [&](uint4 (&v)[8], const uint4* p) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = ptx::ld_relaxed_gpu_b128(p + i * 128);
@@ -1321,45 +1321,32 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
 #pragma unroll
         for (int i = 0; i < 8; ++i) ptx::st_relaxed_gpu_b128(p + i * 128, kSplitEmpty, kSplitEmpty, kSplitEmpty, kSplitEmpty);
       };
-      // 32 accumulator columns from `col` on: a unit that is not the last stores them in
-      // its slot; the last one replaces them by slot 0 + slot 1 + ... + its own.
+      // 32 accumulator columns from `col` on.  The units form a chain: unit k > 0 adds
+      // the running sum of units 0..k-1 from slot k-1 to its own sums (the same
+      // association, ((p0 + p1) + p2) + ..., for every run and policy); a unit that is not
+      // the last stores the result in its slot k.  Each unit reads one slot, chunk by
+      // chunk as its predecessor writes it, so the units' epilogues overlap.
       auto split_add = [&](uint32_t (&x)[32], int col) {
         uint4* w = ws_row + (col / 4) * 128;  // column group col/4 + i is at w + i * 128
+        if (tr.ks > 0) {
+          uint4* prev = w + (tr.ks - 1) * kSlotF4;
+          uint4 a[8];
+          split_issue(a, prev);
+          split_settle(a, prev);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            x[4 * i + 0] = __float_as_uint(__uint_as_float(a[i].x) + __uint_as_float(x[4 * i + 0]));
+            x[4 * i + 1] = __float_as_uint(__uint_as_float(a[i].y) + __uint_as_float(x[4 * i + 1]));
+            x[4 * i + 2] = __float_as_uint(__uint_as_float(a[i].z) + __uint_as_float(x[4 * i + 2]));
+            x[4 * i + 3] = __float_as_uint(__uint_as_float(a[i].w) + __uint_as_float(x[4 * i + 3]));
+          }
+        }
         if (!last_unit) {
           uint4* ws = w + tr.ks * kSlotF4;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             ptx::st_relaxed_gpu_b128(ws + i * 128, split_canon(x[4 * i]), split_canon(x[4 * i + 1]),
                                      split_canon(x[4 * i + 2]), split_canon(x[4 * i + 3]));
-          return;
-        }
-        uint4 a[8];
-        split_issue(a, w);
-        if (g.ksplit > 2) {
-          uint4 b[8];
-          split_issue(b, w + kSlotF4);
-          split_settle(a, w);
-          for (int k = 1;; ++k) {
-            split_settle(b, w + k * kSlotF4);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              a[i].x = __float_as_uint(__uint_as_float(a[i].x) + __uint_as_float(b[i].x));
-              a[i].y = __float_as_uint(__uint_as_float(a[i].y) + __uint_as_float(b[i].y));
-              a[i].z = __float_as_uint(__uint_as_float(a[i].z) + __uint_as_float(b[i].z));
-              a[i].w = __float_as_uint(__uint_as_float(a[i].w) + __uint_as_float(b[i].w));
-            }
-            if (k + 1 >= g.ksplit - 1) break;
-            split_issue(b, w + (k + 1) * kSlotF4);
-          }
-        } else {
-          split_settle(a, w);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          x[4 * i + 0] = __float_as_uint(__uint_as_float(a[i].x) + __uint_as_float(x[4 * i + 0]));
-          x[4 * i + 1] = __float_as_uint(__uint_as_float(a[i].y) + __uint_as_float(x[4 * i + 1]));
-          x[4 * i + 2] = __float_as_uint(__uint_as_float(a[i].z) + __uint_as_float(x[4 * i + 2]));
-          x[4 * i + 3] = __float_as_uint(__uint_as_float(a[i].w) + __uint_as_float(x[4 * i + 3]));
         }
       };
       for (int j = 0; j < nchunks; ++j) {
