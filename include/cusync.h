@@ -135,6 +135,9 @@ typedef enum {
 /* Fault injection for tests; each makes a device wait expire, never a GPU fault. */
 #define CUSYNC_DEBUG_SKIP_POST (1u << 8)     /* the producer never posts tile (0,0) */
 #define CUSYNC_DEBUG_SKIP_INIT (1u << 9)     /* SENTINEL: skip the sentinel fill */
+#define CUSYNC_DEBUG_SKIP_SPLIT (1u << 10)   /* K split: the first unit of producer tile
+                                                (0,0) stores no partial sums, so the next
+                                                unit's bounded read of its slot expires */
 
 typedef struct {
   int32_t kind;     /* cusync_chain_kind_t */

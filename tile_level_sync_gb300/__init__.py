@@ -24,6 +24,7 @@ FLAG_NO_REORDER = 1 << 0
 FLAG_TRACE = 1 << 1
 DEBUG_SKIP_POST = 1 << 8
 DEBUG_SKIP_INIT = 1 << 9
+DEBUG_SKIP_SPLIT = 1 << 10
 
 POLICY_NAMES = {"STREAM": POLICY_STREAM, "ROW": POLICY_ROW, "TILE": POLICY_TILE,
                 "STRIDED": POLICY_STRIDED_TILE, "SENTINEL": POLICY_SENTINEL, "AUTO": POLICY_AUTO}

@@ -71,6 +71,7 @@ enum : uint32_t { ERRC_FLAG_TIMEOUT = 1, ERRC_SENTINEL_TIMEOUT = 2, ERRC_PIPELIN
 // Flag bits shared with cusync.h.
 constexpr uint32_t kFlagNoReorder = 1u << 0;
 constexpr uint32_t kDebugSkipPost = 1u << 8;
+constexpr uint32_t kDebugSkipSplit = 1u << 10;
 // Semaphores read in one round trip when a wait finds its semaphore not yet known ready.
 constexpr int kProbe = 32;
 
@@ -1288,6 +1289,8 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         ws_row = reinterpret_cast<uint4*>(split_ws) + tile_id * (g.ksplit - 1) * kSlotF4 + row;
       }
       const uint64_t split_t0 = (split && tr.ks > 0) ? ptx::globaltimer() : 0;
+      // fault injection: the first unit of producer tile (0, 0) withholds its sums
+      const bool split_skip = (args.flags_bits & kDebugSkipSplit) && tr.s == 0 && tr.ks == 0 && tr.m == 0 && tr.c == 0;
       bool split_late = false;  // a slot word stayed empty past the timeout (error recorded)
       // The 8 words of one slot at p (stride 128 words): split_issue loads them into v;
       // split_settle re-reads those that still hold kSplitEmpty and then marks the 8
@@ -1341,7 +1344,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
             x[4 * i + 3] = __float_as_uint(__uint_as_float(a[i].w) + __uint_as_float(x[4 * i + 3]));
           }
         }
-        if (!last_unit) {
+        if (!last_unit && !split_skip) {
           uint4* ws = w + tr.ks * kSlotF4;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
