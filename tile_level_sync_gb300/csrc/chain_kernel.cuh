@@ -85,6 +85,10 @@ struct StageArgs {
   int32_t a_rows, b_rows;
   StageGeo g;
   int32_t b_half_rows;   // SwiGLU: row offset of the up-projection half of B
+  // Operand maps that are 3-D k-block views [K/64][rows][64] (box {64, rows, KPS}): one
+  // copy brings all of a pipeline stage's k-blocks.  Otherwise the map is 2-D (or the
+  // convolution / stack map) and a stage takes one copy per k-block.
+  int32_t a3d, b3d;
 };
 
 // One tile of a traced run (same layout as cusync_trace_rec_t).
@@ -142,6 +146,13 @@ struct KCfg {
   static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (192 * 1024) / kStageBytes;  // 4, 6 or 8
+  // k-blocks per pipeline stage: where the ring has at least six k-block buffers, two
+  // consecutive k-blocks share a stage and, for GEMM operands, one copy (a 3-D box of two
+  // k-blocks).  Each copy costs the SM a fixed time whatever its size (measured: 380 ns
+  // per k-block with one 16 KB and one 16-32 KB copy, 250-260 ns with one copy of each
+  // operand per two k-blocks), so halving the copies is what lifts the mainloop towards
+  // the L2 port and tensor rates.  The sentinel-checked kernels keep one k-block.
+  __host__ __device__ static constexpr int kps(bool check) { return (!check && kStages >= 6) ? 2 : 1; }
   static constexpr int kTmemCols = 2 * BN;           // two fp32 accumulators of BN columns
   static constexpr int kSlots = 4;                   // tile hand-off ring
   // 7 warps (loader, MMA, 4 epilogue, prefetch), + 2 sentinel checkers under that policy
@@ -436,7 +447,10 @@ __device__ __forceinline__ bool xwait(uint64_t* bar, uint32_t parity, uint64_t t
 template <int BN, int PAIR, bool CHECK>
 __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kernel(const __grid_constant__ ChainArgs args) {
   using C = KCfg<BN, PAIR>;
-  constexpr int S = C::kStages;
+  constexpr int S = C::kStages;          // k-block buffers of the ring
+  constexpr int KPS = C::kps(CHECK);     // k-blocks per stage
+  constexpr int NS = S / KPS;            // stages; stage st holds buffers st*KPS .. st*KPS+KPS-1
+  static_assert(S % KPS == 0, "whole stages");
   constexpr uint32_t FULL = 0xFFFFFFFFu;
   constexpr bool kPair = PAIR == 2;
 
@@ -467,8 +481,12 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
   uint32_t* ready_sink = const_cast<uint32_t*>(run_no + 3);
   uint8_t* epi_stage = smem + S * C::kStageBytes + 1024;  // 1024-byte aligned TMA store boxes
 
-  auto smem_a = [&](int st) { return stage_base + st * C::kStageBytes; };
-  auto smem_b = [&](int st) { return stage_base + st * C::kStageBytes + C::kABytes; };
+  // Stage st holds its k-blocks' A tiles one after the other, then their B tiles (the
+  // layout of a 3-D box of KPS k-blocks); k-block h of the stage is at smem_a(st, h).
+  auto smem_a = [&](int st, int h = 0) { return stage_base + st * KPS * C::kStageBytes + h * C::kABytes; };
+  auto smem_b = [&](int st, int h = 0) {
+    return stage_base + st * KPS * C::kStageBytes + KPS * C::kABytes + h * C::kBBytes;
+  };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -562,7 +580,8 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       const uint64_t pol_a = ptx::l2_policy_evict_last();
       const uint64_t pol_b = ptx::l2_policy_evict_normal();
       const bool reorder = !(args.flags_bits & kFlagNoReorder);
-      uint32_t it = 0, tcount = 0, pw_seen = 0;
+      uint32_t it = 0, tcount = 0, pw_seen = 0;  // it: stages armed (every tile starts a stage)
+      uint32_t kit = 0;                           // k-blocks loaded, for the prefetch warp
       bool ok = true;
       while (true) {
         const int slot = tcount % C::kSlots;
@@ -608,7 +627,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         const StageArgs& SA = stage_args(args, tr.s);
         const int32_t KB = tr.nkb;            // k-blocks of this work unit
         const int32_t kx0 = tr.kb0 * kBK;     // its first reduction coordinate
-        const uint32_t tx = a_tile_bytes(SA.g) + (uint32_t)C::kBBytes;
+        const uint32_t abytes = a_tile_bytes(SA.g);
         TraceRec* trec = (args.trace && leader) ? args.trace + chain_tile(args, tr.q) : nullptr;
         if (trec) {
           trec->tile = (uint32_t)chain_tile(args, tr.q);
@@ -639,7 +658,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         gdt.reset();
         ConvDepTracker cdt;  // touched (stack arrays) only by convolution tiles
         if (SA.g.a_mode != AMODE_GEMM) cdt.reset();
-        int32_t bnext = 0;   // next k-block whose stage slot is armed and whose B load is issued
+        int32_t snext = 0;   // next stage of this tile to arm (its slot drained, its B copies issued)
         // Per-tile invariants of the k-loop, so that the single loader thread spends as few
         // instructions per k-block as possible (its latency is on the critical path).
         const bool gemm = SA.g.a_mode == AMODE_GEMM;
@@ -650,7 +669,13 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         const int32_t brow1 = (PAIR == 1 && SA.g.epi == EPI_SWIGLU) ? b_row<BN, PAIR>(SA, tr, rank, 1) : -1;
         const bool direct = direct_tile(tr);
         const bool to_leader = direct && !leader;
-        const uint32_t txs = direct ? 2 * tx : tx;
+        const int32_t NSK = (KB + KPS - 1) / KPS;  // stages of this work unit
+        // bytes a stage of nk k-blocks brings into this CTA: a 3-D box always brings KPS
+        // k-blocks (past the unit's or the tensor's end: unused, or zero-filled)
+        auto stage_bytes = [&](int32_t nk) -> uint32_t {
+          const uint32_t b = (uint32_t)(SA.a3d ? KPS : nk) * abytes + (uint32_t)(SA.b3d ? KPS : nk) * (uint32_t)C::kBBytes;
+          return direct ? 2u * b : b;  // a direct pair tile: the leader's barrier counts both CTAs
+        };
         // a tile that the checker warp validates completes its copies on cfull, which only
         // the checker waits on; every other tile on full, which only the MMA issuer waits on
         const bool checked = CHECK && cons;
@@ -686,28 +711,38 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           cv_img = tr.m / SA.g.tpi;
           cv_h0 = (tr.m % SA.g.tpi) * SA.g.th - 1;
         }
-        // Arm the stage slot of k-block kbb and issue its weight (B) load.  Blocking waits
-        // for the slot to drain; non-blocking returns 0 if it has not drained yet.
-        auto arm_b = [&](int32_t kbb, bool blocking) -> int {
-          const uint32_t j = it + (uint32_t)kbb;
-          const int st = (int)(j % S);
-          const uint32_t par = ((j / S) & 1u) ^ 1u;
+        // Arm stage sj of the tile: wait for its slot to drain (blocking) or return 0 if it
+        // has not (non-blocking), set the bytes its barrier expects and issue its weight (B)
+        // copies -- one 3-D box of KPS k-blocks, or one copy per k-block.
+        auto arm_b = [&](int32_t sj, bool blocking) -> int {
+          const uint32_t j = it + (uint32_t)sj;
+          const int st = (int)(j % NS);
+          const uint32_t par = ((j / NS) & 1u) ^ 1u;
           if (blocking) {
             if (!ptx::mbar_wait_bounded(&empty[st], par, pto) || *abort_flag) return -1;
           } else if (!ptx::mbar_test_wait(&empty[st], par)) {
             return 0;
           }
-          uint8_t* dst = smem_b(st);
           stage_kind[st] = checked ? 1 : 0;
-          if (stacked) {
-            ptx::mbar_arrive_expect_tx(&lbar[st], txs);
-            ptx::tma_load_3d(dst, tmB, &lbar[st], kx0 + kbb * kBK, brow0, tr.s, pol_b);
-          } else if (to_leader) {
-            ptx::tma_load_2d_to_leader(dst, tmB, ptx::mapa(&full[st], 0), kx0 + kbb * kBK, brow0, pol_b);
-          } else {
-            ptx::mbar_arrive_expect_tx(&lbar[st], txs);
-            ptx::tma_load_2d(dst, tmB, &lbar[st], kx0 + kbb * kBK, brow0, pol_b);
-            if (brow1 >= 0) ptx::tma_load_2d(dst + (BN / 2) * 128, tmB, &lbar[st], kx0 + kbb * kBK, brow1, pol_b);
+          const int32_t kb = sj * KPS;
+          const int32_t nk = min(KPS, KB - kb);
+          if (!to_leader) ptx::mbar_arrive_expect_tx(&lbar[st], stage_bytes(nk));
+          if (SA.b3d) {
+            if (to_leader) ptx::tma_load_3d_to_leader(smem_b(st), tmB, ptx::mapa(&full[st], 0), 0, brow0, tr.kb0 + kb, pol_b);
+            else ptx::tma_load_3d(smem_b(st), tmB, &lbar[st], 0, brow0, tr.kb0 + kb, pol_b);
+            return 1;
+          }
+          for (int32_t h = 0; h < nk; ++h) {
+            uint8_t* dst = smem_b(st, h);
+            const int32_t x = kx0 + (kb + h) * kBK;
+            if (stacked) {
+              ptx::tma_load_3d(dst, tmB, &lbar[st], x, brow0, tr.s, pol_b);
+            } else if (to_leader) {
+              ptx::tma_load_2d_to_leader(dst, tmB, ptx::mapa(&full[st], 0), x, brow0, pol_b);
+            } else {
+              ptx::tma_load_2d(dst, tmB, &lbar[st], x, brow0, pol_b);
+              if (brow1 >= 0) ptx::tma_load_2d(dst + (BN / 2) * 128, tmB, &lbar[st], x, brow1, pol_b);
+            }
           }
           return 1;
         };
@@ -748,8 +783,8 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
             const uint64_t t0 = ptx::globaltimer();
             uint32_t iter = 0, backoff = 64;
             while (true) {
-              if (reorder && bnext < min(KB, kb + S) && arm_b(bnext, false) > 0) {
-                ++bnext;
+              if (reorder && snext < min(NSK, kb / KPS + NS) && arm_b(snext, false) > 0) {
+                ++snext;
               } else {
                 __nanosleep(backoff);
                 if (backoff < 256) backoff <<= 1;
@@ -773,62 +808,89 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
             ptx::fence_proxy_async_global();
           }
         };
-        // The GEMM and convolution k-loops are kept apart: the single loader thread's
-        // instruction latency per k-block is on the critical path of the GEMM mainloop.
+        // The loops visit the unit's stages.  Before a stage's A copies, the waits of each
+        // of its k-blocks that can need a semaphore (the B copies go first: cuSync §V).  The
+        // GEMM and convolution loops are kept apart: the single loader thread's instruction
+        // latency per stage is on the critical path of the mainloop.
         if (gemm) {
-          for (int32_t kb = 0; kb < KB; ++kb) {
-            // every dep_every-th k-block of the unit (unit_dep_kblock); one more term in this
-            // test measured 9-12% slower: the loader thread's latency per k-block is the
-            // mainloop's critical path
-            const bool dep_kb = dep_every > 0 && (kb % dep_every) == 0;
-            if (dep_kb && !reorder) wait_deps(kb);
-            if (bnext == kb) {
-              if (arm_b(kb, true) < 0) {
+          for (int32_t sj = 0; sj < NSK; ++sj) {
+            const int32_t kb = sj * KPS;
+            const int32_t nk = min(KPS, KB - kb);
+            // every dep_every-th k-block of the unit (unit_dep_kblock)
+            bool dep_st = false;
+#pragma unroll
+            for (int h = 0; h < KPS; ++h) dep_st |= h < nk && dep_every > 0 && ((kb + h) % dep_every) == 0;
+            if (dep_st && !reorder)
+              for (int h = 0; h < nk; ++h)
+                if (dep_every > 0 && ((kb + h) % dep_every) == 0) wait_deps(kb + h);
+            if (snext == sj) {
+              if (arm_b(sj, true) < 0) {
                 record_error(args, ERRC_PIPELINE, t, 2);
                 *abort_flag = 1;
                 ok = false;
                 break;
               }
-              ++bnext;
+              ++snext;
             }
-            if (dep_kb && reorder) wait_deps(kb);
+            if (dep_st && reorder)
+              for (int h = 0; h < nk; ++h)
+                if (dep_every > 0 && ((kb + h) % dep_every) == 0) wait_deps(kb + h);
             if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
-            const int st = (int)((it + (uint32_t)kb) % S);
-            if (to_leader) ptx::tma_load_2d_to_leader(smem_a(st), tmA, ptx::mapa(&full[st], 0), kx0 + kb * kBK, a_row, pol_a);
-            else ptx::tma_load_2d(smem_a(st), tmA, &lbar[st], kx0 + kb * kBK, a_row, pol_a);
-            *progress = it + (uint32_t)kb + 1u;
+            const int st = (int)((it + (uint32_t)sj) % NS);
+            if (SA.a3d) {
+              if (to_leader) ptx::tma_load_3d_to_leader(smem_a(st), tmA, ptx::mapa(&full[st], 0), 0, a_row, tr.kb0 + kb, pol_a);
+              else ptx::tma_load_3d(smem_a(st), tmA, &lbar[st], 0, a_row, tr.kb0 + kb, pol_a);
+            } else {
+              for (int32_t h = 0; h < nk; ++h) {
+                if (to_leader)
+                  ptx::tma_load_2d_to_leader(smem_a(st, h), tmA, ptx::mapa(&full[st], 0), kx0 + (kb + h) * kBK, a_row, pol_a);
+                else
+                  ptx::tma_load_2d(smem_a(st, h), tmA, &lbar[st], kx0 + (kb + h) * kBK, a_row, pol_a);
+              }
+            }
+            *progress = kit + (uint32_t)(kb + nk);
           }
         } else {
-          for (int32_t kb = 0; kb < KB; ++kb) {
-            const bool dep_kb = kb < 64 ? ((dep_mask >> kb) & 1ull) != 0 : dep_every > 0;
-            if (dep_kb && !reorder) wait_deps(kb);
-            if (bnext == kb) {
-              if (arm_b(kb, true) < 0) {
+          for (int32_t sj = 0; sj < NSK; ++sj) {
+            const int32_t kb = sj * KPS;
+            const int32_t nk = min(KPS, KB - kb);
+            bool dep_st = false;
+            for (int h = 0; h < nk; ++h) dep_st |= (kb + h) < 64 ? ((dep_mask >> (kb + h)) & 1ull) != 0 : dep_every > 0;
+            auto deps_of_stage = [&]() {
+              for (int h = 0; h < nk; ++h)
+                if ((kb + h) < 64 ? ((dep_mask >> (kb + h)) & 1ull) != 0 : dep_every > 0) wait_deps(kb + h);
+            };
+            if (dep_st && !reorder) deps_of_stage();
+            if (snext == sj) {
+              if (arm_b(sj, true) < 0) {
                 record_error(args, ERRC_PIPELINE, t, 2);
                 *abort_flag = 1;
                 ok = false;
                 break;
               }
-              ++bnext;
+              ++snext;
             }
-            if (dep_kb && reorder) wait_deps(kb);
+            if (dep_st && reorder) deps_of_stage();
             if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
-            const int st = (int)((it + (uint32_t)kb) % S);
-            if (a_buf >= 0)
-              ptx::tma_load_5d(smem_a(st), tmA, &lbar[st], cv_cb * kBK, cv_s - 1, cv_h0 + cv_r, cv_img, a_buf, pol_a);
-            else
-              ptx::tma_load_4d(smem_a(st), tmA, &lbar[st], cv_cb * kBK, cv_s - 1, cv_h0 + cv_r, cv_img, pol_a);
-            if (++cv_cb == SA.g.cblocks) {
-              cv_cb = 0;
-              if (++cv_s == 3) {
-                cv_s = 0;
-                ++cv_r;
+            const int st = (int)((it + (uint32_t)sj) % NS);
+            for (int32_t h = 0; h < nk; ++h) {
+              if (a_buf >= 0)
+                ptx::tma_load_5d(smem_a(st, h), tmA, &lbar[st], cv_cb * kBK, cv_s - 1, cv_h0 + cv_r, cv_img, a_buf, pol_a);
+              else
+                ptx::tma_load_4d(smem_a(st, h), tmA, &lbar[st], cv_cb * kBK, cv_s - 1, cv_h0 + cv_r, cv_img, pol_a);
+              if (++cv_cb == SA.g.cblocks) {
+                cv_cb = 0;
+                if (++cv_s == 3) {
+                  cv_s = 0;
+                  ++cv_r;
+                }
               }
             }
-            *progress = it + (uint32_t)kb + 1u;
+            *progress = kit + (uint32_t)(kb + nk);
           }
         }
-        it += (uint32_t)bnext;
+        it += (uint32_t)snext;
+        kit += (uint32_t)KB;
         *it_issued = (int32_t)it;
         if (!ok && leader) {
           // hand a terminator to the other roles so that they stop
@@ -898,12 +960,12 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       // The peer of a pair issues nothing: its direct copies complete on the leader's
       // `full`, and its checker arrives on the leader's `ready`.
       if (!leader) {
-        it += (uint32_t)tr.nkb;
+        it += (uint32_t)((tr.nkb + KPS - 1) / KPS);
         continue;
       }
       uint32_t land_clk = 0;  // traced runs: SM cycles spent waiting for stages
-      for (int32_t kb = 0; kb < tr.nkb; ++kb, ++it) {
-        const int st = (int)(it % S);
+      for (int32_t kb = 0; kb < tr.nkb; kb += KPS, ++it) {
+        const int st = (int)(it % NS);
         const uint32_t c0 = args.trace ? (uint32_t)clock64() : 0u;
         bool landed;
         if (checked) {
@@ -922,16 +984,22 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         ptx::tc_fence_after();
         if (lane == 0 && kb == 0 && args.trace) args.trace[chain_tile(args, tr.q)].t_mma0 = ptx::globaltimer();
         if (lane == 0) {
-          const uint32_t a0 = ptx::smem_u32(smem_a(st));
-          const uint32_t b0 = ptx::smem_u32(smem_b(st));
+          // the stage's k-blocks (the unit's last stage may hold fewer than KPS); the k-th
+          // 16-wide slice of a 128-byte swizzled row starts 32 bytes further (+2 in the
+          // descriptors' address field)
+          const int nk = min(KPS, tr.nkb - kb);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            if (kPair)
-              ptx::umma_bf16_pair(d_tmem, ptx::smem_desc_k128(a0 + 32u * k), ptx::smem_desc_k128(b0 + 32u * k),
-                                  idesc, (kb | k) != 0 ? 1u : 0u);
-            else
-              ptx::umma_bf16(d_tmem, ptx::smem_desc_k128(a0 + 32u * k), ptx::smem_desc_k128(b0 + 32u * k), idesc,
-                             (kb | k) != 0 ? 1u : 0u);
+          for (int h = 0; h < KPS; ++h) {
+            if (h < nk) {
+              const uint64_t da = ptx::smem_desc_k128(ptx::smem_u32(smem_a(st, h)));
+              const uint64_t db = ptx::smem_desc_k128(ptx::smem_u32(smem_b(st, h)));
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k) {
+                const uint32_t accum = (kb + h + k) != 0 ? 1u : 0u;
+                if (kPair) ptx::umma_bf16_pair(d_tmem, da + 2u * k, db + 2u * k, idesc, accum);
+                else ptx::umma_bf16(d_tmem, da + 2u * k, db + 2u * k, idesc, accum);
+              }
+            }
           }
           if (kPair) ptx::umma_commit_pair_multicast(&empty[st], 0x3);
           else ptx::umma_commit(&empty[st]);
@@ -965,8 +1033,8 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
     // consumed (the checker drains `cfull`).
     if (lane == 0 && !ok && leader) {
       const uint32_t issued = (uint32_t)*it_issued;
-      for (uint32_t j = it; j < issued && j < it + S; ++j) {
-        const int st = (int)(j % S);
+      for (uint32_t j = it; j < issued && j < it + NS; ++j) {
+        const int st = (int)(j % NS);
         if (stage_kind[st] != 0) continue;
         ptx::mbar_wait_bounded(&full[st], (fpar >> st) & 1u, pto);
         fpar ^= 1u << st;
@@ -981,6 +1049,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
     // count is even, so a stage always belongs to the same warp and each warp's barrier
     // phases are its own).
     static_assert(S % 2 == 0, "the checkers split the stages by parity");
+    static_assert(!CHECK || KPS == 1, "checked kernels load one k-block per stage");
     const int ck = warp - 7;
     if constexpr (CHECK) {
       const uint64_t pol_a = ptx::l2_policy_evict_last();

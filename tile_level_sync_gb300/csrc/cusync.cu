@@ -466,6 +466,27 @@ bool encode_3d(CUtensorMap* m, const void* ptr, uint64_t depth, uint64_t rows, u
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D row-major bf16 [rows, cols] seen as 3-D [cols/64][rows][64] (cols a multiple of 64):
+// a {64, box_rows, kps} box brings kps consecutive 64-column k-blocks of box_rows rows,
+// laid out in shared memory one k-block after the other, each as a 2-D box would be.
+bool encode_kview(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t kps) {
+  cuuint64_t dims[3] = {(cuuint64_t)kBK, rows, cols / kBK};
+  cuuint64_t strides[2] = {cols * 2, (cuuint64_t)kBK * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kBK, box_rows, kps};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// A GEMM operand's map: the k-block view when the kernel's stages hold two k-blocks and
+// the reduction length is a whole number of k-blocks (*kview = 1), else the 2-D map.
+bool encode_operand(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows, int32_t kps,
+                    int32_t* kview) {
+  *kview = (kps > 1 && cols % kBK == 0) ? 1 : 0;
+  return *kview ? encode_kview(m, ptr, rows, cols, box_rows, (uint32_t)kps) : encode_2d(m, ptr, rows, cols, box_rows);
+}
+
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 template <int BN, int PAIR, bool CHECK>
@@ -733,10 +754,20 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
   return CUSYNC_OK;
 }
 
-// TMA descriptors of a run: 2-D maps for GEMM operands, 4-D NHWC maps for conv images.
+// k-blocks per pipeline stage of the kernel that runs plan p (the sentinel policy runs the
+// checked instantiation).
+int32_t kernel_kps(const Plan& p, bool check) {
+  if (p.pair == 2) return p.bn == 256 ? KCfg<256, 2>::kps(check) : KCfg<128, 2>::kps(check);
+  return p.bn == 256 ? KCfg<256, 1>::kps(check) : KCfg<128, 1>::kps(check);
+}
+
+// TMA descriptors of a run: k-block views or 2-D maps for GEMM operands (encode_operand),
+// 4-D NHWC maps for conv images.
 bool encode_maps(const cusync_chain_desc_t& d, const Plan& p, ChainArgs& A, const void* a0, const void* b0,
                  const void* b1, const void* h, const void* y, const void* h2 = nullptr) {
   bool ok = true;
+  const int32_t kps = kernel_kps(p, d.policy == CUSYNC_POLICY_SENTINEL);
+  for (int s = 0; s < 3; ++s) A.st[s].a3d = A.st[s].b3d = 0;
   if (d.kind == CUSYNC_CHAIN_ATTENTION) {
     // stage 0: XQKV = X x QKV; stage 1 reads XQKV and writes XDot (no maps);
     // stage 2: Y = XDot x W2
@@ -752,11 +783,11 @@ bool encode_maps(const cusync_chain_desc_t& d, const Plan& p, ChainArgs& A, cons
     A.st[2].b_ptr = static_cast<const uint16_t*>(b1);
     A.st[2].b_rows = (int32_t)d.N2;
     ok &= h2 != nullptr;
-    ok &= encode_2d(&A.st[0].tmA, a0, (uint64_t)d.M, (uint64_t)d.K, 128u);
-    ok &= encode_2d(&A.st[0].tmB, b0, n3, (uint64_t)d.K, b_box_rows(p, false));
+    ok &= encode_operand(&A.st[0].tmA, a0, (uint64_t)d.M, (uint64_t)d.K, 128u, kps, &A.st[0].a3d);
+    ok &= encode_operand(&A.st[0].tmB, b0, n3, (uint64_t)d.K, b_box_rows(p, false), kps, &A.st[0].b3d);
     ok &= encode_2d(&A.st[0].tmO, h, (uint64_t)d.M, n3, 32u);
-    ok &= encode_2d(&A.st[2].tmA, h2, (uint64_t)d.M, (uint64_t)d.N1, 128u);
-    ok &= encode_2d(&A.st[2].tmB, b1, (uint64_t)d.N2, (uint64_t)d.N1, b_box_rows(p, false));
+    ok &= encode_operand(&A.st[2].tmA, h2, (uint64_t)d.M, (uint64_t)d.N1, 128u, kps, &A.st[2].a3d);
+    ok &= encode_operand(&A.st[2].tmB, b1, (uint64_t)d.N2, (uint64_t)d.N1, b_box_rows(p, false), kps, &A.st[2].b3d);
     ok &= encode_2d(&A.st[2].tmO, y, (uint64_t)d.M, (uint64_t)d.N2, 32u);
   } else if (d.kind == CUSYNC_CHAIN_CONV_STACK) {
     // stage 0 reads x, every later stage one of the workspace's buffers; all stages take
@@ -769,9 +800,10 @@ bool encode_maps(const cusync_chain_desc_t& d, const Plan& p, ChainArgs& A, cons
   } else if (d.kind == CUSYNC_CHAIN_CONV_RELU) {
     const StageGeo& g0 = p.geo[0];
     ok &= encode_nhwc(&A.st[0].tmA, a0, d.n, d.h, d.w, d.c, (uint32_t)g0.th);
-    ok &= encode_2d(&A.st[0].tmB, b0, (uint64_t)d.k_out, (uint64_t)9 * d.c, b_box_rows(p, false));
+    ok &= encode_operand(&A.st[0].tmB, b0, (uint64_t)d.k_out, (uint64_t)9 * d.c, b_box_rows(p, false), kps, &A.st[0].b3d);
     ok &= encode_nhwc(&A.st[1].tmA, h, d.n, d.h, d.w, d.k_out, (uint32_t)g0.th);
-    ok &= encode_2d(&A.st[1].tmB, b1, (uint64_t)d.k_out, (uint64_t)9 * d.k_out, b_box_rows(p, false));
+    ok &= encode_operand(&A.st[1].tmB, b1, (uint64_t)d.k_out, (uint64_t)9 * d.k_out, b_box_rows(p, false), kps,
+                         &A.st[1].b3d);
   } else {
     const bool swiglu = d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
     A.st[0].a_ptr = static_cast<const uint16_t*>(a0);
@@ -782,10 +814,13 @@ bool encode_maps(const cusync_chain_desc_t& d, const Plan& p, ChainArgs& A, cons
     A.st[1].a_rows = (int32_t)d.M;
     A.st[1].b_ptr = static_cast<const uint16_t*>(b1);
     A.st[1].b_rows = (int32_t)d.N2;
-    ok &= encode_2d(&A.st[0].tmA, a0, (uint64_t)d.M, (uint64_t)d.K, 128u);
-    ok &= encode_2d(&A.st[0].tmB, b0, (uint64_t)(swiglu ? 2 * d.N1 : d.N1), (uint64_t)d.K, b_box_rows(p, swiglu));
-    ok &= encode_2d(&A.st[1].tmA, h, (uint64_t)d.M, (uint64_t)d.N1, 128u);
-    ok &= encode_2d(&A.st[1].tmB, b1, (uint64_t)d.N2, (uint64_t)d.N1, b_box_rows(p, false));
+    ok &= encode_operand(&A.st[0].tmA, a0, (uint64_t)d.M, (uint64_t)d.K, 128u, kps, &A.st[0].a3d);
+    // a single CTA of a SwiGLU chain copies the gate and up halves of its weight tile
+    // separately for every k-block (the 2-D map)
+    ok &= encode_operand(&A.st[0].tmB, b0, (uint64_t)(swiglu ? 2 * d.N1 : d.N1), (uint64_t)d.K, b_box_rows(p, swiglu),
+                         (swiglu && p.pair == 1) ? 1 : kps, &A.st[0].b3d);
+    ok &= encode_operand(&A.st[1].tmA, h, (uint64_t)d.M, (uint64_t)d.N1, 128u, kps, &A.st[1].a3d);
+    ok &= encode_operand(&A.st[1].tmB, b1, (uint64_t)d.N2, (uint64_t)d.N1, b_box_rows(p, false), kps, &A.st[1].b3d);
     ok &= encode_2d(&A.st[0].tmO, h, (uint64_t)d.M, (uint64_t)d.N1, 32u);
     ok &= encode_2d(&A.st[1].tmO, y, (uint64_t)d.M, (uint64_t)d.N2, 32u);
   }

@@ -417,6 +417,16 @@ __device__ __forceinline__ void tma_load_2d_to_leader(void* dst, const CUtensorM
       : "memory");
 }
 
+// The same for a 3-D box (several consecutive k-blocks of a [k-blocks][rows][64] view).
+__device__ __forceinline__ void tma_load_3d_to_leader(void* dst, const CUtensorMap* m, uint32_t leader_bar, int32_t c0,
+                                                      int32_t c1, int32_t c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(leader_bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
 // Pair (cta_group::2) forms of the TMEM and MMA instructions.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
