@@ -146,13 +146,16 @@ struct KCfg {
   static constexpr int kBBytes = kBRows * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (192 * 1024) / kStageBytes;  // 4, 6 or 8
-  // k-blocks per pipeline stage: where the ring has at least six k-block buffers, two
-  // consecutive k-blocks share a stage and, for GEMM operands, one copy (a 3-D box of two
-  // k-blocks).  Each copy costs the SM a fixed time whatever its size (measured: 380 ns
-  // per k-block with one 16 KB and one 16-32 KB copy, 250-260 ns with one copy of each
-  // operand per two k-blocks), so halving the copies is what lifts the mainloop towards
-  // the L2 port and tensor rates.  The sentinel-checked kernels keep one k-block.
-  __host__ __device__ static constexpr int kps(bool check) { return (!check && kStages >= 6) ? 2 : 1; }
+  // k-blocks per pipeline stage: in a CTA pair two consecutive k-blocks share a stage and,
+  // for GEMM operands, one copy (a 3-D box of two k-blocks).  Each copy costs the SM a
+  // fixed time whatever its size (measured on a minimal copy->MMA pipeline of CTA pairs
+  // with operands in L2: 417 ns per k-block with one copy per operand and k-block, 262 ns
+  // with one per two k-blocks), so halving the copies lifts the mainloop towards the L2
+  // port and tensor rates.  A single CTA keeps one k-block per stage: its stages of two
+  // k-blocks measured 5-10% slower on the attention and convolution chains (a drained
+  // stage is refilled only once both of its k-blocks are consumed, which leaves fewer
+  // bytes in flight), as do the sentinel-checked kernels.
+  __host__ __device__ static constexpr int kps(bool check) { return (!check && PAIR == 2 && kStages >= 6) ? 2 : 1; }
   static constexpr int kTmemCols = 2 * BN;           // two fp32 accumulators of BN columns
   static constexpr int kSlots = 4;                   // tile hand-off ring
   // 7 warps (loader, MMA, 4 epilogue, prefetch), + 2 sentinel checkers under that policy
@@ -672,10 +675,12 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         const int32_t NSK = (KB + KPS - 1) / KPS;  // stages of this work unit
         // bytes a stage of nk k-blocks brings into this CTA: a 3-D box always brings KPS
         // k-blocks (past the unit's or the tensor's end: unused, or zero-filled)
+        const bool a3d = SA.a3d != 0, b3d = SA.b3d != 0;
         auto stage_bytes = [&](int32_t nk) -> uint32_t {
-          const uint32_t b = (uint32_t)(SA.a3d ? KPS : nk) * abytes + (uint32_t)(SA.b3d ? KPS : nk) * (uint32_t)C::kBBytes;
+          const uint32_t b = (uint32_t)(a3d ? KPS : nk) * abytes + (uint32_t)(b3d ? KPS : nk) * (uint32_t)C::kBBytes;
           return direct ? 2u * b : b;  // a direct pair tile: the leader's barrier counts both CTAs
         };
+        const uint32_t tx_full = stage_bytes(KPS);  // a whole stage (every stage when KPS = 1)
         // a tile that the checker warp validates completes its copies on cfull, which only
         // the checker waits on; every other tile on full, which only the MMA issuer waits on
         const bool checked = CHECK && cons;
@@ -725,14 +730,16 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           }
           stage_kind[st] = checked ? 1 : 0;
           const int32_t kb = sj * KPS;
-          const int32_t nk = min(KPS, KB - kb);
-          if (!to_leader) ptx::mbar_arrive_expect_tx(&lbar[st], stage_bytes(nk));
-          if (SA.b3d) {
+          const int32_t nk = KPS == 1 ? 1 : min(KPS, KB - kb);
+          if (!to_leader) ptx::mbar_arrive_expect_tx(&lbar[st], (KPS == 1 || nk == KPS) ? tx_full : stage_bytes(nk));
+          if (KPS > 1 && b3d) {
             if (to_leader) ptx::tma_load_3d_to_leader(smem_b(st), tmB, ptx::mapa(&full[st], 0), 0, brow0, tr.kb0 + kb, pol_b);
             else ptx::tma_load_3d(smem_b(st), tmB, &lbar[st], 0, brow0, tr.kb0 + kb, pol_b);
             return 1;
           }
-          for (int32_t h = 0; h < nk; ++h) {
+#pragma unroll
+          for (int32_t h = 0; h < KPS; ++h) {
+            if (h >= nk) break;
             uint8_t* dst = smem_b(st, h);
             const int32_t x = kx0 + (kb + h) * kBK;
             if (stacked) {
@@ -815,11 +822,12 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         if (gemm) {
           for (int32_t sj = 0; sj < NSK; ++sj) {
             const int32_t kb = sj * KPS;
-            const int32_t nk = min(KPS, KB - kb);
-            // every dep_every-th k-block of the unit (unit_dep_kblock)
-            bool dep_st = false;
-#pragma unroll
-            for (int h = 0; h < KPS; ++h) dep_st |= h < nk && dep_every > 0 && ((kb + h) % dep_every) == 0;
+            const int32_t nk = KPS == 1 ? 1 : min(KPS, KB - kb);
+            // every dep_every-th k-block of the unit (unit_dep_kblock); the loader thread's
+            // instructions per stage are on the mainloop's critical path (one more term in
+            // this test measured 9-12% slower with one k-block per stage)
+            bool dep_st = dep_every > 0 && (kb % dep_every) == 0;
+            if (KPS > 1 && nk > 1) dep_st |= dep_every > 0 && ((kb + 1) % dep_every) == 0;
             if (dep_st && !reorder)
               for (int h = 0; h < nk; ++h)
                 if (dep_every > 0 && ((kb + h) % dep_every) == 0) wait_deps(kb + h);
@@ -837,11 +845,13 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
                 if (dep_every > 0 && ((kb + h) % dep_every) == 0) wait_deps(kb + h);
             if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
             const int st = (int)((it + (uint32_t)sj) % NS);
-            if (SA.a3d) {
+            if (KPS > 1 && a3d) {
               if (to_leader) ptx::tma_load_3d_to_leader(smem_a(st), tmA, ptx::mapa(&full[st], 0), 0, a_row, tr.kb0 + kb, pol_a);
               else ptx::tma_load_3d(smem_a(st), tmA, &lbar[st], 0, a_row, tr.kb0 + kb, pol_a);
             } else {
-              for (int32_t h = 0; h < nk; ++h) {
+#pragma unroll
+              for (int32_t h = 0; h < KPS; ++h) {
+                if (h >= nk) break;
                 if (to_leader)
                   ptx::tma_load_2d_to_leader(smem_a(st, h), tmA, ptx::mapa(&full[st], 0), kx0 + (kb + h) * kBK, a_row, pol_a);
                 else
@@ -853,9 +863,11 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         } else {
           for (int32_t sj = 0; sj < NSK; ++sj) {
             const int32_t kb = sj * KPS;
-            const int32_t nk = min(KPS, KB - kb);
+            const int32_t nk = KPS == 1 ? 1 : min(KPS, KB - kb);
             bool dep_st = false;
-            for (int h = 0; h < nk; ++h) dep_st |= (kb + h) < 64 ? ((dep_mask >> (kb + h)) & 1ull) != 0 : dep_every > 0;
+#pragma unroll
+            for (int h = 0; h < KPS; ++h)
+              if (h < nk) dep_st |= (kb + h) < 64 ? ((dep_mask >> (kb + h)) & 1ull) != 0 : dep_every > 0;
             auto deps_of_stage = [&]() {
               for (int h = 0; h < nk; ++h)
                 if ((kb + h) < 64 ? ((dep_mask >> (kb + h)) & 1ull) != 0 : dep_every > 0) wait_deps(kb + h);
@@ -873,7 +885,9 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
             if (dep_st && reorder) deps_of_stage();
             if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
             const int st = (int)((it + (uint32_t)sj) % NS);
-            for (int32_t h = 0; h < nk; ++h) {
+#pragma unroll
+            for (int32_t h = 0; h < KPS; ++h) {
+              if (h >= nk) break;
               if (a_buf >= 0)
                 ptx::tma_load_5d(smem_a(st, h), tmA, &lbar[st], cv_cb * kBK, cv_s - 1, cv_h0 + cv_r, cv_img, a_buf, pol_a);
               else
