@@ -724,7 +724,8 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           const int st = (int)(j % NS);
           const uint32_t par = ((j / NS) & 1u) ^ 1u;
           if (blocking) {
-            if (!ptx::mbar_wait_bounded(&empty[st], par, pto) || *abort_flag) return -1;
+            const int32_t aborted = *abort_flag;  // read before the wait: off the critical path
+            if (!ptx::mbar_wait_bounded(&empty[st], par, pto) || aborted) return -1;
           } else if (!ptx::mbar_test_wait(&empty[st], par)) {
             return 0;
           }
@@ -820,17 +821,22 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         // GEMM and convolution loops are kept apart: the single loader thread's instruction
         // latency per stage is on the critical path of the mainloop.
         if (gemm) {
+          // the next k-block of the unit that consults the tracker: every dep_every-th
+          // (unit_dep_kblock), kept as a running index because the loader thread's
+          // instructions per stage are on the mainloop's critical path (one more term in
+          // the test measured 9-12% slower with one k-block per stage)
+          int32_t dep_next = dep_every > 0 ? 0 : 0x7FFFFFFF;
           for (int32_t sj = 0; sj < NSK; ++sj) {
             const int32_t kb = sj * KPS;
             const int32_t nk = KPS == 1 ? 1 : min(KPS, KB - kb);
-            // every dep_every-th k-block of the unit (unit_dep_kblock); the loader thread's
-            // instructions per stage are on the mainloop's critical path (one more term in
-            // this test measured 9-12% slower with one k-block per stage)
-            bool dep_st = dep_every > 0 && (kb % dep_every) == 0;
-            if (KPS > 1 && nk > 1) dep_st |= dep_every > 0 && ((kb + 1) % dep_every) == 0;
-            if (dep_st && !reorder)
-              for (int h = 0; h < nk; ++h)
-                if (dep_every > 0 && ((kb + h) % dep_every) == 0) wait_deps(kb + h);
+            const bool dep_st = dep_next < kb + nk;
+            auto deps_of_stage = [&]() {
+              while (dep_next < kb + nk) {
+                wait_deps(dep_next);
+                dep_next += dep_every;
+              }
+            };
+            if (dep_st && !reorder) deps_of_stage();
             if (snext == sj) {
               if (arm_b(sj, true) < 0) {
                 record_error(args, ERRC_PIPELINE, t, 2);
@@ -840,9 +846,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
               }
               ++snext;
             }
-            if (dep_st && reorder)
-              for (int h = 0; h < nk; ++h)
-                if (dep_every > 0 && ((kb + h) % dep_every) == 0) wait_deps(kb + h);
+            if (dep_st && reorder) deps_of_stage();
             if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
             const int st = (int)((it + (uint32_t)sj) % NS);
             if (KPS > 1 && a3d) {
