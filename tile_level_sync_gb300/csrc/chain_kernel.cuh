@@ -585,6 +585,11 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       const bool reorder = !(args.flags_bits & kFlagNoReorder);
       uint32_t it = 0, tcount = 0, pw_seen = 0;  // it: stages armed (every tile starts a stage)
       uint32_t kit = 0;                           // k-blocks loaded, for the prefetch warp
+      // ring cursors: the slot (and the parity of its `empty` phase) of the next stage to
+      // arm, and the slot of the next stage to receive its A copies; they advance one stage
+      // at a time, which spares the loader a division per stage
+      int b_slot = 0, a_slot = 0;
+      uint32_t b_par = 1u;
       bool ok = true;
       while (true) {
         const int slot = tcount % C::kSlots;
@@ -720,16 +725,19 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         // has not (non-blocking), set the bytes its barrier expects and issue its weight (B)
         // copies -- one 3-D box of KPS k-blocks, or one copy per k-block.
         auto arm_b = [&](int32_t sj, bool blocking) -> int {
-          const uint32_t j = it + (uint32_t)sj;
-          const int st = (int)(j % NS);
-          const uint32_t par = ((j / NS) & 1u) ^ 1u;
+          const int st = b_slot;  // the slot of stage it + sj (sj is always the next to arm)
+          const uint32_t par = b_par;
           if (blocking) {
             const int32_t aborted = *abort_flag;  // read before the wait: off the critical path
             if (!ptx::mbar_wait_bounded(&empty[st], par, pto) || aborted) return -1;
           } else if (!ptx::mbar_test_wait(&empty[st], par)) {
             return 0;
           }
-          stage_kind[st] = checked ? 1 : 0;
+          if (++b_slot == NS) {
+            b_slot = 0;
+            b_par ^= 1u;
+          }
+          if (CHECK) stage_kind[st] = checked ? 1 : 0;  // (always 0 without the checkers)
           const int32_t kb = sj * KPS;
           const int32_t nk = KPS == 1 ? 1 : min(KPS, KB - kb);
           if (!to_leader) ptx::mbar_arrive_expect_tx(&lbar[st], (KPS == 1 || nk == KPS) ? tx_full : stage_bytes(nk));
@@ -848,7 +856,8 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
             }
             if (dep_st && reorder) deps_of_stage();
             if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
-            const int st = (int)((it + (uint32_t)sj) % NS);
+            const int st = a_slot;
+            if (++a_slot == NS) a_slot = 0;
             if (KPS > 1 && a3d) {
               if (to_leader) ptx::tma_load_3d_to_leader(smem_a(st), tmA, ptx::mapa(&full[st], 0), 0, a_row, tr.kb0 + kb, pol_a);
               else ptx::tma_load_3d(smem_a(st), tmA, &lbar[st], 0, a_row, tr.kb0 + kb, pol_a);
@@ -888,7 +897,8 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
             }
             if (dep_st && reorder) deps_of_stage();
             if (kb == 0 && trec) trec->t_ready = ptx::globaltimer();
-            const int st = (int)((it + (uint32_t)sj) % NS);
+            const int st = a_slot;
+            if (++a_slot == NS) a_slot = 0;
 #pragma unroll
             for (int32_t h = 0; h < KPS; ++h) {
               if (h >= nk) break;
