@@ -156,8 +156,10 @@ typedef struct {
   uint64_t timeout_ns;               /* bound of every device wait on a semaphore or a
                                         sentinel; 0 = 1e9 (one second) */
   int32_t l2_prefetch;               /* k-blocks a prefetch warp runs ahead of the TMA
-                                        loader, prefetching weight (and producer
-                                        activation) rows into L2; 0 or -1 = none */
+                                        loader, prefetching the weight boxes into L2
+                                        through the copy engine; -1 = none; 0 = planner:
+                                        4 for MLP chains on CTA pairs whose producer
+                                        GEMM is K-split (weight streaming), else none */
   int32_t cta_pair;                  /* CTAs per tile: 1, or 2 = a CTA pair (cluster of
                                         two) computes a 256-row tile with cta_group::2
                                         MMAs, each CTA loading half of the weight tile

@@ -27,7 +27,7 @@
 //                   validity report), then arrives on the MMA issuer's `ready` barrier
 //                   (the leader's, in a pair), so that the scan overlaps the MMAs of the
 //                   stages before it.
-//   warp 6          L2 prefetch of the k-blocks ahead of the loader.
+//   warp 6          L2 prefetch of the weight boxes a few k-blocks ahead of the loader.
 //   warps 2..5      epilogue.  tcgen05.ld of this CTA's 128 accumulator rows
 //                   (double-buffered in TMEM so the next tile's mainloop overlaps this
 //                   epilogue), GeLU / SwiGLU / ReLU, bf16 round-to-nearest-even, -0 -> +0
@@ -80,8 +80,8 @@ struct StageArgs {
   CUtensorMap tmB;       // weights [N (or 2*N1), K]
   CUtensorMap tmO;       // GEMM output [M, N]: 64-column x 32-row store boxes, 128-byte swizzle
   void* out;             // bf16 [M, N] row-major (conv: [pixels, channels])
-  const uint16_t* a_ptr; // GEMM activations [a_rows, K] row-major, for L2 prefetch
-  const uint16_t* b_ptr; // weights [b_rows, K] row-major, for L2 prefetch
+  const uint16_t* a_ptr; // activations [a_rows, K] row-major (read directly by the pointwise stage)
+  const uint16_t* b_ptr; // weights [b_rows, K] row-major
   int32_t a_rows, b_rows;
   StageGeo g;
   int32_t b_half_rows;   // SwiGLU: row offset of the up-projection half of B
@@ -280,20 +280,6 @@ __device__ __forceinline__ int32_t b_row(const StageArgs& S, const TileRef& tr, 
     return which == 0 ? row0 : S.b_half_rows + row0;
   }
   return tr.c * BN + (PAIR == 2 ? (int32_t)rank * (BN / 2) : 0);
-}
-
-// Prefetch into L2, one 128-byte line per row, the k-block kb of `rows` rows starting at
-// `row0` of a row-major bf16 matrix with `nrows` rows and K columns; rows are spread over
-// the warp's lanes.  Lines that would reach past the end of the matrix are skipped.
-__device__ __forceinline__ void prefetch_rows(const uint16_t* base, int32_t nrows, int32_t K, int32_t row0,
-                                              int32_t rows, int32_t kb, int lane) {
-  const int32_t col = kb * kBK;
-  if (base == nullptr || col >= K) return;
-  for (int32_t r = lane; r < rows; r += 32) {
-    const int32_t row = row0 + r;
-    if (row >= nrows || (row == nrows - 1 && col + kBK > K)) continue;
-    ptx::prefetch_l2(base + (int64_t)row * K + col);
-  }
 }
 
 __device__ __forceinline__ void record_error(const ChainArgs& a, uint32_t cls, int32_t tile, int32_t detail) {
@@ -1238,11 +1224,11 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
     __syncwarp();
   } else if (warp == 6) {
     // ------------------------------------------------------------ L2 prefetch warp
-    // Follows the tile ring and, paced by the loader's progress counter, prefetches the
-    // k-blocks up to l2_prefetch ahead of the loader into L2 with plain prefetch
-    // instructions: this CTA's weight rows for every GEMM tile and its activation rows
-    // for producer tiles.  The TMA loads that follow then hit L2 instead of waiting for
-    // HBM, which the shared-memory ring alone cannot hide.
+    // Follows the tile ring and, paced by the loader's progress counter, prefetches this
+    // CTA's weight box of the k-blocks up to l2_prefetch ahead of the loader into L2, one
+    // copy-engine prefetch per box.  The copies that follow then find the weights in L2
+    // instead of waiting for HBM, which the shared-memory ring alone cannot hide when the
+    // chain streams its weights (a few CTAs per weight tile, small M).
     const int32_t pd = args.l2_prefetch;
     uint32_t tcount = 0, it0 = 0;
     while (true) {
@@ -1259,8 +1245,6 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       const StageGeo& g = SA.g;
       const int32_t KB = tr.nkb;
       if (pd > 0 && g.a_mode == AMODE_GEMM) {
-        const int32_t a_row0 = tr.m * (128 * PAIR) + (int32_t)rank * 128;
-        const int32_t b_rows = (PAIR == 1 && g.epi == EPI_SWIGLU) ? BN / 2 : BN / PAIR;
         const int32_t b0 = b_row<BN, PAIR>(SA, tr, rank, 0);
         const int32_t b1 = (PAIR == 1 && g.epi == EPI_SWIGLU) ? b_row<BN, PAIR>(SA, tr, rank, 1) : -1;
         bool live = true;
@@ -1278,9 +1262,14 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           }
           live = __shfl_sync(FULL, live ? 1 : 0, 0) != 0;
           if (!live) break;
-          prefetch_rows(SA.b_ptr, SA.b_rows, g.K, b0, b_rows, tr.kb0 + kb, lane);
-          if (b1 >= 0) prefetch_rows(SA.b_ptr, SA.b_rows, g.K, b1, b_rows, tr.kb0 + kb, lane);
-          if (tr.s == 0) prefetch_rows(SA.a_ptr, SA.a_rows, g.K, a_row0, 128, tr.kb0 + kb, lane);
+          // the weight tile's box through the copy engine: one instruction per box
+          if (lane == 0 && !(SA.b3d && (kb & 1))) {
+            if (SA.b3d) ptx::tma_prefetch_3d(&SA.tmB, 0, b0, tr.kb0 + kb);
+            else if (!args.stack) {
+              ptx::tma_prefetch_2d(&SA.tmB, (tr.kb0 + kb) * kBK, b0);
+              if (b1 >= 0) ptx::tma_prefetch_2d(&SA.tmB, (tr.kb0 + kb) * kBK, b1);
+            }
+          }
         }
       }
       it0 += (uint32_t)KB;
