@@ -52,6 +52,8 @@ def test_tiny_mlp_all_policies_bit_identical(tile_n, pair):
     (384, 1024, 2048, 1024, 128),  # several row and column tiles, longer K
     (1, 64, 512, 128, 256),        # a single token
     (520, 512, 1536, 512, 256),    # more tiles than a persistent CTA's ring holds
+    (264, 200, 512, 256, 256),     # K not a whole number of k-blocks: 2-D copies inside two-k-block stages
+    (136, 320, 768, 200, 128),     # an odd k-block count: a pair's last stage holds one k-block of its box
 ])
 @pytest.mark.parametrize("pair", [1, 2])
 def test_mlp_shapes_all_policies(M, K, N1, N2, tile_n, pair):
