@@ -772,7 +772,7 @@ def sweep(a, torch, cs, synth, out_path):
     results = []
     # (raster rows, L2 prefetch, CTAs per tile; 0 = the planner's choice): every policy and
     # launch mode on the planner's tiling, Stream/Row/Tile on the others
-    variants = [(1, -1, 0), (1, -1, 1), (1, -1, 2), (16, -1, 0)]
+    variants = [(1, 0, 0), (1, 0, 1), (1, 0, 2), (16, 0, 0)]
     for name in names:
         wl = synth.WORKLOADS[name]
         inputs = synth.workload_inputs(wl, seed=0)
