@@ -572,8 +572,9 @@ Grids make_grids(const Plan& p, int sms, int max_clusters) {
 // ----------------------------------------------------------------------------- latency model
 
 // GB300 constants of the latency model for plan p, from the in-kernel trace of the bench
-// workloads: mainloop ns per k-block (single CTAs 345-375, CTA pairs 390-420 per pair
-// k-block, convolutions 355-400, consumers slightly slower than producers), a consumer
+// workloads: mainloop ns per k-block (single CTAs 345-375; CTA pairs, whose stages of
+// two k-blocks take one copy per operand, 320-360 per pair k-block; convolutions
+// 355-400), a consumer
 // k-block under the sentinel check once its data is valid (420-440 ns: two checker warps
 // scan alternate stages), a tile's first copy about 1 us,
 // the post seen by a consumer about 1.5 us after the stores, 2 us between stream-ordered
@@ -587,8 +588,8 @@ LatencyModel default_model(const Plan& p) {
     m.kblock_ns[1] = 360.0;
     m.sentinel_kblock_ns = 420.0;
   } else if (p.pair == 2) {
-    m.kblock_ns[0] = 395.0;
-    m.kblock_ns[1] = 415.0;
+    m.kblock_ns[0] = 340.0;
+    m.kblock_ns[1] = 330.0;
     m.sentinel_kblock_ns = 435.0;
   } else {
     m.kblock_ns[0] = p.bn == 128 ? 355.0 : 350.0;
