@@ -781,7 +781,7 @@ def sweep(a, torch, cs, synth, out_path):
             row = {"workload": name, "tile_n": tile_n, "gflop": wl.gemm_flops() / 1e9, "us": {}}
             for vi, (raster, pf, pair) in enumerate(variants):
                 pols = ["STREAM", "ROW", "TILE", "STRIDED", "SENTINEL"] if vi == 0 else ["STREAM", "ROW", "TILE"]
-                if wl.kind == "attention":   # single CTAs only; its policies are Row, Tile, Strided+Tile
+                if wl.kind == "attention":   # its policies are Row, Tile, Strided+Tile
                     pols = ["STREAM", "ROW", "TILE", "STRIDED"]
                 for pol in pols:
                     for launch in (cs.LAUNCH_PERSISTENT, cs.LAUNCH_PDL):

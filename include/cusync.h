@@ -163,8 +163,10 @@ typedef struct {
   int32_t cta_pair;                  /* CTAs per tile: 1, or 2 = a CTA pair (cluster of
                                         two) computes a 256-row tile with cta_group::2
                                         MMAs, each CTA loading half of the weight tile
-                                        (MLP chains only); 0 = 2 for MLP chains with
-                                        M >= 256, else 1 */
+                                        (MLP and attention chains; in the attention
+                                        chain's pointwise stage each CTA computes its
+                                        128 rows); 0 = 2 for MLP and attention chains
+                                        with M >= 256, else 1 */
   int32_t ksplit;                    /* K split of the producer GEMM (MLP chains): each
                                         producer tile is computed by this many work units
                                         over consecutive k-block ranges, whose fp32 partial

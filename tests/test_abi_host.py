@@ -132,7 +132,7 @@ def test_plan_waves_cta_pairs(M, prod, cons, stream, fused):
     assert info.cta_pair == 2 and info.grid[0] == 2 * min(74, prod + cons)
 
 
-def test_cta_pair_only_for_mlp_chains():
+def test_cta_pairs_not_for_convolution_chains():
     d = cs.make_desc(cs.CHAIN_CONV_RELU, "ROW", n=1, h=14, w=14, c=64, k_out=64, num_sms=148, cta_pair=2)
     with pytest.raises(cs.CusyncError) as e:
         cs.cusync_plan_info(d)
@@ -407,8 +407,7 @@ def test_attention_output_gemm_waits_match_oracle(case, policy):
 
 def test_attention_refusals():
     base = dict(M=64, K=128, N1=256, N2=128, tile_n=256, num_sms=148)
-    for kw, status in [(dict(policy="SENTINEL"), cs.ERR_UNSUPPORTED), (dict(policy="ROW", N1=192), cs.ERR_UNSUPPORTED),
-                       (dict(policy="ROW", cta_pair=2), cs.ERR_UNSUPPORTED)]:
+    for kw, status in [(dict(policy="SENTINEL"), cs.ERR_UNSUPPORTED), (dict(policy="ROW", N1=192), cs.ERR_UNSUPPORTED)]:
         args = dict(base, **kw)
         pol = args.pop("policy")
         with pytest.raises(cs.CusyncError) as e:
@@ -417,6 +416,14 @@ def test_attention_refusals():
     # the latency model covers the two-stage chains only
     with pytest.raises(cs.CusyncError):
         cs.cusync_predict_policies(cs.make_desc(cs.CHAIN_ATTENTION, "ROW", **base))
+    # CTA pairs: 256-row tiles in all three stages, every CTA of a pair posting; the
+    # convolution chains keep single CTAs
+    info = cs.cusync_plan_info(cs.make_desc(cs.CHAIN_ATTENTION, "ROW", **dict(base, M=600, cta_pair=2)))
+    assert info.cta_pair == 2 and info.m_tiles[0] == info.m_tiles[1] == info.m_tiles2 == 3
+    assert cs.cusync_pointwise_waits(cs.make_desc(cs.CHAIN_ATTENTION, "TILE", **dict(base, cta_pair=2)), 0, 0)[0][1] == 2
+    with pytest.raises(cs.CusyncError) as e:
+        cs.cusync_plan_info(cs.make_desc(cs.CHAIN_CONV_RELU, "ROW", n=1, h=14, w=14, c=64, k_out=64, cta_pair=2))
+    assert e.value.status == cs.ERR_UNSUPPORTED
 
 
 STACK_CASES = [

@@ -47,7 +47,8 @@ def _run(d, ops, M, N1, N2, runs=2):
     (256, 256, 768, 256, 128, 1),     # 18 QKV column tiles, 6 heads
     (130, 2048, 512, 264, 256, 3),    # K split of the QKV GEMM, ragged N2
 ])
-def test_attention_all_policies(M, K, N1, N2, tile_n, ksplit):
+@pytest.mark.parametrize("pair", [1, 2])
+def test_attention_all_policies(M, K, N1, N2, tile_n, ksplit, pair):
     ops, (xqkv_ref, xdot_ref, y_ref) = _operands(M, K, N1, N2, seed=31)
     ref = None
     for pol in POLICIES:
@@ -55,7 +56,7 @@ def test_attention_all_policies(M, K, N1, N2, tile_n, ksplit):
             if pol == "STREAM" and launch != cs.LAUNCH_PERSISTENT:
                 continue
             d = cs.make_desc(cs.CHAIN_ATTENTION, pol, launch, M=M, K=K, N1=N1, N2=N2, tile_n=tile_n,
-                             cta_pair=1, ksplit=ksplit)
+                             cta_pair=pair, ksplit=ksplit)
             xqkv, xdot, y = _run(d, ops, M, N1, N2)
             assert_within_tol(f64(xqkv), xqkv_ref, f"XQKV {pol} {launch}")
             assert_within_tol(f64(xdot), xdot_ref, f"XDot {pol} {launch}")

@@ -345,7 +345,7 @@ __device__ __forceinline__ float silu_f(float g) {
 // Kernels", Fig. fig:gpt-3:attention, fused dot-product kernel; dropout is the identity
 // of inference).  Two passes over the row: an online maximum and sum of exponentials,
 // then the outputs.  Then cuSync §IV-E "Post" for the GEMM that reads XDot.
-__device__ __noinline__ void pointwise_tile(const ChainArgs& args, const TileRef& tr, int32_t t, int row,
+__device__ __noinline__ void pointwise_tile(const ChainArgs& args, const TileRef& tr, int32_t t, int64_t grow,
                                             uint64_t* pw_done, uint32_t pw_parity, uint32_t runs, bool leader,
                                             uint64_t pto, volatile int32_t* abort_flag) {
   const StageArgs& SA = stage_args(args, tr.s);
@@ -364,8 +364,7 @@ __device__ __noinline__ void pointwise_tile(const ChainArgs& args, const TileRef
       }
     }
   }
-  const int64_t grow = (int64_t)tr.m * 128 + row;
-  if (grow < g.M) {
+  if (grow < g.M) {  // this thread's token row (a CTA of a pair holds 128 of the tile's 256)
     const int32_t n1 = g.N;
     const uint16_t* xr = SA.a_ptr + grow * (int64_t)g.K + (int64_t)tr.c * kHead;  // XQKV row: Q | V | K
     const uint4* qp = reinterpret_cast<const uint4*>(xr);
@@ -1308,7 +1307,8 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       const StageArgs& SA = stage_args(args, tr.s);
       const StageGeo& g = SA.g;
       if (g.a_mode == AMODE_POINTWISE) {
-        pointwise_tile(args, tr, t, row, pw_done, pwcount & 1u, *run_no, leader, pto, abort_flag);
+        pointwise_tile(args, tr, t, (int64_t)tr.m * (128 * PAIR) + (int64_t)rank * 128 + row, pw_done, pwcount & 1u,
+                       *run_no, leader, pto, abort_flag);
         ++pwcount;
         continue;
       }

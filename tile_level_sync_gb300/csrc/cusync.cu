@@ -129,12 +129,13 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   const bool mlp = d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
   const bool attn = d.kind == CUSYNC_CHAIN_ATTENTION;
   const bool stack = d.kind == CUSYNC_CHAIN_CONV_STACK;
-  // CTA pairs (cta_group::2, 256-row tiles) for MLP chains with at least 256 tokens,
-  // where they measured faster on GB300 (GPT-3 M=256: 91 against 97 us; SwiGLU M=256
-  // even); single-CTA 128-row tiles otherwise.
-  const int32_t pair = d.cta_pair ? d.cta_pair : ((mlp && d.M >= 256) ? 2 : 1);
+  // CTA pairs (cta_group::2, 256-row tiles) for MLP and attention chains with at least
+  // 256 tokens, where they measured faster on GB300 (GPT-3 MLP M=256: 91 against 97 us;
+  // SwiGLU M=256 even; GPT-3 attention M=1024: 148.6 against 155.1 us, M=256 84.1 against
+  // 85.9 us); single-CTA 128-row tiles otherwise.
+  const int32_t pair = d.cta_pair ? d.cta_pair : (((mlp || attn) && d.M >= 256) ? 2 : 1);
   if (pair != 1 && pair != 2) return CUSYNC_ERR_INVALID_ARG;
-  if (pair == 2 && !mlp) return CUSYNC_ERR_UNSUPPORTED;
+  if (pair == 2 && !mlp && !attn) return CUSYNC_ERR_UNSUPPORTED;  // (convolutions: single CTAs)
   std::memset(p, 0, sizeof(*p));
   p->bn = bn;
   p->pair = pair;
@@ -346,7 +347,7 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
     dep.prod_n_out = g1.n_out;
     dep.G = 1;
     dep.D = g1.n_tiles;
-    dep.posts = 1;
+    dep.posts = pair;  // each CTA of a pair posts its 128 rows of the pointwise tile
     p->num_flags = num_flags(dep);
     p->num_flags_pw = num_flags(dp);
     if (p->num_flags + p->num_flags_pw > (1ll << 24)) return CUSYNC_ERR_UNSUPPORTED;
