@@ -183,9 +183,10 @@ typedef struct {
   int32_t ksplit_consumer;           /* K split of the consumer GEMM of an MLP chain, as
                                         ksplit: each consumer tile computed by this many
                                         units, added in unit order by the last.  0 =
-                                        planner: when the consumer tiles fill at most half
-                                        of a wave, as many units per tile as fit in one
-                                        wave (at most 4, at least 16 k-blocks each);
+                                        planner: when single-CTA consumer tiles fill at
+                                        most half of a wave, as many units per tile as fit
+                                        in one wave (at most 4, at least 16 k-blocks each);
+                                        none on CTA pairs;
                                         none under STRIDED_TILE with more than 64 groups.
                                         1 = none */
 } cusync_chain_desc_t;

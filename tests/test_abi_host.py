@@ -496,7 +496,7 @@ def test_stack_plan_and_refusals():
 @pytest.mark.parametrize("kind,dims,pair,want", [
     (cs.CHAIN_MLP_GELU, dict(M=256, **GPT), 2, 1),      # 48 pair tiles: more than half of 76 pairs
     (cs.CHAIN_MLP_GELU, dict(M=1024, **GPT), 2, 1),
-    (cs.CHAIN_MLP_SWIGLU, dict(M=256, K=8192, N1=3584, N2=8192), 2, 2),   # 32 pair tiles: 2 units fit
+    (cs.CHAIN_MLP_SWIGLU, dict(M=256, K=8192, N1=3584, N2=8192), 2, 1),   # CTA pairs keep whole tiles
     (cs.CHAIN_MLP_SWIGLU, dict(M=256, K=8192, N1=3584, N2=8192), 1, 2),   # 64 tiles on 152 SMs
     (cs.CHAIN_MLP_GELU, dict(M=64, K=12288, N1=6144, N2=12288), 1, 3),    # 48 tiles: 3 units fit in a wave
     (cs.CHAIN_MLP_GELU, dict(M=64, K=256, N1=1024, N2=256), 1, 1),        # 16 k-blocks: nothing to split

@@ -291,16 +291,16 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   g0.kb_per_split = (int32_t)ceil_div(g0.k_blocks, ks);
   g0.ksplit = (int32_t)ceil_div(g0.k_blocks, g0.kb_per_split);  // no empty unit
   // K split of the consumer GEMM of an MLP chain (cusync_chain_desc_t::ksplit_consumer):
-  // consumer tiles that fill at most half of a wave get as many units per tile as fit in
-  // one wave (at most 4, at least 16 k-blocks each).  Measured on GB300: 5-10% faster for
-  // the SwiGLU M=256 slice (32 pair tiles of 56 k-blocks), but 4-9% slower for the GPT-3
-  // M=256 and M=512 slices (48 and 96 pair tiles of 96 k-blocks) with three units, whose
-  // consumers' partial sums cost more than the fuller waves gain.
+  // single-CTA consumer tiles that fill at most half of a wave get as many units per tile
+  // as fit in one wave (at most 4, at least 16 k-blocks each).  CTA pairs keep whole
+  // consumer tiles: with their two-k-block copies the SwiGLU M=256 slice (32 pair tiles
+  // of 56 k-blocks) measured 60.7 us unsplit against 61.7 us with two units, and the
+  // GPT-3 M=256 and M=512 slices 4-9% slower with three units.
   if (d.ksplit_consumer < 0 || d.ksplit_consumer > 16) return CUSYNC_ERR_INVALID_ARG;
   int32_t ks1 = d.ksplit_consumer;
   if (ks1 == 0) {
     ks1 = 1;
-    if (mlp) {
+    if (mlp && pair == 1) {
       int sms = 0;
       if (query_num_sms(d.num_sms, &sms) != 0) sms = 148;
       const int64_t slots = std::max<int64_t>(1, sms / pair);
