@@ -146,7 +146,10 @@ typedef struct {
   int32_t _pad0;
   int64_t M, K, N1, N2;              /* MLP chains (see cusync_chain_kind_t) */
   int32_t n, h, w, c, k_out;         /* CONV_RELU: NHWC image and output channels */
-  int32_t tile_n;                    /* accumulator tile width: 128 or 256; 0 = choose */
+  int32_t tile_n;                    /* accumulator tile width: 128 or 256; 0 = planner:
+                                        128 for a single-CTA MLP chain whose producer
+                                        tiles at 256 would fill at most 1/16 of the SMs,
+                                        else 256 */
   int32_t strided_group;             /* G for STRIDED_TILE; 0 = 2 */
   uint32_t flags;                    /* CUSYNC_FLAG_* | CUSYNC_DEBUG_* */
   int32_t num_sms;                   /* SMs the kernels may use; 0 = all of the device */

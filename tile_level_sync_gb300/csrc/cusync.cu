@@ -107,13 +107,25 @@ int32_t conv_rows_per_tile(int32_t h, int32_t w) {
   return (int32_t)ceil_div(h, tpi);
 }
 
+int query_num_sms(int32_t requested, int* out);
+
 int32_t default_tile_n(const cusync_chain_desc_t& d) {
   if (d.tile_n) return d.tile_n;
+  // A single-CTA MLP chain whose producer tiles at width 256 would occupy at most a
+  // sixteenth of the SMs is bound by the latency of a few tiles: 128-wide tiles double
+  // their number (the 64-token chain of 256 x 1024 x 256: 19.0 against 22.7 us, RowSync).
+  const bool mlp = d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
+  const bool single = d.cta_pair == 1 || (d.cta_pair == 0 && d.M < 256);
+  if (mlp && single && d.M > 0 && d.N1 > 0) {
+    int sms = 0;
+    if (query_num_sms(d.num_sms, &sms) != 0) sms = 148;
+    const int64_t tiles = ((d.M + 127) / 128) * ((d.N1 + 255) / 256);
+    if (16 * tiles <= sms) return 128;
+  }
   return 256;
 }
 
 cusync_status_t resolve_auto(const cusync_chain_desc_t& d, cusync_chain_desc_t* out);
-int query_num_sms(int32_t requested, int* out);
 
 cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   if (d.kind < CUSYNC_CHAIN_MLP_GELU || d.kind > CUSYNC_CHAIN_CONV_STACK) return CUSYNC_ERR_INVALID_ARG;
