@@ -44,7 +44,7 @@ NCU_TRAFFIC = {
     # (workload, policy, launch, tile_n, CTAs per tile): (dram__bytes_read.sum +
     # dram__bytes_write.sum per launch of the chain kernel, hash of the kernel sources the
     # capture was taken with)
-    ("gpt3_mlp_m256", "ROW", "persistent", 256, 2): (311404800 + 17874688, "9172aeed71f6d97d"),
+    ("gpt3_mlp_m256", "ROW", "persistent", 256, 2): (311140608 + 18001920, "90220715f9271dae"),
 }
 
 
