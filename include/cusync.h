@@ -401,6 +401,10 @@ cusync_status_t cusync_producer_col(const cusync_chain_desc_t* d, int32_t y, int
 cusync_status_t cusync_tile_at(const cusync_chain_desc_t* d, int32_t stage, int32_t u, int32_t* m_tile,
                                int32_t* n_tile);
 
+/* Semaphores that cusync_run_mlp_noalloc's fixed array holds: 16384 words less the 48
+ * control words in front of the semaphores. */
+#define CUSYNC_NOALLOC_MAX_SEMAPHORES 16336
+
 /* Allocation-free variant of cusync_run_mlp, for callers that cannot allocate device
  * memory themselves (for example an operator running inside a runtime that owns the
  * device memory pool, or a serving loop that must avoid cudaMalloc's synchronisation).
@@ -408,9 +412,13 @@ cusync_status_t cusync_tile_at(const cusync_chain_desc_t* d, int32_t stage, int3
  *
  * It needs no chain object: it plans the chain described by *d and runs it with the same
  * kernels, keeping the synchronisation state (error word, tile counters, semaphores) in a
- * fixed 64 KiB array inside the library (16368 semaphores at most; larger plans return
- * CUSYNC_ERR_UNSUPPORTED).  It calls no cudaMalloc or cudaFree.  Inputs and outputs are
- * as for cusync_run_mlp.
+ * fixed 64 KiB array inside the library (CUSYNC_NOALLOC_MAX_SEMAPHORES semaphores at
+ * most; larger plans return CUSYNC_ERR_UNSUPPORTED).  It calls no cudaMalloc or
+ * cudaFree.  Inputs and outputs are as for cusync_run_mlp.
+ *  - There is no workspace for K-split partial sums: d->ksplit and d->ksplit_consumer
+ *    must be 0 or 1 (CUSYNC_ERR_UNSUPPORTED otherwise), and 0 means 1 here, where
+ *    cusync_run_mlp's planner may split.  With both set to 1, cusync_run_mlp on the same
+ *    descriptor writes byte-identical H and Y.
  *  - The first call on each device looks up the array's device address and prepares the
  *    kernels for that device; make that first call before any stream capture.
  *  - Every call clears the part of the array it uses on `stream`, then launches; the

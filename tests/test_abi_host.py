@@ -40,6 +40,8 @@ def _header_constants():
     vals = {k: int(v) for k, v in re.findall(r"\b(CUSYNC_[A-Z0-9_]+)\s*=\s*(\d+)", src)}
     for k, sh in re.findall(r"#define\s+(CUSYNC_[A-Z0-9_]+)\s+\(1u\s*<<\s*(\d+)\)", src):
         vals[k] = 1 << int(sh)
+    for k, v in re.findall(r"#define\s+(CUSYNC_[A-Z0-9_]+)\s+(\d+)\s*$", src, flags=re.M):
+        vals[k] = int(v)
     return vals
 
 
@@ -51,7 +53,7 @@ def test_binding_constants_match_header():
         if py.startswith("POLICY_") or py.startswith("CHAIN_") or py.startswith("LAUNCH_") or \
                 py.startswith("FLAG_") or py.startswith("DEBUG_"):
             assert getattr(cs, py) == v, name
-        elif py == "OK" or py.startswith("ERR_"):
+        elif py == "OK" or py.startswith("ERR_") or py.startswith("NOALLOC_"):
             assert getattr(cs, py) == v, name
 
 
@@ -558,3 +560,30 @@ def test_consumer_unit_waits_match_oracle(case, policy, G, ks):
                 got[kb] |= _members(policy, flag, nt, D, Gc)
             want = deps.wait_sets(ch, policy, m, Gc, kbs=kbs)
             assert [got[kb] for kb in kbs] == want, (policy, m, u)
+
+
+def test_noalloc_semaphore_limit_is_exact():
+    """The allocation-free entry point accepts a plan of exactly
+    CUSYNC_NOALLOC_MAX_SEMAPHORES semaphores (it gets past the size check to the pointer
+    check: null operands are INVALID_ARG) and refuses one more as UNSUPPORTED, before it
+    touches a device.  Single-CTA RowSync plans have one semaphore per 128-row tile."""
+    import ctypes
+    lib = cs.load()
+    n = cs.NOALLOC_MAX_SEMAPHORES
+    for tiles, want in ((n, cs.ERR_INVALID_ARG), (n + 1, cs.ERR_UNSUPPORTED)):
+        d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=128 * tiles, K=64, N1=64, N2=64, cta_pair=1, tile_n=128,
+                         num_sms=148)
+        assert cs.cusync_plan_info(d).num_flags == tiles
+        st = lib.cusync_run_mlp_noalloc(ctypes.byref(d), None, None, None, None, None, None, None)
+        assert st == want, (tiles, cs.status_string(st))
+
+
+def test_noalloc_refuses_k_split():
+    """No workspace for K-split partial sums: a split of either GEMM is refused."""
+    import ctypes
+    lib = cs.load()
+    for ks, ks1 in ((2, 0), (0, 2), (1, 3)):
+        d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=256, K=2048, N1=1024, N2=512, tile_n=256, cta_pair=1,
+                         ksplit=ks, ksplit_consumer=ks1, num_sms=148)
+        st = lib.cusync_run_mlp_noalloc(ctypes.byref(d), None, None, None, None, None, None, None)
+        assert st == cs.ERR_UNSUPPORTED, (ks, ks1, cs.status_string(st))

@@ -25,6 +25,7 @@ FLAG_TRACE = 1 << 1
 DEBUG_SKIP_POST = 1 << 8
 DEBUG_SKIP_INIT = 1 << 9
 DEBUG_SKIP_SPLIT = 1 << 10
+NOALLOC_MAX_SEMAPHORES = 16336
 
 POLICY_NAMES = {"STREAM": POLICY_STREAM, "ROW": POLICY_ROW, "TILE": POLICY_TILE,
                 "STRIDED": POLICY_STRIDED_TILE, "SENTINEL": POLICY_SENTINEL, "AUTO": POLICY_AUTO}

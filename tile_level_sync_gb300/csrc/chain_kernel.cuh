@@ -31,8 +31,9 @@
 //   warps 2..5      epilogue.  tcgen05.ld of this CTA's 128 accumulator rows
 //                   (double-buffered in TMEM so the next tile's mainloop overlaps this
 //                   epilogue), GeLU / SwiGLU / ReLU, bf16 round-to-nearest-even, -0 -> +0
-//                   (CUDA-FGS §4.6.4.3), whole 16-byte chunks written with one 128-bit
-//                   store each; for a producer tile one thread posts the tile's semaphore
+//                   (CUDA-FGS §4.6.4.3), then TMA stores of 32-row x 64-column boxes
+//                   (GEMM outputs) or 16-byte stores (convolution outputs); for a
+//                   producer tile one thread posts the tile's semaphore
 //                   after all of the CTA's stores (cuSync §IV-E "Post": barrier,
 //                   device-scope fence, atomic increment).  Each CTA of a pair posts its
 //                   own half, so a pair tile's semaphore receives two posts.
@@ -1073,27 +1074,31 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       uint32_t clean_ahead = 0;
       bool ok = true;
       // Whether the A tile in stage sx still holds the sentinel anywhere (all lanes).
-      // The check inspects one 32-bit word (two bf16 elements) of every aligned 16-byte
-      // chunk, the granularity of CUDA-FGS's per-16-byte validity report: the producer
-      // writes each chunk with one 128-bit store under this policy, so a chunk is either
-      // all sentinel or all data.  Lane l reads word (c / 8) % 4 of chunk c = 32 i + l,
-      // which puts a warp's 32 reads in 32 different banks.  Shared-memory loads are slow
-      // to return while TMA writes and the MMAs read the same memory, so a 16 KB tile's 32
-      // loads per lane are all issued before the first one is tested.
+      // Every bf16 element of the landed tile is inspected.  The PTX memory model treats
+      // a vector store as independent scalar stores in no fixed order, so a copy that
+      // overlaps the producer's 128-bit store of a chunk may bring some of its words
+      // written and others not; a sampled word would then pass a chunk that is partly
+      // sentinel.  Scanning every word makes the check independent of how the producer's
+      // stores are split: any element still holding 0x8000 sends the tile back.  Lane l
+      // reads 16-byte chunk c = 32 i + l, so a warp's load covers 512 contiguous bytes
+      // without bank conflicts.  Shared-memory loads are slow to return while TMA writes
+      // and the MMAs read the same memory, so all of a 16 KB tile's loads (32 per lane)
+      // are issued before the first one is tested.
       auto stage_has_sentinel = [&](int sx, uint32_t nbytes) -> bool {
         uint32_t sbits = 0;
         const uint8_t* base = smem_a(sx);
         const uint32_t nchunks = nbytes / 16u;
-        const uint32_t word = ((uint32_t)lane >> 3) & 3u;
         for (uint32_t c0 = (uint32_t)lane; c0 < nchunks; c0 += 32u * 32u) {
-          uint32_t v[32];
+          uint4 v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const uint32_t c = c0 + (uint32_t)j * 32u;
-            v[j] = c < nchunks ? ptx::ld_shared_u32(base + c * 16u + word * 4u) : 0u;
+            v[j] = c < nchunks ? ptx::ld_shared_v4(base + c * 16u) : make_uint4(0u, 0u, 0u, 0u);
           }
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sbits |= sentinel_bits_bf16x2(v[j]);
+          for (int j = 0; j < 32; ++j)
+            sbits |= sentinel_bits_bf16x2(v[j].x) | sentinel_bits_bf16x2(v[j].y) | sentinel_bits_bf16x2(v[j].z) |
+                     sentinel_bits_bf16x2(v[j].w);
         }
         return __any_sync(FULL, (sbits & 0x80008000u) != 0u);
       };
@@ -1347,10 +1352,10 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       const int nchunks = g.n_out / 32;
       // GEMM outputs leave through TMA stores of 32-row x 64-column boxes staged in this
       // warp's two shared-memory buffers; convolution outputs (a tile's pixels are not a
-      // box of the output tensor) through 16-byte stores from registers.
-      // (under the sentinel policy the tile that the consumer checks is written with one
-      // 128-bit store per 16-byte chunk, as the per-chunk check requires)
-      const bool tma_out = g.a_mode == AMODE_GEMM && !(CHECK && tr.s == args.nst - 2);
+      // box of the output tensor) through 16-byte stores from registers.  Under the
+      // sentinel policy the consumer's check inspects every element it loads, so it does
+      // not matter how the stores of the tile it checks are split.
+      const bool tma_out = g.a_mode == AMODE_GEMM;
       uint8_t* ebuf = epi_stage + (q * 2) * C::kEpiBufBytes;
       const int32_t row_w0 = tr.m * (128 * PAIR) + (int32_t)rank * 128 + q * 32;
       // K split: unit k of a tile adds the running sum of units 0..k-1 to its fp32 partial

@@ -1402,8 +1402,9 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
                                                   uint32_t* error_word) {
   if (!d) return CUSYNC_ERR_INVALID_ARG;
   if (d->kind != CUSYNC_CHAIN_MLP_GELU && d->kind != CUSYNC_CHAIN_MLP_SWIGLU) return CUSYNC_ERR_INVALID_ARG;
-  // No workspace to hold K-split partial sums: the producer tiles are not split.
-  if (d->ksplit > 1) return CUSYNC_ERR_UNSUPPORTED;
+  // No workspace to hold K-split partial sums: neither GEMM is split.  0 (the planner's
+  // choice elsewhere) means 1 here.
+  if (d->ksplit > 1 || d->ksplit_consumer > 1) return CUSYNC_ERR_UNSUPPORTED;
   cusync_chain_desc_t dd = *d;
   dd.ksplit = 1;
   dd.ksplit_consumer = 1;
@@ -1411,10 +1412,12 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
   cusync_status_t st = make_plan(dd, &p);
   if (st != CUSYNC_OK) return st;
   dd.policy = (cusync_policy_t)p.dep.policy;  // CUSYNC_POLICY_AUTO resolved
-  // The fixed array bounds the number of semaphores this entry point can use.
-  if ((int64_t)CTRL_WORDS + p.num_flags > kNoAllocWords) {
-    CUSYNC_LOG("no-alloc run needs %lld semaphores; the fixed scratch holds %d", (long long)p.num_flags,
-               kNoAllocWords - CTRL_WORDS);
+  // The fixed array bounds the chain's state: control words and every semaphore.
+  static_assert(CUSYNC_NOALLOC_MAX_SEMAPHORES == kNoAllocWords - CTRL_WORDS, "no-alloc limit in cusync.h");
+  const int64_t words = state_words(p);
+  if (words > kNoAllocWords) {
+    CUSYNC_LOG("no-alloc run needs %lld semaphores; the fixed scratch holds %d", (long long)(words - CTRL_WORDS),
+               CUSYNC_NOALLOC_MAX_SEMAPHORES);
     return CUSYNC_ERR_UNSUPPORTED;
   }
   if (!aligned16(X) || !aligned16(W1t) || !aligned16(W2t) || !aligned16(H) || !aligned16(Y))
@@ -1445,7 +1448,7 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // Clear what must start at zero: error word, tile counters, run count, semaphores.
-  e = cudaMemsetAsync(scratch, 0, ((size_t)CTRL_WORDS + (size_t)p.num_flags) * sizeof(uint32_t), s);
+  e = cudaMemsetAsync(scratch, 0, (size_t)words * sizeof(uint32_t), s);
   if (e != cudaSuccess) return cuda_fail(e, "no-alloc scratch clear");
   if ((st = launch_run(dd, p, A, grids, H, sms, s)) != CUSYNC_OK) return st;
   if (error_word) {
