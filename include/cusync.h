@@ -146,7 +146,8 @@ typedef struct {
   int32_t _pad0;
   int64_t M, K, N1, N2;              /* MLP chains (see cusync_chain_kind_t) */
   int32_t n, h, w, c, k_out;         /* CONV_RELU: NHWC image and output channels */
-  int32_t tile_n;                    /* accumulator tile width: 128 or 256; 0 = planner:
+  int32_t tile_n;                    /* accumulator tile width: 128, 192 (GeLU MLP chains
+                                        on CTA pairs only) or 256; 0 = planner:
                                         128 for a single-CTA MLP chain whose producer
                                         tiles at 256 would fill at most 1/16 of the SMs,
                                         else 256 */
@@ -229,6 +230,9 @@ typedef struct {
   uint32_t reloads;   /* consumer, sentinel policy: A k-blocks loaded again */
   uint32_t land_clk;  /* SM cycles the MMA issuer waited for this tile's stages to land */
   uint32_t check_clk; /* SM cycles of the sentinel check of this tile (scans and reloads) */
+  uint64_t t_acc;     /* the epilogue found the tile's accumulator complete */
+  uint64_t t_xchg;    /* K split, a unit after the first: the epilogue (first warp) had read
+                         every partial sum it adds from the unit before it (0 otherwise) */
 } cusync_trace_rec_t;
 
 /* Geometry of a chain (for tests and introspection). */

@@ -214,6 +214,8 @@ CASES = [
     dict(kind=cs.CHAIN_MLP_GELU, M=300, K=128, N1=1024, N2=256, tile_n=256),
     dict(kind=cs.CHAIN_MLP_GELU, M=256, K=128, N1=1536, N2=256, tile_n=128),
     dict(kind=cs.CHAIN_MLP_GELU, M=130, K=64, N1=640, N2=64, tile_n=128),           # ragged M and N1
+    dict(kind=cs.CHAIN_MLP_GELU, M=520, K=128, N1=1152, N2=256, tile_n=192),        # 192-wide (pairs only)
+    dict(kind=cs.CHAIN_MLP_GELU, M=300, K=128, N1=1000, N2=64, tile_n=192),         # ... with a ragged N1
     dict(kind=cs.CHAIN_MLP_SWIGLU, M=200, K=64, N1=512, N2=64, tile_n=256),
     dict(kind=cs.CHAIN_CONV_RELU, n=2, h=14, w=14, c=64, k_out=256, tile_n=128),
     dict(kind=cs.CHAIN_CONV_RELU, n=2, h=9, w=30, c=64, k_out=128, tile_n=128),     # 4 rows per tile
@@ -231,7 +233,8 @@ def test_consumer_waits_match_oracle(case, policy, G, pair):
     try:
         info = cs.cusync_plan_info(desc)
     except cs.CusyncError as e:
-        assert policy == "STRIDED" and e.status == cs.ERR_UNSUPPORTED
+        # StridedSync needs a column-tile count divisible by G; 192-wide tiles need pairs
+        assert (policy == "STRIDED" or (case["tile_n"] == 192 and pair == 1)) and e.status == cs.ERR_UNSUPPORTED
         return
     ch = _oracle_chain(desc, info)
     nt = info.n_tiles[0]
@@ -533,13 +536,16 @@ def test_consumer_split_requests():
     dict(M=300, K=128, N1=1024, N2=256, tile_n=256),
     dict(M=256, K=128, N1=1536, N2=256, tile_n=128),
     dict(M=130, K=64, N1=2304, N2=64, tile_n=128),
+    dict(M=520, K=128, N1=2304, N2=256, tile_n=192, cta_pair=2),
 ])
 @pytest.mark.parametrize("policy,G", [("TILE", 1), ("ROW", 1), ("STRIDED", 2), ("STRIDED", 3)])
 @pytest.mark.parametrize("ks", [2, 3])
 def test_consumer_unit_waits_match_oracle(case, policy, G, ks):
     """Every K-split unit of a consumer tile waits, from its own first k-block on, for the
     producer tiles the oracle's policy sets name for exactly the k-blocks it computes."""
-    desc = cs.make_desc(cs.CHAIN_MLP_GELU, policy, strided_group=G, num_sms=148, cta_pair=1, ksplit_consumer=ks,
+    case = dict(case)
+    pair = case.pop("cta_pair", 1)
+    desc = cs.make_desc(cs.CHAIN_MLP_GELU, policy, strided_group=G, num_sms=148, cta_pair=pair, ksplit_consumer=ks,
                         **case)
     try:
         info = cs.cusync_plan_info(desc)

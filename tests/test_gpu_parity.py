@@ -309,3 +309,46 @@ def test_k_split_swiglu():
         b = (bits(H), bits(Y))
         ref = ref or b
         assert np.array_equal(b[0], ref[0]) and np.array_equal(b[1], ref[1]), pol
+
+
+@pytest.mark.parametrize("M,K,N1,N2,ksplit,ksplit_consumer", [
+    (256, 1024, 1152, 768, 0, 0),    # the planner's K split
+    (520, 512, 1536, 512, 1, 0),     # several row tiles, ragged M
+    (300, 384, 1000, 264, 1, 0),     # ragged N1 (the last producer tile is partly outside H) and N2
+    (264, 2048, 1152, 512, 3, 2),    # K-split producer and consumer
+])
+def test_192_wide_pair_tiles_all_policies(M, K, N1, N2, ksplit, ksplit_consumer):
+    """256 x 192 tiles on CTA pairs (the accumulators 256 TMEM columns apart, three
+    64-column store boxes per tile, a consumer k-block reading producer column tile
+    kb*64/192): every policy and launch mode within tolerance of the oracle and
+    byte-identical to one another."""
+    (X, W1, W2), (H_ref, Y_ref) = _mlp_case(M, K, N1, N2, seed=13)
+    ops = device_mlp_operands(X, W1, W2)
+    ref_bits = None
+    for pol in POLICIES:
+        for launch in LAUNCHES:
+            if pol == "STREAM" and launch != cs.LAUNCH_PERSISTENT:
+                continue
+            d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, launch, M=M, K=K, N1=N1, N2=N2, tile_n=192, cta_pair=2,
+                             ksplit=ksplit, ksplit_consumer=ksplit_consumer)
+            try:
+                info = cs.cusync_plan_info(d)
+            except cs.CusyncError as e:
+                assert pol == "STRIDED" and e.status == cs.ERR_UNSUPPORTED
+                continue
+            assert info.tile_n == 192 and info.cta_pair == 2
+            H, Y, _ = run_mlp(d, *ops, runs=3)
+            assert_within_tol(f64(H), H_ref, f"H {pol} {launch}")
+            assert_within_tol(f64(Y), Y_ref, f"Y {pol} {launch}")
+            b = (bits(H), bits(Y))
+            if ref_bits is None:
+                ref_bits = b
+            else:
+                assert np.array_equal(b[0], ref_bits[0]) and np.array_equal(b[1], ref_bits[1]), (pol, launch)
+
+
+def test_192_wide_tiles_only_for_gelu_pairs():
+    for kw in (dict(kind=cs.CHAIN_MLP_GELU, cta_pair=1), dict(kind=cs.CHAIN_MLP_SWIGLU, cta_pair=2)):
+        with pytest.raises(cs.CusyncError) as e:
+            cs.cusync_plan_info(cs.make_desc(policy="ROW", M=256, K=512, N1=1152, N2=256, tile_n=192, **kw))
+        assert e.value.status == cs.ERR_UNSUPPORTED

@@ -55,7 +55,7 @@ class cusync_trace_rec_t(ctypes.Structure):
     _fields_ = [("tile", c_u32), ("smid", c_u32), ("cta", c_u32), ("stage", c_u32),
                 ("t_claim", c_u64), ("t_ready", c_u64), ("t_mma0", c_u64), ("t_mma1", c_u64),
                 ("t_epi", c_u64), ("t_post", c_u64), ("polls", c_u32), ("reloads", c_u32),
-                ("land_clk", c_u32), ("check_clk", c_u32)]
+                ("land_clk", c_u32), ("check_clk", c_u32), ("t_acc", c_u64), ("t_xchg", c_u64)]
 
 
 class cusync_chain_info_t(ctypes.Structure):

@@ -98,6 +98,7 @@ struct TraceRec {
   uint64_t t_claim, t_ready, t_mma0, t_mma1, t_epi, t_post;
   uint32_t polls, reloads;
   uint32_t land_clk, check_clk;
+  uint64_t t_acc, t_xchg;
 };
 
 struct ChainArgs {
@@ -157,13 +158,22 @@ struct KCfg {
   // stage is refilled only once both of its k-blocks are consumed, which leaves fewer
   // bytes in flight), as do the sentinel-checked kernels.
   __host__ __device__ static constexpr int kps(bool check) { return (!check && PAIR == 2 && kStages >= 6) ? 2 : 1; }
-  static constexpr int kTmemCols = 2 * BN;           // two fp32 accumulators of BN columns
+  // Two fp32 accumulators of BN columns, kAccStride columns apart.  A TMEM allocation is
+  // a power of two of columns: a 192-wide tile's accumulators start at columns 0 and 256
+  // of a 512-column allocation.
+  static constexpr int kAccStride = (BN & (BN - 1)) == 0 ? BN : 256;
+  static constexpr int kTmemCols = 2 * kAccStride;
   static constexpr int kSlots = 4;                   // tile hand-off ring
-  // 7 warps (loader, MMA, 4 epilogue, prefetch), + 2 sentinel checkers under that policy
-  static constexpr int threads(bool check) { return check ? 288 : 224; }
-  // epilogue staging for TMA stores: per epilogue warp two 32-row x 64-column bf16 boxes
+  // Warps: 0 loader, 1 MMA, 2..5 epilogue, 6 prefetch; then, under the sentinel policy,
+  // 7..8 the checkers, otherwise 7..10 a second group of epilogue warps (two warps per
+  // TMEM lane quarter, each storing every other 64-column box of a tile).
+  __host__ __device__ static constexpr int epi_warps(bool check) { return check ? 4 : 8; }
+  static constexpr int threads(bool check) { return check ? 288 : 352; }
+  // epilogue staging for TMA stores: 32-row x 64-column bf16 boxes, 32 KB in all (two
+  // boxes per epilogue warp with four warps, one with eight)
   static constexpr int kEpiBufBytes = 32 * 64 * 2;
-  static constexpr int kEpiBytes = 4 * 2 * kEpiBufBytes;
+  static constexpr int kEpiBytes = 8 * kEpiBufBytes;
+  __host__ __device__ static constexpr int epi_bufs(bool check) { return 8 / epi_warps(check); }
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + 1024 + kEpiBytes;
 };
 
@@ -297,6 +307,7 @@ __device__ __forceinline__ uint32_t sentinel_bits_bf16x2(uint32_t x) {
   const uint32_t t = x ^ 0x80008000u;
   return (t - 0x00010001u) & ~t;
 }
+
 
 // K-split workspace words that hold no partial sum hold kSplitEmpty, a NaN (sign set,
 // all payload bits set); a unit stores a sum equal to it as the canonical NaN instead,
@@ -442,6 +453,9 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
   static_assert(S % KPS == 0, "whole stages");
   constexpr uint32_t FULL = 0xFFFFFFFFu;
   constexpr bool kPair = PAIR == 2;
+  constexpr int kEpiWarps = C::epi_warps(CHECK);
+  constexpr int kEpiGroups = kEpiWarps / 4;  // epilogue warps per TMEM lane quarter
+  constexpr int kEpiBufs = C::epi_bufs(CHECK);  // staging boxes per epilogue warp
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -507,15 +521,15 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       }
       for (int i = 0; i < 2; ++i) {
         ptx::mbar_init(&tfull[i], 1);
-        ptx::mbar_init(&tempty[i], kPair ? 8 : 128);
-        ptx::mbar_init(&epi_done[i], 128);
+        ptx::mbar_init(&tempty[i], kPair ? 2 * kEpiWarps : 32 * kEpiWarps);
+        ptx::mbar_init(&epi_done[i], 32 * kEpiWarps);
       }
       for (int i = 0; i < C::kSlots; ++i) {
         ptx::mbar_init(&qfull[i], 1);
-        // consumers of a slot: MMA warp, 4 epilogue warps, the prefetch warp and, under
+        // consumers of a slot: MMA warp, the epilogue warps, the prefetch warp and, under
         // the sentinel policy, the two checker warps (+ the peer's loader and the same
         // warps in a pair)
-        const uint32_t nloc = CHECK ? 8u : 6u;
+        const uint32_t nloc = 2u + (uint32_t)kEpiWarps + (CHECK ? 2u : 0u);
         ptx::mbar_init(&qempty[i], kPair ? 2u * nloc + 1u : nloc);
       }
       ptx::mbar_init(mma_done, 1);
@@ -634,6 +648,8 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           trec->reloads = 0;
           trec->land_clk = 0;
           trec->check_clk = 0;
+          trec->t_acc = 0;
+          trec->t_xchg = 0;
         }
         if (SA.g.a_mode == AMODE_POINTWISE) {
           // Computed by this CTA's epilogue warps; nothing to load.  The next claim waits
@@ -969,7 +985,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         }
         ptx::tc_fence_after();
       }
-      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::kAccStride);
       const bool checked = CHECK && stage_consumes(args, tr.s);
       // The peer of a pair issues nothing: its direct copies complete on the leader's
       // `full`, and its checker arrives on the leader's `ready`.
@@ -1055,7 +1071,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       }
     }
     __syncwarp();
-  } else if (warp >= 7) {
+  } else if (CHECK && warp >= 7) {
     // ------------------------------------------------------------ sentinel checkers
     // Under the sentinel policy every consumer k-block's A tile is validated here, off the
     // MMA issuer's path, and handed to it through `ready` (the leader's, in a pair).  Two
@@ -1279,10 +1295,13 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       it0 += (uint32_t)KB;
     }
     __syncwarp();
-  } else if (warp >= 2 && warp <= 5) {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
+  } else if ((warp >= 2 && warp <= 5) || (kEpiGroups == 2 && warp >= 7 && warp <= 10)) {
+    // ------------------------------------------------------------ epilogue (warps 2..5, 7..10)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
+    const int egrp = warp >= 7 ? 1 : 0;            // this warp's group: it stores boxes egrp, egrp + kEpiGroups, ...
+    const int ew = egrp * 4 + (warp - (egrp ? 7 : 2));  // epilogue warp ordinal
+    const int et = ew * 32 + lane;                 // epilogue thread ordinal
     uint32_t tcount = 0, acount = 0, pwcount = 0;  // pwcount: pointwise tiles done
     // Attention chain: a pointwise tile (see pointwise_tile) -- out of line, so that its
     // registers do not weigh on the GEMM epilogue.
@@ -1306,14 +1325,16 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         const int64_t c1 = min(c0 + args.fill_unit_chunks, args.set_chunks);
         const uint4 v = make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
         // streaming stores: L2 keeps the lines of the stages still running, not these
-        for (int64_t c = c0 + (threadIdx.x - 64); c < c1; c += 128) __stcs(base + c, v);
+        for (int64_t c = c0 + et; c < c1; c += 32 * kEpiWarps) __stcs(base + c, v);
         continue;
       }
       const StageArgs& SA = stage_args(args, tr.s);
       const StageGeo& g = SA.g;
       if (g.a_mode == AMODE_POINTWISE) {
-        pointwise_tile(args, tr, t, (int64_t)tr.m * (128 * PAIR) + (int64_t)rank * 128 + row, pw_done, pwcount & 1u,
-                       *run_no, leader, pto, abort_flag);
+        // one token row per thread of the first group (the second has nothing to do)
+        if (egrp == 0)
+          pointwise_tile(args, tr, t, (int64_t)tr.m * (128 * PAIR) + (int64_t)rank * 128 + row, pw_done,
+                         pwcount & 1u, *run_no, leader, pto, abort_flag);
         ++pwcount;
         continue;
       }
@@ -1326,6 +1347,9 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         break;
       }
       ptx::tc_fence_after();
+      const bool tracer = args.trace && leader && threadIdx.x == 64;  // records this tile's epilogue times
+      if (tracer) args.trace[chain_tile(args, tr.q)].t_acc = ptx::globaltimer();
+      uint64_t t_xchg = 0;
 
       int64_t grow;
       bool valid;
@@ -1348,15 +1372,16 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
                                              : reinterpret_cast<__nv_bfloat16*>(SA.out);
       __nv_bfloat16* orow = obase + (valid ? grow * (int64_t)g.N : 0);
       const int32_t col0 = tr.c * g.n_out;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * C::kAccStride);
       const int nchunks = g.n_out / 32;
       // GEMM outputs leave through TMA stores of 32-row x 64-column boxes staged in this
-      // warp's two shared-memory buffers; convolution outputs (a tile's pixels are not a
-      // box of the output tensor) through 16-byte stores from registers.  Under the
+      // warp's shared-memory buffers; convolution outputs (a tile's pixels are not a box
+      // of the output tensor) through 16-byte stores from registers.  With two warps per
+      // lane quarter, each takes every other 64-column box (two 32-column chunks).  Under the
       // sentinel policy the consumer's check inspects every element it loads, so it does
       // not matter how the stores of the tile it checks are split.
       const bool tma_out = g.a_mode == AMODE_GEMM;
-      uint8_t* ebuf = epi_stage + (q * 2) * C::kEpiBufBytes;
+      uint8_t* ebuf = epi_stage + ew * kEpiBufs * C::kEpiBufBytes;
       const int32_t row_w0 = tr.m * (128 * PAIR) + (int32_t)rank * 128 + q * 32;
       // K split: unit k of a tile adds the running sum of units 0..k-1 to its fp32 partial
       // sums; the units other than the last store the result in their workspace slot, and
@@ -1427,6 +1452,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           uint4 a[8];
           split_issue(a, prev);
           split_settle(a, prev);
+          if (tracer) t_xchg = ptx::globaltimer();
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             x[4 * i + 0] = __float_as_uint(__uint_as_float(a[i].x) + __uint_as_float(x[4 * i + 0]));
@@ -1444,6 +1470,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         }
       };
       for (int j = 0; j < nchunks; ++j) {
+        if (kEpiGroups > 1 && ((j >> 1) % kEpiGroups) != egrp) continue;  // the other group's box
         uint32_t v[32];
         float f[32];
         if (g.epi == EPI_SWIGLU) {
@@ -1484,9 +1511,10 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           // bytes) with the 16-byte units permuted as the 128-byte swizzle expects, which
           // also spreads a warp's stores over all banks.
           const int box = j >> 1;
-          uint8_t* buf = ebuf + (box & 1) * C::kEpiBufBytes;
-          if ((j & 1) == 0 && box >= 2) {
-            if (lane == 0) ptx::bulk_wait_group_read<1>();  // the store that last read `buf`
+          const int lbox = box / kEpiGroups;  // this warp's box ordinal
+          uint8_t* buf = ebuf + (lbox % kEpiBufs) * C::kEpiBufBytes;
+          if ((j & 1) == 0 && lbox >= kEpiBufs) {
+            if (lane == 0) ptx::bulk_wait_group_read<kEpiBufs - 1>();  // the store that last read `buf`
             __syncwarp();
           }
 #pragma unroll
@@ -1512,6 +1540,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           }
         }
       }
+      if (tracer && t_xchg) args.trace[chain_tile(args, tr.q)].t_xchg = t_xchg;
       if (tma_out) {
         // The tile's stores have completed (not only read their source) before this warp
         // reports them done: the semaphore post below may follow right after.

@@ -137,7 +137,7 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   if (d.policy < CUSYNC_POLICY_STREAM || d.policy > CUSYNC_POLICY_SENTINEL) return CUSYNC_ERR_INVALID_ARG;
   if (d.launch != CUSYNC_LAUNCH_PERSISTENT && d.launch != CUSYNC_LAUNCH_PDL) return CUSYNC_ERR_INVALID_ARG;
   const int32_t bn = default_tile_n(d);
-  if (bn != 128 && bn != 256) return CUSYNC_ERR_UNSUPPORTED;
+  if (bn != 128 && bn != 192 && bn != 256) return CUSYNC_ERR_UNSUPPORTED;
   const bool mlp = d.kind == CUSYNC_CHAIN_MLP_GELU || d.kind == CUSYNC_CHAIN_MLP_SWIGLU;
   const bool attn = d.kind == CUSYNC_CHAIN_ATTENTION;
   const bool stack = d.kind == CUSYNC_CHAIN_CONV_STACK;
@@ -148,6 +148,9 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   const int32_t pair = d.cta_pair ? d.cta_pair : (((mlp || attn) && d.M >= 256) ? 2 : 1);
   if (pair != 1 && pair != 2) return CUSYNC_ERR_INVALID_ARG;
   if (pair == 2 && !mlp && !attn) return CUSYNC_ERR_UNSUPPORTED;  // (convolutions: single CTAs)
+  // 192-wide tiles: GeLU MLP chains on CTA pairs (a SwiGLU tile would write 96 columns, not
+  // whole 64-column store boxes)
+  if (bn == 192 && (pair != 2 || d.kind != CUSYNC_CHAIN_MLP_GELU)) return CUSYNC_ERR_UNSUPPORTED;
   std::memset(p, 0, sizeof(*p));
   p->bn = bn;
   p->pair = pair;
@@ -523,6 +526,7 @@ cudaError_t set_kernel_attrs_all_tiles() {
   cudaError_t e = set_kernel_attrs<256, 1, CHECK>();
   if (e == cudaSuccess) e = set_kernel_attrs<128, 1, CHECK>();
   if (e == cudaSuccess) e = set_kernel_attrs<256, 2, CHECK>();
+  if (e == cudaSuccess) e = set_kernel_attrs<192, 2, CHECK>();
   if (e == cudaSuccess) e = set_kernel_attrs<128, 2, CHECK>();
   return e;
 }
@@ -722,8 +726,10 @@ cudaError_t launch_chain(const ChainArgs& a, int grid, bool pdl_secondary, cudaS
 
 template <bool CHECK>
 cudaError_t launch_tiles(const Plan& p, const ChainArgs& a, int grid, bool pdl2, cudaStream_t s) {
-  if (p.pair == 2)
+  if (p.pair == 2) {
+    if (p.bn == 192) return launch_chain<192, 2, CHECK>(a, grid, pdl2, s);
     return p.bn == 256 ? launch_chain<256, 2, CHECK>(a, grid, pdl2, s) : launch_chain<128, 2, CHECK>(a, grid, pdl2, s);
+  }
   return p.bn == 256 ? launch_chain<256, 1, CHECK>(a, grid, pdl2, s) : launch_chain<128, 1, CHECK>(a, grid, pdl2, s);
 }
 
@@ -774,7 +780,10 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
 // k-blocks per pipeline stage of the kernel that runs plan p (the sentinel policy runs the
 // checked instantiation).
 int32_t kernel_kps(const Plan& p, bool check) {
-  if (p.pair == 2) return p.bn == 256 ? KCfg<256, 2>::kps(check) : KCfg<128, 2>::kps(check);
+  if (p.pair == 2) {
+    if (p.bn == 192) return KCfg<192, 2>::kps(check);
+    return p.bn == 256 ? KCfg<256, 2>::kps(check) : KCfg<128, 2>::kps(check);
+  }
   return p.bn == 256 ? KCfg<256, 1>::kps(check) : KCfg<128, 1>::kps(check);
 }
 
@@ -999,7 +1008,10 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
   if (query_num_sms(0, &dev_sms) != 0) return CUSYNC_ERR_CUDA;
   const int sms = d->num_sms > 0 ? std::min(d->num_sms, dev_sms) : dev_sms;
   if ((e = set_all_kernel_attrs()) != cudaSuccess) return cuda_fail(e, "kernel attributes");
-  const int max_clusters = p.pair == 2 ? (p.bn == 256 ? max_pair_clusters<256>() : max_pair_clusters<128>()) : 0;
+  const int max_clusters = p.pair != 2 ? 0
+                           : p.bn == 256 ? max_pair_clusters<256>()
+                           : p.bn == 192 ? max_pair_clusters<192>()
+                                         : max_pair_clusters<128>();
   if (p.pair == 2 && max_clusters < 1) {
     CUSYNC_LOG("no CTA-pair cluster can be resident on this device");
     return CUSYNC_ERR_UNSUPPORTED;
@@ -1372,7 +1384,7 @@ static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocWords];
 
 constexpr int kMaxDevices = 64;
 uint32_t* g_noalloc_ptr[kMaxDevices] = {};
-int g_noalloc_clusters[kMaxDevices][2] = {};  // co-resident CTA-pair clusters (BN 256, 128)
+int g_noalloc_clusters[kMaxDevices][3] = {};  // co-resident CTA-pair clusters (BN 256, 128, 192)
 std::mutex g_noalloc_mu;
 
 // Device address of the scratch array and the kernels' attributes for the current device,
@@ -1389,6 +1401,7 @@ cusync_status_t noalloc_setup(int dev, uint32_t** out) {
     if (e != cudaSuccess || p == nullptr) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
     g_noalloc_clusters[dev][0] = max_pair_clusters<256>();
     g_noalloc_clusters[dev][1] = max_pair_clusters<128>();
+    g_noalloc_clusters[dev][2] = max_pair_clusters<192>();
     g_noalloc_ptr[dev] = p;
   }
   *out = g_noalloc_ptr[dev];
@@ -1442,7 +1455,7 @@ extern "C" cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, 
   fill_static_args(dd, p, scratch, nullptr, A);
   A.st[0].out = H;
   A.st[1].out = Y;
-  const int max_clusters = g_noalloc_clusters[dev][p.bn == 256 ? 0 : 1];
+  const int max_clusters = g_noalloc_clusters[dev][p.bn == 256 ? 0 : (p.bn == 128 ? 1 : 2)];
   if (p.pair == 2 && max_clusters < 1) return CUSYNC_ERR_UNSUPPORTED;
   const Grids grids = make_grids(p, sms, max_clusters);
 
