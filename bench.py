@@ -95,6 +95,8 @@ def parse():
     p.add_argument("--l2-prefetch", type=int, default=0)
     p.add_argument("--cta-pair", type=int, default=0)
     p.add_argument("--ksplit", type=int, default=0, help="producer K split (0 = the planner's choice)")
+    p.add_argument("--no-run-overlap", action="store_true", help="launch each run's first kernel in plain "
+                   "stream order (CUSYNC_FLAG_NO_RUN_OVERLAP)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-per-config", action="store_true", help="skip the per-configuration table")
     p.add_argument("--no-graph", action="store_true", help="one library call per run in the timed loops "
@@ -314,7 +316,7 @@ def run_reference(a):
 class Setup:
     """Device operands and chains of one workload."""
 
-    def __init__(self, wl, inputs, tile_n, launch, raster=0, l2_prefetch=0, cta_pair=0, ksplit=0):
+    def __init__(self, wl, inputs, tile_n, launch, raster=0, l2_prefetch=0, cta_pair=0, ksplit=0, flags=0):
         import torch
         import tile_level_sync_gb300 as cs
         self.cs = cs
@@ -374,6 +376,7 @@ class Setup:
         self.l2_prefetch = l2_prefetch
         self.cta_pair = cta_pair
         self.ksplit = ksplit
+        self.flags = flags
         self.chains = {}
 
     def chain(self, policy, launch=None, tile_n=None, raster=None, l2_prefetch=None, cta_pair=None, flags=0):
@@ -386,8 +389,8 @@ class Setup:
         key = (policy, launch, tile_n, raster, l2_prefetch, cta_pair, flags)
         if key not in self.chains:
             self.chains[key] = cs.Chain(cs.make_desc(policy=policy, launch=launch, tile_n=tile_n, raster_rows=raster,
-                                                     l2_prefetch=l2_prefetch, cta_pair=cta_pair, flags=flags,
-                                                     ksplit=self.ksplit, **self.base))
+                                                     l2_prefetch=l2_prefetch, cta_pair=cta_pair,
+                                                     flags=flags | self.flags, ksplit=self.ksplit, **self.base))
         return self.chains[key]
 
     def run(self, ch):
@@ -715,7 +718,8 @@ def main():
     wl = synth.WORKLOADS[a.workload]
     inputs = synth.workload_inputs(wl, seed=0)
     launch = cs.LAUNCH_PDL if a.launch == "pdl" else cs.LAUNCH_PERSISTENT
-    setup = Setup(wl, inputs, a.tile_n, launch, a.raster, a.l2_prefetch, a.cta_pair, a.ksplit)
+    setup = Setup(wl, inputs, a.tile_n, launch, a.raster, a.l2_prefetch, a.cta_pair, a.ksplit,
+                  cs.FLAG_NO_RUN_OVERLAP if a.no_run_overlap else 0)
     flops = wl.gemm_flops()
     peaks, peak_src = load_peaks()
 

@@ -132,6 +132,11 @@ typedef enum {
                                              Synchronization": weight tiles are then
                                              loaded only after the A-tile wait */
 #define CUSYNC_FLAG_TRACE (1u << 1)       /* record a per-tile timeline (cusync_chain_trace) */
+#define CUSYNC_FLAG_NO_RUN_OVERLAP (1u << 2) /* launch a run's first kernel in plain stream order
+                                            (by default it is a programmatic dependent of the
+                                            kernel before it in the stream: its set-up overlaps
+                                            that kernel's tail, and it waits for that kernel
+                                            to complete before touching memory) */
 /* Fault injection for tests; each makes a device wait expire, never a GPU fault. */
 #define CUSYNC_DEBUG_SKIP_POST (1u << 8)     /* the producer never posts tile (0,0) */
 #define CUSYNC_DEBUG_SKIP_INIT (1u << 9)     /* SENTINEL: skip the sentinel fill */

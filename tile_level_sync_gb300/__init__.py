@@ -22,6 +22,7 @@ LAUNCH_PERSISTENT, LAUNCH_PDL = range(2)
 (OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NOMEM, ERR_TIMEOUT, ERR_DEVICE) = range(7)
 FLAG_NO_REORDER = 1 << 0
 FLAG_TRACE = 1 << 1
+FLAG_NO_RUN_OVERLAP = 1 << 2
 DEBUG_SKIP_POST = 1 << 8
 DEBUG_SKIP_INIT = 1 << 9
 DEBUG_SKIP_SPLIT = 1 << 10

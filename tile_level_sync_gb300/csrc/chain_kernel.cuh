@@ -131,7 +131,12 @@ struct ChainArgs {
   int64_t fill_unit_chunks;  // 16-byte chunks per fill unit
   int64_t set_chunks;        // 16-byte chunks of one set
   uint32_t flags_bits;
-  int32_t pdl_role;      // bit 0: trigger dependents at start; bit 1: wait on the primary at exit
+  int32_t pdl_role;      // bit 0: trigger dependents at start; bit 1: wait on the primary at exit;
+                         // bit 2: the run's first launch, started early (programmatic launch after
+                         // the kernel before it in the stream): wait for that kernel before
+                         // reading the run number or touching global memory;
+                         // bit 3: the run's last launch: trigger dependents once this CTA has
+                         // claimed its last tile
   int32_t sentinel_check;
   int32_t num_flags;     // semaphores in `flags`
   int32_t l2_prefetch;   // k-blocks the prefetch warp runs ahead of the loader (0: none)
@@ -549,8 +554,6 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
     }
   }
   if (warp == 0 && lane == 0) {
-    epoch = ptx::ld_relaxed_gpu(args.ctrl + CTRL_RUNS) + 1u;
-    *run_no = epoch;
     for (int s = args.first_stage; s <= args.last_stage; ++s) {
       const StageArgs& S = stage_args(args, s);
       ptx::prefetch_tmap(&S.tmA);
@@ -558,6 +561,13 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       if (S.g.a_mode == AMODE_GEMM) ptx::prefetch_tmap(&S.tmO);
       if (args.stack && s >= 1) break;  // the later stages of a stack share these maps
     }
+    // A run's first launch may start while the kernel before it in the stream (the last
+    // launch of the previous run, or any kernel of the caller) is finishing: everything
+    // above touches no global memory; from here on this CTA needs that kernel complete and
+    // its writes visible (CUDA-FGS §4.6.5, programmatic dependent launch).
+    if (args.pdl_role & 4) ptx::pdl_wait();
+    epoch = ptx::ld_relaxed_gpu(args.ctrl + CTRL_RUNS) + 1u;
+    *run_no = epoch;
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -937,6 +947,9 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         }
         if (!ok) break;
       }
+      // The run's last launch lets the next run's first launch start once every CTA has
+      // claimed its last tile (that launch waits for this one before it touches memory).
+      if (args.pdl_role & 8) ptx::pdl_launch_dependents();
       if (leader) {
         // The last CTA (pair) to finish claiming resets this launch's tile counter.
         __threadfence();

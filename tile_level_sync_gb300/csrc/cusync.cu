@@ -754,12 +754,17 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "sentinel fill launch");
   }
   const bool per_stage = d.policy == CUSYNC_POLICY_STREAM || d.launch == CUSYNC_LAUNCH_PDL;
+  // Unless the caller opts out, the run's first launch is a programmatic dependent of the
+  // kernel before it in the stream: its set-up overlaps that kernel's tail, and it waits
+  // for that kernel's completion before it touches memory (pdl_role bit 2); the run's last
+  // launch lets such a launch start once all of its tiles are claimed (bit 3).
+  const bool overlap = !(d.flags & CUSYNC_FLAG_NO_RUN_OVERLAP);
   if (!per_stage) {
     A.queue = 0;
     A.first_stage = 0;
     A.last_stage = p.nst - 1;
-    A.pdl_role = 0;
-    e = launch_any(p, A, g.fused, false, stream);
+    A.pdl_role = overlap ? (4 | 8) : 0;
+    e = launch_any(p, A, g.fused, overlap, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fused chain launch");
     return CUSYNC_OK;
   }
@@ -771,7 +776,9 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
     A.first_stage = s;
     A.last_stage = s;
     A.pdl_role = pdl ? ((s + 1 < p.nst ? 1 : 0) | (s > 0 ? 2 : 0)) : 0;
-    e = launch_any(p, A, g.stage[s], /*pdl2=*/pdl && s > 0, stream);
+    if (overlap && s == 0) A.pdl_role |= 4;
+    if (overlap && s == p.nst - 1) A.pdl_role |= 8;
+    e = launch_any(p, A, g.stage[s], /*pdl2=*/(pdl && s > 0) || (overlap && s == 0), stream);
     if (e != cudaSuccess) return cuda_fail(e, s == 0 ? "producer launch" : "later stage launch");
   }
   return CUSYNC_OK;
