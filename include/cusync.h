@@ -198,6 +198,12 @@ typedef struct {
                                         none on CTA pairs;
                                         none under STRIDED_TILE with more than 64 groups.
                                         1 = none */
+  int32_t bands;                     /* MLP chains: row bands of the output Y, each with a
+                                        semaphore that its consumer tiles post after their
+                                        stores, for cusync_run_mlp_bands / cusync_band_wait
+                                        (at most 16 and at most the consumer's row tiles;
+                                        row-major tile order).  0 = none */
+  int32_t _pad1;
 } cusync_chain_desc_t;
 
 /* Wave arithmetic of a two-kernel chain ([cuSync] §II-A "Thread block Wave Execution",
@@ -439,6 +445,38 @@ cusync_status_t cusync_tile_at(const cusync_chain_desc_t* d, int32_t stage, int3
 cusync_status_t cusync_run_mlp_noalloc(const cusync_chain_desc_t* d, const void* X, const void* W1t,
                                        const void* W2t, void* H, void* Y, cusync_stream_t stream,
                                        uint32_t* error_word);
+
+/* Tensor-parallel MLP shard with the reduction of its output overlapped band by band.
+ *
+ * The pages' MLP block is one shard of a tensor-parallel layer: X x W1 split by columns,
+ * x W2 split by rows, the shards' outputs summed across GPUs ([cuSync] §II-B "GPT-3", the
+ * H/8 shard of Fig. fig:gpt-3:mlp); overlapping that communication with the computation is
+ * the pages' next step ([cuSync] "Conclusion"), and [CUDA-FGS] §4.6 notes that the same
+ * readiness protocol reaches another GPU when the consumer reads at a scope that covers
+ * both.  Here each consumer tile posts its row band's semaphore after its stores, so a
+ * reduction of band b (an all-reduce across the shards, on another stream) can start
+ * while later bands are still being computed.
+ *
+ * cusync_run_mlp_bands runs the chain (chain created with desc.bands > 0) on `stream` as
+ * cusync_run_mlp does, with band semaphores cleared first; band_stream (not `stream`) is
+ * made to wait until they are cleared.  Then, for each band b in turn, the caller calls
+ * cusync_band_wait(chain, b, band_stream) and enqueues its reduction of rows
+ * cusync_band_rows(desc, b) of Y on band_stream.  After the run's kernels, `stream` runs a
+ * one-thread-block kernel that raises every band semaphore to the count of a complete run,
+ * so every band wait ends even if a tile of the run gave up waiting (reported by
+ * cusync_chain_check); normally it changes nothing.
+ *  - Before the next run of the chain, make `stream` wait for band_stream's work of this
+ *    run: the next run overwrites Y and clears the semaphores.
+ *  - Not inside CUDA stream capture (CUSYNC_ERR_UNSUPPORTED): a band wait is a stream
+ *    memory operation (cuStreamWaitValue32), which graph dependencies do not see.
+ *  - cusync_band_wait returns INVALID_ARG before a successful cusync_run_mlp_bands of the
+ *    chain, for a band out of range, and after cusync_chain_reset. */
+cusync_status_t cusync_run_mlp_bands(cusync_chain_t chain, const void* X, const void* W1t, const void* W2t,
+                                     void* H, void* Y, cusync_stream_t stream, cusync_stream_t band_stream);
+cusync_status_t cusync_band_wait(cusync_chain_t chain, int32_t band, cusync_stream_t band_stream);
+/* Rows [*row0, *row0 + *rows) of Y in band `band` of the chain described by *d (pure host
+ * computation). */
+cusync_status_t cusync_band_rows(const cusync_chain_desc_t* d, int32_t band, int64_t* row0, int64_t* rows);
 
 /* Copy the timeline of the last traced run into out[0..max) (one record per tile, in tile
  * order) after synchronising `stream`; *n_out receives the number of tiles.  INVALID_ARG

@@ -39,7 +39,7 @@ class cusync_chain_desc_t(ctypes.Structure):
         ("n", c_i32), ("h", c_i32), ("w", c_i32), ("c", c_i32), ("k_out", c_i32),
         ("tile_n", c_i32), ("strided_group", c_i32), ("flags", c_u32), ("num_sms", c_i32), ("raster_rows", c_i32),
         ("timeout_ns", c_u64), ("l2_prefetch", c_i32), ("cta_pair", c_i32), ("ksplit", c_i32),
-        ("stages", c_i32), ("ksplit_consumer", c_i32),
+        ("stages", c_i32), ("ksplit_consumer", c_i32), ("bands", c_i32), ("_pad1", c_i32),
     ]
 
 
@@ -112,6 +112,10 @@ _SIGNATURES = {
                                              ctypes.POINTER(cusync_latency_model_t)]),
     "cusync_predict_policies": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), ctypes.POINTER(cusync_latency_model_t),
                                         ctypes.POINTER(cusync_policy_prediction_t)]),
+    "cusync_run_mlp_bands": (c_i32, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "cusync_band_wait": (c_i32, [_VP, c_i32, _VP]),
+    "cusync_band_rows": (c_i32, [ctypes.POINTER(cusync_chain_desc_t), c_i32, ctypes.POINTER(c_i64),
+                                 ctypes.POINTER(c_i64)]),
     "cusync_destroy_chain": (c_i32, [_VP]),
 }
 
@@ -175,14 +179,14 @@ def status_string(status):
 
 def make_desc(kind=CHAIN_MLP_GELU, policy=POLICY_ROW, launch=LAUNCH_PERSISTENT, M=0, K=0, N1=0, N2=0,
               n=0, h=0, w=0, c=0, k_out=0, tile_n=0, strided_group=0, flags=0, num_sms=0, timeout_ns=0,
-              raster_rows=0, l2_prefetch=0, cta_pair=0, ksplit=0, stages=0, ksplit_consumer=0):
+              raster_rows=0, l2_prefetch=0, cta_pair=0, ksplit=0, stages=0, ksplit_consumer=0, bands=0):
     if isinstance(policy, str):
         policy = POLICY_NAMES[policy]
     return cusync_chain_desc_t(kind=kind, policy=policy, launch=launch, M=M, K=K, N1=N1, N2=N2, n=n, h=h, w=w,
                                c=c, k_out=k_out, tile_n=tile_n, strided_group=strided_group, flags=flags,
                                num_sms=num_sms, timeout_ns=timeout_ns, raster_rows=raster_rows,
                                l2_prefetch=l2_prefetch, cta_pair=cta_pair, ksplit=ksplit, stages=stages,
-                               ksplit_consumer=ksplit_consumer)
+                               ksplit_consumer=ksplit_consumer, bands=bands)
 
 
 # ---------------------------------------------------------------- the C functions
@@ -307,6 +311,21 @@ def cusync_run_mlp_noalloc(desc, X, W1t, W2t, H, Y, stream=None, wait=False):
     if st not in (OK, ERR_TIMEOUT, ERR_DEVICE):
         raise CusyncError(st, "cusync_run_mlp_noalloc")
     return st, (err.value if wait else None)
+
+
+def cusync_run_mlp_bands(chain, X, W1t, W2t, H, Y, band_stream, stream=None):
+    _check(load().cusync_run_mlp_bands(chain, _ptr(X), _ptr(W1t), _ptr(W2t), _ptr(H), _ptr(Y), _stream(stream),
+                                       _stream(band_stream)), "cusync_run_mlp_bands")
+
+
+def cusync_band_wait(chain, band, band_stream):
+    _check(load().cusync_band_wait(chain, band, _stream(band_stream)), "cusync_band_wait")
+
+
+def cusync_band_rows(desc, band):
+    r0, n = c_i64(), c_i64()
+    _check(load().cusync_band_rows(ctypes.byref(desc), band, ctypes.byref(r0), ctypes.byref(n)), "cusync_band_rows")
+    return r0.value, n.value
 
 
 def cusync_chain_check(chain, stream=None):

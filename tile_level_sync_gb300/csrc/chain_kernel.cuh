@@ -108,6 +108,9 @@ struct ChainArgs {
   DepCfg dep_pw;         // attention: what the pointwise stage waits for on stage 0
   uint32_t* flags;       // semaphores of `dep`
   uint32_t* flags_pw;    // semaphores of `dep_pw`
+  uint32_t* band_flags;  // MLP chains with row bands: one semaphore per band of consumer row tiles,
+                         // posted once per CTA by each consumer tile of the band after its stores
+  int32_t n_bands;
   uint32_t* ctrl;        // CTRL_* words
   TraceRec* trace;       // per-tile timeline, or null
   float* split_ws;       // K split: fp32 partial sums, per (tile, pair rank) ksplit-1 slots of 128 x BN;
@@ -1583,6 +1586,20 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       }
       if (!last_unit) {
         // K split: this unit's sums are in its workspace slot, which marks itself ready
+      } else if (args.band_flags && tr.s == args.nst - 1 && threadIdx.x == 64) {
+        // Row bands of the output: once all of this CTA's stores of the tile are complete
+        // (the epi_done barrier; TMA stores waited for and proxy-fenced by each warp), one
+        // device-scope release on the band's semaphore, so that a reduction of the band
+        // across tensor-parallel shards can start while later bands are still computed.
+        const int32_t mt = args.st[args.nst - 1].g.m_tiles;
+        const int32_t band = (int32_t)(((int64_t)(tr.m + 1) * args.n_bands - 1) / mt);
+        if (!ptx::mbar_wait_bounded(&epi_done[acc], apar, pto)) {
+          record_error(args, ERRC_PIPELINE, t, 12);
+          *abort_flag = 1;
+        } else {
+          ptx::fence_acq_rel_gpu();
+          ptx::red_release_gpu_add(args.band_flags + band, 1u);
+        }
       } else if ((args.stack ? stack_mid : tr.s == 0) && threadIdx.x == 64) {
         // stage 0 feeds the last stage (two-stage chains) or the pointwise stage (attention);
         // a stack's stage s feeds stage s + 1 through the semaphores of boundary s
@@ -1616,6 +1633,18 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
     else ptx::tmem_dealloc(tmem_base, C::kTmemCols);
   }
   if ((args.pdl_role & 2) && threadIdx.x == 0) ptx::pdl_wait();
+}
+
+// After a run with row bands: raise each band semaphore to at least the count a complete
+// run posts, so that every stream wait on a band ends even when a tile of this run gave up
+// (its timeout is reported through the error word).  Normally the run has posted them all
+// and this changes nothing.
+struct BandTargets {
+  uint32_t v[16];
+};
+__global__ void band_release_kernel(uint32_t* band_flags, BandTargets targets, int32_t n) {
+  const int32_t i = (int32_t)threadIdx.x;
+  if (i < n) atomicMax(band_flags + i, targets.v[i]);
 }
 
 // Fill a buffer with the bf16 sentinel 0x8000 using 16-byte stores (CUDA-FGS §4.6.4.2,

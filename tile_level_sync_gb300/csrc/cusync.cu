@@ -71,7 +71,14 @@ struct Plan {
   int64_t num_flags_pw;
   int64_t split_rows;   // K split: workspace row blocks (producer tiles x pair), else 0
   int64_t split_rows1;  // K split of the consumer: its row blocks, else 0
+  int32_t n_bands;      // MLP chains: row bands of the output with their own semaphore, else 0
 };
+
+// Row bands of an MLP chain's output: band b covers consumer row tiles
+// [b * m_tiles / n_bands, (b + 1) * m_tiles / n_bands) (the kernel maps a row tile to its band
+// with the inverse of this split).
+constexpr int32_t kMaxBands = 16;
+int32_t band_lo(int32_t m_tiles, int32_t n_bands, int32_t b) { return (int32_t)((int64_t)b * m_tiles / n_bands); }
 
 // Geometry of stage s.
 const StageGeo& sgeo(const Plan& p, int s) { return p.geo[p.stack ? (s > 0 ? 1 : 0) : s]; }
@@ -86,9 +93,9 @@ int64_t total_units(const Plan& p) {
 // Elements of one intermediate of a convolution stack.
 int64_t stack_buf_elems(const cusync_chain_desc_t& d) { return (int64_t)d.n * d.h * d.w * d.c; }
 
-// Words of a chain's device state: control words and semaphores.
+// Words of a chain's device state: control words, semaphores and band semaphores.
 int64_t state_words(const Plan& p) {
-  return CTRL_WORDS + p.num_flags + p.num_flags_pw;
+  return CTRL_WORDS + p.num_flags + p.num_flags_pw + p.n_bands;
 }
 // fp32 elements of the K-split workspace: ksplit - 1 slots of a 128-row accumulator per
 // row block.
@@ -336,6 +343,13 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   }
   g2.ksplit = 1;
   g2.kb_per_split = g2.k_blocks;
+  // row bands of the output (MLP chains; cusync_chain_desc_t::bands)
+  if (d.bands < 0) return CUSYNC_ERR_INVALID_ARG;
+  if (d.bands > 0) {
+    if (!mlp || d.bands > kMaxBands || d.bands > g1.m_tiles) return CUSYNC_ERR_UNSUPPORTED;
+    if (g1.raster > 1) return CUSYNC_ERR_UNSUPPORTED;  // a band's tiles are consecutive in row-major order
+    p->n_bands = d.bands;
+  }
   if (d.l2_prefetch < -1 || d.l2_prefetch > 64) return CUSYNC_ERR_INVALID_ARG;
   if (attn) {
     // the pointwise stage waits on the QKV GEMM: StridedSync with G = 3 (the Q, V and K
@@ -434,6 +448,21 @@ bool load_encoder() {
       q != cudaDriverEntryPointSuccess || fn == nullptr)
     return false;
   g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// cuStreamWaitValue32 (driver API) through the runtime's entry-point query.
+PFN_cuStreamWaitValue32_v11070 g_wait_value = nullptr;
+
+bool load_wait_value() {
+  std::lock_guard<std::mutex> lk(g_encode_mu);
+  if (g_wait_value) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuStreamWaitValue32", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  g_wait_value = reinterpret_cast<PFN_cuStreamWaitValue32_v11070>(fn);
   return true;
 }
 
@@ -536,6 +565,7 @@ cudaError_t set_all_kernel_attrs() {
   if (e == cudaSuccess) e = set_kernel_attrs_all_tiles<true>();
   cudaFuncAttributes fa;
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, sentinel_fill_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, band_release_kernel);
   return e;
 }
 
@@ -694,6 +724,8 @@ struct cusync_chain {
   ChainArgs args;
   const void* filled_ws;  // rotating sentinel stack: the workspace whose sets hold the sentinel
   bool need_fill;         // rotating sentinel stack: fill both sets before the next run
+  cudaEvent_t band_ev;    // row bands: recorded after the band semaphores are cleared for a run
+  bool bands_ready;       // row bands: a run with band semaphores was enqueued (band waits allowed)
 };
 
 namespace {
@@ -875,6 +907,8 @@ void fill_static_args(const cusync_chain_desc_t& d, const Plan& p, uint32_t* sta
   A.ctrl = state;
   A.flags = state + CTRL_WORDS;
   A.flags_pw = state + CTRL_WORDS + p.num_flags;
+  A.band_flags = p.n_bands > 0 ? state + CTRL_WORDS + p.num_flags + p.num_flags_pw : nullptr;
+  A.n_bands = p.n_bands;
   A.split_ws = p.split_rows > 0 ? split_ws : nullptr;
   A.split_ws1 = p.split_rows1 > 0 ? split_ws + split_ws_floats0(p) : nullptr;
   A.tiles0 = (int32_t)t0;
@@ -1077,6 +1111,15 @@ cusync_status_t cusync_create_chain(const cusync_chain_desc_t* d, cusync_chain_t
   ch->maps_valid = false;
   ch->filled_ws = nullptr;
   ch->need_fill = true;
+  ch->band_ev = nullptr;
+  ch->bands_ready = false;
+  if (p.n_bands > 0 && (e = cudaEventCreateWithFlags(&ch->band_ev, cudaEventDisableTiming)) != cudaSuccess) {
+    if (ch->trace) cudaFree(ch->trace);
+    if (ch->split_ws) cudaFree(ch->split_ws);
+    cudaFree(ch->state);
+    delete ch;
+    return cuda_fail(e, "band event");
+  }
   *out = ch;
   CUSYNC_LOG("chain kind=%d policy=%d launch=%d tiles=%d+%d bn=%d pair=%d sms=%d clusters=%d flags=%lld", d->kind,
              d->policy, d->launch, A.tiles0, A.tiles1, p.bn, p.pair, sms, max_clusters, (long long)p.num_flags);
@@ -1124,6 +1167,7 @@ cusync_status_t cusync_chain_reset(cusync_chain_t ch, cusync_stream_t stream) {
     if (e != cudaSuccess) return cuda_fail(e, "K-split workspace reset");
   }
   ch->need_fill = true;  // a run that stopped early may have left the next set unfilled
+  ch->bands_ready = false;
   return CUSYNC_OK;
 }
 
@@ -1343,6 +1387,80 @@ cusync_status_t cusync_producer_col(const cusync_chain_desc_t* d, int32_t y, int
   return CUSYNC_OK;
 }
 
+// Posts a complete run makes on band b's semaphore: one per CTA of every consumer tile in
+// the band (the last K-split unit of a tile posts).
+static uint32_t band_posts(const Plan& p, int32_t b) {
+  const StageGeo& g = p.geo[1];
+  const int32_t rows = band_lo(g.m_tiles, p.n_bands, b + 1) - band_lo(g.m_tiles, p.n_bands, b);
+  return (uint32_t)rows * (uint32_t)g.n_tiles * (uint32_t)p.pair;
+}
+
+static bool stream_capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  return cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone;
+}
+
+cusync_status_t cusync_run_mlp_bands(cusync_chain_t ch, const void* X, const void* W1t, const void* W2t, void* H,
+                                     void* Y, cusync_stream_t stream, cusync_stream_t band_stream) {
+  if (!ch) return CUSYNC_ERR_INVALID_ARG;
+  if (ch->d.kind != CUSYNC_CHAIN_MLP_GELU && ch->d.kind != CUSYNC_CHAIN_MLP_SWIGLU) return CUSYNC_ERR_INVALID_ARG;
+  const Plan& p = ch->plan;
+  if (p.n_bands < 1) return CUSYNC_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t bs = reinterpret_cast<cudaStream_t>(band_stream);
+  if (s == bs) return CUSYNC_ERR_INVALID_ARG;
+  // band waits are stream memory operations that CUDA's graph dependencies do not see
+  if (stream_capturing(s) || stream_capturing(bs)) return CUSYNC_ERR_UNSUPPORTED;
+  if (!load_wait_value()) return CUSYNC_ERR_UNSUPPORTED;
+  ch->bands_ready = false;
+  uint32_t* const bands = ch->args.band_flags;
+  cudaError_t e = cudaMemsetAsync(bands, 0, (size_t)p.n_bands * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return cuda_fail(e, "band semaphores clear");
+  if ((e = cudaEventRecord(ch->band_ev, s)) != cudaSuccess) return cuda_fail(e, "band event record");
+  const cusync_status_t st = run_chain(ch, X, W1t, W2t, H, nullptr, Y, s);
+  BandTargets tg;
+  std::memset(&tg, 0, sizeof(tg));
+  for (int32_t b = 0; b < p.n_bands; ++b) tg.v[b] = band_posts(p, b);
+  // launched whatever the run's launch status, so that band waits always end
+  band_release_kernel<<<1, 32, 0, s>>>(bands, tg, p.n_bands);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "band release launch");
+  if (st != CUSYNC_OK) return st;
+  // the band stream's waits start only once this run's band semaphores are cleared
+  if ((e = cudaStreamWaitEvent(bs, ch->band_ev, 0)) != cudaSuccess) return cuda_fail(e, "band stream wait");
+  ch->bands_ready = true;
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_band_wait(cusync_chain_t ch, int32_t band, cusync_stream_t band_stream) {
+  if (!ch || !ch->bands_ready) return CUSYNC_ERR_INVALID_ARG;
+  const Plan& p = ch->plan;
+  if (band < 0 || band >= p.n_bands) return CUSYNC_ERR_INVALID_ARG;
+  cudaStream_t bs = reinterpret_cast<cudaStream_t>(band_stream);
+  if (stream_capturing(bs)) return CUSYNC_ERR_UNSUPPORTED;
+  const CUresult r = g_wait_value(reinterpret_cast<CUstream>(bs),
+                                  reinterpret_cast<CUdeviceptr>(ch->args.band_flags + band), band_posts(p, band),
+                                  CU_STREAM_WAIT_VALUE_GEQ);
+  if (r != CUDA_SUCCESS) {
+    CUSYNC_LOG("cuStreamWaitValue32: error %d", (int)r);
+    return CUSYNC_ERR_CUDA;
+  }
+  return CUSYNC_OK;
+}
+
+cusync_status_t cusync_band_rows(const cusync_chain_desc_t* d, int32_t band, int64_t* row0, int64_t* rows) {
+  if (!d || !row0 || !rows) return CUSYNC_ERR_INVALID_ARG;
+  Plan p;
+  cusync_status_t st = make_plan(*d, &p);
+  if (st != CUSYNC_OK) return st;
+  if (p.n_bands < 1 || band < 0 || band >= p.n_bands) return CUSYNC_ERR_INVALID_ARG;
+  const int64_t tm = (int64_t)kBM * p.pair;
+  const int64_t r0 = band_lo(p.geo[1].m_tiles, p.n_bands, band) * tm;
+  const int64_t r1 = std::min<int64_t>((int64_t)band_lo(p.geo[1].m_tiles, p.n_bands, band + 1) * tm, p.geo[1].M);
+  *row0 = r0;
+  *rows = r1 - r0;
+  return CUSYNC_OK;
+}
+
 cusync_status_t cusync_chain_trace(cusync_chain_t ch, cusync_stream_t stream, cusync_trace_rec_t* out, int32_t max,
                                    int32_t* n_out) {
   static_assert(sizeof(cusync_trace_rec_t) == sizeof(TraceRec), "trace record layout");
@@ -1362,6 +1480,7 @@ cusync_status_t cusync_destroy_chain(cusync_chain_t ch) {
   cudaError_t e = cudaSuccess;
   if (ch->trace) cudaFree(ch->trace);
   if (ch->split_ws) cudaFree(ch->split_ws);
+  if (ch->band_ev) cudaEventDestroy(ch->band_ev);
   if (ch->state) e = cudaFree(ch->state);
   delete ch;
   return e == cudaSuccess ? CUSYNC_OK : CUSYNC_ERR_CUDA;
