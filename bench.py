@@ -642,7 +642,7 @@ def per_config(torch, cs, synth, peaks):
         setup = Setup(wl, inputs, 0, cs.LAUNCH_PERSISTENT)
         flops = wl.gemm_flops()
         n = 40 if flops > 1e11 else 200
-        us, identical, ref = {}, True, None
+        us, identical, ref, graphs = {}, True, None, {}
         for pol in ("STREAM", "ROW", "TILE", "STRIDED", "SENTINEL"):
             for launch in (cs.LAUNCH_PERSISTENT, cs.LAUNCH_PDL):
                 if pol == "STREAM" and launch == cs.LAUNCH_PDL:
@@ -659,12 +659,30 @@ def per_config(torch, cs, synth, peaks):
                     us[key] = f"{cs.status_string(st)} 0x{code:08x}"
                     identical = False
                     continue
-                us[key] = time_runs(torch, setup, ch, n) * 1e3
                 hb, yb = setup.h.view(torch.int16), setup.y.view(torch.int16)
                 if ref is None:
                     ref = (hb.clone(), yb.clone())
                 elif not (torch.equal(hb, ref[0]) and torch.equal(yb, ref[1])):
                     identical = False
+                graphs[key] = ChainGraph(torch, setup, ch, n)
+                graphs[key].replay()   # uploads the graph: untimed
+        # the variants in turn, several rounds, each variant's median: clock and power
+        # state drift between back-to-back measurements would otherwise favour whichever
+        # variant runs first
+        s = torch.cuda.current_stream()
+        samples = {k: [] for k in graphs}
+        for _ in range(5):
+            for key, g in graphs.items():
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record(s)
+                g.replay()
+                e1.record(s)
+                torch.cuda.synchronize()
+                samples[key].append(e0.elapsed_time(e1) / n * 1e3)
+        for key, v in samples.items():
+            us[key] = statistics.median(v)
+        del graphs
         timed = {k: v for k, v in us.items() if isinstance(v, float)}
         sync = {k: v for k, v in timed.items() if k != "STREAM"}
         best = min(sync, key=sync.get)
@@ -681,7 +699,8 @@ def per_config(torch, cs, synth, peaks):
             "stream_us": timed.get("STREAM"), "speedup_vs_stream": timed["STREAM"] / sync[best] if "STREAM" in timed
             else None, "tflops": tflops, "pct_bf16_peak_measured": tflops / peaks["bf16_tflops"] * 100,
             "tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "cta_pair": info.cta_pair, "ksplit": info.ksplit,
-            "us": us, "runs_timed": n, "bit_identical_all_variants": identical,
+            "us": us, "runs_timed": n, "timing": "median of 5 rounds over the variants in turn",
+            "bit_identical_all_variants": identical,
             "parity_sampled": parity, "parity_sample": sample,
             "waves_148": {"tbs": list(w148.tbs), "waves": list(w148.waves), "stream_waves": w148.stream_waves,
                           "fused_waves": w148.fused_waves, "last_wave_tbs": w148.last_wave_tbs,

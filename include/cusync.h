@@ -160,8 +160,10 @@ typedef struct {
   uint32_t flags;                    /* CUSYNC_FLAG_* | CUSYNC_DEBUG_* */
   int32_t num_sms;                   /* SMs the kernels may use; 0 = all of the device */
   int32_t raster_rows;               /* tile order: row tiles per raster group (columns
-                                        outer, rows inner within a group); 0 or 1 =
-                                        plain row-major */
+                                        outer, rows inner within a group); 1 = plain
+                                        row-major; 0 = planner: half the row tiles for an
+                                        MLP chain on CTA pairs with at least four row
+                                        tiles and no row bands, else row-major */
   uint64_t timeout_ns;               /* bound of every device wait on a semaphore or a
                                         sentinel; 0 = 1e9 (one second) */
   int32_t l2_prefetch;               /* k-blocks a prefetch warp runs ahead of the TMA
@@ -271,6 +273,8 @@ typedef struct {
                                  bf16 per buffer) */
   int32_t ksplit_consumer;    /* K-split units per consumer tile (1 = none) */
   int32_t kb_per_split_consumer;
+  int32_t raster_rows;        /* row tiles per group of the tile order (1 = row-major) */
+  int32_t _pad;
 } cusync_chain_info_t;
 
 /* Latency model of one chain run, in nanoseconds (cusync_predict_policies).  A tile

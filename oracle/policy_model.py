@@ -20,8 +20,9 @@ The model written out here, step by step:
   k_blocks(s) x kblock_ns[s] of main loop, then epilogue_ns[s]; a persistent CTA starts
   its next tile's main loop when the previous one ends, and a tile's epilogue starts
   after both its main loop and the CTA's previous epilogue have finished;
-* the queue holds the producer tiles (row-major; StridedSync visits each group's
-  columns one after another) before the consumer tiles (row-major); CTA q takes tile q
+* the queue holds the producer tiles (row-major, or row tiles taken in groups with the
+  column outer within a group; StridedSync visits each group's columns one after
+  another) before the consumer tiles (in the same row order); CTA q takes tile q
   first, and every later tile goes to the CTA whose main loop frees up first (the lowest
   index on a tie);
 * with a K split of S, each producer tile is S consecutive queue entries; entry k runs
@@ -177,16 +178,27 @@ def predict_fused(chain, policy, slots, model):
     return end
 
 
-def gemm_chain(M, N1, N2, tile_n, n_out, pair, policy, G=2):
-    """Queue order of an MLP chain's tiles ([cuSync] §IV-C row-major; StridedSync's
-    producer order) and its dependency geometry."""
+def _grouped_rows(mt, nt, raster):
+    """(row, column position) in queue order: row tiles taken in groups of `raster`, the
+    column position outer and the row inner within a group; raster = 1 is row-major
+    ([cuSync] §IV-C, tile processing order)."""
+    out = []
+    for g0 in range(0, mt, raster):
+        rows = range(g0, min(g0 + raster, mt))
+        out += [(m, y) for y in range(nt) for m in rows]
+    return out
+
+
+def gemm_chain(M, N1, N2, tile_n, n_out, pair, policy, G=2, raster=1):
+    """Queue order of an MLP chain's tiles ([cuSync] §IV-C row-major, or grouped rows;
+    StridedSync's producer order) and its dependency geometry."""
     bm = 128 * pair
     mt = -(-M // bm)
     nt0 = -(-N1 // n_out)
     nt1 = -(-N2 // tile_n)
     order = deps.strided_producer_order(nt0, G) if policy == "STRIDED" else list(range(nt0))
-    prod = [(m, order[y]) for m in range(mt) for y in range(nt0)]
-    cons = [m for m in range(mt) for _ in range(nt1)]
+    prod = [(m, order[y]) for m, y in _grouped_rows(mt, nt0, raster)]
+    cons = [m for m, _ in _grouped_rows(mt, nt1, raster)]
     return prod, cons, deps.GemmChain(M=M, N1=N1, BM=bm, BNo=n_out, BK=64)
 
 

@@ -593,3 +593,19 @@ def test_noalloc_refuses_k_split():
                          ksplit=ks, ksplit_consumer=ks1, num_sms=148)
         st = lib.cusync_run_mlp_noalloc(ctypes.byref(d), None, None, None, None, None, None, None)
         assert st == cs.ERR_UNSUPPORTED, (ks, ks1, cs.status_string(st))
+
+
+@pytest.mark.parametrize("M,pair,bands,group", [(1024, 2, 0, 2), (2048, 2, 0, 4), (4096, 2, 0, 8), (512, 2, 0, 1),
+                                                (1024, 1, 0, 1), (1024, 2, 2, 1)])
+def test_planner_default_tile_order(M, pair, bands, group):
+    """The planner groups half of the row tiles (columns outer, rows inner) for MLP chains
+    on CTA pairs with at least four row tiles and no row bands; row-major otherwise."""
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, K=512, N1=1024, N2=512, cta_pair=pair, num_sms=148,
+                     bands=bands)
+    info = cs.cusync_plan_info(d)
+    for stage in (0, 1):
+        order = [cs.cusync_tile_at(d, stage, u) for u in range(info.m_tiles[stage] * info.n_tiles[stage])]
+        # the first `group` positions walk down the rows of column 0
+        assert order[:group] == [(m, 0) for m in range(group)]
+        if group < info.m_tiles[stage]:
+            assert order[group] == (0, 1) if group > 1 else order[1] == (0, 1)

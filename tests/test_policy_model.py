@@ -90,7 +90,7 @@ def _oracle_predict(desc, info, model, policy):
         h_mb = desc.n * desc.h * desc.w * desc.k_out * 2 / 1e6
     else:
         prod, cons, dc = pm.gemm_chain(desc.M, desc.N1, desc.N2, info.tile_n, n_out, info.cta_pair, policy,
-                                       G=info.strided_group if policy == "STRIDED" else 2)
+                                       G=info.strided_group if policy == "STRIDED" else 2, raster=info.raster_rows)
         h_mb = desc.M * desc.N1 * 2 / 1e6
     G = info.strided_group if policy == "STRIDED" else 1
     ch = pm.Chain(prod, cons, tuple(info.k_blocks), dc, G=G, h_mb=h_mb, ksplit=info.ksplit,
@@ -189,3 +189,19 @@ def test_k_split_closed_form():
     want = max(u1 + 7 + 100, cons_start) + 4 * 20 + 3
     want = max(want, u0) + 40
     assert pm.predict_fused(ch, "ROW", 2, m) == pytest.approx(want, rel=1e-12)
+
+
+def test_grouped_queue_order():
+    """The oracle model's queue order with row tiles in groups (column outer, row inner
+    within a group), written out by hand for 3 row tiles x 2 columns in groups of 2, and
+    equal to the library's tile order for the planner's groups."""
+    assert pm._grouped_rows(3, 2, 2) == [(0, 0), (1, 0), (0, 1), (1, 1), (2, 0), (2, 1)]
+    assert pm._grouped_rows(2, 3, 1) == [(0, 0), (0, 1), (0, 2), (1, 0), (1, 1), (1, 2)]
+    for M in (1024, 2048, 1280):
+        d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=M, K=256, N1=1024, N2=512, cta_pair=2, num_sms=148)
+        info = cs.cusync_plan_info(d)
+        assert info.raster_rows == (info.m_tiles[0] // 2 if info.m_tiles[0] >= 4 else 1)
+        for stage in (0, 1):
+            mt, nt = info.m_tiles[stage], info.n_tiles[stage]
+            lib = [cs.cusync_tile_at(d, stage, u) for u in range(mt * nt)]
+            assert lib == pm._grouped_rows(mt, nt, info.raster_rows)

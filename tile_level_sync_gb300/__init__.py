@@ -69,6 +69,7 @@ class cusync_chain_info_t(ctypes.Structure):
         ("nst", c_i32), ("m_tiles2", c_i32), ("n_tiles2", c_i32), ("k_blocks2", c_i32), ("n_out2", c_i32),
         ("grid2", c_i32), ("num_flags_pw", c_i32), ("strided_group_pw", c_i32), ("strided_distance_pw", c_i32),
         ("work_buffers", c_i32), ("work_bytes", c_i64), ("ksplit_consumer", c_i32), ("kb_per_split_consumer", c_i32),
+        ("raster_rows", c_i32), ("_pad", c_i32),
     ]
 
 
