@@ -164,8 +164,9 @@ struct KCfg {
   // port and tensor rates.  A single CTA keeps one k-block per stage: its stages of two
   // k-blocks measured 5-10% slower on the attention and convolution chains (a drained
   // stage is refilled only once both of its k-blocks are consumed, which leaves fewer
-  // bytes in flight), as do the sentinel-checked kernels.
-  __host__ __device__ static constexpr int kps(bool check) { return (!check && PAIR == 2 && kStages >= 6) ? 2 : 1; }
+  // bytes in flight).  Sentinel-checked pair kernels take two k-blocks per stage too: both
+  // checker warps then scan every stage, one k-block each.
+  __host__ __device__ static constexpr int kps(bool check) { return (PAIR == 2 && kStages >= 6) ? 2 : 1; }
   // Two fp32 accumulators of BN columns, kAccStride columns apart.  A TMEM allocation is
   // a power of two of columns: a 192-wide tile's accumulators start at columns 0 and 256
   // of a 512-column allocation.
@@ -490,6 +491,10 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
   volatile uint8_t* stage_kind = reinterpret_cast<volatile uint8_t*>(run_no + 1);
   // pair, sentinel check: words the peer's checker stores into to signal `ready` (S <= 8)
   uint32_t* ready_sink = const_cast<uint32_t*>(run_no + 3);
+  // sentinel check with two k-blocks per stage: each checker warp's finding per round (two
+  // rounds in turn), and the barrier both warps arrive on once they wrote it
+  volatile uint32_t* scan_flag = run_no + 11;  // [2][2]
+  uint64_t* scan_done = reinterpret_cast<uint64_t*>(const_cast<uint32_t*>(run_no + 16));  // 8-byte aligned
   uint8_t* epi_stage = smem + S * C::kStageBytes + 1024;  // 1024-byte aligned TMA store boxes
 
   // Stage st holds its k-blocks' A tiles one after the other, then their B tiles (the
@@ -542,6 +547,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       }
       ptx::mbar_init(mma_done, 1);
       ptx::mbar_init(pw_done, 128);
+      ptx::mbar_init(scan_done, 2);
       *abort_flag = 0;
       *it_issued = 0;
       *progress = 0;
@@ -1090,50 +1096,50 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
   } else if (CHECK && warp >= 7) {
     // ------------------------------------------------------------ sentinel checkers
     // Under the sentinel policy every consumer k-block's A tile is validated here, off the
-    // MMA issuer's path, and handed to it through `ready` (the leader's, in a pair).  Two
-    // warps share the work: warp 7 owns the even stages, warp 8 the odd ones (the stage
-    // count is even, so a stage always belongs to the same warp and each warp's barrier
-    // phases are its own).
-    static_assert(S % 2 == 0, "the checkers split the stages by parity");
-    static_assert(!CHECK || KPS == 1, "checked kernels load one k-block per stage");
+    // MMA issuer's path, and handed to it through `ready` (the leader's, in a pair).  With
+    // one k-block per stage (single CTAs) warp 7 owns the even stages, warp 8 the odd ones
+    // (the stage count is even, so a stage always belongs to the same warp and each warp's
+    // barrier phases are its own); with two k-blocks per stage (pairs) both warps take
+    // every stage (below).
     const int ck = warp - 7;
-    if constexpr (CHECK) {
-      const uint64_t pol_a = ptx::l2_policy_evict_last();
+    const uint64_t pol_a = ptx::l2_policy_evict_last();
+    // Whether k-block h of the A tile in stage sx still holds the sentinel anywhere (all
+    // lanes).  Every bf16 element of the landed tile is inspected.  The PTX memory model
+    // treats a vector store as independent scalar stores in no fixed order, so a copy that
+    // overlaps the producer's 128-bit store of a chunk may bring some of its words written
+    // and others not; a sampled word would then pass a chunk that is partly sentinel.
+    // Scanning every word makes the check independent of how the producer's stores are
+    // split: any element still holding 0x8000 sends the tile back.  Lane l reads 16-byte
+    // chunk c = 32 i + l, so a warp's load covers 512 contiguous bytes without bank
+    // conflicts.  Shared-memory loads are slow to return while TMA writes and the MMAs
+    // read the same memory, so all of a 16 KB tile's loads (32 per lane) are issued before
+    // the first one is tested.
+    auto stage_has_sentinel = [&](int sx, int h, uint32_t nbytes) -> bool {
+      uint32_t sbits = 0;
+      const uint8_t* base = smem_a(sx, h);
+      const uint32_t nchunks = nbytes / 16u;
+      for (uint32_t c0 = (uint32_t)lane; c0 < nchunks; c0 += 32u * 32u) {
+        uint4 v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const uint32_t c = c0 + (uint32_t)j * 32u;
+          v[j] = c < nchunks ? ptx::ld_shared_v4(base + c * 16u) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          sbits |= sentinel_bits_bf16x2(v[j].x) | sentinel_bits_bf16x2(v[j].y) | sentinel_bits_bf16x2(v[j].z) |
+                   sentinel_bits_bf16x2(v[j].w);
+      }
+      return __any_sync(FULL, (sbits & 0x80008000u) != 0u);
+    };
+    if constexpr (CHECK && KPS == 1) {
+      static_assert(S % 2 == 0, "the checkers split the stages by parity");
       uint32_t it = 0, tcount = 0;
       uint32_t cpar = 0;  // parity of each stage's next `cfull` phase
       // Stages of later k-blocks of the current tile that were found landed and clean
       // while an earlier one was reloaded (their cfull phase is consumed).
       uint32_t clean_ahead = 0;
       bool ok = true;
-      // Whether the A tile in stage sx still holds the sentinel anywhere (all lanes).
-      // Every bf16 element of the landed tile is inspected.  The PTX memory model treats
-      // a vector store as independent scalar stores in no fixed order, so a copy that
-      // overlaps the producer's 128-bit store of a chunk may bring some of its words
-      // written and others not; a sampled word would then pass a chunk that is partly
-      // sentinel.  Scanning every word makes the check independent of how the producer's
-      // stores are split: any element still holding 0x8000 sends the tile back.  Lane l
-      // reads 16-byte chunk c = 32 i + l, so a warp's load covers 512 contiguous bytes
-      // without bank conflicts.  Shared-memory loads are slow to return while TMA writes
-      // and the MMAs read the same memory, so all of a 16 KB tile's loads (32 per lane)
-      // are issued before the first one is tested.
-      auto stage_has_sentinel = [&](int sx, uint32_t nbytes) -> bool {
-        uint32_t sbits = 0;
-        const uint8_t* base = smem_a(sx);
-        const uint32_t nchunks = nbytes / 16u;
-        for (uint32_t c0 = (uint32_t)lane; c0 < nchunks; c0 += 32u * 32u) {
-          uint4 v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const uint32_t c = c0 + (uint32_t)j * 32u;
-            v[j] = c < nchunks ? ptx::ld_shared_v4(base + c * 16u) : make_uint4(0u, 0u, 0u, 0u);
-          }
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            sbits |= sentinel_bits_bf16x2(v[j].x) | sentinel_bits_bf16x2(v[j].y) | sentinel_bits_bf16x2(v[j].z) |
-                     sentinel_bits_bf16x2(v[j].w);
-        }
-        return __any_sync(FULL, (sbits & 0x80008000u) != 0u);
-      };
       while (ok) {
         const int slot = tcount % C::kSlots;
         if (!xwait<PAIR>(&qfull[slot], (tcount / C::kSlots) & 1u, pto)) {
@@ -1173,7 +1179,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
             uint64_t t0 = 0;
             bool reloaded = false;
             while (true) {
-              if (!stage_has_sentinel(st, abytes)) break;
+              if (!stage_has_sentinel(st, 0, abytes)) break;
               if (ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u) break;
               const uint64_t now = ptx::globaltimer();
               if (t0 == 0) t0 = now;
@@ -1209,7 +1215,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
                 if (lane == 0) landed = ptx::mbar_test_wait(&cfull[sj], (cpar >> sj) & 1u);
                 if (!__shfl_sync(FULL, landed ? 1 : 0, 0)) continue;
                 cpar ^= 1u << sj;
-                if (stage_has_sentinel(sj, abytes)) {
+                if (stage_has_sentinel(sj, 0, abytes)) {
                   if (lane == 0) {
                     ptx::fence_proxy_async_smem();
                     ptx::mbar_arrive_expect_tx(&cfull[sj], abytes);
@@ -1251,6 +1257,122 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           for (uint32_t j = it; j < issued && j < it + S; ++j) {
             const int st = (int)(j % S);
             if ((st & 1) != ck || stage_kind[st] != 1 || ((clean_ahead >> st) & 1u)) continue;
+            ptx::mbar_wait_bounded(&cfull[st], (cpar >> st) & 1u, pto);
+            cpar ^= 1u << st;
+          }
+        }
+      }
+    } else if constexpr (CHECK) {
+      // Two k-blocks per stage: warp 7 + h scans k-block h of every checked stage.  The two
+      // warps combine their findings each round through scan_flag and the scan_done
+      // barrier (bounded waits, one arrival per warp); warp 7 alone decides to reload the
+      // stage's A box or to give up after the timeout, and hands the clean stage to the
+      // MMA issuer.  Both warps follow every stage and round, so their barrier phases agree.
+      uint32_t it = 0, tcount = 0, cpar = 0, xround = 0;
+      bool ok = true;
+      while (ok) {
+        const int slot = tcount % C::kSlots;
+        if (!xwait<PAIR>(&qfull[slot], (tcount / C::kSlots) & 1u, pto)) {
+          ok = false;
+          break;
+        }
+        const int32_t t = qtile[slot];
+        __syncwarp();
+        if (lane == 0) ring_release(slot);
+        ++tcount;
+        if (t < 0) break;
+        const TileRef tr = decode_tile(args, t);
+        if (tr.s == kFillStage) continue;
+        const StageArgs& SA = stage_args(args, tr.s);
+        const StageGeo& g = SA.g;
+        if (g.a_mode == AMODE_POINTWISE) continue;
+        const int32_t NSK = (tr.nkb + KPS - 1) / KPS;
+        if (!stage_consumes(args, tr.s)) {
+          it += (uint32_t)NSK;  // loaded on `full`, consumed by the MMA issuer alone
+          continue;
+        }
+        const uint32_t abytes = a_tile_bytes(g);
+        const int32_t a_row = tr.m * (128 * PAIR) + (int32_t)rank * 128;
+        uint32_t check_clk = 0, reloads = 0;
+        for (int32_t sj = 0; sj < NSK; ++sj, ++it) {
+          const int st = (int)(it % NS);
+          const int32_t kb = sj * KPS;
+          const int32_t nk = min(KPS, tr.nkb - kb);
+          if (!ptx::mbar_wait_bounded(&cfull[st], (cpar >> st) & 1u, pto)) {
+            ok = false;
+            break;
+          }
+          cpar ^= 1u << st;
+          const uint32_t c1 = args.trace ? (uint32_t)clock64() : 0u;
+          uint64_t t0 = 0;
+          while (true) {
+            // this warp's k-block (only those of the unit: a box may reach into the next)
+            const bool dirty = ck < nk && stage_has_sentinel(st, ck, abytes);
+            bool late = false;
+            if (ck == 0 && t0 != 0)
+              late = ptx::globaltimer() - t0 > args.timeout_ns || ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u;
+            if (lane == 0) {
+              scan_flag[(xround & 1u) * 2u + (uint32_t)ck] = (dirty ? 1u : 0u) | (late ? 2u : 0u);
+              ptx::mbar_arrive(scan_done);
+            }
+            if (!ptx::mbar_wait_bounded(scan_done, xround & 1u, pto)) {
+              ok = false;
+              break;
+            }
+            const uint32_t f0 = scan_flag[(xround & 1u) * 2u], f1 = scan_flag[(xround & 1u) * 2u + 1u];
+            ++xround;
+            if (((f0 | f1) & 1u) == 0u) break;  // the stage is clean
+            if (f0 & 2u) {
+              if (ck == 0 && lane == 0) record_error(args, ERRC_SENTINEL_TIMEOUT, t, kb);
+              break;
+            }
+            if (t0 == 0) t0 = ptx::globaltimer();
+            // Load the stage's A box again (warp 7); both warps wait for it to land.
+            if (ck == 0 && lane == 0) {
+              __nanosleep(128);
+              ptx::fence_proxy_async_smem();
+              if (SA.a3d) {
+                ptx::mbar_arrive_expect_tx(&cfull[st], (uint32_t)KPS * abytes);
+                ptx::tma_load_3d(smem_a(st), &SA.tmA, &cfull[st], 0, a_row, tr.kb0 + kb, pol_a);
+              } else {
+                ptx::mbar_arrive_expect_tx(&cfull[st], (uint32_t)nk * abytes);
+                for (int h = 0; h < nk; ++h)
+                  ptx::tma_load_2d(smem_a(st, h), &SA.tmA, &cfull[st], (tr.kb0 + kb + h) * kBK, a_row, pol_a);
+              }
+            }
+            ++reloads;
+            __syncwarp();
+            if (!ptx::mbar_wait_bounded(&cfull[st], (cpar >> st) & 1u, pto)) {
+              ok = false;
+              break;
+            }
+            cpar ^= 1u << st;
+          }
+          if (!ok) break;
+          if (args.trace) check_clk += (uint32_t)clock64() - c1;
+          // Hand the checked stage to the MMA issuer (warp 7; see the one-k-block path).
+          __syncwarp();
+          if (ck == 0 && lane == 0) {
+            if (leader) ptx::mbar_arrive_expect_tx(&ready[st], 4u);
+            else ptx::st_async_u32(ptx::mapa(&ready_sink[st], 0), 1u, ptx::mapa(&ready[st], 0));
+          }
+        }
+        if (!ok) break;
+        if (args.trace && leader && lane == 0) {
+          TraceRec* r = args.trace + chain_tile(args, tr.q);
+          atomicAdd(&r->check_clk, check_clk);
+          if (ck == 0) atomicAdd(&r->reloads, reloads);
+        }
+      }
+      if (!ok) {
+        record_error(args, ERRC_PIPELINE, 0xFFFFFF, 10);
+        *abort_flag = 1;
+        // wait (bounded) for copies on `cfull` that were issued but not consumed
+        if (ck == 0 && lane == 0) {
+          const uint32_t issued = (uint32_t)*it_issued;
+          for (uint32_t j = it; j < issued && j < it + NS; ++j) {
+            const int st = (int)(j % NS);
+            if (stage_kind[st] != 1) continue;
             ptx::mbar_wait_bounded(&cfull[st], (cpar >> st) & 1u, pto);
             cpar ^= 1u << st;
           }
