@@ -174,10 +174,12 @@ struct KCfg {
   static constexpr int kTmemCols = 2 * kAccStride;
   static constexpr int kSlots = 4;                   // tile hand-off ring
   // Warps: 0 loader, 1 MMA, 2..5 epilogue, 6 prefetch; then, under the sentinel policy,
-  // 7..8 the checkers, otherwise 7..10 a second group of epilogue warps (two warps per
-  // TMEM lane quarter, each storing every other 64-column box of a tile).
+  // the checkers (7..8 on single CTAs, 7..10 on CTA pairs, whose stages hold two k-blocks:
+  // each checker scans half of one), otherwise 7..10 a second group of epilogue warps (two
+  // warps per TMEM lane quarter, each storing every other 64-column box of a tile).
   __host__ __device__ static constexpr int epi_warps(bool check) { return check ? 4 : 8; }
-  static constexpr int threads(bool check) { return check ? 288 : 352; }
+  __host__ __device__ static constexpr int check_warps() { return PAIR == 2 ? 4 : 2; }
+  static constexpr int threads(bool check) { return check ? 32 * (7 + check_warps()) : 352; }
   // epilogue staging for TMA stores: 32-row x 64-column bf16 boxes, 32 KB in all (two
   // boxes per epilogue warp with four warps, one with eight)
   static constexpr int kEpiBufBytes = 32 * 64 * 2;
@@ -492,9 +494,9 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
   // pair, sentinel check: words the peer's checker stores into to signal `ready` (S <= 8)
   uint32_t* ready_sink = const_cast<uint32_t*>(run_no + 3);
   // sentinel check with two k-blocks per stage: each checker warp's finding per round (two
-  // rounds in turn), and the barrier both warps arrive on once they wrote it
-  volatile uint32_t* scan_flag = run_no + 11;  // [2][2]
-  uint64_t* scan_done = reinterpret_cast<uint64_t*>(const_cast<uint32_t*>(run_no + 16));  // 8-byte aligned
+  // rounds in turn), and the barrier the checkers arrive on once they wrote it
+  volatile uint32_t* scan_flag = run_no + 11;  // [2][4]
+  uint64_t* scan_done = reinterpret_cast<uint64_t*>(const_cast<uint32_t*>(run_no + 20));  // 8-byte aligned
   uint8_t* epi_stage = smem + S * C::kStageBytes + 1024;  // 1024-byte aligned TMA store boxes
 
   // Stage st holds its k-blocks' A tiles one after the other, then their B tiles (the
@@ -542,12 +544,12 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         // consumers of a slot: MMA warp, the epilogue warps, the prefetch warp and, under
         // the sentinel policy, the two checker warps (+ the peer's loader and the same
         // warps in a pair)
-        const uint32_t nloc = 2u + (uint32_t)kEpiWarps + (CHECK ? 2u : 0u);
+        const uint32_t nloc = 2u + (uint32_t)kEpiWarps + (CHECK ? (uint32_t)C::check_warps() : 0u);
         ptx::mbar_init(&qempty[i], kPair ? 2u * nloc + 1u : nloc);
       }
       ptx::mbar_init(mma_done, 1);
       ptx::mbar_init(pw_done, 128);
-      ptx::mbar_init(scan_done, 2);
+      ptx::mbar_init(scan_done, (uint32_t)C::check_warps());
       *abort_flag = 0;
       *it_issued = 0;
       *progress = 0;
@@ -1132,6 +1134,20 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       }
       return __any_sync(FULL, (sbits & 0x80008000u) != 0u);
     };
+    // The same for half (part 0 or 1) of a GEMM A k-block (128 rows x 64 = 16 KB, so 8 KB:
+    // 16 loads per lane).
+    auto half_has_sentinel = [&](int sx, int h, int part) -> bool {
+      const uint8_t* base = smem_a(sx, h) + part * (C::kABytes / 2);
+      uint4 v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = ptx::ld_shared_v4(base + ((uint32_t)lane + (uint32_t)j * 32u) * 16u);
+      uint32_t sbits = 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        sbits |= sentinel_bits_bf16x2(v[j].x) | sentinel_bits_bf16x2(v[j].y) | sentinel_bits_bf16x2(v[j].z) |
+                 sentinel_bits_bf16x2(v[j].w);
+      return __any_sync(FULL, (sbits & 0x80008000u) != 0u);
+    };
     if constexpr (CHECK && KPS == 1) {
       static_assert(S % 2 == 0, "the checkers split the stages by parity");
       uint32_t it = 0, tcount = 0;
@@ -1263,11 +1279,15 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
         }
       }
     } else if constexpr (CHECK) {
-      // Two k-blocks per stage: warp 7 + h scans k-block h of every checked stage.  The two
-      // warps combine their findings each round through scan_flag and the scan_done
-      // barrier (bounded waits, one arrival per warp); warp 7 alone decides to reload the
-      // stage's A box or to give up after the timeout, and hands the clean stage to the
-      // MMA issuer.  Both warps follow every stage and round, so their barrier phases agree.
+      // Two k-blocks per stage: checker warp 7 + c scans half c & 1 of k-block c >> 1 of
+      // every checked stage.  The checkers combine their findings each round through
+      // scan_flag and the scan_done barrier (bounded waits, one arrival per warp); warp 7
+      // alone decides to reload the stage's A box or to give up after the timeout, and
+      // hands the clean stage to the MMA issuer.  Every checker follows every stage and
+      // round, so their barrier phases agree.
+      constexpr int kCW = C::check_warps();
+      static_assert(kCW == 2 * KPS, "two checkers per k-block of a stage");
+      const int h_ck = ck >> 1;                // this warp's k-block of the stage
       uint32_t it = 0, tcount = 0, cpar = 0, xround = 0;
       bool ok = true;
       while (ok) {
@@ -1306,22 +1326,25 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           const uint32_t c1 = args.trace ? (uint32_t)clock64() : 0u;
           uint64_t t0 = 0;
           while (true) {
-            // this warp's k-block (only those of the unit: a box may reach into the next)
-            const bool dirty = ck < nk && stage_has_sentinel(st, ck, abytes);
+            // this warp's half k-block (only those of the unit: a box may reach into the next)
+            const bool dirty = h_ck < nk && half_has_sentinel(st, h_ck, ck & 1);
             bool late = false;
             if (ck == 0 && t0 != 0)
               late = ptx::globaltimer() - t0 > args.timeout_ns || ptx::ld_relaxed_gpu(args.ctrl + CTRL_ERR) != 0u;
             if (lane == 0) {
-              scan_flag[(xround & 1u) * 2u + (uint32_t)ck] = (dirty ? 1u : 0u) | (late ? 2u : 0u);
+              scan_flag[(xround & 1u) * kCW + (uint32_t)ck] = (dirty ? 1u : 0u) | (late ? 2u : 0u);
               ptx::mbar_arrive(scan_done);
             }
             if (!ptx::mbar_wait_bounded(scan_done, xround & 1u, pto)) {
               ok = false;
               break;
             }
-            const uint32_t f0 = scan_flag[(xround & 1u) * 2u], f1 = scan_flag[(xround & 1u) * 2u + 1u];
+            const uint32_t f0 = scan_flag[(xround & 1u) * kCW];
+            uint32_t fa = 0;
+#pragma unroll
+            for (int c = 0; c < kCW; ++c) fa |= scan_flag[(xround & 1u) * kCW + (uint32_t)c];
             ++xround;
-            if (((f0 | f1) & 1u) == 0u) break;  // the stage is clean
+            if ((fa & 1u) == 0u) break;  // the stage is clean
             if (f0 & 2u) {
               if (ck == 0 && lane == 0) record_error(args, ERRC_SENTINEL_TIMEOUT, t, kb);
               break;
