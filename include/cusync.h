@@ -294,6 +294,12 @@ typedef struct {
   double post_ns;            /* producer stores done to the post seen by a consumer */
   double gap_ns;             /* producer kernel end to consumer kernel start (stream) */
   double fill_ns_per_mb;     /* sentinel fill of the intermediate, per MB */
+  double tile_ns;            /* a tile that is not its CTA's first: from the previous tile's
+                                last k-block to its first (the next claim, the arming and
+                                the first copy behind the previous tile's last copies) */
+  double tile_wait_ns;       /* a consumer tile's first semaphore consult, even when the
+                                semaphores are already posted (the probe's round trip, the
+                                acquire and proxy fences) */
 } cusync_latency_model_t;
 
 typedef struct {

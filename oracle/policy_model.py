@@ -18,8 +18,9 @@ The model written out here, step by step:
 
 * a tile of stage s costs T_init (start_ns) when it is its CTA's first tile, then
   k_blocks(s) x kblock_ns[s] of main loop, then epilogue_ns[s]; a persistent CTA starts
-  its next tile's main loop when the previous one ends, and a tile's epilogue starts
-  after both its main loop and the CTA's previous epilogue have finished;
+  its next tile's main loop tile_ns after the previous one ends (the next claim, the
+  arming and the first copy), and a tile's epilogue starts after both its main loop and
+  the CTA's previous epilogue have finished;
 * the queue holds the producer tiles (row-major, or row tiles taken in groups with the
   column outer within a group; StridedSync visits each group's columns one after
   another) before the consumer tiles (in the same row order); CTA q takes tile q
@@ -33,12 +34,20 @@ The model written out here, step by step:
   the tile waits for the producer tiles its policy waits for there (``deps.wait_sets``);
   if they are posted later than the k-block could start, the k-block starts start_ns
   after the last post (the copy pipeline refills); a k-block that waited on anything
-  costs wait_kblock_ns more (TileSync, StridedSync, RowSync's first k-block);
+  costs wait_kblock_ns more (TileSync, StridedSync, RowSync's first k-block), and the
+  first such k-block of a tile tile_wait_ns more before the wait (the probe of the
+  semaphores and the fences after it, paid whether or not they are posted);
 * the sentinel policy waits on exactly the producer tiles each k-block reads (the
   TileSync sets), costs sentinel_kblock_ns per consumer k-block and starts after the
   intermediate is filled (fill_ns_per_mb per MB);
 * stream order runs the producer tiles as one launch, then, gap_ns after its last
-  epilogue, the consumer tiles as a second launch with no waits.
+  epilogue, the consumer tiles as a second launch with no waits;
+* a convolution stack of S stages ([cuSync] §II-B "ResNet", Table ``tab:resnet-sizes``)
+  is the same with every stage after the first a consumer of the stage before it: stream
+  order runs S launches gap_ns apart; the fused launch queues stage 0's tiles, then stage
+  1's, and so on (under the sentinel policy followed by fill units of 64 KB for the next
+  run's intermediates, each fill_ns_per_mb x 0.065536 of epilogue time); the last stage's
+  tiles take epilogue_ns[1], the others epilogue_ns[0].
 """
 
 from dataclasses import dataclass
@@ -56,6 +65,8 @@ class Model:
     post_ns: float
     gap_ns: float
     fill_ns_per_mb: float
+    tile_ns: float = 0.0
+    tile_wait_ns: float = 0.0
 
 
 @dataclass
@@ -83,7 +94,7 @@ def play(tiles, slots, t0, model, cost):
         else:
             k = min(range(len(ctas)), key=lambda i: (ctas[i]["free"], i))
         c = ctas[k]
-        start = c["free"] if c["used"] else c["free"] + model.start_ns
+        start = c["free"] + model.tile_ns if c["used"] else c["free"] + model.start_ns
         c["used"] = True
         main_end = cost(tile, start)
         done = max(main_end, c["last_done"]) + model.epilogue_ns[tile[0]]
@@ -114,7 +125,7 @@ def _play_producers(chain, slots, t0, model, ctas=None):
     for q, (tile, k, nkb) in enumerate(units):
         i = q if q < len(ctas) else min(range(len(ctas)), key=lambda j: (ctas[j]["free"], j))
         c = ctas[i]
-        start = c["free"] if c["used"] else c["free"] + model.start_ns
+        start = c["free"] + model.tile_ns if c["used"] else c["free"] + model.start_ns
         c["used"] = True
         main_end = start + nkb * model.kblock_ns[0]
         ready = max(main_end, c["last_done"])
@@ -157,13 +168,17 @@ def predict_fused(chain, policy, slots, model):
     for q, m in enumerate(chain.cons_rows, start=n_units):
         i = q if q < len(ctas) else min(range(len(ctas)), key=lambda j: (ctas[j]["free"], j))
         c = ctas[i]
-        t = c["free"] if c["used"] else c["free"] + model.start_ns
+        t = c["free"] + model.tile_ns if c["used"] else c["free"] + model.start_ns
         c["used"] = True
         if m not in wait_cache:
             wait_cache[m] = deps.wait_sets(chain.dep_chain, wait_policy, m, chain.G)
+        consulted = False
         for kb in range(kb1):
             need = wait_cache[m][kb]
             if need:
+                if not sentinel and not consulted:
+                    t += model.tile_wait_ns
+                    consulted = True
                 ready = max(posted[p] for p in need)
                 if ready > t:
                     t = ready + model.start_ns
@@ -211,3 +226,60 @@ def conv_chain(n, h, w, c, k, tile_n, th):
     prod = [(m, y) for m in range(mt) for y in range(nt)]
     cons = [m for m in range(mt) for _ in range(nt)]
     return prod, cons, deps.ConvChain(N=n, P=h, Q=w, C=k, TH=th, BNo=tile_n, BK=64)
+
+
+def predict_stack(stages, tiles, k_blocks, dep_chain, policy, slots_fused, slots_stage, model, fill_units=0):
+    """Predicted ns of one run of a convolution stack: `tiles` is one stage's (m, c) tiles in
+    queue order (every stage has the same), `k_blocks` the k-blocks of a tile."""
+    S = stages
+
+    def run(queue, slots, t0, posts):
+        ctas = [{"free": t0, "last_done": t0, "used": False} for _ in range(max(1, min(slots, len(queue))))]
+        posted = {}
+        end = t0
+        for q, item in enumerate(queue):
+            i = q if q < len(ctas) else min(range(len(ctas)), key=lambda j: (ctas[j]["free"], j))
+            c = ctas[i]
+            t = c["free"] + model.tile_ns if c["used"] else c["free"] + model.start_ns
+            c["used"] = True
+            if item is None:   # a fill unit: stores of the epilogue warps
+                done = max(t, c["last_done"]) + model.fill_ns_per_mb * 65536 / 1e6
+                c["last_done"] = done
+                end = max(end, done)
+                continue
+            s, (m, col) = item
+            if s == 0 or not posts:
+                t += k_blocks * model.kblock_ns[0 if s == 0 else 1]
+            else:
+                sets = deps.wait_sets(dep_chain, "TILE" if policy == "SENTINEL" else policy, m, 1)
+                consulted = False
+                for kb in range(k_blocks):
+                    need = sets[kb]
+                    if need:
+                        if policy != "SENTINEL" and not consulted:
+                            t += model.tile_wait_ns
+                            consulted = True
+                        ready = max(posted[(s - 1, p)] for p in need)
+                        if ready > t:
+                            t = ready + model.start_ns
+                    if policy == "SENTINEL":
+                        t += model.sentinel_kblock_ns
+                    else:
+                        t += model.kblock_ns[1] + (model.wait_kblock_ns if need else 0.0)
+            done = max(t, c["last_done"]) + model.epilogue_ns[0 if s < S - 1 else 1]
+            c["free"] = t
+            c["last_done"] = done
+            end = max(end, done)
+            if posts and s < S - 1:
+                posted[(s, (m, col))] = done + model.post_ns
+        return end
+
+    if policy == "STREAM":
+        t = 0.0
+        for s in range(S):
+            t = run([(s, tile) for tile in tiles], slots_stage, t + model.gap_ns if s else 0.0, False)
+        return t
+    queue = [(s, tile) for s in range(S) for tile in tiles]
+    if policy == "SENTINEL":
+        queue += [None] * fill_units
+    return run(queue, slots_fused, 0.0, True)

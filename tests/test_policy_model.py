@@ -98,7 +98,7 @@ def _oracle_predict(desc, info, model, policy):
     mo = pm.Model(kblock_ns=tuple(model.kblock_ns), wait_kblock_ns=model.wait_kblock_ns,
                   sentinel_kblock_ns=model.sentinel_kblock_ns, start_ns=model.start_ns,
                   epilogue_ns=tuple(model.epilogue_ns), post_ns=model.post_ns, gap_ns=model.gap_ns,
-                  fill_ns_per_mb=model.fill_ns_per_mb)
+                  fill_ns_per_mb=model.fill_ns_per_mb, tile_ns=model.tile_ns, tile_wait_ns=model.tile_wait_ns)
     slots = info.num_sms // info.cta_pair
     units = len(prod) * info.ksplit
     if policy == "STREAM":
@@ -205,3 +205,74 @@ def test_grouped_queue_order():
             mt, nt = info.m_tiles[stage], info.n_tiles[stage]
             lib = [cs.cusync_tile_at(d, stage, u) for u in range(mt * nt)]
             assert lib == pm._grouped_rows(mt, nt, info.raster_rows)
+
+
+def test_tile_costs_closed_form():
+    """tile_ns and tile_wait_ns written out by hand: one CTA, two producer tiles of 4
+    k-blocks, then one consumer tile that consults a semaphore at k-blocks 0 and 2."""
+    prod, cons, dc = pm.gemm_chain(128, 256, 128, 128, 128, 1, "TILE")
+    ch = pm.Chain(prod, cons, (4, 4), dc)
+    m = _model(tile_ns=7.0, tile_wait_ns=11.0)
+    p0 = 100 + 4 * 10                          # first tile: start_ns, then its k-blocks
+    p1 = p0 + 7 + 4 * 10                       # a later tile: tile_ns before its k-blocks
+    cons_start = p1 + 7
+    main_end = cons_start + 11 + 4 * 20 + 2 * 3   # the first consult costs tile_wait_ns once
+    last_epi = max(p1, p0 + 30) + 30
+    want = max(main_end, last_epi) + 40
+    assert pm.predict_fused(ch, "TILE", 1, m) == pytest.approx(want, rel=1e-12)
+    # stream order: each later tile of a launch pays tile_ns, no consult
+    s0 = 100 + 4 * 10
+    s1 = s0 + 7 + 4 * 10
+    e0 = max(s1, s0 + 30) + 30
+    c0 = e0 + 500 + 100 + 4 * 20               # gap_ns, then the consumer launch's first tile
+    assert pm.predict_stream(ch, 1, 1, m) == pytest.approx(c0 + 40, rel=1e-12)
+
+
+def test_stack_closed_form_and_pair_consistency():
+    """A two-stage stack is the convolution pair: the same tiles, waits and costs; stream
+    order of a stack is its stages' launches gap_ns apart."""
+    prod, cons, dc = pm.conv_chain(1, 4, 4, 64, 64, 64, 4)     # one 16-pixel tile per stage
+    ch = pm.Chain(prod, cons, (9, 9), dc)
+    m = _model()
+    for pol in ("ROW", "TILE"):
+        assert pm.predict_stack(2, prod, 9, dc, pol, 1, 1, m) == pytest.approx(pm.predict_fused(ch, pol, 1, m))
+    assert pm.predict_stack(2, prod, 9, dc, "STREAM", 1, 1, m) == pytest.approx(pm.predict_stream(ch, 1, 1, m))
+    one = 100 + 9 * 10 + 30                    # stage 0 alone: start, k-blocks, epilogue
+    later = 100 + 9 * 20 + 30
+    want = one + 500 + later + 500 + (100 + 9 * 20 + 40)
+    assert pm.predict_stack(3, prod, 9, dc, "STREAM", 1, 1, m) == pytest.approx(want)
+
+
+STACK_CASES = [dict(n=2, h=14, w=14, c=64, stages=4, tile_n=128, num_sms=8),
+               dict(n=4, h=8, w=8, c=128, stages=3, tile_n=128, num_sms=6),
+               dict(n=2, h=7, w=7, c=256, stages=5, tile_n=256, num_sms=4)]
+
+
+@pytest.mark.parametrize("case", STACK_CASES)
+def test_library_stack_model_matches_oracle(case):
+    base = cs.make_desc(cs.CHAIN_CONV_STACK, "ROW", **case)
+    model = cs.cusync_default_latency_model(base)
+    pred = cs.cusync_predict_policies(base)
+    mo = pm.Model(kblock_ns=tuple(model.kblock_ns), wait_kblock_ns=model.wait_kblock_ns,
+                  sentinel_kblock_ns=model.sentinel_kblock_ns, start_ns=model.start_ns,
+                  epilogue_ns=tuple(model.epilogue_ns), post_ns=model.post_ns, gap_ns=model.gap_ns,
+                  fill_ns_per_mb=model.fill_ns_per_mb, tile_ns=model.tile_ns, tile_wait_ns=model.tile_wait_ns)
+    for pol, idx in POLICY_IDX.items():
+        d = cs.make_desc(cs.CHAIN_CONV_STACK, pol, **case)
+        try:
+            info = cs.cusync_plan_info(d)
+        except cs.CusyncError as e:
+            assert pol == "STRIDED" and e.status == cs.ERR_UNSUPPORTED
+            assert pred.us[idx] == -1.0
+            continue
+        tiles, _, dc = pm.conv_chain(case["n"], case["h"], case["w"], case["c"], case["c"], info.tile_n,
+                                     info.conv_rows_per_tile)
+        units = len(tiles)
+        fill = 0
+        if pol == "SENTINEL":
+            chunks = (case["stages"] - 1) * case["n"] * case["h"] * case["w"] * case["c"] // 8
+            fill = -(-chunks // 4096)
+        want = pm.predict_stack(case["stages"], tiles, info.k_blocks[0], dc, pol,
+                                min(case["num_sms"], units * case["stages"]), min(case["num_sms"], units), mo,
+                                fill_units=fill) / 1e3
+        assert pred.us[idx] == pytest.approx(want, rel=1e-9), pol

@@ -76,7 +76,7 @@ class cusync_chain_info_t(ctypes.Structure):
 class cusync_latency_model_t(ctypes.Structure):
     _fields_ = [("kblock_ns", c_dbl * 2), ("wait_kblock_ns", c_dbl), ("sentinel_kblock_ns", c_dbl),
                 ("start_ns", c_dbl), ("epilogue_ns", c_dbl * 2), ("post_ns", c_dbl), ("gap_ns", c_dbl),
-                ("fill_ns_per_mb", c_dbl)]
+                ("fill_ns_per_mb", c_dbl), ("tile_ns", c_dbl), ("tile_wait_ns", c_dbl)]
 
 
 class cusync_policy_prediction_t(ctypes.Structure):

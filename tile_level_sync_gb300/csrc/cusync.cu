@@ -640,21 +640,31 @@ Grids make_grids(const Plan& p, int sms, int max_clusters) {
 // the post seen by a consumer about 1.5 us after the stores, 2 us between stream-ordered
 // kernels, and epilogue time per output column by activation (tanh-GeLU 22 ns, SwiGLU
 // 26 ns, ReLU 22 ns, none 17 ns for a 128-row tile).
+// Per-tile costs, from the same traces: a CTA's next tile starts its mainloop 2.2-2.9 us
+// after the previous one's last k-block (stacks and the GPT-3 M = 1024 slice alike), and a
+// consumer tile's first semaphore consult costs 1.8 us (CTA pairs) to 2.6 us (convolution
+// tiles) even when the semaphores are already posted.
 LatencyModel default_model(const Plan& p) {
   LatencyModel m;
   const bool conv = p.geo[0].a_mode == AMODE_CONV;
   if (conv) {
-    m.kblock_ns[0] = 365.0;
-    m.kblock_ns[1] = 360.0;
-    m.sentinel_kblock_ns = 420.0;
+    m.kblock_ns[0] = 375.0;
+    m.kblock_ns[1] = 375.0;
+    m.sentinel_kblock_ns = 500.0;
+    m.tile_ns = 2500.0;
+    m.tile_wait_ns = 2600.0;
   } else if (p.pair == 2) {
     m.kblock_ns[0] = 340.0;
     m.kblock_ns[1] = 330.0;
     m.sentinel_kblock_ns = 435.0;
+    m.tile_ns = 2700.0;
+    m.tile_wait_ns = 1800.0;
   } else {
     m.kblock_ns[0] = p.bn == 128 ? 355.0 : 350.0;
     m.kblock_ns[1] = p.bn == 128 ? 365.0 : 370.0;
     m.sentinel_kblock_ns = 440.0;
+    m.tile_ns = 2500.0;
+    m.tile_wait_ns = 2000.0;
   }
   m.wait_kblock_ns = 150.0;
   m.start_ns = 1000.0;
@@ -681,7 +691,7 @@ void predict_all(const cusync_chain_desc_t& d, const cusync_latency_model_t* mod
     c.policy = (cusync_policy_t)pol;
     c.ksplit_consumer = 1;  // the model plays whole consumer tiles
     Plan q;
-    if (make_plan(c, &q) != CUSYNC_OK || q.nst != 2) {  // the model covers two-stage chains
+    if (make_plan(c, &q) != CUSYNC_OK || (q.nst != 2 && !q.stack)) {  // two-stage chains and stacks
       us[pol] = -1.0;
       continue;
     }
@@ -689,6 +699,22 @@ void predict_all(const cusync_chain_desc_t& d, const cusync_latency_model_t* mod
     if (model) std::memcpy(&lm, model, sizeof(lm));
     else lm = default_model(q);
     const Grids g = make_grids(q, sms, 0);
+    if (q.stack) {
+      ModelStack ms;
+      ms.geo[0] = q.geo[0];
+      ms.geo[1] = q.geo[1];
+      ms.dep = q.dep;
+      ms.stages = q.nst;
+      ms.slots_fused = g.fused;
+      ms.slots_stage = g.stage[0];
+      ms.fill_units = 0;
+      if (q.rotate) {
+        const int64_t set_chunks = (int64_t)(q.nst - 1) * stack_buf_elems(c) / 8;
+        ms.fill_units = (int32_t)ceil_div(set_chunks, 4096);
+      }
+      us[pol] = predict_stack_ns(ms, lm) / 1000.0;
+      continue;
+    }
     ModelChain mc;
     mc.geo[0] = q.geo[0];
     mc.geo[1] = q.geo[1];

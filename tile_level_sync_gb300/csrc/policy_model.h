@@ -17,10 +17,13 @@
 // unit's epilogue -- adding the others' partial sums -- follows all of theirs), and the
 // threadblock batches are not assumed but played out: a persistent CTA takes the next
 // tile of the queue as soon as its mainloop finishes (its epilogue overlaps the next
-// tile's mainloop), the first tile of each CTA is its own index, later tiles go to the
-// CTA that frees up first, and a consumer k-block cannot start before the semaphores it
-// waits for (the same waits the device performs) are posted.  A wait that blocks costs
-// a pipeline refill (T_start) after the post is seen.
+// tile's mainloop) and starts its k-blocks tile_ns later (the claim, the arming and the
+// first copy), the first tile of each CTA is its own index, later tiles go to the CTA that
+// frees up first, and a consumer k-block cannot start before the semaphores it waits for
+// (the same waits the device performs) are posted.  A tile's first semaphore consult costs
+// tile_wait_ns whether or not they are posted (the probe and the fences), and a wait that
+// blocks costs a pipeline refill (T_start) after the post is seen.  Convolution stacks
+// (predict_stack_ns) chain the same rules over all of their stages.
 #pragma once
 #include <algorithm>
 #include <cstdint>
@@ -39,6 +42,8 @@ struct LatencyModel {
   double post_ns;             // stores done to the post seen by a waiting consumer
   double gap_ns;              // end of one kernel to the start of the next (stream order)
   double fill_ns_per_mb;      // sentinel fill of the intermediate
+  double tile_ns;             // a CTA's later tile: previous tile's last k-block to its first
+  double tile_wait_ns;        // a consumer tile's first semaphore consult, posted or not
 };
 
 struct ModelChain {
@@ -108,7 +113,7 @@ inline double play_queue(const ModelChain& c, const LatencyModel& lm, int s0, in
         if (cta[i].free_main < cta[k].free_main) k = i;
     }
     SimCta& x = cta[k];
-    double t = x.used ? x.free_main : x.free_main + lm.start_ns;
+    double t = x.used ? x.free_main + lm.tile_ns : x.free_main + lm.start_ns;
     x.used = true;
     const StageGeo& g = c.geo[s];
     if (s == 0 || !waits) {
@@ -116,9 +121,14 @@ inline double play_queue(const ModelChain& c, const LatencyModel& lm, int s0, in
     } else {
       consumer_wait_lists(c, m, &wl);
       const double kb_ns = sentinel ? lm.sentinel_kblock_ns : lm.kblock_ns[1];
+      bool consulted = false;
       for (int32_t kb = 0; kb < g.k_blocks; ++kb) {
         double ready = -1.0;
         for (int32_t f : wl[kb]) ready = std::max(ready, (*flag_ready)[(size_t)f]);
+        if (!wl[kb].empty() && !sentinel && !consulted) {
+          t += lm.tile_wait_ns;
+          consulted = true;
+        }
         if (ready > t) t = ready + lm.start_ns;  // the pipeline refills after the post
         t += kb_ns + ((!sentinel && !wl[kb].empty()) ? lm.wait_kblock_ns : 0.0);
       }
@@ -152,6 +162,98 @@ inline double predict_chain_ns(const ModelChain& c, const LatencyModel& lm) {
   std::vector<double> ready((size_t)std::max<int64_t>(1, nflags), 0.0);
   const double t0 = sentinel ? c.h_mb * lm.fill_ns_per_mb : 0.0;
   return play_queue(cc, lm, 0, 1, c.slots_fused, t0, sentinel, &ready);
+}
+
+// A convolution stack of `stages` dependent convolutions ([cuSync] §II-B "ResNet", Table
+// tab:resnet-sizes): stage 0 reads the input, every later stage the stage before it (the
+// halo dependency sets of the pair, `dep`); all stages have the same tiles.  Under the
+// sentinel policy the intermediates of the next run are filled by fill units at the end of
+// the run's queue (units of 64 KB, fill_ns_per_mb each).
+struct ModelStack {
+  StageGeo geo[2];       // stage 0; every later stage
+  DepCfg dep;            // a stage's waits on the stage before it (dep.policy = the policy)
+  int32_t stages;
+  int32_t slots_fused;   // CTAs of the fused launch
+  int32_t slots_stage;   // CTAs of one stage's launch in stream order
+  int32_t fill_units;    // sentinel: fill units at the end of the queue
+};
+
+inline double predict_stack_ns(const ModelStack& c, const LatencyModel& lm) {
+  const int32_t S = c.stages;
+  const int64_t n = stage_units(c.geo[0]);
+  const bool stream = c.dep.policy == POL_STREAM;
+  const bool sentinel = c.dep.policy == POL_SENTINEL;
+  DepCfg dep = c.dep;
+  if (sentinel) dep.policy = POL_TILE;  // the sentinel waits on exactly the data of each k-block
+  ModelChain mc;                        // for the consumer wait lists of stages >= 1
+  mc.geo[0] = c.geo[0];
+  mc.geo[1] = c.geo[1];
+  mc.dep = dep;
+  const int64_t nflags = std::max<int64_t>(1, num_flags(dep));
+  std::vector<std::vector<double>> posted((size_t)S, std::vector<double>((size_t)nflags, 0.0));
+  std::vector<std::vector<int32_t>> wl;
+  const double fill_unit_ns = lm.fill_ns_per_mb * (65536.0 / 1e6);
+  // one queue: the fused launch (stages 0 .. S-1, then fill units), or one stage of stream order
+  auto play = [&](int32_t s0, int32_t s1, int32_t slots, double t0, int32_t fills) -> double {
+    const int64_t total = (int64_t)(s1 - s0 + 1) * n + fills;
+    std::vector<SimCta> cta((size_t)std::max<int64_t>(1, std::min<int64_t>(slots, total)));
+    for (auto& x : cta) x = SimCta{t0, t0, false};
+    double end = t0;
+    for (int64_t q = 0; q < total; ++q) {
+      size_t k = 0;
+      if (q < (int64_t)cta.size()) {
+        k = (size_t)q;
+      } else {
+        for (size_t i = 1; i < cta.size(); ++i)
+          if (cta[i].free_main < cta[k].free_main) k = i;
+      }
+      SimCta& x = cta[k];
+      double t = x.used ? x.free_main + lm.tile_ns : x.free_main + lm.start_ns;
+      x.used = true;
+      if (q >= (int64_t)(s1 - s0 + 1) * n) {  // a fill unit: the epilogue warps' stores
+        const double done = std::max(t, x.last_done) + fill_unit_ns;
+        x.last_done = done;
+        end = std::max(end, done);
+        continue;
+      }
+      const int32_t s = s0 + (int32_t)(q / n);
+      int32_t m, y;
+      tile_at(c.geo[s == 0 ? 0 : 1], (int32_t)(q % n), &m, &y);
+      const StageGeo& g = c.geo[s == 0 ? 0 : 1];
+      if (s == 0 || stream) {
+        t += (double)g.k_blocks * lm.kblock_ns[s == 0 ? 0 : 1];
+      } else {
+        consumer_wait_lists(mc, m, &wl);
+        const double kb_ns = sentinel ? lm.sentinel_kblock_ns : lm.kblock_ns[1];
+        bool consulted = false;
+        for (int32_t kb = 0; kb < g.k_blocks; ++kb) {
+          double ready = -1.0;
+          for (int32_t f : wl[kb]) ready = std::max(ready, posted[(size_t)(s - 1)][(size_t)f]);
+          if (!wl[kb].empty() && !sentinel && !consulted) {
+            t += lm.tile_wait_ns;
+            consulted = true;
+          }
+          if (ready > t) t = ready + lm.start_ns;
+          t += kb_ns + ((!sentinel && !wl[kb].empty()) ? lm.wait_kblock_ns : 0.0);
+        }
+      }
+      const double done = std::max(t, x.last_done) + lm.epilogue_ns[s < S - 1 ? 0 : 1];
+      x.free_main = t;
+      x.last_done = done;
+      end = std::max(end, done);
+      if (!stream && s < S - 1) {
+        const int32_t f = producer_flag(dep, m, y);
+        if (f >= 0) posted[(size_t)s][(size_t)f] = std::max(posted[(size_t)s][(size_t)f], done + lm.post_ns);
+      }
+    }
+    return end;
+  };
+  if (stream) {
+    double t = 0.0;
+    for (int32_t s = 0; s < S; ++s) t = play(s, s, c.slots_stage, s == 0 ? 0.0 : t + lm.gap_ns, 0);
+    return t;
+  }
+  return play(0, S - 1, c.slots_fused, 0.0, sentinel ? c.fill_units : 0);
 }
 
 }  // namespace cusync
