@@ -44,7 +44,8 @@ NCU_TRAFFIC = {
     # (workload, policy, launch, tile_n, CTAs per tile): (dram__bytes_read.sum +
     # dram__bytes_write.sum per launch of the chain kernel, hash of the kernel sources the
     # capture was taken with)
-    ("gpt3_mlp_m256", "ROW", "persistent", 256, 2): (311140608 + 18001920, "90220715f9271dae"),
+    ("gpt3_mlp_m256", "ROW", "persistent", 256, 2): (311500544 + 19335168, "f98b63074f8798a1"),
+    ("gpt3_mlp_m1024", "ROW", "persistent", 256, 2): (554264832 + 31522048, "f98b63074f8798a1"),
 }
 
 
