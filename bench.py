@@ -96,6 +96,8 @@ def parse():
     p.add_argument("--l2-prefetch", type=int, default=0)
     p.add_argument("--cta-pair", type=int, default=0)
     p.add_argument("--ksplit", type=int, default=0, help="producer K split (0 = the planner's choice)")
+    p.add_argument("--ksplit-skew", type=int, default=0, help="graded producer K split: k-blocks each unit "
+                   "adds to the one before it (0 = the planner's choice, -1 = equal units)")
     p.add_argument("--no-run-overlap", action="store_true", help="launch each run's first kernel in plain "
                    "stream order (CUSYNC_FLAG_NO_RUN_OVERLAP)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -317,7 +319,8 @@ def run_reference(a):
 class Setup:
     """Device operands and chains of one workload."""
 
-    def __init__(self, wl, inputs, tile_n, launch, raster=0, l2_prefetch=0, cta_pair=0, ksplit=0, flags=0):
+    def __init__(self, wl, inputs, tile_n, launch, raster=0, l2_prefetch=0, cta_pair=0, ksplit=0, flags=0,
+                 ksplit_skew=0):
         import torch
         import tile_level_sync_gb300 as cs
         self.cs = cs
@@ -377,6 +380,7 @@ class Setup:
         self.l2_prefetch = l2_prefetch
         self.cta_pair = cta_pair
         self.ksplit = ksplit
+        self.ksplit_skew = ksplit_skew
         self.flags = flags
         self.chains = {}
 
@@ -391,7 +395,8 @@ class Setup:
         if key not in self.chains:
             self.chains[key] = cs.Chain(cs.make_desc(policy=policy, launch=launch, tile_n=tile_n, raster_rows=raster,
                                                      l2_prefetch=l2_prefetch, cta_pair=cta_pair,
-                                                     flags=flags | self.flags, ksplit=self.ksplit, **self.base))
+                                                     flags=flags | self.flags, ksplit=self.ksplit,
+                                                     ksplit_skew=self.ksplit_skew, **self.base))
         return self.chains[key]
 
     def run(self, ch):
@@ -479,7 +484,7 @@ def trace_stats(torch, setup, policy, launch):
     cs = setup.cs
     d = cs.make_desc(policy=policy, launch=launch, tile_n=setup.tile_n, raster_rows=setup.raster,
                      l2_prefetch=setup.l2_prefetch, cta_pair=setup.cta_pair, ksplit=setup.ksplit,
-                     flags=cs.FLAG_TRACE, **setup.base)
+                     ksplit_skew=setup.ksplit_skew, flags=cs.FLAG_TRACE, **setup.base)
     ch = cs.Chain(d)
     try:
         for _ in range(3):
@@ -700,7 +705,7 @@ def per_config(torch, cs, synth, peaks):
             "stream_us": timed.get("STREAM"), "speedup_vs_stream": timed["STREAM"] / sync[best] if "STREAM" in timed
             else None, "tflops": tflops, "pct_bf16_peak_measured": tflops / peaks["bf16_tflops"] * 100,
             "tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "cta_pair": info.cta_pair, "ksplit": info.ksplit,
-            "us": us, "runs_timed": n, "timing": "median of 5 rounds over the variants in turn",
+            "ksplit_skew": info.ksplit_skew, "us": us, "runs_timed": n, "timing": "median of 5 rounds over the variants in turn",
             "bit_identical_all_variants": identical,
             "parity_sampled": parity, "parity_sample": sample,
             "waves_148": {"tbs": list(w148.tbs), "waves": list(w148.waves), "stream_waves": w148.stream_waves,
@@ -739,7 +744,7 @@ def main():
     inputs = synth.workload_inputs(wl, seed=0)
     launch = cs.LAUNCH_PDL if a.launch == "pdl" else cs.LAUNCH_PERSISTENT
     setup = Setup(wl, inputs, a.tile_n, launch, a.raster, a.l2_prefetch, a.cta_pair, a.ksplit,
-                  cs.FLAG_NO_RUN_OVERLAP if a.no_run_overlap else 0)
+                  cs.FLAG_NO_RUN_OVERLAP if a.no_run_overlap else 0, a.ksplit_skew)
     flops = wl.gemm_flops()
     peaks, peak_src = load_peaks()
 
@@ -858,7 +863,8 @@ def main():
 
     plan = cs.cusync_plan_waves(setup.chain(best).desc)
     plan148 = cs.cusync_plan_waves(cs.make_desc(policy=best, launch=launch, tile_n=a.tile_n, num_sms=148,
-                                                cta_pair=a.cta_pair, ksplit=a.ksplit, **setup.base))
+                                                cta_pair=a.cta_pair, ksplit=a.ksplit, ksplit_skew=a.ksplit_skew,
+                                                **setup.base))
     info = setup.chain(best).info()
 
     cpu = None
@@ -885,6 +891,7 @@ def main():
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, **wl.dims, "policy": best, "launch": a.launch,
                    "tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "cta_pair": info.cta_pair,
+                   "ksplit": info.ksplit, "ksplit_skew": info.ksplit_skew,
                    "parallelism": "replicas only",
                    "enqueue": "library call per run" if a.no_graph else "CUDA-graph replay, 50 captured runs per graph",
                    "l2": f"inputs {alg_bytes / 1e6:.0f} MB of operands > 129 MB L2; no flush between steps"

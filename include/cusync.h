@@ -205,7 +205,12 @@ typedef struct {
                                         stores, for cusync_run_mlp_bands / cusync_band_wait
                                         (at most 16 and at most the consumer's row tiles;
                                         row-major tile order).  0 = none */
-  int32_t _pad1;
+  int32_t ksplit_skew;               /* graded K split of the producer: each unit this
+                                        many k-blocks longer than the one before it (the
+                                        last takes the remainder), so the units finish one
+                                        after the other and each exchange of partial sums
+                                        overlaps the later units' mainloops.  0 =
+                                        planner; -1 = equal units */
 } cusync_chain_desc_t;
 
 /* Wave arithmetic of a two-kernel chain ([cuSync] §II-A "Thread block Wave Execution",
@@ -262,7 +267,7 @@ typedef struct {
   int32_t policy;             /* the policy the plan uses (CUSYNC_POLICY_AUTO resolved) */
   int32_t ksplit;             /* K-split units per producer tile (1 = none); the
                                  producer launch has m_tiles*n_tiles*ksplit units */
-  int32_t kb_per_split;       /* k-blocks per unit */
+  int32_t kb_per_split;       /* k-blocks per unit (graded split: of unit 0) */
   /* ATTENTION (three stages): stage 1 is the pointwise kernel, stage 2 the output GEMM */
   int32_t nst;                /* stages of the chain: 2, or 3 */
   int32_t m_tiles2, n_tiles2, k_blocks2, n_out2, grid2;
@@ -274,7 +279,8 @@ typedef struct {
   int32_t ksplit_consumer;    /* K-split units per consumer tile (1 = none) */
   int32_t kb_per_split_consumer;
   int32_t raster_rows;        /* row tiles per group of the tile order (1 = row-major) */
-  int32_t _pad;
+  int32_t ksplit_skew;        /* k-blocks each producer unit adds to the one before it
+                                 (kb_per_split is then unit 0's length) */
 } cusync_chain_info_t;
 
 /* Latency model of one chain run, in nanoseconds (cusync_predict_policies).  A tile

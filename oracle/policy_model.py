@@ -26,8 +26,9 @@ The model written out here, step by step:
   another) before the consumer tiles (in the same row order); CTA q takes tile q
   first, and every later tile goes to the CTA whose main loop frees up first (the lowest
   index on a tie);
-* with a K split of S, each producer tile is S consecutive queue entries; entry k runs
-  k-blocks [k * kb_per_split, min((k + 1) * kb_per_split, k_blocks)); the last entry's
+* with a K split of S, each producer tile is S consecutive queue entries over
+  consecutive k-block ranges: entry k runs kb_per_split + k * kb_skew k-blocks (a graded
+  split; kb_skew = 0: equal entries), and the last entry what remains; the last entry's
   epilogue (adding the others' partial sums) also waits for all the others' epilogues;
   only the last entry posts;
 * a producer tile's post is seen post_ns after its epilogue; before consumer k-block kb
@@ -81,6 +82,7 @@ class Chain:
     h_mb: float = 0.0
     ksplit: int = 1       # producer units per tile (K split), each over consecutive k-blocks
     kb_per_split: int = 0
+    kb_skew: int = 0      # k-blocks each unit runs more than the one before it
 
 
 def play(tiles, slots, t0, model, cost):
@@ -107,9 +109,15 @@ def play(tiles, slots, t0, model, cost):
 def _units(chain):
     """Producer queue entries (tile, unit, k-blocks)."""
     S = max(1, chain.ksplit)
-    kb0 = chain.k_blocks[0]
-    per = chain.kb_per_split if S > 1 else kb0
-    return [(t, k, min(per, kb0 - k * per)) for t in chain.prod_tiles for k in range(S)]
+    total = chain.k_blocks[0]
+    if S == 1:
+        return [(t, 0, total) for t in chain.prod_tiles]
+    lengths, start = [], 0
+    for k in range(S):
+        n = total - start if k == S - 1 else min(chain.kb_per_split + k * chain.kb_skew, total - start)
+        lengths.append(n)
+        start += n
+    return [(t, k, lengths[k]) for t in chain.prod_tiles for k in range(S)]
 
 
 def _play_producers(chain, slots, t0, model, ctas=None):

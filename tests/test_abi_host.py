@@ -326,16 +326,28 @@ def test_planner_k_split(kind, dims, pair, want):
     d = cs.make_desc(kind, "ROW", num_sms=152, cta_pair=pair, tile_n=256, **dims)
     info = cs.cusync_plan_info(d)
     assert info.ksplit == want
-    assert info.kb_per_split * want >= info.k_blocks[0] > info.kb_per_split * (want - 1)
+    lens = _unit_lengths(info)
+    assert sum(lens) == info.k_blocks[0] and min(lens) >= 1
+    if pair == 2 and want > 1:
+        # graded split: each unit an eighth of an equal unit (even, at least 2) longer
+        assert info.ksplit_skew == max(2, (info.k_blocks[0] // want // 8) & ~1)
+        assert all(b - a == info.ksplit_skew for a, b in zip(lens[:-2], lens[1:-1])) and lens[-1] >= lens[-2]
+    else:
+        assert info.ksplit_skew == 0
+        assert info.kb_per_split * want >= info.k_blocks[0] > info.kb_per_split * (want - 1)
     r = cs.cusync_plan_waves(d)
     assert r.tbs[0] == info.m_tiles[0] * info.n_tiles[0] * want   # the producer launch runs units
     assert r.tbs[0] * pair <= 2 * 152
 
 
 def test_k_split_requests():
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=256, num_sms=152, ksplit=5, ksplit_skew=-1, tile_n=256, **GPT)
+    info = cs.cusync_plan_info(d)
+    assert info.ksplit == 5 and info.kb_per_split == 39            # 192 k-blocks in 5 equal units
     d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=256, num_sms=152, ksplit=5, tile_n=256, **GPT)
     info = cs.cusync_plan_info(d)
-    assert info.ksplit == 5 and info.kb_per_split == 39            # 192 k-blocks in 5 units
+    assert (info.ksplit, info.kb_per_split, info.ksplit_skew) == (5, 30, 4)  # graded: 30, 34, 38, 42, 48
+    assert _unit_lengths(info) == [30, 34, 38, 42, 48]
     d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=64, K=320, N1=512, N2=256, ksplit=4, num_sms=152)
     info = cs.cusync_plan_info(d)
     assert (info.ksplit, info.kb_per_split) == (3, 2)              # 5 k-blocks: no empty unit
@@ -351,6 +363,48 @@ def test_k_split_requests():
         cs.cusync_plan_info(cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=64, K=64, N1=256, N2=64, ksplit=-1,
                                          num_sms=152))
     assert e.value.status == cs.ERR_INVALID_ARG
+
+
+def _unit_lengths(info):
+    """k-blocks of each producer unit, as the header defines the graded split."""
+    S, K = info.ksplit, info.k_blocks[0]
+    out, start = [], 0
+    for k in range(S):
+        n = K - start if k == S - 1 else min(info.kb_per_split + k * info.ksplit_skew, K - start)
+        out.append(n)
+        start += n
+    return out
+
+
+@pytest.mark.parametrize("S,skew,want", [(3, 8, [56, 64, 72]), (3, 16, [48, 64, 80]), (2, 10, [91, 101]),
+                                         (4, 5, [40, 45, 50, 57]), (3, -1, [64, 64, 64])])
+def test_graded_k_split(S, skew, want):
+    """Each producer unit runs ksplit_skew k-blocks more than the one before it and the
+    last takes the remainder; the units cover the 192 k-blocks of the GPT-3 slice once,
+    in order."""
+    d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=256, num_sms=152, ksplit=S, ksplit_skew=skew, tile_n=256, **GPT)
+    info = cs.cusync_plan_info(d)
+    assert info.ksplit == S and info.ksplit_skew == max(skew, 0)
+    lens = _unit_lengths(info)
+    assert lens == want and sum(lens) == info.k_blocks[0] == 192
+    assert all(b > a for a, b in zip(lens, lens[1:])) or skew < 0
+
+
+def test_graded_k_split_requests():
+    for bad in (-2, 65):
+        with pytest.raises(cs.CusyncError) as e:
+            cs.cusync_plan_info(cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=256, num_sms=152, ksplit=3,
+                                             ksplit_skew=bad, **GPT))
+        assert e.value.status == cs.ERR_INVALID_ARG
+    # a skew that leaves unit 0 without k-blocks
+    with pytest.raises(cs.CusyncError) as e:
+        cs.cusync_plan_info(cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=256, K=1024, N1=512, N2=512, num_sms=152,
+                                         ksplit=4, ksplit_skew=6))
+    assert e.value.status == cs.ERR_UNSUPPORTED
+    # no split: the skew is ignored
+    info = cs.cusync_plan_info(cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=256, num_sms=152, ksplit=1,
+                                            ksplit_skew=8, **GPT))
+    assert info.ksplit == 1 and info.ksplit_skew == 0
 
 
 # ----------------------------------------------------------------- attention chain

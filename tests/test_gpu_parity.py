@@ -240,6 +240,34 @@ def test_auto_policy_runs_the_predicted_policy():
     assert np.array_equal(bits(Y), bits(Y2)) and np.array_equal(bits(H), bits(H2))
 
 
+@pytest.mark.parametrize("ksplit,skew", [(3, 3), (2, 6), (4, 2)])
+@pytest.mark.parametrize("pair", [1, 2])
+def test_graded_k_split_all_policies(ksplit, skew, pair):
+    """Producer units of growing length (ksplit_skew; e.g. 7, 10 and 15 of 32 k-blocks):
+    every policy and launch mode within tolerance of the oracle and byte-identical to one
+    another."""
+    M, K, N1, N2 = 264, 2048, 1024, 512
+    (X, W1, W2), (H_ref, Y_ref) = _mlp_case(M, K, N1, N2, seed=18)
+    ops = device_mlp_operands(X, W1, W2)
+    ref_bits = None
+    for pol in POLICIES:
+        for launch in LAUNCHES:
+            if pol == "STREAM" and launch != cs.LAUNCH_PERSISTENT:
+                continue
+            d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, launch, M=M, K=K, N1=N1, N2=N2, tile_n=256, cta_pair=pair,
+                             ksplit=ksplit, ksplit_skew=skew)
+            info = cs.cusync_plan_info(d)
+            assert (info.ksplit, info.ksplit_skew) == (ksplit, skew)
+            H, Y, _ = run_mlp(d, *ops, runs=3)
+            assert_within_tol(f64(H), H_ref, f"H {pol} {launch} ksplit={ksplit} skew={skew}")
+            assert_within_tol(f64(Y), Y_ref, f"Y {pol} {launch} ksplit={ksplit} skew={skew}")
+            b = (bits(H), bits(Y))
+            if ref_bits is None:
+                ref_bits = b
+            else:
+                assert np.array_equal(b[0], ref_bits[0]) and np.array_equal(b[1], ref_bits[1]), (pol, launch)
+
+
 @pytest.mark.parametrize("ksplit", [0, 2, 3, 5])
 @pytest.mark.parametrize("pair", [1, 2])
 def test_k_split_producer_all_policies(ksplit, pair):

@@ -94,7 +94,7 @@ def _oracle_predict(desc, info, model, policy):
         h_mb = desc.M * desc.N1 * 2 / 1e6
     G = info.strided_group if policy == "STRIDED" else 1
     ch = pm.Chain(prod, cons, tuple(info.k_blocks), dc, G=G, h_mb=h_mb, ksplit=info.ksplit,
-                  kb_per_split=info.kb_per_split)
+                  kb_per_split=info.kb_per_split, kb_skew=info.ksplit_skew)
     mo = pm.Model(kblock_ns=tuple(model.kblock_ns), wait_kblock_ns=model.wait_kblock_ns,
                   sentinel_kblock_ns=model.sentinel_kblock_ns, start_ns=model.start_ns,
                   epilogue_ns=tuple(model.epilogue_ns), post_ns=model.post_ns, gap_ns=model.gap_ns,
@@ -115,6 +115,9 @@ CASES = [
     # K split: 2 x 2 producer tiles on 16 CTAs -> 4 units each (4 k-blocks per unit)
     dict(kind=cs.CHAIN_MLP_GELU, M=256, K=1024, N1=512, N2=512, tile_n=256, cta_pair=1, num_sms=16),
     dict(kind=cs.CHAIN_MLP_GELU, M=256, K=1024, N1=512, N2=512, tile_n=256, cta_pair=1, num_sms=40, ksplit=3),
+    # graded K split: units of 2, 5 and 9 k-blocks
+    dict(kind=cs.CHAIN_MLP_GELU, M=256, K=1024, N1=512, N2=512, tile_n=256, cta_pair=1, num_sms=40, ksplit=3,
+         ksplit_skew=3),
 ]
 
 

@@ -39,7 +39,7 @@ class cusync_chain_desc_t(ctypes.Structure):
         ("n", c_i32), ("h", c_i32), ("w", c_i32), ("c", c_i32), ("k_out", c_i32),
         ("tile_n", c_i32), ("strided_group", c_i32), ("flags", c_u32), ("num_sms", c_i32), ("raster_rows", c_i32),
         ("timeout_ns", c_u64), ("l2_prefetch", c_i32), ("cta_pair", c_i32), ("ksplit", c_i32),
-        ("stages", c_i32), ("ksplit_consumer", c_i32), ("bands", c_i32), ("_pad1", c_i32),
+        ("stages", c_i32), ("ksplit_consumer", c_i32), ("bands", c_i32), ("ksplit_skew", c_i32),
     ]
 
 
@@ -69,7 +69,7 @@ class cusync_chain_info_t(ctypes.Structure):
         ("nst", c_i32), ("m_tiles2", c_i32), ("n_tiles2", c_i32), ("k_blocks2", c_i32), ("n_out2", c_i32),
         ("grid2", c_i32), ("num_flags_pw", c_i32), ("strided_group_pw", c_i32), ("strided_distance_pw", c_i32),
         ("work_buffers", c_i32), ("work_bytes", c_i64), ("ksplit_consumer", c_i32), ("kb_per_split_consumer", c_i32),
-        ("raster_rows", c_i32), ("_pad", c_i32),
+        ("raster_rows", c_i32), ("ksplit_skew", c_i32),
     ]
 
 
@@ -180,14 +180,15 @@ def status_string(status):
 
 def make_desc(kind=CHAIN_MLP_GELU, policy=POLICY_ROW, launch=LAUNCH_PERSISTENT, M=0, K=0, N1=0, N2=0,
               n=0, h=0, w=0, c=0, k_out=0, tile_n=0, strided_group=0, flags=0, num_sms=0, timeout_ns=0,
-              raster_rows=0, l2_prefetch=0, cta_pair=0, ksplit=0, stages=0, ksplit_consumer=0, bands=0):
+              raster_rows=0, l2_prefetch=0, cta_pair=0, ksplit=0, stages=0, ksplit_consumer=0, bands=0,
+              ksplit_skew=0):
     if isinstance(policy, str):
         policy = POLICY_NAMES[policy]
     return cusync_chain_desc_t(kind=kind, policy=policy, launch=launch, M=M, K=K, N1=N1, N2=N2, n=n, h=h, w=w,
                                c=c, k_out=k_out, tile_n=tile_n, strided_group=strided_group, flags=flags,
                                num_sms=num_sms, timeout_ns=timeout_ns, raster_rows=raster_rows,
                                l2_prefetch=l2_prefetch, cta_pair=cta_pair, ksplit=ksplit, stages=stages,
-                               ksplit_consumer=ksplit_consumer, bands=bands)
+                               ksplit_consumer=ksplit_consumer, bands=bands, ksplit_skew=ksplit_skew)
 
 
 # ---------------------------------------------------------------- the C functions

@@ -263,8 +263,7 @@ __device__ __forceinline__ TileRef decode_tile(const ChainArgs& a, int32_t t) {
   if (g.ksplit > 1) {
     ks = u % g.ksplit;
     u /= g.ksplit;
-    kb0 = ks * g.kb_per_split;
-    nkb = min(g.kb_per_split, g.k_blocks - kb0);
+    split_unit(g, ks, &kb0, &nkb);
   }
   int32_t m, y;
   tile_at(g, u, &m, &y);

@@ -134,6 +134,17 @@ int32_t default_tile_n(const cusync_chain_desc_t& d) {
 
 cusync_status_t resolve_auto(const cusync_chain_desc_t& d, cusync_chain_desc_t* out);
 
+// Planner's graded split of a K-split producer on CTA pairs: each unit an eighth of an
+// equal unit (an even count of k-blocks, at least 2) longer than the one before it.
+// Measured against equal units, same box: GPT-3 M=256 slice (3 units of 64 k-blocks)
+// 75.9 against 77.7 us with 8; SwiGLU M=256 (2 x 64) 57.3 against 59.2 with 8; GPT-3
+// M=512 (2 x 96, two waves) 120.0 against 123.8 with 12; 6 and 12 for the 64-k-block
+// units and 8 for the 96-k-block units measured in between.
+int32_t default_split_skew(int32_t k_blocks, int32_t ksplit) {
+  const int32_t per = k_blocks / ksplit;
+  return std::max(2, (per / 8) & ~1);
+}
+
 cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   if (d.kind < CUSYNC_CHAIN_MLP_GELU || d.kind > CUSYNC_CHAIN_CONV_STACK) return CUSYNC_ERR_INVALID_ARG;
   if (d.policy == CUSYNC_POLICY_AUTO) {
@@ -325,6 +336,19 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   g0.ksplit = ks;
   g0.kb_per_split = (int32_t)ceil_div(g0.k_blocks, ks);
   g0.ksplit = (int32_t)ceil_div(g0.k_blocks, g0.kb_per_split);  // no empty unit
+  // Graded split (cusync_chain_desc_t::ksplit_skew): each unit kb_skew k-blocks longer
+  // than the one before it, so that the units finish one after the other and each
+  // unit's exchange overlaps the mainloops of the units after it.
+  if (d.ksplit_skew < -1 || d.ksplit_skew > 64) return CUSYNC_ERR_INVALID_ARG;
+  int32_t skew = d.ksplit_skew;
+  if (skew == 0) skew = (mlp && pair == 2 && g0.ksplit > 1) ? default_split_skew(g0.k_blocks, g0.ksplit) : -1;
+  if (skew > 0 && g0.ksplit > 1) {
+    const int32_t S = g0.ksplit;
+    const int32_t base = (g0.k_blocks - skew * (S * (S - 1) / 2)) / S;
+    if (base < 1) return CUSYNC_ERR_UNSUPPORTED;
+    g0.kb_per_split = base;
+    g0.kb_skew = skew;
+  }
   // K split of the consumer GEMM of an MLP chain (cusync_chain_desc_t::ksplit_consumer):
   // single-CTA consumer tiles that fill at most half of a wave get as many units per tile
   // as fit in one wave (at most 4, at least 16 k-blocks each).  CTA pairs keep whole
@@ -1261,6 +1285,7 @@ cusync_status_t cusync_plan_info(const cusync_chain_desc_t* d, cusync_chain_info
   out->policy = p.nst == 3 ? p.dep_pw.policy : p.dep.policy;
   out->ksplit = p.geo[0].ksplit;
   out->kb_per_split = p.geo[0].kb_per_split;
+  out->ksplit_skew = p.geo[0].kb_skew;
   out->ksplit_consumer = p.geo[1].ksplit;
   out->kb_per_split_consumer = p.geo[1].kb_per_split;
   out->raster_rows = p.geo[0].raster;
@@ -1370,8 +1395,8 @@ cusync_status_t cusync_consumer_unit_waits(const cusync_chain_desc_t* d, int32_t
   if (g.a_mode != AMODE_GEMM) return CUSYNC_ERR_INVALID_ARG;
   if (m_tile < 0 || m_tile >= g.m_tiles || unit < 0 || unit >= g.ksplit) return CUSYNC_ERR_INVALID_ARG;
   if (max > 0 && (!kb || !flag || !per_run)) return CUSYNC_ERR_INVALID_ARG;
-  const int32_t kb0 = unit * g.kb_per_split;
-  const int32_t nkb = std::min(g.kb_per_split, g.k_blocks - kb0);
+  int32_t kb0 = 0, nkb = 0;
+  split_unit(g, unit, &kb0, &nkb);
   GemmDepTracker t;
   t.reset();
   int32_t n = 0;

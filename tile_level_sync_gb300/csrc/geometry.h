@@ -55,12 +55,25 @@ struct StageGeo {
   int32_t th;                        // image rows per row tile
   int32_t tpi;                       // row tiles per image = ceil(img_h / th)
   int32_t cblocks;                   // cin / kBK channel blocks per filter tap
-  // K split (GEMM producers): each tile is computed by ksplit work units, unit k taking
-  // k-blocks [k * kb_per_split, (k + 1) * kb_per_split); their fp32 partial sums are added
-  // in unit order and the last unit applies the epilogue.  1 = no split.
+  // K split (GEMM producers): each tile is computed by ksplit work units over
+  // consecutive k-block ranges (split_unit); their fp32 partial sums are added in unit
+  // order and the last unit applies the epilogue.  1 = no split.  Unit 0 takes
+  // kb_per_split k-blocks and each later unit kb_skew more than the one before it; the
+  // last unit takes what remains.
   int32_t ksplit;
   int32_t kb_per_split;
+  int32_t kb_skew;
 };
+
+// First k-block and k-block count of K-split unit ks of a stage.  With kb_skew = 0 the
+// units are kb_per_split long but the last, which takes the remainder.
+CUSYNC_HD void split_unit(const StageGeo& g, int32_t ks, int32_t* kb0, int32_t* nkb) {
+  const int32_t k0 = ks * g.kb_per_split + g.kb_skew * (ks * (ks - 1) / 2);
+  const int32_t rest = g.k_blocks - k0;
+  const int32_t len = g.kb_per_split + ks * g.kb_skew;
+  *kb0 = k0;
+  *nkb = (ks == g.ksplit - 1 || rest < len) ? rest : len;
+}
 
 // Work units of a stage's queue: tiles x K-split units (the split units of one tile are
 // consecutive in the queue).

@@ -99,7 +99,8 @@ inline double play_queue(const ModelChain& c, const LatencyModel& lm, int s0, in
     if (s == 0 && S > 1) {
       ks = (int32_t)(u % S);
       u /= S;
-      nkb = std::min(c.geo[0].kb_per_split, c.geo[0].k_blocks - ks * c.geo[0].kb_per_split);
+      int32_t kb0 = 0;
+      split_unit(c.geo[0], ks, &kb0, &nkb);
     }
     int32_t m, y;
     tile_at(c.geo[s], (int32_t)u, &m, &y);
