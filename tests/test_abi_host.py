@@ -329,8 +329,8 @@ def test_planner_k_split(kind, dims, pair, want):
     lens = _unit_lengths(info)
     assert sum(lens) == info.k_blocks[0] and min(lens) >= 1
     if pair == 2 and want > 1:
-        # graded split: each unit an eighth of an equal unit (even, at least 2) longer
-        assert info.ksplit_skew == max(2, (info.k_blocks[0] // want // 8) & ~1)
+        # graded split: each unit 8 k-blocks longer (short units: a quarter of one, even)
+        assert info.ksplit_skew == max(2, min(8, info.k_blocks[0] // want // 4) & ~1)
         assert all(b - a == info.ksplit_skew for a, b in zip(lens[:-2], lens[1:-1])) and lens[-1] >= lens[-2]
     else:
         assert info.ksplit_skew == 0
@@ -346,8 +346,8 @@ def test_k_split_requests():
     assert info.ksplit == 5 and info.kb_per_split == 39            # 192 k-blocks in 5 equal units
     d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=256, num_sms=152, ksplit=5, tile_n=256, **GPT)
     info = cs.cusync_plan_info(d)
-    assert (info.ksplit, info.kb_per_split, info.ksplit_skew) == (5, 30, 4)  # graded: 30, 34, 38, 42, 48
-    assert _unit_lengths(info) == [30, 34, 38, 42, 48]
+    assert (info.ksplit, info.kb_per_split, info.ksplit_skew) == (5, 22, 8)  # graded: 22, 30, 38, 46, 56
+    assert _unit_lengths(info) == [22, 30, 38, 46, 56]
     d = cs.make_desc(cs.CHAIN_MLP_GELU, "ROW", M=64, K=320, N1=512, N2=256, ksplit=4, num_sms=152)
     info = cs.cusync_plan_info(d)
     assert (info.ksplit, info.kb_per_split) == (3, 2)              # 5 k-blocks: no empty unit

@@ -186,17 +186,25 @@ struct KCfg {
   static constexpr int kSlots = 4;                   // tile hand-off ring
   // Warps: 0 loader, 1 MMA, 2..5 epilogue, 6 prefetch; then, under the sentinel policy,
   // the checkers (7..8 on single CTAs, 7..10 on CTA pairs, whose stages hold two k-blocks:
-  // each checker scans half of one), otherwise 7..10 a second group of epilogue warps (two
-  // warps per TMEM lane quarter, each storing every other 64-column box of a tile).
+  // each checker scans half of one), and a second group of epilogue warps (two warps per
+  // TMEM lane quarter, each storing every other 64-column box of a tile): 7..10 without
+  // the checkers, 11..14 after them on CTA pairs (15 warps, 128 registers a thread; the
+  // sentinel policy's GPT-3 M=256 / M=512 MLP chains 91.3 / 146.0 against 93.2 / 150.1 us
+  // with one group).  Single-CTA sentinel kernels keep one group: 13 warps would also
+  // cap them at 128 registers, where they spill.
   // Single-CTA kernels without the checkers issue each stage's weight (B) copies from
   // warp 11 (split_b): their loader, with one copy per operand and k-block, bounds the
   // mainloop, and the stacks of short convolution tiles measured 2-4% faster with the
   // second issuer (ResNet-38 28x28x128: 157.7 against 163.2 us); CTA pairs, which bring two
   // k-blocks per copy, measured 2-9% slower with it (GPT-3 M=1024: 226.4 against 208.6 us).
-  __host__ __device__ static constexpr int epi_warps(bool check) { return check ? 4 : 8; }
+  __host__ __device__ static constexpr int epi_warps(bool check) { return (check && PAIR == 1) ? 4 : 8; }
   __host__ __device__ static constexpr int check_warps() { return PAIR == 2 ? 4 : 2; }
+  // first warp of the second epilogue group: after the checkers when there are any
+  __host__ __device__ static constexpr int epi2_warp(bool check) { return check ? 7 + check_warps() : 7; }
   __host__ __device__ static constexpr bool split_b(bool check) { return !check && PAIR == 1; }
-  static constexpr int threads(bool check) { return check ? 32 * (7 + check_warps()) : (split_b(check) ? 384 : 352); }
+  static constexpr int threads(bool check) {
+    return 32 * (check ? 7 + check_warps() + (epi_warps(check) - 4) : (split_b(check) ? 12 : 11));
+  }
   // epilogue staging for TMA stores: 32-row x 64-column bf16 boxes, 32 KB in all (two
   // boxes per epilogue warp with four warps, one with eight)
   static constexpr int kEpiBufBytes = 32 * 64 * 2;
@@ -482,6 +490,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
   constexpr bool kPair = PAIR == 2;
   constexpr int kEpiWarps = C::epi_warps(CHECK);
   constexpr int kEpiGroups = kEpiWarps / 4;  // epilogue warps per TMEM lane quarter
+  constexpr int kEpi2 = C::epi2_warp(CHECK);  // first warp of the second epilogue group
   constexpr int kEpiBufs = C::epi_bufs(CHECK);  // staging boxes per epilogue warp
 
   extern __shared__ uint8_t smem_raw[];
@@ -1137,7 +1146,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       }
     }
     __syncwarp();
-  } else if (CHECK && warp >= 7) {
+  } else if (CHECK && warp >= 7 && warp < 7 + C::check_warps()) {
     // ------------------------------------------------------------ sentinel checkers
     // Under the sentinel policy every consumer k-block's A tile is validated here, off the
     // MMA issuer's path, and handed to it through `ready` (the leader's, in a pair).  With
@@ -1551,12 +1560,13 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       it0 += (uint32_t)KB;
     }
     __syncwarp();
-  } else if ((warp >= 2 && warp <= 5) || (kEpiGroups == 2 && warp >= 7 && warp <= 10)) {
-    // ------------------------------------------------------------ epilogue (warps 2..5, 7..10)
+  } else if ((warp >= 2 && warp <= 5) || (kEpiGroups == 2 && warp >= kEpi2 && warp < kEpi2 + 4)) {
+    // ------------------------------------------------------------ epilogue (warps 2..5 and
+    // 7..10; with the sentinel checkers, 2..5 and the four warps after the checkers)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;
-    const int egrp = warp >= 7 ? 1 : 0;            // this warp's group: it stores boxes egrp, egrp + kEpiGroups, ...
-    const int ew = egrp * 4 + (warp - (egrp ? 7 : 2));  // epilogue warp ordinal
+    const int egrp = warp >= kEpi2 ? 1 : 0;        // this warp's group: it stores boxes egrp, egrp + kEpiGroups, ...
+    const int ew = egrp * 4 + (warp - (egrp ? kEpi2 : 2));  // epilogue warp ordinal
     const int et = ew * 32 + lane;                 // epilogue thread ordinal
     uint32_t tcount = 0, acount = 0, pwcount = 0;  // pwcount: pointwise tiles done
     // Attention chain: a pointwise tile (see pointwise_tile) -- out of line, so that its

@@ -134,15 +134,16 @@ int32_t default_tile_n(const cusync_chain_desc_t& d) {
 
 cusync_status_t resolve_auto(const cusync_chain_desc_t& d, cusync_chain_desc_t* out);
 
-// Planner's graded split of a K-split producer on CTA pairs: each unit an eighth of an
-// equal unit (an even count of k-blocks, at least 2) longer than the one before it.
-// Measured against equal units, same box: GPT-3 M=256 slice (3 units of 64 k-blocks)
-// 75.9 against 77.7 us with 8; SwiGLU M=256 (2 x 64) 57.3 against 59.2 with 8; GPT-3
-// M=512 (2 x 96, two waves) 120.0 against 123.8 with 12; 6 and 12 for the 64-k-block
-// units and 8 for the 96-k-block units measured in between.
+// Planner's graded split of a K-split producer on CTA pairs: each unit 8 k-blocks longer
+// than the one before it (units shorter than 32 k-blocks: a quarter of one, even, at
+// least 2).  Measured against equal units, same box: GPT-3 M=256 MLP slice (3 units of
+// 64 k-blocks) 75.9 against 77.7 us, SwiGLU M=256 (2 x 64) 57.3 against 59.2, GPT-3 M=512
+// (2 x 96, two waves) 120.1 against 123.8, GPT-3 attention M=256 (4 x 48) 78.4 against
+// 82.9; skews of 4, 6, 10, 12 and 16 measured slower than 8 on the first and the last,
+// 12 equal on the third.
 int32_t default_split_skew(int32_t k_blocks, int32_t ksplit) {
   const int32_t per = k_blocks / ksplit;
-  return std::max(2, (per / 8) & ~1);
+  return std::max(2, std::min(8, per / 4) & ~1);
 }
 
 cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
@@ -341,7 +342,7 @@ cusync_status_t make_plan(const cusync_chain_desc_t& d, Plan* p) {
   // unit's exchange overlaps the mainloops of the units after it.
   if (d.ksplit_skew < -1 || d.ksplit_skew > 64) return CUSYNC_ERR_INVALID_ARG;
   int32_t skew = d.ksplit_skew;
-  if (skew == 0) skew = (mlp && pair == 2 && g0.ksplit > 1) ? default_split_skew(g0.k_blocks, g0.ksplit) : -1;
+  if (skew == 0) skew = ((mlp || attn) && pair == 2 && g0.ksplit > 1) ? default_split_skew(g0.k_blocks, g0.ksplit) : -1;
   if (skew > 0 && g0.ksplit > 1) {
     const int32_t S = g0.ksplit;
     const int32_t base = (g0.k_blocks - skew * (S * (S - 1) / 2)) / S;
