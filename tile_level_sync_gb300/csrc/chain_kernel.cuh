@@ -150,7 +150,11 @@ struct ChainArgs {
                          // the kernel before it in the stream): wait for that kernel before
                          // reading the run number or touching global memory;
                          // bit 3: the run's last launch: trigger dependents once this CTA has
-                         // claimed its last tile
+                         // claimed its last tile;
+                         // bit 4: started early after the sentinel fill of the intermediate (a
+                         // programmatic dependent that lets this launch start once the run before
+                         // has ended): wait for the fill before the first store or load of the
+                         // intermediate
   int32_t sentinel_check;
   int32_t num_flags;     // semaphores in `flags`
   int32_t l2_prefetch;   // k-blocks the prefetch warp runs ahead of the loader (0: none)
@@ -644,6 +648,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
       int b_slot = 0, a_slot = 0;
       uint32_t b_par = 1u;
       bool ok = true;
+      bool fill_seen = false;  // pdl_role bit 4: the intermediate's fill has ended
       while (true) {
         const int slot = tcount % C::kSlots;
         const uint32_t tpar = (tcount / C::kSlots) & 1u;
@@ -685,6 +690,10 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
 
         const TileRef tr = decode_tile(args, t);
         if (tr.s == kFillStage) continue;  // written by this CTA's epilogue warps; nothing to load
+        if ((args.pdl_role & 16) && tr.s > 0 && !fill_seen) {
+          ptx::pdl_wait();  // the sentinel fill of the intermediate has ended (pdl_role bit 4)
+          fill_seen = true;
+        }
         const StageArgs& SA = stage_args(args, tr.s);
         const int32_t KB = tr.nkb;            // k-blocks of this work unit
         const int32_t kx0 = tr.kb0 * kBK;     // its first reduction coordinate
@@ -1569,6 +1578,7 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
     const int ew = egrp * 4 + (warp - (egrp ? kEpi2 : 2));  // epilogue warp ordinal
     const int et = ew * 32 + lane;                 // epilogue thread ordinal
     uint32_t tcount = 0, acount = 0, pwcount = 0;  // pwcount: pointwise tiles done
+    bool fill_seen = false;                        // pdl_role bit 4: the intermediate's fill has ended
     // Attention chain: a pointwise tile (see pointwise_tile) -- out of line, so that its
     // registers do not weigh on the GEMM epilogue.
 
@@ -1603,6 +1613,10 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
                          pwcount & 1u, *run_no, leader, pto, abort_flag);
         ++pwcount;
         continue;
+      }
+      if ((args.pdl_role & 16) && !fill_seen) {
+        ptx::pdl_wait();  // before this CTA's first store of the intermediate (pdl_role bit 4)
+        fill_seen = true;
       }
       const int acc = acount & 1;
       const uint32_t apar = (acount >> 1) & 1u;
@@ -1898,8 +1912,14 @@ __global__ void band_release_kernel(uint32_t* band_flags, BandTargets targets, i
 }
 
 // Fill a buffer with the bf16 sentinel 0x8000 using 16-byte stores (CUDA-FGS §4.6.4.2,
-// initialisation "in a separate kernel").
-__global__ void sentinel_fill_kernel(uint4* buf, int64_t n16) {
+// initialisation "in a separate kernel").  overlap: launched as a programmatic dependent
+// of the kernel before it, whose reads of the buffer must end first; once they have, the
+// chain after this kernel may start (it waits for this fill before it touches the buffer).
+__global__ void sentinel_fill_kernel(uint4* buf, int64_t n16, int32_t overlap) {
+  if (overlap) {
+    ptx::pdl_wait();
+    ptx::pdl_launch_dependents();
+  }
   const uint4 s = make_uint4(0x80008000u, 0x80008000u, 0x80008000u, 0x80008000u);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
     buf[i] = s;

@@ -840,26 +840,41 @@ cusync_status_t launch_run(const cusync_chain_desc_t& d, const Plan& p, ChainArg
   cudaError_t e;
   // Sentinel fill before the run; a rotating stack fills both of its sets only when asked
   // (a new workspace, or after a reset), its runs otherwise fill the next run's set.
-  if (d.policy == CUSYNC_POLICY_SENTINEL && !(d.flags & CUSYNC_DEBUG_SKIP_INIT) && (!p.rotate || fill_sets)) {
-    // the intermediate (a stack: all of its intermediates, one buffer each)
-    const int64_t bytes = (int64_t)p.geo[0].M * p.geo[0].N * 2 * (p.stack ? p.nbuf : 1);
-    const int64_t n16 = bytes / 16;
-    int blocks = (int)std::min<int64_t>(ceil_div(n16, 256), (int64_t)sms * 8);
-    if (blocks < 1) blocks = 1;
-    sentinel_fill_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<uint4*>(h), n16);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "sentinel fill launch");
-  }
   const bool per_stage = d.policy == CUSYNC_POLICY_STREAM || d.launch == CUSYNC_LAUNCH_PDL;
   // Unless the caller opts out, the run's first launch is a programmatic dependent of the
   // kernel before it in the stream: its set-up overlaps that kernel's tail, and it waits
   // for that kernel's completion before it touches memory (pdl_role bit 2); the run's last
   // launch lets such a launch start once all of its tiles are claimed (bit 3).
   const bool overlap = !(d.flags & CUSYNC_FLAG_NO_RUN_OVERLAP);
+  // A two-stage chain's fused run under the sentinel policy overlaps its fill: the fill is
+  // a programmatic dependent of the kernel before it (it waits for that kernel's end, then
+  // lets the chain start), and the chain waits for the fill only before it first stores
+  // or loads the intermediate (pdl_role bit 4), so the producers' mainloops run meanwhile.
+  const bool fill = d.policy == CUSYNC_POLICY_SENTINEL && !(d.flags & CUSYNC_DEBUG_SKIP_INIT) && (!p.rotate || fill_sets);
+  const bool fill_overlap = fill && overlap && !per_stage && !p.stack && p.nst == 2;
+  if (fill) {
+    // the intermediate (a stack: all of its intermediates, one buffer each)
+    const int64_t bytes = (int64_t)p.geo[0].M * p.geo[0].N * 2 * (p.stack ? p.nbuf : 1);
+    const int64_t n16 = bytes / 16;
+    int blocks = (int)std::min<int64_t>(ceil_div(n16, 256), (int64_t)sms * 8);
+    if (blocks < 1) blocks = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = fill_overlap ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, sentinel_fill_kernel, reinterpret_cast<uint4*>(h), n16, fill_overlap ? 1 : 0);
+    if (e != cudaSuccess) return cuda_fail(e, "sentinel fill launch");
+  }
   if (!per_stage) {
     A.queue = 0;
     A.first_stage = 0;
     A.last_stage = p.nst - 1;
-    A.pdl_role = overlap ? (4 | 8) : 0;
+    A.pdl_role = fill_overlap ? (16 | 8) : (overlap ? (4 | 8) : 0);
     e = launch_any(p, A, g.fused, overlap, stream);
     if (e != cudaSuccess) return cuda_fail(e, "fused chain launch");
     return CUSYNC_OK;
