@@ -1717,8 +1717,14 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
             split_late = true;
           }
         }
+        // the last unit marks the words as it reads them; a unit between the first and the
+        // last marks them after all of its own slot's stores (below), which the next unit
+        // is waiting for
+        if (last_unit) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ptx::st_relaxed_gpu_b128(p + i * 128, kSplitEmpty, kSplitEmpty, kSplitEmpty, kSplitEmpty);
+          for (int i = 0; i < 8; ++i)
+            ptx::st_relaxed_gpu_b128(p + i * 128, kSplitEmpty, kSplitEmpty, kSplitEmpty, kSplitEmpty);
+        }
       };
       // 32 accumulator columns from `col` on.  The units form a chain: unit k > 0 adds
       // the running sum of units 0..k-1 from slot k-1 to its own sums (the same
@@ -1817,6 +1823,19 @@ __global__ void __launch_bounds__(KCfg<BN, PAIR>::threads(CHECK), 1) chain_kerne
           for (int ch = 0; ch < 4; ++ch) {
             const int32_t col = col0 + j * 32 + ch * 8;
             if (col < g.N) ptx::st_relaxed_gpu_b128(orow + col, p[4 * ch], p[4 * ch + 1], p[4 * ch + 2], p[4 * ch + 3]);
+          }
+        }
+      }
+      if (split && !last_unit && tr.ks > 0) {
+        // the predecessor's slot, read above, marked empty for the next run
+        const int ncol = g.epi == EPI_SWIGLU ? 2 : 1;  // SwiGLU: gate and up columns
+        for (int j = 0; j < nchunks; ++j) {
+          if (kEpiGroups > 1 && ((j >> 1) % kEpiGroups) != egrp) continue;  // the other group's box
+          for (int h = 0; h < ncol; ++h) {
+            uint4* w = ws_row + ((h * (BN / 2) + j * 32) / 4) * 128 + (tr.ks - 1) * kSlotF4;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              ptx::st_relaxed_gpu_b128(w + i * 128, kSplitEmpty, kSplitEmpty, kSplitEmpty, kSplitEmpty);
           }
         }
       }
