@@ -44,8 +44,10 @@ NCU_TRAFFIC = {
     # (workload, policy, launch, tile_n, CTAs per tile): (dram__bytes_read.sum +
     # dram__bytes_write.sum per launch of the chain kernel, hash of the kernel sources the
     # capture was taken with)
-    ("gpt3_mlp_m256", "ROW", "persistent", 256, 2): (311500544 + 19335168, "f98b63074f8798a1"),
-    ("gpt3_mlp_m1024", "ROW", "persistent", 256, 2): (554264832 + 31522048, "f98b63074f8798a1"),
+    ("gpt3_mlp_m256", "ROW", "persistent", 256, 2): (309893632 + 19175936, "59b5104be33df0ba"),
+    ("gpt3_mlp_m1024", "ROW", "persistent", 256, 2): (554258432 + 31390464, "59b5104be33df0ba"),
+    ("gpt3_mlp_m1024", "SENTINEL", "persistent", 256, 2): (553572864 + 35731200, "59b5104be33df0ba"),
+    ("gpt3_mlp_m256", "SENTINEL", "persistent", 256, 2): (313405696 + 20307712, "59b5104be33df0ba"),
 }
 
 
