@@ -50,6 +50,23 @@ NCU_TRAFFIC = {
     ("gpt3_mlp_m256", "SENTINEL", "persistent", 256, 2): (313405696 + 20307712, "59b5104be33df0ba"),
 }
 
+# DRAM bytes (read + write) of one fused RowSync launch with the planner's defaults, per
+# workload, from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum -k regex:chain_kernel
+# -s 3 -c 1 python bench.py --workload W --policies ROW --profile-runs 2`, with the hash of the
+# kernel sources of the capture (reported in the per-configuration table only while it matches).
+NCU_ROW_TRAFFIC = {
+    "mlp_tiny_m64": (1212928 + 0, "59b5104be33df0ba"),
+    "gpt3_mlp_m512": (531374336 + 29944576, "59b5104be33df0ba"),
+    "gpt3_mlp_m1024": (554258432 + 31390464, "59b5104be33df0ba"),
+    "gpt3_mlp_m2048": (725913088 + 74533888, "59b5104be33df0ba"),
+    "gpt3_mlp_m4096": (1035433216 + 153161472, "59b5104be33df0ba"),
+    "swiglu_m256": (181392640 + 5762304, "59b5104be33df0ba"),
+    "swiglu_m1024": (307443968 + 14522112, "59b5104be33df0ba"),
+    "conv_resnet14_n32": (5716992 + 6656, "59b5104be33df0ba"),
+    "gpt3_attn_m256": (157476352 + 4235008, "59b5104be33df0ba"),
+    "gpt3_attn_m1024": (295312384 + 36664064, "59b5104be33df0ba"),
+}
+
 
 def kernel_source_hash():
     import hashlib
@@ -715,6 +732,12 @@ def per_config(torch, cs, synth, peaks):
                           "util": list(w148.util)},
             "l2": "operands larger than L2" if algorithmic_bytes(wl) > 129e6 else "operands fit in L2 (not flushed)",
         }
+        rec = NCU_ROW_TRAFFIC.get(name)
+        if rec and rec[1] == kernel_source_hash():
+            alg = algorithmic_bytes(wl)
+            out[name]["dram_traffic_row_fused"] = {"bytes": rec[0], "algorithmic_bytes": alg, "ratio": rec[0] / alg,
+                                                   "source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, one "
+                                                             "fused RowSync launch (planner defaults)"}
         for c in setup.chains.values():
             c.close()
         del setup, ref
