@@ -28,9 +28,9 @@ The model written out here, step by step:
   index on a tie);
 * with a K split of S, each producer tile is S consecutive queue entries over
   consecutive k-block ranges: entry k runs kb_per_split + k * kb_skew k-blocks (a graded
-  split; kb_skew = 0: equal entries), and the last entry what remains; the last entry's
-  epilogue (adding the others' partial sums) also waits for all the others' epilogues;
-  only the last entry posts;
+  split; kb_skew = 0: equal entries), and the last entry what remains; the entries form
+  a chain: the epilogue of entry k > 0 (adding the running sum of the entries before it)
+  also waits for entry k - 1's epilogue; only the last entry posts;
 * a producer tile's post is seen post_ns after its epilogue; before consumer k-block kb
   the tile waits for the producer tiles its policy waits for there (``deps.wait_sets``);
   if they are posted later than the k-block could start, the k-block starts start_ns
@@ -137,11 +137,10 @@ def _play_producers(chain, slots, t0, model, ctas=None):
         c["used"] = True
         main_end = start + nkb * model.kblock_ns[0]
         ready = max(main_end, c["last_done"])
-        if S > 1 and k == S - 1:
-            ready = max(ready, prev_done[tile])
+        if S > 1 and k > 0:
+            ready = max(ready, prev_done[tile])   # the running sum of the entries before it
         done = ready + model.epilogue_ns[0]
-        if k < S - 1:
-            prev_done[tile] = max(prev_done.get(tile, done), done)
+        prev_done[tile] = done
         c["free"] = main_end
         c["last_done"] = done
         end = max(end, done)

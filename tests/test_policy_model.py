@@ -194,6 +194,29 @@ def test_k_split_closed_form():
     assert pm.predict_fused(ch, "ROW", 2, m) == pytest.approx(want, rel=1e-12)
 
 
+def test_graded_k_split_closed_form():
+    """Three units of one tile of 24 k-blocks graded by 4 (4, 8, 12 k-blocks) on three
+    CTAs, stream order: the units form a chain, so each unit's epilogue follows its own
+    mainloop and the epilogue of the unit before it; the consumer launch follows the last
+    epilogue.  With equal units (8 each) every mainloop ends at once and the three
+    epilogues queue behind one another, so the chain ends later."""
+    prod, cons, dc = pm.gemm_chain(128, 256, 128, 256, 256, 1, "ROW")
+    ch = pm.Chain(prod, cons, (24, 4), dc, ksplit=3, kb_per_split=4, kb_skew=4)
+    assert [n for _, _, n in pm._units(ch)] == [4, 8, 12]
+    m = _model()
+    u0 = 100 + 4 * 10 + 30
+    u1 = max(100 + 8 * 10, u0) + 30
+    u2 = max(100 + 12 * 10, u1) + 30
+    want = u2 + 500 + (100 + 4 * 20 + 40)
+    assert pm.predict_stream(ch, 3, 1, m) == pytest.approx(want, rel=1e-12)
+    eq = pm.Chain(prod, cons, (24, 4), dc, ksplit=3, kb_per_split=8)
+    e0 = 100 + 8 * 10 + 30
+    e1 = max(100 + 8 * 10, e0) + 30
+    e2 = max(100 + 8 * 10, e1) + 30
+    assert pm.predict_stream(eq, 3, 1, m) == pytest.approx(e2 + 500 + (100 + 4 * 20 + 40), rel=1e-12)
+    assert pm.predict_stream(eq, 3, 1, m) > pm.predict_stream(ch, 3, 1, m)
+
+
 def test_grouped_queue_order():
     """The oracle model's queue order with row tiles in groups (column outer, row inner
     within a group), written out by hand for 3 row tiles x 2 columns in groups of 2, and

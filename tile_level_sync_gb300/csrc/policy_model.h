@@ -13,8 +13,9 @@
 //    every shape).
 //
 // Here a tile's latency is T_start + (k-blocks x per-k-block time) + T_epilogue (with a
-// K split, each unit of a producer tile runs its share of the k-blocks, and the last
-// unit's epilogue -- adding the others' partial sums -- follows all of theirs), and the
+// K split, each unit of a producer tile runs its share of the k-blocks, and each unit's
+// epilogue after the first -- adding the running sum of the units before it -- follows
+// that of the unit before it), and the
 // threadblock batches are not assumed but played out: a persistent CTA takes the next
 // tile of the queue as soon as its mainloop finishes (its epilogue overlaps the next
 // tile's mainloop) and starts its k-blocks tile_ns later (the claim, the arming and the
@@ -83,7 +84,8 @@ inline double play_queue(const ModelChain& c, const LatencyModel& lm, int s0, in
   const int64_t n0 = stage_units(c.geo[0]);
   const int64_t n1 = stage_units(c.geo[1]);
   const int32_t S = c.geo[0].ksplit > 1 ? c.geo[0].ksplit : 1;
-  // K split: when the other units of each producer tile have all stored their sums
+  // K split: when the latest unit of each producer tile has stored its running sum (the
+  // units of a tile form a chain)
   std::vector<double> unit_done(S > 1 ? (size_t)(n0 / S) : 0, 0.0);
   const int64_t total = (s0 == 0 ? n0 : 0) + (s1 == 1 ? n1 : 0);
   if (total == 0) return t0;
@@ -135,10 +137,9 @@ inline double play_queue(const ModelChain& c, const LatencyModel& lm, int s0, in
       }
     }
     double ready = std::max(t, x.last_done);
-    const bool last = s != 0 || ks == S - 1;
-    if (s == 0 && S > 1 && last) ready = std::max(ready, unit_done[(size_t)u]);  // all other units stored
+    if (s == 0 && S > 1 && ks > 0) ready = std::max(ready, unit_done[(size_t)u]);  // the running sum before it
     const double done = ready + lm.epilogue_ns[s];
-    if (s == 0 && S > 1 && !last) unit_done[(size_t)u] = std::max(unit_done[(size_t)u], done);
+    if (s == 0 && S > 1) unit_done[(size_t)u] = done;
     x.free_main = t;
     x.last_done = done;
     end = std::max(end, done);
