@@ -210,7 +210,10 @@ typedef struct {
                                         last takes the remainder), so the units finish one
                                         after the other and each exchange of partial sums
                                         overlaps the later units' mainloops.  0 =
-                                        planner; -1 = equal units */
+                                        planner: 8 for MLP and attention chains on CTA
+                                        pairs (a quarter of a unit, even, when units are
+                                        shorter than 32 k-blocks), else none; -1 = equal
+                                        units; at most 64 */
 } cusync_chain_desc_t;
 
 /* Wave arithmetic of a two-kernel chain ([cuSync] §II-A "Thread block Wave Execution",
