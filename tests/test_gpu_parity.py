@@ -240,6 +240,34 @@ def test_auto_policy_runs_the_predicted_policy():
     assert np.array_equal(bits(Y), bits(Y2)) and np.array_equal(bits(H), bits(H2))
 
 
+def test_many_tiles_all_policies():
+    """A long token dimension with small weights: 128 row tiles of 256 tokens and 256
+    producer plus 256 consumer pair tiles, several waves of the persistent queue, row
+    tiles taken in groups of 64 (half of them): every policy and launch mode byte-identical,
+    the oracle on the first and last row of every tile."""
+    M, K, N1, N2 = 32768, 256, 512, 512
+    X, W1, W2 = synth.mlp_gelu_inputs(M, K, N1, N2, seed=27)
+    ops = device_mlp_operands(X, W1, W2)
+    ref_bits = None
+    for pol in POLICIES:
+        for launch in LAUNCHES:
+            if pol == "STREAM" and launch != cs.LAUNCH_PERSISTENT:
+                continue
+            d = cs.make_desc(cs.CHAIN_MLP_GELU, pol, launch, M=M, K=K, N1=N1, N2=N2)
+            info = cs.cusync_plan_info(d)
+            assert info.cta_pair == 2 and info.m_tiles[0] == 128 and info.raster_rows == 64
+            H, Y, _ = run_mlp(d, *ops, runs=2)
+            b = (bits(H), bits(Y))
+            if ref_bits is None:
+                ref_bits = b
+            else:
+                assert np.array_equal(b[0], ref_bits[0]) and np.array_equal(b[1], ref_bits[1]), (pol, launch)
+    rows = sorted({r for t0 in range(0, M, 256) for r in (t0, t0 + 255)})
+    H_ref, Y_ref = chains.mlp_gelu(f64(X[rows]), f64(W1), f64(W2))
+    assert_within_tol(f64(H[rows]), H_ref, "H sampled rows")
+    assert_within_tol(f64(Y[rows]), Y_ref, "Y sampled rows")
+
+
 @pytest.mark.parametrize("ksplit,skew", [(3, 3), (2, 6), (4, 2)])
 @pytest.mark.parametrize("pair", [1, 2])
 def test_graded_k_split_all_policies(ksplit, skew, pair):
