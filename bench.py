@@ -964,7 +964,7 @@ def main():
                    "tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "cta_pair": info.cta_pair,
                    "ksplit": info.ksplit, "ksplit_skew": info.ksplit_skew,
                    "parallelism": "replicas only",
-                   "enqueue": "library call per run" if a.no_graph else "CUDA-graph replay, 50 captured runs per graph",
+                   "enqueue": "library call per run" if a.no_graph else "CUDA-graph replay, up to 50 captured runs (steps) per graph",
                    "l2": f"inputs {alg_bytes / 1e6:.0f} MB of operands > 129 MB L2; no flush between steps"
                    if alg_bytes > 129e6 else "inputs smaller than L2",
                    "vs_baseline_note": "speed-up over the stream-serialised chain (same kernel, tiles and k "
