@@ -38,8 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Tesla V100 in fp16 ([cuSync] Table tab:waves:mlp).  Context on other hardware.
 PAGES_US_B256 = 840.0
 # DRAM bytes (read + write) per launch of the fused chain kernel from one ncu capture
-# (profiles/chain_kernel_full_<workload>_row.md), valid only for the kernel sources the
-# capture was taken on (sha256 of tile_level_sync_gb300/csrc/*).
+# (profiles/chain_kernel_full_<workload>_*.md), valid only for the kernel sources the
+# capture was taken on (kernel_source_hash).
 NCU_TRAFFIC = {
     # (workload, policy, launch, tile_n, CTAs per tile): (dram__bytes_read.sum +
     # dram__bytes_write.sum per launch of the chain kernel, hash of the kernel sources the
@@ -728,6 +728,7 @@ def per_config(torch, cs, synth, peaks):
             "dims": wl.dims, "gflop": flops / 1e9, "best": best, "best_us": sync[best],
             "stream_us": timed.get("STREAM"), "speedup_vs_stream": timed["STREAM"] / sync[best] if "STREAM" in timed
             else None, "tflops": tflops, "pct_bf16_peak_measured": tflops / peaks["bf16_tflops"] * 100,
+            "pct_bf16_sustained_peak_measured": tflops / peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * 100,
             "tile": f"{info.tile_m}x{info.tile_n}x{info.tile_k}", "cta_pair": info.cta_pair, "ksplit": info.ksplit,
             "ksplit_skew": info.ksplit_skew, "us": us, "runs_timed": n, "timing": "median of 5 rounds over the variants in turn",
             "bit_identical_all_variants": identical,
